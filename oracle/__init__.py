@@ -1,0 +1,9 @@
+"""Plain fp64 CPU oracle for the FAVOR+ forward pass (test infrastructure only).
+
+This package is the independent checker for the CUDA library.  It is imported
+only by the tests, by ``__graft_entry__.smoke()`` and by ``bench.py``'s CPU
+baseline / reference arm.  The product path (``linear_softmax_attention_gb300``)
+never imports it, and it never imports the product path.
+"""
+
+from .favor import *  # noqa: F401,F403

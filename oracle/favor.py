@@ -1,0 +1,347 @@
+"""fp64 NumPy oracle for FAVOR+ (positive orthogonal random features).
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import this
+module; it shares no code with the CUDA library and imports nothing from it.
+
+Sources (web pages on "Rethinking Attention with Performers"):
+  [digest]  "Performer — Rethinking Attention with Performers" (Korean blog
+            digest): §Methods (FAVOR+), §Theoretical bounds, §Key equations
+            (핵심 수식), §Method / key components (핵심 구성요소), flowchart.
+  [su]      "From Performer to Linear Attention" (Su Jianlin): §Simple
+            Derivation (the scale-invariance argument).
+  [summary] "Rethinking Attention with Performers" (arXiv:2009.14794v4
+            section summary): §2 FAVOR+ mechanism, §3 theoretical results,
+            §A.2 unidirectional attention, §B.3 complexity.
+
+Readings where the pages are silent (each also listed in the design notes):
+  * A temperature ``scale`` multiplies q and k before the feature map
+    (x' = scale * x).  The pages write softmax(QK^T) with no temperature;
+    scale = d**-0.25 gives the usual exp(q.k / sqrt(d)).
+  * No stabiliser and no epsilon: in fp64 every exponent here is far inside
+    the exp range, so the estimator is evaluated literally.
+  * The random numbers: a counter-based SplitMix64 (Steele, Lea & Flood,
+    "Fast splittable pseudorandom number generators", OOPSLA 2014) turned into
+    normals by the Box–Muller transform (cosine branch).  The pages fix no RNG.
+  * ORF rows: Gram–Schmidt on the rows of independent d x d Gaussian blocks,
+    each row then given the length of an independent N(0, I_d) vector (a chi_d
+    sample) so that every row keeps the N(0, I_d) marginal; the first m rows of
+    the stacked blocks form Omega.
+
+Parity pins for every function live in ``tests/test_oracle_*.py``.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "SPLITMIX_GAMMA",
+    "splitmix64_stream",
+    "normals_from_words",
+    "counter_normals",
+    "gram_schmidt_rows",
+    "build_omega",
+    "orf_index_layout",
+    "prf_features",
+    "trig_features",
+    "softmax_kernel",
+    "prf_estimator",
+    "lemma2_mse",
+    "favor_bidirectional",
+    "favor_bidirectional_quadratic",
+    "favor_causal",
+    "favor_causal_quadratic",
+    "favor_rows",
+    "softmax_attention",
+    "rowwise_rel_err",
+]
+
+# --------------------------------------------------------------------------
+# Random numbers (not on the pages; published generator definitions)
+# --------------------------------------------------------------------------
+
+SPLITMIX_GAMMA = 0x9E3779B97F4A7C15
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+
+def _mix64(z: np.ndarray) -> np.ndarray:
+    """SplitMix64 output function (variant 13 of Stafford's mixer)."""
+    z = (z ^ (z >> np.uint64(30))) * _M1
+    z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def splitmix64_stream(seed: int, counters) -> np.ndarray:
+    """Word number ``i`` of the SplitMix64 sequence started at ``seed``.
+
+    The sequential generator adds the golden-ratio increment to its state and
+    then mixes; word i is therefore mix(seed + (i + 1) * gamma) mod 2**64,
+    which makes the generator counter-based.
+    """
+    c = np.asarray(counters, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        state = np.uint64(seed & 0xFFFFFFFFFFFFFFFF) + (c + np.uint64(1)) * np.uint64(SPLITMIX_GAMMA)
+        return _mix64(state)
+
+
+def normals_from_words(words: np.ndarray) -> np.ndarray:
+    """One standard normal per 64-bit word by the Box–Muller transform.
+
+    Two 24-bit fields of the word give u1, u2 = (k + 1/2) / 2**24 in (0, 1)
+    (exactly representable in fp32 as well), and z = sqrt(-2 ln u1) cos(2 pi u2).
+    """
+    w = np.asarray(words, dtype=np.uint64)
+    k1 = (w >> np.uint64(40)).astype(np.float64)
+    k2 = ((w >> np.uint64(16)) & np.uint64(0xFFFFFF)).astype(np.float64)
+    u1 = (k1 + 0.5) / 16777216.0
+    u2 = (k2 + 0.5) / 16777216.0
+    return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
+
+
+def counter_normals(seed: int, counters) -> np.ndarray:
+    return normals_from_words(splitmix64_stream(seed, counters))
+
+
+def orf_index_layout(block: int, row: int, col: int, d: int, kind: int) -> int:
+    """Counter of one normal used by :func:`build_omega`.
+
+    kind 0 = entry (row, col) of Gaussian block ``block``; kind 1 = component
+    ``col`` of the chi_d length vector of that block's row ``row``.
+    """
+    return ((block * d + row) * d + col) * 2 + kind
+
+
+# --------------------------------------------------------------------------
+# Omega (the projection): ORF and iid  —  [digest] §Methods (ORF bullet),
+# [digest] Zettelkasten "orthogonality strictly reduces variance" (block-wise
+# orthogonalisation when m > d), [summary] §A.2 (marginals preserved).
+# --------------------------------------------------------------------------
+
+
+def gram_schmidt_rows(G: np.ndarray) -> np.ndarray:
+    """Orthonormalise the rows of ``G`` in order by Gram–Schmidt (fp64).
+
+    Row i loses its components along the already orthonormal rows 0..i-1 (one
+    at a time, the modified form), then is divided by its length.
+    """
+    G = np.asarray(G, dtype=np.float64)
+    n = G.shape[0]
+    Qm = np.zeros_like(G)
+    for i in range(n):
+        v = G[i].copy()
+        for j in range(i):
+            v -= np.dot(Qm[j], v) * Qm[j]
+        Qm[i] = v / np.linalg.norm(v)
+    return Qm
+
+
+def build_omega(seed: int, m: int, d: int, orthogonal: bool = True,
+                return_parts: bool = False):
+    """Projection matrix Omega, shape [m, d], row i = omega_i.
+
+    orthogonal=True: ceil(m/d) independent d x d Gaussian blocks, rows of each
+    orthonormalised by Gram–Schmidt, row r of block b rescaled to the length
+    of the independent Gaussian vector (kind 1 counters); the first m rows of
+    the stacked blocks are kept.  orthogonal=False: iid N(0, 1) entries
+    (counter of entry (i, c) = (i*d + c)*2).
+    """
+    if orthogonal:
+        nb = -(-m // d)
+        rows = []
+        parts = []
+        r = np.arange(d)[:, None]
+        c = np.arange(d)[None, :]
+        for b in range(nb):
+            g_idx = ((b * d + r) * d + c) * 2
+            G = counter_normals(seed, g_idx)
+            chi = counter_normals(seed, g_idx + 1)
+            lengths = np.sqrt(np.sum(chi * chi, axis=1))
+            Qb = gram_schmidt_rows(G)
+            rows.append(Qb * lengths[:, None])
+            parts.append((G, Qb, lengths))
+        Omega = np.concatenate(rows, axis=0)[:m]
+        return (Omega, parts) if return_parts else Omega
+    i = np.arange(m)[:, None]
+    c = np.arange(d)[None, :]
+    Omega = counter_normals(seed, (i * d + c) * 2)
+    return (Omega, None) if return_parts else Omega
+
+
+# --------------------------------------------------------------------------
+# Feature maps and the softmax-kernel estimator — [digest] §Key equations,
+# [digest] §Methods (softmax-kernel decomposition, PRF), [su] §Simple
+# Derivation (the m-dimensional vectors q~, k~).
+# --------------------------------------------------------------------------
+
+
+def softmax_kernel(x: np.ndarray, y: np.ndarray) -> np.ndarray:
+    """SM(x, y) = exp(x^T y) over the last axis."""
+    return np.exp(np.sum(np.asarray(x, np.float64) * np.asarray(y, np.float64), axis=-1))
+
+
+def prf_features(X: np.ndarray, Omega: np.ndarray) -> np.ndarray:
+    """Positive random features phi(x) = m^{-1/2} exp(Omega x - ||x||^2 / 2).
+
+    X [..., L, d] (already multiplied by the temperature), Omega [m, d].
+    Returns [..., L, m].
+    """
+    X = np.asarray(X, dtype=np.float64)
+    Om = np.asarray(Omega, dtype=np.float64)
+    m = Om.shape[0]
+    proj = X @ Om.T
+    half_sq = 0.5 * np.sum(X * X, axis=-1, keepdims=True)
+    return np.exp(proj - half_sq) / math.sqrt(m)
+
+
+def trig_features(X: np.ndarray, Omega: np.ndarray) -> np.ndarray:
+    """Trigonometric (sin/cos) random features for the softmax kernel.
+
+    SM(x, y) = exp(||x||^2/2) exp(||y||^2/2) exp(-||x-y||^2/2) and the last
+    factor is E[cos(omega^T (x - y))]; so phi(x) = m^{-1/2} exp(||x||^2/2)
+    [sin(Omega x), cos(Omega x)] gives an unbiased estimator that can take
+    negative values ([digest] §Methods "why positive"; [summary] §2).
+    """
+    X = np.asarray(X, dtype=np.float64)
+    Om = np.asarray(Omega, dtype=np.float64)
+    m = Om.shape[0]
+    proj = X @ Om.T
+    amp = np.exp(0.5 * np.sum(X * X, axis=-1, keepdims=True)) / math.sqrt(m)
+    return np.concatenate([amp * np.sin(proj), amp * np.cos(proj)], axis=-1)
+
+
+def prf_estimator(x: np.ndarray, y: np.ndarray, Omega: np.ndarray) -> np.ndarray:
+    """SM^_m^PRF(x, y) = (1/m) sum_i exp(w_i.x - |x|^2/2) exp(w_i.y - |y|^2/2)."""
+    return np.sum(prf_features(x, Omega) * prf_features(y, Omega), axis=-1)
+
+
+def lemma2_mse(x: np.ndarray, y: np.ndarray, m: int) -> float:
+    """Lemma 2: MSE = (1/m) exp(|x+y|^2) SM(x,y)^2 (1 - exp(-|x+y|^2))."""
+    s2 = float(np.sum((np.asarray(x) + np.asarray(y)) ** 2))
+    sm = float(softmax_kernel(x, y))
+    return math.exp(s2) * sm * sm * (1.0 - math.exp(-s2)) / m
+
+
+# --------------------------------------------------------------------------
+# Attention — [digest] §Key equations (Attn^ = D^-1 phi(Q)(phi(K)^T V),
+# D = diag(phi(Q) phi(K)^T 1_L)), [digest] flowchart, [digest] §Methods
+# (causal prefix sum G_t), [summary] §2 (lower-triangular part), §A.2.
+# --------------------------------------------------------------------------
+
+
+def _features_qk(Q, K, Omega, scale):
+    q = scale * np.asarray(Q, dtype=np.float64)
+    k = scale * np.asarray(K, dtype=np.float64)
+    return prf_features(q, Omega), prf_features(k, Omega)
+
+
+def favor_bidirectional(Q, K, V, Omega, scale: float) -> np.ndarray:
+    """Bidirectional FAVOR+: D^{-1} phi(Q) (phi(K)^T V), linear order.
+
+    Q, K, V [..., L, d]; returns [..., L, d] in fp64.
+    """
+    pq, pk = _features_qk(Q, K, Omega, scale)
+    V = np.asarray(V, dtype=np.float64)
+    kv = np.swapaxes(pk, -1, -2) @ V              # [..., m, d]  phi(K)^T V
+    z = np.sum(pk, axis=-2)                       # [..., m]     phi(K)^T 1_L
+    num = pq @ kv                                 # [..., L, d]
+    den = np.einsum("...lm,...m->...l", pq, z)    # [..., L]     diag of D
+    return num / den[..., None]
+
+
+def favor_bidirectional_quadratic(Q, K, V, Omega, scale: float) -> np.ndarray:
+    """Same estimator in quadratic order: row-normalise phi(Q) phi(K)^T, times V."""
+    pq, pk = _features_qk(Q, K, Omega, scale)
+    A = pq @ np.swapaxes(pk, -1, -2)              # [..., L, L]
+    A = A / np.sum(A, axis=-1, keepdims=True)
+    return A @ np.asarray(V, dtype=np.float64)
+
+
+def favor_causal(Q, K, V, Omega, scale: float) -> np.ndarray:
+    """Unidirectional FAVOR+ by the prefix sum of the pages.
+
+    G_t = sum_{s<=t} phi(k_s) v_s^T and z_t = sum_{s<=t} phi(k_s) are carried
+    forward one token at a time; out_t = phi(q_t)^T G_t / phi(q_t)^T z_t.
+    """
+    pq, pk = _features_qk(Q, K, Omega, scale)
+    V = np.asarray(V, dtype=np.float64)
+    lead = V.shape[:-2]
+    L, d = V.shape[-2:]
+    m = pk.shape[-1]
+    G = np.zeros(lead + (m, d))
+    z = np.zeros(lead + (m,))
+    out = np.empty(lead + (L, d))
+    for t in range(L):
+        G += pk[..., t, :, None] * V[..., t, None, :]
+        z += pk[..., t, :]
+        num = np.einsum("...m,...md->...d", pq[..., t, :], G)
+        den = np.einsum("...m,...m->...", pq[..., t, :], z)
+        out[..., t, :] = num / den[..., None]
+    return out
+
+
+def favor_causal_quadratic(Q, K, V, Omega, scale: float) -> np.ndarray:
+    """Unidirectional FAVOR+ as the lower-triangular part (diagonal included)
+    of phi(Q) phi(K)^T, row-normalised, times V."""
+    pq, pk = _features_qk(Q, K, Omega, scale)
+    A = pq @ np.swapaxes(pk, -1, -2)
+    L = A.shape[-1]
+    A = A * np.tril(np.ones((L, L)))
+    A = A / np.sum(A, axis=-1, keepdims=True)
+    return A @ np.asarray(V, dtype=np.float64)
+
+
+def favor_rows(Q, K, V, Omega, scale: float, bh_rows, causal: bool) -> np.ndarray:
+    """Selected output rows of the estimator, for large inputs.
+
+    Q, K, V [BH, L, d]; ``bh_rows`` is a list of (head index, t).  Row t of
+    head h is sum_{s in S} (phi(q_t).phi(k_s)) v_s / sum_{s in S} phi(q_t).phi(k_s)
+    with S = all tokens (bidirectional) or s <= t (causal).  phi(K)^T V over S
+    is evaluated as one matrix product per head and range.
+    """
+    bh_rows = list(bh_rows)
+    out = np.empty((len(bh_rows), np.asarray(V).shape[-1]))
+    by_head: dict[int, list[tuple[int, int]]] = {}
+    for n, (h, t) in enumerate(bh_rows):
+        by_head.setdefault(int(h), []).append((int(t), n))
+    for h, items in by_head.items():
+        k = scale * np.asarray(K[h], dtype=np.float64)
+        v = np.asarray(V[h], dtype=np.float64)
+        pk = prf_features(k, Omega)
+        if not causal:
+            kv = pk.T @ v
+            z = pk.sum(axis=0)
+        for t, n in items:
+            q = scale * np.asarray(Q[h][t], dtype=np.float64)
+            pq = prf_features(q[None, :], Omega)[0]
+            if causal:
+                kv = pk[: t + 1].T @ v[: t + 1]
+                z = pk[: t + 1].sum(axis=0)
+            out[n] = (pq @ kv) / (pq @ z)
+    return out
+
+
+def softmax_attention(Q, K, V, scale: float, causal: bool = False) -> np.ndarray:
+    """Exact softmax((scale Q)(scale K)^T) V, the quantity FAVOR+ estimates."""
+    q = scale * np.asarray(Q, dtype=np.float64)
+    k = scale * np.asarray(K, dtype=np.float64)
+    S = q @ np.swapaxes(k, -1, -2)
+    if causal:
+        L = S.shape[-1]
+        S = np.where(np.tril(np.ones((L, L), dtype=bool)), S, -np.inf)
+    S = S - np.max(S, axis=-1, keepdims=True)
+    P = np.exp(S)
+    P = P / np.sum(P, axis=-1, keepdims=True)
+    return P @ np.asarray(V, dtype=np.float64)
+
+
+def rowwise_rel_err(got: np.ndarray, ref: np.ndarray) -> float:
+    """max over rows of max_j |got - ref| / max_j |ref| (normwise per row)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    num = np.max(np.abs(got - ref), axis=-1)
+    den = np.max(np.abs(ref), axis=-1)
+    den = np.where(den == 0, 1.0, den)
+    return float(np.max(num / den))
