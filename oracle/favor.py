@@ -90,14 +90,16 @@ def splitmix64_stream(seed: int, counters) -> np.ndarray:
 def normals_from_words(words: np.ndarray) -> np.ndarray:
     """One standard normal per 64-bit word by the Box–Muller transform.
 
-    Two 24-bit fields of the word give u1, u2 = (k + 1/2) / 2**24 in (0, 1)
-    (exactly representable in fp32 as well), and z = sqrt(-2 ln u1) cos(2 pi u2).
+    Two 23-bit fields of the word (bits 41..63 and 18..40) give
+    u1, u2 = (k + 1/2) / 2**23 in (0, 1) -- (2k + 1) / 2**24 has at most 24
+    significant bits, so the same u is exact in fp32 -- and
+    z = sqrt(-2 ln u1) cos(2 pi u2).
     """
     w = np.asarray(words, dtype=np.uint64)
-    k1 = (w >> np.uint64(40)).astype(np.float64)
-    k2 = ((w >> np.uint64(16)) & np.uint64(0xFFFFFF)).astype(np.float64)
-    u1 = (k1 + 0.5) / 16777216.0
-    u2 = (k2 + 0.5) / 16777216.0
+    k1 = (w >> np.uint64(41)).astype(np.float64)
+    k2 = ((w >> np.uint64(18)) & np.uint64(0x7FFFFF)).astype(np.float64)
+    u1 = (k1 + 0.5) / 8388608.0
+    u2 = (k2 + 0.5) / 8388608.0
     return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
 
 

@@ -45,18 +45,23 @@ def test_box_muller_normals_are_standard_normal():
 
 
 def test_box_muller_field_extraction():
-    # word with k1 = 2**23 (u1 = (2**23 + .5) / 2**24) and k2 = 0 (u2 = .5 / 2**24)
+    # word with k1 = 2**22 (u1 = (2**22 + .5) / 2**23) and k2 = 0 (u2 = .5 / 2**23)
     w = np.array([(1 << 63)], dtype=np.uint64)
-    u1 = (2 ** 23 + 0.5) / 2 ** 24
-    u2 = 0.5 / 2 ** 24
+    u1 = (2 ** 22 + 0.5) / 2 ** 23
+    u2 = 0.5 / 2 ** 23
     want = math.sqrt(-2 * math.log(u1)) * math.cos(2 * math.pi * u2)
     assert orc.normals_from_words(w)[0] == pytest.approx(want, rel=1e-15)
-    # k2 field taken from bits 16..39
-    w2 = np.array([(5 << 16)], dtype=np.uint64)
-    u1 = 0.5 / 2 ** 24
-    u2 = 5.5 / 2 ** 24
+    # k2 field taken from bits 18..40; bits below 18 are ignored
+    w2 = np.array([(5 << 18) | 0x3FFFF], dtype=np.uint64)
+    u1 = 0.5 / 2 ** 23
+    u2 = 5.5 / 2 ** 23
     want2 = math.sqrt(-2 * math.log(u1)) * math.cos(2 * math.pi * u2)
     assert orc.normals_from_words(w2)[0] == pytest.approx(want2, rel=1e-15)
+    # every u is exactly representable in fp32
+    words = orc.splitmix64_stream(3, np.arange(1000))
+    k = (words >> np.uint64(41)).astype(np.float64)
+    u = (k + 0.5) / 2 ** 23
+    assert np.array_equal(u.astype(np.float32).astype(np.float64), u)
 
 
 @pytest.mark.parametrize("d", [4, 16, 64])
