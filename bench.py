@@ -1,0 +1,482 @@
+"""Throughput of the FAVOR+ forward hot path on GB300.
+
+One step = the whole hot path over one batch of synthetic input:
+  build Omega (ORF) -> bidirectional FAVOR+ (state + output) -> causal
+  FAVOR+ (superchunk states + scan/output), on the same Q, K, V.
+Metric: tokens per second, a token being one (batch, position) with all H
+heads, processed by both the bidirectional and the causal forward pass.
+
+Default workload: bidir/causal bf16, B=8 H=8 L=4096 d=64 m=256 (the Regular
+Transformer attention shape, 8 heads of 64).  ``--workload`` selects another
+(see ``workloads``).  Prints ONE JSON line (rank 0).
+
+Timed region: K replays of a CUDA graph holding one step, input sets rotated
+so that the bytes touched between two uses of a set exceed L2; CUDA events on
+the launching stream; barrier + synchronize on both sides; max over ranks.
+Per-kernel durations (roofline) come from an event-instrumented pass of the
+same steps.  ``--impl reference`` times the fp64 CPU oracle instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+DEFAULT_WORKLOAD = "bidir-bf16-B8H8L4096-d64-m256"
+L2_BYTES = 129 * 1024 * 1024
+STAGES = ("build_orf", "bidir_state", "bidir_output", "causal_state", "causal_output")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def workload_for(name: str):
+    w = wl.get(name)
+    return w
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work per launch (per head-token figures times B*H*L)
+# ---------------------------------------------------------------------------
+
+def algorithmic(w, stage: str):
+    """(bytes, flops) that the stage must move / compute for one launch."""
+    e = 4 if w.dtype == "f32" else 2
+    ht = w.B * w.H * w.L
+    md, md1 = w.m * w.d, w.m * (w.d + 1)
+    state_bytes = w.B * w.H * w.m * (w.d + 1) * 4
+    if stage == "bidir_state":
+        return ht * 2 * w.d * e + state_bytes, ht * (2 * md + 2 * md1)
+    if stage == "bidir_output":
+        return ht * 2 * w.d * e + state_bytes, ht * (2 * md + 2 * md1)
+    if stage == "causal_state":
+        return ht * 2 * w.d * e, ht * (2 * md + 2 * md1)
+    if stage == "causal_output":
+        return ht * 4 * w.d * e, ht * (4 * md + 4 * md1)
+    if stage == "build_orf":
+        return w.m * w.d * 4, 0
+    raise KeyError(stage)
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            out_dir = os.path.join(ROOT, "gpurun_out")
+            os.makedirs(out_dir, exist_ok=True)
+            self.path = os.path.join(out_dir, f"clocks_{os.getpid()}.csv")
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# traffic from the committed ncu summary (null when the kernel source changed)
+# ---------------------------------------------------------------------------
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_softmax_attention_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(stage: str, workload: str):
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    src = kernel_source_hash()
+    for f in sorted(os.listdir(pdir)):
+        if not f.endswith(".md"):
+            continue
+        text = open(os.path.join(pdir, f)).read()
+        m_stage = re.search(r"^stage:\s*(\S+)", text, re.M)
+        m_wl = re.search(r"^workload:\s*(\S+)", text, re.M)
+        m_src = re.search(r"^source_hash:\s*(\S+)", text, re.M)
+        m_tr = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+        if m_stage and m_wl and m_src and m_tr and m_stage.group(1) == stage and m_wl.group(1) == workload:
+            return float(m_tr.group(1)) if m_src.group(1) == src else None
+    return None
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, rank, world, local_rank):
+    import linear_softmax_attention_gb300 as favor
+
+    favor.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = workload_for(args.workload)
+    dt = w.torch_dtype
+    B, H, L, d, m = w.B, w.H, w.L, w.d, w.m
+    bytes_per_set = 3 * B * H * L * d * (4 if w.dtype == "f32" else 2)
+    n_sets = max(2, -(-2 * L2_BYTES // bytes_per_set) + 1)
+    n_sets = min(n_sets, 8)
+    sets = []
+    for i in range(n_sets):
+        q, k, v = wl.make_qkv(w, seed=1000 * rank + i, device=dev)
+        sets.append((q, k, v))
+    O_b = torch.empty_like(sets[0][0])
+    O_c = torch.empty_like(sets[0][0])
+    omega = torch.empty((m, d), dtype=torch.float32, device=dev)
+    ws_b = favor.new_workspace(False, B, H, L, d, m, dt, device=dev)
+    ws_c = favor.new_workspace(True, B, H, L, d, m, dt, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    s = w.qk_scale
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, seed_call):
+        q, k, v = sets[i % n_sets]
+        favor.build_orf(seed_call, omega, stream=stream)
+        favor.bidir_state(k, v, omega, s, ws_b, dev_status=status, stream=stream)
+        favor.bidir_output(q, omega, s, ws_b, O=O_b, dev_status=status, stream=stream)
+        favor.causal_state(k, v, omega, s, ws_c, dev_status=status, stream=stream)
+        favor.causal_output(q, k, v, omega, s, ws_c, O=O_c, dev_status=status, stream=stream)
+
+    launches_per_step = 5 + (1 if favor.path_name(False, d, m, dt) == "simt" else 0)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            step(i, wl.omega_seed_for_call(w, i))
+    torch.cuda.synchronize(dev)
+
+    # per-kernel durations: events around each stage on the launching stream
+    n_inst = min(args.steps, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(n_inst)]
+    with torch.cuda.stream(stream):
+        for i in range(n_inst):
+            q, k, v = sets[i % n_sets]
+            e = evs[i]
+            e[0].record(stream)
+            favor.build_orf(wl.omega_seed_for_call(w, i), omega, stream=stream)
+            e[1].record(stream)
+            favor.bidir_state(k, v, omega, s, ws_b, dev_status=status, stream=stream)
+            e[2].record(stream)
+            favor.bidir_output(q, omega, s, ws_b, O=O_b, dev_status=status, stream=stream)
+            e[3].record(stream)
+            favor.causal_state(k, v, omega, s, ws_c, dev_status=status, stream=stream)
+            e[4].record(stream)
+            favor.causal_output(q, k, v, omega, s, ws_c, O=O_c, dev_status=status, stream=stream)
+            e[5].record(stream)
+    torch.cuda.synchronize(dev)
+    stage_ms = {st: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n_inst))
+                for j, st in enumerate(STAGES)}
+
+    # graphs: one per input set (and per Omega seed when Omega is redrawn)
+    graphs = []
+    n_graphs = n_sets if not w.redraw_omega else max(n_sets, 4)
+    with torch.cuda.stream(stream):
+        for i in range(n_graphs):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(i, wl.omega_seed_for_call(w, i))
+            graphs.append(g)
+    torch.cuda.synchronize(dev)
+    for i in range(max(3, args.warmup)):
+        graphs[i % n_graphs].replay()
+    torch.cuda.synchronize(dev)
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    t_wall0 = time.perf_counter()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(args.steps):
+            graphs[i % n_graphs].replay()
+        end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    elapsed_ms = start.elapsed_time(end)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        dist.barrier()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after the timed region")
+
+    ms_per_step = elapsed_ms / args.steps
+    tokens_per_step = B * L
+    value = world * tokens_per_step * args.steps / (elapsed_ms / 1e3)
+
+    # e2e: pinned host buffers -> H2D, the same step, D2H of both outputs
+    e2e = None
+    if args.e2e_steps > 0:
+        hq, hk, hv = (t.cpu().pin_memory() for t in sets[0])
+        dq, dk, dv = (torch.empty_like(t) for t in sets[0])
+        ho_b = torch.empty(O_b.shape, dtype=O_b.dtype, pin_memory=True)
+        ho_c = torch.empty(O_c.shape, dtype=O_c.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        d2h = ho_b.numel() * ho_b.element_size() * 2
+
+        def e2e_step(i):
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            favor.build_orf(wl.omega_seed_for_call(w, i), omega, stream=stream)
+            favor.fwd_bidir(dq, dk, dv, omega, s, ws_b, O=O_b, dev_status=status, stream=stream)
+            favor.fwd_causal(dq, dk, dv, omega, s, ws_c, O=O_c, dev_status=status, stream=stream)
+            ho_b.copy_(O_b, non_blocking=True)
+            ho_c.copy_(O_c, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                e2e_step(i)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(args.e2e_steps):
+                e2e_step(i)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        e2e = {"value": world * tokens_per_step / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    hbm, tc_burst, tc_sus, peak_kind = load_peaks()
+    # dominant kernel: largest share of the step
+    dom = max((st for st in STAGES if st != "build_orf"), key=lambda st: stage_ms[st])
+    nbytes, nflops = algorithmic(w, dom)
+    t_dom = stage_ms[dom] / 1e3
+    t_hbm = nbytes / (hbm * 1e9)
+    t_tc = nflops / (tc_sus * 1e12)
+    if t_tc > t_hbm:
+        roof = {"bound": "tensor", "achieved": nflops / t_dom / 1e12, "peak": tc_sus, "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": nbytes / t_dom / 1e9, "peak": hbm, "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = profiled_traffic(dom, w.name)
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peak_kind} ({'sustained bf16' if roof['bound'] == 'tensor' else 'HBM copy'})"
+    roof["algorithmic_bytes_per_launch"] = nbytes
+    roof["algorithmic_flops_per_launch"] = nflops
+    stages_out = {}
+    for st in STAGES:
+        b_, f_ = algorithmic(w, st)
+        t_ = stage_ms[st] / 1e3
+        stages_out[st] = {"ms": stage_ms[st], "GB/s": b_ / t_ / 1e9, "TFLOP/s": f_ / t_ / 1e12,
+                          "hbm_frac": b_ / t_ / 1e9 / hbm,
+                          "roofline_frac": max(b_ / (hbm * 1e9), f_ / (tc_sus * 1e12)) / t_}
+    bidir_ms = stage_ms["bidir_state"] + stage_ms["bidir_output"]
+    causal_ms = stage_ms["causal_state"] + stage_ms["causal_output"]
+
+    line = {
+        "metric": "FAVOR+ fwd tokens/sec (bidir & causal) on 1 GB300; % of roofline",
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded; workloads module)",
+        "config": {"workload": w.name, "B": B, "H": H, "L": L, "d": d, "m": m, "qk_scale": s,
+                   "step": "build Omega + bidirectional + causal forward", "tokens_per_step": tokens_per_step,
+                   "path": favor.path_name(False, d, m, dt), "l2": f"{n_sets} rotating input sets "
+                   f"({n_sets * bytes_per_set / 2**20:.0f} MiB > L2)", "timing": "CUDA graph replay per step",
+                   "parallelism": f"replicas x{world}"},
+        "modes": {"bidir_tokens_per_s": tokens_per_step / (bidir_ms / 1e3),
+                  "causal_tokens_per_s": tokens_per_step / (causal_ms / 1e3),
+                  "build_orf_ms": stage_ms["build_orf"]},
+        "stages": stages_out,
+        "roofline": roof,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s_timed": t_wall,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=12.0)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle: the reported baseline and the reference arm
+# ---------------------------------------------------------------------------
+
+def oracle_sample_step(w, heads: int, seed: int, L: int | None = None):
+    """One bounded oracle step: Omega + bidirectional + causal on `heads` heads
+    of the workload (optionally its first L tokens)."""
+    import numpy as np
+
+    import oracle as orc
+    q, k, v = wl.make_qkv(w, seed=seed, B=1, H=heads, L=L)
+    f64 = (lambda t: t.float().numpy().astype(np.float64))
+    Q, K, V = f64(q), f64(k), f64(v)
+    om = orc.build_omega(wl.omega_seed_for_call(w, seed), w.m, w.d)
+    orc.favor_bidirectional(Q, K, V, om, w.qk_scale)
+    orc.favor_causal(Q, K, V, om, w.qk_scale)
+
+
+def cpu_baseline(w, budget_s: float):
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    heads = 1
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle_sample_step(w, heads, seed=n)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt_s = time.perf_counter() - t0
+    # a step covers B*L tokens x H heads; the sample covers `heads` heads of L tokens
+    tokens = n * w.L * heads / w.H
+    return {"value": tokens / dt_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} x (Omega build + bidirectional + causal) on {heads} head(s) of L={w.L}, "
+                      f"d={w.d}, m={w.m} in fp64 NumPy; tokens = head-tokens / H"}
+
+
+def run_reference(args, rank, world):
+    """The fp64 CPU oracle as the reference arm: exactly K timed steps, each
+    on one head of a token prefix sized so that the run stays within minutes."""
+    if rank != 0:
+        return
+    w = workload_for(args.workload)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    t0 = time.perf_counter()
+    oracle_sample_step(w, 1, seed=0)
+    t_full = time.perf_counter() - t0
+    budget = 90.0
+    Ls = w.L if args.steps * t_full <= budget else max(64, int(w.L * budget / (args.steps * t_full)))
+    for i in range(max(0, min(args.warmup, 3) - 1)):
+        oracle_sample_step(w, 1, seed=1 + i, L=Ls)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_sample_step(w, 1, seed=100 + i, L=Ls)
+    dt_s = time.perf_counter() - t0
+    tokens_per_step = Ls / w.H
+    value = tokens_per_step * args.steps / dt_s
+    sample = f"one head of {Ls} tokens per step (Omega build + bidirectional + causal, fp64 NumPy); " \
+             f"tokens = head-tokens / H"
+    line = {
+        "impl": "reference",
+        "metric": "FAVOR+ fwd tokens/sec (bidir & causal) on 1 GB300; % of roofline",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt_s / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; workloads module)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "m": w.m,
+                   "step": "build Omega + bidirectional + causal forward"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

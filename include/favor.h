@@ -1,0 +1,182 @@
+/*
+ * favor.h — C ABI of the FAVOR+ forward pass for one GB300 GPU (sm_103a).
+ *
+ * FAVOR+ ("Fast Attention Via positive Orthogonal Random features") replaces
+ * softmax(QK^T)V by a product of random-feature matrices:
+ *
+ *   phi(x)       = m^{-1/2} exp(Omega x - ||x||^2 / 2)            (PRF map)
+ *   bidirectional:  Attn^(Q,K,V) = D^{-1} phi(Q) (phi(K)^T V),
+ *                   D = diag(phi(Q) (phi(K)^T 1_L))
+ *   unidirectional: out_t = phi(q_t)^T G_t / phi(q_t)^T z_t,
+ *                   G_t = sum_{s<=t} phi(k_s) v_s^T,  z_t = sum_{s<=t} phi(k_s)
+ *
+ * Sources: "Performer — Rethinking Attention with Performers" (blog digest),
+ * §Key equations and §Methods (FAVOR+); "Rethinking Attention with
+ * Performers" (arXiv:2009.14794v4 summary), §2 FAVOR+ mechanism and §A.2
+ * unidirectional attention; "From Performer to Linear Attention" (Su), §Simple
+ * Derivation.
+ *
+ * Conventions shared by every call:
+ *  - Q, K, V, O: device pointers to contiguous [B, H, L, d] tensors, d
+ *    fastest, all of dtype `dt`; 16-byte aligned.  O may not alias Q, K, V.
+ *  - omega: device pointer to fp32 [m, d], row i = omega_i, shared by every
+ *    (b, h) and by Q and K.
+ *  - qk_scale: temperature s; q and k enter the feature map as s*q and s*k
+ *    (s = d^{-1/4} reproduces softmax(QK^T / sqrt(d))).
+ *  - workspace: caller-owned device scratch of at least
+ *    favor_workspace_bytes(...) bytes, 256-byte aligned; its contents between
+ *    calls do not matter.  Calls that share a workspace must be ordered on
+ *    one stream.
+ *  - dev_status: optional device int32 (may be NULL).  Kernels store a
+ *    non-zero favor_status there when they detect a bounded wait that ran out
+ *    (FAVOR_ERR_TIMEOUT) or a non-finite / non-positive normaliser
+ *    (FAVOR_ERR_NONFINITE); the library never clears it.  Read it after the
+ *    stream has synchronised.
+ *  - stream: a cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - The library never allocates, frees or synchronises; all launches are
+ *    asynchronous on `stream`.  The return value reports argument checks
+ *    (made before anything is launched) and launch errors.
+ *  - Supported: 1 <= L, 1 <= d <= 128, 1 <= m <= 512, B*H >= 1,
+ *    B*H*L*d < 2^31.  bf16 with d in {64, 128} and m a multiple of 128 runs on
+ *    the tcgen05 tensor-core kernels; every other supported shape runs on
+ *    CUDA-core kernels with fp32 arithmetic.
+ */
+#ifndef FAVOR_H_
+#define FAVOR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FAVOR_API_VERSION 1
+
+typedef enum favor_status {
+  FAVOR_OK = 0,
+  FAVOR_ERR_INVALID_ARG = 1,  /* a pointer, size or alignment is out of contract */
+  FAVOR_ERR_UNSUPPORTED = 2,  /* well-formed but outside the supported shapes    */
+  FAVOR_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed      */
+  FAVOR_ERR_TIMEOUT = 4,      /* device only: a bounded wait gave up              */
+  FAVOR_ERR_NONFINITE = 5     /* device only: non-finite or <= 0 normaliser       */
+} favor_status;
+
+typedef enum favor_dtype {
+  FAVOR_F32 = 0,   /* fp32 storage, fp32 arithmetic                            */
+  FAVOR_BF16 = 1   /* bf16 storage, bf16 tensor-core operands, fp32 accumulate */
+} favor_dtype;
+
+/* Library version (FAVOR_API_VERSION of the build). */
+int favor_api_version(void);
+
+/* Static English text for a status code (never NULL). */
+const char* favor_status_string(favor_status s);
+
+/*
+ * favor_build_orf — draw the projection Omega [m, d] (fp32, row-major) into
+ * the caller's device buffer `omega`, on `stream`.
+ *
+ * orthogonal = 1 (ORF): ceil(m/d) independent d x d blocks; block b's rows
+ * are the Gram–Schmidt orthonormalisation of a Gaussian matrix, and row r is
+ * then scaled to the length of an independent N(0, I_d) vector (a chi_d
+ * sample), so each row keeps the N(0, I_d) marginal ("Performer" digest,
+ * §Methods ORF bullet and the block-wise rule for m > d; arXiv summary §A.2:
+ * orthogonality with marginals preserved).  The first m stacked rows are
+ * kept.  orthogonal = 0: iid N(0, 1) entries.
+ *
+ * Random numbers: SplitMix64 word i = mix(seed + (i+1)*0x9E3779B97F4A7C15);
+ * one normal per word by Box–Muller, z = sqrt(-2 ln u1) cos(2 pi u2) with
+ * u1 = (bits[41..63] + 1/2) / 2^23 and u2 = (bits[18..40] + 1/2) / 2^23.
+ * Counter of Gaussian entry (r, c) of block b: ((b*d + r)*d + c)*2; of
+ * component c of row r's length vector: the same + 1; iid entry (i, c):
+ * (i*d + c)*2.  Arithmetic is fp32 (two Gram–Schmidt sweeps).
+ *
+ * Errors: FAVOR_ERR_INVALID_ARG if omega is NULL or m, d out of range
+ * (1 <= d <= 128, 1 <= m <= 512).
+ */
+favor_status favor_build_orf(uint64_t seed, int m, int d, int orthogonal,
+                             float* omega, void* stream);
+
+/*
+ * favor_workspace_bytes — scratch bytes needed by favor_fwd_bidir (causal = 0)
+ * or favor_fwd_causal (causal = 1) and by their stage calls for the given
+ * shape.  Returns 0 for arguments outside the supported shapes.
+ */
+size_t favor_workspace_bytes(int causal, int B, int H, int L, int d, int m,
+                             favor_dtype dt);
+
+/*
+ * favor_fwd_bidir — bidirectional FAVOR+:
+ *   O = D^{-1} phi(s Q) (phi(s K)^T V),  D = diag(phi(s Q) phi(s K)^T 1_L)
+ * ("Performer" digest, §Key equations, linear attention line; flowchart:
+ * phi(K)^T V and phi(K)^T 1 first, then phi(Q) times each, then the
+ * row-wise divide).  Equivalent to favor_bidir_state then favor_bidir_output.
+ */
+favor_status favor_fwd_bidir(const void* Q, const void* K, const void* V, void* O,
+                             int B, int H, int L, int d,
+                             const float* omega, int m, favor_dtype dt, float qk_scale,
+                             void* workspace, size_t ws_bytes,
+                             int32_t* dev_status, void* stream);
+
+/*
+ * favor_fwd_causal — unidirectional FAVOR+ (diagonal included):
+ *   O_t = phi(s q_t)^T G_t / phi(s q_t)^T z_t,
+ *   G_t = sum_{s<=t} phi(s k_s) v_s^T,  z_t = sum_{s<=t} phi(s k_s)
+ * ("Performer" digest, §Methods causal bullet; arXiv summary §2 "lower
+ * triangular part" and §A.2 prefix sums).  Equivalent to favor_causal_state
+ * then favor_causal_output.
+ */
+favor_status favor_fwd_causal(const void* Q, const void* K, const void* V, void* O,
+                              int B, int H, int L, int d,
+                              const float* omega, int m, favor_dtype dt, float qk_scale,
+                              void* workspace, size_t ws_bytes,
+                              int32_t* dev_status, void* stream);
+
+/*
+ * Stage calls (same arguments as the full calls; pointers a stage does not
+ * read may be NULL).  They let a caller time or reuse each half:
+ *
+ * favor_bidir_state  — reads K, V; writes phi(K)^T [V | 1] (stabilised, one
+ *                      shared scale per head) into the workspace.
+ * favor_bidir_output — reads Q and the workspace state; writes O.
+ * favor_causal_state — reads K, V; writes one phi(K)^T [V | 1] per
+ *                      superchunk of the sequence into the workspace.
+ * favor_causal_output— reads Q, K, V and those superchunk states; writes O.
+ *
+ * A *_output call must follow the matching *_state call with the same shape,
+ * omega, qk_scale and workspace on the same stream.
+ */
+favor_status favor_bidir_state(const void* Q, const void* K, const void* V, void* O,
+                               int B, int H, int L, int d,
+                               const float* omega, int m, favor_dtype dt, float qk_scale,
+                               void* workspace, size_t ws_bytes,
+                               int32_t* dev_status, void* stream);
+favor_status favor_bidir_output(const void* Q, const void* K, const void* V, void* O,
+                                int B, int H, int L, int d,
+                                const float* omega, int m, favor_dtype dt, float qk_scale,
+                                void* workspace, size_t ws_bytes,
+                                int32_t* dev_status, void* stream);
+favor_status favor_causal_state(const void* Q, const void* K, const void* V, void* O,
+                                int B, int H, int L, int d,
+                                const float* omega, int m, favor_dtype dt, float qk_scale,
+                                void* workspace, size_t ws_bytes,
+                                int32_t* dev_status, void* stream);
+favor_status favor_causal_output(const void* Q, const void* K, const void* V, void* O,
+                                 int B, int H, int L, int d,
+                                 const float* omega, int m, favor_dtype dt, float qk_scale,
+                                 void* workspace, size_t ws_bytes,
+                                 int32_t* dev_status, void* stream);
+
+/*
+ * favor_path_name — which kernel family a call with these arguments uses:
+ * "tcgen05" (bf16 tensor-core kernels), "simt" (CUDA-core fp32 kernels) or
+ * "unsupported".  Static string, never NULL.
+ */
+const char* favor_path_name(int causal, int d, int m, favor_dtype dt);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FAVOR_H_ */

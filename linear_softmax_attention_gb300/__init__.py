@@ -1,0 +1,168 @@
+"""FAVOR+ attention forward pass on one GB300 — thin Python binding.
+
+Every function here only marshals arguments (device pointers, sizes, the
+current CUDA stream) into the C ABI of ``libfavor.so`` (``include/favor.h``);
+all arithmetic runs in the library's CUDA kernels.  PyTorch provides device
+memory and streams.  There is no fallback: if the library is missing or a
+call fails, an exception is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "load", "lib_path", "FavorError", "F32", "BF16", "api_version", "path_name", "build_orf", "new_omega",
+    "workspace_bytes", "new_workspace", "fwd_bidir", "fwd_causal", "bidir_state", "bidir_output",
+    "causal_state", "causal_output", "status_string", "ENTRY_POINTS",
+]
+
+F32 = 0
+BF16 = 1
+_DT = {torch.float32: F32, torch.bfloat16: BF16}
+
+ENTRY_POINTS = ("favor_fwd_bidir", "favor_fwd_causal", "favor_bidir_state", "favor_bidir_output",
+                "favor_causal_state", "favor_causal_output")
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lib = None
+
+
+class FavorError(RuntimeError):
+    pass
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "libfavor.so")
+
+
+def load():
+    """Load libfavor.so (built by ``linear_softmax_attention_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise FavorError(f"{path} is missing: build it with `python -m linear_softmax_attention_gb300.build`")
+    lib = ctypes.CDLL(path)
+    c_int, c_size, c_vp, c_float = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
+    lib.favor_api_version.restype = c_int
+    lib.favor_status_string.restype = ctypes.c_char_p
+    lib.favor_status_string.argtypes = [c_int]
+    lib.favor_path_name.restype = ctypes.c_char_p
+    lib.favor_path_name.argtypes = [c_int, c_int, c_int, c_int]
+    lib.favor_build_orf.restype = c_int
+    lib.favor_build_orf.argtypes = [ctypes.c_uint64, c_int, c_int, c_int, c_vp, c_vp]
+    lib.favor_workspace_bytes.restype = c_size
+    lib.favor_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int, c_int]
+    fwd_args = [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_vp, c_int, c_int, c_float, c_vp, c_size,
+                c_vp, c_vp]
+    for name in ENTRY_POINTS:
+        fn = getattr(lib, name)
+        fn.restype = c_int
+        fn.argtypes = fwd_args
+    _lib = lib
+    return lib
+
+
+def api_version() -> int:
+    return load().favor_api_version()
+
+
+def status_string(code: int) -> str:
+    return load().favor_status_string(code).decode()
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise FavorError(f"{what}: {status_string(code)} (status {code})")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def path_name(causal: bool, d: int, m: int, dtype) -> str:
+    return load().favor_path_name(int(causal), d, m, _DT[dtype]).decode()
+
+
+def build_orf(seed: int, omega: torch.Tensor, orthogonal: bool = True, stream=None) -> torch.Tensor:
+    """Fill ``omega`` (fp32 [m, d] on the GPU) with the projection for ``seed``."""
+    if omega.dtype != torch.float32 or not omega.is_cuda or not omega.is_contiguous() or omega.dim() != 2:
+        raise FavorError("omega must be a contiguous fp32 CUDA tensor [m, d]")
+    m, d = omega.shape
+    _check(load().favor_build_orf(ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), m, d, int(bool(orthogonal)),
+                                  omega.data_ptr(), _stream_handle(stream)), "favor_build_orf")
+    return omega
+
+
+def new_omega(seed: int, m: int, d: int, orthogonal: bool = True, device="cuda") -> torch.Tensor:
+    om = torch.empty((m, d), dtype=torch.float32, device=device)
+    return build_orf(seed, om, orthogonal)
+
+
+def workspace_bytes(causal: bool, B: int, H: int, L: int, d: int, m: int, dtype) -> int:
+    n = load().favor_workspace_bytes(int(causal), B, H, L, d, m, _DT[dtype])
+    if n == 0:
+        raise FavorError(f"unsupported shape B={B} H={H} L={L} d={d} m={m} {dtype}")
+    return n
+
+
+def new_workspace(causal: bool, B: int, H: int, L: int, d: int, m: int, dtype, device="cuda") -> torch.Tensor:
+    n = workspace_bytes(causal, B, H, L, d, m, dtype)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def _call(name: str, Q, K, V, O, omega, qk_scale, workspace, dev_status, stream):
+    ref = next(t for t in (Q, K, V, O) if t is not None)
+    B, H, L, d = ref.shape
+    m = omega.shape[0]
+    dt = _DT[ref.dtype]
+    for t in (Q, K, V, O):
+        if t is not None and (not t.is_cuda or not t.is_contiguous() or t.dtype != ref.dtype
+                              or tuple(t.shape) != (B, H, L, d)):
+            raise FavorError(f"{name}: Q/K/V/O must be contiguous CUDA tensors of one dtype and shape [B,H,L,d]")
+    if omega.dtype != torch.float32 or omega.shape[1] != d or not omega.is_contiguous():
+        raise FavorError(f"{name}: omega must be contiguous fp32 [m, {d}]")
+    ptr = (lambda t: t.data_ptr() if t is not None else None)
+    code = getattr(load(), name)(ptr(Q), ptr(K), ptr(V), ptr(O), B, H, L, d, omega.data_ptr(), m, dt,
+                                 float(qk_scale), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                 ptr(dev_status), _stream_handle(stream))
+    _check(code, name)
+    return O
+
+
+def _out_like(x, O):
+    return torch.empty_like(x) if O is None else O
+
+
+def fwd_bidir(Q, K, V, omega, qk_scale, workspace, O=None, dev_status=None, stream=None):
+    """Bidirectional FAVOR+; returns O [B, H, L, d] (dtype of Q)."""
+    return _call("favor_fwd_bidir", Q, K, V, _out_like(Q, O), omega, qk_scale, workspace, dev_status, stream)
+
+
+def fwd_causal(Q, K, V, omega, qk_scale, workspace, O=None, dev_status=None, stream=None):
+    """Unidirectional (causal, prefix-sum) FAVOR+; returns O [B, H, L, d]."""
+    return _call("favor_fwd_causal", Q, K, V, _out_like(Q, O), omega, qk_scale, workspace, dev_status, stream)
+
+
+def bidir_state(K, V, omega, qk_scale, workspace, dev_status=None, stream=None):
+    _call("favor_bidir_state", None, K, V, None, omega, qk_scale, workspace, dev_status, stream)
+
+
+def bidir_output(Q, omega, qk_scale, workspace, O=None, dev_status=None, stream=None):
+    return _call("favor_bidir_output", Q, None, None, _out_like(Q, O), omega, qk_scale, workspace, dev_status,
+                 stream)
+
+
+def causal_state(K, V, omega, qk_scale, workspace, dev_status=None, stream=None):
+    _call("favor_causal_state", None, K, V, None, omega, qk_scale, workspace, dev_status, stream)
+
+
+def causal_output(Q, K, V, omega, qk_scale, workspace, O=None, dev_status=None, stream=None):
+    return _call("favor_causal_output", Q, K, V, _out_like(Q, O), omega, qk_scale, workspace, dev_status, stream)

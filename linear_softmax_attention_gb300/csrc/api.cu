@@ -1,0 +1,140 @@
+// C ABI entry points: argument checks, workspace planning and dispatch.
+#include <cmath>
+
+#include "common.cuh"
+#include "tc.cuh"
+
+#include <mutex>
+#include <unordered_map>
+
+using favor::Shape;
+
+namespace favor {
+
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, size_t> done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& have = done[dev][kernel];
+  if (have >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
+
+}  // namespace favor
+
+namespace {
+
+constexpr int kVersion = FAVOR_API_VERSION;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+favor_status shape_ok(int B, int H, int L, int d, int m, favor_dtype dt) {
+  if (B < 1 || H < 1 || L < 1 || d < 1 || m < 1) return FAVOR_ERR_INVALID_ARG;
+  if (dt != FAVOR_F32 && dt != FAVOR_BF16) return FAVOR_ERR_INVALID_ARG;
+  if (d > favor::kMaxD || m > favor::kMaxM) return FAVOR_ERR_UNSUPPORTED;
+  const long long bh = (long long)B * H;
+  if (bh > 65535) return FAVOR_ERR_UNSUPPORTED;
+  if (bh * L * (long long)d >= (1ll << 31)) return FAVOR_ERR_UNSUPPORTED;
+  return FAVOR_OK;
+}
+
+bool use_tc(bool causal, int d, int m, favor_dtype dt) { return favor::tc_supported(causal, d, m, dt == FAVOR_BF16); }
+
+size_t ws_bytes_for(bool causal, const Shape& s, favor_dtype dt) {
+  if (use_tc(causal, s.d, s.m, dt)) return favor::tc_workspace_bytes(causal, s);
+  return favor::simt_plan(causal, s).bytes;
+}
+
+enum Stage { kState = 1, kOutput = 2, kBoth = 3 };
+
+favor_status run(bool causal, int stage, const void* Q, const void* K, const void* V, void* O, int B, int H, int L,
+                 int d, const float* omega, int m, favor_dtype dt, float qk_scale, void* workspace,
+                 size_t ws_bytes, int32_t* dev_status, void* stream_) {
+  favor_status st = shape_ok(B, H, L, d, m, dt);
+  if (st != FAVOR_OK) return st;
+  if (!std::isfinite(qk_scale)) return FAVOR_ERR_INVALID_ARG;
+  const bool need_q = (stage & kOutput) != 0;
+  const bool need_kv = (stage & kState) != 0 || causal;
+  if (omega == nullptr || workspace == nullptr) return FAVOR_ERR_INVALID_ARG;
+  if (need_q && (Q == nullptr || O == nullptr)) return FAVOR_ERR_INVALID_ARG;
+  if (need_kv && (K == nullptr || V == nullptr)) return FAVOR_ERR_INVALID_ARG;
+  for (const void* p : {Q, K, V, static_cast<const void*>(O), static_cast<const void*>(omega)})
+    if (p != nullptr && !aligned(p, 16)) return FAVOR_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return FAVOR_ERR_INVALID_ARG;
+  if (need_q && (O == Q || O == K || O == V)) return FAVOR_ERR_INVALID_ARG;
+  const Shape s{B, H, L, d, m};
+  if (ws_bytes < ws_bytes_for(causal, s, dt)) return FAVOR_ERR_INVALID_ARG;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const bool bf16 = dt == FAVOR_BF16;
+  cudaError_t e = cudaSuccess;
+  if (use_tc(causal, d, m, dt)) {
+    if (stage & kState) e = favor::tc_state(causal, K, V, omega, qk_scale, s, workspace, dev_status, stream);
+    if (e == cudaSuccess && (stage & kOutput))
+      e = favor::tc_output(causal, Q, K, V, O, omega, qk_scale, s, workspace, dev_status, stream);
+  } else if (!causal) {
+    if (stage & kState) e = favor::simt_bidir_state(K, V, omega, qk_scale, s, bf16, workspace, dev_status, stream);
+    if (e == cudaSuccess && (stage & kOutput))
+      e = favor::simt_bidir_output(Q, O, omega, qk_scale, s, bf16, workspace, dev_status, stream);
+  } else {
+    if (stage & kState) e = favor::simt_causal_state(K, V, omega, qk_scale, s, bf16, workspace, dev_status, stream);
+    if (e == cudaSuccess && (stage & kOutput))
+      e = favor::simt_causal_output(Q, K, V, O, omega, qk_scale, s, bf16, workspace, dev_status, stream);
+  }
+  return e == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int favor_api_version(void) { return kVersion; }
+
+const char* favor_status_string(favor_status s) {
+  switch (s) {
+    case FAVOR_OK: return "ok";
+    case FAVOR_ERR_INVALID_ARG: return "invalid argument";
+    case FAVOR_ERR_UNSUPPORTED: return "unsupported shape";
+    case FAVOR_ERR_CUDA: return "CUDA error";
+    case FAVOR_ERR_TIMEOUT: return "device wait timed out";
+    case FAVOR_ERR_NONFINITE: return "non-finite or non-positive normaliser";
+  }
+  return "unknown status";
+}
+
+const char* favor_path_name(int causal, int d, int m, favor_dtype dt) {
+  if (shape_ok(1, 1, 1, d, m, dt) != FAVOR_OK) return "unsupported";
+  return use_tc(causal != 0, d, m, dt) ? "tcgen05" : "simt";
+}
+
+favor_status favor_build_orf(uint64_t seed, int m, int d, int orthogonal, float* omega, void* stream) {
+  if (omega == nullptr || m < 1 || d < 1 || m > favor::kMaxM || d > favor::kMaxD) return FAVOR_ERR_INVALID_ARG;
+  cudaError_t e = favor::launch_build_orf(seed, m, d, orthogonal, omega, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
+}
+
+size_t favor_workspace_bytes(int causal, int B, int H, int L, int d, int m, favor_dtype dt) {
+  if (shape_ok(B, H, L, d, m, dt) != FAVOR_OK) return 0;
+  return ws_bytes_for(causal != 0, Shape{B, H, L, d, m}, dt);
+}
+
+#define FAVOR_ARGS                                                                                      \
+  const void *Q, const void *K, const void *V, void *O, int B, int H, int L, int d, const float *omega, \
+      int m, favor_dtype dt, float qk_scale, void *workspace, size_t ws_bytes, int32_t *dev_status,     \
+      void *stream
+#define FAVOR_PASS Q, K, V, O, B, H, L, d, omega, m, dt, qk_scale, workspace, ws_bytes, dev_status, stream
+
+favor_status favor_fwd_bidir(FAVOR_ARGS) { return run(false, kBoth, FAVOR_PASS); }
+favor_status favor_fwd_causal(FAVOR_ARGS) { return run(true, kBoth, FAVOR_PASS); }
+favor_status favor_bidir_state(FAVOR_ARGS) { return run(false, kState, FAVOR_PASS); }
+favor_status favor_bidir_output(FAVOR_ARGS) { return run(false, kOutput, FAVOR_PASS); }
+favor_status favor_causal_state(FAVOR_ARGS) { return run(true, kState, FAVOR_PASS); }
+favor_status favor_causal_output(FAVOR_ARGS) { return run(true, kOutput, FAVOR_PASS); }
+
+}  // extern "C"

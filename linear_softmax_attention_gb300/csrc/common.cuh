@@ -1,0 +1,92 @@
+// Shared device/host helpers of the FAVOR+ library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "favor.h"
+
+namespace favor {
+
+constexpr int kMaxD = 128;
+constexpr int kMaxM = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---- element loads / stores -------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// ---- device-side status -----------------------------------------------------
+// First non-zero code wins; later errors do not overwrite it.
+__device__ __forceinline__ void report_status(int32_t* status, int code) {
+  if (status != nullptr) atomicCAS(reinterpret_cast<int*>(status), 0, code);
+}
+
+// ---- reductions -------------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+// Block-wide max; `scratch` holds >= 32 floats; every thread gets the result.
+__device__ __forceinline__ float block_max(float v, float* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  v = warp_max(v);
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  float r = (lane < nwarps) ? scratch[lane] : -INFINITY;
+  r = warp_max(r);
+  return r;
+}
+
+}  // namespace favor
+
+// ---- host-side launchers (defined in the .cu files) -------------------------
+namespace favor {
+
+struct Shape {
+  int B, H, L, d, m;
+  int BH() const { return B * H; }
+};
+
+// Workspace plan of the CUDA-core path.
+struct SimtPlan {
+  int n_fb;          // feature blocks of kSimtFB features
+  int n_split;       // bidirectional: L splits per head; causal: superchunks
+  int chunk;         // tokens per split / superchunk (multiple of the tile)
+  size_t off_partS, off_partM, off_state, bytes;
+};
+
+SimtPlan simt_plan(bool causal, const Shape& s);
+cudaError_t simt_bidir_state(const void* K, const void* V, const float* omega, float scale,
+                             const Shape& s, bool bf16, void* ws, int32_t* st, cudaStream_t stream);
+cudaError_t simt_bidir_output(const void* Q, void* O, const float* omega, float scale,
+                              const Shape& s, bool bf16, void* ws, int32_t* st, cudaStream_t stream);
+cudaError_t simt_causal_state(const void* K, const void* V, const float* omega, float scale,
+                              const Shape& s, bool bf16, void* ws, int32_t* st, cudaStream_t stream);
+cudaError_t simt_causal_output(const void* Q, const void* K, const void* V, void* O,
+                               const float* omega, float scale, const Shape& s, bool bf16, void* ws,
+                               int32_t* st, cudaStream_t stream);
+
+// Raises a kernel's dynamic shared-memory limit once per device and size, so
+// that calls made later (including under CUDA graph capture) issue no
+// attribute call.
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
+
+cudaError_t launch_build_orf(uint64_t seed, int m, int d, int orthogonal, float* omega,
+                             cudaStream_t stream);
+
+}  // namespace favor

@@ -1,0 +1,522 @@
+// CUDA-core FAVOR+ kernels (fp32 arithmetic): the path for fp32 storage and
+// for shapes the tensor-core kernels do not cover.
+//
+// Formulas: "Performer — Rethinking Attention with Performers" (digest),
+// §Key equations: phi(x) = m^-1/2 exp(Omega x - |x|^2/2) and
+// Attn^ = D^-1 phi(Q)(phi(K)^T V), D = diag(phi(Q) phi(K)^T 1); §Methods:
+// causal prefix sum G_t = sum_{s<=t} phi(k_s) v_s^T.
+//
+// Stabilisers (exact rewrites, not approximations):
+//  * key side: phi(k) is evaluated as exp(l - M) with one M per partial sum;
+//    partial sums are brought to a common M per head before they are added,
+//    so the shared factor exp(-M) cancels between numerator and normaliser;
+//  * query side: the per-row constant max_i(s w_i.q) is subtracted, and
+//    |q|^2/2 and m^-1/2 are dropped -- per-query constants cancel ("From
+//    Performer to Linear Attention", §Simple Derivation).
+#include "common.cuh"
+
+namespace favor {
+namespace {
+
+constexpr int kFB = 64;        // features per CTA (state kernel) / per block of Omega
+constexpr int kTT = 32;        // tokens per tile
+constexpr int kThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ void load_rows(const T* __restrict__ src, int nt, int d, float* dst, int ld) {
+  for (int e = threadIdx.x; e < kTT * d; e += kThreads) {
+    const int t = e / d, c = e - t * d;
+    dst[t * ld + c] = (t < nt) ? to_f32(src[(size_t)t * d + c]) : 0.f;
+  }
+}
+
+__device__ __forceinline__ void load_omega_block(const float* __restrict__ omega, int f0, int nf, int d,
+                                                 float* om) {
+  const int ld = d + 1;
+  for (int e = threadIdx.x; e < kFB * d; e += kThreads) {
+    const int f = e / d, c = e - f * d;
+    om[f * ld + c] = (f < nf) ? omega[(size_t)(f0 + f) * d + c] : 0.f;
+  }
+}
+
+__device__ __forceinline__ void row_norms(const float* xs, int d, float* kn) {
+  if (threadIdx.x < kTT) {
+    const float* row = xs + threadIdx.x * (d + 1);
+    float acc = 0.f;
+    for (int c = 0; c < d; ++c) acc = fmaf(row[c], row[c], acc);
+    kn[threadIdx.x] = acc;
+  }
+}
+
+// s * (x_t . w_f) for tile rows t and block features f; 8 (t, f) per thread.
+__device__ __forceinline__ float dot_row(const float* x, const float* w, int d) {
+  float acc = 0.f;
+  for (int c = 0; c < d; ++c) acc = fmaf(x[c], w[c], acc);
+  return acc;
+}
+
+// ---------------------------------------------------------------------------
+// State partials: for (split, feature block, head) the CTA sums
+//   S_p[f, :] = sum_t exp(l_tf - M_p) [v_t ; 1],  l_tf = s w_f.k_t - s^2 |k_t|^2 / 2
+// over its token range, with M_p = max of l over that range and block (pass 1).
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads) state_partial_kernel(
+    const T* __restrict__ K, const T* __restrict__ V, const float* __restrict__ omega, int L, int d, int m,
+    float scale, int chunk, int n_split, float* __restrict__ partS, float* __restrict__ partM) {
+  extern __shared__ float smem[];
+  const int split = blockIdx.x, fb = blockIdx.y, bh = blockIdx.z;
+  const int n_fb = gridDim.y;
+  const int ld = d + 1;
+  float* om = smem;                       // [kFB][ld]
+  float* ks = om + kFB * ld;              // [kTT][ld]
+  float* vs = ks + kTT * ld;              // [kTT][ld]
+  float* ph = vs + kTT * ld;              // [kTT][kFB + 1]
+  float* kn = ph + kTT * (kFB + 1);       // [kTT]
+  float* red = kn + kTT;                  // [32]
+
+  const int f0 = fb * kFB, nf = min(kFB, m - f0);
+  const int l0 = split * chunk, l1 = min(L, l0 + chunk);
+  const T* Kh = K + (size_t)bh * L * d;
+  const T* Vh = V + (size_t)bh * L * d;
+  const float hs2 = 0.5f * scale * scale;
+  const int f_own = threadIdx.x % kFB;
+  const int t_base = threadIdx.x / kFB;   // 0..3
+
+  load_omega_block(omega, f0, nf, d, om);
+
+  // pass 1: the exponent maximum of this partial
+  float mx = -INFINITY;
+  for (int t0 = l0; t0 < l1; t0 += kTT) {
+    const int nt = min(kTT, l1 - t0);
+    __syncthreads();
+    load_rows(Kh + (size_t)t0 * d, nt, d, ks, ld);
+    __syncthreads();
+    row_norms(ks, d, kn);
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kTT / 4; ++j) {
+      const int t = t_base + 4 * j;
+      if (t < nt && f_own < nf) {
+        const float l = scale * dot_row(ks + t * ld, om + f_own * ld, d) - hs2 * kn[t];
+        mx = fmaxf(mx, l);
+      }
+    }
+  }
+  const float M = block_max(mx, red);
+
+  // pass 2: accumulate; thread owns feature f = tid/4 and columns tid%4 + 4k
+  const int fa = threadIdx.x / 4, jb = threadIdx.x % 4;
+  float acc[33];
+#pragma unroll
+  for (int k = 0; k < 33; ++k) acc[k] = 0.f;
+  for (int t0 = l0; t0 < l1; t0 += kTT) {
+    const int nt = min(kTT, l1 - t0);
+    __syncthreads();
+    load_rows(Kh + (size_t)t0 * d, nt, d, ks, ld);
+    load_rows(Vh + (size_t)t0 * d, nt, d, vs, ld);
+    __syncthreads();
+    row_norms(ks, d, kn);
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kTT / 4; ++j) {
+      const int t = t_base + 4 * j;
+      float p = 0.f;
+      if (t < nt && f_own < nf) {
+        const float l = scale * dot_row(ks + t * ld, om + f_own * ld, d) - hs2 * kn[t];
+        p = expf(l - M);
+      }
+      ph[t * (kFB + 1) + f_own] = p;
+    }
+    __syncthreads();
+    for (int t = 0; t < nt; ++t) {
+      const float p = ph[t * (kFB + 1) + fa];
+      const float* vr = vs + t * ld;
+#pragma unroll
+      for (int k = 0; k < 33; ++k) {
+        const int j = jb + 4 * k;
+        if (j < d) acc[k] = fmaf(p, vr[j], acc[k]);
+        else if (j == d) acc[k] += p;
+      }
+    }
+  }
+  if (fa < nf) {
+    float* dst = partS + (((size_t)bh * n_split + split) * m + f0 + fa) * ld;
+#pragma unroll
+    for (int k = 0; k < 33; ++k) {
+      const int j = jb + 4 * k;
+      if (j <= d) dst[j] = acc[k];
+    }
+  }
+  if (threadIdx.x == 0) partM[((size_t)bh * n_split + split) * n_fb + fb] = M;
+}
+
+// Bidirectional: state[h] = sum_split exp(M_p - M_h) S_p, in split order.
+__global__ void __launch_bounds__(kThreads) merge_kernel(const float* __restrict__ partS,
+                                                         const float* __restrict__ partM, int d, int m,
+                                                         int n_split, int n_fb, float* __restrict__ state) {
+  const int bh = blockIdx.x;
+  const int ld = d + 1;
+  const float* pm = partM + (size_t)bh * n_split * n_fb;
+  float Mh = -INFINITY;
+  for (int e = 0; e < n_split * n_fb; ++e) Mh = fmaxf(Mh, pm[e]);
+  const size_t per = (size_t)m * ld;
+  for (int e = threadIdx.x; e < m * ld; e += kThreads) {
+    const int fb = (e / ld) / kFB;
+    float acc = 0.f;
+    for (int p = 0; p < n_split; ++p)
+      acc = fmaf(expf(pm[p * n_fb + fb] - Mh), partS[((size_t)bh * n_split + p) * per + e], acc);
+    state[(size_t)bh * per + e] = acc;
+  }
+}
+
+// Query-side features of one tile: pq[t][i] = exp(s w_i.q_t - max_i s w_i.q_t)
+// (all m features, exact row maximum), rows t >= nt set to 0.
+__device__ void query_features(const float* qs, int nt, int d, int m, float scale,
+                               const float* __restrict__ omega, float* om, float* pq, float* rowmax) {
+  const int ld = d + 1, ldq = m + 1;
+  const int f_own = threadIdx.x % kFB, t_base = threadIdx.x / kFB;
+  const int n_fb = (m + kFB - 1) / kFB;
+  for (int fb = 0; fb < n_fb; ++fb) {
+    const int f0 = fb * kFB, nf = min(kFB, m - f0);
+    __syncthreads();
+    load_omega_block(omega, f0, nf, d, om);
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kTT / 4; ++j) {
+      const int t = t_base + 4 * j;
+      if (f_own < nf) pq[t * ldq + f0 + f_own] = scale * dot_row(qs + t * ld, om + f_own * ld, d);
+    }
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t = warp; t < kTT; t += kThreads / 32) {
+    float mx = -INFINITY;
+    for (int f = lane; f < m; f += 32) mx = fmaxf(mx, pq[t * ldq + f]);
+    mx = warp_max(mx);
+    if (lane == 0) rowmax[t] = mx;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < kTT * m; e += kThreads) {
+    const int t = e / m, f = e - t * m;
+    pq[t * ldq + f] = (t < nt) ? expf(pq[t * ldq + f] - rowmax[t]) : 0.f;
+  }
+  __syncthreads();
+}
+
+// num[t][j] (j <= d) in smem -> O = num[:, :d] / num[:, d]; flags bad normalisers.
+template <typename T>
+__device__ __forceinline__ void store_output(const float* num, int nt, int d, T* __restrict__ Oh,
+                                             int32_t* status) {
+  const int ld = d + 1;
+  for (int e = threadIdx.x; e < nt * d; e += kThreads) {
+    const int t = e / d, j = e - t * d;
+    const float den = num[t * ld + d];
+    if (!(den > 0.f) || !isfinite(den)) report_status(status, FAVOR_ERR_NONFINITE);
+    Oh[(size_t)t * d + j] = from_f32<T>(num[t * ld + j] / den);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) bidir_output_kernel(
+    const T* __restrict__ Q, T* __restrict__ O, const float* __restrict__ omega,
+    const float* __restrict__ state, int L, int d, int m, float scale, int32_t* status) {
+  extern __shared__ float smem[];
+  const int ld = d + 1, ldq = m + 1;
+  const int bh = blockIdx.y;
+  const int t0 = blockIdx.x * kTT;
+  const int nt = min(kTT, L - t0);
+  float* qs = smem;                   // [kTT][ld]
+  float* om = qs + kTT * ld;          // [kFB][ld]
+  float* st = om + kFB * ld;          // [kFB][ld]
+  float* pq = st + kFB * ld;          // [kTT][ldq]
+  float* rowmax = pq + kTT * ldq;     // [kTT]
+
+  load_rows(Q + ((size_t)bh * L + t0) * d, nt, d, qs, ld);
+  query_features(qs, nt, d, m, scale, omega, om, pq, rowmax);
+
+  const int ta = threadIdx.x / 8, jb = threadIdx.x % 8;
+  float acc[17];
+#pragma unroll
+  for (int k = 0; k < 17; ++k) acc[k] = 0.f;
+  const float* sh = state + (size_t)bh * m * ld;
+  const int n_fb = (m + kFB - 1) / kFB;
+  for (int fb = 0; fb < n_fb; ++fb) {
+    const int f0 = fb * kFB, nf = min(kFB, m - f0);
+    __syncthreads();
+    for (int e = threadIdx.x; e < nf * ld; e += kThreads) st[e] = sh[(size_t)f0 * ld + e];
+    __syncthreads();
+    for (int f = 0; f < nf; ++f) {
+      const float p = pq[ta * ldq + f0 + f];
+      const float* sr = st + f * ld;
+#pragma unroll
+      for (int k = 0; k < 17; ++k) {
+        const int j = jb + 8 * k;
+        if (j <= d) acc[k] = fmaf(p, sr[j], acc[k]);
+      }
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 17; ++k) {
+    const int j = jb + 8 * k;
+    if (j <= d) qs[ta * ld + j] = acc[k];
+  }
+  __syncthreads();
+  store_output(qs, nt, d, O + ((size_t)bh * L + t0) * d, status);
+}
+
+// ---------------------------------------------------------------------------
+// Causal output: CTA = one superchunk of one head.  G starts as the exclusive
+// prefix of earlier superchunk states (common scale M_w = max over p <= sc);
+// each tile adds the masked intra-tile term, the inter term phi(Q) G and then
+// G += phi(K)^T [V | 1].  G lives in the workspace (fp32).
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads) causal_output_kernel(
+    const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V, T* __restrict__ O,
+    const float* __restrict__ omega, const float* __restrict__ partS, const float* __restrict__ partM,
+    float* __restrict__ Gws, int L, int d, int m, float scale, int chunk, int n_sc, int32_t* status) {
+  extern __shared__ float smem[];
+  const int ld = d + 1, ldq = m + 1;
+  const int sc = blockIdx.x, bh = blockIdx.y;
+  const int n_fb = (m + kFB - 1) / kFB;
+  float* qs = smem;                   // [kTT][ld]
+  float* ks = qs + kTT * ld;          // [kTT][ld]
+  float* vs = ks + kTT * ld;          // [kTT][ld]
+  float* om = vs + kTT * ld;          // [kFB][ld]
+  float* pq = om + kFB * ld;          // [kTT][ldq]
+  float* pk = pq + kTT * ldq;         // [kTT][ldq]
+  float* A = pk + kTT * ldq;          // [kTT][kTT + 1]
+  float* kn = A + kTT * (kTT + 1);    // [kTT]
+  float* rowmax = kn + kTT;           // [kTT]
+
+  const float* pm = partM + (size_t)bh * n_sc * n_fb;
+  float Mw = -INFINITY;
+  for (int e = 0; e < (sc + 1) * n_fb; ++e) Mw = fmaxf(Mw, pm[e]);
+  const size_t per = (size_t)m * ld;
+  float* G = Gws + ((size_t)bh * n_sc + sc) * per;
+  for (int e = threadIdx.x; e < m * ld; e += kThreads) {
+    const int fb = (e / ld) / kFB;
+    float acc = 0.f;
+    for (int p = 0; p < sc; ++p)
+      acc = fmaf(expf(pm[p * n_fb + fb] - Mw), partS[((size_t)bh * n_sc + p) * per + e], acc);
+    G[e] = acc;
+  }
+
+  const float hs2 = 0.5f * scale * scale;
+  const int l0 = sc * chunk, l1 = min(L, l0 + chunk);
+  const size_t hoff = (size_t)bh * L * d;
+  const int f_own = threadIdx.x % kFB, t_base = threadIdx.x / kFB;
+  const int ta = threadIdx.x / 8, jb = threadIdx.x % 8;
+
+  for (int t0 = l0; t0 < l1; t0 += kTT) {
+    const int nt = min(kTT, l1 - t0);
+    __syncthreads();
+    load_rows(Q + hoff + (size_t)t0 * d, nt, d, qs, ld);
+    load_rows(K + hoff + (size_t)t0 * d, nt, d, ks, ld);
+    load_rows(V + hoff + (size_t)t0 * d, nt, d, vs, ld);
+    __syncthreads();
+    row_norms(ks, d, kn);
+    // key features with the common scale M_w
+    for (int fb = 0; fb < n_fb; ++fb) {
+      const int f0 = fb * kFB, nf = min(kFB, m - f0);
+      __syncthreads();
+      load_omega_block(omega, f0, nf, d, om);
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < kTT / 4; ++j) {
+        const int t = t_base + 4 * j;
+        if (f_own < nf) {
+          const float l = scale * dot_row(ks + t * ld, om + f_own * ld, d) - hs2 * kn[t];
+          pk[t * ldq + f0 + f_own] = (t < nt) ? expf(l - Mw) : 0.f;
+        }
+      }
+    }
+    query_features(qs, nt, d, m, scale, omega, om, pq, rowmax);
+    // intra-tile scores, lower triangle with the diagonal
+    for (int e = threadIdx.x; e < kTT * kTT; e += kThreads) {
+      const int t = e / kTT, s = e - t * kTT;
+      float a = 0.f;
+      if (s <= t && t < nt) {
+        const float* qr = pq + t * ldq;
+        const float* kr = pk + s * ldq;
+        for (int i = 0; i < m; ++i) a = fmaf(qr[i], kr[i], a);
+      }
+      A[t * (kTT + 1) + s] = a;
+    }
+    __syncthreads();
+    float acc[17];
+#pragma unroll
+    for (int k = 0; k < 17; ++k) acc[k] = 0.f;
+    {
+      const float* qr = pq + ta * ldq;
+      for (int i = 0; i < m; ++i) {
+        const float p = qr[i];
+        const float* gr = G + (size_t)i * ld;
+#pragma unroll
+        for (int k = 0; k < 17; ++k) {
+          const int j = jb + 8 * k;
+          if (j <= d) acc[k] = fmaf(p, gr[j], acc[k]);
+        }
+      }
+      for (int s = 0; s <= ta && s < nt; ++s) {
+        const float a = A[ta * (kTT + 1) + s];
+        const float* vr = vs + s * ld;
+#pragma unroll
+        for (int k = 0; k < 17; ++k) {
+          const int j = jb + 8 * k;
+          if (j < d) acc[k] = fmaf(a, vr[j], acc[k]);
+          else if (j == d) acc[k] += a;
+        }
+      }
+    }
+    __syncthreads();   // all reads of qs (projections) and G done
+#pragma unroll
+    for (int k = 0; k < 17; ++k) {
+      const int j = jb + 8 * k;
+      if (j <= d) qs[ta * ld + j] = acc[k];
+    }
+    __syncthreads();
+    store_output(qs, nt, d, O + hoff + (size_t)t0 * d, status);
+    // G += phi(K)^T [V | 1]
+    for (int e = threadIdx.x; e < m * ld; e += kThreads) {
+      const int i = e / ld, j = e - i * ld;
+      float g = G[e];
+      for (int s = 0; s < nt; ++s) g = fmaf(pk[s * ldq + i], (j < d) ? vs[s * ld + j] : 1.f, g);
+      G[e] = g;
+    }
+  }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+SimtPlan simt_plan(bool causal, const Shape& s) {
+  SimtPlan p{};
+  const int BH = s.BH();
+  p.n_fb = (s.m + kFB - 1) / kFB;
+  const int tiles = (s.L + kTT - 1) / kTT;
+  const int target = 2 * 152;
+  int want = causal ? (target + BH - 1) / BH : (target + BH * p.n_fb - 1) / (BH * p.n_fb);
+  want = max(1, min(want, tiles));
+  const int tiles_per = (tiles + want - 1) / want;
+  p.chunk = tiles_per * kTT;
+  p.n_split = (s.L + p.chunk - 1) / p.chunk;
+  const size_t per = (size_t)s.m * (s.d + 1) * sizeof(float);
+  size_t off = 0;
+  p.off_partS = off;
+  off = align256(off + (size_t)BH * p.n_split * per);
+  p.off_partM = off;
+  off = align256(off + (size_t)BH * p.n_split * p.n_fb * sizeof(float));
+  p.off_state = off;
+  off = align256(off + (size_t)BH * (causal ? p.n_split : 1) * per);
+  p.bytes = off;
+  return p;
+}
+
+static size_t state_smem(int d) {
+  const int ld = d + 1;
+  return sizeof(float) * ((size_t)kFB * ld + 2 * kTT * ld + kTT * (kFB + 1) + kTT + 32);
+}
+static size_t bidir_out_smem(int d, int m) {
+  const int ld = d + 1;
+  return sizeof(float) * ((size_t)kTT * ld + 2 * kFB * ld + kTT * (m + 1) + kTT);
+}
+static size_t causal_out_smem(int d, int m) {
+  const int ld = d + 1;
+  return sizeof(float) * ((size_t)3 * kTT * ld + kFB * ld + 2 * kTT * (m + 1) + kTT * (kTT + 1) + 2 * kTT);
+}
+
+template <typename KernelT>
+static cudaError_t set_smem(KernelT k, size_t bytes) {
+  return ensure_dynamic_smem(reinterpret_cast<const void*>(k), bytes);
+}
+
+template <typename T>
+static cudaError_t state_impl(const void* K, const void* V, const float* omega, float scale, const Shape& s,
+                              const SimtPlan& p, char* ws, cudaStream_t stream) {
+  const size_t smem = state_smem(s.d);
+  auto kern = state_partial_kernel<T>;
+  cudaError_t e = set_smem(kern, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.n_split, p.n_fb, s.BH());
+  kern<<<grid, kThreads, smem, stream>>>(static_cast<const T*>(K), static_cast<const T*>(V), omega, s.L, s.d,
+                                         s.m, scale, p.chunk, p.n_split,
+                                         reinterpret_cast<float*>(ws + p.off_partS),
+                                         reinterpret_cast<float*>(ws + p.off_partM));
+  return cudaGetLastError();
+}
+
+cudaError_t simt_bidir_state(const void* K, const void* V, const float* omega, float scale, const Shape& s,
+                             bool bf16, void* ws, int32_t* st, cudaStream_t stream) {
+  (void)st;
+  const SimtPlan p = simt_plan(false, s);
+  char* w = static_cast<char*>(ws);
+  cudaError_t e = bf16 ? state_impl<__nv_bfloat16>(K, V, omega, scale, s, p, w, stream)
+                       : state_impl<float>(K, V, omega, scale, s, p, w, stream);
+  if (e != cudaSuccess) return e;
+  merge_kernel<<<s.BH(), kThreads, 0, stream>>>(reinterpret_cast<float*>(w + p.off_partS),
+                                                reinterpret_cast<float*>(w + p.off_partM), s.d, s.m, p.n_split,
+                                                p.n_fb, reinterpret_cast<float*>(w + p.off_state));
+  return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t bidir_out_impl(const void* Q, void* O, const float* omega, float scale, const Shape& s,
+                                  const SimtPlan& p, char* ws, int32_t* st, cudaStream_t stream) {
+  const size_t smem = bidir_out_smem(s.d, s.m);
+  auto kern = bidir_output_kernel<T>;
+  cudaError_t e = set_smem(kern, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((s.L + kTT - 1) / kTT, s.BH());
+  kern<<<grid, kThreads, smem, stream>>>(static_cast<const T*>(Q), static_cast<T*>(O), omega,
+                                         reinterpret_cast<const float*>(ws + p.off_state), s.L, s.d, s.m, scale,
+                                         st);
+  return cudaGetLastError();
+}
+
+cudaError_t simt_bidir_output(const void* Q, void* O, const float* omega, float scale, const Shape& s,
+                              bool bf16, void* ws, int32_t* st, cudaStream_t stream) {
+  const SimtPlan p = simt_plan(false, s);
+  char* w = static_cast<char*>(ws);
+  return bf16 ? bidir_out_impl<__nv_bfloat16>(Q, O, omega, scale, s, p, w, st, stream)
+              : bidir_out_impl<float>(Q, O, omega, scale, s, p, w, st, stream);
+}
+
+cudaError_t simt_causal_state(const void* K, const void* V, const float* omega, float scale, const Shape& s,
+                              bool bf16, void* ws, int32_t* st, cudaStream_t stream) {
+  (void)st;
+  const SimtPlan p = simt_plan(true, s);
+  char* w = static_cast<char*>(ws);
+  return bf16 ? state_impl<__nv_bfloat16>(K, V, omega, scale, s, p, w, stream)
+              : state_impl<float>(K, V, omega, scale, s, p, w, stream);
+}
+
+template <typename T>
+static cudaError_t causal_out_impl(const void* Q, const void* K, const void* V, void* O, const float* omega,
+                                   float scale, const Shape& s, const SimtPlan& p, char* ws, int32_t* st,
+                                   cudaStream_t stream) {
+  const size_t smem = causal_out_smem(s.d, s.m);
+  auto kern = causal_output_kernel<T>;
+  cudaError_t e = set_smem(kern, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.n_split, s.BH());
+  kern<<<grid, kThreads, smem, stream>>>(
+      static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V), static_cast<T*>(O), omega,
+      reinterpret_cast<const float*>(ws + p.off_partS), reinterpret_cast<const float*>(ws + p.off_partM),
+      reinterpret_cast<float*>(ws + p.off_state), s.L, s.d, s.m, scale, p.chunk, p.n_split, st);
+  return cudaGetLastError();
+}
+
+cudaError_t simt_causal_output(const void* Q, const void* K, const void* V, void* O, const float* omega,
+                               float scale, const Shape& s, bool bf16, void* ws, int32_t* st,
+                               cudaStream_t stream) {
+  const SimtPlan p = simt_plan(true, s);
+  char* w = static_cast<char*>(ws);
+  return bf16 ? causal_out_impl<__nv_bfloat16>(Q, K, V, O, omega, scale, s, p, w, st, stream)
+              : causal_out_impl<float>(Q, K, V, O, omega, scale, s, p, w, st, stream);
+}
+
+}  // namespace favor

@@ -1,0 +1,15 @@
+// Tensor-core (tcgen05) FAVOR+ path: bf16 operands, fp32 accumulation.
+#pragma once
+
+#include "common.cuh"
+
+namespace favor {
+
+bool tc_supported(bool causal, int d, int m, bool bf16);
+size_t tc_workspace_bytes(bool causal, const Shape& s);
+cudaError_t tc_state(bool causal, const void* K, const void* V, const float* omega, float scale, const Shape& s,
+                     void* ws, int32_t* status, cudaStream_t stream);
+cudaError_t tc_output(bool causal, const void* Q, const void* K, const void* V, void* O, const float* omega,
+                      float scale, const Shape& s, void* ws, int32_t* status, cudaStream_t stream);
+
+}  // namespace favor

@@ -1,0 +1,98 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+declared in include/favor.h, and rejects bad arguments before launching."""
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import linear_softmax_attention_gb300 as favor
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "favor.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(favor_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(favor.lib_path()):
+        from linear_softmax_attention_gb300 import build
+        build.build()
+    return favor.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_status_strings(lib):
+    assert favor.api_version() == 1
+    for code, text in [(0, "ok"), (1, "invalid argument"), (2, "unsupported shape"), (4, "device wait timed out")]:
+        assert favor.status_string(code) == text
+
+
+def test_workspace_sizes(lib):
+    assert favor.workspace_bytes(False, 1, 1, 512, 64, 64, torch.float32) > 0
+    assert favor.workspace_bytes(True, 4, 8, 8192, 64, 256, torch.bfloat16) > 0
+    assert lib.favor_workspace_bytes(0, 1, 1, 0, 64, 64, 0) == 0          # L = 0
+    assert lib.favor_workspace_bytes(0, 1, 1, 16, 129, 64, 0) == 0        # d too large
+    assert lib.favor_workspace_bytes(0, 1, 1, 16, 64, 513, 0) == 0        # m too large
+    assert lib.favor_workspace_bytes(0, 1, 1, 16, 64, 64, 7) == 0         # bad dtype
+
+
+def test_path_names(lib):
+    assert favor.path_name(False, 64, 64, torch.float32) == "simt"
+    assert favor.path_name(False, 200, 64, torch.float32) == "unsupported"
+
+
+def _call(lib, name, **kw):
+    args = dict(Q=16, K=16, V=16, O=32, B=1, H=1, L=8, d=8, omega=48, m=8, dt=0, s=1.0, ws=256, nbytes=1 << 30,
+                st=None, stream=None)
+    args.update(kw)
+    return getattr(lib, name)(args["Q"], args["K"], args["V"], args["O"], args["B"], args["H"], args["L"],
+                              args["d"], args["omega"], args["m"], args["dt"], args["s"], args["ws"],
+                              args["nbytes"], args["st"], args["stream"])
+
+
+@pytest.mark.parametrize("name", favor.ENTRY_POINTS)
+def test_bad_arguments_rejected_before_launch(lib, name):
+    # every case fails the host-side checks, so nothing reaches the GPU
+    assert _call(lib, name, omega=None) == 1
+    assert _call(lib, name, ws=None) == 1
+    assert _call(lib, name, L=0) == 1
+    assert _call(lib, name, d=129) == 2
+    assert _call(lib, name, m=600) == 2
+    assert _call(lib, name, dt=3) == 1
+    assert _call(lib, name, s=float("nan")) == 1
+    assert _call(lib, name, ws=8) == 1                 # workspace not 256-byte aligned
+    assert _call(lib, name, nbytes=16) == 1            # workspace too small
+    if "state" not in name:
+        assert _call(lib, name, Q=None) == 1
+        assert _call(lib, name, O=16) == 1             # O aliases Q
+        assert _call(lib, name, Q=24) == 1             # misaligned
+    if "bidir_output" not in name:
+        assert _call(lib, name, K=None) == 1
+
+
+def test_build_orf_rejects_bad_arguments(lib):
+    assert lib.favor_build_orf(ctypes.c_uint64(0), 8, 8, 1, None, None) == 1
+    assert lib.favor_build_orf(ctypes.c_uint64(0), 0, 8, 1, 16, None) == 1
+    assert lib.favor_build_orf(ctypes.c_uint64(0), 8, 200, 1, 16, None) == 1
+
+
+def test_product_code_does_not_touch_the_oracle():
+    pkg = os.path.join(ROOT, "linear_softmax_attention_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower(), f
