@@ -21,8 +21,9 @@
  *    fastest, all of dtype `dt`; 16-byte aligned.  O may not alias Q, K, V.
  *  - omega: device pointer to fp32 [m, d], row i = omega_i, shared by every
  *    (b, h) and by Q and K.
- *  - qk_scale: temperature s; q and k enter the feature map as s*q and s*k
- *    (s = d^{-1/4} reproduces softmax(QK^T / sqrt(d))).
+ *  - qk_scale: temperature s > 0; q and k enter the feature map as s*q and
+ *    s*k (s = d^{-1/4} reproduces softmax(QK^T / sqrt(d))).  A non-positive
+ *    or non-finite s is FAVOR_ERR_INVALID_ARG.
  *  - workspace: caller-owned device scratch of at least
  *    favor_workspace_bytes(...) bytes, 256-byte aligned; its contents between
  *    calls do not matter.  Calls that share a workspace must be ordered on

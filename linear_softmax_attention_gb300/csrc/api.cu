@@ -58,7 +58,7 @@ favor_status run(bool causal, int stage, const void* Q, const void* K, const voi
                  size_t ws_bytes, int32_t* dev_status, void* stream_) {
   favor_status st = shape_ok(B, H, L, d, m, dt);
   if (st != FAVOR_OK) return st;
-  if (!std::isfinite(qk_scale)) return FAVOR_ERR_INVALID_ARG;
+  if (!std::isfinite(qk_scale) || !(qk_scale > 0.f)) return FAVOR_ERR_INVALID_ARG;
   const bool need_q = (stage & kOutput) != 0;
   const bool need_kv = (stage & kState) != 0 || causal;
   if (omega == nullptr || workspace == nullptr) return FAVOR_ERR_INVALID_ARG;

@@ -62,12 +62,16 @@ struct Shape {
   int BH() const { return B * H; }
 };
 
+// Every workspace starts with a 256-byte header: float key reference R at
+// offset 0 (written by launch_prep at the start of each state stage).
+constexpr size_t kWsHeader = 256;
+
 // Workspace plan of the CUDA-core path.
 struct SimtPlan {
   int n_fb;          // feature blocks of kSimtFB features
   int n_split;       // bidirectional: L splits per head; causal: superchunks
   int chunk;         // tokens per split / superchunk (multiple of the tile)
-  size_t off_partS, off_partM, off_state, bytes;
+  size_t off_partS, off_state, bytes;
 };
 
 SimtPlan simt_plan(bool causal, const Shape& s);
@@ -85,6 +89,9 @@ cudaError_t simt_causal_output(const void* Q, const void* K, const void* V, void
 // that calls made later (including under CUDA graph capture) issue no
 // attribute call.
 cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
+
+// Key reference R (and optionally the bf16 Omega image) into the workspace.
+cudaError_t launch_prep(const float* omega, int m, int d, float* key_ref, uint8_t* image, cudaStream_t stream);
 
 cudaError_t launch_build_orf(uint64_t seed, int m, int d, int orthogonal, float* omega,
                              cudaStream_t stream);

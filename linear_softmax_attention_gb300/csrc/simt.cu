@@ -7,9 +7,11 @@
 // causal prefix sum G_t = sum_{s<=t} phi(k_s) v_s^T.
 //
 // Stabilisers (exact rewrites, not approximations):
-//  * key side: phi(k) is evaluated as exp(l - M) with one M per partial sum;
-//    partial sums are brought to a common M per head before they are added,
-//    so the shared factor exp(-M) cancels between numerator and normaliser;
+//  * key side: phi(k) is evaluated as exp(l - R) with one constant R for the
+//    whole call, R = max_i |w_i|^2 / 2 - 40 (see key_reference in prep.cu);
+//    since l = |w|^2/2 - |s k - w|^2/2 <= max_i |w_i|^2/2, every key feature
+//    is <= e^40 and the shared factor exp(-R) cancels between numerator and
+//    normaliser;
 //  * query side: the per-row constant max_i(s w_i.q) is subtracted, and
 //    |q|^2/2 and m^-1/2 are dropped -- per-query constants cancel ("From
 //    Performer to Linear Attention", §Simple Derivation).
@@ -57,55 +59,35 @@ __device__ __forceinline__ float dot_row(const float* x, const float* w, int d) 
 
 // ---------------------------------------------------------------------------
 // State partials: for (split, feature block, head) the CTA sums
-//   S_p[f, :] = sum_t exp(l_tf - M_p) [v_t ; 1],  l_tf = s w_f.k_t - s^2 |k_t|^2 / 2
-// over its token range, with M_p = max of l over that range and block (pass 1).
+//   S_p[f, :] = sum_t exp(l_tf - R) [v_t ; 1],  l_tf = s w_f.k_t - s^2 |k_t|^2 / 2
+// over its token range.
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(kThreads) state_partial_kernel(
-    const T* __restrict__ K, const T* __restrict__ V, const float* __restrict__ omega, int L, int d, int m,
-    float scale, int chunk, int n_split, float* __restrict__ partS, float* __restrict__ partM) {
+    const T* __restrict__ K, const T* __restrict__ V, const float* __restrict__ omega,
+    const float* __restrict__ key_ref, int L, int d, int m, float scale, int chunk, int n_split,
+    float* __restrict__ partS) {
   extern __shared__ float smem[];
   const int split = blockIdx.x, fb = blockIdx.y, bh = blockIdx.z;
-  const int n_fb = gridDim.y;
   const int ld = d + 1;
   float* om = smem;                       // [kFB][ld]
   float* ks = om + kFB * ld;              // [kTT][ld]
   float* vs = ks + kTT * ld;              // [kTT][ld]
   float* ph = vs + kTT * ld;              // [kTT][kFB + 1]
   float* kn = ph + kTT * (kFB + 1);       // [kTT]
-  float* red = kn + kTT;                  // [32]
 
   const int f0 = fb * kFB, nf = min(kFB, m - f0);
   const int l0 = split * chunk, l1 = min(L, l0 + chunk);
   const T* Kh = K + (size_t)bh * L * d;
   const T* Vh = V + (size_t)bh * L * d;
   const float hs2 = 0.5f * scale * scale;
+  const float R = *key_ref;
   const int f_own = threadIdx.x % kFB;
   const int t_base = threadIdx.x / kFB;   // 0..3
 
   load_omega_block(omega, f0, nf, d, om);
 
-  // pass 1: the exponent maximum of this partial
-  float mx = -INFINITY;
-  for (int t0 = l0; t0 < l1; t0 += kTT) {
-    const int nt = min(kTT, l1 - t0);
-    __syncthreads();
-    load_rows(Kh + (size_t)t0 * d, nt, d, ks, ld);
-    __syncthreads();
-    row_norms(ks, d, kn);
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < kTT / 4; ++j) {
-      const int t = t_base + 4 * j;
-      if (t < nt && f_own < nf) {
-        const float l = scale * dot_row(ks + t * ld, om + f_own * ld, d) - hs2 * kn[t];
-        mx = fmaxf(mx, l);
-      }
-    }
-  }
-  const float M = block_max(mx, red);
-
-  // pass 2: accumulate; thread owns feature f = tid/4 and columns tid%4 + 4k
+  // thread owns feature f = tid/4 and columns tid%4 + 4k
   const int fa = threadIdx.x / 4, jb = threadIdx.x % 4;
   float acc[33];
 #pragma unroll
@@ -124,7 +106,7 @@ __global__ void __launch_bounds__(kThreads) state_partial_kernel(
       float p = 0.f;
       if (t < nt && f_own < nf) {
         const float l = scale * dot_row(ks + t * ld, om + f_own * ld, d) - hs2 * kn[t];
-        p = expf(l - M);
+        p = expf(l - R);
       }
       ph[t * (kFB + 1) + f_own] = p;
     }
@@ -148,24 +130,16 @@ __global__ void __launch_bounds__(kThreads) state_partial_kernel(
       if (j <= d) dst[j] = acc[k];
     }
   }
-  if (threadIdx.x == 0) partM[((size_t)bh * n_split + split) * n_fb + fb] = M;
 }
 
-// Bidirectional: state[h] = sum_split exp(M_p - M_h) S_p, in split order.
-__global__ void __launch_bounds__(kThreads) merge_kernel(const float* __restrict__ partS,
-                                                         const float* __restrict__ partM, int d, int m,
-                                                         int n_split, int n_fb, float* __restrict__ state) {
+// Bidirectional: state[h] = sum over splits of S_p, in split order.
+__global__ void __launch_bounds__(kThreads) merge_kernel(const float* __restrict__ partS, int d, int m, int n_split,
+                                                         float* __restrict__ state) {
   const int bh = blockIdx.x;
-  const int ld = d + 1;
-  const float* pm = partM + (size_t)bh * n_split * n_fb;
-  float Mh = -INFINITY;
-  for (int e = 0; e < n_split * n_fb; ++e) Mh = fmaxf(Mh, pm[e]);
-  const size_t per = (size_t)m * ld;
-  for (int e = threadIdx.x; e < m * ld; e += kThreads) {
-    const int fb = (e / ld) / kFB;
+  const size_t per = (size_t)m * (d + 1);
+  for (int e = threadIdx.x; e < (int)per; e += kThreads) {
     float acc = 0.f;
-    for (int p = 0; p < n_split; ++p)
-      acc = fmaf(expf(pm[p * n_fb + fb] - Mh), partS[((size_t)bh * n_split + p) * per + e], acc);
+    for (int p = 0; p < n_split; ++p) acc += partS[((size_t)bh * n_split + p) * per + e];
     state[(size_t)bh * per + e] = acc;
   }
 }
@@ -268,14 +242,14 @@ __global__ void __launch_bounds__(kThreads) bidir_output_kernel(
 
 // ---------------------------------------------------------------------------
 // Causal output: CTA = one superchunk of one head.  G starts as the exclusive
-// prefix of earlier superchunk states (common scale M_w = max over p <= sc);
+// prefix of earlier superchunk states (sum in superchunk order);
 // each tile adds the masked intra-tile term, the inter term phi(Q) G and then
 // G += phi(K)^T [V | 1].  G lives in the workspace (fp32).
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(kThreads) causal_output_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V, T* __restrict__ O,
-    const float* __restrict__ omega, const float* __restrict__ partS, const float* __restrict__ partM,
+    const float* __restrict__ omega, const float* __restrict__ key_ref, const float* __restrict__ partS,
     float* __restrict__ Gws, int L, int d, int m, float scale, int chunk, int n_sc, int32_t* status) {
   extern __shared__ float smem[];
   const int ld = d + 1, ldq = m + 1;
@@ -291,16 +265,12 @@ __global__ void __launch_bounds__(kThreads) causal_output_kernel(
   float* kn = A + kTT * (kTT + 1);    // [kTT]
   float* rowmax = kn + kTT;           // [kTT]
 
-  const float* pm = partM + (size_t)bh * n_sc * n_fb;
-  float Mw = -INFINITY;
-  for (int e = 0; e < (sc + 1) * n_fb; ++e) Mw = fmaxf(Mw, pm[e]);
+  const float Rk = *key_ref;
   const size_t per = (size_t)m * ld;
   float* G = Gws + ((size_t)bh * n_sc + sc) * per;
   for (int e = threadIdx.x; e < m * ld; e += kThreads) {
-    const int fb = (e / ld) / kFB;
     float acc = 0.f;
-    for (int p = 0; p < sc; ++p)
-      acc = fmaf(expf(pm[p * n_fb + fb] - Mw), partS[((size_t)bh * n_sc + p) * per + e], acc);
+    for (int p = 0; p < sc; ++p) acc += partS[((size_t)bh * n_sc + p) * per + e];
     G[e] = acc;
   }
 
@@ -329,7 +299,7 @@ __global__ void __launch_bounds__(kThreads) causal_output_kernel(
         const int t = t_base + 4 * j;
         if (f_own < nf) {
           const float l = scale * dot_row(ks + t * ld, om + f_own * ld, d) - hs2 * kn[t];
-          pk[t * ldq + f0 + f_own] = (t < nt) ? expf(l - Mw) : 0.f;
+          pk[t * ldq + f0 + f_own] = (t < nt) ? expf(l - Rk) : 0.f;
         }
       }
     }
@@ -405,11 +375,9 @@ SimtPlan simt_plan(bool causal, const Shape& s) {
   p.chunk = tiles_per * kTT;
   p.n_split = (s.L + p.chunk - 1) / p.chunk;
   const size_t per = (size_t)s.m * (s.d + 1) * sizeof(float);
-  size_t off = 0;
+  size_t off = kWsHeader;
   p.off_partS = off;
   off = align256(off + (size_t)BH * p.n_split * per);
-  p.off_partM = off;
-  off = align256(off + (size_t)BH * p.n_split * p.n_fb * sizeof(float));
   p.off_state = off;
   off = align256(off + (size_t)BH * (causal ? p.n_split : 1) * per);
   p.bytes = off;
@@ -418,7 +386,7 @@ SimtPlan simt_plan(bool causal, const Shape& s) {
 
 static size_t state_smem(int d) {
   const int ld = d + 1;
-  return sizeof(float) * ((size_t)kFB * ld + 2 * kTT * ld + kTT * (kFB + 1) + kTT + 32);
+  return sizeof(float) * ((size_t)kFB * ld + 2 * kTT * ld + kTT * (kFB + 1) + kTT);
 }
 static size_t bidir_out_smem(int d, int m) {
   const int ld = d + 1;
@@ -437,15 +405,17 @@ static cudaError_t set_smem(KernelT k, size_t bytes) {
 template <typename T>
 static cudaError_t state_impl(const void* K, const void* V, const float* omega, float scale, const Shape& s,
                               const SimtPlan& p, char* ws, cudaStream_t stream) {
+  float* key_ref = reinterpret_cast<float*>(ws);
+  cudaError_t e = launch_prep(omega, s.m, s.d, key_ref, nullptr, stream);
+  if (e != cudaSuccess) return e;
   const size_t smem = state_smem(s.d);
   auto kern = state_partial_kernel<T>;
-  cudaError_t e = set_smem(kern, smem);
+  e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_split, p.n_fb, s.BH());
-  kern<<<grid, kThreads, smem, stream>>>(static_cast<const T*>(K), static_cast<const T*>(V), omega, s.L, s.d,
-                                         s.m, scale, p.chunk, p.n_split,
-                                         reinterpret_cast<float*>(ws + p.off_partS),
-                                         reinterpret_cast<float*>(ws + p.off_partM));
+  kern<<<grid, kThreads, smem, stream>>>(static_cast<const T*>(K), static_cast<const T*>(V), omega, key_ref, s.L,
+                                         s.d, s.m, scale, p.chunk, p.n_split,
+                                         reinterpret_cast<float*>(ws + p.off_partS));
   return cudaGetLastError();
 }
 
@@ -457,9 +427,8 @@ cudaError_t simt_bidir_state(const void* K, const void* V, const float* omega, f
   cudaError_t e = bf16 ? state_impl<__nv_bfloat16>(K, V, omega, scale, s, p, w, stream)
                        : state_impl<float>(K, V, omega, scale, s, p, w, stream);
   if (e != cudaSuccess) return e;
-  merge_kernel<<<s.BH(), kThreads, 0, stream>>>(reinterpret_cast<float*>(w + p.off_partS),
-                                                reinterpret_cast<float*>(w + p.off_partM), s.d, s.m, p.n_split,
-                                                p.n_fb, reinterpret_cast<float*>(w + p.off_state));
+  merge_kernel<<<s.BH(), kThreads, 0, stream>>>(reinterpret_cast<float*>(w + p.off_partS), s.d, s.m, p.n_split,
+                                                reinterpret_cast<float*>(w + p.off_state));
   return cudaGetLastError();
 }
 
@@ -505,7 +474,7 @@ static cudaError_t causal_out_impl(const void* Q, const void* K, const void* V, 
   dim3 grid(p.n_split, s.BH());
   kern<<<grid, kThreads, smem, stream>>>(
       static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V), static_cast<T*>(O), omega,
-      reinterpret_cast<const float*>(ws + p.off_partS), reinterpret_cast<const float*>(ws + p.off_partM),
+      reinterpret_cast<const float*>(ws), reinterpret_cast<const float*>(ws + p.off_partS),
       reinterpret_cast<float*>(ws + p.off_state), s.L, s.d, s.m, scale, p.chunk, p.n_split, st);
   return cudaGetLastError();
 }

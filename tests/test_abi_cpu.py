@@ -73,6 +73,8 @@ def test_bad_arguments_rejected_before_launch(lib, name):
     assert _call(lib, name, m=600) == 2
     assert _call(lib, name, dt=3) == 1
     assert _call(lib, name, s=float("nan")) == 1
+    assert _call(lib, name, s=0.0) == 1
+    assert _call(lib, name, s=-0.5) == 1
     assert _call(lib, name, ws=8) == 1                 # workspace not 256-byte aligned
     assert _call(lib, name, nbytes=16) == 1            # workspace too small
     if "state" not in name:
