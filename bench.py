@@ -228,6 +228,9 @@ def run_gpu(args, rank, world, local_rank):
         for i in range(max(3, args.warmup)):
             step(i, wl.omega_seed_for_call(w, i))
     torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after warm-up: "
+                           f"{favor.status_string(int(status.item()))}")
 
     # per-kernel durations: events around each stage on the launching stream
     n_inst = min(args.steps, 200)

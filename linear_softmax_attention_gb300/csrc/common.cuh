@@ -62,8 +62,9 @@ struct Shape {
   int BH() const { return B * H; }
 };
 
-// Every workspace starts with a 256-byte header: float key reference R at
-// offset 0 (written by launch_prep at the start of each state stage).
+// Every workspace starts with a 256-byte header written by launch_prep at the
+// start of each state stage: float key reference R at offset 0 and the
+// largest row norm W of Omega at offset 4.
 constexpr size_t kWsHeader = 256;
 
 // Workspace plan of the CUDA-core path.
@@ -90,7 +91,7 @@ cudaError_t simt_causal_output(const void* Q, const void* K, const void* V, void
 // attribute call.
 cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
 
-// Key reference R (and optionally the bf16 Omega image) into the workspace.
+// Key reference R and W (and optionally the bf16 Omega images) into the workspace.
 cudaError_t launch_prep(const float* omega, int m, int d, float* key_ref, uint8_t* image, cudaStream_t stream);
 
 cudaError_t launch_build_orf(uint64_t seed, int m, int d, int orthogonal, float* omega,

@@ -30,7 +30,6 @@ __device__ __forceinline__ float normal_from_word(uint64_t w) {
 }
 
 constexpr int kTPR = 4;                 // threads per row of a block
-constexpr int kCW = kMaxD / kTPR;       // max columns per thread
 
 __device__ __forceinline__ float group4_sum(float v) {
   v += __shfl_xor_sync(0xffffffffu, v, 1);
@@ -39,26 +38,29 @@ __device__ __forceinline__ float group4_sum(float v) {
 }
 
 // One CTA per d x d block; thread (row r = tid/4, part p = tid%4) keeps
-// columns p*cw .. p*cw+cw-1 of row r in registers.  Two Gram–Schmidt sweeps
-// (the second re-orthogonalises, which fp32 needs), then row r is scaled by
-// the length of its own Gaussian vector.
+// columns p*CW .. p*CW+CW-1 of row r in registers (CW = ceil(d/4) rounded up
+// to a multiple of 4; columns >= d are zero).  Two Gram–Schmidt sweeps (the
+// second re-orthogonalises, which fp32 needs), then row r is scaled by the
+// length of its own Gaussian vector.  Each step reads the new unit row into
+// registers once and uses four partial sums, so the step latency is a few
+// short dependency chains rather than one CW-long chain per product.
+template <int CW>
 __global__ void __launch_bounds__(kMaxD * kTPR) orf_block_kernel(uint64_t seed, int m, int d,
                                                                  float* __restrict__ omega) {
-  __shared__ float qbuf[2][kMaxD];
+  __shared__ __align__(16) float qbuf[2][kTPR * CW];
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int r = tid / kTPR;
   const int p = tid % kTPR;
-  const int cw = (d + kTPR - 1) / kTPR;
   const bool row_ok = r < d;
 
-  float g[kCW];
+  float g[CW];
   float len2 = 0.f;
 #pragma unroll
-  for (int k = 0; k < kCW; ++k) {
-    const int c = p * cw + k;
+  for (int k = 0; k < CW; ++k) {
+    const int c = p * CW + k;
     g[k] = 0.f;
-    if (k < cw && c < d && row_ok) {
+    if (c < d && row_ok) {
       const uint64_t idx = (((uint64_t)b * d + r) * d + c) * 2ull;
       g[k] = normal_from_word(splitmix_word(seed, idx));
       const float x = normal_from_word(splitmix_word(seed, idx + 1ull));
@@ -67,45 +69,55 @@ __global__ void __launch_bounds__(kMaxD * kTPR) orf_block_kernel(uint64_t seed, 
   }
   const float len = sqrtf(group4_sum(len2));
 
+  // every thread executes every shuffle (full-warp masks); only the values
+  // they carry depend on the thread's role in the step
   for (int sweep = 0; sweep < 2; ++sweep) {
     for (int i = 0; i < d; ++i) {
       float* q = qbuf[i & 1];
-      float n2 = 0.f;
+      const bool norm_row = (r == i);
+      float n2[4] = {0.f, 0.f, 0.f, 0.f};
+      if (norm_row) {
 #pragma unroll
-      for (int k = 0; k < kCW; ++k) n2 = fmaf(g[k], g[k], n2);
-      n2 = group4_sum(n2);
-      if (r == i) {
-        const float inv = 1.0f / sqrtf(n2);
+        for (int k = 0; k < CW; ++k) n2[k & 3] = fmaf(g[k], g[k], n2[k & 3]);
+      }
+      const float nn = group4_sum((n2[0] + n2[1]) + (n2[2] + n2[3]));
+      if (norm_row) {
+        const float inv = 1.0f / sqrtf(nn);
 #pragma unroll
-        for (int k = 0; k < kCW; ++k) {
+        for (int k = 0; k < CW; ++k) {
           g[k] *= inv;
-          const int c = p * cw + k;
-          if (k < cw && c < d) q[c] = g[k];
+          q[p * CW + k] = g[k];
         }
       }
       __syncthreads();
-      float dot = 0.f;
+      const bool upd = row_ok && r > i;
+      float qv[CW];
+      float dp[4] = {0.f, 0.f, 0.f, 0.f};
+      if (upd) {
 #pragma unroll
-      for (int k = 0; k < kCW; ++k) {
-        const int c = p * cw + k;
-        if (k < cw && c < d) dot = fmaf(q[c], g[k], dot);
-      }
-      dot = group4_sum(dot);
-      if (row_ok && r > i) {
-#pragma unroll
-        for (int k = 0; k < kCW; ++k) {
-          const int c = p * cw + k;
-          if (k < cw && c < d) g[k] = fmaf(-dot, q[c], g[k]);
+        for (int k = 0; k < CW; k += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(q + p * CW + k);
+          qv[k] = v.x;
+          qv[k + 1] = v.y;
+          qv[k + 2] = v.z;
+          qv[k + 3] = v.w;
         }
+#pragma unroll
+        for (int k = 0; k < CW; ++k) dp[k & 3] = fmaf(qv[k], g[k], dp[k & 3]);
+      }
+      const float dot = group4_sum((dp[0] + dp[1]) + (dp[2] + dp[3]));
+      if (upd) {
+#pragma unroll
+        for (int k = 0; k < CW; ++k) g[k] = fmaf(-dot, qv[k], g[k]);
       }
     }
   }
   const int row = b * d + r;
   if (row_ok && row < m) {
 #pragma unroll
-    for (int k = 0; k < kCW; ++k) {
-      const int c = p * cw + k;
-      if (k < cw && c < d) omega[(size_t)row * d + c] = g[k] * len;
+    for (int k = 0; k < CW; ++k) {
+      const int c = p * CW + k;
+      if (c < d) omega[(size_t)row * d + c] = g[k] * len;
     }
   }
 }
@@ -124,7 +136,15 @@ cudaError_t launch_build_orf(uint64_t seed, int m, int d, int orthogonal, float*
   if (orthogonal) {
     const int nb = (m + d - 1) / d;
     const int threads = ((d * kTPR + 31) / 32) * 32;
-    orf_block_kernel<<<nb, threads, 0, stream>>>(seed, m, d, omega);
+    const int cw = (d + kTPR - 1) / kTPR;
+    if (cw <= 4)
+      orf_block_kernel<4><<<nb, threads, 0, stream>>>(seed, m, d, omega);
+    else if (cw <= 8)
+      orf_block_kernel<8><<<nb, threads, 0, stream>>>(seed, m, d, omega);
+    else if (cw <= 16)
+      orf_block_kernel<16><<<nb, threads, 0, stream>>>(seed, m, d, omega);
+    else
+      orf_block_kernel<32><<<nb, threads, 0, stream>>>(seed, m, d, omega);
   } else {
     const int n = m * d;
     iid_kernel<<<(n + 255) / 256, 256, 0, stream>>>(seed, m, d, omega);

@@ -3,17 +3,22 @@
 //
 // "Performer — Rethinking Attention with Performers" (digest), §Key equations
 // and the flowchart: phi(K)^T V and phi(K)^T 1 are formed first, then
-// phi(Q) times each, then the row-wise divide.  The three contractions are
-// dense GEMMs and run on the tensor cores:
-//   projection   P   = X Omega^T           (M = 128 tokens, N = 128 features, K = d)
-//   state        S~ += phi(K)^T [V | 1]    (M = 128 features, N = d + 16,   K = 128 tokens)
-//   output       O   = phi(Q) S~           (M = 128 tokens,   N = d + 16,   K = m)
+// phi(Q) times each, then the row-wise divide; §Methods, causal bullet: the
+// prefix sum G_t = sum_{s<=t} phi(k_s) v_s^T.  The contractions are dense
+// GEMMs and run on the tensor cores:
+//   projection  P  = X Omega^T         M = 128 tokens,   N = 128 features, K = d
+//                                      (Omega = hi + lo, two bf16 MMAs)
+//   state       S~ += phi(K)^T [V|1]   M = 128 features, N = d (+16),      K = 128 tokens
+//   output      O  = phi(Q) S~         M = 128 tokens,   N = d + 16,       K = m
+//   causal      A  = phi(Q_c) phi(K_c)^T (lower triangle kept), O += A [V_c|1]
 // The exponentials of the feature map run on the CUDA cores between them
 // (TMEM -> registers -> bf16 in shared memory).
 //
-// Warp roles in both kernels (192 threads): warp 0 issues TMA loads, warp 1
-// owns tensor memory and issues the MMAs (one elected thread), warps 2-5 are
-// the epilogue (thread = one TMEM lane = one token or one feature).
+// Warp roles: warp 0 issues TMA loads, warp 1 owns tensor memory and issues
+// MMAs (one elected thread), warp 2 (state and causal kernels) computes the
+// squared row norms of the K (and Q) tiles, and eight epilogue warps form two
+// warpgroups that split the columns of each 128-row tile (thread = one TMEM
+// lane = one token or one feature).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -27,18 +32,21 @@ namespace {
 using namespace tc;
 
 constexpr int kBM = 128;          // tokens per tile
-constexpr int kFB = 128;          // features per state CTA
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
+constexpr int kFB = 128;          // features per block
 constexpr uint32_t kTmemCols = 512;
 constexpr int kAtom = 128 * 128;  // bytes of one [128 rows][128 B] swizzle block
+constexpr int kOnesBytes = 4096;  // K-major all-ones B operand: 16 rows x 128 tokens
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = 256;
 
 // ---------------------------------------------------------------------------
 // workspace layout of the tensor-core path
 // ---------------------------------------------------------------------------
 struct TcPlan {
-  int n_fb, n_tiles, n_split, tiles_per_split;   // state kernel
-  int out_tiles_per_cta, out_ctas;               // output kernel
+  bool causal;
+  int n_fb, n_tiles;
+  int tiles_per_split, n_split;      // state partials (bidir: L splits; causal: superchunks - 1)
+  int out_tiles_per_cta, out_ctas;   // output kernel (bidir) / superchunks (causal)
   size_t off_omega_img, off_counters, off_partS, off_state_img, bytes;
 };
 
@@ -48,6 +56,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // fewest splits minimising waves x (tiles per CTA + per-CTA set-up, counted
 // as kCtaOverheadTiles tiles).
 constexpr int kCtaOverheadTiles = 3;
+constexpr int kSMs = 152;
 int pick_split(int units, int tiles, int sms) {
   int best = 1;
   long best_cost = -1;
@@ -63,34 +72,41 @@ int pick_split(int units, int tiles, int sms) {
   return best;
 }
 
-TcPlan tc_plan(const Shape& s) {
+TcPlan tc_plan(bool causal, const Shape& s) {
   TcPlan p{};
   const int BH = s.BH();
-  const int sms = 152;
+  p.causal = causal;
   p.n_fb = s.m / kFB;
   p.n_tiles = (s.L + kBM - 1) / kBM;
-  p.n_split = pick_split(BH * p.n_fb, p.n_tiles, sms);
-  p.tiles_per_split = (p.n_tiles + p.n_split - 1) / p.n_split;
-  p.n_split = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
-  const int oc = pick_split(BH, p.n_tiles, sms);
-  p.out_tiles_per_cta = (p.n_tiles + oc - 1) / oc;
-  p.out_ctas = (p.n_tiles + p.out_tiles_per_cta - 1) / p.out_tiles_per_cta;
-  size_t off = kWsHeader;
-  off = align_up(off, 1024);
+  if (!causal) {
+    const int sp = pick_split(BH * p.n_fb, p.n_tiles, kSMs);
+    p.tiles_per_split = (p.n_tiles + sp - 1) / sp;
+    p.n_split = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    const int oc = pick_split(BH, p.n_tiles, kSMs);
+    p.out_tiles_per_cta = (p.n_tiles + oc - 1) / oc;
+    p.out_ctas = (p.n_tiles + p.out_tiles_per_cta - 1) / p.out_tiles_per_cta;
+  } else {
+    const int sc = pick_split(BH, p.n_tiles, kSMs);
+    p.out_tiles_per_cta = (p.n_tiles + sc - 1) / sc;                          // tiles per superchunk
+    p.out_ctas = (p.n_tiles + p.out_tiles_per_cta - 1) / p.out_tiles_per_cta;  // superchunks
+    p.tiles_per_split = p.out_tiles_per_cta;
+    p.n_split = p.out_ctas - 1;                                               // all but the last
+  }
+  size_t off = align_up(kWsHeader, 1024);
   p.off_omega_img = off;
-  off = align_up(off + (size_t)s.m * s.d * 2, 1024);
+  off = align_up(off + (size_t)s.m * s.d * 4, 1024);   // hi and lo images
   p.off_counters = off;
   off = align_up(off + (size_t)BH * p.n_fb * sizeof(uint32_t), 1024);
   p.off_partS = off;
-  off = align_up(off + (size_t)BH * p.n_fb * p.n_split * (s.d + 1) * kFB * sizeof(float), 1024);
+  off = align_up(off + (size_t)BH * p.n_fb * max(p.n_split, 1) * (s.d + 1) * kFB * sizeof(float), 1024);
   p.off_state_img = off;
-  off = align_up(off + (size_t)BH * s.m * (s.d + 16) * 2, 1024);
+  if (!causal) off = align_up(off + (size_t)BH * s.m * (s.d + 16) * 2, 1024);
   p.bytes = off;
   return p;
 }
 
 // ---------------------------------------------------------------------------
-// shared epilogue pieces
+// shared device pieces
 // ---------------------------------------------------------------------------
 
 // Squared norm of row t of a [128][d] bf16 tile stored as 64-column swizzle
@@ -116,27 +132,57 @@ __device__ __forceinline__ float tile_row_sq(const uint8_t* tile, int t) {
   return acc;
 }
 
-// phi for 32 consecutive features of one row, written as bf16 into the
-// swizzled [feature atom][128 rows][128 B] buffer: phi = 2^(p*c1 - b).
-__device__ __forceinline__ void write_phi32(uint32_t phi_base, int t, int f0, const uint32_t (&p)[32], float c1,
-                                            float b, bool valid) {
+// 32 consecutive columns (f0 .. f0+31) of row t written as bf16 into a
+// swizzled [64-column atom][128 rows][128 B] buffer.  MODE 0: 2^(p*c1 - b)
+// (zero if !valid); MODE 1: the raw values, zeroed where column > t.
+template <int MODE>
+__device__ __forceinline__ void write_row32(uint32_t base, int t, int f0, const uint32_t (&p)[32], float c1, float b,
+                                            bool valid) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     uint32_t w[4];
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
-      const float x0 = valid ? ex2(fmaf(__uint_as_float(p[8 * j + 2 * h]), c1, -b)) : 0.f;
-      const float x1 = valid ? ex2(fmaf(__uint_as_float(p[8 * j + 2 * h + 1]), c1, -b)) : 0.f;
+      const int f = f0 + 8 * j + 2 * h;
+      float x0 = __uint_as_float(p[8 * j + 2 * h]);
+      float x1 = __uint_as_float(p[8 * j + 2 * h + 1]);
+      if (MODE == 0) {
+        x0 = valid ? ex2(fmaf(x0, c1, -b)) : 0.f;
+        x1 = valid ? ex2(fmaf(x1, c1, -b)) : 0.f;
+      } else {
+        x0 = (f <= t) ? x0 : 0.f;
+        x1 = (f + 1 <= t) ? x1 : 0.f;
+      }
       w[h] = pack_bf16(x0, x1);
     }
     const int f = f0 + 8 * j;
     const int atom = f >> 6, chunk = (f & 63) >> 3;
-    st_shared_v4(phi_base + atom * kAtom + t * 128 + ((chunk ^ (t & 7)) << 4), w[0], w[1], w[2], w[3]);
+    st_shared_v4(base + atom * kAtom + t * 128 + ((chunk ^ (t & 7)) << 4), w[0], w[1], w[2], w[3]);
   }
 }
 
+__device__ __forceinline__ void fill_ones(uint8_t* p, int tid0, int nthreads) {
+  const uint32_t one2 = 0x3F803F80u;
+  for (int e = threadIdx.x - tid0; e < kOnesBytes / 16; e += nthreads)
+    *reinterpret_cast<uint4*>(p + e * 16) = make_uint4(one2, one2, one2, one2);
+}
+
+// MMA descriptors of the fixed layouts
+__device__ __forceinline__ uint64_t kmajor(uint32_t base, int k) {      // K-major SW128, k-step of 16
+  return sdesc(base + (k >> 2) * kAtom + (k & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t mnmajor(uint32_t base, int k) {     // MN-major SW128, 16-row k-step
+  return sdesc(base + k * 2048, kAtom, 1024);
+}
+__device__ __forceinline__ uint64_t ones_desc(uint32_t base, int k) {   // K-major ones, 16 rows
+  return sdesc(base + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024);
+}
+
 // ---------------------------------------------------------------------------
-// state kernel: one (L split, 128-feature block, head) per CTA
+// state kernel: one (token split, 128-feature block, head) per CTA.
+// Bidirectional: the last CTA of a (head, block) adds the splits (fixed order)
+// into the bf16 state image read by the output kernel.  Causal: the partial
+// of each superchunk but the last is kept for the scan.
 // ---------------------------------------------------------------------------
 struct StateParams {
   const float* key_ref;
@@ -145,34 +191,38 @@ struct StateParams {
   uint32_t* counters;      // [BH][n_fb]
   uint8_t* state_img;      // [BH][m/64][d+16][128 B]
   int32_t* status;
-  int L, m, n_split, tiles_per_split;
+  int L, m, n_split, tiles_per_split, merge;
   float scale;
 };
 
+constexpr int kStateThreads = 352;   // warps 0 TMA, 1 MMA, 2 norms, 3-10 epilogue
+
 template <int D>
 struct StateCfg {
-  static constexpr int NS = (D == 64) ? 3 : 2;      // K/V stages
-  static constexpr int NPHI = (D == 64) ? 2 : 1;    // phi buffers
-  static constexpr int kTileBytes = D * kBM * 2;    // one K or V tile
-  static constexpr int kOmega = 0;
-  static constexpr int kOnes = kOmega + kFB * D * 2;
-  static constexpr int kStages = kOnes + kAtom;
+  static constexpr int NS = 3;                     // K/V stages
+  static constexpr int NPHI = 2;                   // phi buffers
+  static constexpr int kTileBytes = D * kBM * 2;   // one K or V tile
+  static constexpr int kOmega = 0;                 // hi, lo
+  static constexpr int kOnes = kOmega + 2 * kFB * D * 2;
+  static constexpr int kStages = kOnes + kOnesBytes;
   static constexpr int kPhi = kStages + NS * 2 * kTileBytes;
-  static constexpr int kBars = kPhi + NPHI * kAtom * 2;
-  static constexpr int kSmem = kBars + 256 + 1024;  // + barriers/slots + alignment slack
+  static constexpr int kNorm = kPhi + NPHI * 2 * kAtom;
+  static constexpr int kBars = kNorm + NS * kBM * 4;
+  static constexpr int kSmem = kBars + 512 + 1024;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) state_kernel(const __grid_constant__ CUtensorMap mapK,
-                                                            const __grid_constant__ CUtensorMap mapV,
-                                                            StateParams prm) {
+__global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_constant__ CUtensorMap mapK,
+                                                                 const __grid_constant__ CUtensorMap mapV,
+                                                                 StateParams prm) {
   using C = StateCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBars);
   uint64_t* full = bars;                      // [NS]
   uint64_t* empty = full + C::NS;             // [NS]
-  uint64_t* p_full = empty + C::NS;           // [2]
+  uint64_t* norm_full = empty + C::NS;        // [NS]
+  uint64_t* p_full = norm_full + C::NS;       // [2]
   uint64_t* p_free = p_full + 2;              // [2]
   uint64_t* phi_full = p_free + 2;            // [NPHI]
   uint64_t* phi_free = phi_full + C::NPHI;    // [NPHI]
@@ -181,6 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const __grid_constan
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* is_last = const_cast<int*>(abort_flag) + 1;
+  float* norm_s = reinterpret_cast<float*>(sm + C::kNorm);   // [NS][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x, fb = blockIdx.y, bh = blockIdx.z;
@@ -194,13 +245,14 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const __grid_constan
     for (int i = 0; i < C::NS; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
+      mbar_init(&norm_full[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 1);
-      mbar_init(&p_free[i], 4);
+      mbar_init(&p_free[i], kEpiWarps);
     }
     for (int i = 0; i < C::NPHI; ++i) {
-      mbar_init(&phi_full[i], 4);
+      mbar_init(&phi_full[i], kEpiWarps);
       mbar_init(&phi_free[i], 1);
     }
     mbar_init(setup_bar, 1);
@@ -212,11 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const __grid_constan
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (warp >= 2) {
-    // all-ones block: the extra 16 columns of [V | 1]
-    const uint32_t one2 = 0x3F803F80u;
-    for (int e = threadIdx.x - 64; e < kAtom / 16; e += kEpiThreads)
-      *reinterpret_cast<uint4*>(sm + C::kOnes + e * 16) = make_uint4(one2, one2, one2, one2);
+  if (warp >= 3) {
+    fill_ones(sm + C::kOnes, 96, kEpiThreads);
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -228,8 +277,10 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const __grid_constan
     if (lane == 0) {
       prefetch_tmap(&mapK);
       prefetch_tmap(&mapV);
-      mbar_arrive_expect_tx(setup_bar, kFB * D * 2);
+      mbar_arrive_expect_tx(setup_bar, 2 * kFB * D * 2);
       bulk_load(sm + C::kOmega, prm.omega_img + (size_t)fb * kFB * D * 2, kFB * D * 2, setup_bar);
+      bulk_load(sm + C::kOmega + kFB * D * 2, prm.omega_img + ((size_t)prm.m + fb * kFB) * D * 2, kFB * D * 2,
+                setup_bar);
       int last_issue[C::NS];
       for (int i = 0; i < C::NS; ++i) last_issue[i] = -1;
       for (int i = 0; i < n_tiles; ++i) {
@@ -246,7 +297,6 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const __grid_constan
         }
         last_issue[st] = i;
       }
-      // drain: every issued load has landed before the CTA can exit
       for (int st = 0; st < C::NS; ++st)
         if (last_issue[st] >= 0) mbar_wait(&full[st], (last_issue[st] / C::NS) & 1, wctx);
     }
@@ -254,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const __grid_constan
     if (lane == 0) {
       const uint32_t id_proj = idesc_bf16(kBM, kFB, false, false);
       const uint32_t id_state = idesc_bf16(kFB, D, true, true);
-      const uint32_t id_ones = idesc_bf16(kFB, 16, true, true);
+      const uint32_t id_ones = idesc_bf16(kFB, 16, true, false);
       const uint32_t s_tm = tmem + 256;           // S~: columns 256 .. 256+d+15
       const uint32_t omega_a = smem_addr(sm + C::kOmega);
       const uint32_t ones_a = smem_addr(sm + C::kOnes);
@@ -267,10 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const __grid_constan
         const uint32_t v_a = smem_addr(sm + C::kStages + (j % C::NS) * 2 * C::kTileBytes + C::kTileBytes);
 #pragma unroll
         for (int k = 0; k < kBM / 16; ++k) {
-          const uint64_t ad = sdesc(phi_a + k * 2048, kAtom, 1024);
+          const uint64_t ad = mnmajor(phi_a, k);
           const bool acc = (j > 0) || (k > 0);
-          mma_bf16(s_tm, ad, sdesc(v_a + k * 2048, kAtom, 1024), id_state, acc);
-          mma_bf16(s_tm + D, ad, sdesc(ones_a + k * 2048, kAtom, 1024), id_ones, acc);
+          mma_bf16(s_tm, ad, mnmajor(v_a, k), id_state, acc);
+          mma_bf16(s_tm + D, ad, ones_desc(ones_a, k), id_ones, acc);
         }
         mma_commit(&phi_free[b]);
         mma_commit(&empty[j % C::NS]);
@@ -284,8 +334,9 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const __grid_constan
         const uint32_t k_a = smem_addr(sm + C::kStages + st * 2 * C::kTileBytes);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * kAtom + (k & 3) * 32;
-          mma_bf16(tmem + pb * kFB, sdesc(k_a + off, 16, 1024), sdesc(omega_a + off, 16, 1024), id_proj, k > 0);
+          const uint64_t ad = kmajor(k_a, k);
+          mma_bf16(tmem + pb * kFB, ad, kmajor(omega_a, k), id_proj, k > 0);
+          mma_bf16(tmem + pb * kFB, ad, kmajor(omega_a + kFB * D * 2, k), id_proj, true);
         }
         mma_commit(&p_full[pb]);
         if (i > 0 && !issue_state(i - 1)) { ok = false; break; }
@@ -294,32 +345,43 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const __grid_constan
       mma_commit(done_bar);
       mbar_wait(done_bar, 0, wctx);
     }
+  } else if (warp == 2) {
+    // squared norms of the K rows of each stage
+    for (int i = 0; i < n_tiles; ++i) {
+      const int st = i % C::NS;
+      if (!mbar_wait(&full[st], (i / C::NS) & 1, wctx)) break;
+      const uint8_t* kt = sm + C::kStages + st * 2 * C::kTileBytes;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) norm_s[st * kBM + lane + 32 * j] = tile_row_sq<D>(kt, lane + 32 * j);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&norm_full[st]);
+    }
   } else {
-    // ---------------- epilogue: 128 threads, one TMEM lane each ----------------
+    // ---------------- epilogue: two warpgroups x 128 lanes ----------------
+    const int wg = (warp - 3) >> 2;
     const int q = warp & 3;
     const int t = q * 32 + lane;                   // token row of P, feature row of S~
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const float R = *prm.key_ref;
+    const float R = prm.key_ref[0];
     const float c1 = prm.scale * kLog2e;
     const float hs2 = 0.5f * prm.scale * prm.scale;
+    const int col0 = wg * 64;
     bool ok = true;
     for (int i = 0; ok && i < n_tiles; ++i) {
       const int st = i % C::NS, pb = i & 1, b = i % C::NPHI;
       if (!mbar_wait(&p_full[pb], (i >> 1) & 1, wctx)) { ok = false; break; }
+      if (!mbar_wait(&norm_full[st], (i / C::NS) & 1, wctx)) { ok = false; break; }
       tc_fence_after();
-      const uint8_t* kt = sm + C::kStages + st * 2 * C::kTileBytes;
-      const float ksq = tile_row_sq<D>(kt, t);
-      const float bias = (hs2 * ksq + R) * kLog2e;
+      const float bias = (hs2 * norm_s[st * kBM + t] + R) * kLog2e;
       const bool valid = (tile0 + i) * kBM + t < prm.L;
       if (i >= C::NPHI && !mbar_wait(&phi_free[b], ((i / C::NPHI) - 1) & 1, wctx)) { ok = false; break; }
+      uint32_t p0[32], p1[32];
+      tmem_ld32(tmem + lane_off + pb * kFB + col0, p0);
+      tmem_ld32(tmem + lane_off + pb * kFB + col0 + 32, p1);
+      tmem_ld_wait();
       const uint32_t phi_a = smem_addr(sm + C::kPhi + b * 2 * kAtom);
-#pragma unroll
-      for (int cb = 0; cb < kFB / 32; ++cb) {
-        uint32_t p[32];
-        tmem_ld32(tmem + lane_off + pb * kFB + cb * 32, p);
-        tmem_ld_wait();
-        write_phi32(phi_a, t, cb * 32, p, c1, bias, valid);
-      }
+      write_row32<0>(phi_a, t, col0, p0, c1, bias, valid);
+      write_row32<0>(phi_a, t, col0 + 32, p1, c1, bias, valid);
       tc_fence_before();
       fence_proxy_async_smem();
       __syncwarp();
@@ -328,47 +390,52 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const __grid_constan
         mbar_arrive(&phi_full[b]);
       }
     }
-    // final state: lane f holds feature f of this block
+    // final state: lane f holds feature f of this block; WG0 columns 0..31,
+    // WG1 columns 32..63 and the normaliser column d
     const bool done = mbar_wait(done_bar, 0, wctx);
     tc_fence_after();
     float* dst = prm.partS + ((((size_t)bh * n_fb + fb) * prm.n_split + split) * (D + 1)) * kFB;
     if (done && !*abort_flag) {
 #pragma unroll
-      for (int cb = 0; cb < D / 32; ++cb) {
+      for (int cb = wg; cb < D / 32; cb += 2) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_off + 256 + cb * 32, v);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j) dst[(size_t)(cb * 32 + j) * kFB + t] = __uint_as_float(v[j]);
       }
-      uint32_t z[16];
-      tmem_ld16(tmem + lane_off + 256 + D, z);
-      tmem_ld_wait();
-      dst[(size_t)D * kFB + t] = __uint_as_float(z[0]);
+      if (wg == 1) {
+        uint32_t z[16];
+        tmem_ld16(tmem + lane_off + 256 + D, z);
+        tmem_ld_wait();
+        dst[(size_t)D * kFB + t] = __uint_as_float(z[0]);
+      }
     }
     tc_fence_before();
-    // the last CTA of this (head, feature block) adds the splits in order
-    named_bar(1, kEpiThreads);
-    if (threadIdx.x == 64) {
-      __threadfence();
-      const uint32_t old = atomicAdd(&prm.counters[bh * n_fb + fb], 1u);
-      *is_last = (old == (uint32_t)(prm.n_split - 1)) ? 1 : 0;
-    }
-    named_bar(1, kEpiThreads);
-    if (*is_last) {
-      __threadfence();
-      const float* src = prm.partS + (((size_t)bh * n_fb + fb) * prm.n_split) * (D + 1) * kFB;
-      uint8_t* img = prm.state_img + (size_t)bh * prm.m * (D + 16) * 2;
-      const int f = fb * kFB + t;               // feature of this thread
-      const int atom = f >> 6, cc = f & 63;
-      for (int n = 0; n < D + 16; ++n) {
-        float acc = 0.f;
-        if (n <= D)
-          for (int p = 0; p < prm.n_split; ++p) acc += src[((size_t)p * (D + 1) + n) * kFB + t];
-        const size_t off = ((size_t)atom * (D + 16) + n) * 128 + (((cc >> 3) ^ (n & 7)) << 4) + (cc & 7) * 2;
-        *reinterpret_cast<__nv_bfloat16*>(img + off) = __float2bfloat16_rn(acc);
+    if (prm.merge) {
+      named_bar(1, kEpiThreads);
+      if (threadIdx.x == 96) {
+        __threadfence();
+        const uint32_t old = atomicAdd(&prm.counters[bh * n_fb + fb], 1u);
+        *is_last = (old == (uint32_t)(prm.n_split - 1)) ? 1 : 0;
       }
-      if (threadIdx.x == 64) prm.counters[bh * n_fb + fb] = 0;
+      named_bar(1, kEpiThreads);
+      if (*is_last) {
+        __threadfence();
+        const float* src = prm.partS + (((size_t)bh * n_fb + fb) * prm.n_split) * (D + 1) * kFB;
+        uint8_t* img = prm.state_img + (size_t)bh * prm.m * (D + 16) * 2;
+        const int f = fb * kFB + t;
+        const int atom = f >> 6, cc = f & 63;
+        const int n0 = wg * ((D + 16) / 2), n1 = n0 + (D + 16) / 2;
+        for (int n = n0; n < n1; ++n) {
+          float acc = 0.f;
+          if (n <= D)
+            for (int p = 0; p < prm.n_split; ++p) acc += src[((size_t)p * (D + 1) + n) * kFB + t];
+          const size_t off = ((size_t)atom * (D + 16) + n) * 128 + (((cc >> 3) ^ (n & 7)) << 4) + (cc & 7) * 2;
+          *reinterpret_cast<__nv_bfloat16*>(img + off) = __float2bfloat16_rn(acc);
+        }
+        if (threadIdx.x == 96) prm.counters[bh * n_fb + fb] = 0;
+      }
     }
   }
   tc_fence_before();
@@ -378,7 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const __grid_constan
 }
 
 // ---------------------------------------------------------------------------
-// output kernel: CTA = a run of 128-token tiles of one head; m <= 256
+// bidirectional output kernel: CTA = a run of 128-token tiles of one head;
+// m <= 256 (all projections of a tile fit in tensor memory: exact row max)
 // ---------------------------------------------------------------------------
 struct OutParams {
   const uint8_t* omega_img;
@@ -388,25 +456,28 @@ struct OutParams {
   float scale;
 };
 
+constexpr int kOutThreads = 320;   // warps 0 TMA, 1 MMA, 2-9 epilogue
+
 template <int D>
 struct OutCfg {
   static constexpr int NSQ = 2;
   static constexpr int kTileBytes = D * kBM * 2;
-  static constexpr int kOmegaMax = 256 * D * 2;
+  static constexpr int kOmegaMax = 2 * 256 * D * 2;     // hi and lo
   static constexpr int kStateMax = 256 * (D + 16) * 2;
   static constexpr int kOmega = 0;
   static constexpr int kState = kOmega + kOmegaMax;
   static constexpr int kQ = kState + kStateMax;
   static constexpr int kPhi = kQ + NSQ * kTileBytes;
-  static constexpr int kOut = kPhi + 4 * kAtom;      // 128 x 256 bf16
-  static constexpr int kBars = kOut + kTileBytes;
-  static constexpr int kSmem = kBars + 256 + 1024;
+  static constexpr int kOut = kPhi + 4 * kAtom;         // 128 x 256 bf16
+  static constexpr int kSmax = kOut + kTileBytes;       // [2 tiles][2 groups][128] floats
+  static constexpr int kBars = kSmax + 2 * 2 * kBM * 4;
+  static constexpr int kSmem = kBars + 512 + 1024;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) output_kernel(const __grid_constant__ CUtensorMap mapQ,
-                                                             const __grid_constant__ CUtensorMap mapO,
-                                                             OutParams prm) {
+__global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_constant__ CUtensorMap mapQ,
+                                                                const __grid_constant__ CUtensorMap mapO,
+                                                                OutParams prm) {
   using C = OutCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -423,6 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) output_kernel(const __grid_consta
   uint64_t* done_bar = setup_bar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* smax = reinterpret_cast<float*>(sm + C::kSmax);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
@@ -440,12 +512,12 @@ __global__ void __launch_bounds__(kThreads, 1) output_kernel(const __grid_consta
       mbar_init(&q_empty[i], 1);
     }
     mbar_init(p_full, 1);
-    mbar_init(p_free, 4);
-    mbar_init(phi_full, 4);
+    mbar_init(p_free, kEpiWarps);
+    mbar_init(phi_full, kEpiWarps);
     mbar_init(phi_free, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&o_full[i], 1);
-      mbar_init(&o_free[i], 4);
+      mbar_init(&o_free[i], kEpiWarps);
     }
     mbar_init(setup_bar, 1);
     mbar_init(done_bar, 1);
@@ -465,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) output_kernel(const __grid_consta
     if (lane == 0) {
       prefetch_tmap(&mapQ);
       prefetch_tmap(&mapO);
-      const uint32_t ob = m * D * 2, sb = m * (D + 16) * 2;
+      const uint32_t ob = 2 * m * D * 2, sb = m * (D + 16) * 2;
       mbar_arrive_expect_tx(setup_bar, ob + sb);
       bulk_load(sm + C::kOmega, prm.omega_img, ob, setup_bar);
       bulk_load(sm + C::kState, prm.state_img + (size_t)bh * sb, sb, setup_bar);
@@ -500,9 +572,9 @@ __global__ void __launch_bounds__(kThreads, 1) output_kernel(const __grid_consta
         for (int f = 0; f < n_fb; ++f) {
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * kAtom + (k & 3) * 32;
-            mma_bf16(tmem + f * kFB, sdesc(q_a + off, 16, 1024),
-                     sdesc(omega_a + f * kFB * D * 2 + off, 16, 1024), id_proj, k > 0);
+            const uint64_t ad = kmajor(q_a, k);
+            mma_bf16(tmem + f * kFB, ad, kmajor(omega_a + f * kFB * D * 2, k), id_proj, k > 0);
+            mma_bf16(tmem + f * kFB, ad, kmajor(omega_a + (m + f * kFB) * D * 2, k), id_proj, true);
           }
         }
         mma_commit(p_full);
@@ -511,9 +583,8 @@ __global__ void __launch_bounds__(kThreads, 1) output_kernel(const __grid_consta
         if (i >= 2 && !mbar_wait(&o_free[ob], ((i >> 1) - 1) & 1, wctx)) { ok = false; break; }
         tc_fence_after();
         for (int kk = 0; kk < m / 16; ++kk) {
-          const uint32_t pa = phi_a + (kk >> 2) * kAtom + (kk & 3) * 32;
           const uint32_t sa = state_a + (kk >> 2) * (D + 16) * 128 + (kk & 3) * 32;
-          mma_bf16(tmem + o_col[ob], sdesc(pa, 16, 1024), sdesc(sa, 16, 1024), id_out, kk > 0);
+          mma_bf16(tmem + o_col[ob], kmajor(phi_a, kk), sdesc(sa, 16, 1024), id_out, kk > 0);
         }
         mma_commit(&o_full[ob]);
         mma_commit(phi_free);
@@ -522,82 +593,79 @@ __global__ void __launch_bounds__(kThreads, 1) output_kernel(const __grid_consta
       mbar_wait(done_bar, 0, wctx);
     }
   } else {
+    const int wg = (warp - 2) >> 2;
     const int q = warp & 3;
     const int t = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const float c1 = prm.scale * kLog2e;
     const uint32_t phi_a = smem_addr(sm + C::kPhi);
     const uint32_t out_a = smem_addr(sm + C::kOut);
+    const int half = m / 2;            // features handled by this warpgroup
+    const int f_lo = wg * half;
     bool ok = true;
-    // writes O of tile j (TMEM buffer j & 1) through the staging tile + TMA store
     auto store_out = [&](int j) {
       const int ob = j & 1;
       const bool have = mbar_wait(&o_full[ob], (j >> 1) & 1, wctx);
       tc_fence_after();
-      float o[D];
-      float den = 1.f;
+      uint32_t v[32], z[16];
       if (have) {
-#pragma unroll
-        for (int cb = 0; cb < D / 32; ++cb) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + o_col[ob] + cb * 32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int x = 0; x < 32; ++x) o[cb * 32 + x] = __uint_as_float(v[x]);
-        }
-        uint32_t z[16];
+        tmem_ld32(tmem + lane_off + o_col[ob] + wg * 32, v);
         tmem_ld16(tmem + lane_off + o_col[ob] + D, z);
         tmem_ld_wait();
-        den = __uint_as_float(z[0]);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_free[ob]);
+      const float den = have ? __uint_as_float(z[0]) : 1.f;
       const int row = (tile0 + j) * kBM + t;
-      if (row < prm.L && (!(den > 0.f) || !isfinite(den))) report_status(prm.status, FAVOR_ERR_NONFINITE);
+      if (have && row < prm.L && (!(den > 0.f) || !isfinite(den))) report_status(prm.status, FAVOR_ERR_NONFINITE);
       const float inv = 1.0f / den;
       if (threadIdx.x == 64 && j > 0) bulk_wait_read0();   // previous store has left the staging tile
       named_bar(1, kEpiThreads);
 #pragma unroll
-      for (int a = 0; a < D / 64; ++a) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float* x = o + a * 64 + c * 8;
-          st_shared_v4(out_a + a * kAtom + t * 128 + ((c ^ (t & 7)) << 4), pack_bf16(x[0] * inv, x[1] * inv),
-                       pack_bf16(x[2] * inv, x[3] * inv), pack_bf16(x[4] * inv, x[5] * inv),
-                       pack_bf16(x[6] * inv, x[7] * inv));
-        }
+      for (int c = 0; c < 4; ++c) {
+        const int chunk = wg * 4 + c;
+        const float* x = reinterpret_cast<const float*>(v) + c * 8;
+        st_shared_v4(out_a + t * 128 + ((chunk ^ (t & 7)) << 4), pack_bf16(x[0] * inv, x[1] * inv),
+                     pack_bf16(x[2] * inv, x[3] * inv), pack_bf16(x[4] * inv, x[5] * inv),
+                     pack_bf16(x[6] * inv, x[7] * inv));
       }
       fence_proxy_async_smem();
       named_bar(1, kEpiThreads);
       if (threadIdx.x == 64 && have && !*abort_flag) {
-#pragma unroll
-        for (int a = 0; a < D / 64; ++a) tma_store_3d(&mapO, a * 64, (tile0 + j) * kBM, bh, sm + C::kOut + a * kAtom);
+        tma_store_3d(&mapO, 0, (tile0 + j) * kBM, bh, sm + C::kOut);
         bulk_commit();
       }
     };
     for (int i = 0; i < n_tiles; ++i) {
       if (ok) ok = mbar_wait(p_full, i & 1, wctx);
       tc_fence_after();
-      // pass 1: exact row maximum over all m features
+      // pass 1: exact row maximum over all m features (both warpgroups)
       float mx = -INFINITY;
       if (ok) {
-        for (int cb = 0; cb < m / 32; ++cb) {
-          uint32_t p[32];
-          tmem_ld32(tmem + lane_off + cb * 32, p);
+        for (int cb = 0; cb < half / 32; cb += 2) {
+          uint32_t p0[32], p1[32];
+          tmem_ld32(tmem + lane_off + f_lo + cb * 32, p0);
+          tmem_ld32(tmem + lane_off + f_lo + cb * 32 + 32, p1);
           tmem_ld_wait();
 #pragma unroll
-          for (int x = 0; x < 32; ++x) mx = fmaxf(mx, __uint_as_float(p[x]));
+          for (int x = 0; x < 32; ++x) mx = fmaxf(mx, fmaxf(__uint_as_float(p0[x]), __uint_as_float(p1[x])));
         }
       }
+      float* sx = smax + (i & 1) * 2 * kBM;
+      sx[wg * kBM + t] = mx;
+      named_bar(2, kEpiThreads);
+      mx = fmaxf(sx[t], sx[kBM + t]);
       const float bias = mx * c1;
       if (ok && i >= 1) ok = mbar_wait(phi_free, (i - 1) & 1, wctx);
       if (ok) {
-        for (int cb = 0; cb < m / 32; ++cb) {
-          uint32_t p[32];
-          tmem_ld32(tmem + lane_off + cb * 32, p);
+        for (int cb = 0; cb < half / 32; cb += 2) {
+          uint32_t p0[32], p1[32];
+          tmem_ld32(tmem + lane_off + f_lo + cb * 32, p0);
+          tmem_ld32(tmem + lane_off + f_lo + cb * 32 + 32, p1);
           tmem_ld_wait();
-          write_phi32(phi_a, t, cb * 32, p, c1, bias, true);
+          write_row32<0>(phi_a, t, f_lo + cb * 32, p0, c1, bias, true);
+          write_row32<0>(phi_a, t, f_lo + cb * 32 + 32, p1, c1, bias, true);
         }
       }
       tc_fence_before();
@@ -611,6 +679,439 @@ __global__ void __launch_bounds__(kThreads, 1) output_kernel(const __grid_consta
     }
     if (n_tiles >= 1) store_out(n_tiles - 1);
     if (threadIdx.x == 64) bulk_wait0();
+    mbar_wait(done_bar, 0, wctx);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// causal kernel: CTA = one superchunk of one head, walking 128-token chunks.
+// G (m x (d+16), fp32) lives in tensor memory; it starts as the sum of the
+// earlier superchunks' partial states.  Per chunk c and 128-feature block fb:
+//   phi(K_c), G_s,fb <- bf16(G_fb), phi(Q_c)                       (CUDA cores)
+//   G_fb += phi(K_c)_fb^T [V_c | 1];  A += phi(Q_c)_fb phi(K_c)_fb^T;
+//   O += phi(Q_c)_fb G_s,fb                                       (tensor cores)
+// then A's upper triangle is zeroed (diagonal kept), O += A [V_c | 1], and
+// O is divided by its normaliser column.  The query row reference is the
+// exact maximum over the first feature block, raised if needed to
+// s |q| max_i |w_i| - 20 (the largest possible exponent less 20), so every
+// phi(q) is at most e^20.
+// ---------------------------------------------------------------------------
+struct CausalParams {
+  const float* key_ref;   // [0] = R, [1] = W
+  const uint8_t* omega_img;
+  const float* partS;     // [BH][n_fb][n_split][d+1][128]
+  int32_t* status;
+  int L, m, n_split, tiles_per_sc;
+  float scale;
+};
+
+constexpr int kCausalThreads = 352;   // warps 0 TMA, 1 MMA, 2 norms, 3-10 epilogue
+
+template <int D>
+struct CausalCfg {
+  static constexpr int kTileBytes = D * kBM * 2;
+  static constexpr int kOmega = 0;                                 // hi, lo: 2 * m * d * 2
+  static constexpr int kOnes = kOmega + 2 * 256 * D * 2;
+  static constexpr int kPhiK = kOnes + kOnesBytes;                  // also the masked A tile
+  static constexpr int kPhiQ = kPhiK + 2 * kAtom;                   // also the output staging tile
+  static constexpr int kGs = kPhiQ + 2 * kAtom;                     // bf16 G, [m/64][d+16][128 B]
+  static constexpr int kK = kGs + 256 * (D + 16) * 2;
+  static constexpr int kQ = kK + kTileBytes;
+  static constexpr int kV = kQ + kTileBytes;
+  static constexpr int kNorm = kV + kTileBytes;                     // [2 chunks][K, Q][128] floats
+  static constexpr int kSmax = kNorm + 2 * 2 * kBM * 4;             // [2 chunks][2 groups][128]
+  static constexpr int kBars = kSmax + 2 * 2 * kBM * 4;
+  static constexpr int kSmem = kBars + 512 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_constant__ CUtensorMap mapQ,
+                                                                   const __grid_constant__ CUtensorMap mapK,
+                                                                   const __grid_constant__ CUtensorMap mapV,
+                                                                   const __grid_constant__ CUtensorMap mapO,
+                                                                   CausalParams prm) {
+  using C = CausalCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* b = reinterpret_cast<uint64_t*>(sm + C::kBars);
+  uint64_t *k_full = b + 0, *q_full = b + 1, *v_full = b + 2, *k_empty = b + 3, *q_empty = b + 4, *v_empty = b + 5;
+  // knorm_full / qnorm_full: [chunk parity]; gs_full, gdone: [feature block], so that
+  // each completes once per chunk and no waiter can fall two phases behind
+  uint64_t *knorm_full = b + 6, *qnorm_full = b + 8, *setup_bar = b + 10, *done_bar = b + 11;
+  uint64_t *pk_full = b + 12, *phik_full = b + 13, *pq_full = b + 14, *phiq_full = b + 15, *gs_full = b + 16;
+  uint64_t *gdone = b + 18, *phik_free = b + 20, *phiq_free = b + 21, *a_full = b + 22, *as_full = b + 23;
+  uint64_t *o_full = b + 24, *o_free = b + 25;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b + 26);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+#ifdef FAVOR_WAIT_DIAG
+  if (threadIdx.x == 0 && blockIdx.x + blockIdx.y == 0) g_favor_wait_diag[255][0] = (int)(smem_addr(b) >> 3);
+#endif
+  float* norms = reinterpret_cast<float*>(sm + C::kNorm);   // [c&1][K=0/Q=1][128]
+  float* smax = reinterpret_cast<float*>(sm + C::kSmax);    // [c&1][wg][128]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sc = blockIdx.x, bh = blockIdx.y;
+  const int m = prm.m, n_fb = m / kFB;
+  const int n_tiles_total = (prm.L + kBM - 1) / kBM;
+  const int tile0 = sc * prm.tiles_per_sc;
+  const int n_chunks = min(prm.tiles_per_sc, n_tiles_total - tile0);
+  const WaitCtx wctx{abort_flag, prm.status};
+  // TMEM columns: X (projection), A (chunk scores), O, then G_fb at G_COL + fb * (D + 16)
+  const uint32_t X_COL = 0, A_COL = 128, O_COL = 256, G_COL = 336;
+
+  if (threadIdx.x == 0) {
+    mbar_init(k_full, 1);
+    mbar_init(q_full, 1);
+    mbar_init(v_full, 1);
+    mbar_init(k_empty, 2);          // MMA commit + norm warp
+    mbar_init(q_empty, 2);
+    mbar_init(v_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&knorm_full[i], 1);
+      mbar_init(&qnorm_full[i], 1);
+      mbar_init(&gdone[i], 1);
+      mbar_init(&gs_full[i], kEpiWarps);
+    }
+    mbar_init(setup_bar, 1);
+    mbar_init(done_bar, 1);
+    mbar_init(pk_full, 1);
+    mbar_init(phik_full, kEpiWarps);
+    mbar_init(pq_full, 1);
+    mbar_init(phiq_full, kEpiWarps);
+    mbar_init(phik_free, 1);
+    mbar_init(phiq_free, 1);
+    mbar_init(a_full, 1);
+    mbar_init(as_full, kEpiWarps);
+    mbar_init(o_full, 1);
+    mbar_init(o_free, kEpiWarps);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp >= 3) {
+    fill_ones(sm + C::kOnes, 96, kEpiThreads);
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&mapQ);
+      prefetch_tmap(&mapK);
+      prefetch_tmap(&mapV);
+      prefetch_tmap(&mapO);
+      mbar_arrive_expect_tx(setup_bar, 2 * m * D * 2);
+      bulk_load(sm + C::kOmega, prm.omega_img, 2 * m * D * 2, setup_bar);
+      int issued = 0;
+      for (int c = 0; c < n_chunks; ++c) {
+        const int row = (tile0 + c) * kBM;
+        if (c >= 1 && !mbar_wait(k_empty, (c - 1) & 1, wctx)) break;
+        mbar_arrive_expect_tx(k_full, C::kTileBytes);
+        for (int a = 0; a < D / 64; ++a) tma_load_3d(sm + C::kK + a * kAtom, &mapK, a * 64, row, bh, k_full);
+        if (c >= 1 && !mbar_wait(q_empty, (c - 1) & 1, wctx)) break;
+        mbar_arrive_expect_tx(q_full, C::kTileBytes);
+        for (int a = 0; a < D / 64; ++a) tma_load_3d(sm + C::kQ + a * kAtom, &mapQ, a * 64, row, bh, q_full);
+        if (c >= 1 && !mbar_wait(v_empty, (c - 1) & 1, wctx)) break;
+        mbar_arrive_expect_tx(v_full, C::kTileBytes);
+        for (int a = 0; a < D / 64; ++a) tma_load_3d(sm + C::kV + a * kAtom, &mapV, a * 64, row, bh, v_full);
+        issued = c + 1;
+      }
+      // drain: the loads of the last chunk issued have landed
+      if (issued > 0) {
+        mbar_wait(k_full, (issued - 1) & 1, wctx);
+        mbar_wait(q_full, (issued - 1) & 1, wctx);
+        mbar_wait(v_full, (issued - 1) & 1, wctx);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_proj = idesc_bf16(kBM, kFB, false, false);
+      const uint32_t id_state = idesc_bf16(kFB, D, true, true);
+      const uint32_t id_ones_mn = idesc_bf16(kFB, 16, true, false);
+      const uint32_t id_a = idesc_bf16(kBM, kBM, false, false);
+      const uint32_t id_og = idesc_bf16(kBM, D + 16, false, false);
+      const uint32_t id_av = idesc_bf16(kBM, D, false, true);
+      const uint32_t id_aones = idesc_bf16(kBM, 16, false, false);
+      const uint32_t om_a = smem_addr(sm + C::kOmega), ones_a = smem_addr(sm + C::kOnes);
+      const uint32_t phik_a = smem_addr(sm + C::kPhiK), phiq_a = smem_addr(sm + C::kPhiQ);
+      const uint32_t gs_a = smem_addr(sm + C::kGs), k_a = smem_addr(sm + C::kK), q_a = smem_addr(sm + C::kQ);
+      const uint32_t v_a = smem_addr(sm + C::kV);
+      bool ok = mbar_wait(setup_bar, 0, wctx);
+      for (int c = 0; ok && c < n_chunks; ++c) {
+        for (int fb = 0; ok && fb < n_fb; ++fb) {
+          const int u = c * n_fb + fb;
+          const uint32_t om_hi = om_a + fb * kFB * D * 2, om_lo = om_a + (m + fb * kFB) * D * 2;
+          // P_K -> X  (X is free once the previous phi(Q) block has been read)
+          if (fb == 0 && !mbar_wait(k_full, c & 1, wctx)) { ok = false; break; }
+          if (u >= 1 && !mbar_wait(phiq_full, (u - 1) & 1, wctx)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            mma_bf16(tmem + X_COL, kmajor(k_a, k), kmajor(om_hi, k), id_proj, k > 0);
+            mma_bf16(tmem + X_COL, kmajor(k_a, k), kmajor(om_lo, k), id_proj, true);
+          }
+          mma_commit(pk_full);
+          if (fb == n_fb - 1) mma_commit(k_empty);
+          // P_Q -> X
+          if (!mbar_wait(phik_full, u & 1, wctx)) { ok = false; break; }
+          if (fb == 0 && !mbar_wait(q_full, c & 1, wctx)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            mma_bf16(tmem + X_COL, kmajor(q_a, k), kmajor(om_hi, k), id_proj, k > 0);
+            mma_bf16(tmem + X_COL, kmajor(q_a, k), kmajor(om_lo, k), id_proj, true);
+          }
+          mma_commit(pq_full);
+          if (fb == n_fb - 1) mma_commit(q_empty);
+          // G_fb += phi(K)_fb^T [V | 1]   (after G_fb was copied to G_s,fb)
+          if (!mbar_wait(&gs_full[fb], c & 1, wctx)) { ok = false; break; }
+          if (fb == 0 && !mbar_wait(v_full, c & 1, wctx)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t g_tm = tmem + G_COL + fb * (D + 16);
+#pragma unroll
+          for (int k = 0; k < kBM / 16; ++k) {
+            mma_bf16(g_tm, mnmajor(phik_a, k), mnmajor(v_a, k), id_state, true);
+            mma_bf16(g_tm + D, mnmajor(phik_a, k), ones_desc(ones_a, k), id_ones_mn, true);
+          }
+          mma_commit(&gdone[fb]);
+          // A += phi(Q)_fb phi(K)_fb^T;  O += phi(Q)_fb G_s,fb
+          if (!mbar_wait(phiq_full, u & 1, wctx)) { ok = false; break; }
+          if (fb == 0 && c >= 1 && !mbar_wait(o_free, (c - 1) & 1, wctx)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kFB / 16; ++k) {
+            mma_bf16(tmem + A_COL, kmajor(phiq_a, k), kmajor(phik_a, k), id_a, fb > 0 || k > 0);
+            const uint32_t ga = gs_a + (2 * fb + (k >> 2)) * (D + 16) * 128 + (k & 3) * 32;
+            mma_bf16(tmem + O_COL, kmajor(phiq_a, k), sdesc(ga, 16, 1024), id_og, fb > 0 || k > 0);
+          }
+          mma_commit(phik_free);
+          mma_commit(phiq_free);
+          if (fb == n_fb - 1) mma_commit(a_full);
+        }
+        if (!ok) break;
+        // O += mask(A) [V | 1]   (the masked A tile sits in the phi(K) buffer)
+        if (!mbar_wait(as_full, c & 1, wctx)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kBM / 16; ++k) {
+          mma_bf16(tmem + O_COL, kmajor(phik_a, k), mnmajor(v_a, k), id_av, true);
+          mma_bf16(tmem + O_COL + D, kmajor(phik_a, k), ones_desc(ones_a, k), id_aones, true);
+        }
+        mma_commit(o_full);
+        mma_commit(v_empty);
+      }
+      mma_commit(done_bar);
+      mbar_wait(done_bar, 0, wctx);
+    }
+  } else if (warp == 2) {
+    // squared row norms of K_c and Q_c (double-buffered by chunk parity)
+    for (int c = 0; c < n_chunks; ++c) {
+      float* nk = norms + (c & 1) * 2 * kBM;
+      if (!mbar_wait(k_full, c & 1, wctx)) break;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) nk[lane + 32 * j] = tile_row_sq<D>(sm + C::kK, lane + 32 * j);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&knorm_full[c & 1]);
+        mbar_arrive(k_empty);
+      }
+      if (!mbar_wait(q_full, c & 1, wctx)) break;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) nk[kBM + lane + 32 * j] = tile_row_sq<D>(sm + C::kQ, lane + 32 * j);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&qnorm_full[c & 1]);
+        mbar_arrive(q_empty);
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int wg = (warp - 3) >> 2;
+    const int q = warp & 3;
+    const int t = q * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const float R = prm.key_ref[0];
+    const float W = prm.key_ref[1];
+    const float c1 = prm.scale * kLog2e;
+    const float hs2 = 0.5f * prm.scale * prm.scale;
+    const uint32_t phik_a = smem_addr(sm + C::kPhiK), phiq_a = smem_addr(sm + C::kPhiQ);
+    uint8_t* gs = sm + C::kGs;
+    const int col0 = wg * 64;
+    // G columns of this warpgroup: WG0 0..31 and d..d+15, WG1 32..63
+    const int n_gparts = (wg == 0) ? 3 : 2;
+    auto g_col = [&](int j) { return wg == 0 ? (j == 0 ? 0 : (j == 1 ? 16 : D)) : (j == 0 ? 32 : 48); };
+    auto write_gs = [&](int fb, int n, float x) {
+      const int f = fb * kFB + t, atom = f >> 6, cc = f & 63;
+      const size_t off = ((size_t)atom * (D + 16) + n) * 128 + (((cc >> 3) ^ (n & 7)) << 4) + (cc & 7) * 2;
+      *reinterpret_cast<__nv_bfloat16*>(gs + off) = __float2bfloat16_rn(x);
+    };
+    // G_init = sum of the earlier superchunks' states, in superchunk order
+    for (int fb = 0; fb < n_fb; ++fb) {
+      const float* src = prm.partS + (((size_t)bh * n_fb + fb) * max(prm.n_split, 1)) * (D + 1) * kFB;
+      for (int j = 0; j < n_gparts; ++j) {
+        const int n0 = g_col(j);
+        uint32_t r[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const int n = min(n0 + x, D);
+          float acc = 0.f;
+          for (int p = 0; p < sc; ++p) acc += src[((size_t)p * (D + 1) + n) * kFB + t];
+          r[x] = __float_as_uint(acc);
+          write_gs(fb, n0 + x, acc);
+        }
+        tmem_st16(tmem + lane_off + G_COL + fb * (D + 16) + n0, r);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&gs_full[fb]);
+    }
+    bool ok = true;
+    for (int c = 0; c < n_chunks; ++c) {
+      const int row = (tile0 + c) * kBM + t;
+      const bool valid = row < prm.L;
+      const float* nk = norms + (c & 1) * 2 * kBM;
+      float bias_q = 0.f;
+      for (int fb = 0; fb < n_fb; ++fb) {
+        const int u = c * n_fb + fb;
+        // phi(K)_fb from X
+        if (ok) ok = mbar_wait(pk_full, u & 1, wctx);
+        if (ok && fb == 0) ok = mbar_wait(&knorm_full[c & 1], (c >> 1) & 1, wctx);
+        if (ok && u >= 1) ok = mbar_wait(phik_free, (u - 1) & 1, wctx);
+        tc_fence_after();
+        if (ok) {
+          const float bias_k = (hs2 * nk[t] + R) * kLog2e;
+          uint32_t p0[32], p1[32];
+          tmem_ld32(tmem + lane_off + X_COL + col0, p0);
+          tmem_ld32(tmem + lane_off + X_COL + col0 + 32, p1);
+          tmem_ld_wait();
+          write_row32<0>(phik_a, t, col0, p0, c1, bias_k, valid);
+          write_row32<0>(phik_a, t, col0 + 32, p1, c1, bias_k, valid);
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(phik_full);
+        // G_s,fb <- bf16(G_fb) of the previous chunk
+        if (c >= 1) {
+          // G_fb of the previous chunk is final; with one feature block the
+          // previous reader of G_s,fb (O MMA) is waited for here, with two it
+          // was waited for by the phi(Q) step of the block before
+          if (ok) ok = mbar_wait(&gdone[fb], (c - 1) & 1, wctx);
+          if (ok && n_fb == 1) ok = mbar_wait(phiq_free, (u - 1) & 1, wctx);
+          tc_fence_after();
+          if (ok) {
+            for (int j = 0; j < n_gparts; ++j) {
+              const int n0 = g_col(j);
+              uint32_t r[16];
+              tmem_ld16(tmem + lane_off + G_COL + fb * (D + 16) + n0, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int x = 0; x < 16; ++x) write_gs(fb, n0 + x, __uint_as_float(r[x]));
+            }
+          }
+          tc_fence_before();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&gs_full[fb]);
+        }
+        // phi(Q)_fb from X
+        if (ok) ok = mbar_wait(pq_full, u & 1, wctx);
+        tc_fence_after();
+        if (fb == 0) {
+          if (c >= 1 && threadIdx.x == 96) bulk_wait_read0();   // the staging tile (phi(Q) buffer) is free
+          float mx = -INFINITY;
+          if (ok) {
+            uint32_t p0[32], p1[32];
+            tmem_ld32(tmem + lane_off + X_COL + col0, p0);
+            tmem_ld32(tmem + lane_off + X_COL + col0 + 32, p1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) mx = fmaxf(mx, fmaxf(__uint_as_float(p0[x]), __uint_as_float(p1[x])));
+          }
+          float* sx = smax + (c & 1) * 2 * kBM;
+          sx[wg * kBM + t] = mx;
+          named_bar(1, kEpiThreads);
+          mx = fmaxf(sx[t], sx[kBM + t]);
+          bias_q = mx * c1;
+          if (n_fb > 1) {
+            if (ok) ok = mbar_wait(&qnorm_full[c & 1], (c >> 1) & 1, wctx);
+            const float bound = prm.scale * W * sqrtf(nk[kBM + t]) - 20.0f;
+            bias_q = fmaxf(bias_q, bound * kLog2e);
+          }
+        }
+        if (ok && u >= 1) ok = mbar_wait(phiq_free, (u - 1) & 1, wctx);
+        if (ok) {
+          uint32_t p0[32], p1[32];
+          tmem_ld32(tmem + lane_off + X_COL + col0, p0);
+          tmem_ld32(tmem + lane_off + X_COL + col0 + 32, p1);
+          tmem_ld_wait();
+          write_row32<0>(phiq_a, t, col0, p0, c1, bias_q, true);
+          write_row32<0>(phiq_a, t, col0 + 32, p1, c1, bias_q, true);
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(phiq_full);
+      }
+      // masked A -> bf16 (phi(K) buffer)
+      if (ok) ok = mbar_wait(a_full, c & 1, wctx);
+      tc_fence_after();
+      if (ok) {
+        uint32_t p0[32], p1[32];
+        tmem_ld32(tmem + lane_off + A_COL + col0, p0);
+        tmem_ld32(tmem + lane_off + A_COL + col0 + 32, p1);
+        tmem_ld_wait();
+        write_row32<1>(phik_a, t, col0, p0, 0.f, 0.f, true);
+        write_row32<1>(phik_a, t, col0 + 32, p1, 0.f, 0.f, true);
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(as_full);
+      // O / normaliser -> staging (phi(Q) buffer) -> TMA store
+      const bool have = ok && mbar_wait(o_full, c & 1, wctx);
+      ok = ok && have;
+      tc_fence_after();
+      uint32_t v[32], z[16];
+      if (have) {
+        tmem_ld32(tmem + lane_off + O_COL + wg * 32, v);
+        tmem_ld16(tmem + lane_off + O_COL + D, z);
+        tmem_ld_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
+      const float den = have ? __uint_as_float(z[0]) : 1.f;
+      if (have && valid && (!(den > 0.f) || !isfinite(den))) report_status(prm.status, FAVOR_ERR_NONFINITE);
+      const float inv = 1.0f / den;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int chunk = wg * 4 + cc;
+        const float* x = reinterpret_cast<const float*>(v) + cc * 8;
+        st_shared_v4(phiq_a + t * 128 + ((chunk ^ (t & 7)) << 4), pack_bf16(x[0] * inv, x[1] * inv),
+                     pack_bf16(x[2] * inv, x[3] * inv), pack_bf16(x[4] * inv, x[5] * inv),
+                     pack_bf16(x[6] * inv, x[7] * inv));
+      }
+      fence_proxy_async_smem();
+      named_bar(1, kEpiThreads);
+      if (threadIdx.x == 96 && have && !*abort_flag) {
+        tma_store_3d(&mapO, 0, (tile0 + c) * kBM, bh, sm + C::kPhiQ);
+        bulk_commit();
+      }
+    }
+    if (threadIdx.x == 96) bulk_wait0();
     mbar_wait(done_bar, 0, wctx);
   }
   tc_fence_before();
@@ -653,6 +1154,7 @@ bool make_map(CUtensorMap* map, const void* base, const Shape& s) {
 template <int D>
 cudaError_t launch_state(const void* K, const void* V, const Shape& s, const TcPlan& p, float scale, char* ws,
                          int32_t* status, cudaStream_t stream) {
+  if (p.n_split < 1) return cudaSuccess;
   CUtensorMap mk, mv;
   if (!make_map(&mk, K, s) || !make_map(&mv, V, s)) return cudaErrorInvalidValue;
   StateParams prm{};
@@ -666,12 +1168,13 @@ cudaError_t launch_state(const void* K, const void* V, const Shape& s, const TcP
   prm.m = s.m;
   prm.n_split = p.n_split;
   prm.tiles_per_split = p.tiles_per_split;
+  prm.merge = p.causal ? 0 : 1;
   prm.scale = scale;
   const size_t smem = StateCfg<D>::kSmem;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(state_kernel<D>), smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_split, p.n_fb, s.BH());
-  state_kernel<D><<<grid, kThreads, smem, stream>>>(mk, mv, prm);
+  state_kernel<D><<<grid, kStateThreads, smem, stream>>>(mk, mv, prm);
   return cudaGetLastError();
 }
 
@@ -692,43 +1195,71 @@ cudaError_t launch_output(const void* Q, void* O, const Shape& s, const TcPlan& 
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(output_kernel<D>), smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.out_ctas, s.BH());
-  output_kernel<D><<<grid, kThreads, smem, stream>>>(mq, mo, prm);
+  output_kernel<D><<<grid, kOutThreads, smem, stream>>>(mq, mo, prm);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_causal(const void* Q, const void* K, const void* V, void* O, const Shape& s, const TcPlan& p,
+                          float scale, char* ws, int32_t* status, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv, mo;
+  if (!make_map(&mq, Q, s) || !make_map(&mk, K, s) || !make_map(&mv, V, s) || !make_map(&mo, O, s))
+    return cudaErrorInvalidValue;
+  CausalParams prm{};
+  prm.key_ref = reinterpret_cast<const float*>(ws);
+  prm.omega_img = reinterpret_cast<const uint8_t*>(ws + p.off_omega_img);
+  prm.partS = reinterpret_cast<const float*>(ws + p.off_partS);
+  prm.status = status;
+  prm.L = s.L;
+  prm.m = s.m;
+  prm.n_split = p.n_split;
+  prm.tiles_per_sc = p.out_tiles_per_cta;
+  prm.scale = scale;
+  const size_t smem = CausalCfg<D>::kSmem;
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(causal_kernel<D>), smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.out_ctas, s.BH());
+  causal_kernel<D><<<grid, kCausalThreads, smem, stream>>>(mq, mk, mv, mo, prm);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool tc_supported(bool causal, int d, int m, bool bf16) {
-  if (!bf16 || causal) return false;
+  (void)causal;
+  if (!bf16) return false;
   return d == 64 && (m == 128 || m == 256);
 }
 
-size_t tc_workspace_bytes(bool causal, const Shape& s) {
-  (void)causal;
-  return tc_plan(s).bytes;
-}
+size_t tc_workspace_bytes(bool causal, const Shape& s) { return tc_plan(causal, s).bytes; }
 
 cudaError_t tc_state(bool causal, const void* K, const void* V, const float* omega, float scale, const Shape& s,
                      void* ws, int32_t* status, cudaStream_t stream) {
-  if (causal) return cudaErrorNotSupported;
-  const TcPlan p = tc_plan(s);
+  const TcPlan p = tc_plan(causal, s);
   char* w = static_cast<char*>(ws);
   cudaError_t e = launch_prep(omega, s.m, s.d, reinterpret_cast<float*>(w),
                               reinterpret_cast<uint8_t*>(w + p.off_omega_img), stream);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(w + p.off_counters, 0, (size_t)s.BH() * p.n_fb * sizeof(uint32_t), stream);
-  if (e != cudaSuccess) return e;
+  if (!causal) {
+    e = cudaMemsetAsync(w + p.off_counters, 0, (size_t)s.BH() * p.n_fb * sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return e;
+  }
   return launch_state<64>(K, V, s, p, scale, w, status, stream);
 }
 
 cudaError_t tc_output(bool causal, const void* Q, const void* K, const void* V, void* O, const float* omega,
                       float scale, const Shape& s, void* ws, int32_t* status, cudaStream_t stream) {
-  (void)K;
-  (void)V;
   (void)omega;
-  if (causal) return cudaErrorNotSupported;
-  const TcPlan p = tc_plan(s);
+  const TcPlan p = tc_plan(causal, s);
+  if (causal) return launch_causal<64>(Q, K, V, O, s, p, scale, static_cast<char*>(ws), status, stream);
   return launch_output<64>(Q, O, s, p, scale, static_cast<char*>(ws), status, stream);
 }
 
 }  // namespace favor
+
+#ifdef FAVOR_WAIT_DIAG
+// Diagnostic builds only: copies the per-warp records of timed-out waits.
+extern "C" int favor_debug_wait_diag(int* out) {
+  return (int)cudaMemcpyFromSymbol(out, favor::tc::g_favor_wait_diag, sizeof(int) * 256 * 4);
+}
+#endif

@@ -50,6 +50,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+#ifdef FAVOR_WAIT_DIAG
+// Diagnostic builds only: the first wait of each warp that ran out records
+// (shared-memory offset of the barrier >> 3, parity, warp, block).
+__device__ int g_favor_wait_diag[256][4];
+__device__ __forceinline__ void favor_wait_diag_record(uint32_t bar, uint32_t parity) {
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0 && blockIdx.x + blockIdx.y + blockIdx.z == 0 && w < 256 &&
+      atomicCAS(&g_favor_wait_diag[w][3], 0, 1) == 0) {
+    g_favor_wait_diag[w][0] = (int)(bar >> 3);
+    g_favor_wait_diag[w][1] = (int)parity;
+    g_favor_wait_diag[w][2] = w;
+  }
+}
+#endif
+
 // Shared abort flag + error status: every wait in a kernel is bounded; the
 // first wait that runs out raises the flag (other waits then return at once)
 // and records FAVOR_ERR_TIMEOUT.  Returns true when the phase completed.
@@ -68,6 +83,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     if (global_timer() - t0 > kWaitLimitNs) {
       *ctx.abort_flag = 1;
       report_status(ctx.status, FAVOR_ERR_TIMEOUT);
+#ifdef FAVOR_WAIT_DIAG
+      favor_wait_diag_record(a, parity);
+#endif
       return false;
     }
   }
@@ -166,6 +184,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 32 lanes x 16 consecutive 32-bit columns from registers (same lane rule as loads)
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---- descriptors ------------------------------------------------------------
 // Shared-memory matrix descriptor (sm_100 family): start address, leading

@@ -135,6 +135,25 @@ def test_workload_full_size_sampled_rows(cuda_lib, name):
     assert err < TOL[w.torch_dtype], (name, err)
 
 
+@pytest.mark.parametrize("m", [128, 256])
+def test_causal_multichunk_walk(cuda_lib, m):
+    # B*H = 128 heads of 512 tokens: one superchunk per head walks 4 chunks
+    # of 128 (G carried across chunks); sampled rows of sampled heads
+    w = wl.Workload("walk", "causal", "bf16", 8, 16, 512, 64, m, "normal")
+    Q, K, V = (t.cuda() for t in wl.make_qkv(w, seed=m))
+    om = cuda_lib.new_omega(m, m, w.d)
+    st = _status()
+    O = _run(cuda_lib, True, Q, K, V, om, w.qk_scale, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    BH = w.B * w.H
+    picks = [(h, t) for h in (0, 37, 127) for t in (0, 127, 128, 300, 511)]
+    q3, k3, v3, o3 = (X.view(BH, w.L, w.d) for X in (Q, K, V, O))
+    ref = orc.favor_rows(to_np(q3), to_np(k3), to_np(v3), to_np(om), w.qk_scale, picks, True)
+    got = np.stack([to_np(o3[h, t]) for h, t in picks])
+    assert orc.rowwise_rel_err(got, ref) < TOL[torch.bfloat16]
+
+
 def test_redrawn_omega_per_call(cuda_lib):
     # the 12288-token pixel workload draws a fresh Omega (seed base + i) each call
     w = wl.get("causal-bf16-B2H8L12288-d64-m256").with_(B=1, H=2, L=1024)
