@@ -170,6 +170,38 @@ favor_status favor_causal_output(const void* Q, const void* K, const void* V, vo
                                  int32_t* dev_status, void* stream);
 
 /*
+ * favor_fwd_bidir_static — favor_fwd_bidir without a caller workspace.  This
+ * entry point has no counterpart in the paper; it exists for callers that
+ * cannot allocate device memory where they call the attention (code inside a
+ * host framework that owns all device memory and forbids allocation on its
+ * request path, or latency-critical code that must not take the allocation
+ * path, which can synchronise the device).
+ *
+ * The scratch memory is one file-scope device array of
+ * favor_static_scratch_bytes() bytes (16 MiB) that every GPU which loads this
+ * library holds until the process exits.  The first call on each device
+ * resolves the array's device address (cudaGetSymbolAddress) for that device,
+ * so make that first call with the device current and outside any stream
+ * capture.  No call allocates or frees memory.
+ *
+ * All calls share the one array and leave their intermediate results in it;
+ * the kernels clear what must start at zero.  Calls whose execution overlaps
+ * on the GPU (different streams, or different host threads on one device)
+ * race on the array: order them on one stream.
+ *
+ * Arguments and results are those of favor_fwd_bidir.  Shapes whose scratch
+ * need (favor_workspace_bytes(0, ...)) exceeds the array return
+ * FAVOR_ERR_UNSUPPORTED without launching anything.
+ */
+favor_status favor_fwd_bidir_static(const void* Q, const void* K, const void* V, void* O,
+                                    int B, int H, int L, int d,
+                                    const float* omega, int m, favor_dtype dt, float qk_scale,
+                                    int32_t* dev_status, void* stream);
+
+/* Size in bytes of the fixed scratch array used by favor_fwd_bidir_static. */
+size_t favor_static_scratch_bytes(void);
+
+/*
  * favor_path_name — which kernel family a call with these arguments uses:
  * "tcgen05" (bf16 tensor-core kernels), "simt" (CUDA-core fp32 kernels) or
  * "unsupported".  Static string, never NULL.

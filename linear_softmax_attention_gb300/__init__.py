@@ -17,7 +17,7 @@ import torch
 __all__ = [
     "load", "lib_path", "FavorError", "F32", "BF16", "api_version", "path_name", "build_orf", "new_omega",
     "workspace_bytes", "new_workspace", "fwd_bidir", "fwd_causal", "bidir_state", "bidir_output",
-    "causal_state", "causal_output", "status_string", "ENTRY_POINTS",
+    "causal_state", "causal_output", "status_string", "ENTRY_POINTS", "fwd_bidir_static", "static_scratch_bytes",
 ]
 
 F32 = 0
@@ -64,6 +64,10 @@ def load():
         fn = getattr(lib, name)
         fn.restype = c_int
         fn.argtypes = fwd_args
+    lib.favor_fwd_bidir_static.restype = c_int
+    lib.favor_fwd_bidir_static.argtypes = [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_vp, c_int, c_int,
+                                           c_float, c_vp, c_vp]
+    lib.favor_static_scratch_bytes.restype = c_size
     _lib = lib
     return lib
 
@@ -166,3 +170,23 @@ def causal_state(K, V, omega, qk_scale, workspace, dev_status=None, stream=None)
 
 def causal_output(Q, K, V, omega, qk_scale, workspace, O=None, dev_status=None, stream=None):
     return _call("favor_causal_output", Q, K, V, _out_like(Q, O), omega, qk_scale, workspace, dev_status, stream)
+
+
+def static_scratch_bytes() -> int:
+    return load().favor_static_scratch_bytes()
+
+
+def fwd_bidir_static(Q, K, V, omega, qk_scale, O=None, dev_status=None, stream=None):
+    """Bidirectional FAVOR+ with the library's fixed device scratch (no
+    workspace argument, nothing allocated by the library)."""
+    O = torch.empty_like(Q) if O is None else O
+    B, H, L, d = Q.shape
+    for t in (Q, K, V, O):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != Q.dtype or tuple(t.shape) != (B, H, L, d):
+            raise FavorError("fwd_bidir_static: Q/K/V/O must be contiguous CUDA tensors of one dtype and shape")
+    code = load().favor_fwd_bidir_static(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), B, H, L, d,
+                                         omega.data_ptr(), omega.shape[0], _DT[Q.dtype], float(qk_scale),
+                                         dev_status.data_ptr() if dev_status is not None else None,
+                                         _stream_handle(stream))
+    _check(code, "favor_fwd_bidir_static")
+    return O

@@ -92,6 +92,14 @@ favor_status run(bool causal, int stage, const void* Q, const void* K, const voi
 
 }  // namespace
 
+namespace favor {
+favor_status run_call(bool causal, int stage, const void* Q, const void* K, const void* V, void* O, int B, int H,
+                      int L, int d, const float* omega, int m, favor_dtype dt, float qk_scale, void* workspace,
+                      size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return run(causal, stage, Q, K, V, O, B, H, L, d, omega, m, dt, qk_scale, workspace, ws_bytes, dev_status, stream);
+}
+}  // namespace favor
+
 extern "C" {
 
 int favor_api_version(void) { return kVersion; }

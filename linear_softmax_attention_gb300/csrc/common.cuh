@@ -86,6 +86,12 @@ cudaError_t simt_causal_output(const void* Q, const void* K, const void* V, void
                                const float* omega, float scale, const Shape& s, bool bf16, void* ws,
                                int32_t* st, cudaStream_t stream);
 
+// The checked, dispatched body of every forward entry point (stage: 1 state,
+// 2 output, 3 both).
+favor_status run_call(bool causal, int stage, const void* Q, const void* K, const void* V, void* O, int B, int H,
+                      int L, int d, const float* omega, int m, favor_dtype dt, float qk_scale, void* workspace,
+                      size_t ws_bytes, int32_t* dev_status, void* stream);
+
 // Raises a kernel's dynamic shared-memory limit once per device and size, so
 // that calls made later (including under CUDA graph capture) issue no
 // attribute call.
