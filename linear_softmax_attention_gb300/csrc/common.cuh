@@ -22,6 +22,21 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
   return __float2bfloat16_rn(x);
 }
 
+// ---- key reference ------------------------------------------------------------
+// The workspace header holds, for each block of 8 rows of Omega, the largest
+// squared row norm (written by the prep kernel).  R = max_i |w_i|^2 / 2 - 40
+// bounds every key-feature exponent from above by 40 (prep.cu explains why);
+// W = max_i |w_i|.
+constexpr float kKeyHeadroom = 40.0f;
+constexpr int kPrepRows = 8;
+__device__ __forceinline__ void key_reference(const float* hdr, int m, float* R, float* W) {
+  const int n = (m + kPrepRows - 1) / kPrepRows;
+  float w2 = hdr[0];
+  for (int i = 1; i < n; ++i) w2 = fmaxf(w2, hdr[i]);
+  *R = 0.5f * w2 - kKeyHeadroom;
+  *W = sqrtf(w2);
+}
+
 // ---- device-side status -----------------------------------------------------
 // First non-zero code wins; later errors do not overwrite it.
 __device__ __forceinline__ void report_status(int32_t* status, int code) {
@@ -63,8 +78,8 @@ struct Shape {
 };
 
 // Every workspace starts with a 256-byte header written by launch_prep at the
-// start of each state stage: float key reference R at offset 0 and the
-// largest row norm W of Omega at offset 4.
+// start of each state stage: per block of 8 rows of Omega, the largest
+// squared row norm (read back through key_reference).
 constexpr size_t kWsHeader = 256;
 
 // Workspace plan of the CUDA-core path.
@@ -97,7 +112,7 @@ favor_status run_call(bool causal, int stage, const void* Q, const void* K, cons
 // attribute call.
 cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
 
-// Key reference R and W (and optionally the bf16 Omega images) into the workspace.
+// Row-norm maxima (and optionally the bf16 Omega images) into the workspace.
 cudaError_t launch_prep(const float* omega, int m, int d, float* key_ref, uint8_t* image, cudaStream_t stream);
 
 cudaError_t launch_build_orf(uint64_t seed, int m, int d, int orthogonal, float* omega,

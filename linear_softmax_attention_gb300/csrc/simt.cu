@@ -8,7 +8,7 @@
 //
 // Stabilisers (exact rewrites, not approximations):
 //  * key side: phi(k) is evaluated as exp(l - R) with one constant R for the
-//    whole call, R = max_i |w_i|^2 / 2 - 40 (see key_reference in prep.cu);
+//    whole call, R = max_i |w_i|^2 / 2 - 40 (see prep.cu and key_reference);
 //    since l = |w|^2/2 - |s k - w|^2/2 <= max_i |w_i|^2/2, every key feature
 //    is <= e^40 and the shared factor exp(-R) cancels between numerator and
 //    normaliser;
@@ -81,7 +81,8 @@ __global__ void __launch_bounds__(kThreads) state_partial_kernel(
   const T* Kh = K + (size_t)bh * L * d;
   const T* Vh = V + (size_t)bh * L * d;
   const float hs2 = 0.5f * scale * scale;
-  const float R = *key_ref;
+  float R, W_unused;
+  key_reference(key_ref, m, &R, &W_unused);
   const int f_own = threadIdx.x % kFB;
   const int t_base = threadIdx.x / kFB;   // 0..3
 
@@ -265,7 +266,8 @@ __global__ void __launch_bounds__(kThreads) causal_output_kernel(
   float* kn = A + kTT * (kTT + 1);    // [kTT]
   float* rowmax = kn + kTT;           // [kTT]
 
-  const float Rk = *key_ref;
+  float Rk, W_unused;
+  key_reference(key_ref, m, &Rk, &W_unused);
   const size_t per = (size_t)m * ld;
   float* G = Gws + ((size_t)bh * n_sc + sc) * per;
   for (int e = threadIdx.x; e < m * ld; e += kThreads) {

@@ -362,7 +362,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     const int q = warp & 3;
     const int t = q * 32 + lane;                   // token row of P, feature row of S~
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const float R = prm.key_ref[0];
+    float R, W_unused;
+    key_reference(prm.key_ref, prm.m, &R, &W_unused);
     const float c1 = prm.scale * kLog2e;
     const float hs2 = 0.5f * prm.scale * prm.scale;
     const int col0 = wg * 64;
@@ -701,7 +702,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
 // phi(q) is at most e^20.
 // ---------------------------------------------------------------------------
 struct CausalParams {
-  const float* key_ref;   // [0] = R, [1] = W
+  const float* key_ref;   // row-norm maxima (key_reference)
   const uint8_t* omega_img;
   const float* partS;     // [BH][n_fb][n_split][d+1][128]
   int32_t* status;
@@ -847,21 +848,30 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
       const uint32_t gs_a = smem_addr(sm + C::kGs), k_a = smem_addr(sm + C::kK), q_a = smem_addr(sm + C::kQ);
       const uint32_t v_a = smem_addr(sm + C::kV);
       bool ok = mbar_wait(setup_bar, 0, wctx);
+      // P_K(c, fb) -> X.  X is free once the phi(Q) block before it was read;
+      // the first block of chunk c + 1 is issued before chunk c's masked tile
+      // is awaited, so that projection overlaps the tail of chunk c.
+      auto issue_pk = [&](int c, int fb) -> bool {
+        const int u = c * n_fb + fb;
+        if (fb == 0 && !mbar_wait(k_full, c & 1, wctx)) return false;
+        if (u >= 1 && !mbar_wait(phiq_full, (u - 1) & 1, wctx)) return false;
+        tc_fence_after();
+        const uint32_t om_hi = om_a + fb * kFB * D * 2, om_lo = om_a + (m + fb * kFB) * D * 2;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          mma_bf16(tmem + X_COL, kmajor(k_a, k), kmajor(om_hi, k), id_proj, k > 0);
+          mma_bf16(tmem + X_COL, kmajor(k_a, k), kmajor(om_lo, k), id_proj, true);
+        }
+        mma_commit(pk_full);
+        if (fb == n_fb - 1) mma_commit(k_empty);
+        return true;
+      };
+      if (ok && n_chunks > 0) ok = issue_pk(0, 0);
       for (int c = 0; ok && c < n_chunks; ++c) {
         for (int fb = 0; ok && fb < n_fb; ++fb) {
           const int u = c * n_fb + fb;
           const uint32_t om_hi = om_a + fb * kFB * D * 2, om_lo = om_a + (m + fb * kFB) * D * 2;
-          // P_K -> X  (X is free once the previous phi(Q) block has been read)
-          if (fb == 0 && !mbar_wait(k_full, c & 1, wctx)) { ok = false; break; }
-          if (u >= 1 && !mbar_wait(phiq_full, (u - 1) & 1, wctx)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            mma_bf16(tmem + X_COL, kmajor(k_a, k), kmajor(om_hi, k), id_proj, k > 0);
-            mma_bf16(tmem + X_COL, kmajor(k_a, k), kmajor(om_lo, k), id_proj, true);
-          }
-          mma_commit(pk_full);
-          if (fb == n_fb - 1) mma_commit(k_empty);
+          if (fb > 0 && !issue_pk(c, fb)) { ok = false; break; }
           // P_Q -> X
           if (!mbar_wait(phik_full, u & 1, wctx)) { ok = false; break; }
           if (fb == 0 && !mbar_wait(q_full, c & 1, wctx)) { ok = false; break; }
@@ -899,6 +909,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
           if (fb == n_fb - 1) mma_commit(a_full);
         }
         if (!ok) break;
+        if (c + 1 < n_chunks && !issue_pk(c + 1, 0)) { ok = false; break; }
         // O += mask(A) [V | 1]   (the masked A tile sits in the phi(K) buffer)
         if (!mbar_wait(as_full, c & 1, wctx)) { ok = false; break; }
         tc_fence_after();
@@ -940,8 +951,8 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
     const int q = warp & 3;
     const int t = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const float R = prm.key_ref[0];
-    const float W = prm.key_ref[1];
+    float R, W;
+    key_reference(prm.key_ref, prm.m, &R, &W);
     const float c1 = prm.scale * kLog2e;
     const float hs2 = 0.5f * prm.scale * prm.scale;
     const uint32_t phik_a = smem_addr(sm + C::kPhiK), phiq_a = smem_addr(sm + C::kPhiQ);
