@@ -446,10 +446,14 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
 }
 
 // ---------------------------------------------------------------------------
-// bidirectional output kernel: CTA = a run of 128-token tiles of one head;
-// m <= 256 (all projections of a tile fit in tensor memory: exact row max)
+// bidirectional output kernel: CTA = a run of 128-token tiles of one head.
+// Query row reference: s |q| max_i |w_i| - 20, the largest exponent s w_i.q
+// can take less 20 ("From Performer to Linear Attention", §Simple Derivation:
+// any per-query constant cancels), so every phi(q) <= e^20 and no pass over
+// the projections is needed to find a maximum.
 // ---------------------------------------------------------------------------
 struct OutParams {
+  const float* key_ref;    // row-norm maxima (key_reference)
   const uint8_t* omega_img;
   const uint8_t* state_img;
   int32_t* status;
@@ -457,7 +461,8 @@ struct OutParams {
   float scale;
 };
 
-constexpr int kOutThreads = 320;   // warps 0 TMA, 1 MMA, 2-9 epilogue
+constexpr int kOutThreads = 352;   // warps 0 TMA, 1 MMA, 2 norms, 3-10 epilogue
+constexpr float kQueryHeadroom = 20.0f;
 
 template <int D>
 struct OutCfg {
@@ -470,8 +475,8 @@ struct OutCfg {
   static constexpr int kQ = kState + kStateMax;
   static constexpr int kPhi = kQ + NSQ * kTileBytes;
   static constexpr int kOut = kPhi + 4 * kAtom;         // 128 x 256 bf16
-  static constexpr int kSmax = kOut + kTileBytes;       // [2 tiles][2 groups][128] floats
-  static constexpr int kBars = kSmax + 2 * 2 * kBM * 4;
+  static constexpr int kNorm = kOut + kTileBytes;       // [NSQ][128] squared query norms
+  static constexpr int kBars = kNorm + NSQ * kBM * 4;
   static constexpr int kSmem = kBars + 512 + 1024;
 };
 
@@ -483,19 +488,20 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBars);
-  uint64_t* q_full = bars;               // [NSQ]
-  uint64_t* q_empty = q_full + C::NSQ;   // [NSQ]
-  uint64_t* p_full = q_empty + C::NSQ;
+  uint64_t* q_full = bars;                  // [NSQ]
+  uint64_t* q_empty = q_full + C::NSQ;      // [NSQ] MMA commit + norm warp
+  uint64_t* qnorm_full = q_empty + C::NSQ;  // [NSQ]
+  uint64_t* p_full = qnorm_full + C::NSQ;
   uint64_t* p_free = p_full + 1;
   uint64_t* phi_full = p_free + 1;
   uint64_t* phi_free = phi_full + 1;
-  uint64_t* o_full = phi_free + 1;       // [2]
-  uint64_t* o_free = o_full + 2;         // [2]
+  uint64_t* o_full = phi_free + 1;          // [2]
+  uint64_t* o_free = o_full + 2;            // [2]
   uint64_t* setup_bar = o_free + 2;
   uint64_t* done_bar = setup_bar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* smax = reinterpret_cast<float*>(sm + C::kSmax);
+  float* qnorm = reinterpret_cast<float*>(sm + C::kNorm);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
@@ -510,7 +516,8 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NSQ; ++i) {
       mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 1);
+      mbar_init(&q_empty[i], 2);
+      mbar_init(&qnorm_full[i], 1);
     }
     mbar_init(p_full, 1);
     mbar_init(p_free, kEpiWarps);
@@ -593,11 +600,27 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
       mma_commit(done_bar);
       mbar_wait(done_bar, 0, wctx);
     }
+  } else if (warp == 2) {
+    // squared norms of the Q rows of each stage
+    for (int i = 0; i < n_tiles; ++i) {
+      const int st = i % C::NSQ;
+      if (!mbar_wait(&q_full[st], (i / C::NSQ) & 1, wctx)) break;
+      const uint8_t* qt = sm + C::kQ + st * C::kTileBytes;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) qnorm[st * kBM + lane + 32 * j] = tile_row_sq<D>(qt, lane + 32 * j);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&qnorm_full[st]);
+        mbar_arrive(&q_empty[st]);
+      }
+    }
   } else {
-    const int wg = (warp - 2) >> 2;
+    const int wg = (warp - 3) >> 2;
     const int q = warp & 3;
     const int t = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    float R_unused, W;
+    key_reference(prm.key_ref, m, &R_unused, &W);
     const float c1 = prm.scale * kLog2e;
     const uint32_t phi_a = smem_addr(sm + C::kPhi);
     const uint32_t out_a = smem_addr(sm + C::kOut);
@@ -621,7 +644,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
       const int row = (tile0 + j) * kBM + t;
       if (have && row < prm.L && (!(den > 0.f) || !isfinite(den))) report_status(prm.status, FAVOR_ERR_NONFINITE);
       const float inv = 1.0f / den;
-      if (threadIdx.x == 64 && j > 0) bulk_wait_read0();   // previous store has left the staging tile
+      if (threadIdx.x == 96 && j > 0) bulk_wait_read0();   // previous store has left the staging tile
       named_bar(1, kEpiThreads);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -633,40 +656,30 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
       }
       fence_proxy_async_smem();
       named_bar(1, kEpiThreads);
-      if (threadIdx.x == 64 && have && !*abort_flag) {
+      if (threadIdx.x == 96 && have && !*abort_flag) {
         tma_store_3d(&mapO, 0, (tile0 + j) * kBM, bh, sm + C::kOut);
         bulk_commit();
       }
     };
     for (int i = 0; i < n_tiles; ++i) {
+      const int st = i % C::NSQ;
       if (ok) ok = mbar_wait(p_full, i & 1, wctx);
+      if (ok) ok = mbar_wait(&qnorm_full[st], (i / C::NSQ) & 1, wctx);
       tc_fence_after();
-      // pass 1: exact row maximum over all m features (both warpgroups)
-      float mx = -INFINITY;
-      if (ok) {
-        for (int cb = 0; cb < half / 32; cb += 2) {
-          uint32_t p0[32], p1[32];
-          tmem_ld32(tmem + lane_off + f_lo + cb * 32, p0);
-          tmem_ld32(tmem + lane_off + f_lo + cb * 32 + 32, p1);
-          tmem_ld_wait();
-#pragma unroll
-          for (int x = 0; x < 32; ++x) mx = fmaxf(mx, fmaxf(__uint_as_float(p0[x]), __uint_as_float(p1[x])));
-        }
-      }
-      float* sx = smax + (i & 1) * 2 * kBM;
-      sx[wg * kBM + t] = mx;
-      named_bar(2, kEpiThreads);
-      mx = fmaxf(sx[t], sx[kBM + t]);
-      const float bias = mx * c1;
+      const float bias = (prm.scale * W * sqrtf(qnorm[st * kBM + t]) - kQueryHeadroom) * kLog2e;
       if (ok && i >= 1) ok = mbar_wait(phi_free, (i - 1) & 1, wctx);
       if (ok) {
-        for (int cb = 0; cb < half / 32; cb += 2) {
-          uint32_t p0[32], p1[32];
+        for (int cb = 0; cb < half / 32; cb += 4) {
+          uint32_t p0[32], p1[32], p2[32], p3[32];
           tmem_ld32(tmem + lane_off + f_lo + cb * 32, p0);
           tmem_ld32(tmem + lane_off + f_lo + cb * 32 + 32, p1);
+          tmem_ld32(tmem + lane_off + f_lo + cb * 32 + 64, p2);
+          tmem_ld32(tmem + lane_off + f_lo + cb * 32 + 96, p3);
           tmem_ld_wait();
           write_row32<0>(phi_a, t, f_lo + cb * 32, p0, c1, bias, true);
           write_row32<0>(phi_a, t, f_lo + cb * 32 + 32, p1, c1, bias, true);
+          write_row32<0>(phi_a, t, f_lo + cb * 32 + 64, p2, c1, bias, true);
+          write_row32<0>(phi_a, t, f_lo + cb * 32 + 96, p3, c1, bias, true);
         }
       }
       tc_fence_before();
@@ -679,7 +692,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
       if (i >= 1) store_out(i - 1);
     }
     if (n_tiles >= 1) store_out(n_tiles - 1);
-    if (threadIdx.x == 64) bulk_wait0();
+    if (threadIdx.x == 96) bulk_wait0();
     mbar_wait(done_bar, 0, wctx);
   }
   tc_fence_before();
@@ -696,8 +709,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
 //   G_fb += phi(K_c)_fb^T [V_c | 1];  A += phi(Q_c)_fb phi(K_c)_fb^T;
 //   O += phi(Q_c)_fb G_s,fb                                       (tensor cores)
 // then A's upper triangle is zeroed (diagonal kept), O += A [V_c | 1], and
-// O is divided by its normaliser column.  The query row reference is the
-// exact maximum over the first feature block, raised if needed to
+// O is divided by its normaliser column.  The query row reference is
 // s |q| max_i |w_i| - 20 (the largest possible exponent less 20), so every
 // phi(q) is at most e^20.
 // ---------------------------------------------------------------------------
@@ -719,13 +731,16 @@ struct CausalCfg {
   static constexpr int kOnes = kOmega + 2 * 256 * D * 2;
   static constexpr int kPhiK = kOnes + kOnesBytes;                  // also the masked A tile
   static constexpr int kPhiQ = kPhiK + 2 * kAtom;                   // also the output staging tile
-  static constexpr int kGs = kPhiQ + 2 * kAtom;                     // bf16 G, [m/64][d+16][128 B]
-  static constexpr int kK = kGs + 256 * (D + 16) * 2;
+  // bf16 copy of G: V columns as an MN-major tile [feature][64 columns] (GsA),
+  // the normaliser column as a K-major block [m/64][16 rows][128 B] (GsB,
+  // rows 1..15 zero)
+  static constexpr int kGs = kPhiQ + 2 * kAtom;
+  static constexpr int kGsB = kGs + 256 * 128;
+  static constexpr int kK = kGsB + 4 * 16 * 128;
   static constexpr int kQ = kK + kTileBytes;
   static constexpr int kV = kQ + kTileBytes;
   static constexpr int kNorm = kV + kTileBytes;                     // [2 chunks][K, Q][128] floats
-  static constexpr int kSmax = kNorm + 2 * 2 * kBM * 4;             // [2 chunks][2 groups][128]
-  static constexpr int kBars = kSmax + 2 * 2 * kBM * 4;
+  static constexpr int kBars = kNorm + 2 * 2 * kBM * 4;
   static constexpr int kSmem = kBars + 512 + 1024;
 };
 
@@ -752,7 +767,6 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
   if (threadIdx.x == 0 && blockIdx.x + blockIdx.y == 0) g_favor_wait_diag[255][0] = (int)(smem_addr(b) >> 3);
 #endif
   float* norms = reinterpret_cast<float*>(sm + C::kNorm);   // [c&1][K=0/Q=1][128]
-  float* smax = reinterpret_cast<float*>(sm + C::kSmax);    // [c&1][wg][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sc = blockIdx.x, bh = blockIdx.y;
@@ -840,12 +854,12 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
       const uint32_t id_state = idesc_bf16(kFB, D, true, true);
       const uint32_t id_ones_mn = idesc_bf16(kFB, 16, true, false);
       const uint32_t id_a = idesc_bf16(kBM, kBM, false, false);
-      const uint32_t id_og = idesc_bf16(kBM, D + 16, false, false);
       const uint32_t id_av = idesc_bf16(kBM, D, false, true);
       const uint32_t id_aones = idesc_bf16(kBM, 16, false, false);
       const uint32_t om_a = smem_addr(sm + C::kOmega), ones_a = smem_addr(sm + C::kOnes);
       const uint32_t phik_a = smem_addr(sm + C::kPhiK), phiq_a = smem_addr(sm + C::kPhiQ);
-      const uint32_t gs_a = smem_addr(sm + C::kGs), k_a = smem_addr(sm + C::kK), q_a = smem_addr(sm + C::kQ);
+      const uint32_t gs_a = smem_addr(sm + C::kGs), gsb_a = smem_addr(sm + C::kGsB);
+      const uint32_t k_a = smem_addr(sm + C::kK), q_a = smem_addr(sm + C::kQ);
       const uint32_t v_a = smem_addr(sm + C::kV);
       bool ok = mbar_wait(setup_bar, 0, wctx);
       // P_K(c, fb) -> X.  X is free once the phi(Q) block before it was read;
@@ -901,8 +915,10 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
 #pragma unroll
           for (int k = 0; k < kFB / 16; ++k) {
             mma_bf16(tmem + A_COL, kmajor(phiq_a, k), kmajor(phik_a, k), id_a, fb > 0 || k > 0);
-            const uint32_t ga = gs_a + (2 * fb + (k >> 2)) * (D + 16) * 128 + (k & 3) * 32;
-            mma_bf16(tmem + O_COL, kmajor(phiq_a, k), sdesc(ga, 16, 1024), id_og, fb > 0 || k > 0);
+            const uint64_t qd = kmajor(phiq_a, k);
+            mma_bf16(tmem + O_COL, qd, sdesc(gs_a + (fb * kFB + 16 * k) * 128, 32768, 1024), id_av, fb > 0 || k > 0);
+            mma_bf16(tmem + O_COL + D, qd, sdesc(gsb_a + (2 * fb + (k >> 2)) * 2048 + (k & 3) * 32, 16, 1024),
+                     id_aones, fb > 0 || k > 0);
           }
           mma_commit(phik_free);
           mma_commit(phiq_free);
@@ -956,31 +972,54 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
     const float c1 = prm.scale * kLog2e;
     const float hs2 = 0.5f * prm.scale * prm.scale;
     const uint32_t phik_a = smem_addr(sm + C::kPhiK), phiq_a = smem_addr(sm + C::kPhiQ);
-    uint8_t* gs = sm + C::kGs;
+    const uint32_t gsa_a = smem_addr(sm + C::kGs);
+    uint8_t* gsb = sm + C::kGsB;
     const int col0 = wg * 64;
-    // G columns of this warpgroup: WG0 0..31 and d..d+15, WG1 32..63
-    const int n_gparts = (wg == 0) ? 3 : 2;
-    auto g_col = [&](int j) { return wg == 0 ? (j == 0 ? 0 : (j == 1 ? 16 : D)) : (j == 0 ? 32 : 48); };
-    auto write_gs = [&](int fb, int n, float x) {
-      const int f = fb * kFB + t, atom = f >> 6, cc = f & 63;
-      const size_t off = ((size_t)atom * (D + 16) + n) * 128 + (((cc >> 3) ^ (n & 7)) << 4) + (cc & 7) * 2;
-      *reinterpret_cast<__nv_bfloat16*>(gs + off) = __float2bfloat16_rn(x);
+    // G columns of this warpgroup: WG0 0..31 and the normaliser d, WG1 32..63
+    // bf16 copy of 32 V columns (n0 .. n0+31) of feature f into GsA
+    auto write_gsa = [&](int f, int n0, const float* x) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int chunk = (n0 >> 3) + c;
+        const float* y = x + 8 * c;
+        st_shared_v4(gsa_a + f * 128 + ((chunk ^ (f & 7)) << 4), pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
+                     pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
+      }
     };
+    auto write_gsb = [&](int f, float z) {
+      *reinterpret_cast<__nv_bfloat16*>(gsb + (f >> 6) * 2048 + ((f & 63) >> 3) * 16 + (f & 7) * 2) =
+          __float2bfloat16_rn(z);
+    };
+    for (int e = threadIdx.x - 96; e < 4 * 16 * 128 / 16; e += kEpiThreads)
+      *reinterpret_cast<uint4*>(gsb + e * 16) = make_uint4(0u, 0u, 0u, 0u);
+    named_bar(1, kEpiThreads);
     // G_init = sum of the earlier superchunks' states, in superchunk order
     for (int fb = 0; fb < n_fb; ++fb) {
       const float* src = prm.partS + (((size_t)bh * n_fb + fb) * max(prm.n_split, 1)) * (D + 1) * kFB;
-      for (int j = 0; j < n_gparts; ++j) {
-        const int n0 = g_col(j);
-        uint32_t r[16];
+      const int f = fb * kFB + t;
+      const int n0 = wg * 32;
+      float x[32];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int n = min(n0 + x, D);
-          float acc = 0.f;
-          for (int p = 0; p < sc; ++p) acc += src[((size_t)p * (D + 1) + n) * kFB + t];
-          r[x] = __float_as_uint(acc);
-          write_gs(fb, n0 + x, acc);
-        }
-        tmem_st16(tmem + lane_off + G_COL + fb * (D + 16) + n0, r);
+      for (int j = 0; j < 32; ++j) {
+        float acc = 0.f;
+        for (int p = 0; p < sc; ++p) acc += src[((size_t)p * (D + 1) + n0 + j) * kFB + t];
+        x[j] = acc;
+      }
+      write_gsa(f, n0, x);
+      uint32_t r[16];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(x[16 * h + j]);
+        tmem_st16(tmem + lane_off + G_COL + fb * (D + 16) + n0 + 16 * h, r);
+      }
+      if (wg == 0) {
+        float z = 0.f;
+        for (int p = 0; p < sc; ++p) z += src[((size_t)p * (D + 1) + D) * kFB + t];
+        write_gsb(f, z);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(z);
+        tmem_st16(tmem + lane_off + G_COL + fb * (D + 16) + D, r);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -1023,14 +1062,12 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
           if (ok && n_fb == 1) ok = mbar_wait(phiq_free, (u - 1) & 1, wctx);
           tc_fence_after();
           if (ok) {
-            for (int j = 0; j < n_gparts; ++j) {
-              const int n0 = g_col(j);
-              uint32_t r[16];
-              tmem_ld16(tmem + lane_off + G_COL + fb * (D + 16) + n0, r);
-              tmem_ld_wait();
-#pragma unroll
-              for (int x = 0; x < 16; ++x) write_gs(fb, n0 + x, __uint_as_float(r[x]));
-            }
+            uint32_t v[32], z[16];
+            tmem_ld32(tmem + lane_off + G_COL + fb * (D + 16) + wg * 32, v);
+            if (wg == 0) tmem_ld16(tmem + lane_off + G_COL + fb * (D + 16) + D, z);
+            tmem_ld_wait();
+            write_gsa(fb * kFB + t, wg * 32, reinterpret_cast<const float*>(v));
+            if (wg == 0) write_gsb(fb * kFB + t, __uint_as_float(z[0]));
           }
           tc_fence_before();
           fence_proxy_async_smem();
@@ -1041,26 +1078,11 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
         if (ok) ok = mbar_wait(pq_full, u & 1, wctx);
         tc_fence_after();
         if (fb == 0) {
-          if (c >= 1 && threadIdx.x == 96) bulk_wait_read0();   // the staging tile (phi(Q) buffer) is free
-          float mx = -INFINITY;
-          if (ok) {
-            uint32_t p0[32], p1[32];
-            tmem_ld32(tmem + lane_off + X_COL + col0, p0);
-            tmem_ld32(tmem + lane_off + X_COL + col0 + 32, p1);
-            tmem_ld_wait();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) mx = fmaxf(mx, fmaxf(__uint_as_float(p0[x]), __uint_as_float(p1[x])));
-          }
-          float* sx = smax + (c & 1) * 2 * kBM;
-          sx[wg * kBM + t] = mx;
+          // the staging tile (phi(Q) buffer) has been read by the previous store
+          if (c >= 1 && threadIdx.x == 96) bulk_wait_read0();
           named_bar(1, kEpiThreads);
-          mx = fmaxf(sx[t], sx[kBM + t]);
-          bias_q = mx * c1;
-          if (n_fb > 1) {
-            if (ok) ok = mbar_wait(&qnorm_full[c & 1], (c >> 1) & 1, wctx);
-            const float bound = prm.scale * W * sqrtf(nk[kBM + t]) - 20.0f;
-            bias_q = fmaxf(bias_q, bound * kLog2e);
-          }
+          if (ok) ok = mbar_wait(&qnorm_full[c & 1], (c >> 1) & 1, wctx);
+          bias_q = (prm.scale * W * sqrtf(nk[kBM + t]) - kQueryHeadroom) * kLog2e;
         }
         if (ok && u >= 1) ok = mbar_wait(phiq_free, (u - 1) & 1, wctx);
         if (ok) {
@@ -1195,6 +1217,7 @@ cudaError_t launch_output(const void* Q, void* O, const Shape& s, const TcPlan& 
   CUtensorMap mq, mo;
   if (!make_map(&mq, Q, s) || !make_map(&mo, O, s)) return cudaErrorInvalidValue;
   OutParams prm{};
+  prm.key_ref = reinterpret_cast<const float*>(ws);
   prm.omega_img = reinterpret_cast<const uint8_t*>(ws + p.off_omega_img);
   prm.state_img = reinterpret_cast<const uint8_t*>(ws + p.off_state_img);
   prm.status = status;
