@@ -222,7 +222,10 @@ def run_gpu(args, rank, world, local_rank):
         favor.causal_state(k, v, omega, s, ws_c, dev_status=status, stream=stream)
         favor.causal_output(q, k, v, omega, s, ws_c, O=O_c, dev_status=status, stream=stream)
 
-    launches_per_step = 5 + (1 if favor.path_name(False, d, m, dt) == "simt" else 0)
+    # kernels of this library per step: tensor-core path = ORF, prep + state,
+    # output, prep + state, causal scan; CUDA-core path = ORF, prep + partial
+    # states + merge, output, prep + partial states, causal scan
+    launches_per_step = 7 if favor.path_name(False, d, m, dt) != "simt" else 8
 
     with torch.cuda.stream(stream):
         for i in range(max(3, args.warmup)):
@@ -232,45 +235,53 @@ def run_gpu(args, rank, world, local_rank):
         raise RuntimeError(f"device status {int(status.item())} after warm-up: "
                            f"{favor.status_string(int(status.item()))}")
 
-    # per-kernel durations: events around each stage on the launching stream
-    n_inst = min(args.steps, 200)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(n_inst)]
-    with torch.cuda.stream(stream):
-        for i in range(n_inst):
-            q, k, v = sets[i % n_sets]
-            e = evs[i]
-            e[0].record(stream)
-            favor.build_orf(wl.omega_seed_for_call(w, i), omega, stream=stream)
-            e[1].record(stream)
-            favor.bidir_state(k, v, omega, s, ws_b, dev_status=status, stream=stream)
-            e[2].record(stream)
-            favor.bidir_output(q, omega, s, ws_b, O=O_b, dev_status=status, stream=stream)
-            e[3].record(stream)
-            favor.causal_state(k, v, omega, s, ws_c, dev_status=status, stream=stream)
-            e[4].record(stream)
-            favor.causal_output(q, k, v, omega, s, ws_c, O=O_c, dev_status=status, stream=stream)
-            e[5].record(stream)
-    torch.cuda.synchronize(dev)
-    stage_ms = {st: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n_inst))
-                for j, st in enumerate(STAGES)}
-
-    # graphs: one per input set (and per Omega seed when Omega is redrawn)
-    graphs = []
+    # graphs: one per input set (and per Omega seed when Omega is redrawn) for
+    # the whole step, and one per stage for the per-kernel durations
     n_graphs = n_sets if not w.redraw_omega else max(n_sets, 4)
+    stage_fns = (
+        lambda i, q, k, v: favor.build_orf(wl.omega_seed_for_call(w, i), omega, stream=stream),
+        lambda i, q, k, v: favor.bidir_state(k, v, omega, s, ws_b, dev_status=status, stream=stream),
+        lambda i, q, k, v: favor.bidir_output(q, omega, s, ws_b, O=O_b, dev_status=status, stream=stream),
+        lambda i, q, k, v: favor.causal_state(k, v, omega, s, ws_c, dev_status=status, stream=stream),
+        lambda i, q, k, v: favor.causal_output(q, k, v, omega, s, ws_c, O=O_c, dev_status=status, stream=stream),
+    )
+    graphs, stage_graphs = [], []
     with torch.cuda.stream(stream):
         for i in range(n_graphs):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 step(i, wl.omega_seed_for_call(w, i))
             graphs.append(g)
+            per = []
+            for fn in stage_fns:
+                gs = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gs, stream=stream):
+                    fn(i, *sets[i % n_sets])
+                per.append(gs)
+            stage_graphs.append(per)
     torch.cuda.synchronize(dev)
-    for i in range(max(3, args.warmup)):
-        graphs[i % n_graphs].replay()
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            graphs[i % n_graphs].replay()
+            for gs in stage_graphs[i % n_graphs]:
+                gs.replay()
     torch.cuda.synchronize(dev)
 
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([x], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+        return x
+
+    # timed region 1: K replays of the whole-step graph (the headline value)
+    barrier()
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
@@ -285,14 +296,26 @@ def run_gpu(args, rank, world, local_rank):
         end.record(stream)
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter() - t_wall0
+    barrier()
+
+    # timed region 2: the same K steps as per-stage graphs, an event on the
+    # launching stream after each stage: per-kernel average launch durations
+    n_ev = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(n_ev)]
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for i in range(n_ev):
+            e = evs[i]
+            e[0].record(stream)
+            for j, gs in enumerate(stage_graphs[i % n_graphs]):
+                gs.replay()
+                e[j + 1].record(stream)
+    torch.cuda.synchronize(dev)
     clocks = sampler.stop()
-    elapsed_ms = start.elapsed_time(end)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-        dist.barrier()
+    barrier()
+    stage_ms = {st: max_over_ranks(statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n_ev)))
+                for j, st in enumerate(STAGES)}
+    elapsed_ms = max_over_ranks(start.elapsed_time(end))
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} after the timed region")
 
@@ -379,7 +402,7 @@ def run_gpu(args, rank, world, local_rank):
         "config": {"workload": w.name, "B": B, "H": H, "L": L, "d": d, "m": m, "qk_scale": s,
                    "step": "build Omega + bidirectional + causal forward", "tokens_per_step": tokens_per_step,
                    "path": favor.path_name(False, d, m, dt), "l2": f"{n_sets} rotating input sets "
-                   f"({n_sets * bytes_per_set / 2**20:.0f} MiB > L2)", "timing": "CUDA graph replay per step",
+                   f"({n_sets * bytes_per_set / 2**20:.0f} MiB > L2)", "timing": "CUDA graph replay per step; per-kernel times from per-stage graphs with events between stages",
                    "parallelism": f"replicas x{world}"},
         "modes": {"bidir_tokens_per_s": tokens_per_step / (bidir_ms / 1e3),
                   "causal_tokens_per_s": tokens_per_step / (causal_ms / 1e3),
