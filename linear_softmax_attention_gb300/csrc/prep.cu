@@ -17,12 +17,10 @@ constexpr int kPrepThreads = 32 * kPrepRows;   // one warp per row of Omega
 
 // Grid of ceil(m / 8) CTAs; warp w of CTA b handles row i = 8b + w: its
 // squared norm (the CTA writes the largest of its 8 into header slot b) and,
-// if `image` is non-null, its bf16 images: hi = bf16(w) at `image` and
-// lo = bf16(w - hi) m*d*2 bytes later, so that hi + lo carries w to about 16
-// significant bits (the projection is two accumulating MMAs; bf16 w alone
-// costs ~2% in the output).  Layout of each image: [feature block of 128]
-// [64-column atom][128 rows][128 B], 16-byte chunk c of row r stored at
-// chunk c ^ (r % 8) (the 128-byte swizzle).
+// if `image` is non-null, its fp16 image (round to nearest, saturating) for
+// the projection MMAs: layout [64-column atom][m rows][128 B], 16-byte chunk
+// c of row r stored at chunk c ^ (r % 8) (the 128-byte swizzle).  fp16
+// carries w to 11 significant bits; bf16 w alone costs ~2.5% in the output.
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const float* __restrict__ omega, int m, int d,
                                                             float* __restrict__ header,
                                                             uint8_t* __restrict__ image) {
@@ -36,18 +34,15 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const float* __restr
     for (int c = lane; c < d; c += 32) acc = fmaf(row[c], row[c], acc);
     n2 = warp_sum(acc);
     if (image != nullptr) {
-      const int n_atoms = (d + 63) / 64;
-      const int fb = i >> 7, r = i & 127;
       for (int c = 2 * lane; c < d; c += 64) {
         const float w0 = row[c];
         const float w1 = (c + 1 < d) ? row[c + 1] : 0.f;
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(w0, w1);
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(w0 - __low2float(hi), w1 - __high2float(hi));
+        uint32_t h;
+        asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(w1), "f"(w0));
         const int atom = c >> 6, cc = c & 63;
-        const int chunk = (cc >> 3) ^ (r & 7);
-        const size_t off = ((size_t)(fb * n_atoms + atom) * 128 + r) * 128 + chunk * 16 + (cc & 7) * 2;
-        *reinterpret_cast<__nv_bfloat162*>(image + off) = hi;
-        *reinterpret_cast<__nv_bfloat162*>(image + (size_t)m * d * 2 + off) = lo;
+        const int chunk = (cc >> 3) ^ (i & 7);
+        const size_t off = ((size_t)atom * m + i) * 128 + chunk * 16 + (cc & 7) * 2;
+        *reinterpret_cast<uint32_t*>(image + off) = h;
       }
     }
   }

@@ -1,24 +1,36 @@
-// Tensor-core (tcgen05) FAVOR+ kernels for sm_103a: bf16 operands in shared
-// memory (TMA, 128-byte swizzle), fp32 accumulators in tensor memory.
+// Tensor-core (tcgen05) FAVOR+ kernels for sm_103a: operands in shared memory
+// (TMA, 128-byte swizzle), fp32 accumulators in tensor memory.
 //
 // "Performer — Rethinking Attention with Performers" (digest), §Key equations
 // and the flowchart: phi(K)^T V and phi(K)^T 1 are formed first, then
 // phi(Q) times each, then the row-wise divide; §Methods, causal bullet: the
 // prefix sum G_t = sum_{s<=t} phi(k_s) v_s^T.  The contractions are dense
 // GEMMs and run on the tensor cores:
-//   projection  P  = X Omega^T         M = 128 tokens,   N = 128 features, K = d
-//                                      (Omega = hi + lo, two bf16 MMAs)
-//   state       S~ += phi(K)^T [V|1]   M = 128 features, N = d (+16),      K = 128 tokens
-//   output      O  = phi(Q) S~         M = 128 tokens,   N = d + 16,       K = m
-//   causal      A  = phi(Q_c) phi(K_c)^T (lower triangle kept), O += A [V_c|1]
+//   projection  P  = X Omega^T         M = 128 tokens,   N = m (or 128), K = d   (fp16 operands)
+//   state       S~ += phi(K)^T [V|1]   M = 128 features, N = d + 16,     K = 128 tokens
+//   output      O  = phi(Q) S~         M = 128 tokens,   N = d + 16,     K = m
+//   causal      [A | O] += phi(Q_c) [phi(K_c)^T | G_s]  (one MMA, N = 128 + d + 16),
+//               O += mask(A) [V_c | 1]
 // The exponentials of the feature map run on the CUDA cores between them
 // (TMEM -> registers -> bf16 in shared memory).
 //
+// Measured on GB300, one M = 128 MMA instruction costs about the same for
+// every N up to 128 and about twice that at N = 256, so the kernels issue few,
+// wide instructions: the projection covers all m features at once where the
+// tensor memory allows, and the normaliser column rides in the same MMA as V
+// (the descriptor's leading-byte offset points from the V tile to a constant
+// block whose first column is 1).  The projection runs in fp16: a warp
+// rewrites each K or Q tile in place as fp16 while it computes the squared
+// row norms, and Omega is kept as an fp16 image, which carries Omega to 11
+// significant bits (bf16 Omega alone costs ~2.5% in the output).
+//
 // Warp roles: warp 0 issues TMA loads, warp 1 owns tensor memory and issues
-// MMAs (one elected thread), warp 2 (state and causal kernels) computes the
-// squared row norms of the K (and Q) tiles, and eight epilogue warps form two
+// MMAs (one elected thread), warps 2-3 compute the squared row norms of the K
+// (and Q) tiles and convert them to fp16, and eight epilogue warps form two
 // warpgroups that split the columns of each 128-row tile (thread = one TMEM
-// lane = one token or one feature).
+// lane = one token or one feature).  Epilogues copy a tile out of tensor
+// memory and release it before they compute on it, so that the next MMA into
+// the same columns overlaps their arithmetic.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -35,9 +47,10 @@ constexpr int kBM = 128;          // tokens per tile
 constexpr int kFB = 128;          // features per block
 constexpr uint32_t kTmemCols = 512;
 constexpr int kAtom = 128 * 128;  // bytes of one [128 rows][128 B] swizzle block
-constexpr int kOnesBytes = 4096;  // K-major all-ones B operand: 16 rows x 128 tokens
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = 256;
+constexpr int kEpiTid0 = 128;   // first epilogue thread (warps 4-11)
+constexpr int kNormWarps = 2;
 
 // ---------------------------------------------------------------------------
 // workspace layout of the tensor-core path
@@ -45,8 +58,10 @@ constexpr int kEpiThreads = 256;
 struct TcPlan {
   bool causal;
   int n_fb, n_tiles;
-  int tiles_per_split, n_split;      // state partials (bidir: L splits; causal: superchunks - 1)
+  int tiles_per_split, n_split;      // state partials (bidir: L splits; causal: sub-splits of all
+                                     // superchunks but the last)
   int out_tiles_per_cta, out_ctas;   // output kernel (bidir) / superchunks (causal)
+  int sub_per_sc;                    // causal: state sub-splits per superchunk
   size_t off_omega_img, off_counters, off_partS, off_state_img, bytes;
 };
 
@@ -79,7 +94,7 @@ TcPlan tc_plan(bool causal, const Shape& s) {
   p.n_fb = s.m / kFB;
   p.n_tiles = (s.L + kBM - 1) / kBM;
   if (!causal) {
-    const int sp = pick_split(BH * p.n_fb, p.n_tiles, kSMs);
+    const int sp = pick_split(BH, p.n_tiles, kSMs);
     p.tiles_per_split = (p.n_tiles + sp - 1) / sp;
     p.n_split = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
     const int oc = pick_split(BH, p.n_tiles, kSMs);
@@ -89,14 +104,29 @@ TcPlan tc_plan(bool causal, const Shape& s) {
     const int sc = pick_split(BH, p.n_tiles, kSMs);
     p.out_tiles_per_cta = (p.n_tiles + sc - 1) / sc;                          // tiles per superchunk
     p.out_ctas = (p.n_tiles + p.out_tiles_per_cta - 1) / p.out_tiles_per_cta;  // superchunks
-    p.tiles_per_split = p.out_tiles_per_cta;
-    p.n_split = p.out_ctas - 1;                                               // all but the last
+    // the states of all superchunks but the last, each computed in k equal
+    // sub-splits (k divides the superchunk) so that enough CTAs run
+    const int tps = p.out_tiles_per_cta;
+    int best_k = 1;
+    long best_cost = -1;
+    for (int k = 1; k <= tps; ++k) {
+      if (tps % k) continue;
+      const long ctas = (long)BH * (p.out_ctas - 1) * k;
+      const long cost = ((ctas + kSMs - 1) / kSMs) * (tps / k + kCtaOverheadTiles);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best_k = k;
+      }
+    }
+    p.sub_per_sc = best_k;
+    p.tiles_per_split = tps / best_k;
+    p.n_split = (p.out_ctas - 1) * best_k;
   }
   size_t off = align_up(kWsHeader, 1024);
   p.off_omega_img = off;
-  off = align_up(off + (size_t)s.m * s.d * 4, 1024);   // hi and lo images
+  off = align_up(off + (size_t)s.m * s.d * 2, 1024);   // fp16 image of Omega
   p.off_counters = off;
-  off = align_up(off + (size_t)BH * p.n_fb * sizeof(uint32_t), 1024);
+  off = align_up(off + (size_t)BH * sizeof(uint32_t), 1024);
   p.off_partS = off;
   off = align_up(off + (size_t)BH * p.n_fb * max(p.n_split, 1) * (s.d + 1) * kFB * sizeof(float), 1024);
   p.off_state_img = off;
@@ -109,124 +139,160 @@ TcPlan tc_plan(bool causal, const Shape& s) {
 // shared device pieces
 // ---------------------------------------------------------------------------
 
-// Squared norm of row t of a [128][d] bf16 tile stored as 64-column swizzle
-// blocks (TMA layout).
+// Squared norm of row t of a [128][D] bf16 tile stored as 64-column swizzle
+// blocks (TMA layout); the row is rewritten in place as fp16 (round to
+// nearest, saturating at +-65504) for the projection MMA.  A key whose
+// entries reach the fp16 limit has |s k|^2 / 2 so far above any projection
+// that its feature is 0 in fp32 either way.
 template <int D>
-__device__ __forceinline__ float tile_row_sq(const uint8_t* tile, int t) {
+__device__ __forceinline__ float tile_row_sq_to_f16(uint8_t* tile, int t) {
+  constexpr int NC = D / 8;                     // 16-byte chunks per row
+  uint4 v[NC];
+#pragma unroll
+  for (int c = 0; c < NC; ++c)
+    v[c] = *reinterpret_cast<const uint4*>(tile + (c >> 3) * kAtom + t * 128 + (((c & 7) ^ (t & 7)) << 4));
   float acc = 0.f;
 #pragma unroll
-  for (int a = 0; a < D / 64; ++a) {
+  for (int c = 0; c < NC; ++c) {
+    const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+    uint32_t o[4];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 v = *reinterpret_cast<const uint4*>(tile + a * kAtom + t * 128 + ((c ^ (t & 7)) << 4));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float lo = __uint_as_float(w[j] << 16);
-        const float hi = __uint_as_float(w[j] & 0xFFFF0000u);
-        acc = fmaf(lo, lo, acc);
-        acc = fmaf(hi, hi, acc);
-      }
+    for (int j = 0; j < 4; ++j) {
+      const float lo = __uint_as_float(w[j] << 16);
+      const float hi = __uint_as_float(w[j] & 0xFFFF0000u);
+      acc = fmaf(lo, lo, acc);
+      acc = fmaf(hi, hi, acc);
+      o[j] = pack_f16_sat(lo, hi);
     }
+    v[c] = make_uint4(o[0], o[1], o[2], o[3]);
   }
+#pragma unroll
+  for (int c = 0; c < NC; ++c)
+    *reinterpret_cast<uint4*>(tile + (c >> 3) * kAtom + t * 128 + (((c & 7) ^ (t & 7)) << 4)) = v[c];
   return acc;
 }
 
-// 32 consecutive columns (f0 .. f0+31) of row t written as bf16 into a
-// swizzled [64-column atom][128 rows][128 B] buffer.  MODE 0: 2^(p*c1 - b)
-// (zero if !valid); MODE 1: the raw values, zeroed where column > t.
-template <int MODE>
-__device__ __forceinline__ void write_row32(uint32_t base, int t, int f0, const uint32_t (&p)[32], float c1, float b,
-                                            bool valid) {
+// tcgen05.ld 32x32b.x32 into r[OFF .. OFF+31]
+template <int OFF, int N>
+__device__ __forceinline__ void tmem_ld32_at(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(OFF + 32 <= N, "range");
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[OFF + 0]), "=r"(r[OFF + 1]), "=r"(r[OFF + 2]), "=r"(r[OFF + 3]), "=r"(r[OFF + 4]), "=r"(r[OFF + 5]),
+        "=r"(r[OFF + 6]), "=r"(r[OFF + 7]), "=r"(r[OFF + 8]), "=r"(r[OFF + 9]), "=r"(r[OFF + 10]), "=r"(r[OFF + 11]),
+        "=r"(r[OFF + 12]), "=r"(r[OFF + 13]), "=r"(r[OFF + 14]), "=r"(r[OFF + 15]), "=r"(r[OFF + 16]),
+        "=r"(r[OFF + 17]), "=r"(r[OFF + 18]), "=r"(r[OFF + 19]), "=r"(r[OFF + 20]), "=r"(r[OFF + 21]),
+        "=r"(r[OFF + 22]), "=r"(r[OFF + 23]), "=r"(r[OFF + 24]), "=r"(r[OFF + 25]), "=r"(r[OFF + 26]),
+        "=r"(r[OFF + 27]), "=r"(r[OFF + 28]), "=r"(r[OFF + 29]), "=r"(r[OFF + 30]), "=r"(r[OFF + 31])
+      : "r"(taddr));
+}
+// 64 consecutive columns into r[0 .. 63]
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  tmem_ld32_at<0>(taddr, r);
+  tmem_ld32_at<32>(taddr + 32, r);
+}
+
+// In place: x[j] = bf16x2(2^(x[2j] c1 - b), 2^(x[2j+1] c1 - b)) for j < N/2
+// (zeros if !valid).
+template <int N>
+__device__ __forceinline__ void exp_pack(uint32_t (&x)[N], float c1, float b, bool valid) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t w[4];
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const int f = f0 + 8 * j + 2 * h;
-      float x0 = __uint_as_float(p[8 * j + 2 * h]);
-      float x1 = __uint_as_float(p[8 * j + 2 * h + 1]);
-      if (MODE == 0) {
-        x0 = valid ? ex2(fmaf(x0, c1, -b)) : 0.f;
-        x1 = valid ? ex2(fmaf(x1, c1, -b)) : 0.f;
-      } else {
-        x0 = (f <= t) ? x0 : 0.f;
-        x1 = (f + 1 <= t) ? x1 : 0.f;
-      }
-      w[h] = pack_bf16(x0, x1);
-    }
-    const int f = f0 + 8 * j;
-    const int atom = f >> 6, chunk = (f & 63) >> 3;
-    st_shared_v4(base + atom * kAtom + t * 128 + ((chunk ^ (t & 7)) << 4), w[0], w[1], w[2], w[3]);
+  for (int j = 0; j < N / 2; ++j) {
+    const float y0 = valid ? ex2(fmaf(__uint_as_float(x[2 * j]), c1, -b)) : 0.f;
+    const float y1 = valid ? ex2(fmaf(__uint_as_float(x[2 * j + 1]), c1, -b)) : 0.f;
+    x[j] = pack_bf16(y0, y1);
   }
 }
 
-__device__ __forceinline__ void fill_ones(uint8_t* p, int tid0, int nthreads) {
-  const uint32_t one2 = 0x3F803F80u;
-  for (int e = threadIdx.x - tid0; e < kOnesBytes / 16; e += nthreads)
-    *reinterpret_cast<uint4*>(p + e * 16) = make_uint4(one2, one2, one2, one2);
+// Row t, columns col0 .. col0 + 2*NW - 1 (col0 a multiple of 8) of a tile of
+// 64-column swizzle blocks `atom_stride` bytes apart, from NW packed words.
+template <int NW, int N>
+__device__ __forceinline__ void store_row(uint32_t base, int atom_stride, int t, int col0, const uint32_t (&x)[N]) {
+#pragma unroll
+  for (int c = 0; c < NW / 4; ++c) {
+    const int col = col0 + 8 * c;
+    const int atom = col >> 6, chunk = (col & 63) >> 3;
+    st_shared_v4(base + atom * atom_stride + t * 128 + ((chunk ^ (t & 7)) << 4), x[4 * c], x[4 * c + 1],
+                 x[4 * c + 2], x[4 * c + 3]);
+  }
+}
+
+// Constant [128 rows][128 B] block, MN-major swizzled: element 0 of every
+// row is 1, the rest 0.  Read as columns d .. d+15 of [V | 1].
+__device__ __forceinline__ void fill_ones_block(uint8_t* p, int tid0, int nthreads) {
+  for (int e = threadIdx.x - tid0; e < kAtom / 16; e += nthreads) {
+    const int row = e >> 3, logical = (e & 7) ^ (row & 7);
+    *reinterpret_cast<uint4*>(p + e * 16) = make_uint4(logical == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
+  }
 }
 
 // MMA descriptors of the fixed layouts
-__device__ __forceinline__ uint64_t kmajor(uint32_t base, int k) {      // K-major SW128, k-step of 16
-  return sdesc(base + (k >> 2) * kAtom + (k & 3) * 32, 16, 1024);
+__device__ __forceinline__ uint64_t kmajor(uint32_t base, int k, int atom_stride = kAtom) {   // K-major, k-step 16
+  return sdesc(base + (k >> 2) * atom_stride + (k & 3) * 32, 16, 1024);
 }
-__device__ __forceinline__ uint64_t mnmajor(uint32_t base, int k) {     // MN-major SW128, 16-row k-step
-  return sdesc(base + k * 2048, kAtom, 1024);
+__device__ __forceinline__ uint64_t mnmajor(uint32_t base, int k, int atom_stride = kAtom) {  // MN-major, 16 rows
+  return sdesc(base + k * 2048, atom_stride, 1024);
 }
-__device__ __forceinline__ uint64_t ones_desc(uint32_t base, int k) {   // K-major ones, 16 rows
-  return sdesc(base + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024);
+// [V | 1] as an MN-major operand of N = d + 16: V's 64 columns, then the
+// ones block `ones - v` bytes further on
+__device__ __forceinline__ uint64_t v_ones(uint32_t v, uint32_t ones, int k) {
+  return sdesc(v + k * 2048, ones - v, 1024);
+}
+// fp16 Omega image [d/64][m rows][128 B], rows f0 .. : K-major B of the projection
+__device__ __forceinline__ uint64_t omega_desc(uint32_t img, int m, int f0, int k) {
+  return sdesc(img + (k >> 2) * m * 128 + f0 * 128 + (k & 3) * 32, 16, 1024);
 }
 
 // ---------------------------------------------------------------------------
-// state kernel: one (token split, 128-feature block, head) per CTA.
-// Bidirectional: the last CTA of a (head, block) adds the splits (fixed order)
-// into the bf16 state image read by the output kernel.  Causal: the partial
-// of each superchunk but the last is kept for the scan.
+// state kernel: one (token split, head) per CTA, all m features.
+// Bidirectional: the last CTA of a head adds the splits (fixed order) into
+// the bf16 state image read by the output kernel.  Causal: the partial of
+// each superchunk but the last is kept for the scan.
 // ---------------------------------------------------------------------------
 struct StateParams {
   const float* key_ref;
   const uint8_t* omega_img;
   float* partS;            // [BH][n_fb][n_split][d+1][128]
-  uint32_t* counters;      // [BH][n_fb]
+  uint32_t* counters;      // [BH]
   uint8_t* state_img;      // [BH][m/64][d+16][128 B]
   int32_t* status;
   int L, m, n_split, tiles_per_split, merge;
   float scale;
 };
 
-constexpr int kStateThreads = 352;   // warps 0 TMA, 1 MMA, 2 norms, 3-10 epilogue
+constexpr int kStateThreads = 384;   // warps 0 TMA, 1 MMA, 2-3 norms, 4-11 epilogue
 
 template <int D>
 struct StateCfg {
   static constexpr int NS = 3;                     // K/V stages
-  static constexpr int NPHI = 2;                   // phi buffers
   static constexpr int kTileBytes = D * kBM * 2;   // one K or V tile
-  static constexpr int kOmega = 0;                 // hi, lo
-  static constexpr int kOnes = kOmega + 2 * kFB * D * 2;
-  static constexpr int kStages = kOnes + kOnesBytes;
-  static constexpr int kPhi = kStages + NS * 2 * kTileBytes;
-  static constexpr int kNorm = kPhi + NPHI * 2 * kAtom;
+  static constexpr int kOmega = 0;                 // fp16 image, up to 256 x D
+  static constexpr int kStages = kOmega + 256 * D * 2;
+  static constexpr int kOnes = kStages + NS * 2 * kTileBytes;   // above every V tile
+  static constexpr int kPhi = kOnes + kAtom;                     // [fb][2 atoms][128][128 B]
+  static constexpr int kNorm = kPhi + 2 * 2 * kAtom;
   static constexpr int kBars = kNorm + NS * kBM * 4;
   static constexpr int kSmem = kBars + 512 + 1024;
 };
 
-template <int D>
+template <int D, int M>
 __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_constant__ CUtensorMap mapK,
                                                                  const __grid_constant__ CUtensorMap mapV,
                                                                  StateParams prm) {
   using C = StateCfg<D>;
+  constexpr int NFB = M / kFB;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBars);
-  uint64_t* full = bars;                      // [NS]
+  uint64_t* full = bars;                      // [NS] K, V landed
   uint64_t* empty = full + C::NS;             // [NS]
-  uint64_t* norm_full = empty + C::NS;        // [NS]
-  uint64_t* p_full = norm_full + C::NS;       // [2]
+  uint64_t* kn_full = empty + C::NS;          // [NS] K in fp16, norms written
+  uint64_t* p_full = kn_full + C::NS;         // [2] per feature block
   uint64_t* p_free = p_full + 2;              // [2]
-  uint64_t* phi_full = p_free + 2;            // [NPHI]
-  uint64_t* phi_free = phi_full + C::NPHI;    // [NPHI]
-  uint64_t* setup_bar = phi_free + C::NPHI;
+  uint64_t* phi_full = p_free + 2;            // [2]
+  uint64_t* phi_free = phi_full + 2;          // [2]
+  uint64_t* setup_bar = phi_free + 2;
   uint64_t* done_bar = setup_bar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -234,24 +300,22 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
   float* norm_s = reinterpret_cast<float*>(sm + C::kNorm);   // [NS][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x, fb = blockIdx.y, bh = blockIdx.z;
-  const int n_fb = gridDim.y;
+  const int split = blockIdx.x, bh = blockIdx.y;
   const int tile0 = split * prm.tiles_per_split;
   const int n_tiles_total = (prm.L + kBM - 1) / kBM;
   const int n_tiles = min(prm.tiles_per_split, n_tiles_total - tile0);
   const WaitCtx wctx{abort_flag, prm.status};
+  constexpr uint32_t S_COL = 256;              // S~ of block fb at S_COL + 128 fb; P at 0
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NS; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
-      mbar_init(&norm_full[i], 1);
+      mbar_init(&kn_full[i], kNormWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 1);
       mbar_init(&p_free[i], kEpiWarps);
-    }
-    for (int i = 0; i < C::NPHI; ++i) {
       mbar_init(&phi_full[i], kEpiWarps);
       mbar_init(&phi_free[i], 1);
     }
@@ -264,8 +328,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (warp >= 3) {
-    fill_ones(sm + C::kOnes, 96, kEpiThreads);
+  if (warp >= 4) {
+    fill_ones_block(sm + C::kOnes, kEpiTid0, kEpiThreads);
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -277,10 +341,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     if (lane == 0) {
       prefetch_tmap(&mapK);
       prefetch_tmap(&mapV);
-      mbar_arrive_expect_tx(setup_bar, 2 * kFB * D * 2);
-      bulk_load(sm + C::kOmega, prm.omega_img + (size_t)fb * kFB * D * 2, kFB * D * 2, setup_bar);
-      bulk_load(sm + C::kOmega + kFB * D * 2, prm.omega_img + ((size_t)prm.m + fb * kFB) * D * 2, kFB * D * 2,
-                setup_bar);
+      mbar_arrive_expect_tx(setup_bar, M * D * 2);
+      bulk_load(sm + C::kOmega, prm.omega_img, M * D * 2, setup_bar);
       int last_issue[C::NS];
       for (int i = 0; i < C::NS; ++i) last_issue[i] = -1;
       for (int i = 0; i < n_tiles; ++i) {
@@ -302,112 +364,116 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t id_proj = idesc_bf16(kBM, kFB, false, false);
-      const uint32_t id_state = idesc_bf16(kFB, D, true, true);
-      const uint32_t id_ones = idesc_bf16(kFB, 16, true, false);
-      const uint32_t s_tm = tmem + 256;           // S~: columns 256 .. 256+d+15
+      constexpr uint32_t id_proj = idesc_f16(kBM, kFB, false, false);
+      constexpr uint32_t id_state = idesc_bf16(kFB, D + 16, true, true);
       const uint32_t omega_a = smem_addr(sm + C::kOmega);
       const uint32_t ones_a = smem_addr(sm + C::kOnes);
       bool ok = mbar_wait(setup_bar, 0, wctx);
-      auto issue_state = [&](int j) -> bool {
-        const int b = j % C::NPHI;
-        if (!mbar_wait(&phi_full[b], (j / C::NPHI) & 1, wctx)) return false;
-        tc_fence_after();
-        const uint32_t phi_a = smem_addr(sm + C::kPhi + b * 2 * kAtom);
-        const uint32_t v_a = smem_addr(sm + C::kStages + (j % C::NS) * 2 * C::kTileBytes + C::kTileBytes);
-#pragma unroll
-        for (int k = 0; k < kBM / 16; ++k) {
-          const uint64_t ad = mnmajor(phi_a, k);
-          const bool acc = (j > 0) || (k > 0);
-          mma_bf16(s_tm, ad, mnmajor(v_a, k), id_state, acc);
-          mma_bf16(s_tm + D, ad, ones_desc(ones_a, k), id_ones, acc);
-        }
-        mma_commit(&phi_free[b]);
-        mma_commit(&empty[j % C::NS]);
-        return true;
-      };
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        const int st = i % C::NS, pb = i & 1;
-        if (!mbar_wait(&full[st], (i / C::NS) & 1, wctx)) { ok = false; break; }
-        if (i >= 2 && !mbar_wait(&p_free[pb], ((i >> 1) - 1) & 1, wctx)) { ok = false; break; }
-        tc_fence_after();
+      // per feature block: projection of tile i, then the state update of
+      // tile i-1, so that a block's state MMA never waits behind the other
+      // block's projection (which waits for the epilogue to free P)
+      for (int i = 0; ok && i <= n_tiles; ++i) {
+        const int st = i % C::NS, sp = (i + C::NS - 1) % C::NS;
+        if (i < n_tiles && !mbar_wait(&kn_full[st], (i / C::NS) & 1, wctx)) { ok = false; break; }
+        if (i >= 1 && !mbar_wait(&full[sp], ((i - 1) / C::NS) & 1, wctx)) { ok = false; break; }
         const uint32_t k_a = smem_addr(sm + C::kStages + st * 2 * C::kTileBytes);
+        const uint32_t v_a = smem_addr(sm + C::kStages + sp * 2 * C::kTileBytes + C::kTileBytes);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint64_t ad = kmajor(k_a, k);
-          mma_bf16(tmem + pb * kFB, ad, kmajor(omega_a, k), id_proj, k > 0);
-          mma_bf16(tmem + pb * kFB, ad, kmajor(omega_a + kFB * D * 2, k), id_proj, true);
+        for (int fb = 0; fb < NFB; ++fb) {
+          if (i < n_tiles) {
+            if (i >= 1 && !mbar_wait(&p_free[fb], (i - 1) & 1, wctx)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll 1
+            for (int k = 0; k < D / 16; ++k)
+              mma_bf16(tmem + fb * kFB, kmajor(k_a, k), omega_desc(omega_a, M, fb * kFB, k), id_proj, k > 0);
+            mma_commit(&p_full[fb]);
+          }
+          if (i >= 1) {
+            if (!mbar_wait(&phi_full[fb], (i - 1) & 1, wctx)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t phi_a = smem_addr(sm + C::kPhi + fb * 2 * kAtom);
+#pragma unroll 1
+            for (int k = 0; k < kBM / 16; ++k)
+              mma_bf16(tmem + S_COL + fb * 128, mnmajor(phi_a, k), v_ones(v_a, ones_a, k), id_state,
+                       (i > 1) || (k > 0));
+            mma_commit(&phi_free[fb]);
+          }
         }
-        mma_commit(&p_full[pb]);
-        if (i > 0 && !issue_state(i - 1)) { ok = false; break; }
+        if (ok && i >= 1) mma_commit(&empty[sp]);
       }
-      if (ok && n_tiles > 0) issue_state(n_tiles - 1);
       mma_commit(done_bar);
       mbar_wait(done_bar, 0, wctx);
     }
-  } else if (warp == 2) {
-    // squared norms of the K rows of each stage
+  } else if (warp < 2 + kNormWarps) {
+    // squared norms of the K rows of each stage; K rewritten as fp16
     for (int i = 0; i < n_tiles; ++i) {
       const int st = i % C::NS;
       if (!mbar_wait(&full[st], (i / C::NS) & 1, wctx)) break;
-      const uint8_t* kt = sm + C::kStages + st * 2 * C::kTileBytes;
+      uint8_t* kt = sm + C::kStages + st * 2 * C::kTileBytes;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) norm_s[st * kBM + lane + 32 * j] = tile_row_sq<D>(kt, lane + 32 * j);
+      for (int j = 0; j < 2; ++j) {
+        const int r = (warp - 2) * 64 + lane + 32 * j;
+        norm_s[st * kBM + r] = tile_row_sq_to_f16<D>(kt, r);
+      }
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&norm_full[st]);
+      if (lane == 0) mbar_arrive(&kn_full[st]);
     }
   } else {
     // ---------------- epilogue: two warpgroups x 128 lanes ----------------
-    const int wg = (warp - 3) >> 2;
+    const int wg = (warp - 4) >> 2;
     const int q = warp & 3;
     const int t = q * 32 + lane;                   // token row of P, feature row of S~
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const int col0 = wg * 64;                      // this warpgroup's columns of each feature block
     float R, W_unused;
     key_reference(prm.key_ref, prm.m, &R, &W_unused);
     const float c1 = prm.scale * kLog2e;
     const float hs2 = 0.5f * prm.scale * prm.scale;
-    const int col0 = wg * 64;
     bool ok = true;
     for (int i = 0; ok && i < n_tiles; ++i) {
-      const int st = i % C::NS, pb = i & 1, b = i % C::NPHI;
-      if (!mbar_wait(&p_full[pb], (i >> 1) & 1, wctx)) { ok = false; break; }
-      if (!mbar_wait(&norm_full[st], (i / C::NS) & 1, wctx)) { ok = false; break; }
-      tc_fence_after();
+      const int st = i % C::NS;
+      if (!mbar_wait(&kn_full[st], (i / C::NS) & 1, wctx)) { ok = false; break; }
       const float bias = (hs2 * norm_s[st * kBM + t] + R) * kLog2e;
       const bool valid = (tile0 + i) * kBM + t < prm.L;
-      if (i >= C::NPHI && !mbar_wait(&phi_free[b], ((i / C::NPHI) - 1) & 1, wctx)) { ok = false; break; }
-      uint32_t p0[32], p1[32];
-      tmem_ld32(tmem + lane_off + pb * kFB + col0, p0);
-      tmem_ld32(tmem + lane_off + pb * kFB + col0 + 32, p1);
-      tmem_ld_wait();
-      const uint32_t phi_a = smem_addr(sm + C::kPhi + b * 2 * kAtom);
-      write_row32<0>(phi_a, t, col0, p0, c1, bias, valid);
-      write_row32<0>(phi_a, t, col0 + 32, p1, c1, bias, valid);
-      tc_fence_before();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&p_free[pb]);
-        mbar_arrive(&phi_full[b]);
+#pragma unroll
+      for (int fb = 0; fb < NFB; ++fb) {
+        if (!mbar_wait(&p_full[fb], i & 1, wctx)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t x[64];
+        tmem_ld64(tmem + lane_off + fb * kFB + col0, x);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_free[fb]);
+        exp_pack<64>(x, c1, bias, valid);
+        if (i >= 1 && !mbar_wait(&phi_free[fb], (i - 1) & 1, wctx)) { ok = false; break; }
+        store_row<32>(smem_addr(sm + C::kPhi + fb * 2 * kAtom), kAtom, t, col0, x);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&phi_full[fb]);
       }
     }
-    // final state: lane f holds feature f of this block; WG0 columns 0..31,
-    // WG1 columns 32..63 and the normaliser column d
+    // final state: lane f holds feature f of a block.  Two blocks: warpgroup
+    // w reads block w; one block: the warpgroups split the d columns.
     const bool done = mbar_wait(done_bar, 0, wctx);
     tc_fence_after();
-    float* dst = prm.partS + ((((size_t)bh * n_fb + fb) * prm.n_split + split) * (D + 1)) * kFB;
     if (done && !*abort_flag) {
+      const int sfb = (NFB == 2) ? wg : 0;
+      float* dst = prm.partS + ((((size_t)bh * NFB + sfb) * prm.n_split + split) * (D + 1)) * kFB;
+      const uint32_t s_col = tmem + lane_off + S_COL + sfb * 128;
 #pragma unroll
-      for (int cb = wg; cb < D / 32; cb += 2) {
+      for (int cb = 0; cb < D / 32; ++cb) {
+        if (NFB == 1 && (cb & 1) != wg) continue;
         uint32_t v[32];
-        tmem_ld32(tmem + lane_off + 256 + cb * 32, v);
+        tmem_ld32(s_col + cb * 32, v);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j) dst[(size_t)(cb * 32 + j) * kFB + t] = __uint_as_float(v[j]);
       }
-      if (wg == 1) {
-        uint32_t z[16];
-        tmem_ld16(tmem + lane_off + 256 + D, z);
+      if (NFB == 2 || wg == 1) {
+        uint32_t z[8];
+        tmem_ld8(s_col + D, z);
         tmem_ld_wait();
         dst[(size_t)D * kFB + t] = __uint_as_float(z[0]);
       }
@@ -415,27 +481,29 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     tc_fence_before();
     if (prm.merge) {
       named_bar(1, kEpiThreads);
-      if (threadIdx.x == 96) {
+      if (threadIdx.x == kEpiTid0) {
         __threadfence();
-        const uint32_t old = atomicAdd(&prm.counters[bh * n_fb + fb], 1u);
+        const uint32_t old = atomicAdd(&prm.counters[bh], 1u);
         *is_last = (old == (uint32_t)(prm.n_split - 1)) ? 1 : 0;
       }
       named_bar(1, kEpiThreads);
       if (*is_last) {
         __threadfence();
-        const float* src = prm.partS + (((size_t)bh * n_fb + fb) * prm.n_split) * (D + 1) * kFB;
-        uint8_t* img = prm.state_img + (size_t)bh * prm.m * (D + 16) * 2;
-        const int f = fb * kFB + t;
-        const int atom = f >> 6, cc = f & 63;
+        uint8_t* img = prm.state_img + (size_t)bh * M * (D + 16) * 2;
         const int n0 = wg * ((D + 16) / 2), n1 = n0 + (D + 16) / 2;
-        for (int n = n0; n < n1; ++n) {
-          float acc = 0.f;
-          if (n <= D)
-            for (int p = 0; p < prm.n_split; ++p) acc += src[((size_t)p * (D + 1) + n) * kFB + t];
-          const size_t off = ((size_t)atom * (D + 16) + n) * 128 + (((cc >> 3) ^ (n & 7)) << 4) + (cc & 7) * 2;
-          *reinterpret_cast<__nv_bfloat16*>(img + off) = __float2bfloat16_rn(acc);
+        for (int b = 0; b < NFB; ++b) {
+          const float* src = prm.partS + (((size_t)bh * NFB + b) * prm.n_split) * (D + 1) * kFB;
+          const int f = b * kFB + t;
+          const int atom = f >> 6, cc = f & 63;
+          for (int n = n0; n < n1; ++n) {
+            float acc = 0.f;
+            if (n <= D)
+              for (int p = 0; p < prm.n_split; ++p) acc += src[((size_t)p * (D + 1) + n) * kFB + t];
+            const size_t off = ((size_t)atom * (D + 16) + n) * 128 + (((cc >> 3) ^ (n & 7)) << 4) + (cc & 7) * 2;
+            *reinterpret_cast<__nv_bfloat16*>(img + off) = __float2bfloat16_rn(acc);
+          }
         }
-        if (threadIdx.x == 96) prm.counters[bh * n_fb + fb] = 0;
+        if (threadIdx.x == kEpiTid0) prm.counters[bh] = 0;
       }
     }
   }
@@ -461,41 +529,40 @@ struct OutParams {
   float scale;
 };
 
-constexpr int kOutThreads = 352;   // warps 0 TMA, 1 MMA, 2 norms, 3-10 epilogue
+constexpr int kOutThreads = 384;   // warps 0 TMA, 1 MMA, 2-3 norms, 4-11 epilogue
 constexpr float kQueryHeadroom = 20.0f;
 
 template <int D>
 struct OutCfg {
-  static constexpr int NSQ = 2;
+  static constexpr int NSQ = 3;
   static constexpr int kTileBytes = D * kBM * 2;
-  static constexpr int kOmegaMax = 2 * 256 * D * 2;     // hi and lo
-  static constexpr int kStateMax = 256 * (D + 16) * 2;
-  static constexpr int kOmega = 0;
-  static constexpr int kState = kOmega + kOmegaMax;
-  static constexpr int kQ = kState + kStateMax;
-  static constexpr int kPhi = kQ + NSQ * kTileBytes;
-  static constexpr int kOut = kPhi + 4 * kAtom;         // 128 x 256 bf16
-  static constexpr int kNorm = kOut + kTileBytes;       // [NSQ][128] squared query norms
+  static constexpr int kOmega = 0;                          // fp16 image, up to 256 x D
+  static constexpr int kState = kOmega + 256 * D * 2;       // bf16 S~ image, up to 256 x (D + 16)
+  static constexpr int kQ = kState + 256 * (D + 16) * 2;
+  static constexpr int kPhi = kQ + NSQ * kTileBytes;        // [fb][2 atoms][128][128 B]
+  static constexpr int kOut = kPhi + 4 * kAtom;             // output staging tile
+  static constexpr int kNorm = kOut + kTileBytes;           // [NSQ][128] squared query norms
   static constexpr int kBars = kNorm + NSQ * kBM * 4;
   static constexpr int kSmem = kBars + 512 + 1024;
 };
 
-template <int D>
+template <int D, int M>
 __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_constant__ CUtensorMap mapQ,
                                                                 const __grid_constant__ CUtensorMap mapO,
                                                                 OutParams prm) {
   using C = OutCfg<D>;
+  constexpr int NFB = M / kFB;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBars);
   uint64_t* q_full = bars;                  // [NSQ]
-  uint64_t* q_empty = q_full + C::NSQ;      // [NSQ] MMA commit + norm warp
-  uint64_t* qnorm_full = q_empty + C::NSQ;  // [NSQ]
-  uint64_t* p_full = qnorm_full + C::NSQ;
-  uint64_t* p_free = p_full + 1;
-  uint64_t* phi_full = p_free + 1;
-  uint64_t* phi_free = phi_full + 1;
-  uint64_t* o_full = phi_free + 1;          // [2]
+  uint64_t* q_empty = q_full + C::NSQ;      // [NSQ] MMA commit + every epilogue warp (norm read)
+  uint64_t* qn_full = q_empty + C::NSQ;     // [NSQ] Q in fp16, norms written
+  uint64_t* p_full = qn_full + C::NSQ;      // [2] per feature block
+  uint64_t* p_free = p_full + 2;            // [2]
+  uint64_t* phi_full = p_free + 2;          // [2]
+  uint64_t* phi_free = phi_full + 2;        // [2]
+  uint64_t* o_full = phi_free + 2;          // [2]
   uint64_t* o_free = o_full + 2;            // [2]
   uint64_t* setup_bar = o_free + 2;
   uint64_t* done_bar = setup_bar + 1;
@@ -508,22 +575,20 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
   const int n_tiles_total = (prm.L + kBM - 1) / kBM;
   const int tile0 = blockIdx.x * prm.tiles_per_cta;
   const int n_tiles = min(prm.tiles_per_cta, n_tiles_total - tile0);
-  const int m = prm.m;
-  const int n_fb = m / kFB;
   const WaitCtx wctx{abort_flag, prm.status};
-  const uint32_t o_col[2] = {256u, 256u + 128u};   // O accumulators (d + 16 <= 128 columns each)
+  const uint32_t o_col[2] = {256u, 384u};   // O accumulators (d + 16 columns each); P at 0
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NSQ; ++i) {
       mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 2);
-      mbar_init(&qnorm_full[i], 1);
+      mbar_init(&q_empty[i], 1 + kEpiWarps);
+      mbar_init(&qn_full[i], kNormWarps);
     }
-    mbar_init(p_full, 1);
-    mbar_init(p_free, kEpiWarps);
-    mbar_init(phi_full, kEpiWarps);
-    mbar_init(phi_free, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&p_full[i], 1);
+      mbar_init(&p_free[i], kEpiWarps);
+      mbar_init(&phi_full[i], kEpiWarps);
+      mbar_init(&phi_free[i], 1);
       mbar_init(&o_full[i], 1);
       mbar_init(&o_free[i], kEpiWarps);
     }
@@ -545,7 +610,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
     if (lane == 0) {
       prefetch_tmap(&mapQ);
       prefetch_tmap(&mapO);
-      const uint32_t ob = 2 * m * D * 2, sb = m * (D + 16) * 2;
+      const uint32_t ob = M * D * 2, sb = M * (D + 16) * 2;
       mbar_arrive_expect_tx(setup_bar, ob + sb);
       bulk_load(sm + C::kOmega, prm.omega_img, ob, setup_bar);
       bulk_load(sm + C::kState, prm.state_img + (size_t)bh * sb, sb, setup_bar);
@@ -565,76 +630,81 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t id_proj = idesc_bf16(kBM, kFB, false, false);
-      const uint32_t id_out = idesc_bf16(kBM, D + 16, false, false);
+      constexpr uint32_t id_proj = idesc_f16(kBM, kFB, false, false);
+      constexpr uint32_t id_out = idesc_bf16(kBM, D + 16, false, false);
       const uint32_t omega_a = smem_addr(sm + C::kOmega);
       const uint32_t state_a = smem_addr(sm + C::kState);
-      const uint32_t phi_a = smem_addr(sm + C::kPhi);
       bool ok = mbar_wait(setup_bar, 0, wctx);
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        const int st = i % C::NSQ, ob = i & 1;
-        if (!mbar_wait(&q_full[st], (i / C::NSQ) & 1, wctx)) { ok = false; break; }
-        if (i >= 1 && !mbar_wait(p_free, (i - 1) & 1, wctx)) { ok = false; break; }
-        tc_fence_after();
+      // per feature block: projection of tile i, then that block's share of
+      // the output MMA of tile i-1
+      for (int i = 0; ok && i <= n_tiles; ++i) {
+        const int st = i % C::NSQ, ob = (i - 1) & 1;
+        if (i < n_tiles && !mbar_wait(&qn_full[st], (i / C::NSQ) & 1, wctx)) { ok = false; break; }
         const uint32_t q_a = smem_addr(sm + C::kQ + st * C::kTileBytes);
-        for (int f = 0; f < n_fb; ++f) {
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint64_t ad = kmajor(q_a, k);
-            mma_bf16(tmem + f * kFB, ad, kmajor(omega_a + f * kFB * D * 2, k), id_proj, k > 0);
-            mma_bf16(tmem + f * kFB, ad, kmajor(omega_a + (m + f * kFB) * D * 2, k), id_proj, true);
+        for (int fb = 0; fb < NFB; ++fb) {
+          if (i < n_tiles) {
+            if (i >= 1 && !mbar_wait(&p_free[fb], (i - 1) & 1, wctx)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll 1
+            for (int k = 0; k < D / 16; ++k)
+              mma_bf16(tmem + fb * kFB, kmajor(q_a, k), omega_desc(omega_a, M, fb * kFB, k), id_proj, k > 0);
+            mma_commit(&p_full[fb]);
+            if (fb == NFB - 1) mma_commit(&q_empty[st]);
+          }
+          if (i >= 1) {
+            if (fb == 0 && i >= 3 && !mbar_wait(&o_free[ob], ((i - 1) >> 1) - 1 & 1, wctx)) { ok = false; break; }
+            if (!mbar_wait(&phi_full[fb], (i - 1) & 1, wctx)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t phi_a = smem_addr(sm + C::kPhi + fb * 2 * kAtom);
+#pragma unroll 1
+            for (int kk = 0; kk < kFB / 16; ++kk) {
+              const int g = fb * (kFB / 16) + kk;
+              const uint32_t sa = state_a + (g >> 2) * (D + 16) * 128 + (g & 3) * 32;
+              mma_bf16(tmem + o_col[ob], kmajor(phi_a, kk), sdesc(sa, 16, 1024), id_out, g > 0);
+            }
+            mma_commit(&phi_free[fb]);
+            if (fb == NFB - 1) mma_commit(&o_full[ob]);
           }
         }
-        mma_commit(p_full);
-        mma_commit(&q_empty[st]);
-        if (!mbar_wait(phi_full, i & 1, wctx)) { ok = false; break; }
-        if (i >= 2 && !mbar_wait(&o_free[ob], ((i >> 1) - 1) & 1, wctx)) { ok = false; break; }
-        tc_fence_after();
-        for (int kk = 0; kk < m / 16; ++kk) {
-          const uint32_t sa = state_a + (kk >> 2) * (D + 16) * 128 + (kk & 3) * 32;
-          mma_bf16(tmem + o_col[ob], kmajor(phi_a, kk), sdesc(sa, 16, 1024), id_out, kk > 0);
-        }
-        mma_commit(&o_full[ob]);
-        mma_commit(phi_free);
       }
       mma_commit(done_bar);
       mbar_wait(done_bar, 0, wctx);
     }
-  } else if (warp == 2) {
-    // squared norms of the Q rows of each stage
+  } else if (warp < 2 + kNormWarps) {
+    // squared norms of the Q rows of each stage; Q rewritten as fp16
     for (int i = 0; i < n_tiles; ++i) {
       const int st = i % C::NSQ;
       if (!mbar_wait(&q_full[st], (i / C::NSQ) & 1, wctx)) break;
-      const uint8_t* qt = sm + C::kQ + st * C::kTileBytes;
+      uint8_t* qt = sm + C::kQ + st * C::kTileBytes;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) qnorm[st * kBM + lane + 32 * j] = tile_row_sq<D>(qt, lane + 32 * j);
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&qnorm_full[st]);
-        mbar_arrive(&q_empty[st]);
+      for (int j = 0; j < 2; ++j) {
+        const int r = (warp - 2) * 64 + lane + 32 * j;
+        qnorm[st * kBM + r] = tile_row_sq_to_f16<D>(qt, r);
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qn_full[st]);
     }
   } else {
-    const int wg = (warp - 3) >> 2;
+    const int wg = (warp - 4) >> 2;
     const int q = warp & 3;
     const int t = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const int col0 = wg * 64;                      // this warpgroup's columns of each feature block
     float R_unused, W;
-    key_reference(prm.key_ref, m, &R_unused, &W);
+    key_reference(prm.key_ref, prm.m, &R_unused, &W);
     const float c1 = prm.scale * kLog2e;
-    const uint32_t phi_a = smem_addr(sm + C::kPhi);
     const uint32_t out_a = smem_addr(sm + C::kOut);
-    const int half = m / 2;            // features handled by this warpgroup
-    const int f_lo = wg * half;
     bool ok = true;
     auto store_out = [&](int j) {
       const int ob = j & 1;
-      const bool have = mbar_wait(&o_full[ob], (j >> 1) & 1, wctx);
+      const bool have = ok && mbar_wait(&o_full[ob], (j >> 1) & 1, wctx);
       tc_fence_after();
-      uint32_t v[32], z[16];
+      uint32_t v[32], z[8];
       if (have) {
         tmem_ld32(tmem + lane_off + o_col[ob] + wg * 32, v);
-        tmem_ld16(tmem + lane_off + o_col[ob] + D, z);
+        tmem_ld8(tmem + lane_off + o_col[ob] + D, z);
         tmem_ld_wait();
       }
       tc_fence_before();
@@ -644,55 +714,59 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
       const int row = (tile0 + j) * kBM + t;
       if (have && row < prm.L && (!(den > 0.f) || !isfinite(den))) report_status(prm.status, FAVOR_ERR_NONFINITE);
       const float inv = 1.0f / den;
-      if (threadIdx.x == 96 && j > 0) bulk_wait_read0();   // previous store has left the staging tile
+      if (threadIdx.x == kEpiTid0 && j > 0) bulk_wait_read0();   // previous store has left the staging tile
       named_bar(1, kEpiThreads);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int chunk = wg * 4 + c;
-        const float* x = reinterpret_cast<const float*>(v) + c * 8;
-        st_shared_v4(out_a + t * 128 + ((chunk ^ (t & 7)) << 4), pack_bf16(x[0] * inv, x[1] * inv),
-                     pack_bf16(x[2] * inv, x[3] * inv), pack_bf16(x[4] * inv, x[5] * inv),
-                     pack_bf16(x[6] * inv, x[7] * inv));
+        const int o = c * 8;
+        st_shared_v4(out_a + t * 128 + ((chunk ^ (t & 7)) << 4),
+                     pack_bf16(__uint_as_float(v[o]) * inv, __uint_as_float(v[o + 1]) * inv),
+                     pack_bf16(__uint_as_float(v[o + 2]) * inv, __uint_as_float(v[o + 3]) * inv),
+                     pack_bf16(__uint_as_float(v[o + 4]) * inv, __uint_as_float(v[o + 5]) * inv),
+                     pack_bf16(__uint_as_float(v[o + 6]) * inv, __uint_as_float(v[o + 7]) * inv));
       }
       fence_proxy_async_smem();
       named_bar(1, kEpiThreads);
-      if (threadIdx.x == 96 && have && !*abort_flag) {
+      if (threadIdx.x == kEpiTid0 && have && !*abort_flag) {
         tma_store_3d(&mapO, 0, (tile0 + j) * kBM, bh, sm + C::kOut);
         bulk_commit();
       }
     };
     for (int i = 0; i < n_tiles; ++i) {
       const int st = i % C::NSQ;
-      if (ok) ok = mbar_wait(p_full, i & 1, wctx);
-      if (ok) ok = mbar_wait(&qnorm_full[st], (i / C::NSQ) & 1, wctx);
+      if (ok) ok = mbar_wait(&p_full[0], i & 1, wctx);
+      if (ok) ok = mbar_wait(&qn_full[st], (i / C::NSQ) & 1, wctx);
       tc_fence_after();
-      const float bias = (prm.scale * W * sqrtf(qnorm[st * kBM + t]) - kQueryHeadroom) * kLog2e;
-      if (ok && i >= 1) ok = mbar_wait(phi_free, (i - 1) & 1, wctx);
-      if (ok) {
-        for (int cb = 0; cb < half / 32; cb += 4) {
-          uint32_t p0[32], p1[32], p2[32], p3[32];
-          tmem_ld32(tmem + lane_off + f_lo + cb * 32, p0);
-          tmem_ld32(tmem + lane_off + f_lo + cb * 32 + 32, p1);
-          tmem_ld32(tmem + lane_off + f_lo + cb * 32 + 64, p2);
-          tmem_ld32(tmem + lane_off + f_lo + cb * 32 + 96, p3);
-          tmem_ld_wait();
-          write_row32<0>(phi_a, t, f_lo + cb * 32, p0, c1, bias, true);
-          write_row32<0>(phi_a, t, f_lo + cb * 32 + 32, p1, c1, bias, true);
-          write_row32<0>(phi_a, t, f_lo + cb * 32 + 64, p2, c1, bias, true);
-          write_row32<0>(phi_a, t, f_lo + cb * 32 + 96, p3, c1, bias, true);
-        }
-      }
-      tc_fence_before();
-      fence_proxy_async_smem();
+      const float qn = qnorm[st * kBM + t];
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(p_free);
-        mbar_arrive(phi_full);
+      if (lane == 0) mbar_arrive(&q_empty[st]);
+      const float bias = (prm.scale * W * sqrtf(qn) - kQueryHeadroom) * kLog2e;
+#pragma unroll
+      for (int fb = 0; fb < NFB; ++fb) {
+        if (ok && fb > 0) ok = mbar_wait(&p_full[fb], i & 1, wctx);
+        tc_fence_after();
+        uint32_t x[64];
+        if (ok) {
+          tmem_ld64(tmem + lane_off + fb * kFB + col0, x);
+          tmem_ld_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_free[fb]);
+        if (ok) {
+          exp_pack<64>(x, c1, bias, true);
+          if (i >= 1) ok = mbar_wait(&phi_free[fb], (i - 1) & 1, wctx);
+          if (ok) store_row<32>(smem_addr(sm + C::kPhi + fb * 2 * kAtom), kAtom, t, col0, x);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&phi_full[fb]);
       }
       if (i >= 1) store_out(i - 1);
     }
     if (n_tiles >= 1) store_out(n_tiles - 1);
-    if (threadIdx.x == 96) bulk_wait0();
+    if (threadIdx.x == kEpiTid0) bulk_wait0();
     mbar_wait(done_bar, 0, wctx);
   }
   tc_fence_before();
@@ -703,11 +777,12 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
 
 // ---------------------------------------------------------------------------
 // causal kernel: CTA = one superchunk of one head, walking 128-token chunks.
-// G (m x (d+16), fp32) lives in tensor memory; it starts as the sum of the
-// earlier superchunks' partial states.  Per chunk c and 128-feature block fb:
-//   phi(K_c), G_s,fb <- bf16(G_fb), phi(Q_c)                       (CUDA cores)
-//   G_fb += phi(K_c)_fb^T [V_c | 1];  A += phi(Q_c)_fb phi(K_c)_fb^T;
-//   O += phi(Q_c)_fb G_s,fb                                       (tensor cores)
+// G (m x (d+16), fp32) lives in tensor memory; it starts as the sum, in
+// order, of the partial states of the sub-splits of the earlier superchunks.  Per chunk c and 128-feature block fb:
+//   phi(K_c)_fb and G_s,fb <- bf16(G_fb), side by side in one operand;
+//   phi(Q_c)_fb                                                   (CUDA cores)
+//   G_fb += phi(K_c)_fb^T [V_c | 1];
+//   [A | O] += phi(Q_c)_fb [phi(K_c)_fb^T | G_s,fb]              (tensor cores)
 // then A's upper triangle is zeroed (diagonal kept), O += A [V_c | 1], and
 // O is divided by its normaliser column.  The query row reference is
 // s |q| max_i |w_i| - 20 (the largest possible exponent less 20), so every
@@ -716,93 +791,85 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
 struct CausalParams {
   const float* key_ref;   // row-norm maxima (key_reference)
   const uint8_t* omega_img;
-  const float* partS;     // [BH][n_fb][n_split][d+1][128]
+  const float* partS;     // [BH][n_fb][n_split][d+1][128], sub_per_sc per superchunk
   int32_t* status;
-  int L, m, n_split, tiles_per_sc;
+  int L, m, n_split, tiles_per_sc, sub_per_sc;
   float scale;
 };
 
-constexpr int kCausalThreads = 352;   // warps 0 TMA, 1 MMA, 2 norms, 3-10 epilogue
+constexpr int kCausalThreads = 384;   // warps 0 TMA, 1 MMA, 2-3 norms, 4-11 epilogue
 
 template <int D>
 struct CausalCfg {
   static constexpr int kTileBytes = D * kBM * 2;
-  static constexpr int kOmega = 0;                                 // hi, lo: 2 * m * d * 2
-  static constexpr int kOnes = kOmega + 2 * 256 * D * 2;
-  static constexpr int kPhiK = kOnes + kOnesBytes;                  // also the masked A tile
-  static constexpr int kPhiQ = kPhiK + 2 * kAtom;                   // also the output staging tile
-  // bf16 copy of G: V columns as an MN-major tile [feature][64 columns] (GsA),
-  // the normaliser column as a K-major block [m/64][16 rows][128 B] (GsB,
-  // rows 1..15 zero)
-  static constexpr int kGs = kPhiQ + 2 * kAtom;
-  static constexpr int kGsB = kGs + 256 * 128;
-  static constexpr int kK = kGsB + 4 * 16 * 128;
+  static constexpr int kKGRows = kBM + D + 16;                      // phi(K) tokens, then G_s columns
+  static constexpr int kKGAtom = kKGRows * 128;
+  static constexpr int kOmega = 0;                                  // fp16 image, up to 256 x D
+  static constexpr int kK = kOmega + 256 * D * 2;
   static constexpr int kQ = kK + kTileBytes;
   static constexpr int kV = kQ + kTileBytes;
-  static constexpr int kNorm = kV + kTileBytes;                     // [2 chunks][K, Q][128] floats
+  static constexpr int kOnes = kV + kTileBytes;                     // above the V tile
+  static constexpr int kKG = kOnes + kAtom;                         // [2 atoms][kKGRows][128 B]
+  static constexpr int kPhiQ = kKG + 2 * kKGAtom;                   // [2 atoms][128][128 B]
+  static constexpr int kMA = kPhiQ + 2 * kAtom;                     // masked A; also the output staging tile
+  static constexpr int kNorm = kMA + 2 * kAtom;                     // [2 chunks][K, Q][128] floats
   static constexpr int kBars = kNorm + 2 * 2 * kBM * 4;
   static constexpr int kSmem = kBars + 512 + 1024;
 };
 
-template <int D>
+template <int D, int M>
 __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_constant__ CUtensorMap mapQ,
                                                                    const __grid_constant__ CUtensorMap mapK,
                                                                    const __grid_constant__ CUtensorMap mapV,
                                                                    const __grid_constant__ CUtensorMap mapO,
                                                                    CausalParams prm) {
   using C = CausalCfg<D>;
+  constexpr int NFB = M / kFB;
+  constexpr int GN = D + 16;                    // columns of G and of [V | 1]
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* b = reinterpret_cast<uint64_t*>(sm + C::kBars);
   uint64_t *k_full = b + 0, *q_full = b + 1, *v_full = b + 2, *k_empty = b + 3, *q_empty = b + 4, *v_empty = b + 5;
-  // knorm_full / qnorm_full: [chunk parity]; gs_full, gdone: [feature block], so that
-  // each completes once per chunk and no waiter can fall two phases behind
-  uint64_t *knorm_full = b + 6, *qnorm_full = b + 8, *setup_bar = b + 10, *done_bar = b + 11;
-  uint64_t *pk_full = b + 12, *phik_full = b + 13, *pq_full = b + 14, *phiq_full = b + 15, *gs_full = b + 16;
-  uint64_t *gdone = b + 18, *phik_free = b + 20, *phiq_free = b + 21, *a_full = b + 22, *as_full = b + 23;
-  uint64_t *o_full = b + 24, *o_free = b + 25;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b + 26);
+  uint64_t *kn_full = b + 6, *qn_full = b + 8;                       // [chunk parity]
+  uint64_t *pk_full = b + 10, *pq_full = b + 11, *x_free = b + 12;
+  uint64_t *kg_full = b + 13, *phiq_full = b + 14, *kg_free = b + 15, *phiq_free = b + 16;
+  uint64_t *gdone = b + 17;                                          // [feature block]
+  uint64_t *a_full = b + 19, *as_full = b + 20, *o_full = b + 21, *o_free = b + 22;
+  uint64_t *setup_bar = b + 23, *done_bar = b + 24;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b + 25);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-#ifdef FAVOR_WAIT_DIAG
-  if (threadIdx.x == 0 && blockIdx.x + blockIdx.y == 0) g_favor_wait_diag[255][0] = (int)(smem_addr(b) >> 3);
-#endif
   float* norms = reinterpret_cast<float*>(sm + C::kNorm);   // [c&1][K=0/Q=1][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sc = blockIdx.x, bh = blockIdx.y;
-  const int m = prm.m, n_fb = m / kFB;
   const int n_tiles_total = (prm.L + kBM - 1) / kBM;
   const int tile0 = sc * prm.tiles_per_sc;
   const int n_chunks = min(prm.tiles_per_sc, n_tiles_total - tile0);
   const WaitCtx wctx{abort_flag, prm.status};
-  // TMEM columns: X (projection), A (chunk scores), O, then G_fb at G_COL + fb * (D + 16)
-  const uint32_t X_COL = 0, A_COL = 128, O_COL = 256, G_COL = 336;
+  // TMEM columns: X (one projection block), A (chunk scores) and O side by
+  // side, then G_fb at G_COL + fb * GN
+  constexpr uint32_t X_COL = 0, A_COL = 128, O_COL = 256, G_COL = 336;
 
   if (threadIdx.x == 0) {
-    mbar_init(k_full, 1);
-    mbar_init(q_full, 1);
-    mbar_init(v_full, 1);
-    mbar_init(k_empty, 2);          // MMA commit + norm warp
-    mbar_init(q_empty, 2);
-    mbar_init(v_empty, 1);
+    for (int i = 0; i < 6; ++i) mbar_init(&b[i], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&knorm_full[i], 1);
-      mbar_init(&qnorm_full[i], 1);
+      mbar_init(&kn_full[i], kNormWarps);
+      mbar_init(&qn_full[i], kNormWarps);
       mbar_init(&gdone[i], 1);
-      mbar_init(&gs_full[i], kEpiWarps);
     }
-    mbar_init(setup_bar, 1);
-    mbar_init(done_bar, 1);
     mbar_init(pk_full, 1);
-    mbar_init(phik_full, kEpiWarps);
     mbar_init(pq_full, 1);
+    mbar_init(x_free, kEpiWarps);
+    mbar_init(kg_full, kEpiWarps);
     mbar_init(phiq_full, kEpiWarps);
-    mbar_init(phik_free, 1);
+    mbar_init(kg_free, 1);
     mbar_init(phiq_free, 1);
     mbar_init(a_full, 1);
     mbar_init(as_full, kEpiWarps);
     mbar_init(o_full, 1);
     mbar_init(o_free, kEpiWarps);
+    mbar_init(setup_bar, 1);
+    mbar_init(done_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -810,8 +877,8 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (warp >= 3) {
-    fill_ones(sm + C::kOnes, 96, kEpiThreads);
+  if (warp >= 4) {
+    fill_ones_block(sm + C::kOnes, kEpiTid0, kEpiThreads);
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -825,8 +892,8 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
       prefetch_tmap(&mapK);
       prefetch_tmap(&mapV);
       prefetch_tmap(&mapO);
-      mbar_arrive_expect_tx(setup_bar, 2 * m * D * 2);
-      bulk_load(sm + C::kOmega, prm.omega_img, 2 * m * D * 2, setup_bar);
+      mbar_arrive_expect_tx(setup_bar, M * D * 2);
+      bulk_load(sm + C::kOmega, prm.omega_img, M * D * 2, setup_bar);
       int issued = 0;
       for (int c = 0; c < n_chunks; ++c) {
         const int row = (tile0 + c) * kBM;
@@ -850,120 +917,116 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t id_proj = idesc_bf16(kBM, kFB, false, false);
-      const uint32_t id_state = idesc_bf16(kFB, D, true, true);
-      const uint32_t id_ones_mn = idesc_bf16(kFB, 16, true, false);
-      const uint32_t id_a = idesc_bf16(kBM, kBM, false, false);
-      const uint32_t id_av = idesc_bf16(kBM, D, false, true);
-      const uint32_t id_aones = idesc_bf16(kBM, 16, false, false);
+      constexpr uint32_t id_proj = idesc_f16(kBM, kFB, false, false);
+      constexpr uint32_t id_g = idesc_bf16(kFB, GN, true, true);
+      constexpr uint32_t id_ao = idesc_bf16(kBM, kBM + GN, false, false);
+      constexpr uint32_t id_oi = idesc_bf16(kBM, GN, false, true);
       const uint32_t om_a = smem_addr(sm + C::kOmega), ones_a = smem_addr(sm + C::kOnes);
-      const uint32_t phik_a = smem_addr(sm + C::kPhiK), phiq_a = smem_addr(sm + C::kPhiQ);
-      const uint32_t gs_a = smem_addr(sm + C::kGs), gsb_a = smem_addr(sm + C::kGsB);
-      const uint32_t k_a = smem_addr(sm + C::kK), q_a = smem_addr(sm + C::kQ);
-      const uint32_t v_a = smem_addr(sm + C::kV);
+      const uint32_t k_a = smem_addr(sm + C::kK), q_a = smem_addr(sm + C::kQ), v_a = smem_addr(sm + C::kV);
+      const uint32_t kg_a = smem_addr(sm + C::kKG), phiq_a = smem_addr(sm + C::kPhiQ);
+      const uint32_t ma_a = smem_addr(sm + C::kMA);
       bool ok = mbar_wait(setup_bar, 0, wctx);
-      // P_K(c, fb) -> X.  X is free once the phi(Q) block before it was read;
-      // the first block of chunk c + 1 is issued before chunk c's masked tile
-      // is awaited, so that projection overlaps the tail of chunk c.
-      auto issue_pk = [&](int c, int fb) -> bool {
-        const int u = c * n_fb + fb;
-        if (fb == 0 && !mbar_wait(k_full, c & 1, wctx)) return false;
-        if (u >= 1 && !mbar_wait(phiq_full, (u - 1) & 1, wctx)) return false;
+      const int U = n_chunks * NFB;
+      // X is written by one projection at a time: P_K(u) after the epilogue
+      // copied P_Q(u-1) out, P_Q(u) after it copied P_K(u) out
+      auto pk = [&](int u) -> bool {
+        const int c = u / NFB, fb = u % NFB;
+        if (u >= 1 && !mbar_wait(x_free, (2 * u - 1) & 1, wctx)) return false;
+        if (fb == 0 && !mbar_wait(&kn_full[c & 1], (c >> 1) & 1, wctx)) return false;
         tc_fence_after();
-        const uint32_t om_hi = om_a + fb * kFB * D * 2, om_lo = om_a + (m + fb * kFB) * D * 2;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          mma_bf16(tmem + X_COL, kmajor(k_a, k), kmajor(om_hi, k), id_proj, k > 0);
-          mma_bf16(tmem + X_COL, kmajor(k_a, k), kmajor(om_lo, k), id_proj, true);
-        }
+#pragma unroll 1
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16(tmem + X_COL, kmajor(k_a, k), omega_desc(om_a, M, fb * kFB, k), id_proj, k > 0);
         mma_commit(pk_full);
-        if (fb == n_fb - 1) mma_commit(k_empty);
+        if (fb == NFB - 1) mma_commit(k_empty);
         return true;
       };
-      if (ok && n_chunks > 0) ok = issue_pk(0, 0);
-      for (int c = 0; ok && c < n_chunks; ++c) {
-        for (int fb = 0; ok && fb < n_fb; ++fb) {
-          const int u = c * n_fb + fb;
-          const uint32_t om_hi = om_a + fb * kFB * D * 2, om_lo = om_a + (m + fb * kFB) * D * 2;
-          if (fb > 0 && !issue_pk(c, fb)) { ok = false; break; }
-          // P_Q -> X
-          if (!mbar_wait(phik_full, u & 1, wctx)) { ok = false; break; }
-          if (fb == 0 && !mbar_wait(q_full, c & 1, wctx)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            mma_bf16(tmem + X_COL, kmajor(q_a, k), kmajor(om_hi, k), id_proj, k > 0);
-            mma_bf16(tmem + X_COL, kmajor(q_a, k), kmajor(om_lo, k), id_proj, true);
-          }
-          mma_commit(pq_full);
-          if (fb == n_fb - 1) mma_commit(q_empty);
-          // G_fb += phi(K)_fb^T [V | 1]   (after G_fb was copied to G_s,fb)
-          if (!mbar_wait(&gs_full[fb], c & 1, wctx)) { ok = false; break; }
-          if (fb == 0 && !mbar_wait(v_full, c & 1, wctx)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t g_tm = tmem + G_COL + fb * (D + 16);
-#pragma unroll
-          for (int k = 0; k < kBM / 16; ++k) {
-            mma_bf16(g_tm, mnmajor(phik_a, k), mnmajor(v_a, k), id_state, true);
-            mma_bf16(g_tm + D, mnmajor(phik_a, k), ones_desc(ones_a, k), id_ones_mn, true);
-          }
-          mma_commit(&gdone[fb]);
-          // A += phi(Q)_fb phi(K)_fb^T;  O += phi(Q)_fb G_s,fb
-          if (!mbar_wait(phiq_full, u & 1, wctx)) { ok = false; break; }
-          if (fb == 0 && c >= 1 && !mbar_wait(o_free, (c - 1) & 1, wctx)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < kFB / 16; ++k) {
-            mma_bf16(tmem + A_COL, kmajor(phiq_a, k), kmajor(phik_a, k), id_a, fb > 0 || k > 0);
-            const uint64_t qd = kmajor(phiq_a, k);
-            mma_bf16(tmem + O_COL, qd, sdesc(gs_a + (fb * kFB + 16 * k) * 128, 32768, 1024), id_av, fb > 0 || k > 0);
-            mma_bf16(tmem + O_COL + D, qd, sdesc(gsb_a + (2 * fb + (k >> 2)) * 2048 + (k & 3) * 32, 16, 1024),
-                     id_aones, fb > 0 || k > 0);
-          }
-          mma_commit(phik_free);
-          mma_commit(phiq_free);
-          if (fb == n_fb - 1) mma_commit(a_full);
-        }
-        if (!ok) break;
-        if (c + 1 < n_chunks && !issue_pk(c + 1, 0)) { ok = false; break; }
-        // O += mask(A) [V | 1]   (the masked A tile sits in the phi(K) buffer)
-        if (!mbar_wait(as_full, c & 1, wctx)) { ok = false; break; }
+      auto pq = [&](int u) -> bool {
+        const int c = u / NFB, fb = u % NFB;
+        if (!mbar_wait(x_free, (2 * u) & 1, wctx)) return false;
+        if (fb == 0 && !mbar_wait(&qn_full[c & 1], (c >> 1) & 1, wctx)) return false;
         tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < kBM / 16; ++k) {
-          mma_bf16(tmem + O_COL, kmajor(phik_a, k), mnmajor(v_a, k), id_av, true);
-          mma_bf16(tmem + O_COL + D, kmajor(phik_a, k), ones_desc(ones_a, k), id_aones, true);
-        }
+#pragma unroll 1
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16(tmem + X_COL, kmajor(q_a, k), omega_desc(om_a, M, fb * kFB, k), id_proj, k > 0);
+        mma_commit(pq_full);
+        if (fb == NFB - 1) mma_commit(q_empty);
+        return true;
+      };
+      // G_fb += phi(K)_fb^T [V | 1]
+      auto gup = [&](int u) -> bool {
+        const int c = u / NFB, fb = u % NFB;
+        if (!mbar_wait(kg_full, u & 1, wctx)) return false;
+        if (fb == 0 && !mbar_wait(v_full, c & 1, wctx)) return false;
+        tc_fence_after();
+#pragma unroll 1
+        for (int k = 0; k < kBM / 16; ++k)
+          mma_bf16(tmem + G_COL + fb * GN, mnmajor(kg_a, k, C::kKGAtom), v_ones(v_a, ones_a, k), id_g, true);
+        mma_commit(&gdone[fb]);
+        return true;
+      };
+      // [A | O] += phi(Q)_fb [phi(K)_fb^T | G_s,fb]
+      auto ao = [&](int u) -> bool {
+        const int c = u / NFB, fb = u % NFB;
+        if (!mbar_wait(phiq_full, u & 1, wctx)) return false;
+        if (fb == 0 && c >= 1 && !mbar_wait(o_free, (c - 1) & 1, wctx)) return false;
+        tc_fence_after();
+#pragma unroll 1
+        for (int k = 0; k < kFB / 16; ++k)
+          mma_bf16(tmem + A_COL, kmajor(phiq_a, k), kmajor(kg_a, k, C::kKGAtom), id_ao, (fb > 0) || (k > 0));
+        mma_commit(kg_free);
+        mma_commit(phiq_free);
+        if (fb == NFB - 1) mma_commit(a_full);
+        return true;
+      };
+      // O += mask(A) [V | 1]
+      auto oi = [&](int c) -> bool {
+        if (!mbar_wait(as_full, c & 1, wctx)) return false;
+        tc_fence_after();
+#pragma unroll 1
+        for (int k = 0; k < kBM / 16; ++k)
+          mma_bf16(tmem + O_COL, kmajor(ma_a, k), v_ones(v_a, ones_a, k), id_oi, true);
         mma_commit(o_full);
         mma_commit(v_empty);
+        return true;
+      };
+      if (ok && U >= 1) ok = pk(0);
+      for (int u = 0; ok && u < U; ++u) {
+        if (!pq(u) || !gup(u)) { ok = false; break; }
+        if (u + 1 < U && !pk(u + 1)) { ok = false; break; }
+        if (!ao(u)) { ok = false; break; }
+        if (u % NFB == NFB - 1 && !oi(u / NFB)) { ok = false; break; }
       }
       mma_commit(done_bar);
       mbar_wait(done_bar, 0, wctx);
     }
-  } else if (warp == 2) {
-    // squared row norms of K_c and Q_c (double-buffered by chunk parity)
+  } else if (warp < 2 + kNormWarps) {
+    // squared row norms of K_c and Q_c (double-buffered by chunk parity);
+    // both tiles rewritten as fp16
     for (int c = 0; c < n_chunks; ++c) {
       float* nk = norms + (c & 1) * 2 * kBM;
       if (!mbar_wait(k_full, c & 1, wctx)) break;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) nk[lane + 32 * j] = tile_row_sq<D>(sm + C::kK, lane + 32 * j);
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&knorm_full[c & 1]);
-        mbar_arrive(k_empty);
+      for (int j = 0; j < 2; ++j) {
+        const int r = (warp - 2) * 64 + lane + 32 * j;
+        nk[r] = tile_row_sq_to_f16<D>(sm + C::kK, r);
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&kn_full[c & 1]);
       if (!mbar_wait(q_full, c & 1, wctx)) break;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) nk[kBM + lane + 32 * j] = tile_row_sq<D>(sm + C::kQ, lane + 32 * j);
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&qnorm_full[c & 1]);
-        mbar_arrive(q_empty);
+      for (int j = 0; j < 2; ++j) {
+        const int r = (warp - 2) * 64 + lane + 32 * j;
+        nk[kBM + r] = tile_row_sq_to_f16<D>(sm + C::kQ, r);
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qn_full[c & 1]);
     }
   } else {
     // ---------------- epilogue ----------------
-    const int wg = (warp - 3) >> 2;
+    const int wg = (warp - 4) >> 2;
     const int q = warp & 3;
     const int t = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
@@ -971,180 +1034,160 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
     key_reference(prm.key_ref, prm.m, &R, &W);
     const float c1 = prm.scale * kLog2e;
     const float hs2 = 0.5f * prm.scale * prm.scale;
-    const uint32_t phik_a = smem_addr(sm + C::kPhiK), phiq_a = smem_addr(sm + C::kPhiQ);
-    const uint32_t gsa_a = smem_addr(sm + C::kGs);
-    uint8_t* gsb = sm + C::kGsB;
-    const int col0 = wg * 64;
-    // G columns of this warpgroup: WG0 0..31 and the normaliser d, WG1 32..63
-    // bf16 copy of 32 V columns (n0 .. n0+31) of feature f into GsA
-    auto write_gsa = [&](int f, int n0, const float* x) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int chunk = (n0 >> 3) + c;
-        const float* y = x + 8 * c;
-        st_shared_v4(gsa_a + f * 128 + ((chunk ^ (f & 7)) << 4), pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
-                     pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
-      }
-    };
-    auto write_gsb = [&](int f, float z) {
-      *reinterpret_cast<__nv_bfloat16*>(gsb + (f >> 6) * 2048 + ((f & 63) >> 3) * 16 + (f & 7) * 2) =
-          __float2bfloat16_rn(z);
-    };
-    for (int e = threadIdx.x - 96; e < 4 * 16 * 128 / 16; e += kEpiThreads)
-      *reinterpret_cast<uint4*>(gsb + e * 16) = make_uint4(0u, 0u, 0u, 0u);
-    named_bar(1, kEpiThreads);
+    const uint32_t kg_a = smem_addr(sm + C::kKG), phiq_a = smem_addr(sm + C::kPhiQ);
+    const uint32_t ma_a = smem_addr(sm + C::kMA);
+    uint8_t* kg = sm + C::kKG;
+    const int col0 = wg * 64;                 // this warpgroup's 64 of a block's 128 columns
+    // G columns of this warpgroup: 0..47 or 48..GN-1
+    constexpr int kG0 = 48;
+    const int n0 = wg ? kG0 : 0;
+    const int ng16 = wg ? (GN - kG0) / 16 : kG0 / 16;
     // G_init = sum of the earlier superchunks' states, in superchunk order
-    for (int fb = 0; fb < n_fb; ++fb) {
-      const float* src = prm.partS + (((size_t)bh * n_fb + fb) * max(prm.n_split, 1)) * (D + 1) * kFB;
-      const int f = fb * kFB + t;
-      const int n0 = wg * 32;
-      float x[32];
+    for (int fb = 0; fb < NFB; ++fb) {
+      const float* src = prm.partS + (((size_t)bh * NFB + fb) * max(prm.n_split, 1)) * (D + 1) * kFB;
+      for (int g = 0; g < ng16; ++g) {
+        uint32_t r[16];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float acc = 0.f;
-        for (int p = 0; p < sc; ++p) acc += src[((size_t)p * (D + 1) + n0 + j) * kFB + t];
-        x[j] = acc;
+        for (int j = 0; j < 16; ++j) {
+          const int n = n0 + 16 * g + j;
+          float acc = 0.f;
+          if (n <= D)
+            for (int p = 0; p < sc * prm.sub_per_sc; ++p) acc += src[((size_t)p * (D + 1) + n) * kFB + t];
+          r[j] = __float_as_uint(acc);
+        }
+        tmem_st16(tmem + lane_off + G_COL + fb * GN + n0 + 16 * g, r);
       }
-      write_gsa(f, n0, x);
-      uint32_t r[16];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(x[16 * h + j]);
-        tmem_st16(tmem + lane_off + G_COL + fb * (D + 16) + n0 + 16 * h, r);
-      }
-      if (wg == 0) {
-        float z = 0.f;
-        for (int p = 0; p < sc; ++p) z += src[((size_t)p * (D + 1) + D) * kFB + t];
-        write_gsb(f, z);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(z);
-        tmem_st16(tmem + lane_off + G_COL + fb * (D + 16) + D, r);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&gs_full[fb]);
     }
+    tmem_st_wait();
     bool ok = true;
-    for (int c = 0; c < n_chunks; ++c) {
-      const int row = (tile0 + c) * kBM + t;
-      const bool valid = row < prm.L;
-      const float* nk = norms + (c & 1) * 2 * kBM;
-      float bias_q = 0.f;
-      for (int fb = 0; fb < n_fb; ++fb) {
-        const int u = c * n_fb + fb;
-        // phi(K)_fb from X
-        if (ok) ok = mbar_wait(pk_full, u & 1, wctx);
-        if (ok && fb == 0) ok = mbar_wait(&knorm_full[c & 1], (c >> 1) & 1, wctx);
-        if (ok && u >= 1) ok = mbar_wait(phik_free, (u - 1) & 1, wctx);
-        tc_fence_after();
-        if (ok) {
-          const float bias_k = (hs2 * nk[t] + R) * kLog2e;
-          uint32_t p0[32], p1[32];
-          tmem_ld32(tmem + lane_off + X_COL + col0, p0);
-          tmem_ld32(tmem + lane_off + X_COL + col0 + 32, p1);
-          tmem_ld_wait();
-          write_row32<0>(phik_a, t, col0, p0, c1, bias_k, valid);
-          write_row32<0>(phik_a, t, col0 + 32, p1, c1, bias_k, valid);
-        }
-        tc_fence_before();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(phik_full);
-        // G_s,fb <- bf16(G_fb) of the previous chunk
-        if (c >= 1) {
-          // G_fb of the previous chunk is final; with one feature block the
-          // previous reader of G_s,fb (O MMA) is waited for here, with two it
-          // was waited for by the phi(Q) step of the block before
-          if (ok) ok = mbar_wait(&gdone[fb], (c - 1) & 1, wctx);
-          if (ok && n_fb == 1) ok = mbar_wait(phiq_free, (u - 1) & 1, wctx);
-          tc_fence_after();
-          if (ok) {
-            uint32_t v[32], z[16];
-            tmem_ld32(tmem + lane_off + G_COL + fb * (D + 16) + wg * 32, v);
-            if (wg == 0) tmem_ld16(tmem + lane_off + G_COL + fb * (D + 16) + D, z);
-            tmem_ld_wait();
-            write_gsa(fb * kFB + t, wg * 32, reinterpret_cast<const float*>(v));
-            if (wg == 0) write_gsb(fb * kFB + t, __uint_as_float(z[0]));
-          }
-          tc_fence_before();
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&gs_full[fb]);
-        }
-        // phi(Q)_fb from X
-        if (ok) ok = mbar_wait(pq_full, u & 1, wctx);
-        tc_fence_after();
-        if (fb == 0) {
-          // the staging tile (phi(Q) buffer) has been read by the previous store
-          if (c >= 1 && threadIdx.x == 96) bulk_wait_read0();
-          named_bar(1, kEpiThreads);
-          if (ok) ok = mbar_wait(&qnorm_full[c & 1], (c >> 1) & 1, wctx);
-          bias_q = (prm.scale * W * sqrtf(nk[kBM + t]) - kQueryHeadroom) * kLog2e;
-        }
-        if (ok && u >= 1) ok = mbar_wait(phiq_free, (u - 1) & 1, wctx);
-        if (ok) {
-          uint32_t p0[32], p1[32];
-          tmem_ld32(tmem + lane_off + X_COL + col0, p0);
-          tmem_ld32(tmem + lane_off + X_COL + col0 + 32, p1);
-          tmem_ld_wait();
-          write_row32<0>(phiq_a, t, col0, p0, c1, bias_q, true);
-          write_row32<0>(phiq_a, t, col0 + 32, p1, c1, bias_q, true);
-        }
-        tc_fence_before();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(phiq_full);
-      }
-      // masked A -> bf16 (phi(K) buffer)
-      if (ok) ok = mbar_wait(a_full, c & 1, wctx);
+    auto out = [&](int j) {
+      const bool have = ok && mbar_wait(o_full, j & 1, wctx);
       tc_fence_after();
-      if (ok) {
-        uint32_t p0[32], p1[32];
-        tmem_ld32(tmem + lane_off + A_COL + col0, p0);
-        tmem_ld32(tmem + lane_off + A_COL + col0 + 32, p1);
-        tmem_ld_wait();
-        write_row32<1>(phik_a, t, col0, p0, 0.f, 0.f, true);
-        write_row32<1>(phik_a, t, col0 + 32, p1, 0.f, 0.f, true);
-      }
-      tc_fence_before();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(as_full);
-      // O / normaliser -> staging (phi(Q) buffer) -> TMA store
-      const bool have = ok && mbar_wait(o_full, c & 1, wctx);
-      ok = ok && have;
-      tc_fence_after();
-      uint32_t v[32], z[16];
-      if (have) {
-        tmem_ld32(tmem + lane_off + O_COL + wg * 32, v);
-        tmem_ld16(tmem + lane_off + O_COL + D, z);
-        tmem_ld_wait();
-      }
+      uint32_t v[32], z[8];
+      tmem_ld32(tmem + lane_off + O_COL + wg * 32, v);
+      tmem_ld8(tmem + lane_off + O_COL + D, z);
+      tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free);
       const float den = have ? __uint_as_float(z[0]) : 1.f;
-      if (have && valid && (!(den > 0.f) || !isfinite(den))) report_status(prm.status, FAVOR_ERR_NONFINITE);
+      if (have && (tile0 + j) * kBM + t < prm.L && (!(den > 0.f) || !isfinite(den)))
+        report_status(prm.status, FAVOR_ERR_NONFINITE);
       const float inv = 1.0f / den;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         const int chunk = wg * 4 + cc;
-        const float* x = reinterpret_cast<const float*>(v) + cc * 8;
-        st_shared_v4(phiq_a + t * 128 + ((chunk ^ (t & 7)) << 4), pack_bf16(x[0] * inv, x[1] * inv),
-                     pack_bf16(x[2] * inv, x[3] * inv), pack_bf16(x[4] * inv, x[5] * inv),
-                     pack_bf16(x[6] * inv, x[7] * inv));
+        const int o = cc * 8;
+        st_shared_v4(ma_a + t * 128 + ((chunk ^ (t & 7)) << 4),
+                     pack_bf16(__uint_as_float(v[o]) * inv, __uint_as_float(v[o + 1]) * inv),
+                     pack_bf16(__uint_as_float(v[o + 2]) * inv, __uint_as_float(v[o + 3]) * inv),
+                     pack_bf16(__uint_as_float(v[o + 4]) * inv, __uint_as_float(v[o + 5]) * inv),
+                     pack_bf16(__uint_as_float(v[o + 6]) * inv, __uint_as_float(v[o + 7]) * inv));
       }
       fence_proxy_async_smem();
       named_bar(1, kEpiThreads);
-      if (threadIdx.x == 96 && have && !*abort_flag) {
-        tma_store_3d(&mapO, 0, (tile0 + c) * kBM, bh, sm + C::kPhiQ);
+      if (threadIdx.x == kEpiTid0 && have && !*abort_flag) {
+        tma_store_3d(&mapO, 0, (tile0 + j) * kBM, bh, sm + C::kMA);
         bulk_commit();
       }
+    };
+    float bias_q = 0.f;
+    for (int c = 0; c < n_chunks; ++c) {
+      const bool valid = (tile0 + c) * kBM + t < prm.L;
+      const float* nk = norms + (c & 1) * 2 * kBM;
+      for (int fb = 0; fb < NFB; ++fb) {
+        const int u = c * NFB + fb;
+        // ---- phi(K)_fb and G_s,fb ----
+        if (ok) ok = mbar_wait(pk_full, u & 1, wctx);
+        if (ok && fb == 0) ok = mbar_wait(&kn_full[c & 1], (c >> 1) & 1, wctx);
+        tc_fence_after();
+        {
+          // loaded even after a failed wait (the kernel is then aborting and the
+          // values are dropped): a conditional load keeps both paths' registers live
+          uint32_t x[64];
+          tmem_ld64(tmem + lane_off + X_COL + col0, x);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(x_free);
+          if (ok) exp_pack<64>(x, c1, (hs2 * nk[t] + R) * kLog2e, valid);
+          if (ok && u >= 1) ok = mbar_wait(kg_free, (u - 1) & 1, wctx);
+          if (ok && c >= 1) ok = mbar_wait(&gdone[fb], (c - 1) & 1, wctx);
+          tc_fence_after();
+          if (ok) store_row<32>(kg_a, C::kKGAtom, t, col0, x);
+        }
+        if (ok) {
+          // G_s,fb: row 128 + n, column t (this lane's feature)
+          uint8_t* gs = kg + (t >> 6) * C::kKGAtom + (t & 7) * 2;
+          const int fchunk = (t & 63) >> 3;
+          for (int g = 0; g < ng16; ++g) {
+            uint32_t r[16];
+            tmem_ld16(tmem + lane_off + G_COL + fb * GN + n0 + 16 * g, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = n0 + 16 * g + j;
+              *reinterpret_cast<__nv_bfloat16*>(gs + (kBM + n) * 128 + ((fchunk ^ (n & 7)) << 4)) =
+                  __float2bfloat16_rn(__uint_as_float(r[j]));
+            }
+          }
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(kg_full);
+        // the previous chunk's output, deferred so that its MMAs overlap
+        if (fb == 0 && c >= 1) out(c - 1);
+        // ---- phi(Q)_fb ----
+        if (ok) ok = mbar_wait(pq_full, u & 1, wctx);
+        if (ok && fb == 0) {
+          ok = mbar_wait(&qn_full[c & 1], (c >> 1) & 1, wctx);
+          bias_q = (prm.scale * W * sqrtf(nk[kBM + t]) - kQueryHeadroom) * kLog2e;
+        }
+        tc_fence_after();
+        {
+          // loaded even after a failed wait (the kernel is then aborting and the
+          // values are dropped): a conditional load keeps both paths' registers live
+          uint32_t x[64];
+          tmem_ld64(tmem + lane_off + X_COL + col0, x);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(x_free);
+          if (ok) exp_pack<64>(x, c1, bias_q, true);
+          if (ok && u >= 1) ok = mbar_wait(phiq_free, (u - 1) & 1, wctx);
+          if (ok) store_row<32>(phiq_a, kAtom, t, col0, x);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(phiq_full);
+      }
+      // ---- masked A -> bf16 (the staging tile of the previous store) ----
+      if (ok) ok = mbar_wait(a_full, c & 1, wctx);
+      tc_fence_after();
+      {
+        uint32_t a[64];
+        tmem_ld64(tmem + lane_off + A_COL + col0, a);
+        tmem_ld_wait();
+        tc_fence_before();
+        if (threadIdx.x == kEpiTid0 && c >= 1) bulk_wait_read0();
+        named_bar(1, kEpiThreads);
+        if (ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int f = col0 + 2 * j;
+            a[j] = pack_bf16(f <= t ? __uint_as_float(a[2 * j]) : 0.f,
+                             f + 1 <= t ? __uint_as_float(a[2 * j + 1]) : 0.f);
+          }
+          store_row<32>(ma_a, kAtom, t, col0, a);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(as_full);
     }
-    if (threadIdx.x == 96) bulk_wait0();
+    if (n_chunks >= 1) out(n_chunks - 1);
+    if (threadIdx.x == kEpiTid0) bulk_wait0();
     mbar_wait(done_bar, 0, wctx);
   }
   tc_fence_before();
@@ -1184,7 +1227,7 @@ bool make_map(CUtensorMap* map, const void* base, const Shape& s) {
   return r == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, int M>
 cudaError_t launch_state(const void* K, const void* V, const Shape& s, const TcPlan& p, float scale, char* ws,
                          int32_t* status, cudaStream_t stream) {
   if (p.n_split < 1) return cudaSuccess;
@@ -1204,14 +1247,14 @@ cudaError_t launch_state(const void* K, const void* V, const Shape& s, const TcP
   prm.merge = p.causal ? 0 : 1;
   prm.scale = scale;
   const size_t smem = StateCfg<D>::kSmem;
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(state_kernel<D>), smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(state_kernel<D, M>), smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_split, p.n_fb, s.BH());
-  state_kernel<D><<<grid, kStateThreads, smem, stream>>>(mk, mv, prm);
+  dim3 grid(p.n_split, s.BH());
+  state_kernel<D, M><<<grid, kStateThreads, smem, stream>>>(mk, mv, prm);
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, int M>
 cudaError_t launch_output(const void* Q, void* O, const Shape& s, const TcPlan& p, float scale, char* ws,
                           int32_t* status, cudaStream_t stream) {
   CUtensorMap mq, mo;
@@ -1226,14 +1269,14 @@ cudaError_t launch_output(const void* Q, void* O, const Shape& s, const TcPlan& 
   prm.tiles_per_cta = p.out_tiles_per_cta;
   prm.scale = scale;
   const size_t smem = OutCfg<D>::kSmem;
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(output_kernel<D>), smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(output_kernel<D, M>), smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.out_ctas, s.BH());
-  output_kernel<D><<<grid, kOutThreads, smem, stream>>>(mq, mo, prm);
+  output_kernel<D, M><<<grid, kOutThreads, smem, stream>>>(mq, mo, prm);
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, int M>
 cudaError_t launch_causal(const void* Q, const void* K, const void* V, void* O, const Shape& s, const TcPlan& p,
                           float scale, char* ws, int32_t* status, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mo;
@@ -1248,12 +1291,13 @@ cudaError_t launch_causal(const void* Q, const void* K, const void* V, void* O, 
   prm.m = s.m;
   prm.n_split = p.n_split;
   prm.tiles_per_sc = p.out_tiles_per_cta;
+  prm.sub_per_sc = p.sub_per_sc;
   prm.scale = scale;
   const size_t smem = CausalCfg<D>::kSmem;
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(causal_kernel<D>), smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(causal_kernel<D, M>), smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.out_ctas, s.BH());
-  causal_kernel<D><<<grid, kCausalThreads, smem, stream>>>(mq, mk, mv, mo, prm);
+  causal_kernel<D, M><<<grid, kCausalThreads, smem, stream>>>(mq, mk, mv, mo, prm);
   return cudaGetLastError();
 }
 
@@ -1275,18 +1319,23 @@ cudaError_t tc_state(bool causal, const void* K, const void* V, const float* ome
                               reinterpret_cast<uint8_t*>(w + p.off_omega_img), stream);
   if (e != cudaSuccess) return e;
   if (!causal) {
-    e = cudaMemsetAsync(w + p.off_counters, 0, (size_t)s.BH() * p.n_fb * sizeof(uint32_t), stream);
+    e = cudaMemsetAsync(w + p.off_counters, 0, (size_t)s.BH() * sizeof(uint32_t), stream);
     if (e != cudaSuccess) return e;
   }
-  return launch_state<64>(K, V, s, p, scale, w, status, stream);
+  return s.m == 256 ? launch_state<64, 256>(K, V, s, p, scale, w, status, stream)
+                    : launch_state<64, 128>(K, V, s, p, scale, w, status, stream);
 }
 
 cudaError_t tc_output(bool causal, const void* Q, const void* K, const void* V, void* O, const float* omega,
                       float scale, const Shape& s, void* ws, int32_t* status, cudaStream_t stream) {
   (void)omega;
   const TcPlan p = tc_plan(causal, s);
-  if (causal) return launch_causal<64>(Q, K, V, O, s, p, scale, static_cast<char*>(ws), status, stream);
-  return launch_output<64>(Q, O, s, p, scale, static_cast<char*>(ws), status, stream);
+  char* w = static_cast<char*>(ws);
+  if (causal)
+    return s.m == 256 ? launch_causal<64, 256>(Q, K, V, O, s, p, scale, w, status, stream)
+                      : launch_causal<64, 128>(Q, K, V, O, s, p, scale, w, status, stream);
+  return s.m == 256 ? launch_output<64, 256>(Q, O, s, p, scale, w, status, stream)
+                    : launch_output<64, 128>(Q, O, s, p, scale, w, status, stream);
 }
 
 }  // namespace favor
@@ -1295,5 +1344,18 @@ cudaError_t tc_output(bool causal, const void* Q, const void* K, const void* V, 
 // Diagnostic builds only: copies the per-warp records of timed-out waits.
 extern "C" int favor_debug_wait_diag(int* out) {
   return (int)cudaMemcpyFromSymbol(out, favor::tc::g_favor_wait_diag, sizeof(int) * 256 * 4);
+}
+#endif
+
+#ifdef FAVOR_TRACE
+// Diagnostic builds only: reset and copy the wait log of block (0, 0, 0).
+extern "C" int favor_debug_trace_reset() {
+  int zero[16] = {0};
+  return (int)cudaMemcpyToSymbol(favor::tc::g_favor_trace_n, zero, sizeof(zero));
+}
+extern "C" int favor_debug_trace(void* recs, int* counts) {
+  cudaError_t e = cudaMemcpyFromSymbol(counts, favor::tc::g_favor_trace_n, sizeof(int) * 16);
+  if (e != cudaSuccess) return (int)e;
+  return (int)cudaMemcpyFromSymbol(recs, favor::tc::g_favor_trace, sizeof(favor::tc::g_favor_trace));
 }
 #endif

@@ -73,12 +73,46 @@ struct WaitCtx {
   int32_t* status;            // caller's device status (nullable)
 };
 
+#ifdef FAVOR_TRACE
+// Diagnostic builds only: every completed wait of lane 0 of each warp of
+// block (0, 0, 0) is logged as (clock at entry, clock at completion, barrier
+// shared-memory address, parity), so that a kernel's timeline can be rebuilt.
+constexpr int kTraceMax = 4096;
+struct TraceRec {
+  unsigned long long t0, t1;
+  unsigned bar, parity;
+};
+__device__ int g_favor_trace_n[16];
+__device__ TraceRec g_favor_trace[16][kTraceMax];
+__device__ __forceinline__ void trace_wait(uint32_t bar, uint32_t parity, unsigned long long t0) {
+  if ((threadIdx.x & 31) == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+    const int w = threadIdx.x >> 5;
+    const int n = g_favor_trace_n[w]++;
+    if (n < kTraceMax) g_favor_trace[w][n] = TraceRec{t0, static_cast<unsigned long long>(clock64()), bar, parity};
+  }
+}
+#define FAVOR_TRACE_DONE(a, parity, t0) trace_wait(a, parity, t0)
+#else
+#define FAVOR_TRACE_DONE(a, parity, t0) ((void)(t0))
+#endif
+
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& ctx) {
   const uint32_t a = smem_addr(bar);
-  if (mbar_try_wait(a, parity)) return true;
+#ifdef FAVOR_TRACE
+  const unsigned long long tt0 = clock64();
+#else
+  const unsigned long long tt0 = 0;
+#endif
+  if (mbar_try_wait(a, parity)) {
+    FAVOR_TRACE_DONE(a, parity, tt0);
+    return true;
+  }
   const uint64_t t0 = global_timer();
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait(a, parity)) {
+      FAVOR_TRACE_DONE(a, parity, tt0);
+      return true;
+    }
     if (*ctx.abort_flag) return false;
     if (global_timer() - t0 > kWaitLimitNs) {
       *ctx.abort_flag = 1;
@@ -183,6 +217,12 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr)
       : "memory");
 }
+// 32 lanes x 8 consecutive 32-bit columns
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 // 32 lanes x 16 consecutive 32-bit columns from registers (same lane rule as loads)
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -221,11 +261,24 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// Instruction descriptor of kind::f16 with fp16 A and B (fp32 D), dense.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // ---- small math -------------------------------------------------------------
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+// Two fp32 -> packed fp16 (lo in the low half), round to nearest, finite
+// values beyond the fp16 range saturate to +-65504.
+__device__ __forceinline__ uint32_t pack_f16_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
