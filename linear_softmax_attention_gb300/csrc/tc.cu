@@ -218,30 +218,30 @@ __device__ __forceinline__ void store_row(uint32_t base, int atom_stride, int t,
   }
 }
 
-// Constant [128 rows][128 B] block, MN-major swizzled: element 0 of every
-// row is 1, the rest 0.  Read as columns d .. d+15 of [V | 1].
+// Constant [16 rows][128 B] block, MN-major swizzled: element 0 of every
+// row is 1, the rest 0.  Read as columns d .. d+15 of [V | 1] by every k-step
+// (each MMA's leading-byte offset points back to it).
+constexpr int kOnesBytes = 16 * 128;
 __device__ __forceinline__ void fill_ones_block(uint8_t* p, int tid0, int nthreads) {
-  for (int e = threadIdx.x - tid0; e < kAtom / 16; e += nthreads) {
+  for (int e = threadIdx.x - tid0; e < kOnesBytes / 16; e += nthreads) {
     const int row = e >> 3, logical = (e & 7) ^ (row & 7);
     *reinterpret_cast<uint4*>(p + e * 16) = make_uint4(logical == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
   }
 }
 
-// MMA descriptors of the fixed layouts
-__device__ __forceinline__ uint64_t kmajor(uint32_t base, int k, int atom_stride = kAtom) {   // K-major, k-step 16
-  return sdesc(base + (k >> 2) * atom_stride + (k & 3) * 32, 16, 1024);
-}
-__device__ __forceinline__ uint64_t mnmajor(uint32_t base, int k, int atom_stride = kAtom) {  // MN-major, 16 rows
-  return sdesc(base + k * 2048, atom_stride, 1024);
-}
-// [V | 1] as an MN-major operand of N = d + 16: V's 64 columns, then the
-// ones block `ones - v` bytes further on
-__device__ __forceinline__ uint64_t v_ones(uint32_t v, uint32_t ones, int k) {
-  return sdesc(v + k * 2048, ones - v, 1024);
-}
-// fp16 Omega image [d/64][m rows][128 B], rows f0 .. : K-major B of the projection
-__device__ __forceinline__ uint64_t omega_desc(uint32_t img, int m, int f0, int k) {
-  return sdesc(img + (k >> 2) * m * 128 + f0 * 128 + (k & 3) * 32, 16, 1024);
+// Descriptor arithmetic.  A descriptor's start-address field holds bytes >> 4
+// in its low bits, so a k-step is an add to the base descriptor built once
+// per MMA group (rebuilding it per MMA costs the issuing thread ~40 issue
+// slots, which halves the MMA rate when epilogue warps share its SMSP).
+__device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+// K-major SW128: k-step k (16 elements) within 64-element atoms `atom` bytes apart
+__host__ __device__ constexpr uint32_t kstep_k(int k, int atom) { return (k >> 2) * atom + (k & 3) * 32; }
+// MN-major SW128: k-step k is 16 rows of 128 B
+__host__ __device__ constexpr uint32_t kstep_mn(int k) { return k * 2048; }
+// [V | 1] at k-step k: start advances by 2048 k, the offset back to the ones
+// block shrinks by the same amount
+__device__ __forceinline__ uint64_t vones_k(uint64_t d0, int k) {
+  return d0 + static_cast<uint64_t>(k * 128) - (static_cast<uint64_t>(k * 128) << 16);
 }
 
 // ---------------------------------------------------------------------------
@@ -270,7 +270,7 @@ struct StateCfg {
   static constexpr int kOmega = 0;                 // fp16 image, up to 256 x D
   static constexpr int kStages = kOmega + 256 * D * 2;
   static constexpr int kOnes = kStages + NS * 2 * kTileBytes;   // above every V tile
-  static constexpr int kPhi = kOnes + kAtom;                     // [fb][2 atoms][128][128 B]
+  static constexpr int kPhi = kOnes + kOnesBytes;                // [fb][2 atoms][128][128 B]
   static constexpr int kNorm = kPhi + 2 * 2 * kAtom;
   static constexpr int kBars = kNorm + NS * kBM * 4;
   static constexpr int kSmem = kBars + 512 + 1024;
@@ -383,19 +383,20 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
           if (i < n_tiles) {
             if (i >= 1 && !mbar_wait(&p_free[fb], (i - 1) & 1, wctx)) { ok = false; break; }
             tc_fence_after();
-#pragma unroll 1
+            const uint64_t a0 = sdesc(k_a, 16, 1024), b0 = sdesc(omega_a + fb * kFB * 128, 16, 1024);
+#pragma unroll
             for (int k = 0; k < D / 16; ++k)
-              mma_bf16(tmem + fb * kFB, kmajor(k_a, k), omega_desc(omega_a, M, fb * kFB, k), id_proj, k > 0);
+              mma_bf16(tmem + fb * kFB, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
             mma_commit(&p_full[fb]);
           }
           if (i >= 1) {
             if (!mbar_wait(&phi_full[fb], (i - 1) & 1, wctx)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t phi_a = smem_addr(sm + C::kPhi + fb * 2 * kAtom);
-#pragma unroll 1
+            const uint64_t a0 = sdesc(smem_addr(sm + C::kPhi + fb * 2 * kAtom), kAtom, 1024);
+            const uint64_t b0 = sdesc(v_a, ones_a - v_a, 1024);
+#pragma unroll
             for (int k = 0; k < kBM / 16; ++k)
-              mma_bf16(tmem + S_COL + fb * 128, mnmajor(phi_a, k), v_ones(v_a, ones_a, k), id_state,
-                       (i > 1) || (k > 0));
+              mma_bf16(tmem + S_COL + fb * 128, dadd(a0, kstep_mn(k)), vones_k(b0, k), id_state, (i > 1) || (k > 0));
             mma_commit(&phi_free[fb]);
           }
         }
@@ -414,6 +415,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
       for (int j = 0; j < 2; ++j) {
         const int r = (warp - 2) * 64 + lane + 32 * j;
         norm_s[st * kBM + r] = tile_row_sq_to_f16<D>(kt, r);
+        FAVOR_TRACE_POINT(10 + j);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -443,13 +445,17 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
         uint32_t x[64];
         tmem_ld64(tmem + lane_off + fb * kFB + col0, x);
         tmem_ld_wait();
+        FAVOR_TRACE_POINT(1);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_free[fb]);
         exp_pack<64>(x, c1, bias, valid);
+        FAVOR_TRACE_POINT(2);
         if (i >= 1 && !mbar_wait(&phi_free[fb], (i - 1) & 1, wctx)) { ok = false; break; }
         store_row<32>(smem_addr(sm + C::kPhi + fb * 2 * kAtom), kAtom, t, col0, x);
+        FAVOR_TRACE_POINT(3);
         fence_proxy_async_smem();
+        FAVOR_TRACE_POINT(4);
         __syncwarp();
         if (lane == 0) mbar_arrive(&phi_full[fb]);
       }
@@ -646,9 +652,10 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
           if (i < n_tiles) {
             if (i >= 1 && !mbar_wait(&p_free[fb], (i - 1) & 1, wctx)) { ok = false; break; }
             tc_fence_after();
-#pragma unroll 1
+            const uint64_t a0 = sdesc(q_a, 16, 1024), b0 = sdesc(omega_a + fb * kFB * 128, 16, 1024);
+#pragma unroll
             for (int k = 0; k < D / 16; ++k)
-              mma_bf16(tmem + fb * kFB, kmajor(q_a, k), omega_desc(omega_a, M, fb * kFB, k), id_proj, k > 0);
+              mma_bf16(tmem + fb * kFB, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
             mma_commit(&p_full[fb]);
             if (fb == NFB - 1) mma_commit(&q_empty[st]);
           }
@@ -656,13 +663,12 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
             if (fb == 0 && i >= 3 && !mbar_wait(&o_free[ob], ((i - 1) >> 1) - 1 & 1, wctx)) { ok = false; break; }
             if (!mbar_wait(&phi_full[fb], (i - 1) & 1, wctx)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t phi_a = smem_addr(sm + C::kPhi + fb * 2 * kAtom);
-#pragma unroll 1
-            for (int kk = 0; kk < kFB / 16; ++kk) {
-              const int g = fb * (kFB / 16) + kk;
-              const uint32_t sa = state_a + (g >> 2) * (D + 16) * 128 + (g & 3) * 32;
-              mma_bf16(tmem + o_col[ob], kmajor(phi_a, kk), sdesc(sa, 16, 1024), id_out, g > 0);
-            }
+            const uint64_t a0 = sdesc(smem_addr(sm + C::kPhi + fb * 2 * kAtom), 16, 1024);
+            const uint64_t b0 = sdesc(state_a + fb * 2 * (D + 16) * 128, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kFB / 16; ++kk)
+              mma_bf16(tmem + o_col[ob], dadd(a0, kstep_k(kk, kAtom)), dadd(b0, kstep_k(kk, (D + 16) * 128)), id_out,
+                       (fb > 0) || (kk > 0));
             mma_commit(&phi_free[fb]);
             if (fb == NFB - 1) mma_commit(&o_full[ob]);
           }
@@ -802,20 +808,21 @@ constexpr int kCausalThreads = 384;   // warps 0 TMA, 1 MMA, 2-3 norms, 4-11 epi
 template <int D>
 struct CausalCfg {
   static constexpr int kTileBytes = D * kBM * 2;
+  static constexpr int kSlots = 4;                                  // ring of K, Q, V tiles
   static constexpr int kKGRows = kBM + D + 16;                      // phi(K) tokens, then G_s columns
   static constexpr int kKGAtom = kKGRows * 128;
   static constexpr int kOmega = 0;                                  // fp16 image, up to 256 x D
-  static constexpr int kK = kOmega + 256 * D * 2;
-  static constexpr int kQ = kK + kTileBytes;
-  static constexpr int kV = kQ + kTileBytes;
-  static constexpr int kOnes = kV + kTileBytes;                     // above the V tile
-  static constexpr int kKG = kOnes + kAtom;                         // [2 atoms][kKGRows][128 B]
+  static constexpr int kRing = kOmega + 256 * D * 2;                // tile x of the sequence K0 Q0 V0 K1 .. in slot x % 4
+  static constexpr int kOnes = kRing + kSlots * kTileBytes;         // above every V tile
+  static constexpr int kKG = kOnes + kOnesBytes;                    // [2 atoms][kKGRows][128 B]
   static constexpr int kPhiQ = kKG + 2 * kKGAtom;                   // [2 atoms][128][128 B]
   static constexpr int kMA = kPhiQ + 2 * kAtom;                     // masked A; also the output staging tile
   static constexpr int kNorm = kMA + 2 * kAtom;                     // [2 chunks][K, Q][128] floats
   static constexpr int kBars = kNorm + 2 * 2 * kBM * 4;
   static constexpr int kSmem = kBars + 512 + 1024;
 };
+static_assert(CausalCfg<64>::kSmem <= 232448, "shared memory");
+static_assert(StateCfg<64>::kSmem <= 232448, "shared memory");
 
 template <int D, int M>
 __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_constant__ CUtensorMap mapQ,
@@ -829,14 +836,14 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* b = reinterpret_cast<uint64_t*>(sm + C::kBars);
-  uint64_t *k_full = b + 0, *q_full = b + 1, *v_full = b + 2, *k_empty = b + 3, *q_empty = b + 4, *v_empty = b + 5;
-  uint64_t *kn_full = b + 6, *qn_full = b + 8;                       // [chunk parity]
-  uint64_t *pk_full = b + 10, *pq_full = b + 11, *x_free = b + 12;
-  uint64_t *kg_full = b + 13, *phiq_full = b + 14, *kg_free = b + 15, *phiq_free = b + 16;
-  uint64_t *gdone = b + 17;                                          // [feature block]
-  uint64_t *a_full = b + 19, *as_full = b + 20, *o_full = b + 21, *o_free = b + 22;
-  uint64_t *setup_bar = b + 23, *done_bar = b + 24;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b + 25);
+  uint64_t *slot_full = b + 0, *slot_free = b + 4;                   // [kSlots]
+  uint64_t *kn_full = b + 8, *qn_full = b + 10;                      // [chunk parity]
+  uint64_t *pk_full = b + 12, *pq_full = b + 13, *x_free = b + 14;
+  uint64_t *kg_full = b + 15, *phiq_full = b + 16, *kg_free = b + 17, *phiq_free = b + 18;
+  uint64_t *gdone = b + 19;                                          // [feature block]
+  uint64_t *a_full = b + 21, *as_full = b + 22, *o_full = b + 23, *o_free = b + 24;
+  uint64_t *setup_bar = b + 25, *done_bar = b + 26;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b + 27);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* norms = reinterpret_cast<float*>(sm + C::kNorm);   // [c&1][K=0/Q=1][128]
 
@@ -851,7 +858,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
   constexpr uint32_t X_COL = 0, A_COL = 128, O_COL = 256, G_COL = 336;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 6; ++i) mbar_init(&b[i], 1);
+    for (int i = 0; i < 2 * C::kSlots; ++i) mbar_init(&b[i], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&kn_full[i], kNormWarps);
       mbar_init(&qn_full[i], kNormWarps);
@@ -894,26 +901,21 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
       prefetch_tmap(&mapO);
       mbar_arrive_expect_tx(setup_bar, M * D * 2);
       bulk_load(sm + C::kOmega, prm.omega_img, M * D * 2, setup_bar);
-      int issued = 0;
-      for (int c = 0; c < n_chunks; ++c) {
-        const int row = (tile0 + c) * kBM;
-        if (c >= 1 && !mbar_wait(k_empty, (c - 1) & 1, wctx)) break;
-        mbar_arrive_expect_tx(k_full, C::kTileBytes);
-        for (int a = 0; a < D / 64; ++a) tma_load_3d(sm + C::kK + a * kAtom, &mapK, a * 64, row, bh, k_full);
-        if (c >= 1 && !mbar_wait(q_empty, (c - 1) & 1, wctx)) break;
-        mbar_arrive_expect_tx(q_full, C::kTileBytes);
-        for (int a = 0; a < D / 64; ++a) tma_load_3d(sm + C::kQ + a * kAtom, &mapQ, a * 64, row, bh, q_full);
-        if (c >= 1 && !mbar_wait(v_empty, (c - 1) & 1, wctx)) break;
-        mbar_arrive_expect_tx(v_full, C::kTileBytes);
-        for (int a = 0; a < D / 64; ++a) tma_load_3d(sm + C::kV + a * kAtom, &mapV, a * 64, row, bh, v_full);
-        issued = c + 1;
+      // tile x = 3c + (0: K, 1: Q, 2: V) of chunk c goes to slot x % 4 once
+      // the tile four places earlier has been consumed
+      const int n_x = 3 * n_chunks;
+      for (int x = 0; x < n_x; ++x) {
+        const int s_ = x % C::kSlots, c = x / 3, kind = x % 3;
+        if (x >= C::kSlots && !mbar_wait(&slot_free[s_], ((x / C::kSlots) - 1) & 1, wctx)) break;
+        mbar_arrive_expect_tx(&slot_full[s_], C::kTileBytes);
+        const CUtensorMap* map = kind == 0 ? &mapK : (kind == 1 ? &mapQ : &mapV);
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_3d(sm + C::kRing + s_ * C::kTileBytes + a * kAtom, map, a * 64, (tile0 + c) * kBM, bh,
+                      &slot_full[s_]);
       }
-      // drain: the loads of the last chunk issued have landed
-      if (issued > 0) {
-        mbar_wait(k_full, (issued - 1) & 1, wctx);
-        mbar_wait(q_full, (issued - 1) & 1, wctx);
-        mbar_wait(v_full, (issued - 1) & 1, wctx);
-      }
+      // drain: the last loads have landed
+      for (int x = max(0, n_x - C::kSlots); x < n_x; ++x)
+        mbar_wait(&slot_full[x % C::kSlots], (x / C::kSlots) & 1, wctx);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -922,7 +924,8 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
       constexpr uint32_t id_ao = idesc_bf16(kBM, kBM + GN, false, false);
       constexpr uint32_t id_oi = idesc_bf16(kBM, GN, false, true);
       const uint32_t om_a = smem_addr(sm + C::kOmega), ones_a = smem_addr(sm + C::kOnes);
-      const uint32_t k_a = smem_addr(sm + C::kK), q_a = smem_addr(sm + C::kQ), v_a = smem_addr(sm + C::kV);
+      const uint32_t ring_a = smem_addr(sm + C::kRing);
+      auto slot_of = [](int c, int kind) { return (3 * c + kind) % C::kSlots; };
       const uint32_t kg_a = smem_addr(sm + C::kKG), phiq_a = smem_addr(sm + C::kPhiQ);
       const uint32_t ma_a = smem_addr(sm + C::kMA);
       bool ok = mbar_wait(setup_bar, 0, wctx);
@@ -934,11 +937,13 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
         if (u >= 1 && !mbar_wait(x_free, (2 * u - 1) & 1, wctx)) return false;
         if (fb == 0 && !mbar_wait(&kn_full[c & 1], (c >> 1) & 1, wctx)) return false;
         tc_fence_after();
-#pragma unroll 1
+        const uint64_t a0 = sdesc(ring_a + slot_of(c, 0) * C::kTileBytes, 16, 1024);
+        const uint64_t b0 = sdesc(om_a + fb * kFB * 128, 16, 1024);
+#pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_bf16(tmem + X_COL, kmajor(k_a, k), omega_desc(om_a, M, fb * kFB, k), id_proj, k > 0);
+          mma_bf16(tmem + X_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
         mma_commit(pk_full);
-        if (fb == NFB - 1) mma_commit(k_empty);
+        if (fb == NFB - 1) mma_commit(&slot_free[slot_of(c, 0)]);
         return true;
       };
       auto pq = [&](int u) -> bool {
@@ -946,22 +951,27 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
         if (!mbar_wait(x_free, (2 * u) & 1, wctx)) return false;
         if (fb == 0 && !mbar_wait(&qn_full[c & 1], (c >> 1) & 1, wctx)) return false;
         tc_fence_after();
-#pragma unroll 1
+        const uint64_t a0 = sdesc(ring_a + slot_of(c, 1) * C::kTileBytes, 16, 1024);
+        const uint64_t b0 = sdesc(om_a + fb * kFB * 128, 16, 1024);
+#pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_bf16(tmem + X_COL, kmajor(q_a, k), omega_desc(om_a, M, fb * kFB, k), id_proj, k > 0);
+          mma_bf16(tmem + X_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
         mma_commit(pq_full);
-        if (fb == NFB - 1) mma_commit(q_empty);
+        if (fb == NFB - 1) mma_commit(&slot_free[slot_of(c, 1)]);
         return true;
       };
       // G_fb += phi(K)_fb^T [V | 1]
       auto gup = [&](int u) -> bool {
         const int c = u / NFB, fb = u % NFB;
         if (!mbar_wait(kg_full, u & 1, wctx)) return false;
-        if (fb == 0 && !mbar_wait(v_full, c & 1, wctx)) return false;
+        const int vs = slot_of(c, 2);
+        if (fb == 0 && !mbar_wait(&slot_full[vs], ((3 * c + 2) / C::kSlots) & 1, wctx)) return false;
         tc_fence_after();
-#pragma unroll 1
+        const uint32_t v_a = ring_a + vs * C::kTileBytes;
+        const uint64_t a0 = sdesc(kg_a, C::kKGAtom, 1024), b0 = sdesc(v_a, ones_a - v_a, 1024);
+#pragma unroll
         for (int k = 0; k < kBM / 16; ++k)
-          mma_bf16(tmem + G_COL + fb * GN, mnmajor(kg_a, k, C::kKGAtom), v_ones(v_a, ones_a, k), id_g, true);
+          mma_bf16(tmem + G_COL + fb * GN, dadd(a0, kstep_mn(k)), vones_k(b0, k), id_g, true);
         mma_commit(&gdone[fb]);
         return true;
       };
@@ -971,9 +981,11 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
         if (!mbar_wait(phiq_full, u & 1, wctx)) return false;
         if (fb == 0 && c >= 1 && !mbar_wait(o_free, (c - 1) & 1, wctx)) return false;
         tc_fence_after();
-#pragma unroll 1
+        const uint64_t a0 = sdesc(phiq_a, 16, 1024), b0 = sdesc(kg_a, 16, 1024);
+#pragma unroll
         for (int k = 0; k < kFB / 16; ++k)
-          mma_bf16(tmem + A_COL, kmajor(phiq_a, k), kmajor(kg_a, k, C::kKGAtom), id_ao, (fb > 0) || (k > 0));
+          mma_bf16(tmem + A_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, C::kKGAtom)), id_ao,
+                   (fb > 0) || (k > 0));
         mma_commit(kg_free);
         mma_commit(phiq_free);
         if (fb == NFB - 1) mma_commit(a_full);
@@ -983,11 +995,13 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
       auto oi = [&](int c) -> bool {
         if (!mbar_wait(as_full, c & 1, wctx)) return false;
         tc_fence_after();
-#pragma unroll 1
+        const uint32_t v_a = ring_a + slot_of(c, 2) * C::kTileBytes;
+        const uint64_t a0 = sdesc(ma_a, 16, 1024), b0 = sdesc(v_a, ones_a - v_a, 1024);
+#pragma unroll
         for (int k = 0; k < kBM / 16; ++k)
-          mma_bf16(tmem + O_COL, kmajor(ma_a, k), v_ones(v_a, ones_a, k), id_oi, true);
+          mma_bf16(tmem + O_COL, dadd(a0, kstep_k(k, kAtom)), vones_k(b0, k), id_oi, true);
         mma_commit(o_full);
-        mma_commit(v_empty);
+        mma_commit(&slot_free[slot_of(c, 2)]);
         return true;
       };
       if (ok && U >= 1) ok = pk(0);
@@ -1005,20 +1019,21 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
     // both tiles rewritten as fp16
     for (int c = 0; c < n_chunks; ++c) {
       float* nk = norms + (c & 1) * 2 * kBM;
-      if (!mbar_wait(k_full, c & 1, wctx)) break;
+      const int ks = (3 * c) % C::kSlots, qs = (3 * c + 1) % C::kSlots;
+      if (!mbar_wait(&slot_full[ks], ((3 * c) / C::kSlots) & 1, wctx)) break;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int r = (warp - 2) * 64 + lane + 32 * j;
-        nk[r] = tile_row_sq_to_f16<D>(sm + C::kK, r);
+        nk[r] = tile_row_sq_to_f16<D>(sm + C::kRing + ks * C::kTileBytes, r);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&kn_full[c & 1]);
-      if (!mbar_wait(q_full, c & 1, wctx)) break;
+      if (!mbar_wait(&slot_full[qs], ((3 * c + 1) / C::kSlots) & 1, wctx)) break;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int r = (warp - 2) * 64 + lane + 32 * j;
-        nk[kBM + r] = tile_row_sq_to_f16<D>(sm + C::kQ, r);
+        nk[kBM + r] = tile_row_sq_to_f16<D>(sm + C::kRing + qs * C::kTileBytes, r);
       }
       fence_proxy_async_smem();
       __syncwarp();

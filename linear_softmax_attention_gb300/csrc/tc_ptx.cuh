@@ -92,8 +92,15 @@ __device__ __forceinline__ void trace_wait(uint32_t bar, uint32_t parity, unsign
   }
 }
 #define FAVOR_TRACE_DONE(a, parity, t0) trace_wait(a, parity, t0)
+// a point event: logged like a wait of zero length on "barrier" 0xF0000000 | id
+#define FAVOR_TRACE_POINT(id)                                                                     \
+  do {                                                                                            \
+    const unsigned long long tp_ = static_cast<unsigned long long>(clock64());                    \
+    trace_wait(0xF0000000u | (id), 0u, tp_);                                                      \
+  } while (0)
 #else
 #define FAVOR_TRACE_DONE(a, parity, t0) ((void)(t0))
+#define FAVOR_TRACE_POINT(id) ((void)0)
 #endif
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& ctx) {
