@@ -207,7 +207,14 @@ def run_gpu(args, rank, world, local_rank):
         sets.append((q, k, v))
     O_b = torch.empty_like(sets[0][0])
     O_c = torch.empty_like(sets[0][0])
-    omega = torch.empty((m, d), dtype=torch.float32, device=dev)
+    # Omega is double-buffered: each step builds the next step's Omega on a
+    # second stream while its own attention kernels (which leave SMs free)
+    # run on the current one; every step builds one Omega and uses one
+    omegas = [torch.empty((m, d), dtype=torch.float32, device=dev) for _ in range(2)]
+    omega = omegas[0]
+    side = torch.cuda.Stream(device=dev)
+    ev_fork = torch.cuda.Event()
+    ev_join = torch.cuda.Event()
     ws_b = favor.new_workspace(False, B, H, L, d, m, dt, device=dev)
     ws_c = favor.new_workspace(True, B, H, L, d, m, dt, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -216,11 +223,18 @@ def run_gpu(args, rank, world, local_rank):
 
     def step(i, seed_call):
         q, k, v = sets[i % n_sets]
-        favor.build_orf(seed_call, omega, stream=stream)
-        favor.bidir_state(k, v, omega, s, ws_b, dev_status=status, stream=stream)
-        favor.bidir_output(q, omega, s, ws_b, O=O_b, dev_status=status, stream=stream)
-        favor.causal_state(k, v, omega, s, ws_c, dev_status=status, stream=stream)
-        favor.causal_output(q, k, v, omega, s, ws_c, O=O_c, dev_status=status, stream=stream)
+        cur, nxt = omegas[i % 2], omegas[(i + 1) % 2]
+        ev_fork.record(stream)
+        side.wait_event(ev_fork)
+        favor.build_orf(seed_call, nxt, stream=side)
+        favor.bidir_state(k, v, cur, s, ws_b, dev_status=status, stream=stream)
+        favor.bidir_output(q, cur, s, ws_b, O=O_b, dev_status=status, stream=stream)
+        favor.causal_state(k, v, cur, s, ws_c, dev_status=status, stream=stream)
+        favor.causal_output(q, k, v, cur, s, ws_c, O=O_c, dev_status=status, stream=stream)
+        ev_join.record(side)
+        stream.wait_event(ev_join)
+
+    favor.build_orf(wl.omega_seed_for_call(w, 0), omegas[0], stream=stream)
 
     # kernels of this library per step: tensor-core path = ORF, prep + state,
     # output, prep + state, causal scan; CUDA-core path = ORF, prep + partial
@@ -229,7 +243,7 @@ def run_gpu(args, rank, world, local_rank):
 
     with torch.cuda.stream(stream):
         for i in range(max(3, args.warmup)):
-            step(i, wl.omega_seed_for_call(w, i))
+            step(i, wl.omega_seed_for_call(w, i + 1))
     torch.cuda.synchronize(dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} after warm-up: "
@@ -238,6 +252,7 @@ def run_gpu(args, rank, world, local_rank):
     # graphs: one per input set (and per Omega seed when Omega is redrawn) for
     # the whole step, and one per stage for the per-kernel durations
     n_graphs = n_sets if not w.redraw_omega else max(n_sets, 4)
+    n_graphs += n_graphs % 2          # graphs alternate the two Omega buffers
     stage_fns = (
         lambda i, q, k, v: favor.build_orf(wl.omega_seed_for_call(w, i), omega, stream=stream),
         lambda i, q, k, v: favor.bidir_state(k, v, omega, s, ws_b, dev_status=status, stream=stream),
@@ -250,7 +265,7 @@ def run_gpu(args, rank, world, local_rank):
         for i in range(n_graphs):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                step(i, wl.omega_seed_for_call(w, i))
+                step(i, wl.omega_seed_for_call(w, i + 1))
             graphs.append(g)
             per = []
             for fn in stage_fns:
@@ -403,6 +418,7 @@ def run_gpu(args, rank, world, local_rank):
                    "step": "build Omega + bidirectional + causal forward", "tokens_per_step": tokens_per_step,
                    "path": favor.path_name(False, d, m, dt), "l2": f"{n_sets} rotating input sets "
                    f"({n_sets * bytes_per_set / 2**20:.0f} MiB > L2)", "timing": "CUDA graph replay per step; per-kernel times from per-stage graphs with events between stages",
+                   "omega": "each step builds the next step's Omega on a second stream (double-buffered) while its attention kernels run",
                    "parallelism": f"replicas x{world}"},
         "modes": {"bidir_tokens_per_s": tokens_per_step / (bidir_ms / 1e3),
                   "causal_tokens_per_s": tokens_per_step / (causal_ms / 1e3),

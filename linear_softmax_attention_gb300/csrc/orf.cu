@@ -39,20 +39,26 @@ __device__ __forceinline__ float group4_sum(float v) {
 
 // One CTA per d x d block; thread (row r = tid/4, part p = tid%4) keeps
 // columns p*CW .. p*CW+CW-1 of row r in registers (CW = ceil(d/4) rounded up
-// to a multiple of 4; columns >= d are zero).  Two Gram–Schmidt sweeps (the
-// second re-orthogonalises, which fp32 needs), then row r is scaled by the
-// length of its own Gaussian vector.  Each step reads the new unit row into
-// registers once and uses four partial sums, so the step latency is a few
-// short dependency chains rather than one CW-long chain per product.
+// to a multiple of 4; columns >= d are zero).
+//
+// Sweep 1 is modified Gram–Schmidt, row by row.  fp32 leaves the rows
+// orthogonal only to about kappa * 2^-24, so a second pass re-orthogonalises
+// them; as the rows are then orthonormal up to that small error E, the pass
+// is one classical step q_r - sum_{s<r} (q_s . q_r) q_s computed for all rows
+// at once, which equals a second modified sweep up to O(E^2).  Finally row r
+// is scaled by the length of its own Gaussian vector.
 template <int CW>
 __global__ void __launch_bounds__(kMaxD * kTPR) orf_block_kernel(uint64_t seed, int m, int d,
                                                                  float* __restrict__ omega) {
-  __shared__ __align__(16) float qbuf[2][kTPR * CW];
+  extern __shared__ __align__(16) float orf_smem[];
+  float* qbuf = orf_smem;                         // [2][kTPR * CW] unit row of the current step
+  float* rows = orf_smem + 2 * kTPR * CW;         // [d][kTPR * CW] all rows after sweep 1
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int r = tid / kTPR;
   const int p = tid % kTPR;
   const bool row_ok = r < d;
+  constexpr int RW = kTPR * CW;                   // floats per stored row
 
   float g[CW];
   float len2 = 0.f;
@@ -69,55 +75,92 @@ __global__ void __launch_bounds__(kMaxD * kTPR) orf_block_kernel(uint64_t seed, 
   }
   const float len = sqrtf(group4_sum(len2));
 
-  // every thread executes every shuffle (full-warp masks); only the values
-  // they carry depend on the thread's role in the step
-  for (int sweep = 0; sweep < 2; ++sweep) {
-    for (int i = 0; i < d; ++i) {
-      float* q = qbuf[i & 1];
-      const bool norm_row = (r == i);
-      float n2[4] = {0.f, 0.f, 0.f, 0.f};
-      if (norm_row) {
+  // ---- sweep 1: modified Gram–Schmidt.  Every thread executes every shuffle
+  // (full-warp masks); only the values they carry depend on the thread's role.
+  for (int i = 0; i < d; ++i) {
+    float* q = qbuf + (i & 1) * RW;
+    const bool norm_row = (r == i);
+    float n2[4] = {0.f, 0.f, 0.f, 0.f};
+    if (norm_row) {
 #pragma unroll
-        for (int k = 0; k < CW; ++k) n2[k & 3] = fmaf(g[k], g[k], n2[k & 3]);
-      }
-      const float nn = group4_sum((n2[0] + n2[1]) + (n2[2] + n2[3]));
-      if (norm_row) {
-        const float inv = 1.0f / sqrtf(nn);
+      for (int k = 0; k < CW; ++k) n2[k & 3] = fmaf(g[k], g[k], n2[k & 3]);
+    }
+    const float nn = group4_sum((n2[0] + n2[1]) + (n2[2] + n2[3]));
+    if (norm_row) {
+      const float inv = rsqrtf(nn);
 #pragma unroll
-        for (int k = 0; k < CW; ++k) {
-          g[k] *= inv;
-          q[p * CW + k] = g[k];
-        }
-      }
-      __syncthreads();
-      const bool upd = row_ok && r > i;
-      float qv[CW];
-      float dp[4] = {0.f, 0.f, 0.f, 0.f};
-      if (upd) {
-#pragma unroll
-        for (int k = 0; k < CW; k += 4) {
-          const float4 v = *reinterpret_cast<const float4*>(q + p * CW + k);
-          qv[k] = v.x;
-          qv[k + 1] = v.y;
-          qv[k + 2] = v.z;
-          qv[k + 3] = v.w;
-        }
-#pragma unroll
-        for (int k = 0; k < CW; ++k) dp[k & 3] = fmaf(qv[k], g[k], dp[k & 3]);
-      }
-      const float dot = group4_sum((dp[0] + dp[1]) + (dp[2] + dp[3]));
-      if (upd) {
-#pragma unroll
-        for (int k = 0; k < CW; ++k) g[k] = fmaf(-dot, qv[k], g[k]);
+      for (int k = 0; k < CW; k += 4) {
+        g[k] *= inv;
+        g[k + 1] *= inv;
+        g[k + 2] *= inv;
+        g[k + 3] *= inv;
+        *reinterpret_cast<float4*>(q + p * CW + k) = make_float4(g[k], g[k + 1], g[k + 2], g[k + 3]);
       }
     }
+    __syncthreads();
+    const bool upd = row_ok && r > i;
+    float qv[CW];
+    float dp[4] = {0.f, 0.f, 0.f, 0.f};
+    if (upd) {
+#pragma unroll
+      for (int k = 0; k < CW; k += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(q + p * CW + k);
+        qv[k] = v.x;
+        qv[k + 1] = v.y;
+        qv[k + 2] = v.z;
+        qv[k + 3] = v.w;
+      }
+#pragma unroll
+      for (int k = 0; k < CW; ++k) dp[k & 3] = fmaf(qv[k], g[k], dp[k & 3]);
+    }
+    const float dot = group4_sum((dp[0] + dp[1]) + (dp[2] + dp[3]));
+    if (upd) {
+#pragma unroll
+      for (int k = 0; k < CW; ++k) g[k] = fmaf(-dot, qv[k], g[k]);
+    }
   }
+
+  // ---- sweep 2: one classical re-orthogonalisation step, all rows at once
+  if (row_ok) {
+#pragma unroll
+    for (int k = 0; k < CW; k += 4)
+      *reinterpret_cast<float4*>(rows + r * RW + p * CW + k) = make_float4(g[k], g[k + 1], g[k + 2], g[k + 3]);
+  }
+  __syncthreads();
+  const int warp_last_row = min(d, (tid / 32 + 1) * (32 / kTPR)) - 1;   // largest row of this warp
+  float corr[CW];
+#pragma unroll
+  for (int k = 0; k < CW; ++k) corr[k] = 0.f;
+  for (int s_ = 0; s_ < warp_last_row; ++s_) {
+    float qv[CW];
+#pragma unroll
+    for (int k = 0; k < CW; k += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(rows + s_ * RW + p * CW + k);
+      qv[k] = v.x;
+      qv[k + 1] = v.y;
+      qv[k + 2] = v.z;
+      qv[k + 3] = v.w;
+    }
+    float dp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < CW; ++k) dp[k & 3] = fmaf(qv[k], g[k], dp[k & 3]);
+    const float c = (row_ok && s_ < r) ? group4_sum((dp[0] + dp[1]) + (dp[2] + dp[3])) : group4_sum(0.f);
+#pragma unroll
+    for (int k = 0; k < CW; ++k) corr[k] = fmaf(c, qv[k], corr[k]);
+  }
+  float n2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < CW; ++k) {
+    g[k] -= corr[k];
+    n2[k & 3] = fmaf(g[k], g[k], n2[k & 3]);
+  }
+  const float inv = rsqrtf(group4_sum((n2[0] + n2[1]) + (n2[2] + n2[3])));
   const int row = b * d + r;
   if (row_ok && row < m) {
 #pragma unroll
     for (int k = 0; k < CW; ++k) {
       const int c = p * CW + k;
-      if (c < d) omega[(size_t)row * d + c] = g[k] * len;
+      if (c < d) omega[(size_t)row * d + c] = g[k] * inv * len;
     }
   }
 }
@@ -137,14 +180,20 @@ cudaError_t launch_build_orf(uint64_t seed, int m, int d, int orthogonal, float*
     const int nb = (m + d - 1) / d;
     const int threads = ((d * kTPR + 31) / 32) * 32;
     const int cw = (d + kTPR - 1) / kTPR;
-    if (cw <= 4)
-      orf_block_kernel<4><<<nb, threads, 0, stream>>>(seed, m, d, omega);
-    else if (cw <= 8)
-      orf_block_kernel<8><<<nb, threads, 0, stream>>>(seed, m, d, omega);
-    else if (cw <= 16)
-      orf_block_kernel<16><<<nb, threads, 0, stream>>>(seed, m, d, omega);
-    else
-      orf_block_kernel<32><<<nb, threads, 0, stream>>>(seed, m, d, omega);
+    // shared memory: two unit rows + all d rows of kTPR * CW floats
+    auto smem_for = [&](int CW) { return (size_t)(2 + d) * kTPR * CW * sizeof(float); };
+    cudaError_t e = cudaSuccess;
+    if (cw <= 4) {
+      orf_block_kernel<4><<<nb, threads, smem_for(4), stream>>>(seed, m, d, omega);
+    } else if (cw <= 8) {
+      orf_block_kernel<8><<<nb, threads, smem_for(8), stream>>>(seed, m, d, omega);
+    } else if (cw <= 16) {
+      orf_block_kernel<16><<<nb, threads, smem_for(16), stream>>>(seed, m, d, omega);
+    } else {
+      e = ensure_dynamic_smem(reinterpret_cast<const void*>(orf_block_kernel<32>), smem_for(32));
+      if (e != cudaSuccess) return e;
+      orf_block_kernel<32><<<nb, threads, smem_for(32), stream>>>(seed, m, d, omega);
+    }
   } else {
     const int n = m * d;
     iid_kernel<<<(n + 255) / 256, 256, 0, stream>>>(seed, m, d, omega);

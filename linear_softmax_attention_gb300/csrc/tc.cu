@@ -307,6 +307,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
   const WaitCtx wctx{abort_flag, prm.status};
   constexpr uint32_t S_COL = 256;              // S~ of block fb at S_COL + 128 fb; P at 0
 
+  FAVOR_TRACE_BEGIN();
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NS; ++i) {
       mbar_init(&full[i], 1);
@@ -369,38 +370,49 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
       const uint32_t omega_a = smem_addr(sm + C::kOmega);
       const uint32_t ones_a = smem_addr(sm + C::kOnes);
       bool ok = mbar_wait(setup_bar, 0, wctx);
-      // per feature block: projection of tile i, then the state update of
-      // tile i-1, so that a block's state MMA never waits behind the other
-      // block's projection (which waits for the epilogue to free P)
-      for (int i = 0; ok && i <= n_tiles; ++i) {
-        const int st = i % C::NS, sp = (i + C::NS - 1) % C::NS;
-        if (i < n_tiles && !mbar_wait(&kn_full[st], (i / C::NS) & 1, wctx)) { ok = false; break; }
-        if (i >= 1 && !mbar_wait(&full[sp], ((i - 1) / C::NS) & 1, wctx)) { ok = false; break; }
-        const uint32_t k_a = smem_addr(sm + C::kStages + st * 2 * C::kTileBytes);
-        const uint32_t v_a = smem_addr(sm + C::kStages + sp * 2 * C::kTileBytes + C::kTileBytes);
-#pragma unroll
-        for (int fb = 0; fb < NFB; ++fb) {
-          if (i < n_tiles) {
-            if (i >= 1 && !mbar_wait(&p_free[fb], (i - 1) & 1, wctx)) { ok = false; break; }
+      // event-driven issue: the next projection step (tile, block) and the
+      // next state step (tile, block) are each issued as soon as their inputs
+      // are ready, projections first
+      Watchdog wd(wctx);
+      int pi = 0, pf = 0, si = 0, sf = 0;
+      while (ok && (pi < n_tiles || si < n_tiles)) {
+        bool progress = false;
+        if (pi < n_tiles) {
+          const int st = pi % C::NS;
+          const bool ready = (pf > 0 || mbar_test_wait(smem_addr(&kn_full[st]), (pi / C::NS) & 1)) &&
+                             (pi == 0 || mbar_test_wait(smem_addr(&p_free[pf]), (pi - 1) & 1));
+          if (ready) {
             tc_fence_after();
-            const uint64_t a0 = sdesc(k_a, 16, 1024), b0 = sdesc(omega_a + fb * kFB * 128, 16, 1024);
+            const uint64_t a0 = sdesc(smem_addr(sm + C::kStages + st * 2 * C::kTileBytes), 16, 1024);
+            const uint64_t b0 = sdesc(omega_a + pf * kFB * 128, 16, 1024);
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
-              mma_bf16(tmem + fb * kFB, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
-            mma_commit(&p_full[fb]);
+              mma_bf16(tmem + pf * kFB, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
+            mma_commit(&p_full[pf]);
+            if (++pf == NFB) { pf = 0; ++pi; }
+            progress = true;
           }
-          if (i >= 1) {
-            if (!mbar_wait(&phi_full[fb], (i - 1) & 1, wctx)) { ok = false; break; }
+        }
+        if (si < n_tiles) {
+          const int st = si % C::NS;
+          const bool ready = mbar_test_wait(smem_addr(&phi_full[sf]), si & 1) &&
+                             (sf > 0 || mbar_test_wait(smem_addr(&full[st]), (si / C::NS) & 1));
+          if (ready) {
             tc_fence_after();
-            const uint64_t a0 = sdesc(smem_addr(sm + C::kPhi + fb * 2 * kAtom), kAtom, 1024);
+            const uint32_t v_a = smem_addr(sm + C::kStages + st * 2 * C::kTileBytes + C::kTileBytes);
+            const uint64_t a0 = sdesc(smem_addr(sm + C::kPhi + sf * 2 * kAtom), kAtom, 1024);
             const uint64_t b0 = sdesc(v_a, ones_a - v_a, 1024);
 #pragma unroll
             for (int k = 0; k < kBM / 16; ++k)
-              mma_bf16(tmem + S_COL + fb * 128, dadd(a0, kstep_mn(k)), vones_k(b0, k), id_state, (i > 1) || (k > 0));
-            mma_commit(&phi_free[fb]);
+              mma_bf16(tmem + S_COL + sf * 128, dadd(a0, kstep_mn(k)), vones_k(b0, k), id_state, (si > 0) || (k > 0));
+            mma_commit(&phi_free[sf]);
+            if (sf == NFB - 1) mma_commit(&empty[st]);
+            if (++sf == NFB) { sf = 0; ++si; }
+            progress = true;
           }
         }
-        if (ok && i >= 1) mma_commit(&empty[sp]);
+        if (progress) wd.progress();
+        else ok = wd.idle();
       }
       mma_commit(done_bar);
       mbar_wait(done_bar, 0, wctx);
@@ -433,6 +445,20 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     const float c1 = prm.scale * kLog2e;
     const float hs2 = 0.5f * prm.scale * prm.scale;
     bool ok = true;
+    // software pipeline over (tile, block) steps: the bf16 features of the
+    // previous step are stored while this step's TMEM load is in flight
+    uint32_t y[32];
+    int prev_i = -1, prev_fb = 0;
+    auto store_prev = [&]() {
+      if (prev_i < 0) return;
+      if (prev_i >= 1 && ok) ok = mbar_wait(&phi_free[prev_fb], (prev_i - 1) & 1, wctx);
+      if (ok) store_row<32>(smem_addr(sm + C::kPhi + prev_fb * 2 * kAtom), kAtom, t, col0, y);
+      FAVOR_TRACE_POINT(3);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&phi_full[prev_fb]);
+      prev_i = -1;
+    };
     for (int i = 0; ok && i < n_tiles; ++i) {
       const int st = i % C::NS;
       if (!mbar_wait(&kn_full[st], (i / C::NS) & 1, wctx)) { ok = false; break; }
@@ -440,10 +466,13 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
       const bool valid = (tile0 + i) * kBM + t < prm.L;
 #pragma unroll
       for (int fb = 0; fb < NFB; ++fb) {
+        // store first if this step's projection is not there yet
+        if (!mbar_try_wait(smem_addr(&p_full[fb]), i & 1)) store_prev();
         if (!mbar_wait(&p_full[fb], i & 1, wctx)) { ok = false; break; }
         tc_fence_after();
         uint32_t x[64];
         tmem_ld64(tmem + lane_off + fb * kFB + col0, x);
+        store_prev();
         tmem_ld_wait();
         FAVOR_TRACE_POINT(1);
         tc_fence_before();
@@ -451,15 +480,13 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
         if (lane == 0) mbar_arrive(&p_free[fb]);
         exp_pack<64>(x, c1, bias, valid);
         FAVOR_TRACE_POINT(2);
-        if (i >= 1 && !mbar_wait(&phi_free[fb], (i - 1) & 1, wctx)) { ok = false; break; }
-        store_row<32>(smem_addr(sm + C::kPhi + fb * 2 * kAtom), kAtom, t, col0, x);
-        FAVOR_TRACE_POINT(3);
-        fence_proxy_async_smem();
-        FAVOR_TRACE_POINT(4);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&phi_full[fb]);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) y[j] = x[j];
+        prev_i = i;
+        prev_fb = fb;
       }
     }
+    store_prev();
     // final state: lane f holds feature f of a block.  Two blocks: warpgroup
     // w reads block w; one block: the warpgroups split the d columns.
     const bool done = mbar_wait(done_bar, 0, wctx);
@@ -516,6 +543,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  FAVOR_TRACE_END();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -584,6 +612,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
   const WaitCtx wctx{abort_flag, prm.status};
   const uint32_t o_col[2] = {256u, 384u};   // O accumulators (d + 16 columns each); P at 0
 
+  FAVOR_TRACE_BEGIN();
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NSQ; ++i) {
       mbar_init(&q_full[i], 1);
@@ -641,38 +670,50 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
       const uint32_t omega_a = smem_addr(sm + C::kOmega);
       const uint32_t state_a = smem_addr(sm + C::kState);
       bool ok = mbar_wait(setup_bar, 0, wctx);
-      // per feature block: projection of tile i, then that block's share of
-      // the output MMA of tile i-1
-      for (int i = 0; ok && i <= n_tiles; ++i) {
-        const int st = i % C::NSQ, ob = (i - 1) & 1;
-        if (i < n_tiles && !mbar_wait(&qn_full[st], (i / C::NSQ) & 1, wctx)) { ok = false; break; }
-        const uint32_t q_a = smem_addr(sm + C::kQ + st * C::kTileBytes);
-#pragma unroll
-        for (int fb = 0; fb < NFB; ++fb) {
-          if (i < n_tiles) {
-            if (i >= 1 && !mbar_wait(&p_free[fb], (i - 1) & 1, wctx)) { ok = false; break; }
+      // event-driven issue: the next projection step (tile, block) and the
+      // next output step (tile, block) are each issued as soon as their
+      // inputs are ready, projections first
+      Watchdog wd(wctx);
+      int pi = 0, pf = 0, oi = 0, of = 0;
+      while (ok && (pi < n_tiles || oi < n_tiles)) {
+        bool progress = false;
+        if (pi < n_tiles) {
+          const int st = pi % C::NSQ;
+          const bool ready = (pf > 0 || mbar_test_wait(smem_addr(&qn_full[st]), (pi / C::NSQ) & 1)) &&
+                             (pi == 0 || mbar_test_wait(smem_addr(&p_free[pf]), (pi - 1) & 1));
+          if (ready) {
             tc_fence_after();
-            const uint64_t a0 = sdesc(q_a, 16, 1024), b0 = sdesc(omega_a + fb * kFB * 128, 16, 1024);
+            const uint64_t a0 = sdesc(smem_addr(sm + C::kQ + st * C::kTileBytes), 16, 1024);
+            const uint64_t b0 = sdesc(omega_a + pf * kFB * 128, 16, 1024);
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
-              mma_bf16(tmem + fb * kFB, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
-            mma_commit(&p_full[fb]);
-            if (fb == NFB - 1) mma_commit(&q_empty[st]);
+              mma_bf16(tmem + pf * kFB, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
+            mma_commit(&p_full[pf]);
+            if (pf == NFB - 1) mma_commit(&q_empty[st]);
+            if (++pf == NFB) { pf = 0; ++pi; }
+            progress = true;
           }
-          if (i >= 1) {
-            if (fb == 0 && i >= 3 && !mbar_wait(&o_free[ob], ((i - 1) >> 1) - 1 & 1, wctx)) { ok = false; break; }
-            if (!mbar_wait(&phi_full[fb], (i - 1) & 1, wctx)) { ok = false; break; }
+        }
+        if (oi < n_tiles) {
+          const int ob = oi & 1;
+          const bool ready = mbar_test_wait(smem_addr(&phi_full[of]), oi & 1) &&
+                             (of > 0 || oi < 2 || mbar_test_wait(smem_addr(&o_free[ob]), ((oi >> 1) - 1) & 1));
+          if (ready) {
             tc_fence_after();
-            const uint64_t a0 = sdesc(smem_addr(sm + C::kPhi + fb * 2 * kAtom), 16, 1024);
-            const uint64_t b0 = sdesc(state_a + fb * 2 * (D + 16) * 128, 16, 1024);
+            const uint64_t a0 = sdesc(smem_addr(sm + C::kPhi + of * 2 * kAtom), 16, 1024);
+            const uint64_t b0 = sdesc(state_a + of * 2 * (D + 16) * 128, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < kFB / 16; ++kk)
               mma_bf16(tmem + o_col[ob], dadd(a0, kstep_k(kk, kAtom)), dadd(b0, kstep_k(kk, (D + 16) * 128)), id_out,
-                       (fb > 0) || (kk > 0));
-            mma_commit(&phi_free[fb]);
-            if (fb == NFB - 1) mma_commit(&o_full[ob]);
+                       (of > 0) || (kk > 0));
+            mma_commit(&phi_free[of]);
+            if (of == NFB - 1) mma_commit(&o_full[ob]);
+            if (++of == NFB) { of = 0; ++oi; }
+            progress = true;
           }
         }
+        if (progress) wd.progress();
+        else ok = wd.idle();
       }
       mma_commit(done_bar);
       mbar_wait(done_bar, 0, wctx);
@@ -778,6 +819,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  FAVOR_TRACE_END();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -857,6 +899,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
   // side, then G_fb at G_COL + fb * GN
   constexpr uint32_t X_COL = 0, A_COL = 128, O_COL = 256, G_COL = 336;
 
+  FAVOR_TRACE_BEGIN();
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2 * C::kSlots; ++i) mbar_init(&b[i], 1);
     for (int i = 0; i < 2; ++i) {
@@ -1208,6 +1251,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  FAVOR_TRACE_END();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 

@@ -50,6 +50,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe: true once the phase with this parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 #ifdef FAVOR_WAIT_DIAG
 // Diagnostic builds only: the first wait of each warp that ran out records
 // (shared-memory offset of the barrier >> 3, parity, warp, block).
@@ -84,13 +97,30 @@ struct TraceRec {
 };
 __device__ int g_favor_trace_n[16];
 __device__ TraceRec g_favor_trace[16][kTraceMax];
+// per-warp record counts of the traced block live in shared memory (a global
+// counter would add a load round trip to every event)
+__device__ __forceinline__ int* trace_counts() {
+  __shared__ int s_trace_n[16];
+  return s_trace_n;
+}
+__device__ __forceinline__ bool trace_block() { return blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0; }
 __device__ __forceinline__ void trace_wait(uint32_t bar, uint32_t parity, unsigned long long t0) {
-  if ((threadIdx.x & 31) == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+  if ((threadIdx.x & 31) == 0 && trace_block()) {
+    const unsigned long long t1 = static_cast<unsigned long long>(clock64());
     const int w = threadIdx.x >> 5;
-    const int n = g_favor_trace_n[w]++;
-    if (n < kTraceMax) g_favor_trace[w][n] = TraceRec{t0, static_cast<unsigned long long>(clock64()), bar, parity};
+    const int n = trace_counts()[w]++;
+    if (n < kTraceMax) g_favor_trace[w][n] = TraceRec{t0, t1, bar, parity};
   }
 }
+// kernel entry (before the first block-wide barrier) and exit (after the last)
+#define FAVOR_TRACE_BEGIN()                                              \
+  do {                                                                   \
+    if (threadIdx.x < 16) trace_counts()[threadIdx.x] = 0;               \
+  } while (0)
+#define FAVOR_TRACE_END()                                                \
+  do {                                                                   \
+    if (threadIdx.x < 16 && trace_block()) g_favor_trace_n[threadIdx.x] = trace_counts()[threadIdx.x]; \
+  } while (0)
 #define FAVOR_TRACE_DONE(a, parity, t0) trace_wait(a, parity, t0)
 // a point event: logged like a wait of zero length on "barrier" 0xF0000000 | id
 #define FAVOR_TRACE_POINT(id)                                                                     \
@@ -101,6 +131,8 @@ __device__ __forceinline__ void trace_wait(uint32_t bar, uint32_t parity, unsign
 #else
 #define FAVOR_TRACE_DONE(a, parity, t0) ((void)(t0))
 #define FAVOR_TRACE_POINT(id) ((void)0)
+#define FAVOR_TRACE_BEGIN() ((void)0)
+#define FAVOR_TRACE_END() ((void)0)
 #endif
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& ctx) {
@@ -131,6 +163,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
   }
 }
+
+// Watchdog of an event-driven loop (several barriers probed in turn): call
+// progress() after each issued step and idle() when nothing was ready; idle()
+// returns false once the kernel aborts or no step was ready for the wait limit.
+struct Watchdog {
+  const WaitCtx& ctx;
+  uint64_t t_last;
+  __device__ explicit Watchdog(const WaitCtx& c) : ctx(c), t_last(global_timer()) {}
+  __device__ void progress() { t_last = global_timer(); }
+  __device__ bool idle() {
+    if (*ctx.abort_flag) return false;
+    if (global_timer() - t_last > kWaitLimitNs) {
+      *ctx.abort_flag = 1;
+      report_status(ctx.status, FAVOR_ERR_TIMEOUT);
+      return false;
+    }
+    return true;
+  }
+};
 
 // ---- fences -----------------------------------------------------------------
 // generic-proxy writes to shared memory -> visible to the async proxy (TMA, MMA)
