@@ -973,86 +973,92 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
       const uint32_t ma_a = smem_addr(sm + C::kMA);
       bool ok = mbar_wait(setup_bar, 0, wctx);
       const int U = n_chunks * NFB;
-      // X is written by one projection at a time: P_K(u) after the epilogue
-      // copied P_Q(u-1) out, P_Q(u) after it copied P_K(u) out
-      auto pk = [&](int u) -> bool {
-        const int c = u / NFB, fb = u % NFB;
-        if (u >= 1 && !mbar_wait(x_free, (2 * u - 1) & 1, wctx)) return false;
-        if (fb == 0 && !mbar_wait(&kn_full[c & 1], (c >> 1) & 1, wctx)) return false;
-        tc_fence_after();
-        const uint64_t a0 = sdesc(ring_a + slot_of(c, 0) * C::kTileBytes, 16, 1024);
-        const uint64_t b0 = sdesc(om_a + fb * kFB * 128, 16, 1024);
+      auto ready = [](uint64_t* bar, int parity) { return mbar_test_wait(smem_addr(bar), parity & 1); };
+      // Event-driven issue over five step kinds of u = (chunk, block): P_K(u)
+      // and P_Q(u) share X (P_K(u) after the epilogue copied P_Q(u-1) out,
+      // P_Q(u) after it copied P_K(u) out); G(u) after phi(K)_u and G_s are in
+      // the KG slot; [A|O](u) after G(u) and phi(Q)_u; O += mask(A) V after the
+      // chunk's last [A|O] and the masked tile.  Each kind is probed only once
+      // its predecessor has been issued, so no barrier can be two phases ahead.
+      Watchdog wd(wctx);
+      int npk = 0, npq = 0, ng = 0, nao = 0, noi = 0;
+      while (ok && noi < n_chunks) {
+        bool progress = false;
+        if (npk < U && npq == npk) {
+          const int c = npk / NFB, fb = npk % NFB;
+          if ((npk == 0 || ready(x_free, 1)) && (fb != 0 || ready(&kn_full[c & 1], c >> 1))) {
+            tc_fence_after();
+            const uint64_t a0 = sdesc(ring_a + slot_of(c, 0) * C::kTileBytes, 16, 1024);
+            const uint64_t b0 = sdesc(om_a + fb * kFB * 128, 16, 1024);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_bf16(tmem + X_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
-        mma_commit(pk_full);
-        if (fb == NFB - 1) mma_commit(&slot_free[slot_of(c, 0)]);
-        return true;
-      };
-      auto pq = [&](int u) -> bool {
-        const int c = u / NFB, fb = u % NFB;
-        if (!mbar_wait(x_free, (2 * u) & 1, wctx)) return false;
-        if (fb == 0 && !mbar_wait(&qn_full[c & 1], (c >> 1) & 1, wctx)) return false;
-        tc_fence_after();
-        const uint64_t a0 = sdesc(ring_a + slot_of(c, 1) * C::kTileBytes, 16, 1024);
-        const uint64_t b0 = sdesc(om_a + fb * kFB * 128, 16, 1024);
+            for (int k = 0; k < D / 16; ++k)
+              mma_bf16(tmem + X_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
+            mma_commit(pk_full);
+            if (fb == NFB - 1) mma_commit(&slot_free[slot_of(c, 0)]);
+            ++npk;
+            progress = true;
+          }
+        }
+        if (npq < npk) {
+          const int c = npq / NFB, fb = npq % NFB;
+          if (ready(x_free, 0) && (fb != 0 || ready(&qn_full[c & 1], c >> 1))) {
+            tc_fence_after();
+            const uint64_t a0 = sdesc(ring_a + slot_of(c, 1) * C::kTileBytes, 16, 1024);
+            const uint64_t b0 = sdesc(om_a + fb * kFB * 128, 16, 1024);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_bf16(tmem + X_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
-        mma_commit(pq_full);
-        if (fb == NFB - 1) mma_commit(&slot_free[slot_of(c, 1)]);
-        return true;
-      };
-      // G_fb += phi(K)_fb^T [V | 1]
-      auto gup = [&](int u) -> bool {
-        const int c = u / NFB, fb = u % NFB;
-        if (!mbar_wait(kg_full, u & 1, wctx)) return false;
-        const int vs = slot_of(c, 2);
-        if (fb == 0 && !mbar_wait(&slot_full[vs], ((3 * c + 2) / C::kSlots) & 1, wctx)) return false;
-        tc_fence_after();
-        const uint32_t v_a = ring_a + vs * C::kTileBytes;
-        const uint64_t a0 = sdesc(kg_a, C::kKGAtom, 1024), b0 = sdesc(v_a, ones_a - v_a, 1024);
+            for (int k = 0; k < D / 16; ++k)
+              mma_bf16(tmem + X_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
+            mma_commit(pq_full);
+            if (fb == NFB - 1) mma_commit(&slot_free[slot_of(c, 1)]);
+            ++npq;
+            progress = true;
+          }
+        }
+        if (ng < npk) {
+          const int c = ng / NFB, fb = ng % NFB;
+          const int vs = slot_of(c, 2);
+          if (ready(kg_full, ng) && (fb != 0 || ready(&slot_full[vs], (3 * c + 2) / C::kSlots))) {
+            tc_fence_after();
+            const uint32_t v_a = ring_a + vs * C::kTileBytes;
+            const uint64_t a0 = sdesc(kg_a, C::kKGAtom, 1024), b0 = sdesc(v_a, ones_a - v_a, 1024);
 #pragma unroll
-        for (int k = 0; k < kBM / 16; ++k)
-          mma_bf16(tmem + G_COL + fb * GN, dadd(a0, kstep_mn(k)), vones_k(b0, k), id_g, true);
-        mma_commit(&gdone[fb]);
-        return true;
-      };
-      // [A | O] += phi(Q)_fb [phi(K)_fb^T | G_s,fb]
-      auto ao = [&](int u) -> bool {
-        const int c = u / NFB, fb = u % NFB;
-        if (!mbar_wait(phiq_full, u & 1, wctx)) return false;
-        if (fb == 0 && c >= 1 && !mbar_wait(o_free, (c - 1) & 1, wctx)) return false;
-        tc_fence_after();
-        const uint64_t a0 = sdesc(phiq_a, 16, 1024), b0 = sdesc(kg_a, 16, 1024);
+            for (int k = 0; k < kBM / 16; ++k)
+              mma_bf16(tmem + G_COL + fb * GN, dadd(a0, kstep_mn(k)), vones_k(b0, k), id_g, true);
+            mma_commit(&gdone[fb]);
+            ++ng;
+            progress = true;
+          }
+        }
+        if (nao < ng && nao < npq) {
+          const int c = nao / NFB, fb = nao % NFB;
+          if (ready(phiq_full, nao) && (fb != 0 || c == 0 || ready(o_free, c - 1))) {
+            tc_fence_after();
+            const uint64_t a0 = sdesc(phiq_a, 16, 1024), b0 = sdesc(kg_a, 16, 1024);
 #pragma unroll
-        for (int k = 0; k < kFB / 16; ++k)
-          mma_bf16(tmem + A_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, C::kKGAtom)), id_ao,
-                   (fb > 0) || (k > 0));
-        mma_commit(kg_free);
-        mma_commit(phiq_free);
-        if (fb == NFB - 1) mma_commit(a_full);
-        return true;
-      };
-      // O += mask(A) [V | 1]
-      auto oi = [&](int c) -> bool {
-        if (!mbar_wait(as_full, c & 1, wctx)) return false;
-        tc_fence_after();
-        const uint32_t v_a = ring_a + slot_of(c, 2) * C::kTileBytes;
-        const uint64_t a0 = sdesc(ma_a, 16, 1024), b0 = sdesc(v_a, ones_a - v_a, 1024);
+            for (int k = 0; k < kFB / 16; ++k)
+              mma_bf16(tmem + A_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, C::kKGAtom)), id_ao,
+                       (fb > 0) || (k > 0));
+            mma_commit(kg_free);
+            mma_commit(phiq_free);
+            if (fb == NFB - 1) mma_commit(a_full);
+            ++nao;
+            progress = true;
+          }
+        }
+        if ((noi + 1) * NFB <= nao && ready(as_full, noi)) {
+          tc_fence_after();
+          const uint32_t v_a = ring_a + slot_of(noi, 2) * C::kTileBytes;
+          const uint64_t a0 = sdesc(ma_a, 16, 1024), b0 = sdesc(v_a, ones_a - v_a, 1024);
 #pragma unroll
-        for (int k = 0; k < kBM / 16; ++k)
-          mma_bf16(tmem + O_COL, dadd(a0, kstep_k(k, kAtom)), vones_k(b0, k), id_oi, true);
-        mma_commit(o_full);
-        mma_commit(&slot_free[slot_of(c, 2)]);
-        return true;
-      };
-      if (ok && U >= 1) ok = pk(0);
-      for (int u = 0; ok && u < U; ++u) {
-        if (!pq(u) || !gup(u)) { ok = false; break; }
-        if (u + 1 < U && !pk(u + 1)) { ok = false; break; }
-        if (!ao(u)) { ok = false; break; }
-        if (u % NFB == NFB - 1 && !oi(u / NFB)) { ok = false; break; }
+          for (int k = 0; k < kBM / 16; ++k)
+            mma_bf16(tmem + O_COL, dadd(a0, kstep_k(k, kAtom)), vones_k(b0, k), id_oi, true);
+          mma_commit(o_full);
+          mma_commit(&slot_free[slot_of(noi, 2)]);
+          ++noi;
+          progress = true;
+        }
+        if (progress) wd.progress();
+        else ok = wd.idle();
       }
       mma_commit(done_bar);
       mbar_wait(done_bar, 0, wctx);
