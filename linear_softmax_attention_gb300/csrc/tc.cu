@@ -512,30 +512,46 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
       }
     }
     tc_fence_before();
+    FAVOR_TRACE_POINT(20);
     if (prm.merge) {
       named_bar(1, kEpiThreads);
+      FAVOR_TRACE_POINT(21);
       if (threadIdx.x == kEpiTid0) {
         __threadfence();
         const uint32_t old = atomicAdd(&prm.counters[bh], 1u);
         *is_last = (old == (uint32_t)(prm.n_split - 1)) ? 1 : 0;
       }
       named_bar(1, kEpiThreads);
+      FAVOR_TRACE_POINT(22);
       if (*is_last) {
         __threadfence();
+        FAVOR_TRACE_POINT(23);
         uint8_t* img = prm.state_img + (size_t)bh * M * (D + 16) * 2;
-        const int n0 = wg * ((D + 16) / 2), n1 = n0 + (D + 16) / 2;
-        for (int b = 0; b < NFB; ++b) {
-          const float* src = prm.partS + (((size_t)bh * NFB + b) * prm.n_split) * (D + 1) * kFB;
-          const int f = b * kFB + t;
-          const int atom = f >> 6, cc = f & 63;
-          for (int n = n0; n < n1; ++n) {
-            float acc = 0.f;
-            if (n <= D)
-              for (int p = 0; p < prm.n_split; ++p) acc += src[((size_t)p * (D + 1) + n) * kFB + t];
-            const size_t off = ((size_t)atom * (D + 16) + n) * 128 + (((cc >> 3) ^ (n & 7)) << 4) + (cc & 7) * 2;
-            *reinterpret_cast<__nv_bfloat16*>(img + off) = __float2bfloat16_rn(acc);
+        // item = (block b, state row n, 4 consecutive features): one float4 per
+        // split, summed in split order, stored as 4 bf16 (8 bytes) of the image
+        constexpr int NG = kFB / 4;
+        constexpr int kItems = NFB * (D + 16) * NG;
+        const float* base = prm.partS + (size_t)bh * NFB * prm.n_split * (D + 1) * kFB;
+#pragma unroll 4
+        for (int e = threadIdx.x - kEpiTid0; e < kItems; e += kEpiThreads) {
+          const int g = e % NG, n = (e / NG) % (D + 16), b = e / (NG * (D + 16));
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (n <= D) {
+            const float* src = base + ((size_t)b * prm.n_split * (D + 1) + n) * kFB + g * 4;
+            for (int p = 0; p < prm.n_split; ++p) {
+              const float4 v = *reinterpret_cast<const float4*>(src + (size_t)p * (D + 1) * kFB);
+              acc.x += v.x;
+              acc.y += v.y;
+              acc.z += v.z;
+              acc.w += v.w;
+            }
           }
+          const int f = b * kFB + g * 4;
+          const int atom = f >> 6, cc = f & 63;
+          const size_t off = ((size_t)atom * (D + 16) + n) * 128 + (((cc >> 3) ^ (n & 7)) << 4) + (cc & 7) * 2;
+          *reinterpret_cast<uint2*>(img + off) = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
         }
+        FAVOR_TRACE_POINT(24);
         if (threadIdx.x == kEpiTid0) prm.counters[bh] = 0;
       }
     }
@@ -1110,15 +1126,20 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
     for (int fb = 0; fb < NFB; ++fb) {
       const float* src = prm.partS + (((size_t)bh * NFB + fb) * max(prm.n_split, 1)) * (D + 1) * kFB;
       for (int g = 0; g < ng16; ++g) {
+        // partials outer, columns inner: the 16 loads of a partial are in flight together
+        float acc[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+        for (int p = 0; p < sc * prm.sub_per_sc; ++p) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int n = n0 + 16 * g + j;
+            if (n <= D) acc[j] += src[((size_t)p * (D + 1) + n) * kFB + t];
+          }
+        }
         uint32_t r[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int n = n0 + 16 * g + j;
-          float acc = 0.f;
-          if (n <= D)
-            for (int p = 0; p < sc * prm.sub_per_sc; ++p) acc += src[((size_t)p * (D + 1) + n) * kFB + t];
-          r[j] = __float_as_uint(acc);
-        }
+        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(acc[j]);
         tmem_st16(tmem + lane_off + G_COL + fb * GN + n0 + 16 * g, r);
       }
     }
@@ -1414,9 +1435,14 @@ extern "C" int favor_debug_wait_diag(int* out) {
 
 #ifdef FAVOR_TRACE
 // Diagnostic builds only: reset and copy the wait log of block (0, 0, 0).
-extern "C" int favor_debug_trace_reset() {
+extern "C" int favor_debug_trace_reset(int target_block) {
   int zero[16] = {0};
+  cudaError_t e = cudaMemcpyToSymbol(favor::tc::g_favor_trace_target, &target_block, sizeof(int));
+  if (e != cudaSuccess) return (int)e;
   return (int)cudaMemcpyToSymbol(favor::tc::g_favor_trace_n, zero, sizeof(zero));
+}
+extern "C" int favor_debug_cta_times(void* out) {
+  return (int)cudaMemcpyFromSymbol(out, favor::tc::g_favor_cta_times, sizeof(favor::tc::g_favor_cta_times));
 }
 extern "C" int favor_debug_trace(void* recs, int* counts) {
   cudaError_t e = cudaMemcpyFromSymbol(counts, favor::tc::g_favor_trace_n, sizeof(int) * 16);

@@ -103,7 +103,10 @@ __device__ __forceinline__ int* trace_counts() {
   __shared__ int s_trace_n[16];
   return s_trace_n;
 }
-__device__ __forceinline__ bool trace_block() { return blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0; }
+__device__ int g_favor_trace_target;   // linear id of the traced block
+__device__ __forceinline__ bool trace_block() {
+  return (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x == g_favor_trace_target;
+}
 __device__ __forceinline__ void trace_wait(uint32_t bar, uint32_t parity, unsigned long long t0) {
   if ((threadIdx.x & 31) == 0 && trace_block()) {
     const unsigned long long t1 = static_cast<unsigned long long>(clock64());
@@ -112,14 +115,21 @@ __device__ __forceinline__ void trace_wait(uint32_t bar, uint32_t parity, unsign
     if (n < kTraceMax) g_favor_trace[w][n] = TraceRec{t0, t1, bar, parity};
   }
 }
+// start and end (%globaltimer) of every block of the traced launch
+__device__ unsigned long long g_favor_cta_times[4096][2];
+__device__ __forceinline__ int trace_block_id() {
+  return (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+}
 // kernel entry (before the first block-wide barrier) and exit (after the last)
 #define FAVOR_TRACE_BEGIN()                                              \
   do {                                                                   \
     if (threadIdx.x < 16) trace_counts()[threadIdx.x] = 0;               \
+    if (threadIdx.x == 0 && trace_block_id() < 4096) g_favor_cta_times[trace_block_id()][0] = global_timer(); \
   } while (0)
 #define FAVOR_TRACE_END()                                                \
   do {                                                                   \
     if (threadIdx.x < 16 && trace_block()) g_favor_trace_n[threadIdx.x] = trace_counts()[threadIdx.x]; \
+    if (threadIdx.x == 0 && trace_block_id() < 4096) g_favor_cta_times[trace_block_id()][1] = global_timer(); \
   } while (0)
 #define FAVOR_TRACE_DONE(a, parity, t0) trace_wait(a, parity, t0)
 // a point event: logged like a wait of zero length on "barrier" 0xF0000000 | id
