@@ -521,46 +521,60 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
         const uint32_t old = atomicAdd(&prm.counters[bh], 1u);
         *is_last = (old == (uint32_t)(prm.n_split - 1)) ? 1 : 0;
       }
-      named_bar(1, kEpiThreads);
-      FAVOR_TRACE_POINT(22);
-      if (*is_last) {
-        __threadfence();
-        FAVOR_TRACE_POINT(23);
-        uint8_t* img = prm.state_img + (size_t)bh * M * (D + 16) * 2;
-        // item = (block b, state row n, 4 consecutive features): one float4 per
-        // split, summed in split order, stored as 4 bf16 (8 bytes) of the image
-        constexpr int NG = kFB / 4;
-        constexpr int kItems = NFB * (D + 16) * NG;
-        const float* base = prm.partS + (size_t)bh * NFB * prm.n_split * (D + 1) * kFB;
-#pragma unroll 4
-        for (int e = threadIdx.x - kEpiTid0; e < kItems; e += kEpiThreads) {
-          const int g = e % NG, n = (e / NG) % (D + 16), b = e / (NG * (D + 16));
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (n <= D) {
-            const float* src = base + ((size_t)b * prm.n_split * (D + 1) + n) * kFB + g * 4;
-            for (int p = 0; p < prm.n_split; ++p) {
-              const float4 v = *reinterpret_cast<const float4*>(src + (size_t)p * (D + 1) * kFB);
-              acc.x += v.x;
-              acc.y += v.y;
-              acc.z += v.z;
-              acc.w += v.w;
-            }
-          }
-          const int f = b * kFB + g * 4;
-          const int atom = f >> 6, cc = f & 63;
-          const size_t off = ((size_t)atom * (D + 16) + n) * 128 + (((cc >> 3) ^ (n & 7)) << 4) + (cc & 7) * 2;
-          *reinterpret_cast<uint2*>(img + off) = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
-        }
-        FAVOR_TRACE_POINT(24);
-        if (threadIdx.x == kEpiTid0) prm.counters[bh] = 0;
-      }
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  FAVOR_TRACE_END();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  // the last CTA of a head adds the splits' partial states (fixed split order)
+  // into the bf16 state image: every thread, eight items' loads in flight per
+  // split.  Item = (block b, state row n, 4 consecutive features).
+  if (prm.merge && *is_last) {
+    __threadfence();
+    FAVOR_TRACE_POINT(23);
+    uint8_t* img = prm.state_img + (size_t)bh * M * (D + 16) * 2;
+    constexpr int NG = kFB / 4;
+    constexpr int kItems = NFB * (D + 16) * NG;
+    constexpr int kBatch = 8;
+    const float* base = prm.partS + (size_t)bh * NFB * prm.n_split * (D + 1) * kFB;
+    for (int e0 = threadIdx.x; e0 < kItems; e0 += kBatch * kStateThreads) {
+      float4 acc[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int p = 0; p < prm.n_split; ++p) {
+        float4 v[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int e = e0 + u * kStateThreads;
+          const int g = e % NG, n = (e / NG) % (D + 16), b = e / (NG * (D + 16));
+          v[u] = (e < kItems && n <= D)
+                     ? *reinterpret_cast<const float4*>(base + (((size_t)b * prm.n_split + p) * (D + 1) + n) * kFB + g * 4)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          acc[u].x += v[u].x;
+          acc[u].y += v[u].y;
+          acc[u].z += v[u].z;
+          acc[u].w += v[u].w;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = e0 + u * kStateThreads;
+        if (e >= kItems) break;
+        const int g = e % NG, n = (e / NG) % (D + 16), b = e / (NG * (D + 16));
+        const int f = b * kFB + g * 4;
+        const int atom = f >> 6, cc = f & 63;
+        const size_t off = ((size_t)atom * (D + 16) + n) * 128 + (((cc >> 3) ^ (n & 7)) << 4) + (cc & 7) * 2;
+        *reinterpret_cast<uint2*>(img + off) = make_uint2(pack_bf16(acc[u].x, acc[u].y), pack_bf16(acc[u].z, acc[u].w));
+      }
+    }
+    FAVOR_TRACE_POINT(24);
+    if (threadIdx.x == 0) prm.counters[bh] = 0;
+  }
+  FAVOR_TRACE_END();
 }
 
 // ---------------------------------------------------------------------------
