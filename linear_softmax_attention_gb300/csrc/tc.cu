@@ -316,8 +316,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 1);
-      mbar_init(&p_free[i], kEpiWarps);
-      mbar_init(&phi_full[i], kEpiWarps);
+      mbar_init(&p_free[i], kEpiWarps / NFB);     // the warps that own block i
+      mbar_init(&phi_full[i], kEpiWarps / NFB);
       mbar_init(&phi_free[i], 1);
     }
     mbar_init(setup_bar, 1);
@@ -445,48 +445,43 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     const float c1 = prm.scale * kLog2e;
     const float hs2 = 0.5f * prm.scale * prm.scale;
     bool ok = true;
-    // software pipeline over (tile, block) steps: the bf16 features of the
-    // previous step are stored while this step's TMEM load is in flight
-    uint32_t y[32];
-    int prev_i = -1, prev_fb = 0;
-    auto store_prev = [&]() {
-      if (prev_i < 0) return;
-      if (prev_i >= 1 && ok) ok = mbar_wait(&phi_free[prev_fb], (prev_i - 1) & 1, wctx);
-      if (ok) store_row<32>(smem_addr(sm + C::kPhi + prev_fb * 2 * kAtom), kAtom, t, col0, y);
-      FAVOR_TRACE_POINT(3);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&phi_full[prev_fb]);
-      prev_i = -1;
-    };
+    // m = 256: warpgroup w owns feature block w (128 columns in two passes),
+    // so the two warps of an SMSP work on different blocks and fall out of
+    // step (one exponentiates while the other loads or stores).  m = 128:
+    // the warpgroups split the block's columns.
+    const int my_fb = (NFB == 2) ? wg : 0;
+    constexpr int kPasses = (NFB == 2) ? 2 : 1;
+    const int c0 = (NFB == 2) ? 0 : col0;
+    const uint32_t phi_a = smem_addr(sm + C::kPhi + my_fb * 2 * kAtom);
     for (int i = 0; ok && i < n_tiles; ++i) {
       const int st = i % C::NS;
       if (!mbar_wait(&kn_full[st], (i / C::NS) & 1, wctx)) { ok = false; break; }
-      const float bias = (hs2 * norm_s[st * kBM + t] + R) * kLog2e;
+      // rows past L get 2^-inf = 0
       const bool valid = (tile0 + i) * kBM + t < prm.L;
+      const float bias = valid ? (hs2 * norm_s[st * kBM + t] + R) * kLog2e : INFINITY;
+      if (!mbar_wait(&p_full[my_fb], i & 1, wctx)) { ok = false; break; }
+      tc_fence_after();
 #pragma unroll
-      for (int fb = 0; fb < NFB; ++fb) {
-        // store first if this step's projection is not there yet
-        if (!mbar_try_wait(smem_addr(&p_full[fb]), i & 1)) store_prev();
-        if (!mbar_wait(&p_full[fb], i & 1, wctx)) { ok = false; break; }
-        tc_fence_after();
+      for (int ps = 0; ps < kPasses; ++ps) {
         uint32_t x[64];
-        tmem_ld64(tmem + lane_off + fb * kFB + col0, x);
-        store_prev();
+        tmem_ld64(tmem + lane_off + my_fb * kFB + c0 + 64 * ps, x);
         tmem_ld_wait();
         FAVOR_TRACE_POINT(1);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_free[fb]);
-        exp_pack<64>(x, c1, bias, valid);
+        if (ps == kPasses - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&p_free[my_fb]);
+        }
+        exp_pack<64>(x, c1, bias, true);
         FAVOR_TRACE_POINT(2);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) y[j] = x[j];
-        prev_i = i;
-        prev_fb = fb;
+        if (ps == 0 && i >= 1 && !mbar_wait(&phi_free[my_fb], (i - 1) & 1, wctx)) { ok = false; break; }
+        store_row<32>(phi_a, kAtom, t, c0 + 64 * ps, x);
+        FAVOR_TRACE_POINT(3);
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&phi_full[my_fb]);
     }
-    store_prev();
     // final state: lane f holds feature f of a block.  Two blocks: warpgroup
     // w reads block w; one block: the warpgroups split the d columns.
     const bool done = mbar_wait(done_bar, 0, wctx);
