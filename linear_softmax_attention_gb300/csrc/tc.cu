@@ -646,8 +646,8 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 1);
-      mbar_init(&p_free[i], kEpiWarps);
-      mbar_init(&phi_full[i], kEpiWarps);
+      mbar_init(&p_free[i], kEpiWarps / NFB);     // the warps that own block i
+      mbar_init(&phi_full[i], kEpiWarps / NFB);
       mbar_init(&phi_free[i], 1);
       mbar_init(&o_full[i], 1);
       mbar_init(&o_free[i], kEpiWarps);
@@ -807,34 +807,40 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
     };
     for (int i = 0; i < n_tiles; ++i) {
       const int st = i % C::NSQ;
-      if (ok) ok = mbar_wait(&p_full[0], i & 1, wctx);
+      const int my_fb = (NFB == 2) ? wg : 0;   // m = 256: warpgroup w owns feature block w
+      if (ok) ok = mbar_wait(&p_full[my_fb], i & 1, wctx);
       if (ok) ok = mbar_wait(&qn_full[st], (i / C::NSQ) & 1, wctx);
       tc_fence_after();
       const float qn = qnorm[st * kBM + t];
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_empty[st]);
       const float bias = (prm.scale * W * sqrtf(qn) - kQueryHeadroom) * kLog2e;
+      // m = 256: two passes of 64 columns over the owned block; m = 128: the
+      // warpgroups split the block's columns
+      constexpr int kPasses = (NFB == 2) ? 2 : 1;
+      const int c0 = (NFB == 2) ? 0 : col0;
+      tc_fence_after();
 #pragma unroll
-      for (int fb = 0; fb < NFB; ++fb) {
-        if (ok && fb > 0) ok = mbar_wait(&p_full[fb], i & 1, wctx);
-        tc_fence_after();
+      for (int ps = 0; ps < kPasses; ++ps) {
         uint32_t x[64];
         if (ok) {
-          tmem_ld64(tmem + lane_off + fb * kFB + col0, x);
+          tmem_ld64(tmem + lane_off + my_fb * kFB + c0 + 64 * ps, x);
           tmem_ld_wait();
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_free[fb]);
+        if (ps == kPasses - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&p_free[my_fb]);
+        }
         if (ok) {
           exp_pack<64>(x, c1, bias, true);
-          if (i >= 1) ok = mbar_wait(&phi_free[fb], (i - 1) & 1, wctx);
-          if (ok) store_row<32>(smem_addr(sm + C::kPhi + fb * 2 * kAtom), kAtom, t, col0, x);
+          if (ps == 0 && i >= 1) ok = mbar_wait(&phi_free[my_fb], (i - 1) & 1, wctx);
+          if (ok) store_row<32>(smem_addr(sm + C::kPhi + my_fb * 2 * kAtom), kAtom, t, c0 + 64 * ps, x);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&phi_full[fb]);
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&phi_full[my_fb]);
       if (i >= 1) store_out(i - 1);
     }
     if (n_tiles >= 1) store_out(n_tiles - 1);
