@@ -26,6 +26,23 @@ cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
   return e;
 }
 
+// Streaming multiprocessors of the current device (cached per device); the
+// workspace plans size their grids by it, so a workspace is planned for the
+// device it is used on.
+int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 }  // namespace favor
 
 namespace {

@@ -111,6 +111,8 @@ favor_status run_call(bool causal, int stage, const void* Q, const void* K, cons
 // that calls made later (including under CUDA graph capture) issue no
 // attribute call.
 cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
+// SM count of the current device (cached).
+int sm_count();
 
 // Row-norm maxima (and optionally the bf16 Omega images) into the workspace.
 cudaError_t launch_prep(const float* omega, int m, int d, float* key_ref, uint8_t* image, cudaStream_t stream);

@@ -370,7 +370,7 @@ SimtPlan simt_plan(bool causal, const Shape& s) {
   const int BH = s.BH();
   p.n_fb = (s.m + kFB - 1) / kFB;
   const int tiles = (s.L + kTT - 1) / kTT;
-  const int target = 2 * 152;
+  const int target = 2 * sm_count();
   int want = causal ? (target + BH - 1) / BH : (target + BH * p.n_fb - 1) / (BH * p.n_fb);
   want = max(1, min(want, tiles));
   const int tiles_per = (tiles + want - 1) / want;

@@ -71,7 +71,6 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // fewest splits minimising waves x (tiles per CTA + per-CTA set-up, counted
 // as kCtaOverheadTiles tiles).
 constexpr int kCtaOverheadTiles = 3;
-constexpr int kSMs = 152;
 int pick_split(int units, int tiles, int sms) {
   int best = 1;
   long best_cost = -1;
@@ -90,18 +89,19 @@ int pick_split(int units, int tiles, int sms) {
 TcPlan tc_plan(bool causal, const Shape& s) {
   TcPlan p{};
   const int BH = s.BH();
+  const int sms = sm_count();
   p.causal = causal;
   p.n_fb = s.m / kFB;
   p.n_tiles = (s.L + kBM - 1) / kBM;
   if (!causal) {
-    const int sp = pick_split(BH, p.n_tiles, kSMs);
+    const int sp = pick_split(BH, p.n_tiles, sms);
     p.tiles_per_split = (p.n_tiles + sp - 1) / sp;
     p.n_split = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
-    const int oc = pick_split(BH, p.n_tiles, kSMs);
+    const int oc = pick_split(BH, p.n_tiles, sms);
     p.out_tiles_per_cta = (p.n_tiles + oc - 1) / oc;
     p.out_ctas = (p.n_tiles + p.out_tiles_per_cta - 1) / p.out_tiles_per_cta;
   } else {
-    const int sc = pick_split(BH, p.n_tiles, kSMs);
+    const int sc = pick_split(BH, p.n_tiles, sms);
     p.out_tiles_per_cta = (p.n_tiles + sc - 1) / sc;                          // tiles per superchunk
     p.out_ctas = (p.n_tiles + p.out_tiles_per_cta - 1) / p.out_tiles_per_cta;  // superchunks
     // the states of all superchunks but the last, each computed in k equal
@@ -112,7 +112,7 @@ TcPlan tc_plan(bool causal, const Shape& s) {
     for (int k = 1; k <= tps; ++k) {
       if (tps % k) continue;
       const long ctas = (long)BH * (p.out_ctas - 1) * k;
-      const long cost = ((ctas + kSMs - 1) / kSMs) * (tps / k + kCtaOverheadTiles);
+      const long cost = ((ctas + sms - 1) / sms) * (tps / k + kCtaOverheadTiles);
       if (best_cost < 0 || cost < best_cost) {
         best_cost = cost;
         best_k = k;
