@@ -114,8 +114,10 @@ cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
 // SM count of the current device (cached).
 int sm_count();
 
-// Row-norm maxima (and optionally the bf16 Omega images) into the workspace.
-cudaError_t launch_prep(const float* omega, int m, int d, float* key_ref, uint8_t* image, cudaStream_t stream);
+// Row-norm maxima (and optionally the fp16 Omega image) into the workspace;
+// also zeroes `n_counters` words at `counters` (the split-merge counters).
+cudaError_t launch_prep(const float* omega, int m, int d, float* header, uint8_t* image, uint32_t* counters,
+                        int n_counters, cudaStream_t stream);
 
 cudaError_t launch_build_orf(uint64_t seed, int m, int d, int orthogonal, float* omega,
                              cudaStream_t stream);

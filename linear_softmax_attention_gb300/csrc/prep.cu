@@ -15,7 +15,8 @@ namespace {
 
 constexpr int kPrepThreads = 32 * kPrepRows;   // one warp per row of Omega
 
-// Grid of ceil(m / 8) CTAs; warp w of CTA b handles row i = 8b + w: its
+// Grid of ceil(m / 8) CTAs; the CTAs also zero `n_counters` merge counters.
+// Warp w of CTA b handles row i = 8b + w: its
 // squared norm (the CTA writes the largest of its 8 into header slot b) and,
 // if `image` is non-null, its fp16 image (round to nearest, saturating) for
 // the projection MMAs: layout [64-column atom][m rows][128 B], 16-byte chunk
@@ -23,8 +24,10 @@ constexpr int kPrepThreads = 32 * kPrepRows;   // one warp per row of Omega
 // carries w to 11 significant bits; bf16 w alone costs ~2.5% in the output.
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const float* __restrict__ omega, int m, int d,
                                                             float* __restrict__ header,
-                                                            uint8_t* __restrict__ image) {
+                                                            uint8_t* __restrict__ image,
+                                                            uint32_t* __restrict__ counters, int n_counters) {
   __shared__ float red[32];
+  for (int i = blockIdx.x * kPrepThreads + threadIdx.x; i < n_counters; i += gridDim.x * kPrepThreads) counters[i] = 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x * kPrepRows + warp;
   float n2 = -INFINITY;
@@ -52,8 +55,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const float* __restr
 
 }  // namespace
 
-cudaError_t launch_prep(const float* omega, int m, int d, float* header, uint8_t* image, cudaStream_t stream) {
-  prep_kernel<<<(m + kPrepRows - 1) / kPrepRows, kPrepThreads, 0, stream>>>(omega, m, d, header, image);
+cudaError_t launch_prep(const float* omega, int m, int d, float* header, uint8_t* image, uint32_t* counters,
+                        int n_counters, cudaStream_t stream) {
+  prep_kernel<<<(m + kPrepRows - 1) / kPrepRows, kPrepThreads, 0, stream>>>(omega, m, d, header, image, counters,
+                                                                             n_counters);
   return cudaGetLastError();
 }
 

@@ -408,7 +408,7 @@ template <typename T>
 static cudaError_t state_impl(const void* K, const void* V, const float* omega, float scale, const Shape& s,
                               const SimtPlan& p, char* ws, cudaStream_t stream) {
   float* key_ref = reinterpret_cast<float*>(ws);
-  cudaError_t e = launch_prep(omega, s.m, s.d, key_ref, nullptr, stream);
+  cudaError_t e = launch_prep(omega, s.m, s.d, key_ref, nullptr, nullptr, 0, stream);
   if (e != cudaSuccess) return e;
   const size_t smem = state_smem(s.d);
   auto kern = state_partial_kernel<T>;

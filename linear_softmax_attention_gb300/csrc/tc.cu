@@ -1416,13 +1416,12 @@ cudaError_t tc_state(bool causal, const void* K, const void* V, const float* ome
                      void* ws, int32_t* status, cudaStream_t stream) {
   const TcPlan p = tc_plan(causal, s);
   char* w = static_cast<char*>(ws);
+  // prep also zeroes the bidirectional merge counters
   cudaError_t e = launch_prep(omega, s.m, s.d, reinterpret_cast<float*>(w),
-                              reinterpret_cast<uint8_t*>(w + p.off_omega_img), stream);
+                              reinterpret_cast<uint8_t*>(w + p.off_omega_img),
+                              causal ? nullptr : reinterpret_cast<uint32_t*>(w + p.off_counters), causal ? 0 : s.BH(),
+                              stream);
   if (e != cudaSuccess) return e;
-  if (!causal) {
-    e = cudaMemsetAsync(w + p.off_counters, 0, (size_t)s.BH() * sizeof(uint32_t), stream);
-    if (e != cudaSuccess) return e;
-  }
   return s.m == 256 ? launch_state<64, 256>(K, V, s, p, scale, w, status, stream)
                     : launch_state<64, 128>(K, V, s, p, scale, w, status, stream);
 }
