@@ -785,7 +785,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
       const float den = have ? __uint_as_float(z[0]) : 1.f;
       const int row = (tile0 + j) * kBM + t;
       if (have && row < prm.L && (!(den > 0.f) || !isfinite(den))) report_status(prm.status, FAVOR_ERR_NONFINITE);
-      const float inv = 1.0f / den;
+      const float inv = __fdividef(1.0f, den);
       if (threadIdx.x == kEpiTid0 && j > 0) bulk_wait_read0();   // previous store has left the staging tile
       named_bar(1, kEpiThreads);
 #pragma unroll
@@ -960,6 +960,11 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
   }
   if (warp >= 4) {
     fill_ones_block(sm + C::kOnes, kEpiTid0, kEpiThreads);
+    // G_s rows D + 8 .. D + 15 of both atoms: zero for the whole kernel
+    for (int e = threadIdx.x - kEpiTid0; e < 2 * 8 * 8; e += kEpiThreads) {
+      const int atom = e >> 6, row = kBM + D + 8 + ((e >> 3) & 7);
+      *reinterpret_cast<uint4*>(sm + C::kKG + atom * C::kKGAtom + row * 128 + (e & 7) * 16) = make_uint4(0, 0, 0, 0);
+    }
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -1131,12 +1136,16 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
     const float hs2 = 0.5f * prm.scale * prm.scale;
     const uint32_t kg_a = smem_addr(sm + C::kKG), phiq_a = smem_addr(sm + C::kPhiQ);
     const uint32_t ma_a = smem_addr(sm + C::kMA);
-    uint8_t* kg = sm + C::kKG;
     const int col0 = wg * 64;                 // this warpgroup's 64 of a block's 128 columns
     // G columns of this warpgroup: 0..47 or 48..GN-1
     constexpr int kG0 = 48;
     const int n0 = wg ? kG0 : 0;
     const int ng16 = wg ? (GN - kG0) / 16 : kG0 / 16;
+    // G_s groups of 8 columns copied per chunk: n < D + 8 (the normaliser
+    // column D and zeros), split between the two warpgroups
+    constexpr int kGGroups = D / 8 + 1;
+    const int g_first = wg ? (kGGroups + 1) / 2 : 0;
+    const int g_end = wg ? kGGroups : (kGGroups + 1) / 2;
     // G_init = sum of the earlier superchunks' states, in superchunk order
     for (int fb = 0; fb < NFB; ++fb) {
       const float* src = prm.partS + (((size_t)bh * NFB + fb) * max(prm.n_split, 1)) * (D + 1) * kFB;
@@ -1159,6 +1168,10 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
       }
     }
     tmem_st_wait();
+    // the G_s copies below read columns the other warpgroup stored
+    tc_fence_before();
+    named_bar(1, kEpiThreads);
+    tc_fence_after();
     bool ok = true;
     auto out = [&](int j) {
       const bool have = ok && mbar_wait(o_full, j & 1, wctx);
@@ -1167,13 +1180,14 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
       tmem_ld32(tmem + lane_off + O_COL + wg * 32, v);
       tmem_ld8(tmem + lane_off + O_COL + D, z);
       tmem_ld_wait();
+      FAVOR_TRACE_POINT(41);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free);
       const float den = have ? __uint_as_float(z[0]) : 1.f;
       if (have && (tile0 + j) * kBM + t < prm.L && (!(den > 0.f) || !isfinite(den)))
         report_status(prm.status, FAVOR_ERR_NONFINITE);
-      const float inv = 1.0f / den;
+      const float inv = __fdividef(1.0f, den);
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         const int chunk = wg * 4 + cc;
@@ -1184,6 +1198,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
                      pack_bf16(__uint_as_float(v[o + 4]) * inv, __uint_as_float(v[o + 5]) * inv),
                      pack_bf16(__uint_as_float(v[o + 6]) * inv, __uint_as_float(v[o + 7]) * inv));
       }
+      FAVOR_TRACE_POINT(42);
       fence_proxy_async_smem();
       named_bar(1, kEpiThreads);
       if (threadIdx.x == kEpiTid0 && have && !*abort_flag) {
@@ -1200,6 +1215,8 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
         // ---- phi(K)_fb and G_s,fb ----
         if (ok) ok = mbar_wait(pk_full, u & 1, wctx);
         if (ok && fb == 0) ok = mbar_wait(&kn_full[c & 1], (c >> 1) & 1, wctx);
+        // rows past the sequence end: an infinite bias makes their features 0
+        const float bias_k = valid ? (hs2 * nk[t] + R) * kLog2e : INFINITY;
         tc_fence_after();
         {
           // loaded even after a failed wait (the kernel is then aborting and the
@@ -1207,37 +1224,53 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
           uint32_t x[64];
           tmem_ld64(tmem + lane_off + X_COL + col0, x);
           tmem_ld_wait();
+          FAVOR_TRACE_POINT(30);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(x_free);
-          if (ok) exp_pack<64>(x, c1, (hs2 * nk[t] + R) * kLog2e, valid);
+          if (ok) exp_pack<64>(x, c1, bias_k, true);
+          FAVOR_TRACE_POINT(31);
           if (ok && u >= 1) ok = mbar_wait(kg_free, (u - 1) & 1, wctx);
           if (ok && c >= 1) ok = mbar_wait(&gdone[fb], (c - 1) & 1, wctx);
           tc_fence_after();
           if (ok) store_row<32>(kg_a, C::kKGAtom, t, col0, x);
+          FAVOR_TRACE_POINT(32);
         }
         if (ok) {
-          // G_s,fb: row 128 + n, column t (this lane's feature)
-          uint8_t* gs = kg + (t >> 6) * C::kKGAtom + (t & 7) * 2;
-          const int fchunk = (t & 63) >> 3;
-          for (int g = 0; g < ng16; ++g) {
-            uint32_t r[16];
-            tmem_ld16(tmem + lane_off + G_COL + fb * GN + n0 + 16 * g, r);
+          // G_s,fb rows 128 + n for n < D + 8 (rows D + 1 .. stay zero: G's
+          // columns there are zero).  Per group of 8 columns n, a 16x256b
+          // load per half of this warp's 32 features gives each thread two
+          // adjacent n of one feature; stmatrix.trans turns each 8x8 block
+          // (features x n) into rows n of 8 features, one swizzle chunk each.
+          const int mi = lane >> 3, kr = lane & 7;
+          const int f0 = 32 * q + 8 * mi;                 // first feature of matrix mi
+          const uint32_t row_base = kg_a + (f0 >> 6) * C::kKGAtom + kBM * 128;
+          const int fch = (f0 & 63) >> 3;
+#pragma unroll 1
+          for (int g = g_first; g < g_end; ++g) {
+            uint32_t lo[4], hi[4];
+            const uint32_t col = G_COL + fb * GN + 8 * g;
+            tmem_ld16x256(tmem + (static_cast<uint32_t>(32 * q) << 16) + col, lo);
+            tmem_ld16x256(tmem + (static_cast<uint32_t>(32 * q + 16) << 16) + col, hi);
             tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int n = n0 + 16 * g + j;
-              *reinterpret_cast<__nv_bfloat16*>(gs + (kBM + n) * 128 + ((fchunk ^ (n & 7)) << 4)) =
-                  __float2bfloat16_rn(__uint_as_float(r[j]));
-            }
+            const int n = 8 * g + kr;
+            stmatrix_x4_trans(row_base + n * 128 + ((fch ^ (n & 7)) << 4),
+                              pack_bf16(__uint_as_float(lo[0]), __uint_as_float(lo[1])),
+                              pack_bf16(__uint_as_float(lo[2]), __uint_as_float(lo[3])),
+                              pack_bf16(__uint_as_float(hi[0]), __uint_as_float(hi[1])),
+                              pack_bf16(__uint_as_float(hi[2]), __uint_as_float(hi[3])));
           }
         }
+        FAVOR_TRACE_POINT(33);
         tc_fence_before();
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(kg_full);
         // the previous chunk's output, deferred so that its MMAs overlap
-        if (fb == 0 && c >= 1) out(c - 1);
+        if (fb == 0 && c >= 1) {
+          out(c - 1);
+          FAVOR_TRACE_POINT(34);
+        }
         // ---- phi(Q)_fb ----
         if (ok) ok = mbar_wait(pq_full, u & 1, wctx);
         if (ok && fb == 0) {
@@ -1251,12 +1284,15 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
           uint32_t x[64];
           tmem_ld64(tmem + lane_off + X_COL + col0, x);
           tmem_ld_wait();
+          FAVOR_TRACE_POINT(35);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(x_free);
           if (ok) exp_pack<64>(x, c1, bias_q, true);
+          FAVOR_TRACE_POINT(36);
           if (ok && u >= 1) ok = mbar_wait(phiq_free, (u - 1) & 1, wctx);
           if (ok) store_row<32>(phiq_a, kAtom, t, col0, x);
+          FAVOR_TRACE_POINT(37);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -1269,9 +1305,11 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
         uint32_t a[64];
         tmem_ld64(tmem + lane_off + A_COL + col0, a);
         tmem_ld_wait();
+        FAVOR_TRACE_POINT(38);
         tc_fence_before();
         if (threadIdx.x == kEpiTid0 && c >= 1) bulk_wait_read0();
         named_bar(1, kEpiThreads);
+        FAVOR_TRACE_POINT(39);
         if (ok) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -1281,6 +1319,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
           }
           store_row<32>(ma_a, kAtom, t, col0, a);
         }
+        FAVOR_TRACE_POINT(40);
       }
       fence_proxy_async_smem();
       __syncwarp();
