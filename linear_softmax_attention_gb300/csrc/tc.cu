@@ -1020,7 +1020,10 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
       int npk = 0, npq = 0, ng = 0, nao = 0, noi = 0;
       while (ok && noi < n_chunks) {
         bool progress = false;
-        if (npk < U && npq == npk) {
+        // P_K of a chunk's first block waits until the previous chunk's last
+        // [A|O] is issued: queued ahead of it, it would delay the scores the
+        // epilogue is waiting for
+        if (npk < U && npq == npk && (npk % NFB != 0 || nao >= npk)) {
           const int c = npk / NFB, fb = npk % NFB;
           if ((npk == 0 || ready(x_free, 1)) && (fb != 0 || ready(&kn_full[c & 1], c >> 1))) {
             tc_fence_after();
@@ -1030,6 +1033,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
             for (int k = 0; k < D / 16; ++k)
               mma_bf16(tmem + X_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
             mma_commit(pk_full);
+            FAVOR_TRACE_POINT(50);
             if (fb == NFB - 1) mma_commit(&slot_free[slot_of(c, 0)]);
             ++npk;
             progress = true;
@@ -1045,6 +1049,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
             for (int k = 0; k < D / 16; ++k)
               mma_bf16(tmem + X_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
             mma_commit(pq_full);
+            FAVOR_TRACE_POINT(51);
             if (fb == NFB - 1) mma_commit(&slot_free[slot_of(c, 1)]);
             ++npq;
             progress = true;
@@ -1061,6 +1066,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
             for (int k = 0; k < kBM / 16; ++k)
               mma_bf16(tmem + G_COL + fb * GN, dadd(a0, kstep_mn(k)), vones_k(b0, k), id_g, true);
             mma_commit(&gdone[fb]);
+            FAVOR_TRACE_POINT(52);
             ++ng;
             progress = true;
           }
@@ -1074,6 +1080,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
             for (int k = 0; k < kFB / 16; ++k)
               mma_bf16(tmem + A_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, C::kKGAtom)), id_ao,
                        (fb > 0) || (k > 0));
+            FAVOR_TRACE_POINT(53);
             mma_commit(kg_free);
             mma_commit(phiq_free);
             if (fb == NFB - 1) mma_commit(a_full);
@@ -1089,6 +1096,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
           for (int k = 0; k < kBM / 16; ++k)
             mma_bf16(tmem + O_COL, dadd(a0, kstep_k(k, kAtom)), vones_k(b0, k), id_oi, true);
           mma_commit(o_full);
+          FAVOR_TRACE_POINT(54);
           mma_commit(&slot_free[slot_of(noi, 2)]);
           ++noi;
           progress = true;
@@ -1311,11 +1319,21 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
         named_bar(1, kEpiThreads);
         FAVOR_TRACE_POINT(39);
         if (ok) {
+          // this warp's rows 32q .. 32q+31 against columns col0 .. col0+63:
+          // entirely kept, entirely masked, or on the diagonal
+          if (col0 + 63 <= 32 * q) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int f = col0 + 2 * j;
-            a[j] = pack_bf16(f <= t ? __uint_as_float(a[2 * j]) : 0.f,
-                             f + 1 <= t ? __uint_as_float(a[2 * j + 1]) : 0.f);
+            for (int j = 0; j < 32; ++j) a[j] = pack_bf16(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1]));
+          } else if (col0 > 32 * q + 31) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a[j] = 0u;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int f = col0 + 2 * j;
+              a[j] = pack_bf16(f <= t ? __uint_as_float(a[2 * j]) : 0.f,
+                               f + 1 <= t ? __uint_as_float(a[2 * j + 1]) : 0.f);
+            }
           }
           store_row<32>(ma_a, kAtom, t, col0, a);
         }
