@@ -202,6 +202,50 @@ favor_status favor_fwd_bidir_static(const void* Q, const void* K, const void* V,
 size_t favor_static_scratch_bytes(void);
 
 /*
+ * Incremental causal FAVOR+ (token-by-token decoding).  The unidirectional
+ * form is a recurrence over the prefix sums of favor_fwd_causal: a causal
+ * linear attention is a unidirectional RNN whose state is (G_t, z_t)
+ * ("From Performer to Linear Attention", §Concentrating Attention; "Performer"
+ * digest, §Methods causal bullet and its related-work note on the prefix-sum
+ * RNN view; arXiv summary, attention preliminaries: unidirectional attention
+ * for autoregressive generation).  These calls carry that state between
+ * calls so that one new token per sequence costs O(m d) instead of a pass
+ * over the prefix.
+ *
+ * State layout: `state` is a caller-owned device fp32 array
+ * [B, H, m, d + 1] (contiguous, 16-byte aligned): row i of head (b, h) holds
+ *   sum_{s<=t} exp(s w_i.k_s - s^2 |k_s|^2 / 2 - R) [v_s ; 1]
+ * with R = max_i |w_i|^2 / 2 - 40, a constant of omega alone that every call
+ * recomputes (it cancels in the output; it keeps every feature <= e^40).
+ * A zero-filled state is the empty prefix.  The state is only meaningful to
+ * these calls with the same omega and qk_scale.
+ *
+ * favor_decode_step — for each (b, h), with q, k, v, o contiguous [B, H, d]
+ * (one token per sequence and head, dtype `dt`, 16-byte aligned):
+ *   state += phi(s k) [v ; 1]^T   (the new token is part of its own prefix)
+ *   o = phi(s q)^T state[:, :d] / phi(s q)^T state[:, d]
+ * which equals row t of favor_fwd_causal over the whole sequence, given the
+ * state of tokens 0 .. t-1.  The state is read and written in place; o may
+ * not alias q, k, v or the state.  A zero or non-finite normaliser is
+ * reported in dev_status (FAVOR_ERR_NONFINITE).  Supported: 1 <= d <= 128,
+ * 1 <= m <= 512, 1 <= B*H <= 65535, bf16 or fp32.
+ *
+ * favor_decode_prefill — state = sum over the L tokens of K, V ([B, H, L, d])
+ * of phi(s k_t) [v_t ; 1]^T in the layout above (overwriting the state):
+ * the state after a prompt, ready for favor_decode_step on token L.  Needs a
+ * workspace of favor_decode_prefill_workspace_bytes(...) bytes.
+ */
+favor_status favor_decode_step(const void* q, const void* k, const void* v, void* o,
+                               int B, int H, int d,
+                               const float* omega, int m, favor_dtype dt, float qk_scale,
+                               float* state, int32_t* dev_status, void* stream);
+favor_status favor_decode_prefill(const void* K, const void* V, int B, int H, int L, int d,
+                                  const float* omega, int m, favor_dtype dt, float qk_scale,
+                                  float* state, void* workspace, size_t ws_bytes,
+                                  int32_t* dev_status, void* stream);
+size_t favor_decode_prefill_workspace_bytes(int B, int H, int L, int d, int m, favor_dtype dt);
+
+/*
  * favor_path_name — which kernel family a call with these arguments uses:
  * "tcgen05" (bf16 tensor-core kernels), "simt" (CUDA-core fp32 kernels) or
  * "unsupported".  Static string, never NULL.

@@ -18,6 +18,7 @@ __all__ = [
     "load", "lib_path", "FavorError", "F32", "BF16", "api_version", "path_name", "build_orf", "new_omega",
     "workspace_bytes", "new_workspace", "fwd_bidir", "fwd_causal", "bidir_state", "bidir_output",
     "causal_state", "causal_output", "status_string", "ENTRY_POINTS", "fwd_bidir_static", "static_scratch_bytes",
+    "new_decode_state", "decode_step", "decode_prefill", "decode_prefill_workspace_bytes",
 ]
 
 F32 = 0
@@ -68,6 +69,14 @@ def load():
     lib.favor_fwd_bidir_static.argtypes = [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_vp, c_int, c_int,
                                            c_float, c_vp, c_vp]
     lib.favor_static_scratch_bytes.restype = c_size
+    lib.favor_decode_step.restype = c_int
+    lib.favor_decode_step.argtypes = [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_vp, c_int, c_int, c_float,
+                                      c_vp, c_vp, c_vp]
+    lib.favor_decode_prefill.restype = c_int
+    lib.favor_decode_prefill.argtypes = [c_vp, c_vp, c_int, c_int, c_int, c_int, c_vp, c_int, c_int, c_float, c_vp,
+                                         c_vp, c_size, c_vp, c_vp]
+    lib.favor_decode_prefill_workspace_bytes.restype = c_size
+    lib.favor_decode_prefill_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int]
     _lib = lib
     return lib
 
@@ -190,3 +199,58 @@ def fwd_bidir_static(Q, K, V, omega, qk_scale, O=None, dev_status=None, stream=N
                                          _stream_handle(stream))
     _check(code, "favor_fwd_bidir_static")
     return O
+
+
+def new_decode_state(B: int, H: int, m: int, d: int, device="cuda") -> torch.Tensor:
+    """Zero decode state (the empty prefix): fp32 [B, H, m, d + 1]."""
+    return torch.zeros((B, H, m, d + 1), dtype=torch.float32, device=device)
+
+
+def decode_step(q, k, v, omega, qk_scale, state, o=None, dev_status=None, stream=None):
+    """One causal step per (b, h): q, k, v [B, H, d]; adds this token to
+    ``state`` (in place) and returns o [B, H, d], the token's causal output."""
+    B, H, d = q.shape
+    m = omega.shape[0]
+    o = torch.empty_like(q) if o is None else o
+    for t in (q, k, v, o):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype or tuple(t.shape) != (B, H, d):
+            raise FavorError("decode_step: q/k/v/o must be contiguous CUDA tensors of one dtype and shape [B,H,d]")
+    if (state.dtype != torch.float32 or not state.is_contiguous() or tuple(state.shape) != (B, H, m, d + 1)):
+        raise FavorError(f"decode_step: state must be contiguous fp32 [B, H, {m}, {d + 1}]")
+    if omega.dtype != torch.float32 or tuple(omega.shape) != (m, d) or not omega.is_contiguous():
+        raise FavorError(f"decode_step: omega must be contiguous fp32 [m, {d}]")
+    code = load().favor_decode_step(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, H, d,
+                                    omega.data_ptr(), m, _DT[q.dtype], float(qk_scale), state.data_ptr(),
+                                    dev_status.data_ptr() if dev_status is not None else None,
+                                    _stream_handle(stream))
+    _check(code, "favor_decode_step")
+    return o
+
+
+def decode_prefill_workspace_bytes(B: int, H: int, L: int, d: int, m: int, dtype) -> int:
+    n = load().favor_decode_prefill_workspace_bytes(B, H, L, d, m, _DT[dtype])
+    if n == 0:
+        raise FavorError("unsupported shape")
+    return n
+
+
+def decode_prefill(K, V, omega, qk_scale, state, workspace=None, dev_status=None, stream=None):
+    """state = the decode state after the L tokens of K, V [B, H, L, d]
+    (overwritten); returns state."""
+    B, H, L, d = K.shape
+    m = omega.shape[0]
+    for t in (K, V):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != K.dtype or tuple(t.shape) != (B, H, L, d):
+            raise FavorError("decode_prefill: K/V must be contiguous CUDA tensors of one dtype and shape [B,H,L,d]")
+    if (state.dtype != torch.float32 or not state.is_contiguous() or tuple(state.shape) != (B, H, m, d + 1)):
+        raise FavorError(f"decode_prefill: state must be contiguous fp32 [B, H, {m}, {d + 1}]")
+    if workspace is None:
+        n = decode_prefill_workspace_bytes(B, H, L, d, m, K.dtype)
+        workspace = torch.empty(n, dtype=torch.uint8, device=K.device)
+    code = load().favor_decode_prefill(K.data_ptr(), V.data_ptr(), B, H, L, d, omega.data_ptr(), m, _DT[K.dtype],
+                                       float(qk_scale), state.data_ptr(), workspace.data_ptr(),
+                                       workspace.numel() * workspace.element_size(),
+                                       dev_status.data_ptr() if dev_status is not None else None,
+                                       _stream_handle(stream))
+    _check(code, "favor_decode_prefill")
+    return state

@@ -162,4 +162,41 @@ favor_status favor_bidir_output(FAVOR_ARGS) { return run(false, kOutput, FAVOR_P
 favor_status favor_causal_state(FAVOR_ARGS) { return run(true, kState, FAVOR_PASS); }
 favor_status favor_causal_output(FAVOR_ARGS) { return run(true, kOutput, FAVOR_PASS); }
 
+favor_status favor_decode_step(const void* q, const void* k, const void* v, void* o, int B, int H, int d,
+                               const float* omega, int m, favor_dtype dt, float qk_scale, float* state,
+                               int32_t* dev_status, void* stream) {
+  favor_status st = shape_ok(B, H, 1, d, m, dt);
+  if (st != FAVOR_OK) return st;
+  if (!std::isfinite(qk_scale) || !(qk_scale > 0.f)) return FAVOR_ERR_INVALID_ARG;
+  for (const void* p : {q, k, v, static_cast<const void*>(o), static_cast<const void*>(omega),
+                        static_cast<const void*>(state)})
+    if (p == nullptr || !aligned(p, 16)) return FAVOR_ERR_INVALID_ARG;
+  if (o == q || o == k || o == v || o == state) return FAVOR_ERR_INVALID_ARG;
+  cudaError_t e = favor::launch_decode_step(q, k, v, o, B * H, d, omega, m, dt == FAVOR_BF16, qk_scale, state,
+                                            dev_status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
+}
+
+size_t favor_decode_prefill_workspace_bytes(int B, int H, int L, int d, int m, favor_dtype dt) {
+  if (shape_ok(B, H, L, d, m, dt) != FAVOR_OK) return 0;
+  return favor::simt_plan(false, Shape{B, H, L, d, m}).bytes;
+}
+
+favor_status favor_decode_prefill(const void* K, const void* V, int B, int H, int L, int d, const float* omega,
+                                  int m, favor_dtype dt, float qk_scale, float* state, void* workspace,
+                                  size_t ws_bytes, int32_t* dev_status, void* stream) {
+  (void)dev_status;
+  favor_status st = shape_ok(B, H, L, d, m, dt);
+  if (st != FAVOR_OK) return st;
+  if (!std::isfinite(qk_scale) || !(qk_scale > 0.f)) return FAVOR_ERR_INVALID_ARG;
+  for (const void* p : {K, V, static_cast<const void*>(omega), static_cast<const void*>(state)})
+    if (p == nullptr || !aligned(p, 16)) return FAVOR_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256)) return FAVOR_ERR_INVALID_ARG;
+  const Shape s{B, H, L, d, m};
+  if (ws_bytes < favor::simt_plan(false, s).bytes) return FAVOR_ERR_INVALID_ARG;
+  cudaError_t e = favor::simt_state_export(K, V, omega, qk_scale, s, dt == FAVOR_BF16, workspace, state,
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
+}
+
 }  // extern "C"

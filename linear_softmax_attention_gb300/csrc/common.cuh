@@ -91,6 +91,12 @@ struct SimtPlan {
 };
 
 SimtPlan simt_plan(bool causal, const Shape& s);
+cudaError_t simt_state_export(const void* K, const void* V, const float* omega, float scale, const Shape& s,
+                              bool bf16, void* ws, float* state, cudaStream_t stream);
+// One decode step for every (b, h): decode.cu.
+cudaError_t launch_decode_step(const void* q, const void* k, const void* v, void* o, int BH, int d,
+                               const float* omega, int m, bool bf16, float scale, float* state, int32_t* status,
+                               cudaStream_t stream);
 cudaError_t simt_bidir_state(const void* K, const void* V, const float* omega, float scale,
                              const Shape& s, bool bf16, void* ws, int32_t* st, cudaStream_t stream);
 cudaError_t simt_bidir_output(const void* Q, void* O, const float* omega, float scale,

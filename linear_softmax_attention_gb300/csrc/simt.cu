@@ -434,6 +434,21 @@ cudaError_t simt_bidir_state(const void* K, const void* V, const float* omega, f
   return cudaGetLastError();
 }
 
+// The summed state of a whole sequence, fp32 [BH][m][d+1], into `state`
+// (the decode state layout): the same partials and fixed-order merge as the
+// bidirectional state, written to the caller's array.
+cudaError_t simt_state_export(const void* K, const void* V, const float* omega, float scale, const Shape& s,
+                              bool bf16, void* ws, float* state, cudaStream_t stream) {
+  const SimtPlan p = simt_plan(false, s);
+  char* w = static_cast<char*>(ws);
+  cudaError_t e = bf16 ? state_impl<__nv_bfloat16>(K, V, omega, scale, s, p, w, stream)
+                       : state_impl<float>(K, V, omega, scale, s, p, w, stream);
+  if (e != cudaSuccess) return e;
+  merge_kernel<<<s.BH(), kThreads, 0, stream>>>(reinterpret_cast<float*>(w + p.off_partS), s.d, s.m, p.n_split,
+                                                state);
+  return cudaGetLastError();
+}
+
 template <typename T>
 static cudaError_t bidir_out_impl(const void* Q, void* O, const float* omega, float scale, const Shape& s,
                                   const SimtPlan& p, char* ws, int32_t* st, cudaStream_t stream) {

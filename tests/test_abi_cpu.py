@@ -98,3 +98,39 @@ def test_product_code_does_not_touch_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower(), f
+
+
+def test_decode_rejects_bad_arguments_before_launch(lib):
+    # favor_decode_step(q, k, v, o, B, H, d, omega, m, dt, s, state, status, stream)
+    def step(**kw):
+        a = dict(q=16, k=16, v=16, o=32, B=1, H=1, d=8, omega=48, m=8, dt=0, s=1.0, state=64, st=None, stream=None)
+        a.update(kw)
+        return lib.favor_decode_step(a["q"], a["k"], a["v"], a["o"], a["B"], a["H"], a["d"], a["omega"], a["m"],
+                                     a["dt"], a["s"], a["state"], a["st"], a["stream"])
+    assert step(q=None) == 1
+    assert step(state=None) == 1
+    assert step(omega=None) == 1
+    assert step(o=16) == 1            # o aliases q
+    assert step(o=64) == 1            # o aliases the state
+    assert step(q=24) == 1            # misaligned
+    assert step(d=129) == 2
+    assert step(m=513) == 2
+    assert step(B=0) == 1
+    assert step(dt=5) == 1
+    assert step(s=float("inf")) == 1
+
+    def prefill(**kw):
+        a = dict(K=16, V=16, B=1, H=1, L=8, d=8, omega=48, m=8, dt=0, s=1.0, state=64, ws=256, nbytes=1 << 30,
+                 st=None, stream=None)
+        a.update(kw)
+        return lib.favor_decode_prefill(a["K"], a["V"], a["B"], a["H"], a["L"], a["d"], a["omega"], a["m"], a["dt"],
+                                        a["s"], a["state"], a["ws"], a["nbytes"], a["st"], a["stream"])
+    assert prefill(K=None) == 1
+    assert prefill(state=None) == 1
+    assert prefill(ws=None) == 1
+    assert prefill(ws=8) == 1
+    assert prefill(nbytes=16) == 1
+    assert prefill(L=0) == 1
+    assert prefill(m=600) == 2
+    assert lib.favor_decode_prefill_workspace_bytes(2, 8, 300, 64, 256, 1) > 0
+    assert lib.favor_decode_prefill_workspace_bytes(2, 8, 0, 64, 256, 1) == 0
