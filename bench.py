@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--decode-steps", type=int, default=200)
     return ap.parse_args()
 
 
@@ -406,6 +407,7 @@ def run_gpu(args, rank, world, local_rank):
                "pipeline": "H2D of step i+1 (one stream per input) and D2H of step i-1 overlap step i"}
 
     hbm, tc_burst, tc_sus, peak_kind = load_peaks()
+    decode = measure_decode(favor, args.decode_steps, stream, status, hbm, dev) if args.decode_steps > 0 else None
     # dominant kernel: largest share of the step
     dom = max((st for st in STAGES if st != "build_orf"), key=lambda st: stage_ms[st])
     nbytes, nflops = algorithmic(w, dom)
@@ -460,6 +462,7 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clocks,
         "wall_s_timed": t_wall,
         "e2e": e2e,
+        "decode": decode,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=12.0)
@@ -540,6 +543,55 @@ def run_reference(args, rank, world):
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
+
+
+DECODE_B, DECODE_H, DECODE_D, DECODE_M = 256, 8, 64, 256
+
+
+def measure_decode(favor, n_steps, stream, status, hbm, dev):
+    """Incremental causal decoding (favor_decode_step): one token for each of
+    B sequences x H heads per step, d64 m256 bf16.  The fp32 state
+    [B, H, d + 1, m] is 136 MB, above the 129 MB L2, so every step reads and
+    writes it from HBM; algorithmic bytes per step = state read + write +
+    q, k, v, o.  Steps are replayed from a CUDA graph of 10 launches."""
+    B, H, d, m = DECODE_B, DECODE_H, DECODE_D, DECODE_M
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(11)
+    q, k, v = (torch.randn((B, H, d), generator=gen).to(torch.bfloat16).to(dev) for _ in range(3))
+    om = favor.new_omega(11, m, d)
+    state = favor.new_decode_state(B, H, m, d)
+    o = torch.empty_like(q)
+    s = d ** -0.25
+    per_graph = 10
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            favor.decode_step(q, k, v, om, s, state, o=o, dev_status=status, stream=stream)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(per_graph):
+            favor.decode_step(q, k, v, om, s, state, o=o, dev_status=status, stream=stream)
+    reps = max(1, n_steps // per_graph)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after the decode steps")
+    ms = e0.elapsed_time(e1) / (reps * per_graph)
+    state_bytes = B * H * m * (d + 1) * 4
+    nbytes = 2 * state_bytes + 4 * B * H * d * 2
+    achieved = nbytes / (ms / 1e3) / 1e9
+    return {"workload": f"decode-bf16-B{B}H{H}-d{d}-m{m}", "value": B / (ms / 1e3), "unit": "tokens/s",
+            "ms_per_step": ms, "steps": reps * per_graph, "state_bytes": state_bytes,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "algorithmic_bytes_per_launch": nbytes}}
 
 
 def main():

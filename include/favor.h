@@ -213,9 +213,11 @@ size_t favor_static_scratch_bytes(void);
  * over the prefix.
  *
  * State layout: `state` is a caller-owned device fp32 array
- * [B, H, m, d + 1] (contiguous, 16-byte aligned): row i of head (b, h) holds
- *   sum_{s<=t} exp(s w_i.k_s - s^2 |k_s|^2 / 2 - R) [v_s ; 1]
- * with R = max_i |w_i|^2 / 2 - 40, a constant of omega alone that every call
+ * [B, H, d + 1, m] (contiguous, 16-byte aligned, feature index fastest):
+ * element (j, i) of head (b, h) holds
+ *   sum_{s<=t} exp(s w_i.k_s - s^2 |k_s|^2 / 2 - R) [v_s ; 1]_j
+ * (row j = d: the normaliser sums) with R = max_i |w_i|^2 / 2 - 40, a
+ * constant of omega alone that every call
  * recomputes (it cancels in the output; it keeps every feature <= e^40).
  * A zero-filled state is the empty prefix.  The state is only meaningful to
  * these calls with the same omega and qk_scale.

@@ -202,8 +202,8 @@ def fwd_bidir_static(Q, K, V, omega, qk_scale, O=None, dev_status=None, stream=N
 
 
 def new_decode_state(B: int, H: int, m: int, d: int, device="cuda") -> torch.Tensor:
-    """Zero decode state (the empty prefix): fp32 [B, H, m, d + 1]."""
-    return torch.zeros((B, H, m, d + 1), dtype=torch.float32, device=device)
+    """Zero decode state (the empty prefix): fp32 [B, H, d + 1, m]."""
+    return torch.zeros((B, H, d + 1, m), dtype=torch.float32, device=device)
 
 
 def decode_step(q, k, v, omega, qk_scale, state, o=None, dev_status=None, stream=None):
@@ -215,8 +215,8 @@ def decode_step(q, k, v, omega, qk_scale, state, o=None, dev_status=None, stream
     for t in (q, k, v, o):
         if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype or tuple(t.shape) != (B, H, d):
             raise FavorError("decode_step: q/k/v/o must be contiguous CUDA tensors of one dtype and shape [B,H,d]")
-    if (state.dtype != torch.float32 or not state.is_contiguous() or tuple(state.shape) != (B, H, m, d + 1)):
-        raise FavorError(f"decode_step: state must be contiguous fp32 [B, H, {m}, {d + 1}]")
+    if (state.dtype != torch.float32 or not state.is_contiguous() or tuple(state.shape) != (B, H, d + 1, m)):
+        raise FavorError(f"decode_step: state must be contiguous fp32 [B, H, {d + 1}, {m}]")
     if omega.dtype != torch.float32 or tuple(omega.shape) != (m, d) or not omega.is_contiguous():
         raise FavorError(f"decode_step: omega must be contiguous fp32 [m, {d}]")
     code = load().favor_decode_step(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, H, d,
@@ -242,8 +242,8 @@ def decode_prefill(K, V, omega, qk_scale, state, workspace=None, dev_status=None
     for t in (K, V):
         if not t.is_cuda or not t.is_contiguous() or t.dtype != K.dtype or tuple(t.shape) != (B, H, L, d):
             raise FavorError("decode_prefill: K/V must be contiguous CUDA tensors of one dtype and shape [B,H,L,d]")
-    if (state.dtype != torch.float32 or not state.is_contiguous() or tuple(state.shape) != (B, H, m, d + 1)):
-        raise FavorError(f"decode_prefill: state must be contiguous fp32 [B, H, {m}, {d + 1}]")
+    if (state.dtype != torch.float32 or not state.is_contiguous() or tuple(state.shape) != (B, H, d + 1, m)):
+        raise FavorError(f"decode_prefill: state must be contiguous fp32 [B, H, {d + 1}, {m}]")
     if workspace is None:
         n = decode_prefill_workspace_bytes(B, H, L, d, m, K.dtype)
         workspace = torch.empty(n, dtype=torch.uint8, device=K.device)

@@ -7,7 +7,8 @@
 // the prefix sum G_t = sum_{s<=t} phi(k_s) v_s^T (with z_t = sum phi(k_s)
 // beside it).  Per call and head:
 //   state += phi(s k) [v ; 1]^T,  o = phi(s q)^T state[:, :d] / phi(s q)^T state[:, d]
-// The state is fp32 [m][d+1] per head, row i = feature i; its key features
+// The state is fp32 [d+1][m] per head (column i = feature i, the last row
+// the normaliser sums); its key features
 // use the reference R = max_i |w_i|^2 / 2 - 40 of the sequence kernels, so a
 // state from favor_decode_prefill continues here.  The query features use
 // s |q| max_i |w_i| - 20 (the largest possible exponent less 20): a per-query
@@ -17,6 +18,8 @@
 // One CTA per head.  Bound by the state's HBM traffic: m (d+1) fp32 read and
 // written per head and token (133 KB at m = 256, d = 64); Omega (m x d fp32)
 // is read by every CTA and stays in L2.
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace favor {
@@ -24,12 +27,12 @@ namespace {
 
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
-constexpr int kDecFeat = kMaxM / kDecThreads;      // features per thread (m <= 512)
-constexpr int kDecCols = (kMaxD + 1 + 31) / 32;    // state columns per lane (d + 1 <= 129)
 constexpr float kDecQueryHeadroom = 20.0f;
+constexpr int kCB = 16;                              // state columns per block of loads
 
-template <typename T>
-__global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k,
+// NF features per thread: 1 for m <= 256, 2 for m <= 512
+template <typename T, int NF>
+__global__ void __launch_bounds__(kDecThreads, 2) decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k,
                                                                   const T* __restrict__ v, T* __restrict__ o,
                                                                   const float* __restrict__ omega, int d, int m,
                                                                   float scale, float* __restrict__ state,
@@ -60,20 +63,61 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const T* __res
     if (lane == 0) sqn[warp] = a;
   }
 
+  // the first super-block of state columns is loaded before the
+  // projections (it does not depend on them), so its HBM round trip overlaps
+  // the Omega reads; every load of a super-block is in flight at once
+  constexpr int NB = NF == 1 ? 5 : 1;              // 16-column blocks per super-block
+  constexpr int SB = NB * kCB;
+  float* st = state + (size_t)bh * ld * m;
+  float g[SB][NF];
+  auto load_sb = [&](int j0) {
+#pragma unroll
+    for (int c = 0; c < SB; ++c) {
+      const int j = j0 + c;
+#pragma unroll
+      for (int i = 0; i < NF; ++i) {
+        const int f = tid + i * kDecThreads;
+        g[c][i] = (j < ld && f < m) ? st[(size_t)j * m + f] : 0.f;
+      }
+    }
+  };
+  load_sb(0);
+
   // w_f.q, w_f.k and |w_f|^2 for the features f = tid + 256 i of this thread
-  float pq[kDecFeat], pk[kDecFeat];
+  float pq[NF], pk[NF];
   float w2max = 0.f;
 #pragma unroll
-  for (int i = 0; i < kDecFeat; ++i) {
+  for (int i = 0; i < NF; ++i) {
     const int f = tid + i * kDecThreads;
     float dq = 0.f, dk = 0.f, w2 = 0.f;
     if (f < m) {
       const float* w = omega + (size_t)f * d;
-      for (int j = 0; j < d; ++j) {
-        const float wj = __ldg(w + j);
-        dq = fmaf(wj, qs[j], dq);
-        dk = fmaf(wj, ks[j], dk);
-        w2 = fmaf(wj, wj, w2);
+      if ((d & 3) == 0) {
+        // rows are 16-byte aligned: 16-byte loads, a quarter of the requests
+        const float4* w4 = reinterpret_cast<const float4*>(w);
+        for (int j4 = 0; j4 < d / 4; ++j4) {
+          const float4 x = __ldg(w4 + j4);
+          const int j = 4 * j4;
+          dq = fmaf(x.x, qs[j], dq);
+          dk = fmaf(x.x, ks[j], dk);
+          w2 = fmaf(x.x, x.x, w2);
+          dq = fmaf(x.y, qs[j + 1], dq);
+          dk = fmaf(x.y, ks[j + 1], dk);
+          w2 = fmaf(x.y, x.y, w2);
+          dq = fmaf(x.z, qs[j + 2], dq);
+          dk = fmaf(x.z, ks[j + 2], dk);
+          w2 = fmaf(x.z, x.z, w2);
+          dq = fmaf(x.w, qs[j + 3], dq);
+          dk = fmaf(x.w, ks[j + 3], dk);
+          w2 = fmaf(x.w, x.w, w2);
+        }
+      } else {
+        for (int j = 0; j < d; ++j) {
+          const float wj = __ldg(w + j);
+          dq = fmaf(wj, qs[j], dq);
+          dk = fmaf(wj, ks[j], dk);
+          w2 = fmaf(wj, wj, w2);
+        }
       }
       w2max = fmaxf(w2max, w2);
     }
@@ -89,7 +133,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const T* __res
   const float bq = scale * sqrtf(w2) * sqrtf(sqn[0]) - kDecQueryHeadroom;
   const float hk = 0.5f * scale * scale * sqn[1];
 #pragma unroll
-  for (int i = 0; i < kDecFeat; ++i) {
+  for (int i = 0; i < NF; ++i) {
     const int f = tid + i * kDecThreads;
     if (f < m) {
       phk[f] = expf(scale * pk[i] - hk - R);
@@ -98,34 +142,59 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const T* __res
   }
   __syncthreads();
 
-  // state rows: warp w takes features w, w + 8, ...; lane l columns l + 32c,
-  // so every row is read and written with whole-warp coalesced accesses
-  float* st = state + (size_t)bh * m * ld;
-  float vr[kDecCols], acc[kDecCols];
+  // state columns j (rows of the [d+1][m] layout): thread t owns features
+  // t (and t + 256), so every access is a whole-warp coalesced 128-byte row
+  // segment.  The column sums sum_f phi(q)_f g_jf are accumulated per
+  // thread, reduced within each warp by a shuffle reduce-scatter over blocks
+  // of 16 columns, then across warps in a fixed order.
+  float fk[NF], fq[NF];
 #pragma unroll
-  for (int c = 0; c < kDecCols; ++c) {
-    const int j = lane + 32 * c;
-    vr[c] = j < ld ? vs[j] : 0.f;
-    acc[c] = 0.f;
+  for (int i = 0; i < NF; ++i) {
+    const int f = tid + i * kDecThreads;
+    fk[i] = f < m ? phk[f] : 0.f;
+    fq[i] = f < m ? phq[f] : 0.f;
   }
-#pragma unroll 4
-  for (int f = warp; f < m; f += kDecWarps) {
-    float* row = st + (size_t)f * ld;
-    const float a = phk[f], b = phq[f];
+  for (int j0 = 0; j0 < ld; j0 += SB) {
+    if (j0 > 0) load_sb(j0);
 #pragma unroll
-    for (int c = 0; c < kDecCols; ++c) {
-      const int j = lane + 32 * c;
-      if (j < ld) {
-        const float g = fmaf(a, vr[c], row[j]);
-        row[j] = g;
-        acc[c] = fmaf(b, g, acc[c]);
+    for (int b = 0; b < NB; ++b) {
+      const int jb = j0 + b * kCB;
+      float p[kCB];
+#pragma unroll
+      for (int c = 0; c < kCB; ++c) {
+        const int j = jb + c;
+        float acc = 0.f;
+        if (j < ld) {
+          const float vj = vs[j];
+#pragma unroll
+          for (int i = 0; i < NF; ++i) {
+            const int f = tid + i * kDecThreads;
+            if (f < m) {
+              const float gn = fmaf(fk[i], vj, g[b * kCB + c][i]);
+              st[(size_t)j * m + f] = gn;
+              acc = fmaf(fq[i], gn, acc);
+            }
+          }
+        }
+        p[c] = acc;
       }
-    }
-  }
+      // reduce-scatter over lane bits 3..0: after the step of offset o each
+      // lane keeps the half of its values whose index bit o matches its lane
+      // bit; then the two 16-lane halves are added
 #pragma unroll
-  for (int c = 0; c < kDecCols; ++c) {
-    const int j = lane + 32 * c;
-    if (j < ld) part[warp][j] = acc[c];
+      for (int o = kCB / 2; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int c = 0; c < o; ++c) {
+          const float keep = up ? p[c + o] : p[c];
+          const float send = up ? p[c] : p[c + o];
+          p[c] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      p[0] += __shfl_xor_sync(0xffffffffu, p[0], kCB);
+      // lane l (and l + 16) holds the warp's sum of column jb + (l & 15)
+      if (lane < kCB && jb + lane < ld) part[warp][jb + lane] = p[0];
+    }
   }
   __syncthreads();
   // numerators and normaliser, warps summed in a fixed order
@@ -146,15 +215,21 @@ __global__ void __launch_bounds__(kDecThreads) decode_step_kernel(const T* __res
 cudaError_t launch_decode_step(const void* q, const void* k, const void* v, void* o, int BH, int d,
                                const float* omega, int m, bool bf16, float scale, float* state, int32_t* status,
                                cudaStream_t stream) {
+  auto go = [&](auto tag, auto nf) {
+    using T = decltype(tag);
+    constexpr int NF = decltype(nf)::value;
+    decode_step_kernel<T, NF><<<BH, kDecThreads, 0, stream>>>(static_cast<const T*>(q), static_cast<const T*>(k),
+                                                              static_cast<const T*>(v), static_cast<T*>(o), omega, d,
+                                                              m, scale, state, status);
+  };
+  using One = std::integral_constant<int, 1>;
+  using Two = std::integral_constant<int, 2>;
   if (bf16) {
-    decode_step_kernel<__nv_bfloat16><<<BH, kDecThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-        static_cast<const __nv_bfloat16*>(v), static_cast<__nv_bfloat16*>(o), omega, d, m, scale, state, status);
+    if (m <= kDecThreads) go(__nv_bfloat16{}, One{});
+    else go(__nv_bfloat16{}, Two{});
   } else {
-    decode_step_kernel<float><<<BH, kDecThreads, 0, stream>>>(static_cast<const float*>(q),
-                                                              static_cast<const float*>(k),
-                                                              static_cast<const float*>(v), static_cast<float*>(o),
-                                                              omega, d, m, scale, state, status);
+    if (m <= kDecThreads) go(float{}, One{});
+    else go(float{}, Two{});
   }
   return cudaGetLastError();
 }

@@ -434,9 +434,24 @@ cudaError_t simt_bidir_state(const void* K, const void* V, const float* omega, f
   return cudaGetLastError();
 }
 
-// The summed state of a whole sequence, fp32 [BH][m][d+1], into `state`
-// (the decode state layout): the same partials and fixed-order merge as the
-// bidirectional state, written to the caller's array.
+// The decode state layout [bh][j][f] (j <= d, f < m: feature index fastest)
+// from the split partials, summed in split order.
+__global__ void __launch_bounds__(kThreads) merge_transposed_kernel(const float* __restrict__ partS, int d, int m,
+                                                                    int n_split, float* __restrict__ state) {
+  const int bh = blockIdx.x;
+  const int ld = d + 1;
+  const size_t per = (size_t)m * ld;
+  for (int e = threadIdx.x; e < (int)per; e += kThreads) {
+    const int j = e / m, f = e - j * m;
+    float acc = 0.f;
+    for (int p = 0; p < n_split; ++p) acc += partS[((size_t)bh * n_split + p) * per + (size_t)f * ld + j];
+    state[(size_t)bh * per + e] = acc;
+  }
+}
+
+// The summed state of a whole sequence into `state` in the decode layout
+// [BH][d+1][m]: the same partials and fixed-order merge as the bidirectional
+// state, written transposed to the caller's array.
 cudaError_t simt_state_export(const void* K, const void* V, const float* omega, float scale, const Shape& s,
                               bool bf16, void* ws, float* state, cudaStream_t stream) {
   const SimtPlan p = simt_plan(false, s);
@@ -444,8 +459,8 @@ cudaError_t simt_state_export(const void* K, const void* V, const float* omega, 
   cudaError_t e = bf16 ? state_impl<__nv_bfloat16>(K, V, omega, scale, s, p, w, stream)
                        : state_impl<float>(K, V, omega, scale, s, p, w, stream);
   if (e != cudaSuccess) return e;
-  merge_kernel<<<s.BH(), kThreads, 0, stream>>>(reinterpret_cast<float*>(w + p.off_partS), s.d, s.m, p.n_split,
-                                                state);
+  merge_transposed_kernel<<<s.BH(), kThreads, 0, stream>>>(reinterpret_cast<float*>(w + p.off_partS), s.d, s.m,
+                                                            p.n_split, state);
   return cudaGetLastError();
 }
 
