@@ -45,6 +45,8 @@ __all__ = [
     "build_omega",
     "orf_index_layout",
     "prf_features",
+    "relu_features",
+    "FEATURES",
     "trig_features",
     "softmax_kernel",
     "prf_estimator",
@@ -198,6 +200,25 @@ def prf_features(X: np.ndarray, Omega: np.ndarray) -> np.ndarray:
     return np.exp(proj - half_sq) / math.sqrt(m)
 
 
+def relu_features(X: np.ndarray, Omega: np.ndarray) -> np.ndarray:
+    """Performer-ReLU features phi(x) = m^{-1/2} ReLU(Omega x), elementwise.
+
+    [summary] §2, "Generalized kernelizable attention": FAVOR+ covers other
+    kernels by changing the feature-map function applied to the random
+    projections; [summary] §3 applications and §D.2 name the Performer-ReLU
+    variant.  The pages print no formula: the plainest reading is
+    f(w_i^T x) with f = ReLU, the same projection Omega and no ||x||^2 term
+    (it belongs to the softmax kernel only).  X [..., L, d] (already times the
+    temperature), Omega [m, d]; returns [..., L, m].
+    """
+    X = np.asarray(X, dtype=np.float64)
+    Om = np.asarray(Omega, dtype=np.float64)
+    return np.maximum(X @ Om.T, 0.0) / math.sqrt(Om.shape[0])
+
+
+FEATURES = {"prf": prf_features, "relu": relu_features}
+
+
 def trig_features(X: np.ndarray, Omega: np.ndarray) -> np.ndarray:
     """Trigonometric (sin/cos) random features for the softmax kernel.
 
@@ -233,18 +254,20 @@ def lemma2_mse(x: np.ndarray, y: np.ndarray, m: int) -> float:
 # --------------------------------------------------------------------------
 
 
-def _features_qk(Q, K, Omega, scale):
+def _features_qk(Q, K, Omega, scale, features="prf"):
     q = scale * np.asarray(Q, dtype=np.float64)
     k = scale * np.asarray(K, dtype=np.float64)
-    return prf_features(q, Omega), prf_features(k, Omega)
+    fn = FEATURES[features]
+    return fn(q, Omega), fn(k, Omega)
 
 
-def favor_bidirectional(Q, K, V, Omega, scale: float) -> np.ndarray:
+def favor_bidirectional(Q, K, V, Omega, scale: float, features: str = "prf") -> np.ndarray:
     """Bidirectional FAVOR+: D^{-1} phi(Q) (phi(K)^T V), linear order.
 
-    Q, K, V [..., L, d]; returns [..., L, d] in fp64.
+    Q, K, V [..., L, d]; returns [..., L, d] in fp64.  ``features`` is "prf"
+    (positive random features, the softmax kernel) or "relu".
     """
-    pq, pk = _features_qk(Q, K, Omega, scale)
+    pq, pk = _features_qk(Q, K, Omega, scale, features)
     V = np.asarray(V, dtype=np.float64)
     kv = np.swapaxes(pk, -1, -2) @ V              # [..., m, d]  phi(K)^T V
     z = np.sum(pk, axis=-2)                       # [..., m]     phi(K)^T 1_L
@@ -253,21 +276,21 @@ def favor_bidirectional(Q, K, V, Omega, scale: float) -> np.ndarray:
     return num / den[..., None]
 
 
-def favor_bidirectional_quadratic(Q, K, V, Omega, scale: float) -> np.ndarray:
+def favor_bidirectional_quadratic(Q, K, V, Omega, scale: float, features: str = "prf") -> np.ndarray:
     """Same estimator in quadratic order: row-normalise phi(Q) phi(K)^T, times V."""
-    pq, pk = _features_qk(Q, K, Omega, scale)
+    pq, pk = _features_qk(Q, K, Omega, scale, features)
     A = pq @ np.swapaxes(pk, -1, -2)              # [..., L, L]
     A = A / np.sum(A, axis=-1, keepdims=True)
     return A @ np.asarray(V, dtype=np.float64)
 
 
-def favor_causal(Q, K, V, Omega, scale: float) -> np.ndarray:
+def favor_causal(Q, K, V, Omega, scale: float, features: str = "prf") -> np.ndarray:
     """Unidirectional FAVOR+ by the prefix sum of the pages.
 
     G_t = sum_{s<=t} phi(k_s) v_s^T and z_t = sum_{s<=t} phi(k_s) are carried
     forward one token at a time; out_t = phi(q_t)^T G_t / phi(q_t)^T z_t.
     """
-    pq, pk = _features_qk(Q, K, Omega, scale)
+    pq, pk = _features_qk(Q, K, Omega, scale, features)
     V = np.asarray(V, dtype=np.float64)
     lead = V.shape[:-2]
     L, d = V.shape[-2:]
@@ -284,10 +307,10 @@ def favor_causal(Q, K, V, Omega, scale: float) -> np.ndarray:
     return out
 
 
-def favor_causal_quadratic(Q, K, V, Omega, scale: float) -> np.ndarray:
+def favor_causal_quadratic(Q, K, V, Omega, scale: float, features: str = "prf") -> np.ndarray:
     """Unidirectional FAVOR+ as the lower-triangular part (diagonal included)
     of phi(Q) phi(K)^T, row-normalised, times V."""
-    pq, pk = _features_qk(Q, K, Omega, scale)
+    pq, pk = _features_qk(Q, K, Omega, scale, features)
     A = pq @ np.swapaxes(pk, -1, -2)
     L = A.shape[-1]
     A = A * np.tril(np.ones((L, L)))
@@ -295,7 +318,7 @@ def favor_causal_quadratic(Q, K, V, Omega, scale: float) -> np.ndarray:
     return A @ np.asarray(V, dtype=np.float64)
 
 
-def favor_rows(Q, K, V, Omega, scale: float, bh_rows, causal: bool) -> np.ndarray:
+def favor_rows(Q, K, V, Omega, scale: float, bh_rows, causal: bool, features: str = "prf") -> np.ndarray:
     """Selected output rows of the estimator, for large inputs.
 
     Q, K, V [BH, L, d]; ``bh_rows`` is a list of (head index, t).  Row t of
@@ -311,13 +334,14 @@ def favor_rows(Q, K, V, Omega, scale: float, bh_rows, causal: bool) -> np.ndarra
     for h, items in by_head.items():
         k = scale * np.asarray(K[h], dtype=np.float64)
         v = np.asarray(V[h], dtype=np.float64)
-        pk = prf_features(k, Omega)
+        fn = FEATURES[features]
+        pk = fn(k, Omega)
         if not causal:
             kv = pk.T @ v
             z = pk.sum(axis=0)
         for t, n in items:
             q = scale * np.asarray(Q[h][t], dtype=np.float64)
-            pq = prf_features(q[None, :], Omega)[0]
+            pq = fn(q[None, :], Omega)[0]
             if causal:
                 kv = pk[: t + 1].T @ v[: t + 1]
                 z = pk[: t + 1].sum(axis=0)
