@@ -68,6 +68,21 @@ typedef enum favor_dtype {
   FAVOR_BF16 = 1   /* bf16 storage, bf16 tensor-core operands, fp32 accumulate */
 } favor_dtype;
 
+/*
+ * Feature map phi of the *_fm calls.  FAVOR_FM_PRF: positive random
+ * features, phi(x) = m^{-1/2} exp(Omega x - ||x||^2 / 2), the softmax kernel
+ * (every call without the _fm suffix).  FAVOR_FM_RELU: Performer-ReLU,
+ * phi(x) = m^{-1/2} relu(Omega x) elementwise ("Rethinking Attention with
+ * Performers" summary, §2 generalized kernelizable attention: other kernels
+ * by changing the feature-map function; §3 and §D.2 name Performer-ReLU; the
+ * pages print no formula, this is the plain reading).  relu is positively
+ * homogeneous, so qk_scale cancels in the ReLU outputs.
+ */
+typedef enum favor_feature_map {
+  FAVOR_FM_PRF = 0,
+  FAVOR_FM_RELU = 1
+} favor_feature_map;
+
 /* Library version (FAVOR_API_VERSION of the build). */
 int favor_api_version(void);
 
@@ -133,6 +148,25 @@ favor_status favor_fwd_causal(const void* Q, const void* K, const void* V, void*
                               const float* omega, int m, favor_dtype dt, float qk_scale,
                               void* workspace, size_t ws_bytes,
                               int32_t* dev_status, void* stream);
+
+/*
+ * favor_fwd_bidir_fm, favor_fwd_causal_fm — favor_fwd_bidir and
+ * favor_fwd_causal with the feature map `fm` (favor_feature_map) in place of
+ * the positive random features; same arguments, workspace sizes and paths.
+ * A row whose features are all zero (every s w_i.q <= 0 under ReLU) has a
+ * zero normaliser: its output is NaN and dev_status gets
+ * FAVOR_ERR_NONFINITE.  fm outside the enum is FAVOR_ERR_INVALID_ARG.
+ */
+favor_status favor_fwd_bidir_fm(const void* Q, const void* K, const void* V, void* O,
+                                int B, int H, int L, int d,
+                                const float* omega, int m, favor_dtype dt, float qk_scale,
+                                favor_feature_map fm, void* workspace, size_t ws_bytes,
+                                int32_t* dev_status, void* stream);
+favor_status favor_fwd_causal_fm(const void* Q, const void* K, const void* V, void* O,
+                                 int B, int H, int L, int d,
+                                 const float* omega, int m, favor_dtype dt, float qk_scale,
+                                 favor_feature_map fm, void* workspace, size_t ws_bytes,
+                                 int32_t* dev_status, void* stream);
 
 /*
  * Stage calls (same arguments as the full calls; pointers a stage does not

@@ -18,12 +18,13 @@ __all__ = [
     "load", "lib_path", "FavorError", "F32", "BF16", "api_version", "path_name", "build_orf", "new_omega",
     "workspace_bytes", "new_workspace", "fwd_bidir", "fwd_causal", "bidir_state", "bidir_output",
     "causal_state", "causal_output", "status_string", "ENTRY_POINTS", "fwd_bidir_static", "static_scratch_bytes",
-    "new_decode_state", "decode_step", "decode_prefill", "decode_prefill_workspace_bytes",
+    "new_decode_state", "decode_step", "decode_prefill", "decode_prefill_workspace_bytes", "FEATURE_MAPS",
 ]
 
 F32 = 0
 BF16 = 1
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
+FEATURE_MAPS = {"prf": 0, "relu": 1}      # favor_feature_map
 
 ENTRY_POINTS = ("favor_fwd_bidir", "favor_fwd_causal", "favor_bidir_state", "favor_bidir_output",
                 "favor_causal_state", "favor_causal_output")
@@ -69,6 +70,11 @@ def load():
     lib.favor_fwd_bidir_static.argtypes = [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_vp, c_int, c_int,
                                            c_float, c_vp, c_vp]
     lib.favor_static_scratch_bytes.restype = c_size
+    fm_args = fwd_args[:12] + [c_int] + fwd_args[12:]
+    for name in ("favor_fwd_bidir_fm", "favor_fwd_causal_fm"):
+        fn = getattr(lib, name)
+        fn.restype = c_int
+        fn.argtypes = fm_args
     lib.favor_decode_step.restype = c_int
     lib.favor_decode_step.argtypes = [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_vp, c_int, c_int, c_float,
                                       c_vp, c_vp, c_vp]
@@ -131,7 +137,7 @@ def new_workspace(causal: bool, B: int, H: int, L: int, d: int, m: int, dtype, d
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
-def _call(name: str, Q, K, V, O, omega, qk_scale, workspace, dev_status, stream):
+def _call(name: str, Q, K, V, O, omega, qk_scale, workspace, dev_status, stream, feature_map=None):
     ref = next(t for t in (Q, K, V, O) if t is not None)
     B, H, L, d = ref.shape
     m = omega.shape[0]
@@ -143,9 +149,16 @@ def _call(name: str, Q, K, V, O, omega, qk_scale, workspace, dev_status, stream)
     if omega.dtype != torch.float32 or omega.shape[1] != d or not omega.is_contiguous():
         raise FavorError(f"{name}: omega must be contiguous fp32 [m, {d}]")
     ptr = (lambda t: t.data_ptr() if t is not None else None)
-    code = getattr(load(), name)(ptr(Q), ptr(K), ptr(V), ptr(O), B, H, L, d, omega.data_ptr(), m, dt,
-                                 float(qk_scale), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                                 ptr(dev_status), _stream_handle(stream))
+    head = (ptr(Q), ptr(K), ptr(V), ptr(O), B, H, L, d, omega.data_ptr(), m, dt, float(qk_scale))
+    tail = (workspace.data_ptr(), workspace.numel() * workspace.element_size(), ptr(dev_status),
+            _stream_handle(stream))
+    if feature_map is None:
+        code = getattr(load(), name)(*head, *tail)
+    else:
+        if feature_map not in FEATURE_MAPS:
+            raise FavorError(f"{name}: feature_map must be one of {sorted(FEATURE_MAPS)}")
+        name = name + "_fm"
+        code = getattr(load(), name)(*head, FEATURE_MAPS[feature_map], *tail)
     _check(code, name)
     return O
 
@@ -154,14 +167,19 @@ def _out_like(x, O):
     return torch.empty_like(x) if O is None else O
 
 
-def fwd_bidir(Q, K, V, omega, qk_scale, workspace, O=None, dev_status=None, stream=None):
-    """Bidirectional FAVOR+; returns O [B, H, L, d] (dtype of Q)."""
-    return _call("favor_fwd_bidir", Q, K, V, _out_like(Q, O), omega, qk_scale, workspace, dev_status, stream)
+def fwd_bidir(Q, K, V, omega, qk_scale, workspace, O=None, dev_status=None, stream=None, feature_map=None):
+    """Bidirectional FAVOR+; returns O [B, H, L, d] (dtype of Q).  feature_map:
+    None or "prf" (positive random features, the softmax kernel) or "relu"
+    (Performer-ReLU)."""
+    fm = None if feature_map in (None, "prf") else feature_map
+    return _call("favor_fwd_bidir", Q, K, V, _out_like(Q, O), omega, qk_scale, workspace, dev_status, stream, fm)
 
 
-def fwd_causal(Q, K, V, omega, qk_scale, workspace, O=None, dev_status=None, stream=None):
-    """Unidirectional (causal, prefix-sum) FAVOR+; returns O [B, H, L, d]."""
-    return _call("favor_fwd_causal", Q, K, V, _out_like(Q, O), omega, qk_scale, workspace, dev_status, stream)
+def fwd_causal(Q, K, V, omega, qk_scale, workspace, O=None, dev_status=None, stream=None, feature_map=None):
+    """Unidirectional (causal, prefix-sum) FAVOR+; returns O [B, H, L, d].
+    feature_map as for fwd_bidir."""
+    fm = None if feature_map in (None, "prf") else feature_map
+    return _call("favor_fwd_causal", Q, K, V, _out_like(Q, O), omega, qk_scale, workspace, dev_status, stream, fm)
 
 
 def bidir_state(K, V, omega, qk_scale, workspace, dev_status=None, stream=None):

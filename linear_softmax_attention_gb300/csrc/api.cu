@@ -72,9 +72,10 @@ enum Stage { kState = 1, kOutput = 2, kBoth = 3 };
 
 favor_status run(bool causal, int stage, const void* Q, const void* K, const void* V, void* O, int B, int H, int L,
                  int d, const float* omega, int m, favor_dtype dt, float qk_scale, void* workspace,
-                 size_t ws_bytes, int32_t* dev_status, void* stream_) {
+                 size_t ws_bytes, int32_t* dev_status, void* stream_, int fm = FAVOR_FM_PRF) {
   favor_status st = shape_ok(B, H, L, d, m, dt);
   if (st != FAVOR_OK) return st;
+  if (fm != FAVOR_FM_PRF && fm != FAVOR_FM_RELU) return FAVOR_ERR_INVALID_ARG;
   if (!std::isfinite(qk_scale) || !(qk_scale > 0.f)) return FAVOR_ERR_INVALID_ARG;
   const bool need_q = (stage & kOutput) != 0;
   const bool need_kv = (stage & kState) != 0 || causal;
@@ -92,17 +93,19 @@ favor_status run(bool causal, int stage, const void* Q, const void* K, const voi
   const bool bf16 = dt == FAVOR_BF16;
   cudaError_t e = cudaSuccess;
   if (use_tc(causal, d, m, dt)) {
-    if (stage & kState) e = favor::tc_state(causal, K, V, omega, qk_scale, s, workspace, dev_status, stream);
+    if (stage & kState) e = favor::tc_state(causal, K, V, omega, qk_scale, s, workspace, dev_status, stream, fm);
     if (e == cudaSuccess && (stage & kOutput))
-      e = favor::tc_output(causal, Q, K, V, O, omega, qk_scale, s, workspace, dev_status, stream);
+      e = favor::tc_output(causal, Q, K, V, O, omega, qk_scale, s, workspace, dev_status, stream, fm);
   } else if (!causal) {
-    if (stage & kState) e = favor::simt_bidir_state(K, V, omega, qk_scale, s, bf16, workspace, dev_status, stream);
+    if (stage & kState)
+      e = favor::simt_bidir_state(K, V, omega, qk_scale, s, bf16, workspace, dev_status, stream, fm);
     if (e == cudaSuccess && (stage & kOutput))
-      e = favor::simt_bidir_output(Q, O, omega, qk_scale, s, bf16, workspace, dev_status, stream);
+      e = favor::simt_bidir_output(Q, O, omega, qk_scale, s, bf16, workspace, dev_status, stream, fm);
   } else {
-    if (stage & kState) e = favor::simt_causal_state(K, V, omega, qk_scale, s, bf16, workspace, dev_status, stream);
+    if (stage & kState)
+      e = favor::simt_causal_state(K, V, omega, qk_scale, s, bf16, workspace, dev_status, stream, fm);
     if (e == cudaSuccess && (stage & kOutput))
-      e = favor::simt_causal_output(Q, K, V, O, omega, qk_scale, s, bf16, workspace, dev_status, stream);
+      e = favor::simt_causal_output(Q, K, V, O, omega, qk_scale, s, bf16, workspace, dev_status, stream, fm);
   }
   return e == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
 }
@@ -161,6 +164,17 @@ favor_status favor_bidir_state(FAVOR_ARGS) { return run(false, kState, FAVOR_PAS
 favor_status favor_bidir_output(FAVOR_ARGS) { return run(false, kOutput, FAVOR_PASS); }
 favor_status favor_causal_state(FAVOR_ARGS) { return run(true, kState, FAVOR_PASS); }
 favor_status favor_causal_output(FAVOR_ARGS) { return run(true, kOutput, FAVOR_PASS); }
+
+favor_status favor_fwd_bidir_fm(const void* Q, const void* K, const void* V, void* O, int B, int H, int L, int d,
+                                const float* omega, int m, favor_dtype dt, float qk_scale, favor_feature_map fm,
+                                void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return run(false, kBoth, FAVOR_PASS, static_cast<int>(fm));
+}
+favor_status favor_fwd_causal_fm(const void* Q, const void* K, const void* V, void* O, int B, int H, int L, int d,
+                                 const float* omega, int m, favor_dtype dt, float qk_scale, favor_feature_map fm,
+                                 void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return run(true, kBoth, FAVOR_PASS, static_cast<int>(fm));
+}
 
 favor_status favor_decode_step(const void* q, const void* k, const void* v, void* o, int B, int H, int d,
                                const float* omega, int m, favor_dtype dt, float qk_scale, float* state,

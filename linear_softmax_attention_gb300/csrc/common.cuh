@@ -97,15 +97,19 @@ cudaError_t simt_state_export(const void* K, const void* V, const float* omega, 
 cudaError_t launch_decode_step(const void* q, const void* k, const void* v, void* o, int BH, int d,
                                const float* omega, int m, bool bf16, float scale, float* state, int32_t* status,
                                cudaStream_t stream);
+// fm: favor_feature_map (FAVOR_FM_PRF or FAVOR_FM_RELU)
 cudaError_t simt_bidir_state(const void* K, const void* V, const float* omega, float scale,
-                             const Shape& s, bool bf16, void* ws, int32_t* st, cudaStream_t stream);
+                             const Shape& s, bool bf16, void* ws, int32_t* st, cudaStream_t stream,
+                             int fm = FAVOR_FM_PRF);
 cudaError_t simt_bidir_output(const void* Q, void* O, const float* omega, float scale,
-                              const Shape& s, bool bf16, void* ws, int32_t* st, cudaStream_t stream);
+                              const Shape& s, bool bf16, void* ws, int32_t* st, cudaStream_t stream,
+                              int fm = FAVOR_FM_PRF);
 cudaError_t simt_causal_state(const void* K, const void* V, const float* omega, float scale,
-                              const Shape& s, bool bf16, void* ws, int32_t* st, cudaStream_t stream);
+                              const Shape& s, bool bf16, void* ws, int32_t* st, cudaStream_t stream,
+                              int fm = FAVOR_FM_PRF);
 cudaError_t simt_causal_output(const void* Q, const void* K, const void* V, void* O,
                                const float* omega, float scale, const Shape& s, bool bf16, void* ws,
-                               int32_t* st, cudaStream_t stream);
+                               int32_t* st, cudaStream_t stream, int fm = FAVOR_FM_PRF);
 
 // The checked, dispatched body of every forward entry point (stage: 1 state,
 // 2 output, 3 both).

@@ -15,6 +15,8 @@
 //  * query side: the per-row constant max_i(s w_i.q) is subtracted, and
 //    |q|^2/2 and m^-1/2 are dropped -- per-query constants cancel ("From
 //    Performer to Linear Attention", §Simple Derivation).
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace favor {
@@ -62,7 +64,16 @@ __device__ __forceinline__ float dot_row(const float* x, const float* w, int d) 
 //   S_p[f, :] = sum_t exp(l_tf - R) [v_t ; 1],  l_tf = s w_f.k_t - s^2 |k_t|^2 / 2
 // over its token range.
 // ---------------------------------------------------------------------------
-template <typename T>
+// Key feature from its scaled projection a = s w.k: exp(a - s^2 |k|^2 / 2 - R)
+// for the positive random features, relu(a) for Performer-ReLU ("y < 0 ? 0
+// : y" keeps a NaN a NaN).
+template <int FM>
+__device__ __forceinline__ float key_feature(float a, float half_sq, float R) {
+  if constexpr (FM == FAVOR_FM_PRF) return expf(a - half_sq - R);
+  else return a < 0.f ? 0.f : a;
+}
+
+template <typename T, int FM>
 __global__ void __launch_bounds__(kThreads) state_partial_kernel(
     const T* __restrict__ K, const T* __restrict__ V, const float* __restrict__ omega,
     const float* __restrict__ key_ref, int L, int d, int m, float scale, int chunk, int n_split,
@@ -106,8 +117,7 @@ __global__ void __launch_bounds__(kThreads) state_partial_kernel(
       const int t = t_base + 4 * j;
       float p = 0.f;
       if (t < nt && f_own < nf) {
-        const float l = scale * dot_row(ks + t * ld, om + f_own * ld, d) - hs2 * kn[t];
-        p = expf(l - R);
+        p = key_feature<FM>(scale * dot_row(ks + t * ld, om + f_own * ld, d), hs2 * kn[t], R);
       }
       ph[t * (kFB + 1) + f_own] = p;
     }
@@ -147,6 +157,7 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const float* __restrict
 
 // Query-side features of one tile: pq[t][i] = exp(s w_i.q_t - max_i s w_i.q_t)
 // (all m features, exact row maximum), rows t >= nt set to 0.
+template <int FM>
 __device__ void query_features(const float* qs, int nt, int d, int m, float scale,
                                const float* __restrict__ omega, float* om, float* pq, float* rowmax) {
   const int ld = d + 1, ldq = m + 1;
@@ -164,6 +175,16 @@ __device__ void query_features(const float* qs, int nt, int d, int m, float scal
     }
   }
   __syncthreads();
+  if constexpr (FM == FAVOR_FM_RELU) {
+    // Performer-ReLU: relu of the scaled projection, no row constant
+    for (int e = threadIdx.x; e < kTT * m; e += kThreads) {
+      const int t = e / m, f = e - t * m;
+      const float a = pq[t * ldq + f];
+      pq[t * ldq + f] = (t < nt) ? (a < 0.f ? 0.f : a) : 0.f;
+    }
+    __syncthreads();
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int t = warp; t < kTT; t += kThreads / 32) {
     float mx = -INFINITY;
@@ -192,7 +213,7 @@ __device__ __forceinline__ void store_output(const float* num, int nt, int d, T*
   }
 }
 
-template <typename T>
+template <typename T, int FM>
 __global__ void __launch_bounds__(kThreads) bidir_output_kernel(
     const T* __restrict__ Q, T* __restrict__ O, const float* __restrict__ omega,
     const float* __restrict__ state, int L, int d, int m, float scale, int32_t* status) {
@@ -208,7 +229,7 @@ __global__ void __launch_bounds__(kThreads) bidir_output_kernel(
   float* rowmax = pq + kTT * ldq;     // [kTT]
 
   load_rows(Q + ((size_t)bh * L + t0) * d, nt, d, qs, ld);
-  query_features(qs, nt, d, m, scale, omega, om, pq, rowmax);
+  query_features<FM>(qs, nt, d, m, scale, omega, om, pq, rowmax);
 
   const int ta = threadIdx.x / 8, jb = threadIdx.x % 8;
   float acc[17];
@@ -247,7 +268,7 @@ __global__ void __launch_bounds__(kThreads) bidir_output_kernel(
 // each tile adds the masked intra-tile term, the inter term phi(Q) G and then
 // G += phi(K)^T [V | 1].  G lives in the workspace (fp32).
 // ---------------------------------------------------------------------------
-template <typename T>
+template <typename T, int FM>
 __global__ void __launch_bounds__(kThreads) causal_output_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V, T* __restrict__ O,
     const float* __restrict__ omega, const float* __restrict__ key_ref, const float* __restrict__ partS,
@@ -300,12 +321,12 @@ __global__ void __launch_bounds__(kThreads) causal_output_kernel(
       for (int j = 0; j < kTT / 4; ++j) {
         const int t = t_base + 4 * j;
         if (f_own < nf) {
-          const float l = scale * dot_row(ks + t * ld, om + f_own * ld, d) - hs2 * kn[t];
-          pk[t * ldq + f0 + f_own] = (t < nt) ? expf(l - Rk) : 0.f;
+          const float a = scale * dot_row(ks + t * ld, om + f_own * ld, d);
+          pk[t * ldq + f0 + f_own] = (t < nt) ? key_feature<FM>(a, hs2 * kn[t], Rk) : 0.f;
         }
       }
     }
-    query_features(qs, nt, d, m, scale, omega, om, pq, rowmax);
+    query_features<FM>(qs, nt, d, m, scale, omega, om, pq, rowmax);
     // intra-tile scores, lower triangle with the diagonal
     for (int e = threadIdx.x; e < kTT * kTT; e += kThreads) {
       const int t = e / kTT, s = e - t * kTT;
@@ -404,14 +425,14 @@ static cudaError_t set_smem(KernelT k, size_t bytes) {
   return ensure_dynamic_smem(reinterpret_cast<const void*>(k), bytes);
 }
 
-template <typename T>
+template <typename T, int FM>
 static cudaError_t state_impl(const void* K, const void* V, const float* omega, float scale, const Shape& s,
                               const SimtPlan& p, char* ws, cudaStream_t stream) {
   float* key_ref = reinterpret_cast<float*>(ws);
   cudaError_t e = launch_prep(omega, s.m, s.d, key_ref, nullptr, nullptr, 0, stream);
   if (e != cudaSuccess) return e;
   const size_t smem = state_smem(s.d);
-  auto kern = state_partial_kernel<T>;
+  auto kern = state_partial_kernel<T, FM>;
   e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_split, p.n_fb, s.BH());
@@ -421,13 +442,23 @@ static cudaError_t state_impl(const void* K, const void* V, const float* omega, 
   return cudaGetLastError();
 }
 
+// (storage type, feature map) as template arguments of `f`
+template <typename F>
+static cudaError_t dispatch(bool bf16, int fm, F&& f) {
+  using Prf = std::integral_constant<int, FAVOR_FM_PRF>;
+  using Relu = std::integral_constant<int, FAVOR_FM_RELU>;
+  if (bf16) return fm == FAVOR_FM_RELU ? f(__nv_bfloat16{}, Relu{}) : f(__nv_bfloat16{}, Prf{});
+  return fm == FAVOR_FM_RELU ? f(float{}, Relu{}) : f(float{}, Prf{});
+}
+
 cudaError_t simt_bidir_state(const void* K, const void* V, const float* omega, float scale, const Shape& s,
-                             bool bf16, void* ws, int32_t* st, cudaStream_t stream) {
+                             bool bf16, void* ws, int32_t* st, cudaStream_t stream, int fm) {
   (void)st;
   const SimtPlan p = simt_plan(false, s);
   char* w = static_cast<char*>(ws);
-  cudaError_t e = bf16 ? state_impl<__nv_bfloat16>(K, V, omega, scale, s, p, w, stream)
-                       : state_impl<float>(K, V, omega, scale, s, p, w, stream);
+  cudaError_t e = dispatch(bf16, fm, [&](auto t, auto f) {
+    return state_impl<decltype(t), decltype(f)::value>(K, V, omega, scale, s, p, w, stream);
+  });
   if (e != cudaSuccess) return e;
   merge_kernel<<<s.BH(), kThreads, 0, stream>>>(reinterpret_cast<float*>(w + p.off_partS), s.d, s.m, p.n_split,
                                                 reinterpret_cast<float*>(w + p.off_state));
@@ -456,19 +487,19 @@ cudaError_t simt_state_export(const void* K, const void* V, const float* omega, 
                               bool bf16, void* ws, float* state, cudaStream_t stream) {
   const SimtPlan p = simt_plan(false, s);
   char* w = static_cast<char*>(ws);
-  cudaError_t e = bf16 ? state_impl<__nv_bfloat16>(K, V, omega, scale, s, p, w, stream)
-                       : state_impl<float>(K, V, omega, scale, s, p, w, stream);
+  cudaError_t e = bf16 ? state_impl<__nv_bfloat16, FAVOR_FM_PRF>(K, V, omega, scale, s, p, w, stream)
+                       : state_impl<float, FAVOR_FM_PRF>(K, V, omega, scale, s, p, w, stream);
   if (e != cudaSuccess) return e;
   merge_transposed_kernel<<<s.BH(), kThreads, 0, stream>>>(reinterpret_cast<float*>(w + p.off_partS), s.d, s.m,
                                                             p.n_split, state);
   return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, int FM>
 static cudaError_t bidir_out_impl(const void* Q, void* O, const float* omega, float scale, const Shape& s,
                                   const SimtPlan& p, char* ws, int32_t* st, cudaStream_t stream) {
   const size_t smem = bidir_out_smem(s.d, s.m);
-  auto kern = bidir_output_kernel<T>;
+  auto kern = bidir_output_kernel<T, FM>;
   cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((s.L + kTT - 1) / kTT, s.BH());
@@ -479,28 +510,30 @@ static cudaError_t bidir_out_impl(const void* Q, void* O, const float* omega, fl
 }
 
 cudaError_t simt_bidir_output(const void* Q, void* O, const float* omega, float scale, const Shape& s,
-                              bool bf16, void* ws, int32_t* st, cudaStream_t stream) {
+                              bool bf16, void* ws, int32_t* st, cudaStream_t stream, int fm) {
   const SimtPlan p = simt_plan(false, s);
   char* w = static_cast<char*>(ws);
-  return bf16 ? bidir_out_impl<__nv_bfloat16>(Q, O, omega, scale, s, p, w, st, stream)
-              : bidir_out_impl<float>(Q, O, omega, scale, s, p, w, st, stream);
+  return dispatch(bf16, fm, [&](auto t, auto f) {
+    return bidir_out_impl<decltype(t), decltype(f)::value>(Q, O, omega, scale, s, p, w, st, stream);
+  });
 }
 
 cudaError_t simt_causal_state(const void* K, const void* V, const float* omega, float scale, const Shape& s,
-                              bool bf16, void* ws, int32_t* st, cudaStream_t stream) {
+                              bool bf16, void* ws, int32_t* st, cudaStream_t stream, int fm) {
   (void)st;
   const SimtPlan p = simt_plan(true, s);
   char* w = static_cast<char*>(ws);
-  return bf16 ? state_impl<__nv_bfloat16>(K, V, omega, scale, s, p, w, stream)
-              : state_impl<float>(K, V, omega, scale, s, p, w, stream);
+  return dispatch(bf16, fm, [&](auto t, auto f) {
+    return state_impl<decltype(t), decltype(f)::value>(K, V, omega, scale, s, p, w, stream);
+  });
 }
 
-template <typename T>
+template <typename T, int FM>
 static cudaError_t causal_out_impl(const void* Q, const void* K, const void* V, void* O, const float* omega,
                                    float scale, const Shape& s, const SimtPlan& p, char* ws, int32_t* st,
                                    cudaStream_t stream) {
   const size_t smem = causal_out_smem(s.d, s.m);
-  auto kern = causal_output_kernel<T>;
+  auto kern = causal_output_kernel<T, FM>;
   cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_split, s.BH());
@@ -513,11 +546,12 @@ static cudaError_t causal_out_impl(const void* Q, const void* K, const void* V, 
 
 cudaError_t simt_causal_output(const void* Q, const void* K, const void* V, void* O, const float* omega,
                                float scale, const Shape& s, bool bf16, void* ws, int32_t* st,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, int fm) {
   const SimtPlan p = simt_plan(true, s);
   char* w = static_cast<char*>(ws);
-  return bf16 ? causal_out_impl<__nv_bfloat16>(Q, K, V, O, omega, scale, s, p, w, st, stream)
-              : causal_out_impl<float>(Q, K, V, O, omega, scale, s, p, w, st, stream);
+  return dispatch(bf16, fm, [&](auto t, auto f) {
+    return causal_out_impl<decltype(t), decltype(f)::value>(Q, K, V, O, omega, scale, s, p, w, st, stream);
+  });
 }
 
 }  // namespace favor

@@ -205,6 +205,33 @@ __device__ __forceinline__ void exp_pack(uint32_t (&x)[N], float c1, float b, bo
   }
 }
 
+// Feature maps: positive random features (the softmax kernel) or
+// Performer-ReLU, relu(s w.x) ("Rethinking Attention with Performers"
+// summary, §2 generalized kernelizable attention: other kernels by changing
+// the feature-map function).  ReLU: b = 0 on valid rows and +inf past the
+// sequence end (feature 0); "y < 0 ? 0 : y" keeps a NaN a NaN.
+template <int N>
+__device__ __forceinline__ void relu_pack(uint32_t (&x)[N], float c1, float b) {
+#pragma unroll
+  for (int j = 0; j < N / 2; ++j) {
+    float y0 = fmaf(__uint_as_float(x[2 * j]), c1, -b);
+    float y1 = fmaf(__uint_as_float(x[2 * j + 1]), c1, -b);
+    y0 = y0 < 0.f ? 0.f : y0;
+    y1 = y1 < 0.f ? 0.f : y1;
+    x[j] = pack_bf16(y0, y1);
+  }
+}
+template <int FM, int N>
+__device__ __forceinline__ void feature_pack(uint32_t (&x)[N], float c1, float b) {
+  if constexpr (FM == FAVOR_FM_PRF) exp_pack<N>(x, c1, b, true);
+  else relu_pack<N>(x, c1, b);
+}
+// multiplier of the projection in the feature exponent / argument
+template <int FM>
+__device__ __forceinline__ float feature_c1(float scale) {
+  return FM == FAVOR_FM_PRF ? scale * kLog2e : scale;
+}
+
 // Row t, columns col0 .. col0 + 2*NW - 1 (col0 a multiple of 8) of a tile of
 // 64-column swizzle blocks `atom_stride` bytes apart, from NW packed words.
 template <int NW, int N>
@@ -276,7 +303,7 @@ struct StateCfg {
   static constexpr int kSmem = kBars + 512 + 1024;
 };
 
-template <int D, int M>
+template <int D, int M, int FM>
 __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_constant__ CUtensorMap mapK,
                                                                  const __grid_constant__ CUtensorMap mapV,
                                                                  StateParams prm) {
@@ -442,7 +469,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     const int col0 = wg * 64;                      // this warpgroup's columns of each feature block
     float R, W_unused;
     key_reference(prm.key_ref, prm.m, &R, &W_unused);
-    const float c1 = prm.scale * kLog2e;
+    const float c1 = feature_c1<FM>(prm.scale);
     const float hs2 = 0.5f * prm.scale * prm.scale;
     bool ok = true;
     // m = 256: warpgroup w owns feature block w (128 columns in two passes),
@@ -458,7 +485,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
       if (!mbar_wait(&kn_full[st], (i / C::NS) & 1, wctx)) { ok = false; break; }
       // rows past L get 2^-inf = 0
       const bool valid = (tile0 + i) * kBM + t < prm.L;
-      const float bias = valid ? (hs2 * norm_s[st * kBM + t] + R) * kLog2e : INFINITY;
+      const float bias = !valid ? INFINITY : (FM == FAVOR_FM_PRF ? (hs2 * norm_s[st * kBM + t] + R) * kLog2e : 0.f);
       if (!mbar_wait(&p_full[my_fb], i & 1, wctx)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
@@ -472,7 +499,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
           __syncwarp();
           if (lane == 0) mbar_arrive(&p_free[my_fb]);
         }
-        exp_pack<64>(x, c1, bias, true);
+        feature_pack<FM>(x, c1, bias);
         FAVOR_TRACE_POINT(2);
         if (ps == 0 && i >= 1 && !mbar_wait(&phi_free[my_fb], (i - 1) & 1, wctx)) { ok = false; break; }
         store_row<32>(phi_a, kAtom, t, c0 + 64 * ps, x);
@@ -605,7 +632,7 @@ struct OutCfg {
   static constexpr int kSmem = kBars + 512 + 1024;
 };
 
-template <int D, int M>
+template <int D, int M, int FM>
 __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_constant__ CUtensorMap mapQ,
                                                                 const __grid_constant__ CUtensorMap mapO,
                                                                 OutParams prm) {
@@ -766,7 +793,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
     const int col0 = wg * 64;                      // this warpgroup's columns of each feature block
     float R_unused, W;
     key_reference(prm.key_ref, prm.m, &R_unused, &W);
-    const float c1 = prm.scale * kLog2e;
+    const float c1 = feature_c1<FM>(prm.scale);
     const uint32_t out_a = smem_addr(sm + C::kOut);
     bool ok = true;
     auto store_out = [&](int j) {
@@ -814,7 +841,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
       const float qn = qnorm[st * kBM + t];
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_empty[st]);
-      const float bias = (prm.scale * W * sqrtf(qn) - kQueryHeadroom) * kLog2e;
+      const float bias = FM == FAVOR_FM_PRF ? (prm.scale * W * sqrtf(qn) - kQueryHeadroom) * kLog2e : 0.f;
       // m = 256: two passes of 64 columns over the owned block; m = 128: the
       // warpgroups split the block's columns
       constexpr int kPasses = (NFB == 2) ? 2 : 1;
@@ -833,7 +860,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
           if (lane == 0) mbar_arrive(&p_free[my_fb]);
         }
         if (ok) {
-          exp_pack<64>(x, c1, bias, true);
+          feature_pack<FM>(x, c1, bias);
           if (ps == 0 && i >= 1) ok = mbar_wait(&phi_free[my_fb], (i - 1) & 1, wctx);
           if (ok) store_row<32>(smem_addr(sm + C::kPhi + my_fb * 2 * kAtom), kAtom, t, c0 + 64 * ps, x);
         }
@@ -897,7 +924,7 @@ struct CausalCfg {
 static_assert(CausalCfg<64>::kSmem <= 232448, "shared memory");
 static_assert(StateCfg<64>::kSmem <= 232448, "shared memory");
 
-template <int D, int M>
+template <int D, int M, int FM>
 __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_constant__ CUtensorMap mapQ,
                                                                    const __grid_constant__ CUtensorMap mapK,
                                                                    const __grid_constant__ CUtensorMap mapV,
@@ -1140,7 +1167,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     float R, W;
     key_reference(prm.key_ref, prm.m, &R, &W);
-    const float c1 = prm.scale * kLog2e;
+    const float c1 = feature_c1<FM>(prm.scale);
     const float hs2 = 0.5f * prm.scale * prm.scale;
     const uint32_t kg_a = smem_addr(sm + C::kKG), phiq_a = smem_addr(sm + C::kPhiQ);
     const uint32_t ma_a = smem_addr(sm + C::kMA);
@@ -1224,7 +1251,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
         if (ok) ok = mbar_wait(pk_full, u & 1, wctx);
         if (ok && fb == 0) ok = mbar_wait(&kn_full[c & 1], (c >> 1) & 1, wctx);
         // rows past the sequence end: an infinite bias makes their features 0
-        const float bias_k = valid ? (hs2 * nk[t] + R) * kLog2e : INFINITY;
+        const float bias_k = !valid ? INFINITY : (FM == FAVOR_FM_PRF ? (hs2 * nk[t] + R) * kLog2e : 0.f);
         tc_fence_after();
         {
           // loaded even after a failed wait (the kernel is then aborting and the
@@ -1236,7 +1263,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(x_free);
-          if (ok) exp_pack<64>(x, c1, bias_k, true);
+          if (ok) feature_pack<FM>(x, c1, bias_k);
           FAVOR_TRACE_POINT(31);
           if (ok && u >= 1) ok = mbar_wait(kg_free, (u - 1) & 1, wctx);
           if (ok && c >= 1) ok = mbar_wait(&gdone[fb], (c - 1) & 1, wctx);
@@ -1283,7 +1310,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
         if (ok) ok = mbar_wait(pq_full, u & 1, wctx);
         if (ok && fb == 0) {
           ok = mbar_wait(&qn_full[c & 1], (c >> 1) & 1, wctx);
-          bias_q = (prm.scale * W * sqrtf(nk[kBM + t]) - kQueryHeadroom) * kLog2e;
+          bias_q = FM == FAVOR_FM_PRF ? (prm.scale * W * sqrtf(nk[kBM + t]) - kQueryHeadroom) * kLog2e : 0.f;
         }
         tc_fence_after();
         {
@@ -1296,7 +1323,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(x_free);
-          if (ok) exp_pack<64>(x, c1, bias_q, true);
+          if (ok) feature_pack<FM>(x, c1, bias_q);
           FAVOR_TRACE_POINT(36);
           if (ok && u >= 1) ok = mbar_wait(phiq_free, (u - 1) & 1, wctx);
           if (ok) store_row<32>(phiq_a, kAtom, t, col0, x);
@@ -1385,7 +1412,7 @@ bool make_map(CUtensorMap* map, const void* base, const Shape& s) {
   return r == CUDA_SUCCESS;
 }
 
-template <int D, int M>
+template <int D, int M, int FM>
 cudaError_t launch_state(const void* K, const void* V, const Shape& s, const TcPlan& p, float scale, char* ws,
                          int32_t* status, cudaStream_t stream) {
   if (p.n_split < 1) return cudaSuccess;
@@ -1405,14 +1432,14 @@ cudaError_t launch_state(const void* K, const void* V, const Shape& s, const TcP
   prm.merge = p.causal ? 0 : 1;
   prm.scale = scale;
   const size_t smem = StateCfg<D>::kSmem;
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(state_kernel<D, M>), smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(state_kernel<D, M, FM>), smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_split, s.BH());
-  state_kernel<D, M><<<grid, kStateThreads, smem, stream>>>(mk, mv, prm);
+  state_kernel<D, M, FM><<<grid, kStateThreads, smem, stream>>>(mk, mv, prm);
   return cudaGetLastError();
 }
 
-template <int D, int M>
+template <int D, int M, int FM>
 cudaError_t launch_output(const void* Q, void* O, const Shape& s, const TcPlan& p, float scale, char* ws,
                           int32_t* status, cudaStream_t stream) {
   CUtensorMap mq, mo;
@@ -1427,14 +1454,14 @@ cudaError_t launch_output(const void* Q, void* O, const Shape& s, const TcPlan& 
   prm.tiles_per_cta = p.out_tiles_per_cta;
   prm.scale = scale;
   const size_t smem = OutCfg<D>::kSmem;
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(output_kernel<D, M>), smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(output_kernel<D, M, FM>), smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.out_ctas, s.BH());
-  output_kernel<D, M><<<grid, kOutThreads, smem, stream>>>(mq, mo, prm);
+  output_kernel<D, M, FM><<<grid, kOutThreads, smem, stream>>>(mq, mo, prm);
   return cudaGetLastError();
 }
 
-template <int D, int M>
+template <int D, int M, int FM>
 cudaError_t launch_causal(const void* Q, const void* K, const void* V, void* O, const Shape& s, const TcPlan& p,
                           float scale, char* ws, int32_t* status, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mo;
@@ -1452,10 +1479,10 @@ cudaError_t launch_causal(const void* Q, const void* K, const void* V, void* O, 
   prm.sub_per_sc = p.sub_per_sc;
   prm.scale = scale;
   const size_t smem = CausalCfg<D>::kSmem;
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(causal_kernel<D, M>), smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(causal_kernel<D, M, FM>), smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.out_ctas, s.BH());
-  causal_kernel<D, M><<<grid, kCausalThreads, smem, stream>>>(mq, mk, mv, mo, prm);
+  causal_kernel<D, M, FM><<<grid, kCausalThreads, smem, stream>>>(mq, mk, mv, mo, prm);
   return cudaGetLastError();
 }
 
@@ -1469,8 +1496,9 @@ bool tc_supported(bool causal, int d, int m, bool bf16) {
 
 size_t tc_workspace_bytes(bool causal, const Shape& s) { return tc_plan(causal, s).bytes; }
 
-cudaError_t tc_state(bool causal, const void* K, const void* V, const float* omega, float scale, const Shape& s,
-                     void* ws, int32_t* status, cudaStream_t stream) {
+template <int FM>
+cudaError_t tc_state_fm(bool causal, const void* K, const void* V, const float* omega, float scale, const Shape& s,
+                        void* ws, int32_t* status, cudaStream_t stream) {
   const TcPlan p = tc_plan(causal, s);
   char* w = static_cast<char*>(ws);
   // prep also zeroes the bidirectional merge counters
@@ -1479,20 +1507,33 @@ cudaError_t tc_state(bool causal, const void* K, const void* V, const float* ome
                               causal ? nullptr : reinterpret_cast<uint32_t*>(w + p.off_counters), causal ? 0 : s.BH(),
                               stream);
   if (e != cudaSuccess) return e;
-  return s.m == 256 ? launch_state<64, 256>(K, V, s, p, scale, w, status, stream)
-                    : launch_state<64, 128>(K, V, s, p, scale, w, status, stream);
+  return s.m == 256 ? launch_state<64, 256, FM>(K, V, s, p, scale, w, status, stream)
+                    : launch_state<64, 128, FM>(K, V, s, p, scale, w, status, stream);
 }
 
-cudaError_t tc_output(bool causal, const void* Q, const void* K, const void* V, void* O, const float* omega,
-                      float scale, const Shape& s, void* ws, int32_t* status, cudaStream_t stream) {
-  (void)omega;
+template <int FM>
+cudaError_t tc_output_fm(bool causal, const void* Q, const void* K, const void* V, void* O, const Shape& s,
+                         float scale, void* ws, int32_t* status, cudaStream_t stream) {
   const TcPlan p = tc_plan(causal, s);
   char* w = static_cast<char*>(ws);
   if (causal)
-    return s.m == 256 ? launch_causal<64, 256>(Q, K, V, O, s, p, scale, w, status, stream)
-                      : launch_causal<64, 128>(Q, K, V, O, s, p, scale, w, status, stream);
-  return s.m == 256 ? launch_output<64, 256>(Q, O, s, p, scale, w, status, stream)
-                    : launch_output<64, 128>(Q, O, s, p, scale, w, status, stream);
+    return s.m == 256 ? launch_causal<64, 256, FM>(Q, K, V, O, s, p, scale, w, status, stream)
+                      : launch_causal<64, 128, FM>(Q, K, V, O, s, p, scale, w, status, stream);
+  return s.m == 256 ? launch_output<64, 256, FM>(Q, O, s, p, scale, w, status, stream)
+                    : launch_output<64, 128, FM>(Q, O, s, p, scale, w, status, stream);
+}
+
+cudaError_t tc_state(bool causal, const void* K, const void* V, const float* omega, float scale, const Shape& s,
+                     void* ws, int32_t* status, cudaStream_t stream, int fm) {
+  return fm == FAVOR_FM_RELU ? tc_state_fm<FAVOR_FM_RELU>(causal, K, V, omega, scale, s, ws, status, stream)
+                             : tc_state_fm<FAVOR_FM_PRF>(causal, K, V, omega, scale, s, ws, status, stream);
+}
+
+cudaError_t tc_output(bool causal, const void* Q, const void* K, const void* V, void* O, const float* omega,
+                      float scale, const Shape& s, void* ws, int32_t* status, cudaStream_t stream, int fm) {
+  (void)omega;
+  return fm == FAVOR_FM_RELU ? tc_output_fm<FAVOR_FM_RELU>(causal, Q, K, V, O, s, scale, ws, status, stream)
+                             : tc_output_fm<FAVOR_FM_PRF>(causal, Q, K, V, O, s, scale, ws, status, stream);
 }
 
 }  // namespace favor

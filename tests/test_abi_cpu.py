@@ -134,3 +134,19 @@ def test_decode_rejects_bad_arguments_before_launch(lib):
     assert prefill(m=600) == 2
     assert lib.favor_decode_prefill_workspace_bytes(2, 8, 300, 64, 256, 1) > 0
     assert lib.favor_decode_prefill_workspace_bytes(2, 8, 0, 64, 256, 1) == 0
+
+
+@pytest.mark.parametrize("name", ["favor_fwd_bidir_fm", "favor_fwd_causal_fm"])
+def test_feature_map_calls_reject_bad_arguments(lib, name):
+    def call(fm=1, **kw):
+        a = dict(Q=16, K=16, V=16, O=32, B=1, H=1, L=8, d=8, omega=48, m=8, dt=0, s=1.0, ws=256, nbytes=1 << 30,
+                 st=None, stream=None)
+        a.update(kw)
+        return getattr(lib, name)(a["Q"], a["K"], a["V"], a["O"], a["B"], a["H"], a["L"], a["d"], a["omega"],
+                                  a["m"], a["dt"], a["s"], fm, a["ws"], a["nbytes"], a["st"], a["stream"])
+    assert call(fm=2) == 1             # not a favor_feature_map
+    assert call(fm=-1) == 1
+    assert call(omega=None) == 1
+    assert call(L=0) == 1
+    assert call(m=600) == 2
+    assert call(nbytes=16) == 1
