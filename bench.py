@@ -51,6 +51,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--decode-steps", type=int, default=200)
+    ap.add_argument("--relu-steps", type=int, default=100)
     return ap.parse_args()
 
 
@@ -408,6 +409,10 @@ def run_gpu(args, rank, world, local_rank):
 
     hbm, tc_burst, tc_sus, peak_kind = load_peaks()
     decode = measure_decode(favor, args.decode_steps, stream, status, hbm, dev) if args.decode_steps > 0 else None
+    relu = None
+    if args.relu_steps > 0:
+        relu = measure_feature_map(favor, "relu", args.relu_steps, sets, omegas[0], s, ws_b, ws_c, O_b, O_c, stream,
+                                   status, dev, tokens_per_step)
     # dominant kernel: largest share of the step
     dom = max((st for st in STAGES if st != "build_orf"), key=lambda st: stage_ms[st])
     nbytes, nflops = algorithmic(w, dom)
@@ -463,6 +468,7 @@ def run_gpu(args, rank, world, local_rank):
         "wall_s_timed": t_wall,
         "e2e": e2e,
         "decode": decode,
+        "relu": relu,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=12.0)
@@ -543,6 +549,39 @@ def run_reference(args, rank, world):
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
+
+
+def measure_feature_map(favor, fm, n_steps, sets, omega, s, ws_b, ws_c, O_b, O_c, stream, status, dev,
+                        tokens_per_step):
+    """The bidirectional and causal forward passes of the step with another
+    feature map (Performer-ReLU): same workload, Omega built once, inputs
+    rotating over the sets (above L2), one CUDA graph per input set."""
+    graphs = []
+    for q, k, v in sets:
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                favor.fwd_bidir(q, k, v, omega, s, ws_b, O=O_b, dev_status=status, stream=stream, feature_map=fm)
+                favor.fwd_causal(q, k, v, omega, s, ws_c, O=O_c, dev_status=status, stream=stream, feature_map=fm)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            favor.fwd_bidir(q, k, v, omega, s, ws_b, O=O_b, dev_status=status, stream=stream, feature_map=fm)
+            favor.fwd_causal(q, k, v, omega, s, ws_c, O=O_c, dev_status=status, stream=stream, feature_map=fm)
+        graphs.append(g)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for g in graphs:
+            g.replay()
+        e0.record(stream)
+        for i in range(n_steps):
+            graphs[i % len(graphs)].replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after the {fm} steps")
+    ms = e0.elapsed_time(e1) / n_steps
+    return {"feature_map": fm, "value": tokens_per_step / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "steps": n_steps, "step": "bidirectional + causal forward (Omega built once)"}
 
 
 DECODE_B, DECODE_H, DECODE_D, DECODE_M = 256, 8, 64, 256
