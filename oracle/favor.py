@@ -56,6 +56,7 @@ __all__ = [
     "favor_causal",
     "favor_causal_quadratic",
     "favor_rows",
+    "favor_bidirectional_grad",
     "softmax_attention",
     "rowwise_rel_err",
 ]
@@ -347,6 +348,52 @@ def favor_rows(Q, K, V, Omega, scale: float, bh_rows, causal: bool, features: st
                 z = pk[: t + 1].sum(axis=0)
             out[n] = (pq @ kv) / (pq @ z)
     return out
+
+
+def favor_bidirectional_grad(Q, K, V, Omega, scale: float, dO, features: str = "prf"):
+    """Gradients (dQ, dK, dV) of sum(dO * favor_bidirectional(Q, K, V)).
+
+    The chain rule through the forward of [digest] §Key equations, step by
+    step (Q, K, V [..., L, d], dO like the output; fp64):
+      N = phi(Q) S,  S = phi(K)^T V,  D = phi(Q) z,  z = phi(K)^T 1,  O = N / D
+      dN = dO / D,   dD = -sum_j(dO O) / D
+      dphi(Q) = dN S^T + dD z^T
+      dS = phi(Q)^T dN,  dz = phi(Q)^T dD
+      dphi(K) = V dS^T + 1 dz^T,  dV = phi(K) dS
+    and through the feature map x' = scale x, phi = f(Omega x' ...):
+      prf:  d phi_i / d x' = phi_i (w_i - x')
+      relu: d phi_i / d x' = m^-1/2 w_i [w_i . x' > 0]
+    then dx = scale dx'.
+    """
+    Q, K, V, dO = (np.asarray(a, dtype=np.float64) for a in (Q, K, V, dO))
+    Om = np.asarray(Omega, dtype=np.float64)
+    qs, ks = scale * Q, scale * K
+    fn = FEATURES[features]
+    pq, pk = fn(qs, Om), fn(ks, Om)
+    S = np.swapaxes(pk, -1, -2) @ V                  # [..., m, d]
+    z = np.sum(pk, axis=-2)                          # [..., m]
+    N = pq @ S                                       # [..., L, d]
+    D = np.einsum("...lm,...m->...l", pq, z)         # [..., L]
+    O = N / D[..., None]
+    dN = dO / D[..., None]
+    dD = -np.sum(dO * O, axis=-1) / D
+    dpq = dN @ np.swapaxes(S, -1, -2) + dD[..., None] * z[..., None, :]
+    dS = np.swapaxes(pq, -1, -2) @ dN
+    dz = np.einsum("...lm,...l->...m", pq, dD)
+    dpk = V @ np.swapaxes(dS, -1, -2) + dz[..., None, :]
+    dV = pk @ dS
+
+    def through_features(x, phi, dphi):
+        if features == "prf":
+            # sum_i dphi_i phi_i (w_i - x)
+            g = dphi * phi
+            return g @ Om - x * np.sum(g, axis=-1, keepdims=True)
+        mask = (x @ Om.T) > 0
+        return ((dphi * mask) @ Om) / math.sqrt(Om.shape[0])
+
+    dQ = scale * through_features(qs, pq, dpq)
+    dK = scale * through_features(ks, pk, dpk)
+    return dQ, dK, dV
 
 
 def softmax_attention(Q, K, V, scale: float, causal: bool = False) -> np.ndarray:
