@@ -236,6 +236,27 @@ favor_status favor_fwd_bidir_static(const void* Q, const void* K, const void* V,
 size_t favor_static_scratch_bytes(void);
 
 /*
+ * favor_bwd_bidir — gradients of the bidirectional pass: given dO = dL/dO
+ * for O = favor_fwd_bidir_fm(Q, K, V), writes dQ, dK, dV (contiguous
+ * [B, H, L, d], dtype `dt`, not aliasing the inputs).  The chain rule
+ * through the forward ("Performer" digest, §Key equations):
+ *   N = phi(Q) S, D = phi(Q) z, O = N / D;  dN^ = [dO / D | -(dO . N) / D^2]
+ *   dphi(Q) = S~ dN^,  dS~ = phi(Q)^T dN^,  dphi(K) = dS~ [V | 1]^T,
+ *   dV = phi(K) dS~[:, :d],  dx = s (sum_i g_i w_i - [prf] s x sum_i g_i)
+ * with g = dphi phi (positive random features) or dphi [s w.x > 0] (ReLU);
+ * Omega is not differentiated (it is a fixed random draw).  CUDA-core
+ * kernels, fp32 arithmetic, any supported shape; workspace of
+ * favor_bwd_workspace_bytes(...) bytes.  A zero or non-finite normaliser is
+ * reported in dev_status.  The causal backward is not provided.
+ */
+favor_status favor_bwd_bidir(const void* Q, const void* K, const void* V, const void* dO,
+                             void* dQ, void* dK, void* dV, int B, int H, int L, int d,
+                             const float* omega, int m, favor_dtype dt, float qk_scale,
+                             favor_feature_map fm, void* workspace, size_t ws_bytes,
+                             int32_t* dev_status, void* stream);
+size_t favor_bwd_workspace_bytes(int B, int H, int L, int d, int m, favor_dtype dt);
+
+/*
  * Incremental causal FAVOR+ (token-by-token decoding).  The unidirectional
  * form is a recurrence over the prefix sums of favor_fwd_causal: a causal
  * linear attention is a unidirectional RNN whose state is (G_t, z_t)

@@ -19,6 +19,7 @@ __all__ = [
     "workspace_bytes", "new_workspace", "fwd_bidir", "fwd_causal", "bidir_state", "bidir_output",
     "causal_state", "causal_output", "status_string", "ENTRY_POINTS", "fwd_bidir_static", "static_scratch_bytes",
     "new_decode_state", "decode_step", "decode_prefill", "decode_prefill_workspace_bytes", "FEATURE_MAPS",
+    "bwd_bidir", "bwd_workspace_bytes",
 ]
 
 F32 = 0
@@ -75,6 +76,11 @@ def load():
         fn = getattr(lib, name)
         fn.restype = c_int
         fn.argtypes = fm_args
+    lib.favor_bwd_bidir.restype = c_int
+    lib.favor_bwd_bidir.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_vp, c_int,
+                                    c_int, c_float, c_int, c_vp, c_size, c_vp, c_vp]
+    lib.favor_bwd_workspace_bytes.restype = c_size
+    lib.favor_bwd_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int]
     lib.favor_decode_step.restype = c_int
     lib.favor_decode_step.argtypes = [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_vp, c_int, c_int, c_float,
                                       c_vp, c_vp, c_vp]
@@ -272,3 +278,37 @@ def decode_prefill(K, V, omega, qk_scale, state, workspace=None, dev_status=None
                                        _stream_handle(stream))
     _check(code, "favor_decode_prefill")
     return state
+
+
+def bwd_workspace_bytes(B: int, H: int, L: int, d: int, m: int, dtype) -> int:
+    n = load().favor_bwd_workspace_bytes(B, H, L, d, m, _DT[dtype])
+    if n == 0:
+        raise FavorError("unsupported shape")
+    return n
+
+
+def bwd_bidir(Q, K, V, dO, omega, qk_scale, workspace=None, feature_map="prf", dQ=None, dK=None, dV=None,
+              dev_status=None, stream=None):
+    """Gradients (dQ, dK, dV) of the bidirectional pass for the output
+    gradient dO (all [B, H, L, d], one dtype)."""
+    B, H, L, d = Q.shape
+    m = omega.shape[0]
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    for t in (Q, K, V, dO, dQ, dK, dV):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != Q.dtype or tuple(t.shape) != (B, H, L, d):
+            raise FavorError("bwd_bidir: tensors must be contiguous CUDA tensors of one dtype and shape [B,H,L,d]")
+    if omega.dtype != torch.float32 or tuple(omega.shape) != (m, d) or not omega.is_contiguous():
+        raise FavorError(f"bwd_bidir: omega must be contiguous fp32 [m, {d}]")
+    if feature_map not in FEATURE_MAPS:
+        raise FavorError(f"bwd_bidir: feature_map must be one of {sorted(FEATURE_MAPS)}")
+    if workspace is None:
+        workspace = torch.empty(bwd_workspace_bytes(B, H, L, d, m, Q.dtype), dtype=torch.uint8, device=Q.device)
+    code = load().favor_bwd_bidir(Q.data_ptr(), K.data_ptr(), V.data_ptr(), dO.data_ptr(), dQ.data_ptr(),
+                                  dK.data_ptr(), dV.data_ptr(), B, H, L, d, omega.data_ptr(), m, _DT[Q.dtype],
+                                  float(qk_scale), FEATURE_MAPS[feature_map], workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(),
+                                  dev_status.data_ptr() if dev_status is not None else None, _stream_handle(stream))
+    _check(code, "favor_bwd_bidir")
+    return dQ, dK, dV

@@ -91,6 +91,16 @@ struct SimtPlan {
 };
 
 SimtPlan simt_plan(bool causal, const Shape& s);
+// Backward of the bidirectional pass (simt.cu): workspace = the forward
+// state's plus dN^ [BH][L][d+1], dS~ partials and dS~.
+struct BwdPlan {
+  SimtPlan fwd;
+  size_t off_dn, off_dpart, off_dstate, bytes;
+};
+BwdPlan bwd_plan(const Shape& s);
+cudaError_t simt_bwd_bidir(const void* Q, const void* K, const void* V, const void* dO, void* dQ, void* dK, void* dV,
+                           const float* omega, float scale, const Shape& s, bool bf16, void* ws, int32_t* st,
+                           cudaStream_t stream, int fm);
 cudaError_t simt_state_export(const void* K, const void* V, const float* omega, float scale, const Shape& s,
                               bool bf16, void* ws, float* state, cudaStream_t stream);
 // One decode step for every (b, h): decode.cu.

@@ -554,4 +554,411 @@ cudaError_t simt_causal_output(const void* Q, const void* K, const void* V, void
   });
 }
 
+// ===========================================================================
+// Backward of the bidirectional pass (CUDA cores, fp32 arithmetic): the
+// chain rule through the forward ("Performer" digest, §Key equations):
+//   N = phi(Q) S,  D = phi(Q) z,  O = N / D;  dN^ = [dO / D | dD] with
+//   dD = -(dO . N) / D^2;
+//   dphi(Q) = S~ dN^,  dS~ = phi(Q)^T dN^,  dphi(K) = dS~ [V | 1]^T,
+//   dV = phi(K) dS~[:, :d];
+//   through the feature map, g = dphi phi (positive random features) or
+//   dphi [s w.x > 0] (Performer-ReLU):  dx = s (sum_i g_i w_i - [prf] s x sum_i g_i).
+// Key features use the per-call reference R and query features the bound
+// s |q| max_i |w_i| - 20 in both passes that meet through dN^: every
+// gradient is invariant to these constants, which cancel as in the forward.
+// ===========================================================================
+namespace {
+
+constexpr int kBT = 16;   // tokens per backward tile
+
+template <typename T>
+__device__ __forceinline__ void load_tile(const T* __restrict__ src, int nt, int d, float* dst) {
+  const int ld = d + 1;
+  for (int e = threadIdx.x; e < kBT * d; e += kThreads) {
+    const int t = e / d, c = e - t * d;
+    dst[t * ld + c] = (t < nt) ? to_f32(src[(size_t)t * d + c]) : 0.f;
+  }
+}
+
+__device__ __forceinline__ void tile_norms(const float* xs, int d, float* out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t = warp; t < kBT; t += kThreads / 32) {
+    float a = 0.f;
+    for (int c = lane; c < d; c += 32) a = fmaf(xs[t * (d + 1) + c], xs[t * (d + 1) + c], a);
+    a = warp_sum(a);
+    if (lane == 0) out[t] = a;
+  }
+}
+
+// feature from p = s w.x and the row constant c
+template <int FM>
+__device__ __forceinline__ float bwd_feature(float p, float c) {
+  if constexpr (FM == FAVOR_FM_PRF) return expf(p - c);
+  else return p < 0.f ? 0.f : p;
+}
+
+// rows [f0, f0 + nf) of a per-head [m][d+1] fp32 matrix into blk [kFB][d+1]
+__device__ __forceinline__ void load_state_block(const float* __restrict__ src, int f0, int nf, int d, float* blk) {
+  const int ld = d + 1;
+  for (int e = threadIdx.x; e < nf * ld; e += kThreads) blk[e] = src[(size_t)f0 * ld + e];
+}
+
+// features of the tile rows xs against all m rows of Omega into P [kBT][ldp]
+template <int FM>
+__device__ void tile_features(const float* xs, const float* rowc, int nt, int d, int m, float scale,
+                              const float* __restrict__ omega, float* om, float* P, int ldp) {
+  const int ld = d + 1;
+  const int n_fb = (m + kFB - 1) / kFB;
+  for (int fb = 0; fb < n_fb; ++fb) {
+    const int f0 = fb * kFB, nf = min(kFB, m - f0);
+    __syncthreads();
+    load_omega_block(omega, f0, nf, d, om);
+    __syncthreads();
+    for (int e = threadIdx.x; e < kBT * kFB; e += kThreads) {
+      const int t = e / kFB, f = e - t * kFB;
+      if (f < nf)
+        P[t * ldp + f0 + f] = t < nt ? bwd_feature<FM>(scale * dot_row(xs + t * ld, om + f * ld, d), rowc[t]) : 0.f;
+    }
+  }
+  __syncthreads();
+}
+
+// g <- dphi * phi (prf) or dphi [phi > 0] (relu) in G; gsum[t] = sum_i g
+template <int FM>
+__device__ void tile_g(const float* P, float* G, int ldp, int m, float* gsum) {
+  for (int e = threadIdx.x; e < kBT * m; e += kThreads) {
+    const int t = e / m, i = e - t * m;
+    const float ph = P[t * ldp + i], dp = G[t * ldp + i];
+    G[t * ldp + i] = FM == FAVOR_FM_PRF ? dp * ph : (ph > 0.f ? dp : 0.f);
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t = warp; t < kBT; t += kThreads / 32) {
+    float a = 0.f;
+    for (int i = lane; i < m; i += 32) a += G[t * ldp + i];
+    a = warp_sum(a);
+    if (lane == 0) gsum[t] = a;
+  }
+  __syncthreads();
+}
+
+// dx_t = s (sum_i g[t][i] w_i - [prf] s x_t sum_i g[t][i]) stored as T [nt][d]
+template <typename T, int FM>
+__device__ void tile_input_grad(const float* xs, const float* G, int ldp, const float* gsum, int nt, int d, int m,
+                                float scale, const float* __restrict__ omega, float* om, T* __restrict__ out) {
+  const int ld = d + 1;
+  constexpr int kPer = (kBT * kMaxD + kThreads - 1) / kThreads;
+  float acc[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
+  const int n_fb = (m + kFB - 1) / kFB;
+  for (int fb = 0; fb < n_fb; ++fb) {
+    const int f0 = fb * kFB, nf = min(kFB, m - f0);
+    __syncthreads();
+    load_omega_block(omega, f0, nf, d, om);
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int e = threadIdx.x + k * kThreads;
+      if (e < kBT * d) {
+        const int t = e / d, c = e - t * d;
+        float a = acc[k];
+        for (int f = 0; f < nf; ++f) a = fmaf(G[t * ldp + f0 + f], om[f * ld + c], a);
+        acc[k] = a;
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int e = threadIdx.x + k * kThreads;
+    if (e < nt * d) {
+      const int t = e / d, c = e - t * d;
+      float gx = acc[k];
+      if constexpr (FM == FAVOR_FM_PRF) gx -= scale * xs[t * ld + c] * gsum[t];
+      out[(size_t)t * d + c] = from_f32<T>(scale * gx);
+    }
+  }
+}
+
+// Query pass, one tile of kBT tokens of one head: phi(Q), N and D from S~,
+// dN^ (also written to the workspace for the feature-block pass), dphi(Q)
+// = S~ dN^ and dQ.
+template <typename T, int FM>
+__global__ void __launch_bounds__(kThreads) bwd_query_kernel(
+    const T* __restrict__ Q, const T* __restrict__ dO, T* __restrict__ dQ, const float* __restrict__ omega,
+    const float* __restrict__ key_ref, const float* __restrict__ state, float* __restrict__ dnw, int L, int d, int m,
+    float scale, int32_t* status) {
+  extern __shared__ float smem[];
+  const int ld = d + 1, ldp = m + 1;
+  const int bh = blockIdx.y, t0 = blockIdx.x * kBT, nt = min(kBT, L - t0);
+  float* xs = smem;                 // [kBT][ld] s-free q rows
+  float* go = xs + kBT * ld;        // [kBT][ld] dO, then dN^
+  float* nd = go + kBT * ld;        // [kBT][ld] N | D
+  float* om = nd + kBT * ld;        // [kFB][ld] Omega block / S~ block
+  float* P = om + kFB * ld;         // [kBT][ldp] phi(Q)
+  float* G = P + kBT * ldp;         // [kBT][ldp] dphi(Q), then g
+  float* rs = G + kBT * ldp;        // [kBT] squared norms, then row constants
+  float* gsum = rs + kBT;           // [kBT]
+  const size_t row0 = (size_t)bh * L + t0;
+  load_tile(Q + row0 * d, nt, d, xs);
+  load_tile(dO + row0 * d, nt, d, go);
+  __syncthreads();
+  tile_norms(xs, d, rs);
+  __syncthreads();
+  float R, W;
+  key_reference(key_ref, m, &R, &W);
+  if (threadIdx.x < kBT)
+    rs[threadIdx.x] = FM == FAVOR_FM_PRF ? scale * sqrtf(rs[threadIdx.x]) * W - 20.0f : 0.f;
+  tile_features<FM>(xs, rs, nt, d, m, scale, omega, om, P, ldp);
+
+  // N | D
+  const float* Sh = state + (size_t)bh * m * ld;
+  constexpr int kPerN = (kBT * (kMaxD + 1) + kThreads - 1) / kThreads;
+  float acc[kPerN];
+#pragma unroll
+  for (int k = 0; k < kPerN; ++k) acc[k] = 0.f;
+  const int n_fb = (m + kFB - 1) / kFB;
+  for (int fb = 0; fb < n_fb; ++fb) {
+    const int f0 = fb * kFB, nf = min(kFB, m - f0);
+    __syncthreads();
+    load_state_block(Sh, f0, nf, d, om);
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kPerN; ++k) {
+      const int e = threadIdx.x + k * kThreads;
+      if (e < kBT * ld) {
+        const int t = e / ld, j = e - t * ld;
+        float a = acc[k];
+        for (int f = 0; f < nf; ++f) a = fmaf(P[t * ldp + f0 + f], om[f * ld + j], a);
+        acc[k] = a;
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kPerN; ++k) {
+    const int e = threadIdx.x + k * kThreads;
+    if (e < kBT * ld) nd[e] = acc[k];
+  }
+  __syncthreads();
+  // dN^ = [dO / D | -(dO . N) / D^2], one warp per row
+  {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int t = warp; t < kBT; t += kThreads / 32) {
+      const float D = nd[t * ld + d];
+      float a = 0.f;
+      for (int j = lane; j < d; j += 32) a = fmaf(go[t * ld + j], nd[t * ld + j], a);
+      a = warp_sum(a);
+      const bool valid = t < nt;
+      if (valid && lane == 0 && (!(D > 0.f) || !isfinite(D))) report_status(status, FAVOR_ERR_NONFINITE);
+      const float inv = 1.0f / D;
+      __syncwarp();
+      for (int j = lane; j < d; j += 32) go[t * ld + j] = valid ? go[t * ld + j] * inv : 0.f;
+      if (lane == 0) go[t * ld + d] = valid ? -a * inv * inv : 0.f;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < nt * ld; e += kThreads) dnw[row0 * ld + e] = go[e];
+  // dphi(Q) = S~ dN^
+  for (int fb = 0; fb < n_fb; ++fb) {
+    const int f0 = fb * kFB, nf = min(kFB, m - f0);
+    __syncthreads();
+    load_state_block(Sh, f0, nf, d, om);
+    __syncthreads();
+    for (int e = threadIdx.x; e < kBT * kFB; e += kThreads) {
+      const int t = e / kFB, f = e - t * kFB;
+      if (f < nf) G[t * ldp + f0 + f] = dot_row(om + f * ld, go + t * ld, ld);
+    }
+  }
+  __syncthreads();
+  tile_g<FM>(P, G, ldp, m, gsum);
+  tile_input_grad<T, FM>(xs, G, ldp, gsum, nt, d, m, scale, omega, om, dQ + row0 * d);
+}
+
+// Feature-block pass: partial dS~ of a token split and a block of features,
+// sum_t phi(q_t)_f dN^_t (the same query features as the query pass).
+template <typename T, int FM>
+__global__ void __launch_bounds__(kThreads) bwd_dstate_partial_kernel(
+    const T* __restrict__ Q, const float* __restrict__ dnw, const float* __restrict__ omega,
+    const float* __restrict__ key_ref, int L, int d, int m, float scale, int chunk, int n_split,
+    float* __restrict__ dpart) {
+  extern __shared__ float smem[];
+  const int split = blockIdx.x, fb = blockIdx.y, bh = blockIdx.z;
+  const int ld = d + 1;
+  float* om = smem;                   // [kFB][ld]
+  float* xs = om + kFB * ld;          // [kBT][ld]
+  float* dn = xs + kBT * ld;          // [kBT][ld]
+  float* ph = dn + kBT * ld;          // [kBT][kFB + 1]
+  float* rs = ph + kBT * (kFB + 1);   // [kBT]
+  const int f0 = fb * kFB, nf = min(kFB, m - f0);
+  const int l0 = split * chunk, l1 = min(L, l0 + chunk);
+  float R, W;
+  key_reference(key_ref, m, &R, &W);
+  load_omega_block(omega, f0, nf, d, om);
+  const int fa = threadIdx.x / 4, jb = threadIdx.x % 4;
+  float acc[33];
+#pragma unroll
+  for (int k = 0; k < 33; ++k) acc[k] = 0.f;
+  for (int t0 = l0; t0 < l1; t0 += kBT) {
+    const int nt = min(kBT, l1 - t0);
+    const size_t row0 = (size_t)bh * L + t0;
+    __syncthreads();
+    load_tile(Q + row0 * d, nt, d, xs);
+    for (int e = threadIdx.x; e < kBT * ld; e += kThreads) dn[e] = e < nt * ld ? dnw[row0 * ld + e] : 0.f;
+    __syncthreads();
+    tile_norms(xs, d, rs);
+    __syncthreads();
+    for (int e = threadIdx.x; e < kBT * kFB; e += kThreads) {
+      const int t = e / kFB, f = e - t * kFB;
+      const float c = FM == FAVOR_FM_PRF ? scale * sqrtf(rs[t]) * W - 20.0f : 0.f;
+      ph[t * (kFB + 1) + f] =
+          (t < nt && f < nf) ? bwd_feature<FM>(scale * dot_row(xs + t * ld, om + f * ld, d), c) : 0.f;
+    }
+    __syncthreads();
+    for (int t = 0; t < nt; ++t) {
+      const float a = ph[t * (kFB + 1) + fa];
+      const float* dr = dn + t * ld;
+#pragma unroll
+      for (int k = 0; k < 33; ++k) {
+        const int j = jb + 4 * k;
+        if (j <= d) acc[k] = fmaf(a, dr[j], acc[k]);
+      }
+    }
+  }
+  if (fa < nf) {
+    float* dst = dpart + (((size_t)bh * n_split + split) * m + f0 + fa) * ld;
+#pragma unroll
+    for (int k = 0; k < 33; ++k) {
+      const int j = jb + 4 * k;
+      if (j <= d) dst[j] = acc[k];
+    }
+  }
+}
+
+// Key pass, one tile of kBT tokens of one head: phi(K), dphi(K) = dS~ [V|1]^T,
+// dV = phi(K) dS~[:, :d] and dK.
+template <typename T, int FM>
+__global__ void __launch_bounds__(kThreads) bwd_key_kernel(
+    const T* __restrict__ K, const T* __restrict__ V, T* __restrict__ dK, T* __restrict__ dV,
+    const float* __restrict__ omega, const float* __restrict__ key_ref, const float* __restrict__ dstate, int L,
+    int d, int m, float scale) {
+  extern __shared__ float smem[];
+  const int ld = d + 1, ldp = m + 1;
+  const int bh = blockIdx.y, t0 = blockIdx.x * kBT, nt = min(kBT, L - t0);
+  float* xs = smem;                 // [kBT][ld] k rows
+  float* vs = xs + kBT * ld;        // [kBT][ld] v | 1
+  float* om = vs + kBT * ld;        // [kFB][ld]
+  float* P = om + kFB * ld;         // [kBT][ldp] phi(K)
+  float* G = P + kBT * ldp;         // [kBT][ldp] dphi(K), then g
+  float* rs = G + kBT * ldp;        // [kBT]
+  float* gsum = rs + kBT;           // [kBT]
+  const size_t row0 = (size_t)bh * L + t0;
+  load_tile(K + row0 * d, nt, d, xs);
+  load_tile(V + row0 * d, nt, d, vs);
+  if (threadIdx.x < kBT) vs[threadIdx.x * ld + d] = threadIdx.x < nt ? 1.f : 0.f;
+  __syncthreads();
+  tile_norms(xs, d, rs);
+  __syncthreads();
+  float R, W;
+  key_reference(key_ref, m, &R, &W);
+  if (threadIdx.x < kBT)
+    rs[threadIdx.x] = FM == FAVOR_FM_PRF ? 0.5f * scale * scale * rs[threadIdx.x] + R : 0.f;
+  tile_features<FM>(xs, rs, nt, d, m, scale, omega, om, P, ldp);
+
+  const float* dS = dstate + (size_t)bh * m * ld;
+  constexpr int kPer = (kBT * kMaxD + kThreads - 1) / kThreads;
+  float accv[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) accv[k] = 0.f;
+  const int n_fb = (m + kFB - 1) / kFB;
+  for (int fb = 0; fb < n_fb; ++fb) {
+    const int f0 = fb * kFB, nf = min(kFB, m - f0);
+    __syncthreads();
+    load_state_block(dS, f0, nf, d, om);
+    __syncthreads();
+    for (int e = threadIdx.x; e < kBT * kFB; e += kThreads) {
+      const int t = e / kFB, f = e - t * kFB;
+      if (f < nf) G[t * ldp + f0 + f] = dot_row(om + f * ld, vs + t * ld, ld);
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int e = threadIdx.x + k * kThreads;
+      if (e < kBT * d) {
+        const int t = e / d, j = e - t * d;
+        float a = accv[k];
+        for (int f = 0; f < nf; ++f) a = fmaf(P[t * ldp + f0 + f], om[f * ld + j], a);
+        accv[k] = a;
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int e = threadIdx.x + k * kThreads;
+    if (e < nt * d) dV[row0 * d + e] = from_f32<T>(accv[k]);
+  }
+  __syncthreads();
+  tile_g<FM>(P, G, ldp, m, gsum);
+  tile_input_grad<T, FM>(xs, G, ldp, gsum, nt, d, m, scale, omega, om, dK + row0 * d);
+}
+
+size_t bwd_tile_smem(int d, int m) {
+  const int ld = d + 1, ldp = m + 1;
+  return sizeof(float) * ((size_t)3 * kBT * ld + (size_t)kFB * ld + (size_t)2 * kBT * ldp + 2 * kBT);
+}
+size_t bwd_dstate_smem(int d) {
+  const int ld = d + 1;
+  return sizeof(float) * ((size_t)kFB * ld + (size_t)2 * kBT * ld + (size_t)kBT * (kFB + 1) + kBT);
+}
+
+}  // namespace
+
+BwdPlan bwd_plan(const Shape& s) {
+  BwdPlan b{};
+  b.fwd = simt_plan(false, s);
+  const size_t ld = (size_t)s.d + 1, BH = (size_t)s.BH();
+  size_t off = align256(b.fwd.bytes);
+  b.off_dn = off;
+  off = align256(off + BH * s.L * ld * sizeof(float));
+  b.off_dpart = off;
+  off = align256(off + BH * b.fwd.n_split * s.m * ld * sizeof(float));
+  b.off_dstate = off;
+  off = align256(off + BH * s.m * ld * sizeof(float));
+  b.bytes = off;
+  return b;
+}
+
+cudaError_t simt_bwd_bidir(const void* Q, const void* K, const void* V, const void* dO, void* dQ, void* dK, void* dV,
+                           const float* omega, float scale, const Shape& s, bool bf16, void* ws, int32_t* st,
+                           cudaStream_t stream, int fm) {
+  const BwdPlan b = bwd_plan(s);
+  char* w = static_cast<char*>(ws);
+  // S~ = [phi(K)^T V | phi(K)^T 1] (and the key reference in the header)
+  cudaError_t e = simt_bidir_state(K, V, omega, scale, s, bf16, ws, st, stream, fm);
+  if (e != cudaSuccess) return e;
+  const float* key_ref = reinterpret_cast<const float*>(w);
+  const float* state = reinterpret_cast<const float*>(w + b.fwd.off_state);
+  float* dnw = reinterpret_cast<float*>(w + b.off_dn);
+  float* dpart = reinterpret_cast<float*>(w + b.off_dpart);
+  float* dstate = reinterpret_cast<float*>(w + b.off_dstate);
+  const dim3 tiles((s.L + kBT - 1) / kBT, s.BH());
+  const size_t tsm = bwd_tile_smem(s.d, s.m), dsm = bwd_dstate_smem(s.d);
+  return dispatch(bf16, fm, [&](auto tag, auto f) {
+    using T = decltype(tag);
+    constexpr int FM = decltype(f)::value;
+    cudaError_t r = set_smem(bwd_query_kernel<T, FM>, tsm);
+    if (r == cudaSuccess) r = set_smem(bwd_key_kernel<T, FM>, tsm);
+    if (r == cudaSuccess) r = set_smem(bwd_dstate_partial_kernel<T, FM>, dsm);
+    if (r != cudaSuccess) return r;
+    bwd_query_kernel<T, FM><<<tiles, kThreads, tsm, stream>>>(static_cast<const T*>(Q), static_cast<const T*>(dO),
+                                                              static_cast<T*>(dQ), omega, key_ref, state, dnw, s.L,
+                                                              s.d, s.m, scale, st);
+    bwd_dstate_partial_kernel<T, FM><<<dim3(b.fwd.n_split, b.fwd.n_fb, s.BH()), kThreads, dsm, stream>>>(
+        static_cast<const T*>(Q), dnw, omega, key_ref, s.L, s.d, s.m, scale, b.fwd.chunk, b.fwd.n_split, dpart);
+    merge_kernel<<<s.BH(), kThreads, 0, stream>>>(dpart, s.d, s.m, b.fwd.n_split, dstate);
+    bwd_key_kernel<T, FM><<<tiles, kThreads, tsm, stream>>>(static_cast<const T*>(K), static_cast<const T*>(V),
+                                                            static_cast<T*>(dK), static_cast<T*>(dV), omega, key_ref,
+                                                            dstate, s.L, s.d, s.m, scale);
+    return cudaGetLastError();
+  });
+}
+
 }  // namespace favor

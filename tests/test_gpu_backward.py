@@ -1,0 +1,60 @@
+"""GPU parity of the bidirectional backward (favor_bwd_bidir) against the
+fp64 oracle gradient (itself pinned by finite differences).
+
+Metric: per head, max |gpu - oracle| over the head's gradient entries
+divided by the head's largest oracle entry (a gradient row can be near zero,
+so a row-wise ratio would measure cancellation, not the kernels).  Bars: the
+fp32 arithmetic of the kernels over sums of at most L m terms gives ~1e-6 for
+fp32 storage (bar 1e-4); bf16 storage rounds every stored gradient to 2^-9
+relative (bar 2e-2, as for the forward).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import workloads as wl
+from helpers import TOL, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _per_head_err(got, ref):
+    g = got.reshape(-1, got.shape[-2] * got.shape[-1])
+    r = ref.reshape(-1, ref.shape[-2] * ref.shape[-1])
+    return float(np.max(np.max(np.abs(g - r), axis=1) / np.max(np.abs(r), axis=1)))
+
+
+@pytest.mark.parametrize("features", ["prf", "relu"])
+@pytest.mark.parametrize("dtype,B,H,L,d,m", [(torch.float32, 2, 2, 200, 64, 128),
+                                             (torch.float32, 1, 3, 65, 32, 100),
+                                             (torch.bfloat16, 2, 4, 1000, 64, 256),
+                                             (torch.bfloat16, 1, 2, 300, 128, 512)])
+def test_backward_matches_oracle(cuda_lib, features, dtype, B, H, L, d, m):
+    w = wl.Workload("bwd", "bidir", "f32" if dtype == torch.float32 else "bf16", B, H, L, d, m, "normal")
+    Q, K, V = (t.cuda() for t in wl.make_qkv(w, seed=L + m))
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(L * m)
+    dO = torch.randn((B, H, L, d), generator=gen).to(dtype).cuda()
+    om = cuda_lib.new_omega(m + 2, m, d)
+    s = d ** -0.25
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dQ, dK, dV = cuda_lib.bwd_bidir(Q, K, V, dO, om, s, feature_map=features, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rQ, rK, rV = orc.favor_bidirectional_grad(to_np(Q), to_np(K), to_np(V), to_np(om), s, to_np(dO), features)
+    errs = {n: _per_head_err(to_np(g), r) for n, g, r in (("dQ", dQ, rQ), ("dK", dK, rK), ("dV", dV, rV))}
+    assert max(errs.values()) < TOL[dtype], errs
+
+
+def test_backward_is_deterministic(cuda_lib):
+    B, H, L, d, m = 1, 2, 300, 64, 128
+    w = wl.Workload("bwd", "bidir", "f32", B, H, L, d, m, "normal")
+    Q, K, V = (t.cuda() for t in wl.make_qkv(w, seed=1))
+    dO = torch.ones_like(Q)
+    om = cuda_lib.new_omega(1, m, d)
+    a = cuda_lib.bwd_bidir(Q, K, V, dO, om, 0.4)
+    b = cuda_lib.bwd_bidir(Q, K, V, dO, om, 0.4)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
