@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--decode-steps", type=int, default=200)
     ap.add_argument("--relu-steps", type=int, default=100)
+    ap.add_argument("--bwd-steps", type=int, default=10)
     return ap.parse_args()
 
 
@@ -409,6 +410,9 @@ def run_gpu(args, rank, world, local_rank):
 
     hbm, tc_burst, tc_sus, peak_kind = load_peaks()
     decode = measure_decode(favor, args.decode_steps, stream, status, hbm, dev) if args.decode_steps > 0 else None
+    bwd = None
+    if args.bwd_steps > 0:
+        bwd = measure_backward(favor, args.bwd_steps, sets, omegas[0], s, stream, status, dev, tokens_per_step, hbm)
     relu = None
     if args.relu_steps > 0:
         relu = measure_feature_map(favor, "relu", args.relu_steps, sets, omegas[0], s, ws_b, ws_c, O_b, O_c, stream,
@@ -469,6 +473,7 @@ def run_gpu(args, rank, world, local_rank):
         "e2e": e2e,
         "decode": decode,
         "relu": relu,
+        "backward": bwd,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=12.0)
@@ -549,6 +554,44 @@ def run_reference(args, rank, world):
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
+
+
+def measure_backward(favor, n_steps, sets, omega, s, stream, status, dev, tokens_per_step, hbm):
+    """favor_bwd_bidir on the step's workload (CUDA-core kernels): dQ, dK, dV
+    for a seeded dO, inputs rotating over the sets, one CUDA graph per set.
+    Algorithmic bytes: read Q, K, V, dO and write dQ, dK, dV (7 d e per
+    head-token)."""
+    q0 = sets[0][0]
+    B, H, L, d = q0.shape
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(5)
+    dO = torch.randn(q0.shape, generator=gen).to(q0.dtype).to(dev)
+    ws = torch.empty(favor.bwd_workspace_bytes(B, H, L, d, omega.shape[0], q0.dtype), dtype=torch.uint8, device=dev)
+    dQ, dK, dV = torch.empty_like(q0), torch.empty_like(q0), torch.empty_like(q0)
+    graphs = []
+    for q, k, v in sets:
+        with torch.cuda.stream(stream):
+            favor.bwd_bidir(q, k, v, dO, omega, s, ws, dQ=dQ, dK=dK, dV=dV, dev_status=status, stream=stream)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            favor.bwd_bidir(q, k, v, dO, omega, s, ws, dQ=dQ, dK=dK, dV=dV, dev_status=status, stream=stream)
+        graphs.append(g)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        graphs[0].replay()
+        e0.record(stream)
+        for i in range(n_steps):
+            graphs[i % len(graphs)].replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after the backward steps")
+    ms = e0.elapsed_time(e1) / n_steps
+    nbytes = 7 * q0.numel() * q0.element_size()
+    return {"value": tokens_per_step / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": n_steps,
+            "step": "bidirectional backward (dQ, dK, dV), CUDA-core kernels",
+            "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm}
 
 
 def measure_feature_map(favor, fm, n_steps, sets, omega, s, ws_b, ws_c, O_b, O_c, stream, status, dev,
