@@ -157,13 +157,18 @@ class ClockSampler:
 # traffic from the committed ncu summary (null when the kernel source changed)
 # ---------------------------------------------------------------------------
 
+# The sources the tensor-core kernels (the profiled stages) are built from:
+# a committed profile's counters stay valid while none of these changes.
+KERNEL_SOURCES = ("linear_softmax_attention_gb300/csrc/tc.cu", "linear_softmax_attention_gb300/csrc/tc_ptx.cuh",
+                  "linear_softmax_attention_gb300/csrc/common.cuh", "linear_softmax_attention_gb300/csrc/prep.cu",
+                  "include/favor.h")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "linear_softmax_attention_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 

@@ -569,7 +569,7 @@ cudaError_t simt_causal_output(const void* Q, const void* K, const void* V, void
 // ===========================================================================
 namespace {
 
-constexpr int kBT = 16;   // tokens per backward tile
+constexpr int kBT = 32;   // tokens per backward tile
 
 template <typename T>
 __device__ __forceinline__ void load_tile(const T* __restrict__ src, int nt, int d, float* dst) {
