@@ -57,6 +57,7 @@ __all__ = [
     "favor_causal_quadratic",
     "favor_rows",
     "favor_bidirectional_grad",
+    "favor_causal_grad",
     "softmax_attention",
     "rowwise_rel_err",
 ]
@@ -394,6 +395,45 @@ def favor_bidirectional_grad(Q, K, V, Omega, scale: float, dO, features: str = "
     dQ = scale * through_features(qs, pq, dpq)
     dK = scale * through_features(ks, pk, dpk)
     return dQ, dK, dV
+
+
+def favor_causal_grad(Q, K, V, Omega, scale: float, dO, features: str = "prf"):
+    """Gradients (dQ, dK, dV) of sum(dO * favor_causal(Q, K, V)).
+
+    The chain rule through the prefix-sum forward ([digest] §Methods causal
+    bullet), written on the lower-triangular form it equals
+    (A = tril(phi(Q) phi(K)^T), diagonal included):
+      N = A V,  D = A 1,  O = N / D;  dN = dO / D,  dD = -sum_j(dO O) / D
+      dA = tril(dN V^T + dD 1^T)
+      dphi(Q) = dA phi(K),  dphi(K) = dA^T phi(Q),  dV = A^T dN
+    then through the feature map as in favor_bidirectional_grad.
+    """
+    Q, K, V, dO = (np.asarray(a, dtype=np.float64) for a in (Q, K, V, dO))
+    Om = np.asarray(Omega, dtype=np.float64)
+    qs, ks = scale * Q, scale * K
+    fn = FEATURES[features]
+    pq, pk = fn(qs, Om), fn(ks, Om)
+    L = Q.shape[-2]
+    mask = np.tril(np.ones((L, L)))
+    A = (pq @ np.swapaxes(pk, -1, -2)) * mask
+    N = A @ V
+    D = np.sum(A, axis=-1)
+    O = N / D[..., None]
+    dN = dO / D[..., None]
+    dD = -np.sum(dO * O, axis=-1) / D
+    dA = (dN @ np.swapaxes(V, -1, -2) + dD[..., None]) * mask
+    dpq = dA @ pk
+    dpk = np.swapaxes(dA, -1, -2) @ pq
+    dV = np.swapaxes(A, -1, -2) @ dN
+
+    def through_features(x, phi, dphi):
+        if features == "prf":
+            g = dphi * phi
+            return g @ Om - x * np.sum(g, axis=-1, keepdims=True)
+        m_ = (x @ Om.T) > 0
+        return ((dphi * m_) @ Om) / math.sqrt(Om.shape[0])
+
+    return scale * through_features(qs, pq, dpq), scale * through_features(ks, pk, dpk), dV
 
 
 def softmax_attention(Q, K, V, scale: float, causal: bool = False) -> np.ndarray:

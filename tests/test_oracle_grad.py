@@ -9,26 +9,35 @@ import pytest
 import oracle as orc
 
 
-def _loss(Q, K, V, Om, s, dO, features):
-    return float(np.sum(dO * orc.favor_bidirectional(Q, K, V, Om, s, features)))
+def _loss(Q, K, V, Om, s, dO, features, causal=False):
+    fwd = orc.favor_causal if causal else orc.favor_bidirectional
+    return float(np.sum(dO * fwd(Q, K, V, Om, s, features)))
 
 
+@pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("features", ["prf", "relu"])
-def test_gradient_matches_central_differences(features):
-    rng = np.random.default_rng(7 if features == "prf" else 8)
-    L, d, m = 5, 3, 6
+def test_gradient_matches_central_differences(features, causal):
+    rng = np.random.default_rng((7 if features == "prf" else 8) + 10 * causal)
+    # enough features that no normaliser is zero (under ReLU a causal row
+    # with one key can have phi(q).phi(k) = 0)
+    L, d, m = 5, 3, 16
     Q, K, V, dO = (rng.standard_normal((L, d)) for _ in range(4))
     Om = rng.standard_normal((m, d))
+    if causal:
+        K[0] = Q[0]          # phi(q0).phi(k0) = |phi(q0)|^2 > 0 for either map
     s = 0.8
-    dQ, dK, dV = orc.favor_bidirectional_grad(Q, K, V, Om, s, dO, features)
+    fwd = orc.favor_causal if causal else orc.favor_bidirectional
+    assert np.all(np.isfinite(fwd(Q, K, V, Om, s, features)))
+    grad = orc.favor_causal_grad if causal else orc.favor_bidirectional_grad
+    dQ, dK, dV = grad(Q, K, V, Om, s, dO, features)
     h = 1e-6
     for X, G in ((Q, dQ), (K, dK), (V, dV)):
         for idx in np.ndindex(X.shape):
             old = X[idx]
             X[idx] = old + h
-            up = _loss(Q, K, V, Om, s, dO, features)
+            up = _loss(Q, K, V, Om, s, dO, features, causal)
             X[idx] = old - h
-            dn = _loss(Q, K, V, Om, s, dO, features)
+            dn = _loss(Q, K, V, Om, s, dO, features, causal)
             X[idx] = old
             num = (up - dn) / (2 * h)
             assert abs(num - G[idx]) < 1e-6 * max(1.0, abs(num)), (features, idx, num, G[idx])
@@ -61,3 +70,17 @@ def test_query_features_get_no_radial_gradient():
     O = N / D[:, None]
     dpq = (dO / D[:, None]) @ S.T + (-np.sum(dO * O, 1) / D)[:, None] * z[None, :]
     assert np.max(np.abs(np.sum(pq * dpq, axis=1))) < 1e-12 * np.max(np.abs(pq * dpq))
+
+
+def test_causal_gradient_of_the_last_row_only_equals_bidirectional():
+    # with dO zero except the last row, the causal and bidirectional losses
+    # coincide (the last causal row sees every token)
+    rng = np.random.default_rng(11)
+    Q, K, V = (rng.standard_normal((9, 4)) for _ in range(3))
+    dO = np.zeros((9, 4))
+    dO[-1] = rng.standard_normal(4)
+    Om = rng.standard_normal((7, 4))
+    a = orc.favor_causal_grad(Q, K, V, Om, 0.6, dO)
+    b = orc.favor_bidirectional_grad(Q, K, V, Om, 0.6, dO)
+    for x, y in zip(a, b):
+        assert np.allclose(x, y, rtol=1e-12, atol=1e-12)
