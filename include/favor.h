@@ -247,13 +247,30 @@ size_t favor_static_scratch_bytes(void);
  * Omega is not differentiated (it is a fixed random draw).  CUDA-core
  * kernels, fp32 arithmetic, any supported shape; workspace of
  * favor_bwd_workspace_bytes(...) bytes.  A zero or non-finite normaliser is
- * reported in dev_status.  The causal backward is not provided.
+ * reported in dev_status.
  */
 favor_status favor_bwd_bidir(const void* Q, const void* K, const void* V, const void* dO,
                              void* dQ, void* dK, void* dV, int B, int H, int L, int d,
                              const float* omega, int m, favor_dtype dt, float qk_scale,
                              favor_feature_map fm, void* workspace, size_t ws_bytes,
                              int32_t* dev_status, void* stream);
+/*
+ * favor_bwd_causal — the same for the causal pass (O = favor_fwd_causal_fm):
+ * with the prefix state G~_c of the tiles before tile c and the suffix state
+ * H_c = sum over later tiles of phi(q) dN^T,
+ *   dphi(q_t) = G~_c dN^_t + sum_{s<=t in the tile} (dN^_t . [v_s ; 1]) phi(k_s)
+ *   dphi(k_s) = H_c [v_s ; 1] + sum_{t>=s in the tile} (dN^_t . [v_s ; 1]) phi(q_t)
+ *   dV_s = H_c[:, :d]^T phi(k_s) + sum_{t>=s in the tile} (phi(k_s).phi(q_t)) dN_t
+ * ("Performer" digest, §Methods causal bullet, differentiated).  One CTA per
+ * head walks the sequence forward then backward.  Same arguments and
+ * workspace size as favor_bwd_bidir.
+ */
+favor_status favor_bwd_causal(const void* Q, const void* K, const void* V, const void* dO,
+                              void* dQ, void* dK, void* dV, int B, int H, int L, int d,
+                              const float* omega, int m, favor_dtype dt, float qk_scale,
+                              favor_feature_map fm, void* workspace, size_t ws_bytes,
+                              int32_t* dev_status, void* stream);
+/* Workspace bytes of favor_bwd_bidir and favor_bwd_causal. */
 size_t favor_bwd_workspace_bytes(int B, int H, int L, int d, int m, favor_dtype dt);
 
 /*

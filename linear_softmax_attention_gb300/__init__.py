@@ -19,7 +19,7 @@ __all__ = [
     "workspace_bytes", "new_workspace", "fwd_bidir", "fwd_causal", "bidir_state", "bidir_output",
     "causal_state", "causal_output", "status_string", "ENTRY_POINTS", "fwd_bidir_static", "static_scratch_bytes",
     "new_decode_state", "decode_step", "decode_prefill", "decode_prefill_workspace_bytes", "FEATURE_MAPS",
-    "bwd_bidir", "bwd_workspace_bytes",
+    "bwd_bidir", "bwd_causal", "bwd_workspace_bytes",
 ]
 
 F32 = 0
@@ -79,6 +79,8 @@ def load():
     lib.favor_bwd_bidir.restype = c_int
     lib.favor_bwd_bidir.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_vp, c_int,
                                     c_int, c_float, c_int, c_vp, c_size, c_vp, c_vp]
+    lib.favor_bwd_causal.restype = c_int
+    lib.favor_bwd_causal.argtypes = lib.favor_bwd_bidir.argtypes
     lib.favor_bwd_workspace_bytes.restype = c_size
     lib.favor_bwd_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int]
     lib.favor_decode_step.restype = c_int
@@ -288,9 +290,9 @@ def bwd_workspace_bytes(B: int, H: int, L: int, d: int, m: int, dtype) -> int:
 
 
 def bwd_bidir(Q, K, V, dO, omega, qk_scale, workspace=None, feature_map="prf", dQ=None, dK=None, dV=None,
-              dev_status=None, stream=None):
-    """Gradients (dQ, dK, dV) of the bidirectional pass for the output
-    gradient dO (all [B, H, L, d], one dtype)."""
+              dev_status=None, stream=None, causal=False):
+    """Gradients (dQ, dK, dV) of the bidirectional (or, with causal=True, the
+    causal) pass for the output gradient dO (all [B, H, L, d], one dtype)."""
     B, H, L, d = Q.shape
     m = omega.shape[0]
     dQ = torch.empty_like(Q) if dQ is None else dQ
@@ -305,10 +307,18 @@ def bwd_bidir(Q, K, V, dO, omega, qk_scale, workspace=None, feature_map="prf", d
         raise FavorError(f"bwd_bidir: feature_map must be one of {sorted(FEATURE_MAPS)}")
     if workspace is None:
         workspace = torch.empty(bwd_workspace_bytes(B, H, L, d, m, Q.dtype), dtype=torch.uint8, device=Q.device)
-    code = load().favor_bwd_bidir(Q.data_ptr(), K.data_ptr(), V.data_ptr(), dO.data_ptr(), dQ.data_ptr(),
+    name = "favor_bwd_causal" if causal else "favor_bwd_bidir"
+    code = getattr(load(), name)(Q.data_ptr(), K.data_ptr(), V.data_ptr(), dO.data_ptr(), dQ.data_ptr(),
                                   dK.data_ptr(), dV.data_ptr(), B, H, L, d, omega.data_ptr(), m, _DT[Q.dtype],
                                   float(qk_scale), FEATURE_MAPS[feature_map], workspace.data_ptr(),
                                   workspace.numel() * workspace.element_size(),
                                   dev_status.data_ptr() if dev_status is not None else None, _stream_handle(stream))
-    _check(code, "favor_bwd_bidir")
+    _check(code, name)
     return dQ, dK, dV
+
+
+def bwd_causal(Q, K, V, dO, omega, qk_scale, workspace=None, feature_map="prf", dQ=None, dK=None, dV=None,
+               dev_status=None, stream=None):
+    """Gradients (dQ, dK, dV) of the causal pass."""
+    return bwd_bidir(Q, K, V, dO, omega, qk_scale, workspace, feature_map, dQ, dK, dV, dev_status, stream,
+                     causal=True)

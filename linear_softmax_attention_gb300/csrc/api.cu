@@ -1,6 +1,7 @@
 // C ABI entry points: argument checks, workspace planning and dispatch.
 #include <cmath>
 
+#include "backward.cuh"
 #include "common.cuh"
 #include "tc.cuh"
 
@@ -120,6 +121,37 @@ favor_status run_call(bool causal, int stage, const void* Q, const void* K, cons
 }
 }  // namespace favor
 
+namespace {
+favor_status bwd_run(bool causal, const void* Q, const void* K, const void* V, const void* dO, void* dQ, void* dK,
+                     void* dV, int B, int H, int L, int d, const float* omega, int m, favor_dtype dt, float qk_scale,
+                     favor_feature_map fm, void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  favor_status st = shape_ok(B, H, L, d, m, dt);
+  if (st != FAVOR_OK) return st;
+  if (fm != FAVOR_FM_PRF && fm != FAVOR_FM_RELU) return FAVOR_ERR_INVALID_ARG;
+  if (!std::isfinite(qk_scale) || !(qk_scale > 0.f)) return FAVOR_ERR_INVALID_ARG;
+  const void* in[] = {Q, K, V, dO, static_cast<const void*>(omega)};
+  const void* out[] = {dQ, dK, dV};
+  for (const void* p : in)
+    if (p == nullptr || !aligned(p, 16)) return FAVOR_ERR_INVALID_ARG;
+  for (const void* p : out) {
+    if (p == nullptr || !aligned(p, 16)) return FAVOR_ERR_INVALID_ARG;
+    for (const void* q : in)
+      if (p == q) return FAVOR_ERR_INVALID_ARG;
+  }
+  if (dQ == dK || dQ == dV || dK == dV) return FAVOR_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256)) return FAVOR_ERR_INVALID_ARG;
+  const Shape s{B, H, L, d, m};
+  if (ws_bytes < favor::bwd_plan(s).bytes) return FAVOR_ERR_INVALID_ARG;
+  const bool bf16 = dt == FAVOR_BF16;
+  cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+  cudaError_t e = causal ? favor::simt_bwd_causal(Q, K, V, dO, dQ, dK, dV, omega, qk_scale, s, bf16, workspace,
+                                                  dev_status, st_, static_cast<int>(fm))
+                         : favor::simt_bwd_bidir(Q, K, V, dO, dQ, dK, dV, omega, qk_scale, s, bf16, workspace,
+                                                 dev_status, st_, static_cast<int>(fm));
+  return e == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
+}
+}  // namespace
+
 extern "C" {
 
 int favor_api_version(void) { return kVersion; }
@@ -181,30 +213,21 @@ size_t favor_bwd_workspace_bytes(int B, int H, int L, int d, int m, favor_dtype 
   return favor::bwd_plan(Shape{B, H, L, d, m}).bytes;
 }
 
+
 favor_status favor_bwd_bidir(const void* Q, const void* K, const void* V, const void* dO, void* dQ, void* dK,
                              void* dV, int B, int H, int L, int d, const float* omega, int m, favor_dtype dt,
                              float qk_scale, favor_feature_map fm, void* workspace, size_t ws_bytes,
                              int32_t* dev_status, void* stream) {
-  favor_status st = shape_ok(B, H, L, d, m, dt);
-  if (st != FAVOR_OK) return st;
-  if (fm != FAVOR_FM_PRF && fm != FAVOR_FM_RELU) return FAVOR_ERR_INVALID_ARG;
-  if (!std::isfinite(qk_scale) || !(qk_scale > 0.f)) return FAVOR_ERR_INVALID_ARG;
-  const void* in[] = {Q, K, V, dO, static_cast<const void*>(omega)};
-  const void* out[] = {dQ, dK, dV};
-  for (const void* p : in)
-    if (p == nullptr || !aligned(p, 16)) return FAVOR_ERR_INVALID_ARG;
-  for (const void* p : out) {
-    if (p == nullptr || !aligned(p, 16)) return FAVOR_ERR_INVALID_ARG;
-    for (const void* q : in)
-      if (p == q) return FAVOR_ERR_INVALID_ARG;
-  }
-  if (dQ == dK || dQ == dV || dK == dV) return FAVOR_ERR_INVALID_ARG;
-  if (workspace == nullptr || !aligned(workspace, 256)) return FAVOR_ERR_INVALID_ARG;
-  const Shape s{B, H, L, d, m};
-  if (ws_bytes < favor::bwd_plan(s).bytes) return FAVOR_ERR_INVALID_ARG;
-  cudaError_t e = favor::simt_bwd_bidir(Q, K, V, dO, dQ, dK, dV, omega, qk_scale, s, dt == FAVOR_BF16, workspace,
-                                        dev_status, static_cast<cudaStream_t>(stream), static_cast<int>(fm));
-  return e == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
+  return bwd_run(false, Q, K, V, dO, dQ, dK, dV, B, H, L, d, omega, m, dt, qk_scale, fm, workspace, ws_bytes,
+                 dev_status, stream);
+}
+
+favor_status favor_bwd_causal(const void* Q, const void* K, const void* V, const void* dO, void* dQ, void* dK,
+                              void* dV, int B, int H, int L, int d, const float* omega, int m, favor_dtype dt,
+                              float qk_scale, favor_feature_map fm, void* workspace, size_t ws_bytes,
+                              int32_t* dev_status, void* stream) {
+  return bwd_run(true, Q, K, V, dO, dQ, dK, dV, B, H, L, d, omega, m, dt, qk_scale, fm, workspace, ws_bytes,
+                 dev_status, stream);
 }
 
 favor_status favor_decode_step(const void* q, const void* k, const void* v, void* o, int B, int H, int d,

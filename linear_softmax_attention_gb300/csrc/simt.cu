@@ -17,6 +17,7 @@
 //    Performer to Linear Attention", §Simple Derivation).
 #include <type_traits>
 
+#include "backward.cuh"
 #include "common.cuh"
 
 namespace favor {
@@ -571,18 +572,19 @@ namespace {
 
 constexpr int kBT = 32;   // tokens per backward tile
 
-template <typename T>
+template <int TT, typename T>
 __device__ __forceinline__ void load_tile(const T* __restrict__ src, int nt, int d, float* dst) {
   const int ld = d + 1;
-  for (int e = threadIdx.x; e < kBT * d; e += kThreads) {
+  for (int e = threadIdx.x; e < TT * d; e += kThreads) {
     const int t = e / d, c = e - t * d;
     dst[t * ld + c] = (t < nt) ? to_f32(src[(size_t)t * d + c]) : 0.f;
   }
 }
 
+template <int TT>
 __device__ __forceinline__ void tile_norms(const float* xs, int d, float* out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int t = warp; t < kBT; t += kThreads / 32) {
+  for (int t = warp; t < TT; t += kThreads / 32) {
     float a = 0.f;
     for (int c = lane; c < d; c += 32) a = fmaf(xs[t * (d + 1) + c], xs[t * (d + 1) + c], a);
     a = warp_sum(a);
@@ -603,8 +605,8 @@ __device__ __forceinline__ void load_state_block(const float* __restrict__ src, 
   for (int e = threadIdx.x; e < nf * ld; e += kThreads) blk[e] = src[(size_t)f0 * ld + e];
 }
 
-// features of the tile rows xs against all m rows of Omega into P [kBT][ldp]
-template <int FM>
+// features of the tile rows xs against all m rows of Omega into P [TT][ldp]
+template <int TT, int FM>
 __device__ void tile_features(const float* xs, const float* rowc, int nt, int d, int m, float scale,
                               const float* __restrict__ omega, float* om, float* P, int ldp) {
   const int ld = d + 1;
@@ -614,7 +616,7 @@ __device__ void tile_features(const float* xs, const float* rowc, int nt, int d,
     __syncthreads();
     load_omega_block(omega, f0, nf, d, om);
     __syncthreads();
-    for (int e = threadIdx.x; e < kBT * kFB; e += kThreads) {
+    for (int e = threadIdx.x; e < TT * kFB; e += kThreads) {
       const int t = e / kFB, f = e - t * kFB;
       if (f < nf)
         P[t * ldp + f0 + f] = t < nt ? bwd_feature<FM>(scale * dot_row(xs + t * ld, om + f * ld, d), rowc[t]) : 0.f;
@@ -624,16 +626,16 @@ __device__ void tile_features(const float* xs, const float* rowc, int nt, int d,
 }
 
 // g <- dphi * phi (prf) or dphi [phi > 0] (relu) in G; gsum[t] = sum_i g
-template <int FM>
+template <int TT, int FM>
 __device__ void tile_g(const float* P, float* G, int ldp, int m, float* gsum) {
-  for (int e = threadIdx.x; e < kBT * m; e += kThreads) {
+  for (int e = threadIdx.x; e < TT * m; e += kThreads) {
     const int t = e / m, i = e - t * m;
     const float ph = P[t * ldp + i], dp = G[t * ldp + i];
     G[t * ldp + i] = FM == FAVOR_FM_PRF ? dp * ph : (ph > 0.f ? dp : 0.f);
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int t = warp; t < kBT; t += kThreads / 32) {
+  for (int t = warp; t < TT; t += kThreads / 32) {
     float a = 0.f;
     for (int i = lane; i < m; i += 32) a += G[t * ldp + i];
     a = warp_sum(a);
@@ -643,11 +645,11 @@ __device__ void tile_g(const float* P, float* G, int ldp, int m, float* gsum) {
 }
 
 // dx_t = s (sum_i g[t][i] w_i - [prf] s x_t sum_i g[t][i]) stored as T [nt][d]
-template <typename T, int FM>
+template <int TT, typename T, int FM>
 __device__ void tile_input_grad(const float* xs, const float* G, int ldp, const float* gsum, int nt, int d, int m,
                                 float scale, const float* __restrict__ omega, float* om, T* __restrict__ out) {
   const int ld = d + 1;
-  constexpr int kPer = (kBT * kMaxD + kThreads - 1) / kThreads;
+  constexpr int kPer = (TT * kMaxD + kThreads - 1) / kThreads;
   float acc[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
@@ -660,7 +662,7 @@ __device__ void tile_input_grad(const float* xs, const float* G, int ldp, const 
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int e = threadIdx.x + k * kThreads;
-      if (e < kBT * d) {
+      if (e < TT * d) {
         const int t = e / d, c = e - t * d;
         float a = acc[k];
         for (int f = 0; f < nf; ++f) a = fmaf(G[t * ldp + f0 + f], om[f * ld + c], a);
@@ -700,16 +702,16 @@ __global__ void __launch_bounds__(kThreads) bwd_query_kernel(
   float* rs = G + kBT * ldp;        // [kBT] squared norms, then row constants
   float* gsum = rs + kBT;           // [kBT]
   const size_t row0 = (size_t)bh * L + t0;
-  load_tile(Q + row0 * d, nt, d, xs);
-  load_tile(dO + row0 * d, nt, d, go);
+  load_tile<kBT>(Q + row0 * d, nt, d, xs);
+  load_tile<kBT>(dO + row0 * d, nt, d, go);
   __syncthreads();
-  tile_norms(xs, d, rs);
+  tile_norms<kBT>(xs, d, rs);
   __syncthreads();
   float R, W;
   key_reference(key_ref, m, &R, &W);
   if (threadIdx.x < kBT)
     rs[threadIdx.x] = FM == FAVOR_FM_PRF ? scale * sqrtf(rs[threadIdx.x]) * W - 20.0f : 0.f;
-  tile_features<FM>(xs, rs, nt, d, m, scale, omega, om, P, ldp);
+  tile_features<kBT, FM>(xs, rs, nt, d, m, scale, omega, om, P, ldp);
 
   // N | D
   const float* Sh = state + (size_t)bh * m * ld;
@@ -770,8 +772,8 @@ __global__ void __launch_bounds__(kThreads) bwd_query_kernel(
     }
   }
   __syncthreads();
-  tile_g<FM>(P, G, ldp, m, gsum);
-  tile_input_grad<T, FM>(xs, G, ldp, gsum, nt, d, m, scale, omega, om, dQ + row0 * d);
+  tile_g<kBT, FM>(P, G, ldp, m, gsum);
+  tile_input_grad<kBT, T, FM>(xs, G, ldp, gsum, nt, d, m, scale, omega, om, dQ + row0 * d);
 }
 
 // Feature-block pass: partial dS~ of a token split and a block of features,
@@ -802,10 +804,10 @@ __global__ void __launch_bounds__(kThreads) bwd_dstate_partial_kernel(
     const int nt = min(kBT, l1 - t0);
     const size_t row0 = (size_t)bh * L + t0;
     __syncthreads();
-    load_tile(Q + row0 * d, nt, d, xs);
+    load_tile<kBT>(Q + row0 * d, nt, d, xs);
     for (int e = threadIdx.x; e < kBT * ld; e += kThreads) dn[e] = e < nt * ld ? dnw[row0 * ld + e] : 0.f;
     __syncthreads();
-    tile_norms(xs, d, rs);
+    tile_norms<kBT>(xs, d, rs);
     __syncthreads();
     for (int e = threadIdx.x; e < kBT * kFB; e += kThreads) {
       const int t = e / kFB, f = e - t * kFB;
@@ -852,17 +854,17 @@ __global__ void __launch_bounds__(kThreads) bwd_key_kernel(
   float* rs = G + kBT * ldp;        // [kBT]
   float* gsum = rs + kBT;           // [kBT]
   const size_t row0 = (size_t)bh * L + t0;
-  load_tile(K + row0 * d, nt, d, xs);
-  load_tile(V + row0 * d, nt, d, vs);
+  load_tile<kBT>(K + row0 * d, nt, d, xs);
+  load_tile<kBT>(V + row0 * d, nt, d, vs);
   if (threadIdx.x < kBT) vs[threadIdx.x * ld + d] = threadIdx.x < nt ? 1.f : 0.f;
   __syncthreads();
-  tile_norms(xs, d, rs);
+  tile_norms<kBT>(xs, d, rs);
   __syncthreads();
   float R, W;
   key_reference(key_ref, m, &R, &W);
   if (threadIdx.x < kBT)
     rs[threadIdx.x] = FM == FAVOR_FM_PRF ? 0.5f * scale * scale * rs[threadIdx.x] + R : 0.f;
-  tile_features<FM>(xs, rs, nt, d, m, scale, omega, om, P, ldp);
+  tile_features<kBT, FM>(xs, rs, nt, d, m, scale, omega, om, P, ldp);
 
   const float* dS = dstate + (size_t)bh * m * ld;
   constexpr int kPer = (kBT * kMaxD + kThreads - 1) / kThreads;
@@ -896,8 +898,8 @@ __global__ void __launch_bounds__(kThreads) bwd_key_kernel(
     if (e < nt * d) dV[row0 * d + e] = from_f32<T>(accv[k]);
   }
   __syncthreads();
-  tile_g<FM>(P, G, ldp, m, gsum);
-  tile_input_grad<T, FM>(xs, G, ldp, gsum, nt, d, m, scale, omega, om, dK + row0 * d);
+  tile_g<kBT, FM>(P, G, ldp, m, gsum);
+  tile_input_grad<kBT, T, FM>(xs, G, ldp, gsum, nt, d, m, scale, omega, om, dK + row0 * d);
 }
 
 size_t bwd_tile_smem(int d, int m) {
@@ -907,6 +909,271 @@ size_t bwd_tile_smem(int d, int m) {
 size_t bwd_dstate_smem(int d) {
   const int ld = d + 1;
   return sizeof(float) * ((size_t)kFB * ld + (size_t)2 * kBT * ld + (size_t)kBT * (kFB + 1) + kBT);
+}
+
+// ---------------------------------------------------------------------------
+// Causal backward: one CTA per head, tiles of kCT tokens.  With the prefix
+// state G~_c = sum over earlier tiles of phi(k) [v ; 1]^T and, inside a tile,
+// A = tril(phi(Q) phi(K)^T):
+//   N^_t = phi(q_t)^T G~_c + sum_{s<=t} A_ts [v_s ; 1]   (N | D)
+//   dphi(q_t) = G~_c dN^_t + sum_{s<=t} (dN^_t . [v_s ; 1]) phi(k_s)
+// (forward walk), and with the suffix state H_c = sum over later tiles of
+// phi(q) dN^T (reverse walk):
+//   dphi(k_s) = H_c [v_s ; 1] + sum_{t>=s} (dN^_t . [v_s ; 1]) phi(q_t)
+//   dV_s = H_c[:, :d]^T phi(k_s) + sum_{t>=s} A_ts dN_t
+// ---------------------------------------------------------------------------
+constexpr int kCT = 16;
+
+template <typename T, int FM>
+__global__ void __launch_bounds__(kThreads) cbwd_query_kernel(
+    const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,
+    T* __restrict__ dQ, const float* __restrict__ omega, const float* __restrict__ key_ref, float* __restrict__ gst,
+    float* __restrict__ dnw, int L, int d, int m, float scale, int32_t* status) {
+  extern __shared__ float smem[];
+  const int ld = d + 1, ldp = m + 1;
+  const int bh = blockIdx.x;
+  float* xs = smem;                   // [kCT][ld] q
+  float* ks = xs + kCT * ld;          // [kCT][ld] k
+  float* vs = ks + kCT * ld;          // [kCT][ld] v | 1
+  float* go = vs + kCT * ld;          // [kCT][ld] dO, then dN^
+  float* nd = go + kCT * ld;          // [kCT][ld] N | D
+  float* om = nd + kCT * ld;          // [kFB][ld]
+  float* P = om + kFB * ld;           // [kCT][ldp] phi(Q)
+  float* Pk = P + kCT * ldp;          // [kCT][ldp] phi(K)
+  float* G = Pk + kCT * ldp;          // [kCT][ldp] dphi(Q), then g
+  float* A = G + kCT * ldp;           // [kCT][kCT + 1]
+  float* Bm = A + kCT * (kCT + 1);    // [kCT][kCT + 1]
+  float* rq = Bm + kCT * (kCT + 1);   // [kCT]
+  float* rk = rq + kCT;               // [kCT]
+  float* gsum = rk + kCT;             // [kCT]
+  float* Gh = gst + (size_t)bh * m * ld;
+  for (int e = threadIdx.x; e < m * ld; e += kThreads) Gh[e] = 0.f;
+  float R, W;
+  key_reference(key_ref, m, &R, &W);
+  const int n_fb = (m + kFB - 1) / kFB;
+  constexpr int kPerN = (kCT * (kMaxD + 1) + kThreads - 1) / kThreads;
+  for (int t0 = 0; t0 < L; t0 += kCT) {
+    const int nt = min(kCT, L - t0);
+    const size_t row0 = (size_t)bh * L + t0;
+    __syncthreads();
+    load_tile<kCT>(Q + row0 * d, nt, d, xs);
+    load_tile<kCT>(K + row0 * d, nt, d, ks);
+    load_tile<kCT>(V + row0 * d, nt, d, vs);
+    load_tile<kCT>(dO + row0 * d, nt, d, go);
+    if (threadIdx.x < kCT) vs[threadIdx.x * ld + d] = threadIdx.x < nt ? 1.f : 0.f;
+    __syncthreads();
+    tile_norms<kCT>(xs, d, rq);
+    tile_norms<kCT>(ks, d, rk);
+    __syncthreads();
+    if (threadIdx.x < kCT) {
+      rq[threadIdx.x] = FM == FAVOR_FM_PRF ? scale * sqrtf(rq[threadIdx.x]) * W - 20.0f : 0.f;
+      rk[threadIdx.x] = FM == FAVOR_FM_PRF ? 0.5f * scale * scale * rk[threadIdx.x] + R : 0.f;
+    }
+    tile_features<kCT, FM>(xs, rq, nt, d, m, scale, omega, om, P, ldp);
+    tile_features<kCT, FM>(ks, rk, nt, d, m, scale, omega, om, Pk, ldp);
+    for (int e = threadIdx.x; e < kCT * kCT; e += kThreads) {
+      const int t = e / kCT, s_ = e - t * kCT;
+      float a = 0.f;
+      if (s_ <= t && t < nt)
+        for (int i = 0; i < m; ++i) a = fmaf(P[t * ldp + i], Pk[s_ * ldp + i], a);
+      A[t * (kCT + 1) + s_] = a;
+    }
+    // N | D: prefix state part, then the tile's own (masked) part
+    float acc[kPerN];
+#pragma unroll
+    for (int k = 0; k < kPerN; ++k) acc[k] = 0.f;
+    for (int fb = 0; fb < n_fb; ++fb) {
+      const int f0 = fb * kFB, nf = min(kFB, m - f0);
+      __syncthreads();
+      load_state_block(Gh, f0, nf, d, om);
+      __syncthreads();
+#pragma unroll
+      for (int k = 0; k < kPerN; ++k) {
+        const int e = threadIdx.x + k * kThreads;
+        if (e < kCT * ld) {
+          const int t = e / ld, j = e - t * ld;
+          float a = acc[k];
+          for (int f = 0; f < nf; ++f) a = fmaf(P[t * ldp + f0 + f], om[f * ld + j], a);
+          acc[k] = a;
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPerN; ++k) {
+      const int e = threadIdx.x + k * kThreads;
+      if (e < kCT * ld) {
+        const int t = e / ld, j = e - t * ld;
+        float a = acc[k];
+        for (int s_ = 0; s_ <= t; ++s_) a = fmaf(A[t * (kCT + 1) + s_], vs[s_ * ld + j], a);
+        nd[e] = a;
+      }
+    }
+    __syncthreads();
+    {
+      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+      for (int t = warp; t < kCT; t += kThreads / 32) {
+        const float D = nd[t * ld + d];
+        float a = 0.f;
+        for (int j = lane; j < d; j += 32) a = fmaf(go[t * ld + j], nd[t * ld + j], a);
+        a = warp_sum(a);
+        const bool valid = t < nt;
+        if (valid && lane == 0 && (!(D > 0.f) || !isfinite(D))) report_status(status, FAVOR_ERR_NONFINITE);
+        const float inv = 1.0f / D;
+        __syncwarp();
+        for (int j = lane; j < d; j += 32) go[t * ld + j] = valid ? go[t * ld + j] * inv : 0.f;
+        if (lane == 0) go[t * ld + d] = valid ? -a * inv * inv : 0.f;
+      }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < nt * ld; e += kThreads) dnw[row0 * ld + e] = go[e];
+    for (int e = threadIdx.x; e < kCT * kCT; e += kThreads) {
+      const int t = e / kCT, s_ = e - t * kCT;
+      float a = 0.f;
+      if (s_ <= t)
+        for (int j = 0; j < ld; ++j) a = fmaf(vs[s_ * ld + j], go[t * ld + j], a);
+      Bm[t * (kCT + 1) + s_] = a;
+    }
+    // dphi(Q) = G~ dN^ + sum_{s<=t} B_ts phi(k_s)
+    for (int fb = 0; fb < n_fb; ++fb) {
+      const int f0 = fb * kFB, nf = min(kFB, m - f0);
+      __syncthreads();
+      load_state_block(Gh, f0, nf, d, om);
+      __syncthreads();
+      for (int e = threadIdx.x; e < kCT * kFB; e += kThreads) {
+        const int t = e / kFB, f = e - t * kFB;
+        if (f < nf) {
+          float a = dot_row(om + f * ld, go + t * ld, ld);
+          for (int s_ = 0; s_ <= t; ++s_) a = fmaf(Bm[t * (kCT + 1) + s_], Pk[s_ * ldp + f0 + f], a);
+          G[t * ldp + f0 + f] = a;
+        }
+      }
+    }
+    __syncthreads();
+    tile_g<kCT, FM>(P, G, ldp, m, gsum);
+    tile_input_grad<kCT, T, FM>(xs, G, ldp, gsum, nt, d, m, scale, omega, om, dQ + row0 * d);
+    // G~ += phi(K)^T [V | 1] of this tile (each element owned by one thread)
+    for (int e = threadIdx.x; e < m * ld; e += kThreads) {
+      const int i = e / ld, j = e - i * ld;
+      float a = 0.f;
+      for (int s_ = 0; s_ < nt; ++s_) a = fmaf(Pk[s_ * ldp + i], vs[s_ * ld + j], a);
+      Gh[e] += a;
+    }
+  }
+}
+
+template <typename T, int FM>
+__global__ void __launch_bounds__(kThreads) cbwd_key_kernel(
+    const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V, T* __restrict__ dK,
+    T* __restrict__ dV, const float* __restrict__ omega, const float* __restrict__ key_ref, float* __restrict__ hst,
+    const float* __restrict__ dnw, int L, int d, int m, float scale) {
+  extern __shared__ float smem[];
+  const int ld = d + 1, ldp = m + 1;
+  const int bh = blockIdx.x;
+  float* xs = smem;                   // [kCT][ld] q
+  float* ks = xs + kCT * ld;          // [kCT][ld] k
+  float* vs = ks + kCT * ld;          // [kCT][ld] v | 1
+  float* go = vs + kCT * ld;          // [kCT][ld] dN^
+  float* nd = go + kCT * ld;          // unused here (same layout as the query kernel)
+  float* om = nd + kCT * ld;          // [kFB][ld]
+  float* P = om + kFB * ld;           // [kCT][ldp] phi(Q)
+  float* Pk = P + kCT * ldp;          // [kCT][ldp] phi(K)
+  float* G = Pk + kCT * ldp;          // [kCT][ldp] dphi(K), then g
+  float* A = G + kCT * ldp;           // [kCT][kCT + 1]  A_st = phi(k_s).phi(q_t), t >= s
+  float* Cm = A + kCT * (kCT + 1);    // [kCT][kCT + 1]  C_st = dN^_t . [v_s ; 1], t >= s
+  float* rq = Cm + kCT * (kCT + 1);   // [kCT]
+  float* rk = rq + kCT;               // [kCT]
+  float* gsum = rk + kCT;             // [kCT]
+  float* Hh = hst + (size_t)bh * m * ld;
+  for (int e = threadIdx.x; e < m * ld; e += kThreads) Hh[e] = 0.f;
+  float R, W;
+  key_reference(key_ref, m, &R, &W);
+  const int n_fb = (m + kFB - 1) / kFB;
+  constexpr int kPer = (kCT * kMaxD + kThreads - 1) / kThreads;
+  const int n_tiles = (L + kCT - 1) / kCT;
+  for (int tile = n_tiles - 1; tile >= 0; --tile) {
+    const int t0 = tile * kCT;
+    const int nt = min(kCT, L - t0);
+    const size_t row0 = (size_t)bh * L + t0;
+    __syncthreads();
+    load_tile<kCT>(Q + row0 * d, nt, d, xs);
+    load_tile<kCT>(K + row0 * d, nt, d, ks);
+    load_tile<kCT>(V + row0 * d, nt, d, vs);
+    for (int e = threadIdx.x; e < kCT * ld; e += kThreads) go[e] = e < nt * ld ? dnw[row0 * ld + e] : 0.f;
+    if (threadIdx.x < kCT) vs[threadIdx.x * ld + d] = threadIdx.x < nt ? 1.f : 0.f;
+    __syncthreads();
+    tile_norms<kCT>(xs, d, rq);
+    tile_norms<kCT>(ks, d, rk);
+    __syncthreads();
+    if (threadIdx.x < kCT) {
+      rq[threadIdx.x] = FM == FAVOR_FM_PRF ? scale * sqrtf(rq[threadIdx.x]) * W - 20.0f : 0.f;
+      rk[threadIdx.x] = FM == FAVOR_FM_PRF ? 0.5f * scale * scale * rk[threadIdx.x] + R : 0.f;
+    }
+    tile_features<kCT, FM>(xs, rq, nt, d, m, scale, omega, om, P, ldp);
+    tile_features<kCT, FM>(ks, rk, nt, d, m, scale, omega, om, Pk, ldp);
+    for (int e = threadIdx.x; e < kCT * kCT; e += kThreads) {
+      const int s_ = e / kCT, t = e - s_ * kCT;
+      float a = 0.f, c = 0.f;
+      if (t >= s_ && t < nt) {
+        for (int i = 0; i < m; ++i) a = fmaf(Pk[s_ * ldp + i], P[t * ldp + i], a);
+        for (int j = 0; j < ld; ++j) c = fmaf(go[t * ld + j], vs[s_ * ld + j], c);
+      }
+      A[s_ * (kCT + 1) + t] = a;
+      Cm[s_ * (kCT + 1) + t] = c;
+    }
+    float accv[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) accv[k] = 0.f;
+    for (int fb = 0; fb < n_fb; ++fb) {
+      const int f0 = fb * kFB, nf = min(kFB, m - f0);
+      __syncthreads();
+      load_state_block(Hh, f0, nf, d, om);
+      __syncthreads();
+      for (int e = threadIdx.x; e < kCT * kFB; e += kThreads) {
+        const int s_ = e / kFB, f = e - s_ * kFB;
+        if (f < nf) {
+          float a = dot_row(om + f * ld, vs + s_ * ld, ld);
+          for (int t = s_; t < kCT; ++t) a = fmaf(Cm[s_ * (kCT + 1) + t], P[t * ldp + f0 + f], a);
+          G[s_ * ldp + f0 + f] = a;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int e = threadIdx.x + k * kThreads;
+        if (e < kCT * d) {
+          const int s_ = e / d, j = e - s_ * d;
+          float a = accv[k];
+          for (int f = 0; f < nf; ++f) a = fmaf(Pk[s_ * ldp + f0 + f], om[f * ld + j], a);
+          accv[k] = a;
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int e = threadIdx.x + k * kThreads;
+      if (e < nt * d) {
+        const int s_ = e / d, j = e - s_ * d;
+        float a = accv[k];
+        for (int t = s_; t < kCT; ++t) a = fmaf(A[s_ * (kCT + 1) + t], go[t * ld + j], a);
+        dV[row0 * d + e] = from_f32<T>(a);
+      }
+    }
+    __syncthreads();
+    tile_g<kCT, FM>(Pk, G, ldp, m, gsum);
+    tile_input_grad<kCT, T, FM>(ks, G, ldp, gsum, nt, d, m, scale, omega, om, dK + row0 * d);
+    // H += phi(Q)^T dN^ of this tile
+    for (int e = threadIdx.x; e < m * ld; e += kThreads) {
+      const int i = e / ld, j = e - i * ld;
+      float a = 0.f;
+      for (int t = 0; t < nt; ++t) a = fmaf(P[t * ldp + i], go[t * ld + j], a);
+      Hh[e] += a;
+    }
+  }
+}
+
+size_t cbwd_smem(int d, int m) {
+  const int ld = d + 1, ldp = m + 1;
+  return sizeof(float) * ((size_t)5 * kCT * ld + (size_t)kFB * ld + (size_t)3 * kCT * ldp +
+                          (size_t)2 * kCT * (kCT + 1) + 3 * kCT);
 }
 
 }  // namespace
@@ -924,6 +1191,33 @@ BwdPlan bwd_plan(const Shape& s) {
   off = align256(off + BH * s.m * ld * sizeof(float));
   b.bytes = off;
   return b;
+}
+
+cudaError_t simt_bwd_causal(const void* Q, const void* K, const void* V, const void* dO, void* dQ, void* dK,
+                            void* dV, const float* omega, float scale, const Shape& s, bool bf16, void* ws, int32_t* st,
+                            cudaStream_t stream, int fm) {
+  const BwdPlan b = bwd_plan(s);
+  char* w = static_cast<char*>(ws);
+  float* key_ref = reinterpret_cast<float*>(w);
+  cudaError_t e = launch_prep(omega, s.m, s.d, key_ref, nullptr, nullptr, 0, stream);
+  if (e != cudaSuccess) return e;
+  float* state = reinterpret_cast<float*>(w + b.off_dstate);   // G~ (forward walk), then H (reverse walk)
+  float* dnw = reinterpret_cast<float*>(w + b.off_dn);
+  const size_t sm = cbwd_smem(s.d, s.m);
+  return dispatch(bf16, fm, [&](auto tag, auto f) {
+    using T = decltype(tag);
+    constexpr int FM = decltype(f)::value;
+    cudaError_t r = set_smem(cbwd_query_kernel<T, FM>, sm);
+    if (r == cudaSuccess) r = set_smem(cbwd_key_kernel<T, FM>, sm);
+    if (r != cudaSuccess) return r;
+    cbwd_query_kernel<T, FM><<<s.BH(), kThreads, sm, stream>>>(
+        static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V), static_cast<const T*>(dO),
+        static_cast<T*>(dQ), omega, key_ref, state, dnw, s.L, s.d, s.m, scale, st);
+    cbwd_key_kernel<T, FM><<<s.BH(), kThreads, sm, stream>>>(
+        static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V), static_cast<T*>(dK),
+        static_cast<T*>(dV), omega, key_ref, state, dnw, s.L, s.d, s.m, scale);
+    return cudaGetLastError();
+  });
 }
 
 cudaError_t simt_bwd_bidir(const void* Q, const void* K, const void* V, const void* dO, void* dQ, void* dK, void* dV,

@@ -152,14 +152,15 @@ def test_feature_map_calls_reject_bad_arguments(lib, name):
     assert call(nbytes=16) == 1
 
 
-def test_backward_rejects_bad_arguments_before_launch(lib):
+@pytest.mark.parametrize("name", ["favor_bwd_bidir", "favor_bwd_causal"])
+def test_backward_rejects_bad_arguments_before_launch(lib, name):
     def call(**kw):
         a = dict(Q=16, K=32, V=48, dO=64, dQ=80, dK=96, dV=112, B=1, H=1, L=8, d=8, omega=128, m=8, dt=0, s=1.0,
                  fm=0, ws=256, nbytes=1 << 30, st=None, stream=None)
         a.update(kw)
-        return lib.favor_bwd_bidir(a["Q"], a["K"], a["V"], a["dO"], a["dQ"], a["dK"], a["dV"], a["B"], a["H"],
-                                   a["L"], a["d"], a["omega"], a["m"], a["dt"], a["s"], a["fm"], a["ws"],
-                                   a["nbytes"], a["st"], a["stream"])
+        return getattr(lib, name)(a["Q"], a["K"], a["V"], a["dO"], a["dQ"], a["dK"], a["dV"], a["B"], a["H"],
+                                  a["L"], a["d"], a["omega"], a["m"], a["dt"], a["s"], a["fm"], a["ws"],
+                                  a["nbytes"], a["st"], a["stream"])
     assert call(dO=None) == 1
     assert call(dQ=None) == 1
     assert call(dQ=16) == 1            # dQ aliases Q

@@ -58,3 +58,42 @@ def test_backward_is_deterministic(cuda_lib):
     b = cuda_lib.bwd_bidir(Q, K, V, dO, om, 0.4)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("features", ["prf", "relu"])
+@pytest.mark.parametrize("dtype,B,H,L,d,m", [(torch.float32, 2, 2, 75, 64, 128),
+                                             (torch.float32, 1, 2, 33, 32, 100),
+                                             (torch.bfloat16, 2, 3, 300, 64, 256),
+                                             (torch.bfloat16, 1, 2, 50, 128, 512)])
+def test_causal_backward_matches_oracle(cuda_lib, features, dtype, B, H, L, d, m):
+    w = wl.Workload("cbwd", "causal", "f32" if dtype == torch.float32 else "bf16", B, H, L, d, m, "normal")
+    Q, K, V = (t.cuda() for t in wl.make_qkv(w, seed=3 * L + m))
+    if features == "relu":
+        # the first row's only key is itself: phi(q0).phi(k0) = |phi(q0)|^2 > 0
+        K[:, :, 0] = Q[:, :, 0]
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(L + 2 * m)
+    dO = torch.randn((B, H, L, d), generator=gen).to(dtype).cuda()
+    om = cuda_lib.new_omega(m + 5, m, d)
+    s = d ** -0.25
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dQ, dK, dV = cuda_lib.bwd_causal(Q, K, V, dO, om, s, feature_map=features, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rQ, rK, rV = orc.favor_causal_grad(to_np(Q), to_np(K), to_np(V), to_np(om), s, to_np(dO), features)
+    errs = {n: _per_head_err(to_np(g), r) for n, g, r in (("dQ", dQ, rQ), ("dK", dK, rK), ("dV", dV, rV))}
+    assert max(errs.values()) < TOL[dtype], errs
+
+
+def test_causal_backward_last_row_equals_bidirectional(cuda_lib):
+    # dO zero except the last row: the two losses coincide
+    B, H, L, d, m = 1, 2, 70, 64, 128
+    w = wl.Workload("cbwd", "causal", "f32", B, H, L, d, m, "normal")
+    Q, K, V = (t.cuda() for t in wl.make_qkv(w, seed=4))
+    dO = torch.zeros_like(Q)
+    dO[:, :, -1] = torch.randn((B, H, d), generator=torch.Generator().manual_seed(4)).cuda()
+    om = cuda_lib.new_omega(4, m, d)
+    a = cuda_lib.bwd_causal(Q, K, V, dO, om, 0.4)
+    b = cuda_lib.bwd_bidir(Q, K, V, dO, om, 0.4)
+    for x, y in zip(a, b):
+        assert _per_head_err(to_np(x), to_np(y)) < 1e-4
