@@ -562,8 +562,9 @@ def run_reference(args, rank, world):
 
 
 def measure_backward(favor, n_steps, sets, omega, s, stream, status, dev, tokens_per_step, hbm):
-    """favor_bwd_bidir on the step's workload (CUDA-core kernels): dQ, dK, dV
-    for a seeded dO, inputs rotating over the sets, one CUDA graph per set.
+    """favor_bwd_bidir and favor_bwd_causal on the step's workload (CUDA-core
+    kernels): dQ, dK, dV for a seeded dO, inputs rotating over the sets, one
+    CUDA graph per set.
     Algorithmic bytes: read Q, K, V, dO and write dQ, dK, dV (7 d e per
     head-token)."""
     q0 = sets[0][0]
@@ -573,30 +574,36 @@ def measure_backward(favor, n_steps, sets, omega, s, stream, status, dev, tokens
     dO = torch.randn(q0.shape, generator=gen).to(q0.dtype).to(dev)
     ws = torch.empty(favor.bwd_workspace_bytes(B, H, L, d, omega.shape[0], q0.dtype), dtype=torch.uint8, device=dev)
     dQ, dK, dV = torch.empty_like(q0), torch.empty_like(q0), torch.empty_like(q0)
-    graphs = []
-    for q, k, v in sets:
+    out = {}
+    for causal in (False, True):
+        graphs = []
+        for q, k, v in sets:
+            with torch.cuda.stream(stream):
+                favor.bwd_bidir(q, k, v, dO, omega, s, ws, dQ=dQ, dK=dK, dV=dV, dev_status=status, stream=stream,
+                                causal=causal)
+            torch.cuda.synchronize(dev)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                favor.bwd_bidir(q, k, v, dO, omega, s, ws, dQ=dQ, dK=dK, dV=dV, dev_status=status, stream=stream,
+                                causal=causal)
+            graphs.append(g)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
-            favor.bwd_bidir(q, k, v, dO, omega, s, ws, dQ=dQ, dK=dK, dV=dV, dev_status=status, stream=stream)
+            graphs[0].replay()
+            e0.record(stream)
+            for i in range(n_steps):
+                graphs[i % len(graphs)].replay()
+            e1.record(stream)
         torch.cuda.synchronize(dev)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            favor.bwd_bidir(q, k, v, dO, omega, s, ws, dQ=dQ, dK=dK, dV=dV, dev_status=status, stream=stream)
-        graphs.append(g)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        graphs[0].replay()
-        e0.record(stream)
-        for i in range(n_steps):
-            graphs[i % len(graphs)].replay()
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item())} after the backward steps")
-    ms = e0.elapsed_time(e1) / n_steps
-    nbytes = 7 * q0.numel() * q0.element_size()
-    return {"value": tokens_per_step / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": n_steps,
-            "step": "bidirectional backward (dQ, dK, dV), CUDA-core kernels",
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())} after the backward steps")
+        ms = e0.elapsed_time(e1) / n_steps
+        nbytes = 7 * q0.numel() * q0.element_size()
+        out["causal" if causal else "bidir"] = {
+            "value": tokens_per_step / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": n_steps,
             "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm}
+    out["step"] = "backward (dQ, dK, dV) of each pass, CUDA-core kernels"
+    return out
 
 
 def measure_feature_map(favor, fm, n_steps, sets, omega, s, ws_b, ws_c, O_b, O_c, stream, status, dev,
