@@ -44,6 +44,9 @@ __all__ = [
     "gram_schmidt_rows",
     "build_omega",
     "orf_index_layout",
+    "walsh_hadamard",
+    "rademacher_signs",
+    "build_omega_hadamard",
     "prf_features",
     "relu_features",
     "FEATURES",
@@ -174,6 +177,46 @@ def build_omega(seed: int, m: int, d: int, orthogonal: bool = True,
     c = np.arange(d)[None, :]
     Omega = counter_normals(seed, (i * d + c) * 2)
     return (Omega, None) if return_parts else Omega
+
+
+def walsh_hadamard(d: int) -> np.ndarray:
+    """The normalised d x d Walsh-Hadamard matrix (Sylvester's doubling,
+    H_1 = [1], H_2k = [[H_k, H_k], [H_k, -H_k]], divided by sqrt(d));
+    d must be a power of two."""
+    if d < 1 or d & (d - 1):
+        raise ValueError("d must be a power of two")
+    H = np.ones((1, 1))
+    while H.shape[0] < d:
+        H = np.block([[H, H], [H, -H]])
+    return H / math.sqrt(d)
+
+
+def rademacher_signs(seed: int, counters) -> np.ndarray:
+    """+1 or -1 from the top bit of SplitMix64 word ``counters`` (1 -> -1)."""
+    w = splitmix64_stream(seed, counters)
+    return np.where((w >> np.uint64(63)) == np.uint64(1), -1.0, 1.0)
+
+
+def build_omega_hadamard(seed: int, m: int, d: int) -> np.ndarray:
+    """Hadamard ORF projection, [m, d].
+
+    [summary] §A.2 (FAVOR+ bullet) and §B.3 name Hadamard ORFs (O(m) space,
+    a small bias that tends to zero as d grows) without printing a
+    construction; the reading: block b = sqrt(d) (H D_1)(H D_2)(H D_3) with H
+    the normalised Walsh-Hadamard matrix and D_p = diag(+-1), sign i of
+    product p of block b from SplitMix64 word (b*3 + p)*d + i (its top bit).
+    Each block is exactly orthogonal with rows of length sqrt(d) (not a chi_d
+    draw: hence the bias).  The first m rows of the stacked blocks are kept.
+    """
+    H = walsh_hadamard(d)
+    blocks = []
+    for b in range(-(-m // d)):
+        M = np.eye(d)
+        for p in range(3):
+            D = rademacher_signs(seed, (b * 3 + p) * d + np.arange(d))
+            M = M @ (H * D[None, :])          # (H D_p): column i of H times sign i
+        blocks.append(math.sqrt(d) * M)
+    return np.concatenate(blocks, axis=0)[:m]
 
 
 # --------------------------------------------------------------------------
