@@ -99,7 +99,14 @@ const char* favor_status_string(favor_status s);
  * sample), so each row keeps the N(0, I_d) marginal ("Performer" digest,
  * §Methods ORF bullet and the block-wise rule for m > d; arXiv summary §A.2:
  * orthogonality with marginals preserved).  The first m stacked rows are
- * kept.  orthogonal = 0: iid N(0, 1) entries.
+ * kept.  orthogonal = 0: iid N(0, 1) entries.  orthogonal = 2 (Hadamard
+ * ORF, d a power of two): block b = sqrt(d) (H D_1)(H D_2)(H D_3), H the
+ * normalised d x d Walsh-Hadamard matrix, D_p = diag(+-1) with sign i of
+ * product p from the top bit of SplitMix64 word (b*3 + p)*d + i (1 -> -1);
+ * exactly orthogonal blocks with rows of length sqrt(d), O(m) random numbers
+ * (arXiv summary §A.2: Hadamard ORFs, a small bias that tends to zero as d
+ * grows; §B.3: their O(m) space; no construction is printed, this is the
+ * plain reading).
  *
  * Random numbers: SplitMix64 word i = mix(seed + (i+1)*0x9E3779B97F4A7C15);
  * one normal per word by Box–Muller, z = sqrt(-2 ln u1) cos(2 pi u2) with
@@ -108,8 +115,9 @@ const char* favor_status_string(favor_status s);
  * component c of row r's length vector: the same + 1; iid entry (i, c):
  * (i*d + c)*2.  Arithmetic is fp32 (two Gram–Schmidt sweeps).
  *
- * Errors: FAVOR_ERR_INVALID_ARG if omega is NULL or m, d out of range
- * (1 <= d <= 128, 1 <= m <= 512).
+ * Errors: FAVOR_ERR_INVALID_ARG if omega is NULL, m, d out of range
+ * (1 <= d <= 128, 1 <= m <= 512) or orthogonal not 0, 1 or 2;
+ * FAVOR_ERR_UNSUPPORTED for orthogonal = 2 with d not a power of two.
  */
 favor_status favor_build_orf(uint64_t seed, int m, int d, int orthogonal,
                              float* omega, void* stream);

@@ -165,6 +165,51 @@ __global__ void __launch_bounds__(kMaxD * kTPR) orf_block_kernel(uint64_t seed, 
   }
 }
 
+// Hadamard ORF block b: sqrt(d) (H D_1)(H D_2)(H D_3), H the normalised
+// Walsh-Hadamard matrix, D_p = diag(+-1) with sign i of product p from the
+// top bit of SplitMix64 word (b*3 + p)*d + i ("Rethinking Attention with
+// Performers" summary, §A.2 and §B.3 name Hadamard ORFs; the construction is
+// the plain reading).  X starts as the identity; X <- X (H D_p) applies the
+// fast Walsh-Hadamard transform to every row of X, then the column signs.
+// One CTA per block, X [d][d+1] in shared memory; d a power of two.
+__global__ void __launch_bounds__(256) hadamard_block_kernel(uint64_t seed, int m, int d, float* __restrict__ omega) {
+  extern __shared__ float X[];
+  const int b = blockIdx.x;
+  const int ld = d + 1;
+  for (int e = threadIdx.x; e < d * d; e += blockDim.x) {
+    const int r = e / d, c = e - r * d;
+    X[r * ld + c] = (r == c) ? 1.f : 0.f;
+  }
+  __syncthreads();
+  const float inv_sqrt_d = rsqrtf(static_cast<float>(d));
+  for (int p = 0; p < 3; ++p) {
+    for (int h = 1; h < d; h <<= 1) {
+      // d rows x d/2 butterflies (i, i + h) with (i & h) == 0
+      for (int e = threadIdx.x; e < d * (d / 2); e += blockDim.x) {
+        const int r = e / (d / 2), k = e - r * (d / 2);
+        const int i = (k / h) * 2 * h + (k % h);
+        const float a = X[r * ld + i], c = X[r * ld + i + h];
+        X[r * ld + i] = a + c;
+        X[r * ld + i + h] = a - c;
+      }
+      __syncthreads();
+    }
+    for (int e = threadIdx.x; e < d * d; e += blockDim.x) {
+      const int r = e / d, c = e - r * d;
+      const uint64_t w = splitmix_word(seed, static_cast<uint64_t>(b * 3 + p) * d + c);
+      const float sgn = (w >> 63) ? -1.f : 1.f;
+      X[r * ld + c] *= sgn * inv_sqrt_d;
+    }
+    __syncthreads();
+  }
+  const float sqrt_d = sqrtf(static_cast<float>(d));
+  for (int e = threadIdx.x; e < d * d; e += blockDim.x) {
+    const int r = e / d, c = e - r * d;
+    const int row = b * d + r;
+    if (row < m) omega[(size_t)row * d + c] = sqrt_d * X[r * ld + c];
+  }
+}
+
 __global__ void iid_kernel(uint64_t seed, int m, int d, float* __restrict__ omega) {
   const int n = m * d;
   for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) {
@@ -176,6 +221,13 @@ __global__ void iid_kernel(uint64_t seed, int m, int d, float* __restrict__ omeg
 
 cudaError_t launch_build_orf(uint64_t seed, int m, int d, int orthogonal, float* omega,
                              cudaStream_t stream) {
+  if (orthogonal == 2) {
+    const size_t smem = (size_t)d * (d + 1) * sizeof(float);
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(hadamard_block_kernel), smem);
+    if (e != cudaSuccess) return e;
+    hadamard_block_kernel<<<(m + d - 1) / d, 256, smem, stream>>>(seed, m, d, omega);
+    return cudaGetLastError();
+  }
   if (orthogonal) {
     const int nb = (m + d - 1) / d;
     const int threads = ((d * kTPR + 31) / 32) * 32;

@@ -89,6 +89,8 @@ def test_build_orf_rejects_bad_arguments(lib):
     assert lib.favor_build_orf(ctypes.c_uint64(0), 8, 8, 1, None, None) == 1
     assert lib.favor_build_orf(ctypes.c_uint64(0), 0, 8, 1, 16, None) == 1
     assert lib.favor_build_orf(ctypes.c_uint64(0), 8, 200, 1, 16, None) == 1
+    assert lib.favor_build_orf(ctypes.c_uint64(0), 8, 8, 3, 16, None) == 1      # unknown kind
+    assert lib.favor_build_orf(ctypes.c_uint64(0), 8, 12, 2, 16, None) == 2     # Hadamard needs a power of two
 
 
 def test_product_code_does_not_touch_the_oracle():

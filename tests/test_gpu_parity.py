@@ -53,6 +53,28 @@ def test_orf_matches_oracle(cuda_lib, seed, m, d):
         assert np.max(np.abs(dirs @ dirs.T - np.eye(dirs.shape[0]))) < 2e-6
 
 
+@pytest.mark.parametrize("seed,m,d", [(0, 64, 64), (1, 256, 64), (2, 512, 128), (3, 100, 32), (4, 3, 2)])
+def test_hadamard_omega_matches_oracle(cuda_lib, seed, m, d):
+    om = torch.empty((m, d), dtype=torch.float32, device="cuda")
+    cuda_lib.build_orf(seed, om, orthogonal="hadamard")
+    got, want = to_np(om), orc.build_omega_hadamard(seed, m, d)
+    assert np.max(np.abs(got - want)) < 1e-5 * np.max(np.abs(want))
+    for b in range(0, m, d):
+        blk = got[b:b + d]
+        assert np.max(np.abs(blk @ blk.T - d * np.eye(blk.shape[0]))) < 1e-4 * d
+
+
+def test_hadamard_omega_in_attention(cuda_lib):
+    # a Hadamard projection runs through the same kernels as any other Omega
+    w = wl.Workload("had", "bidir", "bf16", 1, 2, 500, 64, 256, "normal")
+    Q, K, V = (t.cuda() for t in wl.make_qkv(w, seed=6))
+    om = torch.empty((w.m, w.d), dtype=torch.float32, device="cuda")
+    cuda_lib.build_orf(6, om, orthogonal="hadamard")
+    O = _run(cuda_lib, False, Q, K, V, om, w.qk_scale)
+    ref = orc.favor_bidirectional(to_np(Q), to_np(K), to_np(V), to_np(om), w.qk_scale)
+    assert orc.rowwise_rel_err(to_np(O), ref) < TOL[torch.bfloat16]
+
+
 def test_iid_omega_matches_oracle(cuda_lib):
     om = to_np(cuda_lib.new_omega(4, 300, 70, orthogonal=False))
     want = orc.build_omega(4, 300, 70, orthogonal=False)
