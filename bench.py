@@ -469,7 +469,8 @@ def run_gpu(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world}"},
         "modes": {"bidir_tokens_per_s": tokens_per_step / (bidir_ms / 1e3),
                   "causal_tokens_per_s": tokens_per_step / (causal_ms / 1e3),
-                  "build_orf_ms": stage_ms["build_orf"]},
+                  "build_orf_ms": stage_ms["build_orf"],
+                  "build_orf_hadamard_ms": time_build(favor, "hadamard", m, d, stream, dev)},
         "stages": stages_out,
         "roofline": roof,
         "gpu_launches": launches_per_step * args.steps,
@@ -559,6 +560,22 @@ def run_reference(args, rank, world):
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
+
+
+def time_build(favor, kind, m, d, stream, dev, reps=20):
+    """Mean duration of favor_build_orf of the given kind (CUDA events)."""
+    om = torch.empty((m, d), dtype=torch.float32, device=dev)
+    with torch.cuda.stream(stream):
+        favor.build_orf(0, om, orthogonal=kind, stream=stream)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(reps):
+            favor.build_orf(i, om, orthogonal=kind, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / reps
 
 
 def measure_backward(favor, n_steps, sets, omega, s, stream, status, dev, tokens_per_step, hbm):
