@@ -91,11 +91,13 @@ struct SimtPlan {
 };
 
 SimtPlan simt_plan(bool causal, const Shape& s);
-// Backward of the bidirectional pass (simt.cu): workspace = the forward
-// state's plus dN^ [BH][L][d+1], dS~ partials and dS~.
+// Backward (simt.cu): workspace = the forward state's plus dN^ [BH][L][d+1],
+// then for the bidirectional pass dS~ partials and dS~, for the causal pass
+// one [m][d+1] state per (head, chunk of c_chunk tokens) in the same place.
 struct BwdPlan {
   SimtPlan fwd;
-  size_t off_dn, off_dpart, off_dstate, bytes;
+  int c_chunk, c_n;  // causal: tokens per chunk, chunks per head
+  size_t off_dn, off_dpart, off_dstate, off_cstate, bytes;
 };
 BwdPlan bwd_plan(const Shape& s);
 cudaError_t simt_bwd_bidir(const void* Q, const void* K, const void* V, const void* dO, void* dQ, void* dK, void* dV,

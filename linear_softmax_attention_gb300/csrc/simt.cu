@@ -912,9 +912,11 @@ size_t bwd_dstate_smem(int d) {
 }
 
 // ---------------------------------------------------------------------------
-// Causal backward: one CTA per head, tiles of kCT tokens.  With the prefix
-// state G~_c = sum over earlier tiles of phi(k) [v ; 1]^T and, inside a tile,
-// A = tril(phi(Q) phi(K)^T):
+// Causal backward: one CTA per (chunk of tokens, head), walking the chunk in
+// tiles of kCT tokens.  Each walk starts from its chunk's exclusive prefix
+// (query walk) or suffix (key walk) state, summed beforehand from per-chunk
+// partials in chunk order.  With the prefix state G~_c = sum over earlier
+// tiles of phi(k) [v ; 1]^T and, inside a tile, A = tril(phi(Q) phi(K)^T):
 //   N^_t = phi(q_t)^T G~_c + sum_{s<=t} A_ts [v_s ; 1]   (N | D)
 //   dphi(q_t) = G~_c dN^_t + sum_{s<=t} (dN^_t . [v_s ; 1]) phi(k_s)
 // (forward walk), and with the suffix state H_c = sum over later tiles of
@@ -928,10 +930,11 @@ template <typename T, int FM>
 __global__ void __launch_bounds__(kThreads) cbwd_query_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,
     T* __restrict__ dQ, const float* __restrict__ omega, const float* __restrict__ key_ref, float* __restrict__ gst,
-    float* __restrict__ dnw, int L, int d, int m, float scale, int32_t* status) {
+    float* __restrict__ dnw, int L, int d, int m, float scale, int chunk, int n_chunk, int32_t* status) {
   extern __shared__ float smem[];
   const int ld = d + 1, ldp = m + 1;
-  const int bh = blockIdx.x;
+  const int c = blockIdx.x, bh = blockIdx.y;
+  const int l0 = c * chunk, l1 = min(L, l0 + chunk);
   float* xs = smem;                   // [kCT][ld] q
   float* ks = xs + kCT * ld;          // [kCT][ld] k
   float* vs = ks + kCT * ld;          // [kCT][ld] v | 1
@@ -946,14 +949,13 @@ __global__ void __launch_bounds__(kThreads) cbwd_query_kernel(
   float* rq = Bm + kCT * (kCT + 1);   // [kCT]
   float* rk = rq + kCT;               // [kCT]
   float* gsum = rk + kCT;             // [kCT]
-  float* Gh = gst + (size_t)bh * m * ld;
-  for (int e = threadIdx.x; e < m * ld; e += kThreads) Gh[e] = 0.f;
+  float* Gh = gst + ((size_t)bh * n_chunk + c) * m * ld;   // the chunk's exclusive prefix state
   float R, W;
   key_reference(key_ref, m, &R, &W);
   const int n_fb = (m + kFB - 1) / kFB;
   constexpr int kPerN = (kCT * (kMaxD + 1) + kThreads - 1) / kThreads;
-  for (int t0 = 0; t0 < L; t0 += kCT) {
-    const int nt = min(kCT, L - t0);
+  for (int t0 = l0; t0 < l1; t0 += kCT) {
+    const int nt = min(kCT, l1 - t0);
     const size_t row0 = (size_t)bh * L + t0;
     __syncthreads();
     load_tile<kCT>(Q + row0 * d, nt, d, xs);
@@ -1065,10 +1067,11 @@ template <typename T, int FM>
 __global__ void __launch_bounds__(kThreads) cbwd_key_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V, T* __restrict__ dK,
     T* __restrict__ dV, const float* __restrict__ omega, const float* __restrict__ key_ref, float* __restrict__ hst,
-    const float* __restrict__ dnw, int L, int d, int m, float scale) {
+    const float* __restrict__ dnw, int L, int d, int m, float scale, int chunk, int n_chunk) {
   extern __shared__ float smem[];
   const int ld = d + 1, ldp = m + 1;
-  const int bh = blockIdx.x;
+  const int c = blockIdx.x, bh = blockIdx.y;
+  const int l0 = c * chunk, l1 = min(L, l0 + chunk);
   float* xs = smem;                   // [kCT][ld] q
   float* ks = xs + kCT * ld;          // [kCT][ld] k
   float* vs = ks + kCT * ld;          // [kCT][ld] v | 1
@@ -1083,16 +1086,15 @@ __global__ void __launch_bounds__(kThreads) cbwd_key_kernel(
   float* rq = Cm + kCT * (kCT + 1);   // [kCT]
   float* rk = rq + kCT;               // [kCT]
   float* gsum = rk + kCT;             // [kCT]
-  float* Hh = hst + (size_t)bh * m * ld;
-  for (int e = threadIdx.x; e < m * ld; e += kThreads) Hh[e] = 0.f;
+  float* Hh = hst + ((size_t)bh * n_chunk + c) * m * ld;   // the chunk's exclusive suffix state
   float R, W;
   key_reference(key_ref, m, &R, &W);
   const int n_fb = (m + kFB - 1) / kFB;
   constexpr int kPer = (kCT * kMaxD + kThreads - 1) / kThreads;
-  const int n_tiles = (L + kCT - 1) / kCT;
+  const int n_tiles = (l1 - l0 + kCT - 1) / kCT;
   for (int tile = n_tiles - 1; tile >= 0; --tile) {
-    const int t0 = tile * kCT;
-    const int nt = min(kCT, L - t0);
+    const int t0 = l0 + tile * kCT;
+    const int nt = min(kCT, l1 - t0);
     const size_t row0 = (size_t)bh * L + t0;
     __syncthreads();
     load_tile<kCT>(Q + row0 * d, nt, d, xs);
@@ -1170,6 +1172,22 @@ __global__ void __launch_bounds__(kThreads) cbwd_key_kernel(
   }
 }
 
+// Chunk states of one head in place: exclusive prefix (reverse = false) or
+// suffix (reverse = true) sums, in chunk order.
+__global__ void __launch_bounds__(kThreads) chunk_scan_kernel(float* __restrict__ cst, int per, int n_chunk,
+                                                              bool reverse) {
+  const int e = blockIdx.x * kThreads + threadIdx.x, bh = blockIdx.y;
+  if (e >= per) return;
+  float* base = cst + (size_t)bh * n_chunk * per + e;
+  float run = 0.f;
+  for (int i = 0; i < n_chunk; ++i) {
+    const int c = reverse ? n_chunk - 1 - i : i;
+    const float x = base[(size_t)c * per];
+    base[(size_t)c * per] = run;
+    run += x;
+  }
+}
+
 size_t cbwd_smem(int d, int m) {
   const int ld = d + 1, ldp = m + 1;
   return sizeof(float) * ((size_t)5 * kCT * ld + (size_t)kFB * ld + (size_t)3 * kCT * ldp +
@@ -1190,6 +1208,14 @@ BwdPlan bwd_plan(const Shape& s) {
   b.off_dstate = off;
   off = align256(off + BH * s.m * ld * sizeof(float));
   b.bytes = off;
+  // causal chunks: about four waves of two CTAs per SM over the heads
+  const int tiles = (s.L + kCT - 1) / kCT;
+  int want = (8 * sm_count() + s.BH() - 1) / s.BH();
+  want = max(1, min(want, tiles));
+  b.c_chunk = max(1, (tiles + want - 1) / want) * kCT;
+  b.c_n = (s.L + b.c_chunk - 1) / b.c_chunk;
+  b.off_cstate = b.off_dpart;
+  b.bytes = max(b.bytes, align256(b.off_cstate + BH * b.c_n * s.m * ld * sizeof(float)));
   return b;
 }
 
@@ -1201,21 +1227,34 @@ cudaError_t simt_bwd_causal(const void* Q, const void* K, const void* V, const v
   float* key_ref = reinterpret_cast<float*>(w);
   cudaError_t e = launch_prep(omega, s.m, s.d, key_ref, nullptr, nullptr, 0, stream);
   if (e != cudaSuccess) return e;
-  float* state = reinterpret_cast<float*>(w + b.off_dstate);   // G~ (forward walk), then H (reverse walk)
+  // per (head, chunk): chunk sums of phi(k) [v ; 1]^T -> exclusive prefixes
+  // (query walks) -> chunk sums of phi(q) dN^T -> exclusive suffixes (key walks)
+  float* cst = reinterpret_cast<float*>(w + b.off_cstate);
   float* dnw = reinterpret_cast<float*>(w + b.off_dn);
-  const size_t sm = cbwd_smem(s.d, s.m);
+  const size_t sm = cbwd_smem(s.d, s.m), ssm = state_smem(s.d), dsm = bwd_dstate_smem(s.d);
+  const int per = s.m * (s.d + 1);
+  const dim3 walks(b.c_n, s.BH()), sums(b.c_n, b.fwd.n_fb, s.BH()), scan((per + kThreads - 1) / kThreads, s.BH());
   return dispatch(bf16, fm, [&](auto tag, auto f) {
     using T = decltype(tag);
     constexpr int FM = decltype(f)::value;
     cudaError_t r = set_smem(cbwd_query_kernel<T, FM>, sm);
     if (r == cudaSuccess) r = set_smem(cbwd_key_kernel<T, FM>, sm);
+    if (r == cudaSuccess) r = set_smem(state_partial_kernel<T, FM>, ssm);
+    if (r == cudaSuccess) r = set_smem(bwd_dstate_partial_kernel<T, FM>, dsm);
     if (r != cudaSuccess) return r;
-    cbwd_query_kernel<T, FM><<<s.BH(), kThreads, sm, stream>>>(
+    state_partial_kernel<T, FM><<<sums, kThreads, ssm, stream>>>(static_cast<const T*>(K), static_cast<const T*>(V),
+                                                                 omega, key_ref, s.L, s.d, s.m, scale, b.c_chunk,
+                                                                 b.c_n, cst);
+    chunk_scan_kernel<<<scan, kThreads, 0, stream>>>(cst, per, b.c_n, false);
+    cbwd_query_kernel<T, FM><<<walks, kThreads, sm, stream>>>(
         static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V), static_cast<const T*>(dO),
-        static_cast<T*>(dQ), omega, key_ref, state, dnw, s.L, s.d, s.m, scale, st);
-    cbwd_key_kernel<T, FM><<<s.BH(), kThreads, sm, stream>>>(
+        static_cast<T*>(dQ), omega, key_ref, cst, dnw, s.L, s.d, s.m, scale, b.c_chunk, b.c_n, st);
+    bwd_dstate_partial_kernel<T, FM><<<sums, kThreads, dsm, stream>>>(
+        static_cast<const T*>(Q), dnw, omega, key_ref, s.L, s.d, s.m, scale, b.c_chunk, b.c_n, cst);
+    chunk_scan_kernel<<<scan, kThreads, 0, stream>>>(cst, per, b.c_n, true);
+    cbwd_key_kernel<T, FM><<<walks, kThreads, sm, stream>>>(
         static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V), static_cast<T*>(dK),
-        static_cast<T*>(dV), omega, key_ref, state, dnw, s.L, s.d, s.m, scale);
+        static_cast<T*>(dV), omega, key_ref, cst, dnw, s.L, s.d, s.m, scale, b.c_chunk, b.c_n);
     return cudaGetLastError();
   });
 }

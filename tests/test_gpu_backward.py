@@ -64,7 +64,11 @@ def test_backward_is_deterministic(cuda_lib):
 @pytest.mark.parametrize("dtype,B,H,L,d,m", [(torch.float32, 2, 2, 75, 64, 128),
                                              (torch.float32, 1, 2, 33, 32, 100),
                                              (torch.bfloat16, 2, 3, 300, 64, 256),
-                                             (torch.bfloat16, 1, 2, 50, 128, 512)])
+                                             (torch.bfloat16, 1, 2, 50, 128, 512),
+                                             # 304 heads: chunks of several tiles (64 and 80
+                                             # tokens on 152 SMs) with a ragged last chunk
+                                             (torch.float32, 16, 19, 200, 32, 64),
+                                             (torch.bfloat16, 8, 38, 264, 64, 128)])
 def test_causal_backward_matches_oracle(cuda_lib, features, dtype, B, H, L, d, m):
     w = wl.Workload("cbwd", "causal", "f32" if dtype == torch.float32 else "bf16", B, H, L, d, m, "normal")
     Q, K, V = (t.cuda() for t in wl.make_qkv(w, seed=3 * L + m))
