@@ -60,6 +60,40 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+class Ranks:
+    """Host-side coordination of the replicas: a barrier around each timed
+    region and the maximum of a per-rank time.  The path shards by (batch,
+    head) with no exchange, so nothing else crosses ranks."""
+
+    def __init__(self, world: int, device):
+        self.world = world
+        self.device = device
+
+    def barrier(self):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(self, x: float) -> float:
+        if self.world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([x], dtype=torch.float64, device=self.device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+        return x
+
+
+def rank_input_seed(rank: int, i: int) -> int:
+    """Seed of input set i on a rank: every rank processes its own units."""
+    return 1000 * rank + i
+
+
+def whole_job_value(world: int, tokens_per_step: int, steps: int, elapsed_ms_max: float) -> float:
+    """Tokens per second of the whole job: every rank's tokens over the
+    slowest rank's time (weak scaling: the per-rank workload is fixed)."""
+    return world * tokens_per_step * steps / (elapsed_ms_max / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -211,7 +245,7 @@ def run_gpu(args, rank, world, local_rank):
     n_sets = min(n_sets, 8)
     sets = []
     for i in range(n_sets):
-        q, k, v = wl.make_qkv(w, seed=1000 * rank + i, device=dev)
+        q, k, v = wl.make_qkv(w, seed=rank_input_seed(rank, i), device=dev)
         sets.append((q, k, v))
     O_b = torch.empty_like(sets[0][0])
     O_c = torch.empty_like(sets[0][0])
@@ -290,18 +324,8 @@ def run_gpu(args, rank, world, local_rank):
                 gs.replay()
     torch.cuda.synchronize(dev)
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
-    def max_over_ranks(x):
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([x], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
-        return x
+    ranks = Ranks(world, dev)
+    barrier, max_over_ranks = ranks.barrier, ranks.max_over_ranks
 
     # timed region 1: K replays of the whole-step graph (the headline value)
     barrier()
@@ -344,7 +368,7 @@ def run_gpu(args, rank, world, local_rank):
 
     ms_per_step = elapsed_ms / args.steps
     tokens_per_step = B * L
-    value = world * tokens_per_step * args.steps / (elapsed_ms / 1e3)
+    value = whole_job_value(world, tokens_per_step, args.steps, elapsed_ms)
 
     # e2e through the public calls (favor_build_orf, favor_fwd_bidir,
     # favor_fwd_causal) with pinned host buffers: every step copies its Q, K,
