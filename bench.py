@@ -192,17 +192,26 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 # The sources the tensor-core kernels (the profiled stages) are built from:
-# a committed profile's counters stay valid while none of these changes.
+# a committed profile's counters stay valid while their code (comments and
+# layout aside) does not change.
 KERNEL_SOURCES = ("linear_softmax_attention_gb300/csrc/tc.cu", "linear_softmax_attention_gb300/csrc/tc_ptx.cuh",
                   "linear_softmax_attention_gb300/csrc/common.cuh", "linear_softmax_attention_gb300/csrc/prep.cu",
                   "include/favor.h")
+_C_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
+def source_code_text(text: str) -> str:
+    """C/C++ source without comments, whitespace runs collapsed (no comment
+    marker sits inside a string literal in these files)."""
+    return " ".join(_C_COMMENT.sub(" ", text).split())
 
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as fh:
+            h.update(source_code_text(fh.read()).encode())
+            h.update(b"\0")
     return h.hexdigest()[:16]
 
 
@@ -494,7 +503,8 @@ def run_gpu(args, rank, world, local_rank):
         "modes": {"bidir_tokens_per_s": tokens_per_step / (bidir_ms / 1e3),
                   "causal_tokens_per_s": tokens_per_step / (causal_ms / 1e3),
                   "build_orf_ms": stage_ms["build_orf"],
-                  "build_orf_hadamard_ms": time_build(favor, "hadamard", m, d, stream, dev)},
+                  "build_orf_hadamard_ms": time_build(favor, "hadamard", m, d, stream, dev),
+                  "build_orf_givens_ms": time_build(favor, "givens", m, d, stream, dev)},
         "stages": stages_out,
         "roofline": roof,
         "gpu_launches": launches_per_step * args.steps,

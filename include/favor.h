@@ -106,7 +106,15 @@ const char* favor_status_string(favor_status s);
  * exactly orthogonal blocks with rows of length sqrt(d), O(m) random numbers
  * (arXiv summary §A.2: Hadamard ORFs, a small bias that tends to zero as d
  * grows; §B.3: their O(m) space; no construction is printed, this is the
- * plain reading).
+ * plain reading).  orthogonal = 3 (Givens ORF, d >= 2): block b = sqrt(d)
+ * G_K ... G_2 G_1 with K = 3 d ceil(log2 d) plane rotations, (G x)_i =
+ * cos(theta) x_i - sin(theta) x_j, (G x)_j = sin(theta) x_i + cos(theta) x_j;
+ * rotation r of block b reads SplitMix64 words 2c and 2c + 1, c = b K + r:
+ * i = floor(hi32 d / 2^32), j' = floor(lo32 (d - 1) / 2^32), j = j' +
+ * [j' >= i] from the first, theta = 2 pi (bits[41..63] + 1/2) / 2^23 from
+ * the second; exactly orthogonal blocks (determinant +1) with rows of length
+ * sqrt(d), O(m log d) random numbers (arXiv summary §A.2 and §B.3: Givens
+ * ORFs, a small bias, O(m log d) space; again the plain reading).
  *
  * Random numbers: SplitMix64 word i = mix(seed + (i+1)*0x9E3779B97F4A7C15);
  * one normal per word by Box–Muller, z = sqrt(-2 ln u1) cos(2 pi u2) with
@@ -116,8 +124,9 @@ const char* favor_status_string(favor_status s);
  * (i*d + c)*2.  Arithmetic is fp32 (two Gram–Schmidt sweeps).
  *
  * Errors: FAVOR_ERR_INVALID_ARG if omega is NULL, m, d out of range
- * (1 <= d <= 128, 1 <= m <= 512) or orthogonal not 0, 1 or 2;
- * FAVOR_ERR_UNSUPPORTED for orthogonal = 2 with d not a power of two.
+ * (1 <= d <= 128, 1 <= m <= 512) or orthogonal not 0, 1, 2 or 3;
+ * FAVOR_ERR_UNSUPPORTED for orthogonal = 2 with d not a power of two and for
+ * orthogonal = 3 with d = 1.
  */
 favor_status favor_build_orf(uint64_t seed, int m, int d, int orthogonal,
                              float* omega, void* stream);

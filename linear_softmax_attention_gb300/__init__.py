@@ -120,12 +120,14 @@ def path_name(causal: bool, d: int, m: int, dtype) -> str:
 
 def build_orf(seed: int, omega: torch.Tensor, orthogonal=True, stream=None) -> torch.Tensor:
     """Fill ``omega`` (fp32 [m, d] on the GPU) with the projection for ``seed``:
-    orthogonal=True (Gaussian ORF), False (iid) or "hadamard" (Hadamard ORF,
-    d a power of two)."""
+    orthogonal=True (Gaussian ORF), False (iid), "hadamard" (Hadamard ORF,
+    d a power of two) or "givens" (Givens ORF, d >= 2)."""
     if omega.dtype != torch.float32 or not omega.is_cuda or not omega.is_contiguous() or omega.dim() != 2:
         raise FavorError("omega must be a contiguous fp32 CUDA tensor [m, d]")
     m, d = omega.shape
-    kind = 2 if orthogonal == "hadamard" else int(bool(orthogonal))
+    kind = {"hadamard": 2, "givens": 3}.get(orthogonal, None) if isinstance(orthogonal, str) else int(bool(orthogonal))
+    if kind is None:
+        raise FavorError(f"unknown projection kind {orthogonal!r}")
     _check(load().favor_build_orf(ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), m, d, kind,
                                   omega.data_ptr(), _stream_handle(stream)), "favor_build_orf")
     return omega

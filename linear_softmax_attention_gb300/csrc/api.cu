@@ -175,8 +175,9 @@ const char* favor_path_name(int causal, int d, int m, favor_dtype dt) {
 
 favor_status favor_build_orf(uint64_t seed, int m, int d, int orthogonal, float* omega, void* stream) {
   if (omega == nullptr || m < 1 || d < 1 || m > favor::kMaxM || d > favor::kMaxD) return FAVOR_ERR_INVALID_ARG;
-  if (orthogonal < 0 || orthogonal > 2) return FAVOR_ERR_INVALID_ARG;
+  if (orthogonal < 0 || orthogonal > 3) return FAVOR_ERR_INVALID_ARG;
   if (orthogonal == 2 && (d & (d - 1)) != 0) return FAVOR_ERR_UNSUPPORTED;   // Hadamard: d a power of two
+  if (orthogonal == 3 && d < 2) return FAVOR_ERR_UNSUPPORTED;                // Givens: a plane needs d >= 2
   cudaError_t e = favor::launch_build_orf(seed, m, d, orthogonal, omega, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
 }

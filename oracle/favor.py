@@ -47,6 +47,9 @@ __all__ = [
     "walsh_hadamard",
     "rademacher_signs",
     "build_omega_hadamard",
+    "givens_rotation_count",
+    "givens_rotations",
+    "build_omega_givens",
     "prf_features",
     "relu_features",
     "FEATURES",
@@ -215,6 +218,65 @@ def build_omega_hadamard(seed: int, m: int, d: int) -> np.ndarray:
         for p in range(3):
             D = rademacher_signs(seed, (b * 3 + p) * d + np.arange(d))
             M = M @ (H * D[None, :])          # (H D_p): column i of H times sign i
+        blocks.append(math.sqrt(d) * M)
+    return np.concatenate(blocks, axis=0)[:m]
+
+
+def givens_rotation_count(d: int) -> int:
+    """Rotations per d x d Givens block: 3 d ceil(log2 d).  Over ceil(m/d)
+    blocks that is the O(m log d) numbers the pages give for Givens ORFs; the
+    factor 3 is the smallest for which the rows' fourth moment reaches that
+    of rows uniform on the sphere of radius sqrt(d) (at d = 64: 5.4 with
+    factor 1, 3.03 with 2, 2.91 with 3, against 3d / (d + 2) = 2.91)."""
+    if d < 2:
+        raise ValueError("a Givens rotation needs d >= 2")
+    return 3 * d * (d - 1).bit_length()
+
+
+def givens_rotations(seed: int, block: int, d: int):
+    """(i, j, theta) of each rotation of ``block``, in the order applied.
+
+    Rotation r of block b reads SplitMix64 words 2c and 2c + 1, c = b*K + r
+    (K rotations per block).  From the first word w0: i = floor(hi32(w0) d /
+    2^32) and j' = floor(lo32(w0) (d - 1) / 2^32), j = j' + [j' >= i] (a
+    uniform ordered pair, i != j).  From the second word w1: theta =
+    2 pi (k + 1/2) / 2^23 with k its top 23 bits (uniform on (0, 2 pi)).
+    """
+    K = givens_rotation_count(d)
+    c = (np.uint64(block) * np.uint64(K) + np.arange(K, dtype=np.uint64)) * np.uint64(2)
+    w0 = splitmix64_stream(seed, c)
+    w1 = splitmix64_stream(seed, c + np.uint64(1))
+    hi = (w0 >> np.uint64(32)).astype(np.float64)
+    lo = (w0 & np.uint64(0xFFFFFFFF)).astype(np.float64)
+    i = np.floor(hi * d / 4294967296.0).astype(np.int64)
+    jp = np.floor(lo * (d - 1) / 4294967296.0).astype(np.int64)
+    j = jp + (jp >= i)
+    k = (w1 >> np.uint64(41)).astype(np.float64)
+    theta = 2.0 * math.pi * (k + 0.5) / 8388608.0
+    return list(zip(i.tolist(), j.tolist(), theta.tolist()))
+
+
+def build_omega_givens(seed: int, m: int, d: int) -> np.ndarray:
+    """Givens ORF projection, [m, d].
+
+    [summary] §A.2 (FAVOR+ bullet) and §B.3 name Givens ORFs (small bias
+    tending to zero with d; O(m log d) space) without a construction; the
+    reading: block b = sqrt(d) G_K ... G_2 G_1 with G_r the rotation by
+    theta_r in the plane of coordinates (i_r, j_r) -- (G x)_i = cos x_i -
+    sin x_j, (G x)_j = sin x_i + cos x_j -- drawn by ``givens_rotations``.
+    Each block is exactly orthogonal with rows of length sqrt(d) (as the
+    Hadamard reading; hence the bias).  The first m stacked rows are kept.
+    """
+    blocks = []
+    for b in range(-(-m // d)):
+        M = np.eye(d)
+        for i, j, th in givens_rotations(seed, b, d):
+            G = np.eye(d)
+            G[i, i] = math.cos(th)
+            G[i, j] = -math.sin(th)
+            G[j, i] = math.sin(th)
+            G[j, j] = math.cos(th)
+            M = G @ M
         blocks.append(math.sqrt(d) * M)
     return np.concatenate(blocks, axis=0)[:m]
 

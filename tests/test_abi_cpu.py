@@ -89,7 +89,9 @@ def test_build_orf_rejects_bad_arguments(lib):
     assert lib.favor_build_orf(ctypes.c_uint64(0), 8, 8, 1, None, None) == 1
     assert lib.favor_build_orf(ctypes.c_uint64(0), 0, 8, 1, 16, None) == 1
     assert lib.favor_build_orf(ctypes.c_uint64(0), 8, 200, 1, 16, None) == 1
-    assert lib.favor_build_orf(ctypes.c_uint64(0), 8, 8, 3, 16, None) == 1      # unknown kind
+    assert lib.favor_build_orf(ctypes.c_uint64(0), 8, 8, 4, 16, None) == 1      # unknown kind
+    assert lib.favor_build_orf(ctypes.c_uint64(0), 8, 8, -1, 16, None) == 1     # unknown kind
+    assert lib.favor_build_orf(ctypes.c_uint64(0), 8, 1, 3, 16, None) == 2      # Givens needs d >= 2
     assert lib.favor_build_orf(ctypes.c_uint64(0), 8, 12, 2, 16, None) == 2     # Hadamard needs a power of two
 
 

@@ -75,6 +75,29 @@ def test_hadamard_omega_in_attention(cuda_lib):
     assert orc.rowwise_rel_err(to_np(O), ref) < TOL[torch.bfloat16]
 
 
+@pytest.mark.parametrize("seed,m,d", [(0, 64, 64), (7, 256, 64), (3, 100, 32), (9, 200, 48), (2, 256, 128),
+                                     (5, 6, 2), (1, 50, 3)])
+def test_givens_omega_matches_oracle(cuda_lib, seed, m, d):
+    om = torch.empty((m, d), dtype=torch.float32, device="cuda")
+    cuda_lib.build_orf(seed, om, orthogonal="givens")
+    got, want = to_np(om), orc.build_omega_givens(seed, m, d)
+    # fp32 rotations, 3 d ceil(log2 d) of them: rounding grows like their square root
+    assert np.max(np.abs(got - want)) < 1e-4 * np.max(np.abs(want))
+    for b in range(0, m, d):
+        blk = got[b:b + d]
+        assert np.max(np.abs(blk @ blk.T - d * np.eye(blk.shape[0]))) < 1e-4 * d
+
+
+def test_givens_omega_in_attention(cuda_lib):
+    w = wl.Workload("giv", "causal", "bf16", 1, 2, 500, 64, 256, "normal")
+    Q, K, V = (t.cuda() for t in wl.make_qkv(w, seed=8))
+    om = torch.empty((w.m, w.d), dtype=torch.float32, device="cuda")
+    cuda_lib.build_orf(8, om, orthogonal="givens")
+    O = _run(cuda_lib, True, Q, K, V, om, w.qk_scale)
+    ref = orc.favor_causal(to_np(Q), to_np(K), to_np(V), to_np(om), w.qk_scale)
+    assert orc.rowwise_rel_err(to_np(O), ref) < TOL[torch.bfloat16]
+
+
 def test_iid_omega_matches_oracle(cuda_lib):
     om = to_np(cuda_lib.new_omega(4, 300, 70, orthogonal=False))
     want = orc.build_omega(4, 300, 70, orthogonal=False)
