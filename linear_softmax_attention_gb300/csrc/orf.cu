@@ -217,32 +217,47 @@ __global__ void __launch_bounds__(256) hadamard_block_kernel(uint64_t seed, int 
 // Rotation r reads SplitMix64 words 2c and 2c + 1, c = b K + r: i =
 // floor(hi32 d / 2^32), j' = floor(lo32 (d - 1) / 2^32), j = j' + [j' >= i]
 // from the first; theta = 2 pi (k + 1/2) / 2^23, k its top 23 bits, from the
-// second.  G_r M changes rows i and j of M within each column, so thread t
-// carries column t of the block through all K rotations on its own (every
-// thread draws the same rotation), with no barrier until the rows are
-// written.  X [d][d] in shared memory, column t touched only by thread t.
+// second.  The CTA first draws all K rotations in parallel into shared
+// memory; G_r M then changes rows i and j of M within each column, so thread
+// t carries column t of the block through the K rotations on its own (every
+// thread reads the same rotation: a broadcast), with no barrier until the
+// rows are written.  Shared memory: rot [K] (i, j, cos, sin), X [d][d]
+// (column t touched only by thread t).
+struct GivensRot {
+  int i, j;
+  float c, s;
+};
+
 __global__ void __launch_bounds__(128) givens_block_kernel(uint64_t seed, int m, int d, int n_rot,
                                                            float* __restrict__ omega) {
-  extern __shared__ float X[];
+  extern __shared__ float4 givens_smem[];
+  GivensRot* rot = reinterpret_cast<GivensRot*>(givens_smem);
+  float* X = reinterpret_cast<float*>(givens_smem + n_rot);
   const int b = blockIdx.x, t = threadIdx.x;
-  if (t < d)
-    for (int r = 0; r < d; ++r) X[r * d + t] = (r == t) ? 1.f : 0.f;
   const uint64_t c0 = static_cast<uint64_t>(b) * static_cast<uint64_t>(n_rot);
-  for (int r = 0; r < n_rot; ++r) {
+  for (int r = t; r < n_rot; r += blockDim.x) {
     const uint64_t c = (c0 + static_cast<uint64_t>(r)) * 2ull;
     const uint64_t w0 = splitmix_word(seed, c);
     const uint64_t w1 = splitmix_word(seed, c + 1ull);
     const int i = static_cast<int>(((w0 >> 32) * static_cast<uint64_t>(d)) >> 32);
     const int jp = static_cast<int>(((w0 & 0xFFFFFFFFull) * static_cast<uint64_t>(d - 1)) >> 32);
-    const int j = jp + (jp >= i ? 1 : 0);
     // 2 u = (k + 1/2) / 2^22, exact in fp32
     const float two_u = (static_cast<float>(static_cast<uint32_t>(w1 >> 41)) + 0.5f) * (1.0f / 4194304.0f);
-    float sn, cs;
-    sincospif(two_u, &sn, &cs);
-    if (t < d) {
-      const float a = X[i * d + t], e = X[j * d + t];
-      X[i * d + t] = cs * a - sn * e;
-      X[j * d + t] = sn * a + cs * e;
+    GivensRot g;
+    g.i = i;
+    g.j = jp + (jp >= i ? 1 : 0);
+    sincospif(two_u, &g.s, &g.c);
+    rot[r] = g;
+  }
+  if (t < d)
+    for (int r = 0; r < d; ++r) X[r * d + t] = (r == t) ? 1.f : 0.f;
+  __syncthreads();
+  if (t < d) {
+    for (int r = 0; r < n_rot; ++r) {
+      const GivensRot g = rot[r];
+      const float a = X[g.i * d + t], e = X[g.j * d + t];
+      X[g.i * d + t] = g.c * a - g.s * e;
+      X[g.j * d + t] = g.s * a + g.c * e;
     }
   }
   __syncthreads();
@@ -265,7 +280,7 @@ cudaError_t launch_build_orf(uint64_t seed, int m, int d, int orthogonal, float*
   if (orthogonal == 3) {
     const int ceil_log2 = 32 - __builtin_clz(static_cast<unsigned>(d - 1));   // d >= 2
     const int n_rot = 3 * d * ceil_log2;
-    const size_t smem = (size_t)d * d * sizeof(float);
+    const size_t smem = (size_t)n_rot * sizeof(float4) + (size_t)d * d * sizeof(float);   // 107 KB at d = 128
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(givens_block_kernel), smem);
     if (e != cudaSuccess) return e;
     const int threads = ((d + 31) / 32) * 32;

@@ -60,6 +60,103 @@ __device__ __forceinline__ float dot_row(const float* x, const float* w, int d) 
   return acc;
 }
 
+// Register tiles of a TT x 64 block (TT = 32 or 16 rows; 64 = kFB columns)
+// over 256 threads: thread (tg, fl) owns rows tg and tg + TT/2 and columns
+// fl + k kLanes, kLanes = 16 (TT = 32) or 32 (TT = 16).  Per step of a
+// reduction a warp reads two row values (broadcasts) and 64 / kLanes column
+// values (kLanes distinct rows or columns, conflict-free for odd strides) for
+// 2 x 64 / kLanes multiply-adds per thread, instead of two shared-memory
+// loads per multiply-add.  Every output is still one sequential fmaf chain
+// in the reduction order of the plain loop.
+template <int TT>
+struct RegTile {
+  static_assert(TT == 32 || TT == 16, "tile rows");
+  static constexpr int kLanes = TT == 32 ? 16 : 32;
+  static constexpr int kCols = kFB / kLanes;
+  static constexpr int kHalf = TT / 2;
+  // column groups covering n <= kMaxD + 1 columns (outer products)
+  static constexpr int kWide = (kMaxD + 1 + kLanes - 1) / kLanes;
+  __device__ static int tg() { return threadIdx.x / kLanes; }
+  __device__ static int fl() { return threadIdx.x % kLanes; }
+  __device__ static int row(int i) { return tg() + i * kHalf; }
+  __device__ static int col(int k) { return fl() + k * kLanes; }
+};
+
+// acc[i][k] = sum_{c < n} A[row_i][c] B[col_k][c] (rows of A and B length n,
+// strides lda, ldb); B has kFB rows.
+template <int TT>
+__device__ __forceinline__ void rowdot_block(const float* A, int lda, const float* B, int ldb, int n,
+                                             float (&acc)[2][RegTile<TT>::kCols]) {
+  using RT = RegTile<TT>;
+  const float* a0 = A + RT::tg() * lda;
+  const float* a1 = a0 + RT::kHalf * lda;
+  const float* b = B + RT::fl() * ldb;
+#pragma unroll
+  for (int k = 0; k < RT::kCols; ++k) acc[0][k] = acc[1][k] = 0.f;
+#pragma unroll 4
+  for (int c = 0; c < n; ++c) {
+    const float x0 = a0[c], x1 = a1[c];
+#pragma unroll
+    for (int k = 0; k < RT::kCols; ++k) {
+      const float w = b[k * RT::kLanes * ldb + c];
+      acc[0][k] = fmaf(x0, w, acc[0][k]);
+      acc[1][k] = fmaf(x1, w, acc[1][k]);
+    }
+  }
+}
+
+// acc[i][k] += sum_{f < nf} P[row_i][f] S[f][col_k] for columns col_k < J
+// (P row stride ldp, S row stride lds); KC column groups cover J.
+template <int TT, int KC>
+__device__ __forceinline__ void outer_acc(const float* P, int ldp, const float* S, int lds, int nf, int J,
+                                          float (&acc)[2][KC]) {
+  using RT = RegTile<TT>;
+  const float* p0 = P + RT::tg() * ldp;
+  const float* p1 = p0 + RT::kHalf * ldp;
+  const float* sc = S + RT::fl();
+  const int kn = (J - RT::fl() + RT::kLanes - 1) / RT::kLanes;   // this thread's columns below J
+  for (int f = 0; f < nf; ++f) {
+    const float x0 = p0[f], x1 = p1[f];
+    const float* sr = sc + f * lds;
+#pragma unroll
+    for (int k = 0; k < KC; ++k) {
+      if (k < kn) {
+        const float w = sr[k * RT::kLanes];
+        acc[0][k] = fmaf(x0, w, acc[0][k]);
+        acc[1][k] = fmaf(x1, w, acc[1][k]);
+      }
+    }
+  }
+}
+
+// Sums over the tokens of a tile for a block of 64 features: acc[i][k] +=
+// sum_{t < nt} X[t][fg + 16 i] Y[t][jl + 16 k] for columns jl + 16 k < J,
+// thread (fg, jl) = (tid / 16, tid % 16).  Per token a warp reads 4 feature
+// values (two addresses each) and KC column values (16 consecutive) for
+// 4 KC multiply-adds per thread; each output is one fmaf chain in token order.
+constexpr int kGramWide = (kMaxD + 1 + 15) / 16;
+template <int KC>
+__device__ __forceinline__ void gram_acc(const float* X, int ldx, const float* Y, int ldy, int nt, int J,
+                                         float (&acc)[4][KC]) {
+  const int fg = threadIdx.x / 16, jl = threadIdx.x % 16;
+  const int kn = (J - jl + 15) / 16;   // this thread's columns below J
+  for (int t = 0; t < nt; ++t) {
+    const float* xr = X + t * ldx + fg;
+    const float* yr = Y + t * ldy + jl;
+    float x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = xr[16 * i];
+#pragma unroll
+    for (int k = 0; k < KC; ++k) {
+      if (k < kn) {
+        const float y = yr[16 * k];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i][k] = fmaf(x[i], y, acc[i][k]);
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // State partials: for (split, feature block, head) the CTA sums
 //   S_p[f, :] = sum_t exp(l_tf - R) [v_t ; 1],  l_tf = s w_f.k_t - s^2 |k_t|^2 / 2
@@ -75,7 +172,7 @@ __device__ __forceinline__ float key_feature(float a, float half_sq, float R) {
 }
 
 template <typename T, int FM>
-__global__ void __launch_bounds__(kThreads) state_partial_kernel(
+__global__ void __launch_bounds__(kThreads, 3) state_partial_kernel(
     const T* __restrict__ K, const T* __restrict__ V, const float* __restrict__ omega,
     const float* __restrict__ key_ref, int L, int d, int m, float scale, int chunk, int n_split,
     float* __restrict__ partS) {
@@ -95,16 +192,17 @@ __global__ void __launch_bounds__(kThreads) state_partial_kernel(
   const float hs2 = 0.5f * scale * scale;
   float R, W_unused;
   key_reference(key_ref, m, &R, &W_unused);
-  const int f_own = threadIdx.x % kFB;
-  const int t_base = threadIdx.x / kFB;   // 0..3
-
   load_omega_block(omega, f0, nf, d, om);
+  // the normaliser column: [v ; 1] (load_rows fills columns < d only)
+  if (threadIdx.x < kTT) vs[threadIdx.x * ld + d] = 1.f;
 
-  // thread owns feature f = tid/4 and columns tid%4 + 4k
-  const int fa = threadIdx.x / 4, jb = threadIdx.x % 4;
-  float acc[33];
+  // thread owns features fg + 16 i (i < 4) and columns jl + 16 k
+  using RT = RegTile<kTT>;
+  float acc[4][kGramWide];
 #pragma unroll
-  for (int k = 0; k < 33; ++k) acc[k] = 0.f;
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int k = 0; k < kGramWide; ++k) acc[i][k] = 0.f;
   for (int t0 = l0; t0 < l1; t0 += kTT) {
     const int nt = min(kTT, l1 - t0);
     __syncthreads();
@@ -113,34 +211,33 @@ __global__ void __launch_bounds__(kThreads) state_partial_kernel(
     __syncthreads();
     row_norms(ks, d, kn);
     __syncthreads();
+    {
+      float a[2][RT::kCols];
+      rowdot_block<kTT>(ks, ld, om, ld, d, a);
 #pragma unroll
-    for (int j = 0; j < kTT / 4; ++j) {
-      const int t = t_base + 4 * j;
-      float p = 0.f;
-      if (t < nt && f_own < nf) {
-        p = key_feature<FM>(scale * dot_row(ks + t * ld, om + f_own * ld, d), hs2 * kn[t], R);
+      for (int i = 0; i < 2; ++i) {
+        const int t = RT::row(i);
+#pragma unroll
+        for (int k = 0; k < RT::kCols; ++k) {
+          const int f = RT::col(k);
+          ph[t * (kFB + 1) + f] = (t < nt && f < nf) ? key_feature<FM>(scale * a[i][k], hs2 * kn[t], R) : 0.f;
+        }
       }
-      ph[t * (kFB + 1) + f_own] = p;
     }
     __syncthreads();
-    for (int t = 0; t < nt; ++t) {
-      const float p = ph[t * (kFB + 1) + fa];
-      const float* vr = vs + t * ld;
-#pragma unroll
-      for (int k = 0; k < 33; ++k) {
-        const int j = jb + 4 * k;
-        if (j < d) acc[k] = fmaf(p, vr[j], acc[k]);
-        else if (j == d) acc[k] += p;
-      }
-    }
+    gram_acc<kGramWide>(ph, kFB + 1, vs, ld, nt, ld, acc);
   }
-  if (fa < nf) {
-    float* dst = partS + (((size_t)bh * n_split + split) * m + f0 + fa) * ld;
+  const int fg = threadIdx.x / 16, jl = threadIdx.x % 16;
+  float* dst = partS + (((size_t)bh * n_split + split) * m + f0) * ld;
 #pragma unroll
-    for (int k = 0; k < 33; ++k) {
-      const int j = jb + 4 * k;
-      if (j <= d) dst[j] = acc[k];
-    }
+  for (int i = 0; i < 4; ++i) {
+    const int f = fg + 16 * i;
+    if (f < nf)
+#pragma unroll
+      for (int k = 0; k < kGramWide; ++k) {
+        const int j = jl + 16 * k;
+        if (j < ld) dst[(size_t)f * ld + j] = acc[i][k];
+      }
   }
 }
 
@@ -611,15 +708,22 @@ __device__ void tile_features(const float* xs, const float* rowc, int nt, int d,
                               const float* __restrict__ omega, float* om, float* P, int ldp) {
   const int ld = d + 1;
   const int n_fb = (m + kFB - 1) / kFB;
+  using RT = RegTile<TT>;
   for (int fb = 0; fb < n_fb; ++fb) {
     const int f0 = fb * kFB, nf = min(kFB, m - f0);
     __syncthreads();
     load_omega_block(omega, f0, nf, d, om);
     __syncthreads();
-    for (int e = threadIdx.x; e < TT * kFB; e += kThreads) {
-      const int t = e / kFB, f = e - t * kFB;
-      if (f < nf)
-        P[t * ldp + f0 + f] = t < nt ? bwd_feature<FM>(scale * dot_row(xs + t * ld, om + f * ld, d), rowc[t]) : 0.f;
+    float acc[2][RT::kCols];
+    rowdot_block<TT>(xs, ld, om, ld, d, acc);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int t = RT::row(i);
+#pragma unroll
+      for (int k = 0; k < RT::kCols; ++k) {
+        const int f = RT::col(k);
+        if (f < nf) P[t * ldp + f0 + f] = t < nt ? bwd_feature<FM>(scale * acc[i][k], rowc[t]) : 0.f;
+      }
     }
   }
   __syncthreads();
@@ -648,36 +752,30 @@ __device__ void tile_g(const float* P, float* G, int ldp, int m, float* gsum) {
 template <int TT, typename T, int FM>
 __device__ void tile_input_grad(const float* xs, const float* G, int ldp, const float* gsum, int nt, int d, int m,
                                 float scale, const float* __restrict__ omega, float* om, T* __restrict__ out) {
+  using RT = RegTile<TT>;
   const int ld = d + 1;
-  constexpr int kPer = (TT * kMaxD + kThreads - 1) / kThreads;
-  float acc[kPer];
+  float acc[2][RT::kWide];
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
+  for (int k = 0; k < RT::kWide; ++k) acc[0][k] = acc[1][k] = 0.f;
   const int n_fb = (m + kFB - 1) / kFB;
   for (int fb = 0; fb < n_fb; ++fb) {
     const int f0 = fb * kFB, nf = min(kFB, m - f0);
     __syncthreads();
     load_omega_block(omega, f0, nf, d, om);
     __syncthreads();
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int e = threadIdx.x + k * kThreads;
-      if (e < TT * d) {
-        const int t = e / d, c = e - t * d;
-        float a = acc[k];
-        for (int f = 0; f < nf; ++f) a = fmaf(G[t * ldp + f0 + f], om[f * ld + c], a);
-        acc[k] = a;
-      }
-    }
+    outer_acc<TT, RT::kWide>(G + f0, ldp, om, ld, nf, d, acc);
   }
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int e = threadIdx.x + k * kThreads;
-    if (e < nt * d) {
-      const int t = e / d, c = e - t * d;
-      float gx = acc[k];
-      if constexpr (FM == FAVOR_FM_PRF) gx -= scale * xs[t * ld + c] * gsum[t];
-      out[(size_t)t * d + c] = from_f32<T>(scale * gx);
+  for (int i = 0; i < 2; ++i) {
+    const int t = RT::row(i);
+#pragma unroll
+    for (int k = 0; k < RT::kWide; ++k) {
+      const int c = RT::col(k);
+      if (t < nt && c < d) {
+        float gx = acc[i][k];
+        if constexpr (FM == FAVOR_FM_PRF) gx -= scale * xs[t * ld + c] * gsum[t];
+        out[(size_t)t * d + c] = from_f32<T>(scale * gx);
+      }
     }
   }
 }
@@ -686,7 +784,7 @@ __device__ void tile_input_grad(const float* xs, const float* G, int ldp, const 
 // dN^ (also written to the workspace for the feature-block pass), dphi(Q)
 // = S~ dN^ and dQ.
 template <typename T, int FM>
-__global__ void __launch_bounds__(kThreads) bwd_query_kernel(
+__global__ void __launch_bounds__(kThreads, 2) bwd_query_kernel(
     const T* __restrict__ Q, const T* __restrict__ dO, T* __restrict__ dQ, const float* __restrict__ omega,
     const float* __restrict__ key_ref, const float* __restrict__ state, float* __restrict__ dnw, int L, int d, int m,
     float scale, int32_t* status) {
@@ -714,33 +812,24 @@ __global__ void __launch_bounds__(kThreads) bwd_query_kernel(
   tile_features<kBT, FM>(xs, rs, nt, d, m, scale, omega, om, P, ldp);
 
   // N | D
+  using RT = RegTile<kBT>;
   const float* Sh = state + (size_t)bh * m * ld;
-  constexpr int kPerN = (kBT * (kMaxD + 1) + kThreads - 1) / kThreads;
-  float acc[kPerN];
+  float acc[2][RT::kWide];
 #pragma unroll
-  for (int k = 0; k < kPerN; ++k) acc[k] = 0.f;
+  for (int k = 0; k < RT::kWide; ++k) acc[0][k] = acc[1][k] = 0.f;
   const int n_fb = (m + kFB - 1) / kFB;
   for (int fb = 0; fb < n_fb; ++fb) {
     const int f0 = fb * kFB, nf = min(kFB, m - f0);
     __syncthreads();
     load_state_block(Sh, f0, nf, d, om);
     __syncthreads();
-#pragma unroll
-    for (int k = 0; k < kPerN; ++k) {
-      const int e = threadIdx.x + k * kThreads;
-      if (e < kBT * ld) {
-        const int t = e / ld, j = e - t * ld;
-        float a = acc[k];
-        for (int f = 0; f < nf; ++f) a = fmaf(P[t * ldp + f0 + f], om[f * ld + j], a);
-        acc[k] = a;
-      }
-    }
+    outer_acc<kBT, RT::kWide>(P + f0, ldp, om, ld, nf, ld, acc);
   }
 #pragma unroll
-  for (int k = 0; k < kPerN; ++k) {
-    const int e = threadIdx.x + k * kThreads;
-    if (e < kBT * ld) nd[e] = acc[k];
-  }
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int k = 0; k < RT::kWide; ++k)
+      if (RT::col(k) < ld) nd[RT::row(i) * ld + RT::col(k)] = acc[i][k];
   __syncthreads();
   // dN^ = [dO / D | -(dO . N) / D^2], one warp per row
   {
@@ -766,10 +855,13 @@ __global__ void __launch_bounds__(kThreads) bwd_query_kernel(
     __syncthreads();
     load_state_block(Sh, f0, nf, d, om);
     __syncthreads();
-    for (int e = threadIdx.x; e < kBT * kFB; e += kThreads) {
-      const int t = e / kFB, f = e - t * kFB;
-      if (f < nf) G[t * ldp + f0 + f] = dot_row(om + f * ld, go + t * ld, ld);
-    }
+    float g[2][RT::kCols];
+    rowdot_block<kBT>(go, ld, om, ld, ld, g);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int k = 0; k < RT::kCols; ++k)
+        if (RT::col(k) < nf) G[RT::row(i) * ldp + f0 + RT::col(k)] = g[i][k];
   }
   __syncthreads();
   tile_g<kBT, FM>(P, G, ldp, m, gsum);
@@ -796,10 +888,12 @@ __global__ void __launch_bounds__(kThreads) bwd_dstate_partial_kernel(
   float R, W;
   key_reference(key_ref, m, &R, &W);
   load_omega_block(omega, f0, nf, d, om);
-  const int fa = threadIdx.x / 4, jb = threadIdx.x % 4;
-  float acc[33];
+  using RT = RegTile<kBT>;
+  float acc[4][kGramWide];
 #pragma unroll
-  for (int k = 0; k < 33; ++k) acc[k] = 0.f;
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int k = 0; k < kGramWide; ++k) acc[i][k] = 0.f;
   for (int t0 = l0; t0 < l1; t0 += kBT) {
     const int nt = min(kBT, l1 - t0);
     const size_t row0 = (size_t)bh * L + t0;
@@ -809,37 +903,41 @@ __global__ void __launch_bounds__(kThreads) bwd_dstate_partial_kernel(
     __syncthreads();
     tile_norms<kBT>(xs, d, rs);
     __syncthreads();
-    for (int e = threadIdx.x; e < kBT * kFB; e += kThreads) {
-      const int t = e / kFB, f = e - t * kFB;
-      const float c = FM == FAVOR_FM_PRF ? scale * sqrtf(rs[t]) * W - 20.0f : 0.f;
-      ph[t * (kFB + 1) + f] =
-          (t < nt && f < nf) ? bwd_feature<FM>(scale * dot_row(xs + t * ld, om + f * ld, d), c) : 0.f;
-    }
-    __syncthreads();
-    for (int t = 0; t < nt; ++t) {
-      const float a = ph[t * (kFB + 1) + fa];
-      const float* dr = dn + t * ld;
+    {
+      float a[2][RT::kCols];
+      rowdot_block<kBT>(xs, ld, om, ld, d, a);
 #pragma unroll
-      for (int k = 0; k < 33; ++k) {
-        const int j = jb + 4 * k;
-        if (j <= d) acc[k] = fmaf(a, dr[j], acc[k]);
+      for (int i = 0; i < 2; ++i) {
+        const int t = RT::row(i);
+        const float c = FM == FAVOR_FM_PRF ? scale * sqrtf(rs[t]) * W - 20.0f : 0.f;
+#pragma unroll
+        for (int k = 0; k < RT::kCols; ++k) {
+          const int f = RT::col(k);
+          ph[t * (kFB + 1) + f] = (t < nt && f < nf) ? bwd_feature<FM>(scale * a[i][k], c) : 0.f;
+        }
       }
     }
+    __syncthreads();
+    gram_acc<kGramWide>(ph, kFB + 1, dn, ld, nt, ld, acc);
   }
-  if (fa < nf) {
-    float* dst = dpart + (((size_t)bh * n_split + split) * m + f0 + fa) * ld;
+  const int fg = threadIdx.x / 16, jl = threadIdx.x % 16;
+  float* dst = dpart + (((size_t)bh * n_split + split) * m + f0) * ld;
 #pragma unroll
-    for (int k = 0; k < 33; ++k) {
-      const int j = jb + 4 * k;
-      if (j <= d) dst[j] = acc[k];
-    }
+  for (int i = 0; i < 4; ++i) {
+    const int f = fg + 16 * i;
+    if (f < nf)
+#pragma unroll
+      for (int k = 0; k < kGramWide; ++k) {
+        const int j = jl + 16 * k;
+        if (j < ld) dst[(size_t)f * ld + j] = acc[i][k];
+      }
   }
 }
 
 // Key pass, one tile of kBT tokens of one head: phi(K), dphi(K) = dS~ [V|1]^T,
 // dV = phi(K) dS~[:, :d] and dK.
 template <typename T, int FM>
-__global__ void __launch_bounds__(kThreads) bwd_key_kernel(
+__global__ void __launch_bounds__(kThreads, 2) bwd_key_kernel(
     const T* __restrict__ K, const T* __restrict__ V, T* __restrict__ dK, T* __restrict__ dV,
     const float* __restrict__ omega, const float* __restrict__ key_ref, const float* __restrict__ dstate, int L,
     int d, int m, float scale) {
@@ -866,37 +964,33 @@ __global__ void __launch_bounds__(kThreads) bwd_key_kernel(
     rs[threadIdx.x] = FM == FAVOR_FM_PRF ? 0.5f * scale * scale * rs[threadIdx.x] + R : 0.f;
   tile_features<kBT, FM>(xs, rs, nt, d, m, scale, omega, om, P, ldp);
 
+  using RT = RegTile<kBT>;
   const float* dS = dstate + (size_t)bh * m * ld;
-  constexpr int kPer = (kBT * kMaxD + kThreads - 1) / kThreads;
-  float accv[kPer];
+  float accv[2][RT::kWide];
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) accv[k] = 0.f;
+  for (int k = 0; k < RT::kWide; ++k) accv[0][k] = accv[1][k] = 0.f;
   const int n_fb = (m + kFB - 1) / kFB;
   for (int fb = 0; fb < n_fb; ++fb) {
     const int f0 = fb * kFB, nf = min(kFB, m - f0);
     __syncthreads();
     load_state_block(dS, f0, nf, d, om);
     __syncthreads();
-    for (int e = threadIdx.x; e < kBT * kFB; e += kThreads) {
-      const int t = e / kFB, f = e - t * kFB;
-      if (f < nf) G[t * ldp + f0 + f] = dot_row(om + f * ld, vs + t * ld, ld);
-    }
+    float g[2][RT::kCols];
+    rowdot_block<kBT>(vs, ld, om, ld, ld, g);
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int e = threadIdx.x + k * kThreads;
-      if (e < kBT * d) {
-        const int t = e / d, j = e - t * d;
-        float a = accv[k];
-        for (int f = 0; f < nf; ++f) a = fmaf(P[t * ldp + f0 + f], om[f * ld + j], a);
-        accv[k] = a;
-      }
-    }
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int k = 0; k < RT::kCols; ++k)
+        if (RT::col(k) < nf) G[RT::row(i) * ldp + f0 + RT::col(k)] = g[i][k];
+    outer_acc<kBT, RT::kWide>(P + f0, ldp, om, ld, nf, d, accv);
   }
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int e = threadIdx.x + k * kThreads;
-    if (e < nt * d) dV[row0 * d + e] = from_f32<T>(accv[k]);
-  }
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int k = 0; k < RT::kWide; ++k) {
+      const int t = RT::row(i), j = RT::col(k);
+      if (t < nt && j < d) dV[(row0 + t) * d + j] = from_f32<T>(accv[i][k]);
+    }
   __syncthreads();
   tile_g<kBT, FM>(P, G, ldp, m, gsum);
   tile_input_grad<kBT, T, FM>(xs, G, ldp, gsum, nt, d, m, scale, omega, om, dK + row0 * d);
@@ -926,6 +1020,35 @@ size_t bwd_dstate_smem(int d) {
 // ---------------------------------------------------------------------------
 constexpr int kCT = 16;
 
+// state[f][j] += sum_{t < nt} X[t][f] Y[t][j] for all m features and j < ld
+// (a per-head [m][ld] state in global memory, each element owned by one
+// thread), by blocks of 64 features.  X rows of stride ldx hold the m
+// features (the block past m reads into the next row: discarded).
+__device__ __forceinline__ void add_tile_gram(const float* X, int ldx, const float* Y, int ld, int nt, int m,
+                                              float* __restrict__ state) {
+  const int fg = threadIdx.x / 16, jl = threadIdx.x % 16;
+  const int n_fb = (m + kFB - 1) / kFB;
+  for (int fb = 0; fb < n_fb; ++fb) {
+    const int f0 = fb * kFB, nf = min(kFB, m - f0);
+    float g[4][kGramWide];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int k = 0; k < kGramWide; ++k) g[i][k] = 0.f;
+    gram_acc<kGramWide>(X + f0, ldx, Y, ld, nt, ld, g);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int f = fg + 16 * i;
+      if (f < nf)
+#pragma unroll
+        for (int k = 0; k < kGramWide; ++k) {
+          const int j = jl + 16 * k;
+          if (j < ld) state[(size_t)(f0 + f) * ld + j] += g[i][k];
+        }
+    }
+  }
+}
+
 template <typename T, int FM>
 __global__ void __launch_bounds__(kThreads) cbwd_query_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,
@@ -953,7 +1076,7 @@ __global__ void __launch_bounds__(kThreads) cbwd_query_kernel(
   float R, W;
   key_reference(key_ref, m, &R, &W);
   const int n_fb = (m + kFB - 1) / kFB;
-  constexpr int kPerN = (kCT * (kMaxD + 1) + kThreads - 1) / kThreads;
+  using RT = RegTile<kCT>;
   for (int t0 = l0; t0 < l1; t0 += kCT) {
     const int nt = min(kCT, l1 - t0);
     const size_t row0 = (size_t)bh * L + t0;
@@ -981,33 +1104,27 @@ __global__ void __launch_bounds__(kThreads) cbwd_query_kernel(
       A[t * (kCT + 1) + s_] = a;
     }
     // N | D: prefix state part, then the tile's own (masked) part
-    float acc[kPerN];
+    float acc[2][RT::kWide];
 #pragma unroll
-    for (int k = 0; k < kPerN; ++k) acc[k] = 0.f;
+    for (int k = 0; k < RT::kWide; ++k) acc[0][k] = acc[1][k] = 0.f;
     for (int fb = 0; fb < n_fb; ++fb) {
       const int f0 = fb * kFB, nf = min(kFB, m - f0);
       __syncthreads();
       load_state_block(Gh, f0, nf, d, om);
       __syncthreads();
-#pragma unroll
-      for (int k = 0; k < kPerN; ++k) {
-        const int e = threadIdx.x + k * kThreads;
-        if (e < kCT * ld) {
-          const int t = e / ld, j = e - t * ld;
-          float a = acc[k];
-          for (int f = 0; f < nf; ++f) a = fmaf(P[t * ldp + f0 + f], om[f * ld + j], a);
-          acc[k] = a;
-        }
-      }
+      outer_acc<kCT, RT::kWide>(P + f0, ldp, om, ld, nf, ld, acc);
     }
 #pragma unroll
-    for (int k = 0; k < kPerN; ++k) {
-      const int e = threadIdx.x + k * kThreads;
-      if (e < kCT * ld) {
-        const int t = e / ld, j = e - t * ld;
-        float a = acc[k];
-        for (int s_ = 0; s_ <= t; ++s_) a = fmaf(A[t * (kCT + 1) + s_], vs[s_ * ld + j], a);
-        nd[e] = a;
+    for (int i = 0; i < 2; ++i) {
+      const int t = RT::row(i);
+#pragma unroll
+      for (int k = 0; k < RT::kWide; ++k) {
+        const int j = RT::col(k);
+        if (j < ld) {
+          float a = acc[i][k];
+          for (int s_ = 0; s_ <= t; ++s_) a = fmaf(A[t * (kCT + 1) + s_], vs[s_ * ld + j], a);
+          nd[t * ld + j] = a;
+        }
       }
     }
     __syncthreads();
@@ -1041,12 +1158,19 @@ __global__ void __launch_bounds__(kThreads) cbwd_query_kernel(
       __syncthreads();
       load_state_block(Gh, f0, nf, d, om);
       __syncthreads();
-      for (int e = threadIdx.x; e < kCT * kFB; e += kThreads) {
-        const int t = e / kFB, f = e - t * kFB;
-        if (f < nf) {
-          float a = dot_row(om + f * ld, go + t * ld, ld);
-          for (int s_ = 0; s_ <= t; ++s_) a = fmaf(Bm[t * (kCT + 1) + s_], Pk[s_ * ldp + f0 + f], a);
-          G[t * ldp + f0 + f] = a;
+      float g[2][RT::kCols];
+      rowdot_block<kCT>(go, ld, om, ld, ld, g);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int t = RT::row(i);
+#pragma unroll
+        for (int k = 0; k < RT::kCols; ++k) {
+          const int f = RT::col(k);
+          if (f < nf) {
+            float a = g[i][k];
+            for (int s_ = 0; s_ <= t; ++s_) a = fmaf(Bm[t * (kCT + 1) + s_], Pk[s_ * ldp + f0 + f], a);
+            G[t * ldp + f0 + f] = a;
+          }
         }
       }
     }
@@ -1054,12 +1178,7 @@ __global__ void __launch_bounds__(kThreads) cbwd_query_kernel(
     tile_g<kCT, FM>(P, G, ldp, m, gsum);
     tile_input_grad<kCT, T, FM>(xs, G, ldp, gsum, nt, d, m, scale, omega, om, dQ + row0 * d);
     // G~ += phi(K)^T [V | 1] of this tile (each element owned by one thread)
-    for (int e = threadIdx.x; e < m * ld; e += kThreads) {
-      const int i = e / ld, j = e - i * ld;
-      float a = 0.f;
-      for (int s_ = 0; s_ < nt; ++s_) a = fmaf(Pk[s_ * ldp + i], vs[s_ * ld + j], a);
-      Gh[e] += a;
-    }
+    add_tile_gram(Pk, ldp, vs, ld, nt, m, Gh);
   }
 }
 
@@ -1090,7 +1209,7 @@ __global__ void __launch_bounds__(kThreads) cbwd_key_kernel(
   float R, W;
   key_reference(key_ref, m, &R, &W);
   const int n_fb = (m + kFB - 1) / kFB;
-  constexpr int kPer = (kCT * kMaxD + kThreads - 1) / kThreads;
+  using RT = RegTile<kCT>;
   const int n_tiles = (l1 - l0 + kCT - 1) / kCT;
   for (int tile = n_tiles - 1; tile >= 0; --tile) {
     const int t0 = l0 + tile * kCT;
@@ -1122,53 +1241,49 @@ __global__ void __launch_bounds__(kThreads) cbwd_key_kernel(
       A[s_ * (kCT + 1) + t] = a;
       Cm[s_ * (kCT + 1) + t] = c;
     }
-    float accv[kPer];
+    float accv[2][RT::kWide];
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) accv[k] = 0.f;
+    for (int k = 0; k < RT::kWide; ++k) accv[0][k] = accv[1][k] = 0.f;
     for (int fb = 0; fb < n_fb; ++fb) {
       const int f0 = fb * kFB, nf = min(kFB, m - f0);
       __syncthreads();
       load_state_block(Hh, f0, nf, d, om);
       __syncthreads();
-      for (int e = threadIdx.x; e < kCT * kFB; e += kThreads) {
-        const int s_ = e / kFB, f = e - s_ * kFB;
-        if (f < nf) {
-          float a = dot_row(om + f * ld, vs + s_ * ld, ld);
-          for (int t = s_; t < kCT; ++t) a = fmaf(Cm[s_ * (kCT + 1) + t], P[t * ldp + f0 + f], a);
-          G[s_ * ldp + f0 + f] = a;
-        }
-      }
+      float g[2][RT::kCols];
+      rowdot_block<kCT>(vs, ld, om, ld, ld, g);
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int e = threadIdx.x + k * kThreads;
-        if (e < kCT * d) {
-          const int s_ = e / d, j = e - s_ * d;
-          float a = accv[k];
-          for (int f = 0; f < nf; ++f) a = fmaf(Pk[s_ * ldp + f0 + f], om[f * ld + j], a);
-          accv[k] = a;
+      for (int i = 0; i < 2; ++i) {
+        const int s_ = RT::row(i);
+#pragma unroll
+        for (int k = 0; k < RT::kCols; ++k) {
+          const int f = RT::col(k);
+          if (f < nf) {
+            float a = g[i][k];
+            for (int t = s_; t < kCT; ++t) a = fmaf(Cm[s_ * (kCT + 1) + t], P[t * ldp + f0 + f], a);
+            G[s_ * ldp + f0 + f] = a;
+          }
         }
       }
+      outer_acc<kCT, RT::kWide>(Pk + f0, ldp, om, ld, nf, d, accv);
     }
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int e = threadIdx.x + k * kThreads;
-      if (e < nt * d) {
-        const int s_ = e / d, j = e - s_ * d;
-        float a = accv[k];
-        for (int t = s_; t < kCT; ++t) a = fmaf(A[s_ * (kCT + 1) + t], go[t * ld + j], a);
-        dV[row0 * d + e] = from_f32<T>(a);
+    for (int i = 0; i < 2; ++i) {
+      const int s_ = RT::row(i);
+#pragma unroll
+      for (int k = 0; k < RT::kWide; ++k) {
+        const int j = RT::col(k);
+        if (s_ < nt && j < d) {
+          float a = accv[i][k];
+          for (int t = s_; t < kCT; ++t) a = fmaf(A[s_ * (kCT + 1) + t], go[t * ld + j], a);
+          dV[(row0 + s_) * d + j] = from_f32<T>(a);
+        }
       }
     }
     __syncthreads();
     tile_g<kCT, FM>(Pk, G, ldp, m, gsum);
     tile_input_grad<kCT, T, FM>(ks, G, ldp, gsum, nt, d, m, scale, omega, om, dK + row0 * d);
     // H += phi(Q)^T dN^ of this tile
-    for (int e = threadIdx.x; e < m * ld; e += kThreads) {
-      const int i = e / ld, j = e - i * ld;
-      float a = 0.f;
-      for (int t = 0; t < nt; ++t) a = fmaf(P[t * ldp + i], go[t * ld + j], a);
-      Hh[e] += a;
-    }
+    add_tile_gram(P, ldp, go, ld, nt, m, Hh);
   }
 }
 
