@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--decode-steps", type=int, default=200)
     ap.add_argument("--relu-steps", type=int, default=100)
+    ap.add_argument("--elu-steps", type=int, default=10)
     ap.add_argument("--bwd-steps", type=int, default=10)
     return ap.parse_args()
 
@@ -455,6 +456,15 @@ def run_gpu(args, rank, world, local_rank):
     if args.relu_steps > 0:
         relu = measure_feature_map(favor, "relu", args.relu_steps, sets, omegas[0], s, ws_b, ws_c, O_b, O_c, stream,
                                    status, dev, tokens_per_step)
+    elu1 = None
+    if args.elu_steps > 0:
+        # 1 + elu runs on the CUDA-core kernels: their workspaces
+        ws_be = favor.new_workspace(False, B, H, L, d, m, dt, device=dev, feature_map="elu1")
+        ws_ce = favor.new_workspace(True, B, H, L, d, m, dt, device=dev, feature_map="elu1")
+        elu1 = measure_feature_map(favor, "elu1", args.elu_steps, sets, omegas[0], s, ws_be, ws_ce, O_b, O_c,
+                                   stream, status, dev, tokens_per_step)
+        elu1["path"] = "CUDA-core kernels"
+        del ws_be, ws_ce
     # dominant kernel: largest share of the step
     dom = max((st for st in STAGES if st != "build_orf"), key=lambda st: stage_ms[st])
     nbytes, nflops = algorithmic(w, dom)
@@ -513,6 +523,7 @@ def run_gpu(args, rank, world, local_rank):
         "e2e": e2e,
         "decode": decode,
         "relu": relu,
+        "elu1": elu1,
         "backward": bwd,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -660,8 +671,8 @@ def measure_backward(favor, n_steps, sets, omega, s, stream, status, dev, tokens
 def measure_feature_map(favor, fm, n_steps, sets, omega, s, ws_b, ws_c, O_b, O_c, stream, status, dev,
                         tokens_per_step):
     """The bidirectional and causal forward passes of the step with another
-    feature map (Performer-ReLU): same workload, Omega built once, inputs
-    rotating over the sets (above L2), one CUDA graph per input set."""
+    feature map (Performer-ReLU, 1 + elu): same workload, Omega built once,
+    inputs rotating over the sets (above L2), one CUDA graph per input set."""
     graphs = []
     for q, k, v in sets:
         with torch.cuda.stream(stream):

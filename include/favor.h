@@ -76,11 +76,17 @@ typedef enum favor_dtype {
  * Performers" summary, §2 generalized kernelizable attention: other kernels
  * by changing the feature-map function; §3 and §D.2 name Performer-ReLU; the
  * pages print no formula, this is the plain reading).  relu is positively
- * homogeneous, so qk_scale cancels in the ReLU outputs.
+ * homogeneous, so qk_scale cancels in the ReLU outputs.  FAVOR_FM_ELU1:
+ * phi(x) = m^{-1/2} (1 + elu(Omega x)), 1 + a for a >= 0 and exp(a) below
+ * ("From Performer to Linear Attention", the linear-attention feature map it
+ * compares against; the "Performer" digest names it as Linear Attention's),
+ * in the same slot as ReLU; with Omega = I_d (m = d) it is linear attention
+ * itself.  Its calls run on the CUDA-core kernels (any supported shape).
  */
 typedef enum favor_feature_map {
   FAVOR_FM_PRF = 0,
-  FAVOR_FM_RELU = 1
+  FAVOR_FM_RELU = 1,
+  FAVOR_FM_ELU1 = 2
 } favor_feature_map;
 
 /* Library version (FAVOR_API_VERSION of the build). */
@@ -169,11 +175,18 @@ favor_status favor_fwd_causal(const void* Q, const void* K, const void* V, void*
 /*
  * favor_fwd_bidir_fm, favor_fwd_causal_fm — favor_fwd_bidir and
  * favor_fwd_causal with the feature map `fm` (favor_feature_map) in place of
- * the positive random features; same arguments, workspace sizes and paths.
+ * the positive random features; same arguments.  FAVOR_FM_PRF and
+ * FAVOR_FM_RELU take the same workspace sizes and paths as the plain calls;
+ * FAVOR_FM_ELU1 runs on the CUDA-core kernels and needs
+ * favor_workspace_bytes_fm(..., FAVOR_FM_ELU1) bytes (more than
+ * favor_workspace_bytes where the plain call takes the tensor cores).
  * A row whose features are all zero (every s w_i.q <= 0 under ReLU) has a
  * zero normaliser: its output is NaN and dev_status gets
- * FAVOR_ERR_NONFINITE.  fm outside the enum is FAVOR_ERR_INVALID_ARG.
+ * FAVOR_ERR_NONFINITE (1 + elu is positive: it never has one).  fm outside
+ * the enum is FAVOR_ERR_INVALID_ARG.
  */
+size_t favor_workspace_bytes_fm(int causal, int B, int H, int L, int d, int m,
+                                favor_dtype dt, favor_feature_map fm);
 favor_status favor_fwd_bidir_fm(const void* Q, const void* K, const void* V, void* O,
                                 int B, int H, int L, int d,
                                 const float* omega, int m, favor_dtype dt, float qk_scale,

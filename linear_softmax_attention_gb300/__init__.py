@@ -25,7 +25,7 @@ __all__ = [
 F32 = 0
 BF16 = 1
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
-FEATURE_MAPS = {"prf": 0, "relu": 1}      # favor_feature_map
+FEATURE_MAPS = {"prf": 0, "relu": 1, "elu1": 2}      # favor_feature_map
 
 ENTRY_POINTS = ("favor_fwd_bidir", "favor_fwd_causal", "favor_bidir_state", "favor_bidir_output",
                 "favor_causal_state", "favor_causal_output")
@@ -61,6 +61,8 @@ def load():
     lib.favor_build_orf.argtypes = [ctypes.c_uint64, c_int, c_int, c_int, c_vp, c_vp]
     lib.favor_workspace_bytes.restype = c_size
     lib.favor_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int, c_int]
+    lib.favor_workspace_bytes_fm.restype = c_size
+    lib.favor_workspace_bytes_fm.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int]
     fwd_args = [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_vp, c_int, c_int, c_float, c_vp, c_size,
                 c_vp, c_vp]
     for name in ENTRY_POINTS:
@@ -138,15 +140,23 @@ def new_omega(seed: int, m: int, d: int, orthogonal: bool = True, device="cuda")
     return build_orf(seed, om, orthogonal)
 
 
-def workspace_bytes(causal: bool, B: int, H: int, L: int, d: int, m: int, dtype) -> int:
-    n = load().favor_workspace_bytes(int(causal), B, H, L, d, m, _DT[dtype])
+def workspace_bytes(causal: bool, B: int, H: int, L: int, d: int, m: int, dtype, feature_map=None) -> int:
+    """Workspace bytes of fwd_bidir / fwd_causal for this shape (and feature
+    map: "elu1" runs on the CUDA-core kernels, whose workspace differs)."""
+    if feature_map in (None, "prf"):
+        n = load().favor_workspace_bytes(int(causal), B, H, L, d, m, _DT[dtype])
+    else:
+        if feature_map not in FEATURE_MAPS:
+            raise FavorError(f"feature_map must be one of {sorted(FEATURE_MAPS)}")
+        n = load().favor_workspace_bytes_fm(int(causal), B, H, L, d, m, _DT[dtype], FEATURE_MAPS[feature_map])
     if n == 0:
         raise FavorError(f"unsupported shape B={B} H={H} L={L} d={d} m={m} {dtype}")
     return n
 
 
-def new_workspace(causal: bool, B: int, H: int, L: int, d: int, m: int, dtype, device="cuda") -> torch.Tensor:
-    n = workspace_bytes(causal, B, H, L, d, m, dtype)
+def new_workspace(causal: bool, B: int, H: int, L: int, d: int, m: int, dtype, device="cuda",
+                  feature_map=None) -> torch.Tensor:
+    n = workspace_bytes(causal, B, H, L, d, m, dtype, feature_map)
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
@@ -182,8 +192,9 @@ def _out_like(x, O):
 
 def fwd_bidir(Q, K, V, omega, qk_scale, workspace, O=None, dev_status=None, stream=None, feature_map=None):
     """Bidirectional FAVOR+; returns O [B, H, L, d] (dtype of Q).  feature_map:
-    None or "prf" (positive random features, the softmax kernel) or "relu"
-    (Performer-ReLU)."""
+    None or "prf" (positive random features, the softmax kernel), "relu"
+    (Performer-ReLU) or "elu1" (1 + elu, the linear-attention map; its
+    workspace comes from new_workspace(..., feature_map="elu1"))."""
     fm = None if feature_map in (None, "prf") else feature_map
     return _call("favor_fwd_bidir", Q, K, V, _out_like(Q, O), omega, qk_scale, workspace, dev_status, stream, fm)
 

@@ -64,8 +64,16 @@ favor_status shape_ok(int B, int H, int L, int d, int m, favor_dtype dt) {
 
 bool use_tc(bool causal, int d, int m, favor_dtype dt) { return favor::tc_supported(causal, d, m, dt == FAVOR_BF16); }
 
-size_t ws_bytes_for(bool causal, const Shape& s, favor_dtype dt) {
-  if (use_tc(causal, s.d, s.m, dt)) return favor::tc_workspace_bytes(causal, s);
+// the tensor-core kernels carry the softmax and ReLU features; 1 + elu runs
+// on the CUDA-core kernels for every shape
+bool use_tc_fm(bool causal, int d, int m, favor_dtype dt, int fm) {
+  return fm != FAVOR_FM_ELU1 && use_tc(causal, d, m, dt);
+}
+
+bool fm_ok(int fm) { return fm == FAVOR_FM_PRF || fm == FAVOR_FM_RELU || fm == FAVOR_FM_ELU1; }
+
+size_t ws_bytes_for(bool causal, const Shape& s, favor_dtype dt, int fm = FAVOR_FM_PRF) {
+  if (use_tc_fm(causal, s.d, s.m, dt, fm)) return favor::tc_workspace_bytes(causal, s);
   return favor::simt_plan(causal, s).bytes;
 }
 
@@ -76,7 +84,7 @@ favor_status run(bool causal, int stage, const void* Q, const void* K, const voi
                  size_t ws_bytes, int32_t* dev_status, void* stream_, int fm = FAVOR_FM_PRF) {
   favor_status st = shape_ok(B, H, L, d, m, dt);
   if (st != FAVOR_OK) return st;
-  if (fm != FAVOR_FM_PRF && fm != FAVOR_FM_RELU) return FAVOR_ERR_INVALID_ARG;
+  if (!fm_ok(fm)) return FAVOR_ERR_INVALID_ARG;
   if (!std::isfinite(qk_scale) || !(qk_scale > 0.f)) return FAVOR_ERR_INVALID_ARG;
   const bool need_q = (stage & kOutput) != 0;
   const bool need_kv = (stage & kState) != 0 || causal;
@@ -88,12 +96,12 @@ favor_status run(bool causal, int stage, const void* Q, const void* K, const voi
   if (!aligned(workspace, 256)) return FAVOR_ERR_INVALID_ARG;
   if (need_q && (O == Q || O == K || O == V)) return FAVOR_ERR_INVALID_ARG;
   const Shape s{B, H, L, d, m};
-  if (ws_bytes < ws_bytes_for(causal, s, dt)) return FAVOR_ERR_INVALID_ARG;
+  if (ws_bytes < ws_bytes_for(causal, s, dt, fm)) return FAVOR_ERR_INVALID_ARG;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   const bool bf16 = dt == FAVOR_BF16;
   cudaError_t e = cudaSuccess;
-  if (use_tc(causal, d, m, dt)) {
+  if (use_tc_fm(causal, d, m, dt, fm)) {
     if (stage & kState) e = favor::tc_state(causal, K, V, omega, qk_scale, s, workspace, dev_status, stream, fm);
     if (e == cudaSuccess && (stage & kOutput))
       e = favor::tc_output(causal, Q, K, V, O, omega, qk_scale, s, workspace, dev_status, stream, fm);
@@ -127,7 +135,7 @@ favor_status bwd_run(bool causal, const void* Q, const void* K, const void* V, c
                      favor_feature_map fm, void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
   favor_status st = shape_ok(B, H, L, d, m, dt);
   if (st != FAVOR_OK) return st;
-  if (fm != FAVOR_FM_PRF && fm != FAVOR_FM_RELU) return FAVOR_ERR_INVALID_ARG;
+  if (!fm_ok(fm)) return FAVOR_ERR_INVALID_ARG;
   if (!std::isfinite(qk_scale) || !(qk_scale > 0.f)) return FAVOR_ERR_INVALID_ARG;
   const void* in[] = {Q, K, V, dO, static_cast<const void*>(omega)};
   const void* out[] = {dQ, dK, dV};
@@ -185,6 +193,12 @@ favor_status favor_build_orf(uint64_t seed, int m, int d, int orthogonal, float*
 size_t favor_workspace_bytes(int causal, int B, int H, int L, int d, int m, favor_dtype dt) {
   if (shape_ok(B, H, L, d, m, dt) != FAVOR_OK) return 0;
   return ws_bytes_for(causal != 0, Shape{B, H, L, d, m}, dt);
+}
+
+size_t favor_workspace_bytes_fm(int causal, int B, int H, int L, int d, int m, favor_dtype dt,
+                                favor_feature_map fm) {
+  if (shape_ok(B, H, L, d, m, dt) != FAVOR_OK || !fm_ok(fm)) return 0;
+  return ws_bytes_for(causal != 0, Shape{B, H, L, d, m}, dt, fm);
 }
 
 #define FAVOR_ARGS                                                                                      \

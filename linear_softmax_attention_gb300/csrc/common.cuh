@@ -109,7 +109,7 @@ cudaError_t simt_state_export(const void* K, const void* V, const float* omega, 
 cudaError_t launch_decode_step(const void* q, const void* k, const void* v, void* o, int BH, int d,
                                const float* omega, int m, bool bf16, float scale, float* state, int32_t* status,
                                cudaStream_t stream);
-// fm: favor_feature_map (FAVOR_FM_PRF or FAVOR_FM_RELU)
+// fm: favor_feature_map (FAVOR_FM_PRF, FAVOR_FM_RELU or FAVOR_FM_ELU1)
 cudaError_t simt_bidir_state(const void* K, const void* V, const float* omega, float scale,
                              const Shape& s, bool bf16, void* ws, int32_t* st, cudaStream_t stream,
                              int fm = FAVOR_FM_PRF);

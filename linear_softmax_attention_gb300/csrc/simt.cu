@@ -162,12 +162,16 @@ __device__ __forceinline__ void gram_acc(const float* X, int ldx, const float* Y
 //   S_p[f, :] = sum_t exp(l_tf - R) [v_t ; 1],  l_tf = s w_f.k_t - s^2 |k_t|^2 / 2
 // over its token range.
 // ---------------------------------------------------------------------------
+// 1 + elu(a): 1 + a for a >= 0, exp(a) below (a NaN stays a NaN)
+__device__ __forceinline__ float elu1(float a) { return a < 0.f ? expf(a) : 1.f + a; }
+
 // Key feature from its scaled projection a = s w.k: exp(a - s^2 |k|^2 / 2 - R)
 // for the positive random features, relu(a) for Performer-ReLU ("y < 0 ? 0
-// : y" keeps a NaN a NaN).
+// : y" keeps a NaN a NaN), 1 + elu(a) for the linear-attention map.
 template <int FM>
 __device__ __forceinline__ float key_feature(float a, float half_sq, float R) {
   if constexpr (FM == FAVOR_FM_PRF) return expf(a - half_sq - R);
+  else if constexpr (FM == FAVOR_FM_ELU1) return elu1(a);
   else return a < 0.f ? 0.f : a;
 }
 
@@ -273,12 +277,12 @@ __device__ void query_features(const float* qs, int nt, int d, int m, float scal
     }
   }
   __syncthreads();
-  if constexpr (FM == FAVOR_FM_RELU) {
-    // Performer-ReLU: relu of the scaled projection, no row constant
+  if constexpr (FM != FAVOR_FM_PRF) {
+    // Performer-ReLU or 1 + elu of the scaled projection, no row constant
     for (int e = threadIdx.x; e < kTT * m; e += kThreads) {
       const int t = e / m, f = e - t * m;
       const float a = pq[t * ldq + f];
-      pq[t * ldq + f] = (t < nt) ? (a < 0.f ? 0.f : a) : 0.f;
+      pq[t * ldq + f] = (t < nt) ? key_feature<FM>(a, 0.f, 0.f) : 0.f;
     }
     __syncthreads();
     return;
@@ -545,8 +549,15 @@ template <typename F>
 static cudaError_t dispatch(bool bf16, int fm, F&& f) {
   using Prf = std::integral_constant<int, FAVOR_FM_PRF>;
   using Relu = std::integral_constant<int, FAVOR_FM_RELU>;
-  if (bf16) return fm == FAVOR_FM_RELU ? f(__nv_bfloat16{}, Relu{}) : f(__nv_bfloat16{}, Prf{});
-  return fm == FAVOR_FM_RELU ? f(float{}, Relu{}) : f(float{}, Prf{});
+  using Elu1 = std::integral_constant<int, FAVOR_FM_ELU1>;
+  if (bf16) {
+    if (fm == FAVOR_FM_RELU) return f(__nv_bfloat16{}, Relu{});
+    if (fm == FAVOR_FM_ELU1) return f(__nv_bfloat16{}, Elu1{});
+    return f(__nv_bfloat16{}, Prf{});
+  }
+  if (fm == FAVOR_FM_RELU) return f(float{}, Relu{});
+  if (fm == FAVOR_FM_ELU1) return f(float{}, Elu1{});
+  return f(float{}, Prf{});
 }
 
 cudaError_t simt_bidir_state(const void* K, const void* V, const float* omega, float scale, const Shape& s,
@@ -693,7 +704,7 @@ __device__ __forceinline__ void tile_norms(const float* xs, int d, float* out) {
 template <int FM>
 __device__ __forceinline__ float bwd_feature(float p, float c) {
   if constexpr (FM == FAVOR_FM_PRF) return expf(p - c);
-  else return p < 0.f ? 0.f : p;
+  else return key_feature<FM>(p, 0.f, 0.f);
 }
 
 // rows [f0, f0 + nf) of a per-head [m][d+1] fp32 matrix into blk [kFB][d+1]
@@ -729,13 +740,17 @@ __device__ void tile_features(const float* xs, const float* rowc, int nt, int d,
   __syncthreads();
 }
 
-// g <- dphi * phi (prf) or dphi [phi > 0] (relu) in G; gsum[t] = sum_i g
+// g <- dphi * phi (prf), dphi [phi > 0] (relu) or dphi min(phi, 1) (1 + elu:
+// its slope is 1 where phi = 1 + a >= 1 and exp(a) = phi below) in G;
+// gsum[t] = sum_i g
 template <int TT, int FM>
 __device__ void tile_g(const float* P, float* G, int ldp, int m, float* gsum) {
   for (int e = threadIdx.x; e < TT * m; e += kThreads) {
     const int t = e / m, i = e - t * m;
     const float ph = P[t * ldp + i], dp = G[t * ldp + i];
-    G[t * ldp + i] = FM == FAVOR_FM_PRF ? dp * ph : (ph > 0.f ? dp : 0.f);
+    if constexpr (FM == FAVOR_FM_PRF) G[t * ldp + i] = dp * ph;
+    else if constexpr (FM == FAVOR_FM_ELU1) G[t * ldp + i] = dp * fminf(ph, 1.f);
+    else G[t * ldp + i] = ph > 0.f ? dp : 0.f;
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

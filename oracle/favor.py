@@ -52,6 +52,7 @@ __all__ = [
     "build_omega_givens",
     "prf_features",
     "relu_features",
+    "elu1_features",
     "FEATURES",
     "trig_features",
     "softmax_kernel",
@@ -323,7 +324,24 @@ def relu_features(X: np.ndarray, Omega: np.ndarray) -> np.ndarray:
     return np.maximum(X @ Om.T, 0.0) / math.sqrt(Om.shape[0])
 
 
-FEATURES = {"prf": prf_features, "relu": relu_features}
+def elu1_features(X: np.ndarray, Omega: np.ndarray) -> np.ndarray:
+    """Linear-attention features phi(x) = m^{-1/2} (1 + elu(Omega x)).
+
+    [su] (the linear-attention choice it compares against): phi(x) = 1 +
+    elu(x), i.e. 1 + x for x >= 0 and exp(x) for x < 0, the first-order
+    Taylor form of exp near 0; [digest] §Related work names it as the feature
+    map of Linear Attention (Katharopoulos 2020).  Read as the same
+    feature-map slot as Performer-ReLU, f(w_i^T x) with f = 1 + elu: with
+    Omega = I_d (m = d) it is that linear attention itself.  X [..., L, d]
+    (already times the temperature), Omega [m, d]; returns [..., L, m].
+    """
+    X = np.asarray(X, dtype=np.float64)
+    Om = np.asarray(Omega, dtype=np.float64)
+    a = X @ Om.T
+    return np.where(a >= 0.0, 1.0 + a, np.exp(np.minimum(a, 0.0))) / math.sqrt(Om.shape[0])
+
+
+FEATURES = {"prf": prf_features, "relu": relu_features, "elu1": elu1_features}
 
 
 def trig_features(X: np.ndarray, Omega: np.ndarray) -> np.ndarray:
@@ -456,6 +474,13 @@ def favor_rows(Q, K, V, Omega, scale: float, bh_rows, causal: bool, features: st
     return out
 
 
+def _map_slope(features: str, a: np.ndarray) -> np.ndarray:
+    """f'(a) of the projected feature maps f(a) (relu, 1 + elu)."""
+    if features == "relu":
+        return (a > 0).astype(np.float64)
+    return np.where(a >= 0.0, 1.0, np.exp(np.minimum(a, 0.0)))
+
+
 def favor_bidirectional_grad(Q, K, V, Omega, scale: float, dO, features: str = "prf"):
     """Gradients (dQ, dK, dV) of sum(dO * favor_bidirectional(Q, K, V)).
 
@@ -469,6 +494,7 @@ def favor_bidirectional_grad(Q, K, V, Omega, scale: float, dO, features: str = "
     and through the feature map x' = scale x, phi = f(Omega x' ...):
       prf:  d phi_i / d x' = phi_i (w_i - x')
       relu: d phi_i / d x' = m^-1/2 w_i [w_i . x' > 0]
+      elu1: d phi_i / d x' = m^-1/2 w_i (1 if w_i . x' >= 0 else exp(w_i . x'))
     then dx = scale dx'.
     """
     Q, K, V, dO = (np.asarray(a, dtype=np.float64) for a in (Q, K, V, dO))
@@ -494,8 +520,7 @@ def favor_bidirectional_grad(Q, K, V, Omega, scale: float, dO, features: str = "
             # sum_i dphi_i phi_i (w_i - x)
             g = dphi * phi
             return g @ Om - x * np.sum(g, axis=-1, keepdims=True)
-        mask = (x @ Om.T) > 0
-        return ((dphi * mask) @ Om) / math.sqrt(Om.shape[0])
+        return ((dphi * _map_slope(features, x @ Om.T)) @ Om) / math.sqrt(Om.shape[0])
 
     dQ = scale * through_features(qs, pq, dpq)
     dK = scale * through_features(ks, pk, dpk)
@@ -535,8 +560,7 @@ def favor_causal_grad(Q, K, V, Omega, scale: float, dO, features: str = "prf"):
         if features == "prf":
             g = dphi * phi
             return g @ Om - x * np.sum(g, axis=-1, keepdims=True)
-        m_ = (x @ Om.T) > 0
-        return ((dphi * m_) @ Om) / math.sqrt(Om.shape[0])
+        return ((dphi * _map_slope(features, x @ Om.T)) @ Om) / math.sqrt(Om.shape[0])
 
     return scale * through_features(qs, pq, dpq), scale * through_features(ks, pk, dpk), dV
 

@@ -148,12 +148,26 @@ def test_feature_map_calls_reject_bad_arguments(lib, name):
         a.update(kw)
         return getattr(lib, name)(a["Q"], a["K"], a["V"], a["O"], a["B"], a["H"], a["L"], a["d"], a["omega"],
                                   a["m"], a["dt"], a["s"], fm, a["ws"], a["nbytes"], a["st"], a["stream"])
-    assert call(fm=2) == 1             # not a favor_feature_map
+    assert call(fm=3) == 1             # not a favor_feature_map
     assert call(fm=-1) == 1
     assert call(omega=None) == 1
     assert call(L=0) == 1
     assert call(m=600) == 2
     assert call(nbytes=16) == 1
+
+
+def test_feature_map_workspace_sizes(lib):
+    for causal in (0, 1):
+        # softmax and ReLU features take the plain call's workspace
+        for fm in (0, 1):
+            assert lib.favor_workspace_bytes_fm(causal, 2, 4, 1000, 64, 256, 1, fm) == \
+                lib.favor_workspace_bytes(causal, 2, 4, 1000, 64, 256, 1)
+        # 1 + elu runs on the CUDA-core kernels: at least the CUDA-core plan of
+        # the same shape, which fp32 calls of that shape also use
+        assert lib.favor_workspace_bytes_fm(causal, 2, 4, 1000, 64, 256, 1, 2) >= \
+            lib.favor_workspace_bytes(causal, 2, 4, 1000, 64, 256, 0) > 0
+        assert lib.favor_workspace_bytes_fm(causal, 2, 4, 1000, 64, 256, 1, 3) == 0
+        assert lib.favor_workspace_bytes_fm(causal, 2, 4, 0, 64, 256, 1, 2) == 0
 
 
 @pytest.mark.parametrize("name", ["favor_bwd_bidir", "favor_bwd_causal"])

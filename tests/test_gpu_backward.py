@@ -26,7 +26,7 @@ def _per_head_err(got, ref):
     return float(np.max(np.max(np.abs(g - r), axis=1) / np.max(np.abs(r), axis=1)))
 
 
-@pytest.mark.parametrize("features", ["prf", "relu"])
+@pytest.mark.parametrize("features", ["prf", "relu", "elu1"])
 @pytest.mark.parametrize("dtype,B,H,L,d,m", [(torch.float32, 2, 2, 200, 64, 128),
                                              (torch.float32, 1, 3, 65, 32, 100),
                                              (torch.bfloat16, 2, 4, 1000, 64, 256),
@@ -60,7 +60,7 @@ def test_backward_is_deterministic(cuda_lib):
         assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("features", ["prf", "relu"])
+@pytest.mark.parametrize("features", ["prf", "relu", "elu1"])
 @pytest.mark.parametrize("dtype,B,H,L,d,m", [(torch.float32, 2, 2, 75, 64, 128),
                                              (torch.float32, 1, 2, 33, 32, 100),
                                              (torch.bfloat16, 2, 3, 300, 64, 256),

@@ -1,5 +1,5 @@
 """Pins of the oracle's bidirectional gradient (CPU only): central finite
-differences of the forward oracle in fp64, for both feature maps, on every
+differences of the forward oracle in fp64, for every feature map, on every
 element of tiny Q, K, V; and the identity that makes the query norm's
 gradient vanish (phi(Q) . dphi(Q) = 0 row by row)."""
 
@@ -15,9 +15,9 @@ def _loss(Q, K, V, Om, s, dO, features, causal=False):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("features", ["prf", "relu"])
+@pytest.mark.parametrize("features", ["prf", "relu", "elu1"])
 def test_gradient_matches_central_differences(features, causal):
-    rng = np.random.default_rng((7 if features == "prf" else 8) + 10 * causal)
+    rng = np.random.default_rng({"prf": 7, "relu": 8, "elu1": 6}[features] + 10 * causal)
     # enough features that no normaliser is zero (under ReLU a causal row
     # with one key can have phi(q).phi(k) = 0)
     L, d, m = 5, 3, 16
