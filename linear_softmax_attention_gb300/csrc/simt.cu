@@ -262,19 +262,21 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const float* __restrict
 template <int FM>
 __device__ void query_features(const float* qs, int nt, int d, int m, float scale,
                                const float* __restrict__ omega, float* om, float* pq, float* rowmax) {
+  using RT = RegTile<kTT>;
   const int ld = d + 1, ldq = m + 1;
-  const int f_own = threadIdx.x % kFB, t_base = threadIdx.x / kFB;
   const int n_fb = (m + kFB - 1) / kFB;
   for (int fb = 0; fb < n_fb; ++fb) {
     const int f0 = fb * kFB, nf = min(kFB, m - f0);
     __syncthreads();
     load_omega_block(omega, f0, nf, d, om);
     __syncthreads();
+    float a[2][RT::kCols];
+    rowdot_block<kTT>(qs, ld, om, ld, d, a);
 #pragma unroll
-    for (int j = 0; j < kTT / 4; ++j) {
-      const int t = t_base + 4 * j;
-      if (f_own < nf) pq[t * ldq + f0 + f_own] = scale * dot_row(qs + t * ld, om + f_own * ld, d);
-    }
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int k = 0; k < RT::kCols; ++k)
+        if (RT::col(k) < nf) pq[RT::row(i) * ldq + f0 + RT::col(k)] = scale * a[i][k];
   }
   __syncthreads();
   if constexpr (FM != FAVOR_FM_PRF) {
@@ -333,10 +335,10 @@ __global__ void __launch_bounds__(kThreads) bidir_output_kernel(
   load_rows(Q + ((size_t)bh * L + t0) * d, nt, d, qs, ld);
   query_features<FM>(qs, nt, d, m, scale, omega, om, pq, rowmax);
 
-  const int ta = threadIdx.x / 8, jb = threadIdx.x % 8;
-  float acc[17];
+  using RT = RegTile<kTT>;
+  float acc[2][RT::kWide];
 #pragma unroll
-  for (int k = 0; k < 17; ++k) acc[k] = 0.f;
+  for (int k = 0; k < RT::kWide; ++k) acc[0][k] = acc[1][k] = 0.f;
   const float* sh = state + (size_t)bh * m * ld;
   const int n_fb = (m + kFB - 1) / kFB;
   for (int fb = 0; fb < n_fb; ++fb) {
@@ -344,22 +346,14 @@ __global__ void __launch_bounds__(kThreads) bidir_output_kernel(
     __syncthreads();
     for (int e = threadIdx.x; e < nf * ld; e += kThreads) st[e] = sh[(size_t)f0 * ld + e];
     __syncthreads();
-    for (int f = 0; f < nf; ++f) {
-      const float p = pq[ta * ldq + f0 + f];
-      const float* sr = st + f * ld;
-#pragma unroll
-      for (int k = 0; k < 17; ++k) {
-        const int j = jb + 8 * k;
-        if (j <= d) acc[k] = fmaf(p, sr[j], acc[k]);
-      }
-    }
+    outer_acc<kTT, RT::kWide>(pq + f0, ldq, st, ld, nf, ld, acc);
   }
   __syncthreads();
 #pragma unroll
-  for (int k = 0; k < 17; ++k) {
-    const int j = jb + 8 * k;
-    if (j <= d) qs[ta * ld + j] = acc[k];
-  }
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int k = 0; k < RT::kWide; ++k)
+      if (RT::col(k) < ld) qs[RT::row(i) * ld + RT::col(k)] = acc[i][k];
   __syncthreads();
   store_output(qs, nt, d, O + ((size_t)bh * L + t0) * d, status);
 }
@@ -402,8 +396,9 @@ __global__ void __launch_bounds__(kThreads) causal_output_kernel(
   const float hs2 = 0.5f * scale * scale;
   const int l0 = sc * chunk, l1 = min(L, l0 + chunk);
   const size_t hoff = (size_t)bh * L * d;
-  const int f_own = threadIdx.x % kFB, t_base = threadIdx.x / kFB;
-  const int ta = threadIdx.x / 8, jb = threadIdx.x % 8;
+  using RT = RegTile<kTT>;
+  // the normaliser column: [v ; 1] (load_rows fills columns < d only)
+  if (threadIdx.x < kTT) vs[threadIdx.x * ld + d] = 1.f;
 
   for (int t0 = l0; t0 < l1; t0 += kTT) {
     const int nt = min(kTT, l1 - t0);
@@ -419,12 +414,15 @@ __global__ void __launch_bounds__(kThreads) causal_output_kernel(
       __syncthreads();
       load_omega_block(omega, f0, nf, d, om);
       __syncthreads();
+      float a[2][RT::kCols];
+      rowdot_block<kTT>(ks, ld, om, ld, d, a);
 #pragma unroll
-      for (int j = 0; j < kTT / 4; ++j) {
-        const int t = t_base + 4 * j;
-        if (f_own < nf) {
-          const float a = scale * dot_row(ks + t * ld, om + f_own * ld, d);
-          pk[t * ldq + f0 + f_own] = (t < nt) ? key_feature<FM>(a, hs2 * kn[t], Rk) : 0.f;
+      for (int i = 0; i < 2; ++i) {
+        const int t = RT::row(i);
+#pragma unroll
+        for (int k = 0; k < RT::kCols; ++k) {
+          const int f = RT::col(k);
+          if (f < nf) pk[t * ldq + f0 + f] = (t < nt) ? key_feature<FM>(scale * a[i][k], hs2 * kn[t], Rk) : 0.f;
         }
       }
     }
@@ -441,45 +439,52 @@ __global__ void __launch_bounds__(kThreads) causal_output_kernel(
       A[t * (kTT + 1) + s] = a;
     }
     __syncthreads();
-    float acc[17];
+    // inter (phi(Q) G, G read from the workspace) then intra (masked A [V | 1])
+    float acc[2][RT::kWide];
 #pragma unroll
-    for (int k = 0; k < 17; ++k) acc[k] = 0.f;
-    {
-      const float* qr = pq + ta * ldq;
-      for (int i = 0; i < m; ++i) {
-        const float p = qr[i];
-        const float* gr = G + (size_t)i * ld;
+    for (int k = 0; k < RT::kWide; ++k) acc[0][k] = acc[1][k] = 0.f;
+    outer_acc<kTT, RT::kWide>(pq, ldq, G, ld, m, ld, acc);
 #pragma unroll
-        for (int k = 0; k < 17; ++k) {
-          const int j = jb + 8 * k;
-          if (j <= d) acc[k] = fmaf(p, gr[j], acc[k]);
-        }
-      }
-      for (int s = 0; s <= ta && s < nt; ++s) {
-        const float a = A[ta * (kTT + 1) + s];
+    for (int i = 0; i < 2; ++i) {
+      const int t = RT::row(i);
+      for (int s = 0; s <= t && s < nt; ++s) {
+        const float a = A[t * (kTT + 1) + s];
         const float* vr = vs + s * ld;
 #pragma unroll
-        for (int k = 0; k < 17; ++k) {
-          const int j = jb + 8 * k;
-          if (j < d) acc[k] = fmaf(a, vr[j], acc[k]);
-          else if (j == d) acc[k] += a;
-        }
+        for (int k = 0; k < RT::kWide; ++k)
+          if (RT::col(k) < ld) acc[i][k] = fmaf(a, vr[RT::col(k)], acc[i][k]);
       }
     }
     __syncthreads();   // all reads of qs (projections) and G done
 #pragma unroll
-    for (int k = 0; k < 17; ++k) {
-      const int j = jb + 8 * k;
-      if (j <= d) qs[ta * ld + j] = acc[k];
-    }
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int k = 0; k < RT::kWide; ++k)
+        if (RT::col(k) < ld) qs[RT::row(i) * ld + RT::col(k)] = acc[i][k];
     __syncthreads();
     store_output(qs, nt, d, O + hoff + (size_t)t0 * d, status);
-    // G += phi(K)^T [V | 1]
-    for (int e = threadIdx.x; e < m * ld; e += kThreads) {
-      const int i = e / ld, j = e - i * ld;
-      float g = G[e];
-      for (int s = 0; s < nt; ++s) g = fmaf(pk[s * ldq + i], (j < d) ? vs[s * ld + j] : 1.f, g);
-      G[e] = g;
+    // G += phi(K)^T [V | 1], each element one fmaf chain from its old value
+    {
+      const int fg = threadIdx.x / 16, jl = threadIdx.x % 16;
+      for (int fb = 0; fb < n_fb; ++fb) {
+        const int f0 = fb * kFB, nf = min(kFB, m - f0);
+        float g[4][kGramWide];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int k = 0; k < kGramWide; ++k) {
+            const int f = fg + 16 * i, j = jl + 16 * k;
+            g[i][k] = (f < nf && j < ld) ? G[(size_t)(f0 + f) * ld + j] : 0.f;
+          }
+        gram_acc<kGramWide>(pk + f0, ldq, vs, ld, nt, ld, g);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int k = 0; k < kGramWide; ++k) {
+            const int f = fg + 16 * i, j = jl + 16 * k;
+            if (f < nf && j < ld) G[(size_t)(f0 + f) * ld + j] = g[i][k];
+          }
+      }
     }
   }
 }
