@@ -7,7 +7,7 @@ namespace favor {
 
 bool tc_supported(bool causal, int d, int m, bool bf16);
 size_t tc_workspace_bytes(bool causal, const Shape& s);
-// fm: favor_feature_map (FAVOR_FM_PRF or FAVOR_FM_RELU)
+// fm: favor_feature_map (FAVOR_FM_PRF or FAVOR_FM_RELU; 1 + elu runs on the CUDA-core kernels)
 cudaError_t tc_state(bool causal, const void* K, const void* V, const float* omega, float scale, const Shape& s,
                      void* ws, int32_t* status, cudaStream_t stream, int fm = FAVOR_FM_PRF);
 cudaError_t tc_output(bool causal, const void* Q, const void* K, const void* V, void* O, const float* omega,
