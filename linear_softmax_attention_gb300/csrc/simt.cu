@@ -44,6 +44,12 @@ __device__ __forceinline__ void load_omega_block(const float* __restrict__ omega
   }
 }
 
+// rows [f0, f0 + nf) of a per-head [m][d+1] fp32 matrix into blk [kFB][d+1]
+__device__ __forceinline__ void load_state_block(const float* __restrict__ src, int f0, int nf, int d, float* blk) {
+  const int ld = d + 1;
+  for (int e = threadIdx.x; e < nf * ld; e += kThreads) blk[e] = src[(size_t)f0 * ld + e];
+}
+
 __device__ __forceinline__ void row_norms(const float* xs, int d, float* kn) {
   if (threadIdx.x < kTT) {
     const float* row = xs + threadIdx.x * (d + 1);
@@ -427,23 +433,44 @@ __global__ void __launch_bounds__(kThreads) causal_output_kernel(
       }
     }
     query_features<FM>(qs, nt, d, m, scale, omega, om, pq, rowmax);
-    // intra-tile scores, lower triangle with the diagonal
-    for (int e = threadIdx.x; e < kTT * kTT; e += kThreads) {
-      const int t = e / kTT, s = e - t * kTT;
-      float a = 0.f;
-      if (s <= t && t < nt) {
-        const float* qr = pq + t * ldq;
-        const float* kr = pk + s * ldq;
-        for (int i = 0; i < m; ++i) a = fmaf(qr[i], kr[i], a);
+    // intra-tile scores, lower triangle with the diagonal: thread (tg, sl)
+    // owns rows tg, tg + 16 and columns sl, sl + 16 (2 x 2 per thread)
+    {
+      const int tg = threadIdx.x / 16, sl = threadIdx.x % 16;
+      const float* q0 = pq + tg * ldq;
+      const float* q1 = q0 + 16 * ldq;
+      const float* k0 = pk + sl * ldq;
+      const float* k1 = k0 + 16 * ldq;
+      float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+#pragma unroll 4
+      for (int i = 0; i < m; ++i) {
+        const float x0 = q0[i], x1 = q1[i], y0 = k0[i], y1 = k1[i];
+        a00 = fmaf(x0, y0, a00);
+        a01 = fmaf(x0, y1, a01);
+        a10 = fmaf(x1, y0, a10);
+        a11 = fmaf(x1, y1, a11);
       }
-      A[t * (kTT + 1) + s] = a;
+      const float av[2][2] = {{a00, a01}, {a10, a11}};
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int t = tg + 16 * i, s_ = sl + 16 * j;
+          A[t * (kTT + 1) + s_] = (s_ <= t && t < nt) ? av[i][j] : 0.f;
+        }
     }
-    __syncthreads();
-    // inter (phi(Q) G, G read from the workspace) then intra (masked A [V | 1])
+    // inter (phi(Q) G, G staged block by block from the workspace) then intra
+    // (masked A [V | 1])
     float acc[2][RT::kWide];
 #pragma unroll
     for (int k = 0; k < RT::kWide; ++k) acc[0][k] = acc[1][k] = 0.f;
-    outer_acc<kTT, RT::kWide>(pq, ldq, G, ld, m, ld, acc);
+    for (int fb = 0; fb < n_fb; ++fb) {
+      const int f0 = fb * kFB, nf = min(kFB, m - f0);
+      __syncthreads();
+      load_state_block(G, f0, nf, d, om);
+      __syncthreads();
+      outer_acc<kTT, RT::kWide>(pq + f0, ldq, om, ld, nf, ld, acc);
+    }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int t = RT::row(i);
@@ -712,11 +739,6 @@ __device__ __forceinline__ float bwd_feature(float p, float c) {
   else return key_feature<FM>(p, 0.f, 0.f);
 }
 
-// rows [f0, f0 + nf) of a per-head [m][d+1] fp32 matrix into blk [kFB][d+1]
-__device__ __forceinline__ void load_state_block(const float* __restrict__ src, int f0, int nf, int d, float* blk) {
-  const int ld = d + 1;
-  for (int e = threadIdx.x; e < nf * ld; e += kThreads) blk[e] = src[(size_t)f0 * ld + e];
-}
 
 // features of the tile rows xs against all m rows of Omega into P [TT][ldp]
 template <int TT, int FM>
