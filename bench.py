@@ -27,6 +27,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -149,10 +150,8 @@ class ClockSampler:
 
     def start(self):
         try:
-            out_dir = os.path.join(ROOT, "gpurun_out")
-            os.makedirs(out_dir, exist_ok=True)
-            self.path = os.path.join(out_dir, f"clocks_{os.getpid()}.csv")
-            self.f = open(self.path, "w")
+            fd, self.path = tempfile.mkstemp(prefix="favor_clocks_", suffix=".csv")
+            self.f = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.QUERY}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
