@@ -1,6 +1,6 @@
 """Plain fp64 CPU oracle for the FAVOR+ forward pass (test infrastructure only).
 
-This package is the independent checker for the CUDA library.  It is imported
+This package is the oracle the CUDA library is tested against.  It is imported
 only by the tests, by ``__graft_entry__.smoke()`` and by ``bench.py``'s CPU
 baseline / reference arm.  The product path (``linear_softmax_attention_gb300``)
 never imports it, and it never imports the product path.
