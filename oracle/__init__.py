@@ -1,4 +1,4 @@
-"""Plain fp64 CPU oracle for the FAVOR+ forward pass (test infrastructure only).
+"""Plain fp64 CPU oracle for FAVOR+: projections, forward passes and their gradients (test infrastructure only).
 
 This package is the oracle the CUDA library is tested against.  It is imported
 only by the tests, by ``__graft_entry__.smoke()`` and by ``bench.py``'s CPU
