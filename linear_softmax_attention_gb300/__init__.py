@@ -19,7 +19,7 @@ __all__ = [
     "workspace_bytes", "new_workspace", "fwd_bidir", "fwd_causal", "bidir_state", "bidir_output",
     "causal_state", "causal_output", "status_string", "ENTRY_POINTS", "fwd_bidir_static", "static_scratch_bytes",
     "new_decode_state", "decode_step", "decode_prefill", "decode_prefill_workspace_bytes", "FEATURE_MAPS",
-    "bwd_bidir", "bwd_causal", "bwd_workspace_bytes",
+    "bwd_bidir", "bwd_causal", "bwd_workspace_bytes", "selftest_wait_timeout",
 ]
 
 F32 = 0
@@ -85,6 +85,8 @@ def load():
     lib.favor_bwd_causal.argtypes = lib.favor_bwd_bidir.argtypes
     lib.favor_bwd_workspace_bytes.restype = c_size
     lib.favor_bwd_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int]
+    lib.favor_selftest_wait_timeout.restype = c_int
+    lib.favor_selftest_wait_timeout.argtypes = [c_vp, c_vp, c_vp, c_vp]
     lib.favor_decode_step.restype = c_int
     lib.favor_decode_step.argtypes = [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_vp, c_int, c_int, c_float,
                                       c_vp, c_vp, c_vp]
@@ -296,6 +298,21 @@ def decode_prefill(K, V, omega, qk_scale, state, workspace=None, dev_status=None
                                        _stream_handle(stream))
     _check(code, "favor_decode_prefill")
     return state
+
+
+def selftest_wait_timeout(stream=None, device="cuda"):
+    """favor_selftest_wait_timeout: two device waits that run out (no fault).
+    Returns (status, returned, times_ns) after synchronising: the device
+    status (FAVOR_ERR_TIMEOUT expected), int32[2] with 2 for each wait that
+    gave up, and int64[3] globaltimer stamps (start, warp 0 return, warp 1
+    return)."""
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    returned = torch.zeros(2, dtype=torch.int32, device=device)
+    times = torch.zeros(3, dtype=torch.int64, device=device)
+    _check(load().favor_selftest_wait_timeout(status.data_ptr(), returned.data_ptr(), times.data_ptr(),
+                                              _stream_handle(stream)), "favor_selftest_wait_timeout")
+    torch.cuda.synchronize(device)
+    return int(status.item()), returned.cpu().tolist(), times.cpu().tolist()
 
 
 def bwd_workspace_bytes(B: int, H: int, L: int, d: int, m: int, dtype) -> int:

@@ -1,5 +1,5 @@
 """C-ABI checks that need no GPU: the library loads, exports every entry point
-declared in include/favor.h, and rejects bad arguments before launching."""
+declared in include/*.h, and rejects bad arguments before launching."""
 
 import ctypes
 import os
@@ -14,9 +14,13 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _declared_functions():
-    text = open(os.path.join(ROOT, "include", "favor.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(favor_[a-z0-9_]+)\s*\(", text)))
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for h in sorted(os.listdir(inc)):
+        if h.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, h)).read(), flags=re.S)
+            names.update(re.findall(r"\b(favor_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 @pytest.fixture(scope="module")
@@ -30,6 +34,7 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = _declared_functions()
     assert len(names) >= 11
+    assert "favor_selftest_wait_timeout" in names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -190,3 +195,9 @@ def test_backward_rejects_bad_arguments_before_launch(lib, name):
     assert call(d=129) == 2
     assert lib.favor_bwd_workspace_bytes(2, 4, 1000, 64, 256, 1) > 0
     assert lib.favor_bwd_workspace_bytes(2, 4, 0, 64, 256, 1) == 0
+
+
+def test_selftest_rejects_null_pointers(lib):
+    assert lib.favor_selftest_wait_timeout(None, 16, 32, None) == 1
+    assert lib.favor_selftest_wait_timeout(16, None, 32, None) == 1
+    assert lib.favor_selftest_wait_timeout(16, 32, None, None) == 1
