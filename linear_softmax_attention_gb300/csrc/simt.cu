@@ -1,5 +1,7 @@
-// CUDA-core FAVOR+ kernels (fp32 arithmetic): the path for fp32 storage and
-// for shapes the tensor-core kernels do not cover.
+// CUDA-core FAVOR+ kernels (fp32 arithmetic): the path for fp32 storage, for
+// shapes the tensor-core kernels do not cover, for the 1 + elu feature map
+// and for the backward of both passes.  Every product runs on per-thread
+// register tiles (RegTile, rowdot_block, outer_acc, gram_acc below).
 //
 // Formulas: "Performer — Rethinking Attention with Performers" (digest),
 // §Key equations: phi(x) = m^-1/2 exp(Omega x - |x|^2/2) and
@@ -57,13 +59,6 @@ __device__ __forceinline__ void row_norms(const float* xs, int d, float* kn) {
     for (int c = 0; c < d; ++c) acc = fmaf(row[c], row[c], acc);
     kn[threadIdx.x] = acc;
   }
-}
-
-// s * (x_t . w_f) for tile rows t and block features f; 8 (t, f) per thread.
-__device__ __forceinline__ float dot_row(const float* x, const float* w, int d) {
-  float acc = 0.f;
-  for (int c = 0; c < d; ++c) acc = fmaf(x[c], w[c], acc);
-  return acc;
 }
 
 // Register tiles of a TT x 64 block (TT = 32 or 16 rows; 64 = kFB columns)
