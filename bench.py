@@ -509,7 +509,8 @@ def run_gpu(args, rank, world, local_rank):
                    f"({n_sets * bytes_per_set / 2**20:.0f} MiB > L2)", "timing": "CUDA graph replay per step; per-kernel times from per-stage graphs with events between stages",
                    "omega": "each step builds the next step's Omega on a second stream (double-buffered) while its attention kernels run",
                    "parallelism": f"replicas x{world}"},
-        "modes": {"bidir_tokens_per_s": tokens_per_step / (bidir_ms / 1e3),
+        "modes": {"head_tokens_per_s": value * H,
+                  "bidir_tokens_per_s": tokens_per_step / (bidir_ms / 1e3),
                   "causal_tokens_per_s": tokens_per_step / (causal_ms / 1e3),
                   "build_orf_ms": stage_ms["build_orf"],
                   "build_orf_hadamard_ms": time_build(favor, "hadamard", m, d, stream, dev),
