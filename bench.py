@@ -55,6 +55,10 @@ def parse():
     ap.add_argument("--relu-steps", type=int, default=100)
     ap.add_argument("--elu-steps", type=int, default=10)
     ap.add_argument("--bwd-steps", type=int, default=10)
+    ap.add_argument("--config-steps", type=int, default=20,
+                    help="calls timed per configuration line (0: no per-configuration lines)")
+    ap.add_argument("--config-cpu-s", type=float, default=1.5,
+                    help="seconds of oracle time per configuration line's cpu_baseline (0: none)")
     return ap.parse_args()
 
 
@@ -285,6 +289,9 @@ def run_gpu(args, rank, world, local_rank):
         ev_join.record(side)
         stream.wait_event(ev_join)
 
+    # the input sets and workspaces were made on the current stream; every
+    # step runs on `stream`
+    torch.cuda.synchronize(dev)
     favor.build_orf(wl.omega_seed_for_call(w, 0), omegas[0], stream=stream)
 
     # kernels of this library per step: tensor-core path = ORF, prep + state,
@@ -464,20 +471,24 @@ def run_gpu(args, rank, world, local_rank):
                                    stream, status, dev, tokens_per_step)
         elu1["path"] = "CUDA-core kernels"
         del ws_be, ws_ce
+    configs = measure_configs(favor, args, dev, stream, status, hbm, tc_burst) if args.config_steps > 0 else None
     # dominant kernel: largest share of the step
+    # the stage times come from sub-millisecond graph replays of one kernel
+    # each: the burst tensor peak applies (the sustained one is for a kernel
+    # timed inside a seconds-long loop)
     dom = max((st for st in STAGES if st != "build_orf"), key=lambda st: stage_ms[st])
     nbytes, nflops = algorithmic(w, dom)
     t_dom = stage_ms[dom] / 1e3
     t_hbm = nbytes / (hbm * 1e9)
-    t_tc = nflops / (tc_sus * 1e12)
+    t_tc = nflops / (tc_burst * 1e12)
     if t_tc > t_hbm:
-        roof = {"bound": "tensor", "achieved": nflops / t_dom / 1e12, "peak": tc_sus, "unit": "TFLOP/s"}
+        roof = {"bound": "tensor", "achieved": nflops / t_dom / 1e12, "peak": tc_burst, "unit": "TFLOP/s"}
     else:
         roof = {"bound": "hbm", "achieved": nbytes / t_dom / 1e9, "peak": hbm, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = profiled_traffic(dom, w.name)
     roof["kernel"] = dom
-    roof["peak_source"] = f"{peak_kind} ({'sustained bf16' if roof['bound'] == 'tensor' else 'HBM copy'})"
+    roof["peak_source"] = f"{peak_kind} ({'burst bf16' if roof['bound'] == 'tensor' else 'HBM copy'})"
     roof["algorithmic_bytes_per_launch"] = nbytes
     roof["algorithmic_flops_per_launch"] = nflops
     stages_out = {}
@@ -486,7 +497,7 @@ def run_gpu(args, rank, world, local_rank):
         t_ = stage_ms[st] / 1e3
         stages_out[st] = {"ms": stage_ms[st], "GB/s": b_ / t_ / 1e9, "TFLOP/s": f_ / t_ / 1e12,
                           "hbm_frac": b_ / t_ / 1e9 / hbm,
-                          "roofline_frac": max(b_ / (hbm * 1e9), f_ / (tc_sus * 1e12)) / t_}
+                          "roofline_frac": max(b_ / (hbm * 1e9), f_ / (tc_burst * 1e12)) / t_}
     bidir_ms = stage_ms["bidir_state"] + stage_ms["bidir_output"]
     causal_ms = stage_ms["causal_state"] + stage_ms["causal_output"]
 
@@ -525,6 +536,7 @@ def run_gpu(args, rank, world, local_rank):
         "relu": relu,
         "elu1": elu1,
         "backward": bwd,
+        "configs": configs,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=12.0)
@@ -533,6 +545,150 @@ def run_gpu(args, rank, world, local_rank):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
+# one line per configuration: the full public call on each workload
+# ---------------------------------------------------------------------------
+
+CONFIGS = [
+    # (configuration number, workload names)
+    (1, ["bidir-f32-B1H1L512-d64-m64"]),
+    (2, ["bidir-bf16-B8H8L4096-d64-m256"]),
+    (3, ["causal-bf16-B4H8L8192-d64-m256"]),
+    (4, ["causal-bf16-B2H8L12288-d64-m256"]),
+    (5, list(wl.SWEEP)),
+]
+
+
+def alu_peak_tflops(dev) -> float:
+    """fp32 FMA peak of the CUDA cores: SMs x 128 lanes x 2 flop x max SM clock."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f)["sm_max_mhz"])
+    except (OSError, KeyError, ValueError):
+        mhz = 2070.0
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def call_roofline(w, ms: float, hbm: float, tc_burst: float, alu: float):
+    """Roofline of one full forward call (state + output): algorithmic bytes
+    4 d e and flops 4 m d + 4 m (d + 1) per head-token.  bf16 runs against the
+    burst tensor peak and the HBM copy rate; fp32 storage runs on the CUDA
+    cores, so against their FMA peak."""
+    e = 4 if w.dtype == "f32" else 2
+    ht = w.B * w.H * w.L
+    nbytes = ht * 4 * w.d * e
+    nflops = ht * (4 * w.m * w.d + 4 * w.m * (w.d + 1))
+    t = ms / 1e3
+    peak_f, unit_f, bound_f = (alu, "TFLOP/s", "alu") if w.dtype == "f32" else (tc_burst, "TFLOP/s", "tensor")
+    if nflops / (peak_f * 1e12) > nbytes / (hbm * 1e9):
+        r = {"bound": bound_f, "achieved": nflops / t / 1e12, "peak": peak_f, "unit": unit_f}
+    else:
+        r = {"bound": "hbm", "achieved": nbytes / t / 1e9, "peak": hbm, "unit": "GB/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["algorithmic_bytes_per_call"] = nbytes
+    r["algorithmic_flops_per_call"] = nflops
+    return r
+
+
+def oracle_mode_rate(w, budget_s: float):
+    """Head-tokens per second of the fp64 oracle on one head of a token
+    prefix of the workload, in the workload's own mode, sized to take about
+    ``budget_s`` (the oracle is linear in L in both modes)."""
+    import numpy as np
+
+    import oracle as orc
+    causal = w.mode == "causal"
+    f64 = (lambda t: t.float().numpy().astype(np.float64))
+    om = orc.build_omega(wl.omega_seed_for_call(w, 0), w.m, w.d)
+
+    def run(L):
+        q, k, v = wl.make_qkv(w, seed=0, B=1, H=1, L=L)
+        t0 = time.perf_counter()
+        (orc.favor_causal if causal else orc.favor_bidirectional)(f64(q), f64(k), f64(v), om, w.qk_scale)
+        return time.perf_counter() - t0
+
+    L0 = min(w.L, 256)
+    t0 = run(L0)
+    Ls = int(min(w.L, max(L0, L0 * budget_s / max(t0, 1e-6))))
+    t = run(Ls) if Ls != L0 else t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return Ls / t, Ls, cores
+
+
+def measure_configs(favor, args, dev, stream, status, hbm, tc_burst):
+    """Every configuration through the public full call (favor_fwd_bidir or
+    favor_fwd_causal; for the redrawn-Omega workload favor_build_orf with the
+    call's seed first, on the same stream).  Each call is timed alone with
+    CUDA events on its stream, after a write of 2 x L2 that flushes the
+    cache; value = B L tokens per mean call time."""
+    alu = alu_peak_tflops(dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    out = {}
+    cpu_done = set()
+    for number, names in CONFIGS:
+        for name in names:
+            w = wl.get(name)
+            causal = w.mode == "causal"
+            q, k, v = wl.make_qkv(w, seed=0, device=dev)
+            O = torch.empty_like(q)
+            om = favor.new_omega(wl.omega_seed_for_call(w, 0), w.m, w.d, device=dev)
+            ws = favor.new_workspace(causal, w.B, w.H, w.L, w.d, w.m, w.torch_dtype, device=dev)
+            fn = favor.fwd_causal if causal else favor.fwd_bidir
+            # inputs, Omega and workspace were made on the current stream; the
+            # calls below run on `stream`
+            torch.cuda.synchronize(dev)
+
+            def call(i, build):
+                if build:
+                    favor.build_orf(wl.omega_seed_for_call(w, i), om, stream=stream)
+                fn(q, k, v, om, w.qk_scale, ws, O=O, dev_status=status, stream=stream)
+
+            def timed(build):
+                with torch.cuda.stream(stream):
+                    for i in range(3):
+                        call(i, build)
+                torch.cuda.synchronize(dev)
+                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(args.config_steps)]
+                with torch.cuda.stream(stream):
+                    for i, (e0, e1) in enumerate(evs):
+                        flush.fill_(i & 0xFF)
+                        e0.record(stream)
+                        call(i + 3, build)
+                        e1.record(stream)
+                torch.cuda.synchronize(dev)
+                if int(status.item()) != 0:
+                    raise RuntimeError(f"device status {int(status.item())} on {name}")
+                return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+            ms = timed(w.redraw_omega)
+            line = {"config": number, "mode": w.mode, "dtype": w.dtype, "B": w.B, "H": w.H, "L": w.L, "d": w.d,
+                    "m": w.m, "path": favor.path_name(causal, w.d, w.m, w.torch_dtype),
+                    "value": w.B * w.L / (ms / 1e3), "unit": "tokens/s",
+                    "head_tokens_per_s": w.B * w.H * w.L / (ms / 1e3), "ms_per_call": ms,
+                    "calls": args.config_steps, "roofline": call_roofline(w, ms, hbm, tc_burst, alu)}
+            if w.redraw_omega:
+                ms_c = timed(False)
+                line["call"] = "favor_build_orf (seed of the call) + favor_fwd_causal, one stream"
+                line["omega_cached"] = {"ms_per_call": ms_c, "value": w.B * w.L / (ms_c / 1e3)}
+                line["build_share"] = (ms - ms_c) / ms
+            # the oracle on a bounded sample: every named workload, and the
+            # longest sequence of each (mode, m) of the sweep
+            key = (w.mode, w.m) if number == 5 else name
+            if args.config_cpu_s > 0 and key not in cpu_done and (number != 5 or w.L == 65536):
+                cpu_done.add(key)
+                rate, Ls, cores = oracle_mode_rate(w, args.config_cpu_s)
+                line["cpu_baseline"] = {"value": rate / w.H, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                        "sample": f"one head of the first {Ls} tokens, {w.mode}, fp64 NumPy; "
+                                                  f"tokens = head-tokens / H"}
+            out[name] = line
+            del q, k, v, O, ws
+    del flush
+    torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -636,6 +792,7 @@ def measure_backward(favor, n_steps, sets, omega, s, stream, status, dev, tokens
     dO = torch.randn(q0.shape, generator=gen).to(q0.dtype).to(dev)
     ws = torch.empty(favor.bwd_workspace_bytes(B, H, L, d, omega.shape[0], q0.dtype), dtype=torch.uint8, device=dev)
     dQ, dK, dV = torch.empty_like(q0), torch.empty_like(q0), torch.empty_like(q0)
+    torch.cuda.synchronize(dev)      # dO was made on the current stream
     out = {}
     for causal in (False, True):
         graphs = []
@@ -719,6 +876,7 @@ def measure_decode(favor, n_steps, stream, status, hbm, dev):
     o = torch.empty_like(q)
     s = d ** -0.25
     per_graph = 10
+    torch.cuda.synchronize(dev)      # inputs, Omega and state were made on the current stream
     with torch.cuda.stream(stream):
         for _ in range(3):
             favor.decode_step(q, k, v, om, s, state, o=o, dev_status=status, stream=stream)

@@ -38,9 +38,9 @@
  *    asynchronous on `stream`.  The return value reports argument checks
  *    (made before anything is launched) and launch errors.
  *  - Supported: 1 <= L, 1 <= d <= 128, 1 <= m <= 512, B*H >= 1,
- *    B*H*L*d < 2^31.  bf16 with d in {64, 128} and m a multiple of 128 runs on
- *    the tcgen05 tensor-core kernels; every other supported shape runs on
- *    CUDA-core kernels with fp32 arithmetic.
+ *    B*H*L*d < 2^31.  bf16 with d = 64 and m in {128, 256} runs on the
+ *    tcgen05 tensor-core kernels (favor_path_name reports which); every other
+ *    supported shape runs on CUDA-core kernels with fp32 arithmetic.
  */
 #ifndef FAVOR_H_
 #define FAVOR_H_
@@ -329,8 +329,9 @@ size_t favor_bwd_workspace_bytes(int B, int H, int L, int d, int m, favor_dtype 
  *   state += phi(s k) [v ; 1]^T   (the new token is part of its own prefix)
  *   o = phi(s q)^T state[:, :d] / phi(s q)^T state[:, d]
  * which equals row t of favor_fwd_causal over the whole sequence, given the
- * state of tokens 0 .. t-1.  The state is read and written in place; o may
- * not alias q, k, v or the state.  A zero or non-finite normaliser is
+ * state of tokens 0 .. t-1.  The state is read and written in place; the
+ * byte ranges of o and of the state may not overlap one another or those of
+ * q, k, v (FAVOR_ERR_INVALID_ARG).  A zero or non-finite normaliser is
  * reported in dev_status (FAVOR_ERR_NONFINITE).  Supported: 1 <= d <= 128,
  * 1 <= m <= 512, 1 <= B*H <= 65535, bf16 or fp32.
  *

@@ -52,6 +52,16 @@ constexpr int kVersion = FAVOR_API_VERSION;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// [p, p + n) as bytes
+struct Range {
+  const void* p;
+  size_t n;
+};
+bool overlaps(const Range& a, const Range& b) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+  return a0 < b0 + b.n && b0 < a0 + a.n;
+}
+
 favor_status shape_ok(int B, int H, int L, int d, int m, favor_dtype dt) {
   if (B < 1 || H < 1 || L < 1 || d < 1 || m < 1) return FAVOR_ERR_INVALID_ARG;
   if (dt != FAVOR_F32 && dt != FAVOR_BF16) return FAVOR_ERR_INVALID_ARG;
@@ -256,7 +266,16 @@ favor_status favor_decode_step(const void* q, const void* k, const void* v, void
   for (const void* p : {q, k, v, static_cast<const void*>(o), static_cast<const void*>(omega),
                         static_cast<const void*>(state)})
     if (p == nullptr || !aligned(p, 16)) return FAVOR_ERR_INVALID_ARG;
-  if (o == q || o == k || o == v || o == state) return FAVOR_ERR_INVALID_ARG;
+  // o and the state are written: neither may overlap anything else
+  const size_t e_sz = dt == FAVOR_BF16 ? 2 : 4;
+  const size_t tok_bytes = (size_t)B * H * d * e_sz;
+  const size_t st_bytes = (size_t)B * H * (d + 1) * m * sizeof(float);
+  const Range ro{o, tok_bytes}, rs{state, st_bytes};
+  for (const void* in : {q, k, v}) {
+    const Range r{in, tok_bytes};
+    if (overlaps(ro, r) || overlaps(rs, r)) return FAVOR_ERR_INVALID_ARG;
+  }
+  if (overlaps(ro, rs)) return FAVOR_ERR_INVALID_ARG;
   cudaError_t e = favor::launch_decode_step(q, k, v, o, B * H, d, omega, m, dt == FAVOR_BF16, qk_scale, state,
                                             dev_status, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;

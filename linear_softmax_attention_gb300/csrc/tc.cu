@@ -334,7 +334,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
   const WaitCtx wctx{abort_flag, prm.status};
   constexpr uint32_t S_COL = 256;              // S~ of block fb at S_COL + 128 fb; P at 0
 
-  FAVOR_TRACE_BEGIN();
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NS; ++i) {
       mbar_init(&full[i], 1);
@@ -454,7 +453,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
       for (int j = 0; j < 2; ++j) {
         const int r = (warp - 2) * 64 + lane + 32 * j;
         norm_s[st * kBM + r] = tile_row_sq_to_f16<D>(kt, r);
-        FAVOR_TRACE_POINT(10 + j);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -493,17 +491,14 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
         uint32_t x[64];
         tmem_ld64(tmem + lane_off + my_fb * kFB + c0 + 64 * ps, x);
         tmem_ld_wait();
-        FAVOR_TRACE_POINT(1);
         if (ps == kPasses - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&p_free[my_fb]);
         }
         feature_pack<FM>(x, c1, bias);
-        FAVOR_TRACE_POINT(2);
         if (ps == 0 && i >= 1 && !mbar_wait(&phi_free[my_fb], (i - 1) & 1, wctx)) { ok = false; break; }
         store_row<32>(phi_a, kAtom, t, c0 + 64 * ps, x);
-        FAVOR_TRACE_POINT(3);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -534,10 +529,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
       }
     }
     tc_fence_before();
-    FAVOR_TRACE_POINT(20);
     if (prm.merge) {
       named_bar(1, kEpiThreads);
-      FAVOR_TRACE_POINT(21);
       if (threadIdx.x == kEpiTid0) {
         __threadfence();
         const uint32_t old = atomicAdd(&prm.counters[bh], 1u);
@@ -554,7 +547,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
   // split.  Item = (block b, state row n, 4 consecutive features).
   if (prm.merge && *is_last) {
     __threadfence();
-    FAVOR_TRACE_POINT(23);
     uint8_t* img = prm.state_img + (size_t)bh * M * (D + 16) * 2;
     constexpr int NG = kFB / 4;
     constexpr int kItems = NFB * (D + 16) * NG;
@@ -593,18 +585,19 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
         *reinterpret_cast<uint2*>(img + off) = make_uint2(pack_bf16(acc[u].x, acc[u].y), pack_bf16(acc[u].z, acc[u].w));
       }
     }
-    FAVOR_TRACE_POINT(24);
     if (threadIdx.x == 0) prm.counters[bh] = 0;
   }
-  FAVOR_TRACE_END();
 }
 
 // ---------------------------------------------------------------------------
 // bidirectional output kernel: CTA = a run of 128-token tiles of one head.
-// Query row reference: s |q| max_i |w_i| - 20, the largest exponent s w_i.q
-// can take less 20 ("From Performer to Linear Attention", §Simple Derivation:
-// any per-query constant cancels), so every phi(q) <= e^20 and no pass over
-// the projections is needed to find a maximum.
+// Query row reference: the row's largest exponent max_i s w_i.q, read from
+// the projection tile in tensor memory before any feature is formed ("From
+// Performer to Linear Attention", §Simple Derivation: any per-query constant
+// cancels), so the largest phi(q) of every row is exactly 1 whatever the
+// norm of q.  Each warpgroup holds half of a row's projections (one feature
+// block each at m = 256, half the columns at m = 128); the two halves meet
+// in shared memory.
 // ---------------------------------------------------------------------------
 struct OutParams {
   const float* key_ref;    // row-norm maxima (key_reference)
@@ -616,7 +609,6 @@ struct OutParams {
 };
 
 constexpr int kOutThreads = 384;   // warps 0 TMA, 1 MMA, 2-3 norms, 4-11 epilogue
-constexpr float kQueryHeadroom = 20.0f;
 
 template <int D>
 struct OutCfg {
@@ -627,8 +619,8 @@ struct OutCfg {
   static constexpr int kQ = kState + 256 * (D + 16) * 2;
   static constexpr int kPhi = kQ + NSQ * kTileBytes;        // [fb][2 atoms][128][128 B]
   static constexpr int kOut = kPhi + 4 * kAtom;             // output staging tile
-  static constexpr int kNorm = kOut + kTileBytes;           // [NSQ][128] squared query norms
-  static constexpr int kBars = kNorm + NSQ * kBM * 4;
+  static constexpr int kXmax = kOut + kTileBytes;           // [tile parity][warpgroup][128] row maxima
+  static constexpr int kBars = kXmax + 2 * 2 * kBM * 4;
   static constexpr int kSmem = kBars + 512 + 1024;
 };
 
@@ -642,8 +634,8 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBars);
   uint64_t* q_full = bars;                  // [NSQ]
-  uint64_t* q_empty = q_full + C::NSQ;      // [NSQ] MMA commit + every epilogue warp (norm read)
-  uint64_t* qn_full = q_empty + C::NSQ;     // [NSQ] Q in fp16, norms written
+  uint64_t* q_empty = q_full + C::NSQ;      // [NSQ] the tile's last projection has read it
+  uint64_t* qn_full = q_empty + C::NSQ;     // [NSQ] Q rewritten as fp16
   uint64_t* p_full = qn_full + C::NSQ;      // [2] per feature block
   uint64_t* p_free = p_full + 2;            // [2]
   uint64_t* phi_full = p_free + 2;          // [2]
@@ -654,7 +646,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
   uint64_t* done_bar = setup_bar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* qnorm = reinterpret_cast<float*>(sm + C::kNorm);
+  float* xmax = reinterpret_cast<float*>(sm + C::kXmax);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
@@ -664,11 +656,10 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
   const WaitCtx wctx{abort_flag, prm.status};
   const uint32_t o_col[2] = {256u, 384u};   // O accumulators (d + 16 columns each); P at 0
 
-  FAVOR_TRACE_BEGIN();
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NSQ; ++i) {
       mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 1 + kEpiWarps);
+      mbar_init(&q_empty[i], 1);
       mbar_init(&qn_full[i], kNormWarps);
     }
     for (int i = 0; i < 2; ++i) {
@@ -771,7 +762,8 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
       mbar_wait(done_bar, 0, wctx);
     }
   } else if (warp < 2 + kNormWarps) {
-    // squared norms of the Q rows of each stage; Q rewritten as fp16
+    // Q rewritten as fp16 for the projection (its norm is not needed: the
+    // query reference comes from the projections themselves)
     for (int i = 0; i < n_tiles; ++i) {
       const int st = i % C::NSQ;
       if (!mbar_wait(&q_full[st], (i / C::NSQ) & 1, wctx)) break;
@@ -779,7 +771,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int r = (warp - 2) * 64 + lane + 32 * j;
-        qnorm[st * kBM + r] = tile_row_sq_to_f16<D>(qt, r);
+        (void)tile_row_sq_to_f16<D>(qt, r);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -791,8 +783,6 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
     const int t = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const int col0 = wg * 64;                      // this warpgroup's columns of each feature block
-    float R_unused, W;
-    key_reference(prm.key_ref, prm.m, &R_unused, &W);
     const float c1 = feature_c1<FM>(prm.scale);
     const uint32_t out_a = smem_addr(sm + C::kOut);
     bool ok = true;
@@ -833,20 +823,35 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
       }
     };
     for (int i = 0; i < n_tiles; ++i) {
-      const int st = i % C::NSQ;
       const int my_fb = (NFB == 2) ? wg : 0;   // m = 256: warpgroup w owns feature block w
       if (ok) ok = mbar_wait(&p_full[my_fb], i & 1, wctx);
-      if (ok) ok = mbar_wait(&qn_full[st], (i / C::NSQ) & 1, wctx);
-      tc_fence_after();
-      const float qn = qnorm[st * kBM + t];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&q_empty[st]);
-      const float bias = FM == FAVOR_FM_PRF ? (prm.scale * W * sqrtf(qn) - kQueryHeadroom) * kLog2e : 0.f;
       // m = 256: two passes of 64 columns over the owned block; m = 128: the
       // warpgroups split the block's columns
       constexpr int kPasses = (NFB == 2) ? 2 : 1;
       const int c0 = (NFB == 2) ? 0 : col0;
       tc_fence_after();
+      float bias = 0.f;
+      if constexpr (FM == FAVOR_FM_PRF) {
+        // the row's largest projection: this thread's columns, then the
+        // other warpgroup's half through shared memory (parity-buffered by
+        // tile, so a slot is rewritten only after both halves passed the
+        // next tile's barrier)
+        float pm = -INFINITY;
+#pragma unroll
+        for (int ps = 0; ps < kPasses; ++ps) {
+          uint32_t x[64];
+          if (ok) {
+            tmem_ld64(tmem + lane_off + my_fb * kFB + c0 + 64 * ps, x);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 64; ++j) pm = fmaxf(pm, __uint_as_float(x[j]));
+          }
+        }
+        float* xm = xmax + (i & 1) * 2 * kBM;
+        xm[wg * kBM + t] = pm;
+        named_bar(2, kEpiThreads);
+        bias = fmaxf(xm[t], xm[kBM + t]) * c1;
+      }
 #pragma unroll
       for (int ps = 0; ps < kPasses; ++ps) {
         uint32_t x[64];
@@ -877,7 +882,6 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  FAVOR_TRACE_END();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -890,9 +894,14 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
 //   G_fb += phi(K_c)_fb^T [V_c | 1];
 //   [A | O] += phi(Q_c)_fb [phi(K_c)_fb^T | G_s,fb]              (tensor cores)
 // then A's upper triangle is zeroed (diagonal kept), O += A [V_c | 1], and
-// O is divided by its normaliser column.  The query row reference is
-// s |q| max_i |w_i| - 20 (the largest possible exponent less 20), so every
-// phi(q) is at most e^20.
+// O is divided by its normaliser column.  The query row reference is the
+// row's largest exponent max_i s w_i.q ("From Performer to Linear
+// Attention", §Simple Derivation: a per-query constant cancels), so the
+// largest phi(q) of each row is exactly 1 at any input norm.  With one
+// feature block the reference comes from the block's own projection; with
+// two, the chunk's query projections are first issued once for their row
+// maxima alone (the tile X holds one block at a time), then again for the
+// features.
 // ---------------------------------------------------------------------------
 struct CausalParams {
   const float* key_ref;   // row-norm maxima (key_reference)
@@ -917,8 +926,9 @@ struct CausalCfg {
   static constexpr int kKG = kOnes + kOnesBytes;                    // [2 atoms][kKGRows][128 B]
   static constexpr int kPhiQ = kKG + 2 * kKGAtom;                   // [2 atoms][128][128 B]
   static constexpr int kMA = kPhiQ + 2 * kAtom;                     // masked A; also the output staging tile
-  static constexpr int kNorm = kMA + 2 * kAtom;                     // [2 chunks][K, Q][128] floats
-  static constexpr int kBars = kNorm + 2 * 2 * kBM * 4;
+  static constexpr int kNorm = kMA + 2 * kAtom;                     // [2 chunks][128] squared key norms
+  static constexpr int kXmax = kNorm + 2 * kBM * 4;                 // [chunk parity][warpgroup][128] row maxima
+  static constexpr int kBars = kXmax + 2 * 2 * kBM * 4;
   static constexpr int kSmem = kBars + 512 + 1024;
 };
 static_assert(CausalCfg<64>::kSmem <= 232448, "shared memory");
@@ -942,10 +952,15 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
   uint64_t *kg_full = b + 15, *phiq_full = b + 16, *kg_free = b + 17, *phiq_free = b + 18;
   uint64_t *gdone = b + 19;                                          // [feature block]
   uint64_t *a_full = b + 21, *as_full = b + 22, *o_full = b + 23, *o_free = b + 24;
-  uint64_t *setup_bar = b + 25, *done_bar = b + 26;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b + 27);
+  uint64_t *setup_bar = b + 25, *done_bar = b + 26, *pm_full = b + 27;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b + 28);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* norms = reinterpret_cast<float*>(sm + C::kNorm);   // [c&1][K=0/Q=1][128]
+  float* norms = reinterpret_cast<float*>(sm + C::kNorm);   // [c&1][128]
+  float* xmax = reinterpret_cast<float*>(sm + C::kXmax);
+  // the query projections issued for their row maxima alone (two or more
+  // feature blocks, softmax features)
+  constexpr int NPM = (FM == FAVOR_FM_PRF && NFB > 1) ? NFB : 0;
+  constexpr int XS = NPM + 2 * NFB;             // uses of the projection tile X per chunk
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sc = blockIdx.x, bh = blockIdx.y;
@@ -957,7 +972,6 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
   // side, then G_fb at G_COL + fb * GN
   constexpr uint32_t X_COL = 0, A_COL = 128, O_COL = 256, G_COL = 336;
 
-  FAVOR_TRACE_BEGIN();
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2 * C::kSlots; ++i) mbar_init(&b[i], 1);
     for (int i = 0; i < 2; ++i) {
@@ -967,6 +981,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
     }
     mbar_init(pk_full, 1);
     mbar_init(pq_full, 1);
+    mbar_init(pm_full, 1);
     mbar_init(x_free, kEpiWarps);
     mbar_init(kg_full, kEpiWarps);
     mbar_init(phiq_full, kEpiWarps);
@@ -1035,50 +1050,50 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
       const uint32_t kg_a = smem_addr(sm + C::kKG), phiq_a = smem_addr(sm + C::kPhiQ);
       const uint32_t ma_a = smem_addr(sm + C::kMA);
       bool ok = mbar_wait(setup_bar, 0, wctx);
-      const int U = n_chunks * NFB;
       auto ready = [](uint64_t* bar, int parity) { return mbar_test_wait(smem_addr(bar), parity & 1); };
-      // Event-driven issue over five step kinds of u = (chunk, block): P_K(u)
-      // and P_Q(u) share X (P_K(u) after the epilogue copied P_Q(u-1) out,
-      // P_Q(u) after it copied P_K(u) out); G(u) after phi(K)_u and G_s are in
-      // the KG slot; [A|O](u) after G(u) and phi(Q)_u; O += mask(A) V after the
-      // chunk's last [A|O] and the masked tile.  Each kind is probed only once
-      // its predecessor has been issued, so no barrier can be two phases ahead.
+      // Event-driven issue.  The projection tile X is used in a fixed order
+      // per chunk c: [P_M(c, fb) for each block] (query projections for the
+      // row maxima, NPM > 0 only), then P_K(c, fb), P_Q(c, fb) per block;
+      // each use waits until the epilogue copied the previous one out.  G(u)
+      // after phi(K)_u and G_s are in the KG slot; [A|O](u) after G(u) and
+      // phi(Q)_u; O += mask(A) V after the chunk's last [A|O] and the masked
+      // tile.  Each kind is probed only once its predecessor has been issued,
+      // so no barrier can be two phases ahead.
       Watchdog wd(wctx);
-      int npk = 0, npq = 0, ng = 0, nao = 0, noi = 0;
+      int nx = 0, npk = 0, npq = 0, ng = 0, nao = 0, noi = 0;
+      const int n_x = n_chunks * XS;
       while (ok && noi < n_chunks) {
         bool progress = false;
-        // P_K of a chunk's first block waits until the previous chunk's last
+        // a chunk's first use of X waits until the previous chunk's last
         // [A|O] is issued: queued ahead of it, it would delay the scores the
         // epilogue is waiting for
-        if (npk < U && npq == npk && (npk % NFB != 0 || nao >= npk)) {
-          const int c = npk / NFB, fb = npk % NFB;
-          if ((npk == 0 || ready(x_free, 1)) && (fb != 0 || ready(&kn_full[c & 1], c >> 1))) {
+        if (nx < n_x) {
+          const int c = nx / XS, r = nx % XS;
+          const bool is_pm = r < NPM;
+          const int fb = is_pm ? r : (r - NPM) >> 1;
+          const bool is_k = !is_pm && ((r - NPM) & 1) == 0;
+          const bool order_ok = r != 0 || nao >= c * NFB;
+          const bool x_ok = nx == 0 || ready(x_free, (nx - 1) & 1);
+          const bool in_ok = is_k ? ready(&kn_full[c & 1], c >> 1) : ready(&qn_full[c & 1], c >> 1);
+          if (order_ok && x_ok && in_ok) {
             tc_fence_after();
-            const uint64_t a0 = sdesc(ring_a + slot_of(c, 0) * C::kTileBytes, 16, 1024);
+            const uint64_t a0 = sdesc(ring_a + slot_of(c, is_k ? 0 : 1) * C::kTileBytes, 16, 1024);
             const uint64_t b0 = sdesc(om_a + fb * kFB * 128, 16, 1024);
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
               mma_bf16(tmem + X_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
-            mma_commit(pk_full);
-            FAVOR_TRACE_POINT(50);
-            if (fb == NFB - 1) mma_commit(&slot_free[slot_of(c, 0)]);
-            ++npk;
-            progress = true;
-          }
-        }
-        if (npq < npk) {
-          const int c = npq / NFB, fb = npq % NFB;
-          if (ready(x_free, 0) && (fb != 0 || ready(&qn_full[c & 1], c >> 1))) {
-            tc_fence_after();
-            const uint64_t a0 = sdesc(ring_a + slot_of(c, 1) * C::kTileBytes, 16, 1024);
-            const uint64_t b0 = sdesc(om_a + fb * kFB * 128, 16, 1024);
-#pragma unroll
-            for (int k = 0; k < D / 16; ++k)
-              mma_bf16(tmem + X_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
-            mma_commit(pq_full);
-            FAVOR_TRACE_POINT(51);
-            if (fb == NFB - 1) mma_commit(&slot_free[slot_of(c, 1)]);
-            ++npq;
+            if (is_pm) {
+              mma_commit(pm_full);
+            } else if (is_k) {
+              mma_commit(pk_full);
+              if (fb == NFB - 1) mma_commit(&slot_free[slot_of(c, 0)]);
+              ++npk;
+            } else {
+              mma_commit(pq_full);
+              if (fb == NFB - 1) mma_commit(&slot_free[slot_of(c, 1)]);
+              ++npq;
+            }
+            ++nx;
             progress = true;
           }
         }
@@ -1093,7 +1108,6 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
             for (int k = 0; k < kBM / 16; ++k)
               mma_bf16(tmem + G_COL + fb * GN, dadd(a0, kstep_mn(k)), vones_k(b0, k), id_g, true);
             mma_commit(&gdone[fb]);
-            FAVOR_TRACE_POINT(52);
             ++ng;
             progress = true;
           }
@@ -1107,7 +1121,6 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
             for (int k = 0; k < kFB / 16; ++k)
               mma_bf16(tmem + A_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, C::kKGAtom)), id_ao,
                        (fb > 0) || (k > 0));
-            FAVOR_TRACE_POINT(53);
             mma_commit(kg_free);
             mma_commit(phiq_free);
             if (fb == NFB - 1) mma_commit(a_full);
@@ -1123,7 +1136,6 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
           for (int k = 0; k < kBM / 16; ++k)
             mma_bf16(tmem + O_COL, dadd(a0, kstep_k(k, kAtom)), vones_k(b0, k), id_oi, true);
           mma_commit(o_full);
-          FAVOR_TRACE_POINT(54);
           mma_commit(&slot_free[slot_of(noi, 2)]);
           ++noi;
           progress = true;
@@ -1135,10 +1147,10 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
       mbar_wait(done_bar, 0, wctx);
     }
   } else if (warp < 2 + kNormWarps) {
-    // squared row norms of K_c and Q_c (double-buffered by chunk parity);
-    // both tiles rewritten as fp16
+    // squared row norms of K_c (double-buffered by chunk parity); K_c and
+    // Q_c rewritten as fp16
     for (int c = 0; c < n_chunks; ++c) {
-      float* nk = norms + (c & 1) * 2 * kBM;
+      float* nk = norms + (c & 1) * kBM;
       const int ks = (3 * c) % C::kSlots, qs = (3 * c + 1) % C::kSlots;
       if (!mbar_wait(&slot_full[ks], ((3 * c) / C::kSlots) & 1, wctx)) break;
 #pragma unroll
@@ -1153,7 +1165,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int r = (warp - 2) * 64 + lane + 32 * j;
-        nk[kBM + r] = tile_row_sq_to_f16<D>(sm + C::kRing + qs * C::kTileBytes, r);
+        (void)tile_row_sq_to_f16<D>(sm + C::kRing + qs * C::kTileBytes, r);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -1165,8 +1177,8 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
     const int q = warp & 3;
     const int t = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    float R, W;
-    key_reference(prm.key_ref, prm.m, &R, &W);
+    float R, W_unused;
+    key_reference(prm.key_ref, prm.m, &R, &W_unused);
     const float c1 = feature_c1<FM>(prm.scale);
     const float hs2 = 0.5f * prm.scale * prm.scale;
     const uint32_t kg_a = smem_addr(sm + C::kKG), phiq_a = smem_addr(sm + C::kPhiQ);
@@ -1215,7 +1227,6 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
       tmem_ld32(tmem + lane_off + O_COL + wg * 32, v);
       tmem_ld8(tmem + lane_off + O_COL + D, z);
       tmem_ld_wait();
-      FAVOR_TRACE_POINT(41);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free);
@@ -1233,7 +1244,6 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
                      pack_bf16(__uint_as_float(v[o + 4]) * inv, __uint_as_float(v[o + 5]) * inv),
                      pack_bf16(__uint_as_float(v[o + 6]) * inv, __uint_as_float(v[o + 7]) * inv));
       }
-      FAVOR_TRACE_POINT(42);
       fence_proxy_async_smem();
       named_bar(1, kEpiThreads);
       if (threadIdx.x == kEpiTid0 && have && !*abort_flag) {
@@ -1241,10 +1251,42 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
         bulk_commit();
       }
     };
+    // the row's largest query projection, this thread's columns and then
+    // the other warpgroup's half through shared memory (slots parity-buffered
+    // by chunk: a slot is rewritten only after both halves passed the next
+    // chunk's exchange)
+    auto row_max = [&](int c, float pm) {
+      float* xm = xmax + (c & 1) * 2 * kBM;
+      xm[wg * kBM + t] = pm;
+      named_bar(2, kEpiThreads);
+      return fmaxf(xm[t], xm[kBM + t]);
+    };
+    auto max64 = [](const uint32_t (&x)[64]) {
+      float pm = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) pm = fmaxf(pm, __uint_as_float(x[j]));
+      return pm;
+    };
     float bias_q = 0.f;
     for (int c = 0; c < n_chunks; ++c) {
       const bool valid = (tile0 + c) * kBM + t < prm.L;
-      const float* nk = norms + (c & 1) * 2 * kBM;
+      const float* nk = norms + (c & 1) * kBM;
+      if constexpr (NPM > 0) {
+        // P_M(c, fb): the query projections once more, for the row maximum only
+        float pm = -INFINITY;
+        for (int fb = 0; fb < NPM; ++fb) {
+          if (ok) ok = mbar_wait(pm_full, (c * NPM + fb) & 1, wctx);
+          tc_fence_after();
+          uint32_t x[64];
+          tmem_ld64(tmem + lane_off + X_COL + col0, x);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(x_free);
+          pm = fmaxf(pm, max64(x));
+        }
+        bias_q = row_max(c, pm) * c1;
+      }
       for (int fb = 0; fb < NFB; ++fb) {
         const int u = c * NFB + fb;
         // ---- phi(K)_fb and G_s,fb ----
@@ -1259,17 +1301,14 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
           uint32_t x[64];
           tmem_ld64(tmem + lane_off + X_COL + col0, x);
           tmem_ld_wait();
-          FAVOR_TRACE_POINT(30);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(x_free);
           if (ok) feature_pack<FM>(x, c1, bias_k);
-          FAVOR_TRACE_POINT(31);
           if (ok && u >= 1) ok = mbar_wait(kg_free, (u - 1) & 1, wctx);
           if (ok && c >= 1) ok = mbar_wait(&gdone[fb], (c - 1) & 1, wctx);
           tc_fence_after();
           if (ok) store_row<32>(kg_a, C::kKGAtom, t, col0, x);
-          FAVOR_TRACE_POINT(32);
         }
         if (ok) {
           // G_s,fb rows 128 + n for n < D + 8 (rows D + 1 .. stay zero: G's
@@ -1296,7 +1335,6 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
                               pack_bf16(__uint_as_float(hi[2]), __uint_as_float(hi[3])));
           }
         }
-        FAVOR_TRACE_POINT(33);
         tc_fence_before();
         fence_proxy_async_smem();
         __syncwarp();
@@ -1304,14 +1342,9 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
         // the previous chunk's output, deferred so that its MMAs overlap
         if (fb == 0 && c >= 1) {
           out(c - 1);
-          FAVOR_TRACE_POINT(34);
         }
         // ---- phi(Q)_fb ----
         if (ok) ok = mbar_wait(pq_full, u & 1, wctx);
-        if (ok && fb == 0) {
-          ok = mbar_wait(&qn_full[c & 1], (c >> 1) & 1, wctx);
-          bias_q = FM == FAVOR_FM_PRF ? (prm.scale * W * sqrtf(nk[kBM + t]) - kQueryHeadroom) * kLog2e : 0.f;
-        }
         tc_fence_after();
         {
           // loaded even after a failed wait (the kernel is then aborting and the
@@ -1319,15 +1352,14 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
           uint32_t x[64];
           tmem_ld64(tmem + lane_off + X_COL + col0, x);
           tmem_ld_wait();
-          FAVOR_TRACE_POINT(35);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(x_free);
+          // one feature block: the row maximum of this very projection
+          if constexpr (FM == FAVOR_FM_PRF && NPM == 0) bias_q = row_max(c, max64(x)) * c1;
           if (ok) feature_pack<FM>(x, c1, bias_q);
-          FAVOR_TRACE_POINT(36);
           if (ok && u >= 1) ok = mbar_wait(phiq_free, (u - 1) & 1, wctx);
           if (ok) store_row<32>(phiq_a, kAtom, t, col0, x);
-          FAVOR_TRACE_POINT(37);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -1340,11 +1372,9 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
         uint32_t a[64];
         tmem_ld64(tmem + lane_off + A_COL + col0, a);
         tmem_ld_wait();
-        FAVOR_TRACE_POINT(38);
         tc_fence_before();
         if (threadIdx.x == kEpiTid0 && c >= 1) bulk_wait_read0();
         named_bar(1, kEpiThreads);
-        FAVOR_TRACE_POINT(39);
         if (ok) {
           // this warp's rows 32q .. 32q+31 against columns col0 .. col0+63:
           // entirely kept, entirely masked, or on the diagonal
@@ -1364,7 +1394,6 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
           }
           store_row<32>(ma_a, kAtom, t, col0, a);
         }
-        FAVOR_TRACE_POINT(40);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -1377,7 +1406,6 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  FAVOR_TRACE_END();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -1537,28 +1565,3 @@ cudaError_t tc_output(bool causal, const void* Q, const void* K, const void* V, 
 }
 
 }  // namespace favor
-
-#ifdef FAVOR_WAIT_DIAG
-// Diagnostic builds only: copies the per-warp records of timed-out waits.
-extern "C" int favor_debug_wait_diag(int* out) {
-  return (int)cudaMemcpyFromSymbol(out, favor::tc::g_favor_wait_diag, sizeof(int) * 256 * 4);
-}
-#endif
-
-#ifdef FAVOR_TRACE
-// Diagnostic builds only: reset and copy the wait log of block (0, 0, 0).
-extern "C" int favor_debug_trace_reset(int target_block) {
-  int zero[16] = {0};
-  cudaError_t e = cudaMemcpyToSymbol(favor::tc::g_favor_trace_target, &target_block, sizeof(int));
-  if (e != cudaSuccess) return (int)e;
-  return (int)cudaMemcpyToSymbol(favor::tc::g_favor_trace_n, zero, sizeof(zero));
-}
-extern "C" int favor_debug_cta_times(void* out) {
-  return (int)cudaMemcpyFromSymbol(out, favor::tc::g_favor_cta_times, sizeof(favor::tc::g_favor_cta_times));
-}
-extern "C" int favor_debug_trace(void* recs, int* counts) {
-  cudaError_t e = cudaMemcpyFromSymbol(counts, favor::tc::g_favor_trace_n, sizeof(int) * 16);
-  if (e != cudaSuccess) return (int)e;
-  return (int)cudaMemcpyFromSymbol(recs, favor::tc::g_favor_trace, sizeof(favor::tc::g_favor_trace));
-}
-#endif

@@ -63,21 +63,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-#ifdef FAVOR_WAIT_DIAG
-// Diagnostic builds only: the first wait of each warp that ran out records
-// (shared-memory offset of the barrier >> 3, parity, warp, block).
-__device__ int g_favor_wait_diag[256][4];
-__device__ __forceinline__ void favor_wait_diag_record(uint32_t bar, uint32_t parity) {
-  const int w = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0 && blockIdx.x + blockIdx.y + blockIdx.z == 0 && w < 256 &&
-      atomicCAS(&g_favor_wait_diag[w][3], 0, 1) == 0) {
-    g_favor_wait_diag[w][0] = (int)(bar >> 3);
-    g_favor_wait_diag[w][1] = (int)parity;
-    g_favor_wait_diag[w][2] = w;
-  }
-}
-#endif
-
 // Shared abort flag + error status: every wait in a kernel is bounded; the
 // first wait that runs out raises the flag (other waits then return at once)
 // and records FAVOR_ERR_TIMEOUT.  Returns true when the phase completed.
@@ -86,89 +71,16 @@ struct WaitCtx {
   int32_t* status;            // caller's device status (nullable)
 };
 
-#ifdef FAVOR_TRACE
-// Diagnostic builds only: every completed wait of lane 0 of each warp of
-// block (0, 0, 0) is logged as (clock at entry, clock at completion, barrier
-// shared-memory address, parity), so that a kernel's timeline can be rebuilt.
-constexpr int kTraceMax = 4096;
-struct TraceRec {
-  unsigned long long t0, t1;
-  unsigned bar, parity;
-};
-__device__ int g_favor_trace_n[16];
-__device__ TraceRec g_favor_trace[16][kTraceMax];
-// per-warp record counts of the traced block live in shared memory (a global
-// counter would add a load round trip to every event)
-__device__ __forceinline__ int* trace_counts() {
-  __shared__ int s_trace_n[16];
-  return s_trace_n;
-}
-__device__ int g_favor_trace_target;   // linear id of the traced block
-__device__ __forceinline__ bool trace_block() {
-  return (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x == g_favor_trace_target;
-}
-__device__ __forceinline__ void trace_wait(uint32_t bar, uint32_t parity, unsigned long long t0) {
-  if ((threadIdx.x & 31) == 0 && trace_block()) {
-    const unsigned long long t1 = static_cast<unsigned long long>(clock64());
-    const int w = threadIdx.x >> 5;
-    const int n = trace_counts()[w]++;
-    if (n < kTraceMax) g_favor_trace[w][n] = TraceRec{t0, t1, bar, parity};
-  }
-}
-// start and end (%globaltimer) of every block of the traced launch
-__device__ unsigned long long g_favor_cta_times[4096][2];
-__device__ __forceinline__ int trace_block_id() {
-  return (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-}
-// kernel entry (before the first block-wide barrier) and exit (after the last)
-#define FAVOR_TRACE_BEGIN()                                              \
-  do {                                                                   \
-    if (threadIdx.x < 16) trace_counts()[threadIdx.x] = 0;               \
-    if (threadIdx.x == 0 && trace_block_id() < 4096) g_favor_cta_times[trace_block_id()][0] = global_timer(); \
-  } while (0)
-#define FAVOR_TRACE_END()                                                \
-  do {                                                                   \
-    if (threadIdx.x < 16 && trace_block()) g_favor_trace_n[threadIdx.x] = trace_counts()[threadIdx.x]; \
-    if (threadIdx.x == 0 && trace_block_id() < 4096) g_favor_cta_times[trace_block_id()][1] = global_timer(); \
-  } while (0)
-#define FAVOR_TRACE_DONE(a, parity, t0) trace_wait(a, parity, t0)
-// a point event: logged like a wait of zero length on "barrier" 0xF0000000 | id
-#define FAVOR_TRACE_POINT(id)                                                                     \
-  do {                                                                                            \
-    const unsigned long long tp_ = static_cast<unsigned long long>(clock64());                    \
-    trace_wait(0xF0000000u | (id), 0u, tp_);                                                      \
-  } while (0)
-#else
-#define FAVOR_TRACE_DONE(a, parity, t0) ((void)(t0))
-#define FAVOR_TRACE_POINT(id) ((void)0)
-#define FAVOR_TRACE_BEGIN() ((void)0)
-#define FAVOR_TRACE_END() ((void)0)
-#endif
-
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& ctx) {
   const uint32_t a = smem_addr(bar);
-#ifdef FAVOR_TRACE
-  const unsigned long long tt0 = clock64();
-#else
-  const unsigned long long tt0 = 0;
-#endif
-  if (mbar_try_wait(a, parity)) {
-    FAVOR_TRACE_DONE(a, parity, tt0);
-    return true;
-  }
+  if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer();
   while (true) {
-    if (mbar_try_wait(a, parity)) {
-      FAVOR_TRACE_DONE(a, parity, tt0);
-      return true;
-    }
+    if (mbar_try_wait(a, parity)) return true;
     if (*ctx.abort_flag) return false;
     if (global_timer() - t0 > kWaitLimitNs) {
       *ctx.abort_flag = 1;
       report_status(ctx.status, FAVOR_ERR_TIMEOUT);
-#ifdef FAVOR_WAIT_DIAG
-      favor_wait_diag_record(a, parity);
-#endif
       return false;
     }
   }

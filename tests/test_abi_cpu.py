@@ -112,16 +112,22 @@ def test_product_code_does_not_touch_the_oracle():
 def test_decode_rejects_bad_arguments_before_launch(lib):
     # favor_decode_step(q, k, v, o, B, H, d, omega, m, dt, s, state, status, stream)
     def step(**kw):
-        a = dict(q=16, k=16, v=16, o=32, B=1, H=1, d=8, omega=48, m=8, dt=0, s=1.0, state=64, st=None, stream=None)
+        # fake, never dereferenced addresses: q, k, v, o 32 bytes each, the state (d + 1) m 4 = 288
+        a = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, B=1, H=1, d=8, omega=0x5000, m=8, dt=0, s=1.0,
+                 state=0x10000, st=None, stream=None)
         a.update(kw)
         return lib.favor_decode_step(a["q"], a["k"], a["v"], a["o"], a["B"], a["H"], a["d"], a["omega"], a["m"],
                                      a["dt"], a["s"], a["state"], a["st"], a["stream"])
     assert step(q=None) == 1
     assert step(state=None) == 1
     assert step(omega=None) == 1
-    assert step(o=16) == 1            # o aliases q
-    assert step(o=64) == 1            # o aliases the state
-    assert step(q=24) == 1            # misaligned
+    assert step(o=0x1000) == 1        # o aliases q
+    assert step(o=0x10000) == 1       # o aliases the state
+    assert step(o=0x1010) == 1        # o overlaps the end of q
+    assert step(q=0x10000) == 1       # q aliases the state
+    assert step(k=0x10010) == 1       # k inside the state
+    assert step(v=0x10000 + 288 - 16) == 1    # v overlaps the end of the state
+    assert step(q=0x1008) == 1        # misaligned
     assert step(d=129) == 2
     assert step(m=513) == 2
     assert step(B=0) == 1

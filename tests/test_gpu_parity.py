@@ -180,6 +180,27 @@ def test_workload_full_size_sampled_rows(cuda_lib, name):
     assert err < TOL[w.torch_dtype], (name, err)
 
 
+@pytest.mark.parametrize("name", ["causal-bf16-B4H8L8192-d64-m256", "causal-bf16-B2H8L12288-d64-m256"])
+def test_causal_full_size_chunk_boundaries(cuda_lib, name):
+    # every 128-token chunk boundary of one head (rows 128k - 1 and 128k),
+    # so every superchunk boundary and the last tile of every superchunk
+    # are checked at the full workload size, whatever the split
+    w = wl.get(name)
+    Q, K, V = (t.cuda() for t in wl.make_qkv(w))
+    om = cuda_lib.new_omega(wl.omega_seed_for_call(w, 0), w.m, w.d)
+    st = _status()
+    O = _run(cuda_lib, True, Q, K, V, om, w.qk_scale, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    BH = w.B * w.H
+    h = BH // 2 + 1
+    rows = sorted({0, w.L - 1} | {t for k in range(1, w.L // 128) for t in (128 * k - 1, 128 * k)})
+    q3, k3, v3, o3 = (X.view(BH, w.L, w.d)[h:h + 1] for X in (Q, K, V, O))
+    ref = orc.favor_rows(to_np(q3), to_np(k3), to_np(v3), to_np(om), w.qk_scale, [(0, t) for t in rows], True)
+    got = to_np(o3[0])[rows]
+    assert orc.rowwise_rel_err(got, ref) < TOL[torch.bfloat16], name
+
+
 @pytest.mark.parametrize("m", [128, 256])
 def test_causal_multichunk_walk(cuda_lib, m):
     # B*H = 128 heads of 512 tokens: one superchunk per head walks 4 chunks
@@ -287,22 +308,31 @@ def test_stage_calls_equal_full_call(cuda_lib):
         assert torch.equal(full, staged)
 
 
-@pytest.mark.parametrize("dtype,q_mult,k_mult", [(torch.float32, 8.0, 3.0), (torch.bfloat16, 2.0, 2.0)])
-def test_large_norm_inputs_stay_finite(cuda_lib, dtype, q_mult, k_mult):
-    # queries 8x the unit scale: s w.q reaches ~100, beyond exp's fp32 range
-    # without the per-row stabiliser; keys scaled too.  (The bf16 path rounds
-    # Omega to bf16, an error that grows with |q|, so it runs at 2x.)
-    w = wl.Workload("p", "bidir", "f32" if dtype == torch.float32 else "bf16", 1, 2, 1024, 64, 256, "normal")
+@pytest.mark.parametrize("dtype,q_mult,k_mult,m", [
+    (torch.float32, 8.0, 3.0, 256), (torch.bfloat16, 8.0, 3.0, 256), (torch.bfloat16, 8.0, 3.0, 128),
+    (torch.bfloat16, 1.0, 4.0, 256), (torch.bfloat16, 1.0, 4.0, 128)])
+def test_large_norm_inputs_stay_finite(cuda_lib, dtype, q_mult, k_mult, m):
+    # queries 8x the unit scale: s w.q reaches ~60 and differs from the
+    # Cauchy-Schwarz bound s |q| max|w| by ~160, so a query reference taken
+    # from that bound would underflow every feature; the per-row maximum
+    # keeps the largest feature at 1.  Keys 3x or 4x the unit scale: their
+    # largest features fall to ~e^-40 under the data-free key reference.
+    # m = 128 (one feature block) and m = 256 (two) take different routes
+    # to the row maximum in the causal kernel.
+    w = wl.Workload("p", "bidir", "f32" if dtype == torch.float32 else "bf16", 1, 2, 1024, 64, m, "normal")
     Q, K, V = (t.cuda() for t in wl.make_qkv(w, seed=10))
     Q = (Q.float() * q_mult).to(dtype)
     K = (K.float() * k_mult).to(dtype)
     om = cuda_lib.new_omega(10, w.m, w.d)
     for causal in (False, True):
-        O = _run(cuda_lib, causal, Q, K, V, om, w.qk_scale)
+        st = _status()
+        O = _run(cuda_lib, causal, Q, K, V, om, w.qk_scale, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
         fn = orc.favor_causal_quadratic if causal else orc.favor_bidirectional
         ref = fn(to_np(Q), to_np(K), to_np(V), to_np(om), w.qk_scale)
         assert np.all(np.isfinite(ref))
-        assert orc.rowwise_rel_err(to_np(O), ref) < TOL[dtype]
+        assert orc.rowwise_rel_err(to_np(O), ref) < TOL[dtype], causal
 
 
 def test_dev_status_flags_nonfinite_normaliser(cuda_lib):

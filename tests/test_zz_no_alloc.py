@@ -81,3 +81,36 @@ def test_static_scratch_rejects_oversized_shapes(cuda_lib):
                                       om.data_ptr(), m, 1, ctypes.c_float(0.35), status.data_ptr(), None)
     assert code == 2                                # FAVOR_ERR_UNSUPPORTED, nothing launched
     assert np.all(to_np(small) == 0)
+
+
+def test_static_scratch_at_its_limit(cuda_lib):
+    # the largest head count whose scratch fits the fixed array (the array's
+    # tail in use) runs and matches favor_fwd_bidir; one head more is rejected
+    lib = cuda_lib.load()
+    limit = lib.favor_static_scratch_bytes()
+    B, L, d, m = 1, 300, 64, 256
+    need = {H: lib.favor_workspace_bytes(0, B, H, L, d, m, 1) for H in range(1, 4097)}
+    fits = [H for H, n in need.items() if 0 < n <= limit]
+    H = max(fits)
+    assert need[H] > 0.9 * limit, (H, need[H], limit)
+    assert need[H + 1] > limit
+    w = wl.Workload("static", "bidir", "bf16", B, H, L, d, m, "normal")
+    Q, K, V = (t.cuda() for t in wl.make_qkv(w, seed=21))
+    om = cuda_lib.new_omega(21, m, d)
+    ws = cuda_lib.new_workspace(False, B, H, L, d, m, torch.bfloat16)
+    ref = cuda_lib.fwd_bidir(Q, K, V, om, w.qk_scale, ws).clone()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    O = torch.full_like(Q, float("nan"))
+    code = _static_call(lib, Q, K, V, O, om, w.qk_scale, status)
+    torch.cuda.synchronize()
+    assert code == 0, cuda_lib.status_string(code)
+    assert int(status.item()) == 0
+    assert orc.rowwise_rel_err(to_np(O), to_np(ref)) < TOL[torch.bfloat16]
+    # one head more: rejected before anything is launched, O untouched
+    w2 = w.with_(H=H + 1)
+    Q2, K2, V2 = (t.cuda() for t in wl.make_qkv(w2, seed=22))
+    O2 = torch.zeros_like(Q2)
+    code = _static_call(lib, Q2, K2, V2, O2, om, w.qk_scale, status)
+    torch.cuda.synchronize()
+    assert code == 2
+    assert torch.count_nonzero(O2).item() == 0
