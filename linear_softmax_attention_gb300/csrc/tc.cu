@@ -36,21 +36,12 @@
 #include <mutex>
 
 #include "tc.cuh"
-#include "tc_ptx.cuh"
+#include "tc_util.cuh"
 
 namespace favor {
 namespace {
 
 using namespace tc;
-
-constexpr int kBM = 128;          // tokens per tile
-constexpr int kFB = 128;          // features per block
-constexpr uint32_t kTmemCols = 512;
-constexpr int kAtom = 128 * 128;  // bytes of one [128 rows][128 B] swizzle block
-constexpr int kEpiWarps = 8;
-constexpr int kEpiThreads = 256;
-constexpr int kEpiTid0 = 128;   // first epilogue thread (warps 4-11)
-constexpr int kNormWarps = 2;
 
 // ---------------------------------------------------------------------------
 // workspace layout of the tensor-core path
@@ -64,27 +55,6 @@ struct TcPlan {
   int sub_per_sc;                    // causal: state sub-splits per superchunk
   size_t off_omega_img, off_counters, off_partS, off_state_img, bytes;
 };
-
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-// Splits of `tiles` tiles for each of `units` independent rows of CTAs: the
-// fewest splits minimising waves x (tiles per CTA + per-CTA set-up, counted
-// as kCtaOverheadTiles tiles).
-constexpr int kCtaOverheadTiles = 3;
-int pick_split(int units, int tiles, int sms) {
-  int best = 1;
-  long best_cost = -1;
-  for (int s = 1; s <= tiles; ++s) {
-    const long ctas = (long)units * s;
-    const long waves = (ctas + sms - 1) / sms;
-    const long cost = waves * ((tiles + s - 1) / s + kCtaOverheadTiles);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best = s;
-    }
-  }
-  return best;
-}
 
 TcPlan tc_plan(bool causal, const Shape& s) {
   TcPlan p{};
@@ -135,141 +105,6 @@ TcPlan tc_plan(bool causal, const Shape& s) {
   return p;
 }
 
-// ---------------------------------------------------------------------------
-// shared device pieces
-// ---------------------------------------------------------------------------
-
-// Squared norm of row t of a [128][D] bf16 tile stored as 64-column swizzle
-// blocks (TMA layout); the row is rewritten in place as fp16 (round to
-// nearest, saturating at +-65504) for the projection MMA.  A key whose
-// entries reach the fp16 limit has |s k|^2 / 2 so far above any projection
-// that its feature is 0 in fp32 either way.
-template <int D>
-__device__ __forceinline__ float tile_row_sq_to_f16(uint8_t* tile, int t) {
-  constexpr int NC = D / 8;                     // 16-byte chunks per row
-  uint4 v[NC];
-#pragma unroll
-  for (int c = 0; c < NC; ++c)
-    v[c] = *reinterpret_cast<const uint4*>(tile + (c >> 3) * kAtom + t * 128 + (((c & 7) ^ (t & 7)) << 4));
-  float acc = 0.f;
-#pragma unroll
-  for (int c = 0; c < NC; ++c) {
-    const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float lo = __uint_as_float(w[j] << 16);
-      const float hi = __uint_as_float(w[j] & 0xFFFF0000u);
-      acc = fmaf(lo, lo, acc);
-      acc = fmaf(hi, hi, acc);
-      o[j] = pack_f16_sat(lo, hi);
-    }
-    v[c] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-#pragma unroll
-  for (int c = 0; c < NC; ++c)
-    *reinterpret_cast<uint4*>(tile + (c >> 3) * kAtom + t * 128 + (((c & 7) ^ (t & 7)) << 4)) = v[c];
-  return acc;
-}
-
-// tcgen05.ld 32x32b.x32 into r[OFF .. OFF+31]
-template <int OFF, int N>
-__device__ __forceinline__ void tmem_ld32_at(uint32_t taddr, uint32_t (&r)[N]) {
-  static_assert(OFF + 32 <= N, "range");
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[OFF + 0]), "=r"(r[OFF + 1]), "=r"(r[OFF + 2]), "=r"(r[OFF + 3]), "=r"(r[OFF + 4]), "=r"(r[OFF + 5]),
-        "=r"(r[OFF + 6]), "=r"(r[OFF + 7]), "=r"(r[OFF + 8]), "=r"(r[OFF + 9]), "=r"(r[OFF + 10]), "=r"(r[OFF + 11]),
-        "=r"(r[OFF + 12]), "=r"(r[OFF + 13]), "=r"(r[OFF + 14]), "=r"(r[OFF + 15]), "=r"(r[OFF + 16]),
-        "=r"(r[OFF + 17]), "=r"(r[OFF + 18]), "=r"(r[OFF + 19]), "=r"(r[OFF + 20]), "=r"(r[OFF + 21]),
-        "=r"(r[OFF + 22]), "=r"(r[OFF + 23]), "=r"(r[OFF + 24]), "=r"(r[OFF + 25]), "=r"(r[OFF + 26]),
-        "=r"(r[OFF + 27]), "=r"(r[OFF + 28]), "=r"(r[OFF + 29]), "=r"(r[OFF + 30]), "=r"(r[OFF + 31])
-      : "r"(taddr));
-}
-// 64 consecutive columns into r[0 .. 63]
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
-  tmem_ld32_at<0>(taddr, r);
-  tmem_ld32_at<32>(taddr + 32, r);
-}
-
-// In place: x[j] = bf16x2(2^(x[2j] c1 - b), 2^(x[2j+1] c1 - b)) for j < N/2
-// (zeros if !valid).
-template <int N>
-__device__ __forceinline__ void exp_pack(uint32_t (&x)[N], float c1, float b, bool valid) {
-#pragma unroll
-  for (int j = 0; j < N / 2; ++j) {
-    const float y0 = valid ? ex2(fmaf(__uint_as_float(x[2 * j]), c1, -b)) : 0.f;
-    const float y1 = valid ? ex2(fmaf(__uint_as_float(x[2 * j + 1]), c1, -b)) : 0.f;
-    x[j] = pack_bf16(y0, y1);
-  }
-}
-
-// Feature maps: positive random features (the softmax kernel) or
-// Performer-ReLU, relu(s w.x) ("Rethinking Attention with Performers"
-// summary, §2 generalized kernelizable attention: other kernels by changing
-// the feature-map function).  ReLU: b = 0 on valid rows and +inf past the
-// sequence end (feature 0); "y < 0 ? 0 : y" keeps a NaN a NaN.
-template <int N>
-__device__ __forceinline__ void relu_pack(uint32_t (&x)[N], float c1, float b) {
-#pragma unroll
-  for (int j = 0; j < N / 2; ++j) {
-    float y0 = fmaf(__uint_as_float(x[2 * j]), c1, -b);
-    float y1 = fmaf(__uint_as_float(x[2 * j + 1]), c1, -b);
-    y0 = y0 < 0.f ? 0.f : y0;
-    y1 = y1 < 0.f ? 0.f : y1;
-    x[j] = pack_bf16(y0, y1);
-  }
-}
-template <int FM, int N>
-__device__ __forceinline__ void feature_pack(uint32_t (&x)[N], float c1, float b) {
-  if constexpr (FM == FAVOR_FM_PRF) exp_pack<N>(x, c1, b, true);
-  else relu_pack<N>(x, c1, b);
-}
-// multiplier of the projection in the feature exponent / argument
-template <int FM>
-__device__ __forceinline__ float feature_c1(float scale) {
-  return FM == FAVOR_FM_PRF ? scale * kLog2e : scale;
-}
-
-// Row t, columns col0 .. col0 + 2*NW - 1 (col0 a multiple of 8) of a tile of
-// 64-column swizzle blocks `atom_stride` bytes apart, from NW packed words.
-template <int NW, int N>
-__device__ __forceinline__ void store_row(uint32_t base, int atom_stride, int t, int col0, const uint32_t (&x)[N]) {
-#pragma unroll
-  for (int c = 0; c < NW / 4; ++c) {
-    const int col = col0 + 8 * c;
-    const int atom = col >> 6, chunk = (col & 63) >> 3;
-    st_shared_v4(base + atom * atom_stride + t * 128 + ((chunk ^ (t & 7)) << 4), x[4 * c], x[4 * c + 1],
-                 x[4 * c + 2], x[4 * c + 3]);
-  }
-}
-
-// Constant [16 rows][128 B] block, MN-major swizzled: element 0 of every
-// row is 1, the rest 0.  Read as columns d .. d+15 of [V | 1] by every k-step
-// (each MMA's leading-byte offset points back to it).
-constexpr int kOnesBytes = 16 * 128;
-__device__ __forceinline__ void fill_ones_block(uint8_t* p, int tid0, int nthreads) {
-  for (int e = threadIdx.x - tid0; e < kOnesBytes / 16; e += nthreads) {
-    const int row = e >> 3, logical = (e & 7) ^ (row & 7);
-    *reinterpret_cast<uint4*>(p + e * 16) = make_uint4(logical == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
-  }
-}
-
-// Descriptor arithmetic.  A descriptor's start-address field holds bytes >> 4
-// in its low bits, so a k-step is an add to the base descriptor built once
-// per MMA group (rebuilding it per MMA costs the issuing thread ~40 issue
-// slots, which halves the MMA rate when epilogue warps share its SMSP).
-__device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
-// K-major SW128: k-step k (16 elements) within 64-element atoms `atom` bytes apart
-__host__ __device__ constexpr uint32_t kstep_k(int k, int atom) { return (k >> 2) * atom + (k & 3) * 32; }
-// MN-major SW128: k-step k is 16 rows of 128 B
-__host__ __device__ constexpr uint32_t kstep_mn(int k) { return k * 2048; }
-// [V | 1] at k-step k: start advances by 2048 k, the offset back to the ones
-// block shrinks by the same amount
-__device__ __forceinline__ uint64_t vones_k(uint64_t d0, int k) {
-  return d0 + static_cast<uint64_t>(k * 128) - (static_cast<uint64_t>(k * 128) << 16);
-}
 
 // ---------------------------------------------------------------------------
 // state kernel: one (token split, head) per CTA, all m features.
@@ -897,11 +732,13 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
 // O is divided by its normaliser column.  The query row reference is the
 // row's largest exponent max_i s w_i.q ("From Performer to Linear
 // Attention", §Simple Derivation: a per-query constant cancels), so the
-// largest phi(q) of each row is exactly 1 at any input norm.  With one
-// feature block the reference comes from the block's own projection; with
-// two, the chunk's query projections are first issued once for their row
-// maxima alone (the tile X holds one block at a time), then again for the
-// features.
+// largest phi(q) of each row is at least 1 at any input norm.  The tile X
+// holds one feature block at a time, so the reference is block 0's row
+// maximum c_0; a later block whose maximum c_b exceeds the reference by more
+// than 20 nats (its features would pass e^20) moves the row's reference to
+// c_b, and the row's accumulated A and O are first scaled by
+// exp(c_ref - c_b) in tensor memory (the previous [A|O] step is complete by
+// then: phi(Q) has a single buffer).
 // ---------------------------------------------------------------------------
 struct CausalParams {
   const float* key_ref;   // row-norm maxima (key_reference)
@@ -952,15 +789,12 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
   uint64_t *kg_full = b + 15, *phiq_full = b + 16, *kg_free = b + 17, *phiq_free = b + 18;
   uint64_t *gdone = b + 19;                                          // [feature block]
   uint64_t *a_full = b + 21, *as_full = b + 22, *o_full = b + 23, *o_free = b + 24;
-  uint64_t *setup_bar = b + 25, *done_bar = b + 26, *pm_full = b + 27;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b + 28);
+  uint64_t *setup_bar = b + 25, *done_bar = b + 26;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b + 27);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* norms = reinterpret_cast<float*>(sm + C::kNorm);   // [c&1][128]
   float* xmax = reinterpret_cast<float*>(sm + C::kXmax);
-  // the query projections issued for their row maxima alone (two or more
-  // feature blocks, softmax features)
-  constexpr int NPM = (FM == FAVOR_FM_PRF && NFB > 1) ? NFB : 0;
-  constexpr int XS = NPM + 2 * NFB;             // uses of the projection tile X per chunk
+  constexpr int XS = 2 * NFB;                   // uses of the projection tile X per chunk
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sc = blockIdx.x, bh = blockIdx.y;
@@ -981,7 +815,6 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
     }
     mbar_init(pk_full, 1);
     mbar_init(pq_full, 1);
-    mbar_init(pm_full, 1);
     mbar_init(x_free, kEpiWarps);
     mbar_init(kg_full, kEpiWarps);
     mbar_init(phiq_full, kEpiWarps);
@@ -1052,9 +885,8 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
       bool ok = mbar_wait(setup_bar, 0, wctx);
       auto ready = [](uint64_t* bar, int parity) { return mbar_test_wait(smem_addr(bar), parity & 1); };
       // Event-driven issue.  The projection tile X is used in a fixed order
-      // per chunk c: [P_M(c, fb) for each block] (query projections for the
-      // row maxima, NPM > 0 only), then P_K(c, fb), P_Q(c, fb) per block;
-      // each use waits until the epilogue copied the previous one out.  G(u)
+      // per chunk c: P_K(c, fb), P_Q(c, fb) per block; each use waits until
+      // the epilogue copied the previous one out.  G(u)
       // after phi(K)_u and G_s are in the KG slot; [A|O](u) after G(u) and
       // phi(Q)_u; O += mask(A) V after the chunk's last [A|O] and the masked
       // tile.  Each kind is probed only once its predecessor has been issued,
@@ -1069,9 +901,8 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
         // epilogue is waiting for
         if (nx < n_x) {
           const int c = nx / XS, r = nx % XS;
-          const bool is_pm = r < NPM;
-          const int fb = is_pm ? r : (r - NPM) >> 1;
-          const bool is_k = !is_pm && ((r - NPM) & 1) == 0;
+          const int fb = r >> 1;
+          const bool is_k = (r & 1) == 0;
           const bool order_ok = r != 0 || nao >= c * NFB;
           const bool x_ok = nx == 0 || ready(x_free, (nx - 1) & 1);
           const bool in_ok = is_k ? ready(&kn_full[c & 1], c >> 1) : ready(&qn_full[c & 1], c >> 1);
@@ -1082,9 +913,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
               mma_bf16(tmem + X_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
-            if (is_pm) {
-              mma_commit(pm_full);
-            } else if (is_k) {
+            if (is_k) {
               mma_commit(pk_full);
               if (fb == NFB - 1) mma_commit(&slot_free[slot_of(c, 0)]);
               ++npk;
@@ -1251,12 +1080,12 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
         bulk_commit();
       }
     };
-    // the row's largest query projection, this thread's columns and then
-    // the other warpgroup's half through shared memory (slots parity-buffered
-    // by chunk: a slot is rewritten only after both halves passed the next
-    // chunk's exchange)
-    auto row_max = [&](int c, float pm) {
-      float* xm = xmax + (c & 1) * 2 * kBM;
+    // the row's largest query projection in block u, this thread's columns
+    // and then the other warpgroup's half through shared memory (slots
+    // parity-buffered by block step: a slot is rewritten only after both
+    // halves passed the next exchange)
+    auto row_max = [&](int u, float pm) {
+      float* xm = xmax + (u & 1) * 2 * kBM;
       xm[wg * kBM + t] = pm;
       named_bar(2, kEpiThreads);
       return fmaxf(xm[t], xm[kBM + t]);
@@ -1267,26 +1096,21 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
       for (int j = 0; j < 64; ++j) pm = fmaxf(pm, __uint_as_float(x[j]));
       return pm;
     };
+    // the row's reference (largest raw projection so far in log2 units, times c1)
     float bias_q = 0.f;
+    // a later block may exceed the reference by this much before the row is
+    // rescaled: its features stay below e^20
+    const float kRescale = 20.0f * kLog2e;
+    // this warpgroup's columns of A (col0 .. col0 + 63) and of O (32 of the
+    // first 64 and 8 of the last 16; warpgroup 0's 8 hold the normaliser),
+    // each access aligned to its width
+    const uint32_t a_cols = tmem + lane_off + A_COL + col0;
+    const uint32_t o_cols = tmem + lane_off + O_COL + wg * 32;
+    const uint32_t o_tail = tmem + lane_off + O_COL + D + wg * 8;
+    static_assert(GN - D == 16, "O tail");
     for (int c = 0; c < n_chunks; ++c) {
       const bool valid = (tile0 + c) * kBM + t < prm.L;
       const float* nk = norms + (c & 1) * kBM;
-      if constexpr (NPM > 0) {
-        // P_M(c, fb): the query projections once more, for the row maximum only
-        float pm = -INFINITY;
-        for (int fb = 0; fb < NPM; ++fb) {
-          if (ok) ok = mbar_wait(pm_full, (c * NPM + fb) & 1, wctx);
-          tc_fence_after();
-          uint32_t x[64];
-          tmem_ld64(tmem + lane_off + X_COL + col0, x);
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(x_free);
-          pm = fmaxf(pm, max64(x));
-        }
-        bias_q = row_max(c, pm) * c1;
-      }
       for (int fb = 0; fb < NFB; ++fb) {
         const int u = c * NFB + fb;
         // ---- phi(K)_fb and G_s,fb ----
@@ -1355,10 +1179,42 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(x_free);
-          // one feature block: the row maximum of this very projection
-          if constexpr (FM == FAVOR_FM_PRF && NPM == 0) bias_q = row_max(c, max64(x)) * c1;
+          float shrink = 1.f;   // factor on the row's A and O so far (block > 0)
+          if constexpr (FM == FAVOR_FM_PRF) {
+            const float bm = row_max(u, max64(x)) * c1;
+            if (fb == 0) {
+              bias_q = bm;
+            } else if (bm > bias_q + kRescale) {
+              shrink = ex2(bias_q - bm);
+              bias_q = bm;
+            }
+          }
           if (ok) feature_pack<FM>(x, c1, bias_q);
+          // [A|O] of the previous block is complete once phi(Q)'s buffer is free
           if (ok && u >= 1) ok = mbar_wait(phiq_free, (u - 1) & 1, wctx);
+          if (fb > 0 && __any_sync(0xffffffffu, shrink != 1.f)) {
+            tc_fence_after();
+            uint32_t r[32], z8[8];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              tmem_ld32(a_cols + 32 * h, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * shrink);
+              tmem_st32(a_cols + 32 * h, r);
+            }
+            tmem_ld32(o_cols, r);
+            tmem_ld8(o_tail, z8);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * shrink);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) z8[j] = __float_as_uint(__uint_as_float(z8[j]) * shrink);
+            tmem_st32(o_cols, r);
+            tmem_st8(o_tail, z8);
+            tmem_st_wait();
+            tc_fence_before();
+          }
           if (ok) store_row<32>(phiq_a, kAtom, t, col0, x);
         }
         fence_proxy_async_smem();
@@ -1412,34 +1268,6 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// [BH, L, d] bf16 viewed as a 3-D tensor {d, L, BH}; box {64, 128, 1}; 128B swizzle.
-bool make_map(CUtensorMap* map, const void* base, const Shape& s) {
-  auto enc = get_encode();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)s.d, (cuuint64_t)s.L, (cuuint64_t)s.BH()};
-  cuuint64_t strides[2] = {(cuuint64_t)s.d * 2, (cuuint64_t)s.L * s.d * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)kBM, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <int D, int M, int FM>
 cudaError_t launch_state(const void* K, const void* V, const Shape& s, const TcPlan& p, float scale, char* ws,
                          int32_t* status, cudaStream_t stream) {
@@ -1517,12 +1345,14 @@ cudaError_t launch_causal(const void* Q, const void* K, const void* V, void* O, 
 }  // namespace
 
 bool tc_supported(bool causal, int d, int m, bool bf16) {
-  (void)causal;
   if (!bf16) return false;
-  return d == 64 && (m == 128 || m == 256);
+  if (d == 64) return m == 128 || m == 256;
+  return fs_supported(causal, d, m, bf16);
 }
 
-size_t tc_workspace_bytes(bool causal, const Shape& s) { return tc_plan(causal, s).bytes; }
+size_t tc_workspace_bytes(bool causal, const Shape& s) {
+  return s.d == 64 ? tc_plan(causal, s).bytes : fs_workspace_bytes(causal, s);
+}
 
 template <int FM>
 cudaError_t tc_state_fm(bool causal, const void* K, const void* V, const float* omega, float scale, const Shape& s,
@@ -1553,6 +1383,7 @@ cudaError_t tc_output_fm(bool causal, const void* Q, const void* K, const void* 
 
 cudaError_t tc_state(bool causal, const void* K, const void* V, const float* omega, float scale, const Shape& s,
                      void* ws, int32_t* status, cudaStream_t stream, int fm) {
+  if (s.d != 64) return fs_state(causal, K, V, omega, scale, s, ws, status, stream, fm);
   return fm == FAVOR_FM_RELU ? tc_state_fm<FAVOR_FM_RELU>(causal, K, V, omega, scale, s, ws, status, stream)
                              : tc_state_fm<FAVOR_FM_PRF>(causal, K, V, omega, scale, s, ws, status, stream);
 }
@@ -1560,6 +1391,7 @@ cudaError_t tc_state(bool causal, const void* K, const void* V, const float* ome
 cudaError_t tc_output(bool causal, const void* Q, const void* K, const void* V, void* O, const float* omega,
                       float scale, const Shape& s, void* ws, int32_t* status, cudaStream_t stream, int fm) {
   (void)omega;
+  if (s.d != 64) return fs_output(causal, Q, K, V, O, scale, s, ws, status, stream, fm);
   return fm == FAVOR_FM_RELU ? tc_output_fm<FAVOR_FM_RELU>(causal, Q, K, V, O, s, scale, ws, status, stream)
                              : tc_output_fm<FAVOR_FM_PRF>(causal, Q, K, V, O, s, scale, ws, status, stream);
 }

@@ -14,4 +14,12 @@ cudaError_t tc_output(bool causal, const void* Q, const void* K, const void* V, 
                       float scale, const Shape& s, void* ws, int32_t* status, cudaStream_t stream,
                       int fm = FAVOR_FM_PRF);
 
+// d = 128, one feature block per CTA (tc_fs.cu); reached through the calls above
+bool fs_supported(bool causal, int d, int m, bool bf16);
+size_t fs_workspace_bytes(bool causal, const Shape& s);
+cudaError_t fs_state(bool causal, const void* K, const void* V, const float* omega, float scale, const Shape& s,
+                     void* ws, int32_t* status, cudaStream_t stream, int fm);
+cudaError_t fs_output(bool causal, const void* Q, const void* K, const void* V, void* O, float scale, const Shape& s,
+                      void* ws, int32_t* status, cudaStream_t stream, int fm);
+
 }  // namespace favor

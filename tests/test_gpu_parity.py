@@ -148,7 +148,8 @@ def test_small_shapes_match_oracle(cuda_lib, causal, dtype, B, H, L, d, m):
 # the workloads at full size: sampled rows against the oracle
 # ---------------------------------------------------------------------------
 
-FULL = list(wl.WORKLOADS) + [n for n in wl.SWEEP if ("L16384" in n) or ("L65536" in n and "m512" in n)]
+FULL = list(wl.WORKLOADS) + [n for n in wl.SWEEP
+                             if ("L16384" in n) or ("L65536" in n and "m512" in n) or n.startswith("sweep-bidir")]
 
 
 @pytest.mark.parametrize("name", FULL)
