@@ -641,15 +641,23 @@ def measure_configs(favor, args, dev, stream, status, hbm, tc_burst):
             # calls below run on `stream`
             torch.cuda.synchronize(dev)
 
-            def call(i, build):
+            def call(i, build, part="both"):
                 if build:
                     favor.build_orf(wl.omega_seed_for_call(w, i), om, stream=stream)
-                fn(q, k, v, om, w.qk_scale, ws, O=O, dev_status=status, stream=stream)
+                if part == "both":
+                    fn(q, k, v, om, w.qk_scale, ws, O=O, dev_status=status, stream=stream)
+                elif part == "state":
+                    (favor.causal_state if causal else favor.bidir_state)(k, v, om, w.qk_scale, ws,
+                                                                         dev_status=status, stream=stream)
+                elif causal:
+                    favor.causal_output(q, k, v, om, w.qk_scale, ws, O=O, dev_status=status, stream=stream)
+                else:
+                    favor.bidir_output(q, om, w.qk_scale, ws, O=O, dev_status=status, stream=stream)
 
-            def timed(build):
+            def timed(build, part="both"):
                 with torch.cuda.stream(stream):
                     for i in range(3):
-                        call(i, build)
+                        call(i, build, part)
                 torch.cuda.synchronize(dev)
                 evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                        for _ in range(args.config_steps)]
@@ -657,7 +665,7 @@ def measure_configs(favor, args, dev, stream, status, hbm, tc_burst):
                     for i, (e0, e1) in enumerate(evs):
                         flush.fill_(i & 0xFF)
                         e0.record(stream)
-                        call(i + 3, build)
+                        call(i + 3, build, part)
                         e1.record(stream)
                 torch.cuda.synchronize(dev)
                 if int(status.item()) != 0:
@@ -669,7 +677,8 @@ def measure_configs(favor, args, dev, stream, status, hbm, tc_burst):
                     "m": w.m, "path": favor.path_name(causal, w.d, w.m, w.torch_dtype),
                     "value": w.B * w.L / (ms / 1e3), "unit": "tokens/s",
                     "head_tokens_per_s": w.B * w.H * w.L / (ms / 1e3), "ms_per_call": ms,
-                    "calls": args.config_steps, "roofline": call_roofline(w, ms, hbm, tc_burst, alu)}
+                    "calls": args.config_steps, "roofline": call_roofline(w, ms, hbm, tc_burst, alu),
+                    "stage_ms": {"state": timed(False, "state"), "output": timed(False, "output")}}
             if w.redraw_omega:
                 ms_c = timed(False)
                 line["call"] = "favor_build_orf (seed of the call) + favor_fwd_causal, one stream"

@@ -38,10 +38,10 @@
  *    asynchronous on `stream`.  The return value reports argument checks
  *    (made before anything is launched) and launch errors.
  *  - Supported: 1 <= L, 1 <= d <= 128, 1 <= m <= 512, B*H >= 1,
- *    B*H*L*d < 2^31.  bf16 with d = 64 and m in {128, 256}, and the
- *    bidirectional pass with d = 128 and m in {128, 256, 512}, run on the
- *    tcgen05 tensor-core kernels (favor_path_name reports which); every other
- *    supported shape runs on CUDA-core kernels with fp32 arithmetic.
+ *    B*H*L*d < 2^31.  bf16 with d = 64 and m in {128, 256}, or with
+ *    d = 128 and m in {128, 256, 512}, runs on the tcgen05 tensor-core
+ *    kernels (favor_path_name reports which); every other supported shape
+ *    runs on CUDA-core kernels with fp32 arithmetic.
  */
 #ifndef FAVOR_H_
 #define FAVOR_H_

@@ -102,3 +102,105 @@ def test_d128_constant_values_reproduced(cuda_lib):
     O = _bidir(cuda_lib, Q, K, V, om, D ** -0.25).float()
     assert torch.allclose(O, torch.full_like(O, -2.25), rtol=1e-2)
 
+
+# ---------------------------------------------------------------------------
+# causal: a cluster of m / 128 CTAs per superchunk, each carrying its block's
+# rows of the prefix state; partial outputs meet in the workspace
+# ---------------------------------------------------------------------------
+
+def _causal(favor, Q, K, V, om, s, status=None, fm=None):
+    B, H, L, d = Q.shape
+    ws = favor.new_workspace(True, B, H, L, d, om.shape[0], Q.dtype)
+    return favor.fwd_causal(Q, K, V, om, s, ws, dev_status=status, feature_map=fm)
+
+
+@pytest.mark.parametrize("m", [128, 256, 512])
+def test_d128_causal_runs_on_tensor_cores(cuda_lib, m):
+    assert cuda_lib.path_name(True, D, m, torch.bfloat16) == "tcgen05"
+
+
+@pytest.mark.parametrize("fm", ["prf", "relu"])
+@pytest.mark.parametrize("B,H,L,m", [(1, 1, 1, 128), (1, 2, 300, 256), (2, 2, 1000, 512), (1, 1, 4100, 512),
+                                     (3, 1, 777, 128), (1, 3, 2049, 256)])
+def test_d128_causal_matches_oracle(cuda_lib, B, H, L, m, fm):
+    # small B H: many one-chunk superchunks (initial states from the partials)
+    Q, K, V = _inputs(B, H, L, seed=L + m + 3)
+    om = cuda_lib.new_omega(L + m, m, D)
+    s = D ** -0.25
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    O = _causal(cuda_lib, Q, K, V, om, s, st, fm)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    fn = orc.favor_causal if L <= 600 else orc.favor_causal_quadratic
+    ref = fn(to_np(Q), to_np(K), to_np(V), to_np(om), s, fm)
+    assert orc.rowwise_rel_err(to_np(O), ref) < TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("m", [128, 256, 512])
+def test_d128_causal_multichunk_walk(cuda_lib, m):
+    # 64 heads of 1024 tokens: one superchunk per head walks 8 chunks; every
+    # chunk boundary of three heads
+    B, H, L = 4, 16, 1024
+    Q, K, V = _inputs(B, H, L, seed=m + 11)
+    om = cuda_lib.new_omega(m + 11, m, D)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    O = _causal(cuda_lib, Q, K, V, om, D ** -0.25, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    BH = B * H
+    rows = sorted({0, L - 1} | {t for k in range(1, L // 128) for t in (128 * k - 1, 128 * k)})
+    picks = [(h, t) for h in (0, 29, 63) for t in rows]
+    q3, k3, v3, o3 = (X.view(BH, L, D) for X in (Q, K, V, O))
+    ref = orc.favor_rows(to_np(q3), to_np(k3), to_np(v3), to_np(om), D ** -0.25, picks, True)
+    got = np.stack([to_np(o3[h, t]) for h, t in picks])
+    assert orc.rowwise_rel_err(got, ref) < TOL[torch.bfloat16]
+
+
+def test_d128_causal_rows_do_not_see_the_future(cuda_lib):
+    Q, K, V = _inputs(1, 2, 1500, seed=3)
+    om = cuda_lib.new_omega(2, 512, D)
+    base = _causal(cuda_lib, Q, K, V, om, D ** -0.25).clone()
+    t = 700
+    g = torch.Generator(device="cuda").manual_seed(9)
+    for X in (Q, K, V):
+        X[:, :, t + 1:] = torch.randn(X[:, :, t + 1:].shape, generator=g, device="cuda").to(X.dtype)
+    pert = _causal(cuda_lib, Q, K, V, om, D ** -0.25)
+    assert torch.equal(base[:, :, : t + 1], pert[:, :, : t + 1])
+    assert not torch.equal(base[:, :, t + 1:], pert[:, :, t + 1:])
+
+
+@pytest.mark.parametrize("m", [128, 256, 512])
+def test_d128_causal_large_norm_queries(cuda_lib, m):
+    # 6x queries, unit keys.  (Large keys as well leave the first causal
+    # rows, which sum over a handful of keys, with an exact normaliser near
+    # e^-130: outside fp32's range for any fixed reference, flagged as a
+    # non-finite normaliser; the bidirectional test covers 3x keys.)
+    Q, K, V = _inputs(1, 2, 700, seed=m + 5, q_mult=6.0, k_mult=1.0)
+    om = cuda_lib.new_omega(m + 5, m, D)
+    s = D ** -0.25
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    O = _causal(cuda_lib, Q, K, V, om, s, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = orc.favor_causal_quadratic(to_np(Q), to_np(K), to_np(V), to_np(om), s)
+    assert np.all(np.isfinite(ref))
+    assert orc.rowwise_rel_err(to_np(O), ref) < TOL[torch.bfloat16]
+
+
+def test_d128_causal_bitwise_repeatable(cuda_lib):
+    Q, K, V = _inputs(2, 4, 4096, seed=15)
+    om = cuda_lib.new_omega(16, 256, D)
+    a = _causal(cuda_lib, Q, K, V, om, D ** -0.25).clone()
+    b = _causal(cuda_lib, Q, K, V, om, D ** -0.25)
+    assert torch.equal(a, b)
+
+
+def test_d128_causal_stage_calls_equal_full_call(cuda_lib):
+    B, H, L, m = 1, 3, 2000, 512
+    Q, K, V = _inputs(B, H, L, seed=18)
+    om = cuda_lib.new_omega(18, m, D)
+    ws = cuda_lib.new_workspace(True, B, H, L, D, m, torch.bfloat16)
+    full = cuda_lib.fwd_causal(Q, K, V, om, D ** -0.25, ws).clone()
+    cuda_lib.causal_state(K, V, om, D ** -0.25, ws)
+    staged = cuda_lib.causal_output(Q, K, V, om, D ** -0.25, ws)
+    assert torch.equal(full, staged)
