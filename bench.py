@@ -59,6 +59,10 @@ def parse():
                     help="calls timed per configuration line (0: no per-configuration lines)")
     ap.add_argument("--config-cpu-s", type=float, default=1.5,
                     help="seconds of oracle time per configuration line's cpu_baseline (0: none)")
+    ap.add_argument("--call", default=None, metavar="WORKLOAD",
+                    help="only run WORKLOAD's full forward call --calls times and print its mean time "
+                         "(a small driver for profilers)")
+    ap.add_argument("--calls", type=int, default=3)
     return ap.parse_args()
 
 
@@ -917,9 +921,40 @@ def measure_decode(favor, n_steps, stream, status, hbm, dev):
                          "algorithmic_bytes_per_launch": nbytes}}
 
 
+def run_call_only(args):
+    """One workload's public full call (favor_fwd_bidir or favor_fwd_causal),
+    --calls times on the current stream, Omega built once."""
+    import linear_softmax_attention_gb300 as favor
+
+    favor.load()
+    dev = torch.device("cuda", 0)
+    w = workload_for(args.call)
+    causal = w.mode == "causal"
+    q, k, v = wl.make_qkv(w, seed=0, device=dev)
+    om = favor.new_omega(wl.omega_seed_for_call(w, 0), w.m, w.d, device=dev)
+    ws = favor.new_workspace(causal, w.B, w.H, w.L, w.d, w.m, w.torch_dtype, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    fn = favor.fwd_causal if causal else favor.fwd_bidir
+    O = torch.empty_like(q)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record()
+    for _ in range(args.calls):
+        fn(q, k, v, om, w.qk_scale, ws, O=O, dev_status=status)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} on {w.name}")
+    print(json.dumps({"call": w.name, "calls": args.calls, "ms_per_call": e0.elapsed_time(e1) / args.calls,
+                      "path": favor.path_name(causal, w.d, w.m, w.torch_dtype)}))
+
+
 def main():
     args = parse()
     rank, world, local_rank = dist_env()
+    if args.call is not None:
+        run_call_only(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:

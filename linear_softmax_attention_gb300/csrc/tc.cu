@@ -1136,28 +1136,10 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
         }
         if (ok) {
           // G_s,fb rows 128 + n for n < D + 8 (rows D + 1 .. stay zero: G's
-          // columns there are zero).  Per group of 8 columns n, a 16x256b
-          // load per half of this warp's 32 features gives each thread two
-          // adjacent n of one feature; stmatrix.trans turns each 8x8 block
-          // (features x n) into rows n of 8 features, one swizzle chunk each.
-          const int mi = lane >> 3, kr = lane & 7;
-          const int f0 = 32 * q + 8 * mi;                 // first feature of matrix mi
-          const uint32_t row_base = kg_a + (f0 >> 6) * C::kKGAtom + kBM * 128;
-          const int fch = (f0 & 63) >> 3;
-#pragma unroll 1
-          for (int g = g_first; g < g_end; ++g) {
-            uint32_t lo[4], hi[4];
-            const uint32_t col = G_COL + fb * GN + 8 * g;
-            tmem_ld16x256(tmem + (static_cast<uint32_t>(32 * q) << 16) + col, lo);
-            tmem_ld16x256(tmem + (static_cast<uint32_t>(32 * q + 16) << 16) + col, hi);
-            tmem_ld_wait();
-            const int n = 8 * g + kr;
-            stmatrix_x4_trans(row_base + n * 128 + ((fch ^ (n & 7)) << 4),
-                              pack_bf16(__uint_as_float(lo[0]), __uint_as_float(lo[1])),
-                              pack_bf16(__uint_as_float(lo[2]), __uint_as_float(lo[3])),
-                              pack_bf16(__uint_as_float(hi[0]), __uint_as_float(hi[1])),
-                              pack_bf16(__uint_as_float(hi[2]), __uint_as_float(hi[3])));
-          }
+          // columns there are zero), three column groups' loads in flight
+          const int f0 = 32 * q + 8 * (lane >> 3);
+          tmem_state_to_rows<3>(tmem, G_COL + fb * GN, q, lane, g_first, g_end,
+                                kg_a + (f0 >> 6) * C::kKGAtom + kBM * 128);
         }
         tc_fence_before();
         fence_proxy_async_smem();

@@ -80,7 +80,7 @@ FsPlan fs_plan(const Shape& s) {
 struct FsCausalPlan {
   int n_fb, n_tiles;
   int tiles_per_sc, n_sc, sub_per_sc, tiles_per_split, n_split;
-  size_t off_omega_img, off_partS, off_xbuf, bytes;
+  size_t off_omega_img, off_partS, off_pre, off_xbuf, bytes;
 };
 
 constexpr int kXWidth = kD + 4;   // floats per row of the exchange buffer
@@ -114,6 +114,8 @@ FsCausalPlan fsc_plan(const Shape& s) {
   off = align_up(off + (size_t)s.m * s.d * 2, 1024);
   p.off_partS = off;   // fp32 [BH][n_fb][max(n_split, 1)][d+1][128]
   off = align_up(off + (size_t)BH * p.n_fb * max(p.n_split, 1) * (s.d + 1) * kFB * sizeof(float), 1024);
+  p.off_pre = off;     // fp32 [BH][n_fb][n_sc][d+1][128]: each superchunk's initial state
+  off = align_up(off + (size_t)BH * p.n_fb * p.n_sc * (s.d + 1) * kFB * sizeof(float), 1024);
   p.off_xbuf = off;    // fp32 [BH][n_sc][2][n_fb][128][d+4]
   if (p.n_fb > 1) off = align_up(off + (size_t)BH * p.n_sc * 2 * p.n_fb * kBM * kXWidth * sizeof(float), 1024);
   p.bytes = off;
@@ -494,8 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1) fs_output_kernel(const __grid_con
     }
     mbar_init(o_full, 1);
     mbar_init(o_free, kEpiWarps);
-    mbar_init(land_full, NC > 1 ? (NC - 1) * kBM : 1);   // every thread holding my columns, per source
-    for (int i = 0; i < 4; ++i) mbar_init(&land_free[i], kBM);   // owner i's finalising threads
+    mbar_init(land_full, NC > 1 ? (NC - 1) * 4 : 1);   // the 4 warps holding my columns, per source
+    for (int i = 0; i < 4; ++i) mbar_init(&land_free[i], 4);   // owner i's finalising warps
     mbar_init(setup_bar, 1);
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -685,7 +687,9 @@ __global__ void __launch_bounds__(kThreads, 1) fs_output_kernel(const __grid_con
                             __uint_as_float(v[sl * W + c + 2]), __uint_as_float(v[sl * W + c + 3]));
             st_cluster_v4(dst + W * 4, den_own, bias, 0.f, 0.f);
           }
-          mbar_arrive_remote(map_to_rank(smem_addr(land_full), static_cast<uint32_t>(owner)));
+          // one release per warp covers its lanes' writes (they precede the warp barrier)
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(map_to_rank(smem_addr(land_full), static_cast<uint32_t>(owner)));
         }
         if (wg == wg_fin) {
           // finalise my columns: every partial rescaled to the largest
@@ -714,8 +718,10 @@ __global__ void __launch_bounds__(kThreads, 1) fs_output_kernel(const __grid_con
             den = fmaf(sc, lr[W], den);
           }
           // the landing rows are read: their writers may send the next tile
-          for (int src = 0; src < NC; ++src)
-            if (src != rank) mbar_arrive_remote(map_to_rank(smem_addr(&land_free[rank]), static_cast<uint32_t>(src)));
+          __syncwarp();
+          if (lane == 0)
+            for (int src = 0; src < NC; ++src)
+              if (src != rank) mbar_arrive_remote(map_to_rank(smem_addr(&land_free[rank]), static_cast<uint32_t>(src)));
           if (have && valid) {
             if (!(den > 0.f) || !isfinite(den)) report_status(prm.status, FAVOR_ERR_NONFINITE);
             const float inv = __fdividef(1.0f, den);
@@ -746,6 +752,34 @@ __global__ void __launch_bounds__(kThreads, 1) fs_output_kernel(const __grid_con
 }
 
 // ---------------------------------------------------------------------------
+// causal initial states: pre[sc] = the sum, in split order, of the partial
+// states of the sub-splits of superchunks 0 .. sc - 1 (block = (head,
+// feature block, state row n), thread = feature; eight loads in flight)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kFB) fs_prefix_kernel(const float* __restrict__ partS, float* __restrict__ pre,
+                                                      int n_fb, int n_split, int sub_per_sc, int n_sc) {
+  const int f = threadIdx.x;
+  const int n = blockIdx.x % (kD + 1), hb = blockIdx.y * n_fb + blockIdx.x / (kD + 1);
+  constexpr size_t kStride = (size_t)(kD + 1) * kFB;
+  const float* src = partS + (size_t)hb * max(n_split, 1) * kStride + (size_t)n * kFB + f;
+  float* dst = pre + (size_t)hb * n_sc * kStride + (size_t)n * kFB + f;
+  float acc = 0.f;
+  for (int p0 = 0; p0 < n_split; p0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = (p0 + u < n_split) ? src[(size_t)(p0 + u) * kStride] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int p = p0 + u;
+      if (p >= n_split) break;
+      if (p % sub_per_sc == 0) dst[(size_t)(p / sub_per_sc) * kStride] = acc;
+      acc += v[u];
+    }
+  }
+  dst[(size_t)(n_sc - 1) * kStride] = acc;
+}
+
+// ---------------------------------------------------------------------------
 // causal kernel: a cluster of NC CTAs (NC = m / 128) per superchunk of one
 // head, walking its 128-token chunks; CTA rank r holds feature block r of
 // Omega and the block's rows of the running state G_r (fp32, tensor memory,
@@ -767,11 +801,11 @@ __global__ void __launch_bounds__(kThreads, 1) fs_output_kernel(const __grid_con
 struct FsCausalParams {
   const float* key_ref;
   const uint8_t* omega_img;
-  const float* partS;     // [BH][n_fb][n_split][d+1][128], sub_per_sc sub-splits per superchunk
+  const float* pre;       // [BH][n_fb][n_sc][d+1][128] initial states
   float* xbuf;            // [BH][n_sc][2][NC][128][kXW] partial outputs
   __nv_bfloat16* O;
   int32_t* status;
-  int L, m, n_fb, n_split, tiles_per_sc, sub_per_sc, n_sc;
+  int L, m, n_fb, tiles_per_sc, n_sc;
   float scale;
 };
 
@@ -843,8 +877,8 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
     mbar_init(ma_free, 1);
     mbar_init(o_full, 1);
     mbar_init(o_free, kEpiWarps);
-    mbar_init(xch_full, NC > 1 ? (NC - 1) * kEpiThreads : 1);   // every epilogue thread of each other CTA
-    for (int i = 0; i < 2; ++i) mbar_init(&xch_free[i], NC > 1 ? (NC - 1) * kBM : 1);   // the owners' finalisers
+    mbar_init(xch_full, NC > 1 ? (NC - 1) * kEpiWarps : 1);   // every epilogue warp of each other CTA
+    for (int i = 0; i < 2; ++i) mbar_init(&xch_free[i], NC > 1 ? (NC - 1) * 4 : 1);   // the owners' finalising warps
     mbar_init(setup_bar, 1);
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -1033,26 +1067,20 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
     const int wg_fin = (rank * W) / 64;   // the warpgroup holding my output columns (NC > 1)
     bool ok = true;
 
-    // G_r = the earlier superchunks' partial states of block r, in order:
-    // warpgroup 0 columns 0 .. 79, warpgroup 1 columns 80 .. 143 (zero past d)
+    // G_r = the superchunk's initial state (the earlier superchunks' partials
+    // of block r, summed in order by the prefix kernel): warpgroup 0 columns
+    // 0 .. 79, warpgroup 1 columns 80 .. 143 (zero past d)
     {
       const int n0 = wg ? 80 : 0;
       const int ng16 = wg ? 4 : 5;
-      const float* src = prm.partS + (((size_t)bh * prm.n_fb + rank) * max(prm.n_split, 1)) * (kD + 1) * kFB;
+      const float* src = prm.pre + (((size_t)bh * prm.n_fb + rank) * prm.n_sc + sc) * (kD + 1) * kFB;
       for (int g = 0; g < ng16; ++g) {
-        float acc[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-        for (int p = 0; p < sc * prm.sub_per_sc; ++p) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int n = n0 + 16 * g + j;
-            if (n <= kD) acc[j] += src[((size_t)p * (kD + 1) + n) * kFB + t];
-          }
-        }
         uint32_t r[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(acc[j]);
+        for (int j = 0; j < 16; ++j) {
+          const int n = n0 + 16 * g + j;
+          r[j] = __float_as_uint(n <= kD ? src[(size_t)n * kFB + t] : 0.f);
+        }
         tmem_st16(tmem + lane_off + G_COL + n0 + 16 * g, r);
       }
       tmem_st_wait();
@@ -1074,26 +1102,10 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
     // stmatrix.trans turns each 8x8 block (features x n) into rows n of 8
     // features, one swizzle chunk each.  Warpgroup 0 takes groups 0 .. 8.
     auto copy_gs = [&]() {
-      const int mi = lane >> 3, kr = lane & 7;
-      const int f0 = 32 * q + 8 * mi;
-      const uint32_t row_base = gs_a + (f0 >> 6) * (kGN * 128);
-      const int fch = (f0 & 63) >> 3;
       constexpr int kGroups = kD / 8 + 1;
       const int g0 = wg ? (kGroups + 1) / 2 : 0, g1 = wg ? kGroups : (kGroups + 1) / 2;
-#pragma unroll 1
-      for (int g = g0; g < g1; ++g) {
-        uint32_t lo[4], hi[4];
-        const uint32_t col = G_COL + 8 * g;
-        tmem_ld16x256(tmem + (static_cast<uint32_t>(32 * q) << 16) + col, lo);
-        tmem_ld16x256(tmem + (static_cast<uint32_t>(32 * q + 16) << 16) + col, hi);
-        tmem_ld_wait();
-        const int n = 8 * g + kr;
-        stmatrix_x4_trans(row_base + n * 128 + ((fch ^ (n & 7)) << 4),
-                          pack_bf16(__uint_as_float(lo[0]), __uint_as_float(lo[1])),
-                          pack_bf16(__uint_as_float(lo[2]), __uint_as_float(lo[3])),
-                          pack_bf16(__uint_as_float(hi[0]), __uint_as_float(hi[1])),
-                          pack_bf16(__uint_as_float(hi[2]), __uint_as_float(hi[3])));
-      }
+      const int f0 = 32 * q + 8 * (lane >> 3);
+      tmem_state_to_rows<3>(tmem, G_COL, q, lane, g0, g1, gs_a + (f0 >> 6) * (kGN * 128));
     };
 
     // the output of chunk j: my partial to the exchange, my columns finalised
@@ -1137,8 +1149,11 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
                                                               __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
           if (wg == 1) *reinterpret_cast<float4*>(dst + 64) = make_float4(den_own, bias, 0.f, 0.f);
         }
-        for (int p = 0; p < NC; ++p)
-          if (p != rank) mbar_arrive_remote(map_to_rank(smem_addr(xch_full), static_cast<uint32_t>(p)));
+        // one release per warp covers its lanes' writes (they precede the warp barrier)
+        __syncwarp();
+        if (lane == 0)
+          for (int p = 0; p < NC; ++p)
+            if (p != rank) mbar_arrive_remote(map_to_rank(smem_addr(xch_full), static_cast<uint32_t>(p)));
         if (wg == wg_fin) {
           // my columns: every partial rescaled to the largest reference; mine
           // first, then the others in rank order
@@ -1169,8 +1184,10 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
             den = fmaf(sc, __ldcg(lr + kD), den);
           }
           // read: the writers may reuse this parity's rows two chunks on
-          for (int p = 0; p < NC; ++p)
-            if (p != rank) mbar_arrive_remote(map_to_rank(smem_addr(&xch_free[par]), static_cast<uint32_t>(p)));
+          __syncwarp();
+          if (lane == 0)
+            for (int p = 0; p < NC; ++p)
+              if (p != rank) mbar_arrive_remote(map_to_rank(smem_addr(&xch_free[par]), static_cast<uint32_t>(p)));
           if (have && valid) {
             if (!(den > 0.f) || !isfinite(den)) report_status(prm.status, FAVOR_ERR_NONFINITE);
             const float inv = __fdividef(1.0f, den);
@@ -1184,6 +1201,12 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
       }
     };
 
+    // G_s(0): the initial state
+    if (ok) copy_gs();
+    tc_fence_before();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(gs_full);
     float bias_prev = 0.f;
     for (int c = 0; c < n_chunks; ++c) {
       const bool valid = (tile0 + c) * kBM + t < prm.L;
@@ -1208,15 +1231,6 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
         __syncwarp();
         if (lane == 0) mbar_arrive(kphi_full);
       }
-      // ---- G_s(c) = bf16(G_r) once G(c - 1) and O(c - 1) are done with it ----
-      if (ok && c >= 1) ok = mbar_wait(g_done, (c - 1) & 1, wctx);
-      if (ok && c >= 1) ok = mbar_wait(oin_done, (c - 1) & 1, wctx);
-      tc_fence_after();
-      if (ok) copy_gs();
-      tc_fence_before();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(gs_full);
       // the previous chunk's output, deferred so that its MMAs overlap
       if (c >= 1) out(c - 1, bias_prev);
       // ---- phi(Q_c)_r over Q_c, with the block's row maximum as reference ----
@@ -1277,6 +1291,18 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(ma_full);
+      }
+      // ---- G_s(c + 1) = bf16(G_r) once G(c) and O(c) are done with it; it
+      // overlaps the next chunk's key projection ----
+      if (c + 1 < n_chunks) {
+        if (ok) ok = mbar_wait(g_done, c & 1, wctx);
+        if (ok) ok = mbar_wait(oin_done, c & 1, wctx);
+        tc_fence_after();
+        if (ok) copy_gs();
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(gs_full);
       }
     }
     if (n_chunks >= 1) out(n_chunks - 1, bias_prev);
@@ -1413,16 +1439,14 @@ cudaError_t launch_fs_causal(const void* Q, const void* K, const void* V, void* 
   FsCausalParams prm{};
   prm.key_ref = reinterpret_cast<const float*>(ws);
   prm.omega_img = reinterpret_cast<const uint8_t*>(ws + p.off_omega_img);
-  prm.partS = reinterpret_cast<const float*>(ws + p.off_partS);
+  prm.pre = reinterpret_cast<const float*>(ws + p.off_pre);
   prm.xbuf = reinterpret_cast<float*>(ws + p.off_xbuf);
   prm.O = static_cast<__nv_bfloat16*>(O);
   prm.status = status;
   prm.L = s.L;
   prm.m = s.m;
   prm.n_fb = p.n_fb;
-  prm.n_split = p.n_split;
   prm.tiles_per_sc = p.tiles_per_sc;
-  prm.sub_per_sc = p.sub_per_sc;
   prm.n_sc = p.n_sc;
   prm.scale = scale;
   cudaLaunchConfig_t cfg{};
@@ -1482,8 +1506,14 @@ cudaError_t fs_state(bool causal, const void* K, const void* V, const float* ome
                               reinterpret_cast<uint8_t*>(w + sl.off_omega_img),
                               n_counters ? reinterpret_cast<uint32_t*>(w + off_counters) : nullptr, n_counters, stream);
   if (e != cudaSuccess) return e;
-  return fm == FAVOR_FM_RELU ? launch_fs_state<FAVOR_FM_RELU>(K, V, s, sl, scale, w, status, stream)
-                             : launch_fs_state<FAVOR_FM_PRF>(K, V, s, sl, scale, w, status, stream);
+  e = fm == FAVOR_FM_RELU ? launch_fs_state<FAVOR_FM_RELU>(K, V, s, sl, scale, w, status, stream)
+                          : launch_fs_state<FAVOR_FM_PRF>(K, V, s, sl, scale, w, status, stream);
+  if (e != cudaSuccess || !causal) return e;
+  const FsCausalPlan p = fsc_plan(s);
+  fs_prefix_kernel<<<dim3(p.n_fb * (kD + 1), s.BH()), kFB, 0, stream>>>(
+      reinterpret_cast<const float*>(w + p.off_partS), reinterpret_cast<float*>(w + p.off_pre), p.n_fb, p.n_split,
+      p.sub_per_sc, p.n_sc);
+  return cudaGetLastError();
 }
 
 cudaError_t fs_output(bool causal, const void* Q, const void* K, const void* V, void* O, float scale, const Shape& s,

@@ -122,6 +122,17 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
 }
+// 16 bytes into another CTA's shared memory; the store counts its bytes
+// against that CTA's mbarrier `remote_bar` (complete_tx), so the receiver
+// sees the data once the barrier's phase completes and the sender needs no
+// fence
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   remote_addr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+               : "memory");
+}
 // arrive on an mbarrier of another CTA of the cluster, releasing this thread's
 // earlier writes (shared::cluster and global) at cluster scope
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {

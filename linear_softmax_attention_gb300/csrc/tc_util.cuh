@@ -180,6 +180,42 @@ __device__ __forceinline__ uint64_t vones_k(uint64_t d0, int k) {
   return d0 + static_cast<uint64_t>(k * 128) - (static_cast<uint64_t>(k * 128) << 16);
 }
 
+// The causal state's bf16 copy: columns n = 8g .. 8g + 7 (groups g0 <= g <
+// g1) of G in tensor memory (lane = feature; this warp's 32 features from
+// lane 32q) into rows n of a K-major operand, 8 features per 16-byte swizzle
+// chunk.  `rows` is the address of row 0 of the atom holding this thread's
+// stmatrix features (32q + 8 (lane / 8) onward).  Per group a 16x256b load
+// per half of the warp's features gives each thread two adjacent n of one
+// feature; stmatrix.trans turns each 8x8 block (features x n) into rows n.
+// KB groups' loads are in flight together (one wait per KB groups).
+template <int KB>
+__device__ __forceinline__ void tmem_state_to_rows(uint32_t tmem, uint32_t g_col, int q, int lane, int g0, int g1,
+                                                   uint32_t rows) {
+  const int kr = lane & 7;
+  const int fch = ((32 * q + 8 * (lane >> 3)) & 63) >> 3;
+#pragma unroll 1
+  for (int gb = g0; gb < g1; gb += KB) {
+    uint32_t lo[KB][4], hi[KB][4];
+#pragma unroll
+    for (int u = 0; u < KB; ++u) {
+      const uint32_t col = g_col + 8 * min(gb + u, g1 - 1);   // a past-the-end group reloads the last one
+      tmem_ld16x256(tmem + (static_cast<uint32_t>(32 * q) << 16) + col, lo[u]);
+      tmem_ld16x256(tmem + (static_cast<uint32_t>(32 * q + 16) << 16) + col, hi[u]);
+    }
+    tmem_ld_wait();
+#pragma unroll
+    for (int u = 0; u < KB; ++u) {
+      if (gb + u >= g1) break;
+      const int n = 8 * (gb + u) + kr;
+      stmatrix_x4_trans(rows + n * 128 + ((fch ^ (n & 7)) << 4),
+                        pack_bf16(__uint_as_float(lo[u][0]), __uint_as_float(lo[u][1])),
+                        pack_bf16(__uint_as_float(lo[u][2]), __uint_as_float(lo[u][3])),
+                        pack_bf16(__uint_as_float(hi[u][0]), __uint_as_float(hi[u][1])),
+                        pack_bf16(__uint_as_float(hi[u][2]), __uint_as_float(hi[u][3])));
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
