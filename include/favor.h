@@ -247,7 +247,11 @@ favor_status favor_causal_output(const void* Q, const void* K, const void* V, vo
  * library holds until the process exits.  The first call on each device
  * resolves the array's device address (cudaGetSymbolAddress) for that device,
  * so make that first call with the device current and outside any stream
- * capture.  No call allocates or frees memory.
+ * capture: a first call on a stream that is being captured returns
+ * FAVOR_ERR_INVALID_ARG without launching anything.  The address is kept for
+ * the life of the process; after cudaDeviceReset (or any other teardown of
+ * the device's primary context) do not call this entry point again.  No call
+ * allocates or frees memory.
  *
  * All calls share the one array and leave their intermediate results in it;
  * the kernels clear what must start at zero.  Calls whose execution overlaps

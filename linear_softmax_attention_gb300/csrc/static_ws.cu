@@ -21,14 +21,22 @@ std::mutex g_scratch_mu;
 void* g_scratch_ptr[64] = {};
 
 // Device address of the array on the current device (resolved once per
-// device; the array's name in host code is only a host-side handle).
-cudaError_t scratch_address(void** out) {
+// device; the array's name in host code is only a host-side handle).  The
+// resolution is refused while `stream` is being captured into a graph:
+// *capturing is set and nothing else happens.
+cudaError_t scratch_address(void** out, cudaStream_t stream, bool* capturing) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (g_scratch_ptr[dev] == nullptr) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+      (void)cudaGetLastError();
+      *capturing = true;
+      return cudaErrorStreamCaptureUnsupported;
+    }
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_favor_static_scratch);
     if (e != cudaSuccess) return e;
@@ -48,7 +56,9 @@ extern "C" favor_status favor_fwd_bidir_static(const void* Q, const void* K, con
     return favor::run_call(false, 3, Q, K, V, O, B, H, L, d, omega, m, dt, qk_scale, nullptr, 0, dev_status, stream);
   if (need > kStaticScratchBytes) return FAVOR_ERR_UNSUPPORTED;
   void* scratch = nullptr;
-  if (scratch_address(&scratch) != cudaSuccess) return FAVOR_ERR_CUDA;
+  bool capturing = false;
+  if (scratch_address(&scratch, static_cast<cudaStream_t>(stream), &capturing) != cudaSuccess)
+    return capturing ? FAVOR_ERR_INVALID_ARG : FAVOR_ERR_CUDA;
   return favor::run_call(false, 3, Q, K, V, O, B, H, L, d, omega, m, dt, qk_scale, scratch, kStaticScratchBytes,
                          dev_status, stream);
 }

@@ -438,14 +438,15 @@ struct FsOutParams {
 template <int NC>
 struct FsOutCfg {
   static constexpr int W = kD / NC;                       // output columns finalised per CTA
-  static constexpr int LW = W + 4;                        // landing row: W numerators, normaliser, reference, pad
+  static constexpr int RB = 2 * W + 16;                   // landing row bytes: W bf16 numerators, fp32 normaliser and reference, pad
+  static constexpr int kLandTile = (NC - 1) * kBM * RB;   // one tile's rows from the other CTAs
   static constexpr int NSQ = 2;                           // Q stages (Q, then phi(Q) in place)
   static constexpr int kOmega = 0;                        // [2 atoms][128 feature rows][128 B]
   static constexpr int kState = kOmega + 2 * kAtom;       // [2 atoms][kGN rows][128 B]
   static constexpr int kQ = kState + 2 * kGN * 128;
   static constexpr int kXmax = kQ + NSQ * kTile;          // [tile parity][warpgroup][128] row maxima
-  static constexpr int kLand = kXmax + 2 * 2 * kBM * 4;   // [NC - 1 sources][128][LW] partials from the others
-  static constexpr int kBars = kLand + (NC - 1) * kBM * LW * 4;
+  static constexpr int kLand = kXmax + 2 * 2 * kBM * 4;   // [tile parity][NC - 1 sources][128][RB]
+  static constexpr int kBars = kLand + 2 * kLandTile;
   static constexpr int kSmem = kBars + 256 + 1024;
 };
 static_assert(FsOutCfg<4>::kSmem <= 232448 && FsOutCfg<2>::kSmem <= 232448, "shared memory");
@@ -467,9 +468,9 @@ __global__ void __launch_bounds__(kThreads, 1) fs_output_kernel(const __grid_con
   uint64_t* phi_full = p_free + 2;          // [2] phi(Q) written over Q
   uint64_t* o_full = phi_full + 2;
   uint64_t* o_free = o_full + 1;
-  uint64_t* land_full = o_free + 1;         // the other CTAs' partials for my columns have landed
-  uint64_t* land_free = land_full + 1;      // [4] owner r has read my previous partial
-  uint64_t* setup_bar = land_free + 4;
+  uint64_t* land_full = o_free + 1;         // [tile parity] the other CTAs' partials for my columns have landed
+  uint64_t* land_free = land_full + 2;      // [tile parity][4] owner r has read my partial of that parity
+  uint64_t* setup_bar = land_free + 8;
   uint64_t* done_bar = setup_bar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -496,12 +497,17 @@ __global__ void __launch_bounds__(kThreads, 1) fs_output_kernel(const __grid_con
     }
     mbar_init(o_full, 1);
     mbar_init(o_free, kEpiWarps);
-    mbar_init(land_full, NC > 1 ? (NC - 1) * 4 : 1);   // the 4 warps holding my columns, per source
-    for (int i = 0; i < 4; ++i) mbar_init(&land_free[i], 4);   // owner i's finalising warps
+    // the partials arrive by st.async, counted in bytes: one arrival per
+    // phase (the expected byte count, posted here for tiles 0 and 1 and by
+    // the finalising warpgroup for tile j + 2 once tile j is read)
+    for (int i = 0; i < 2; ++i) mbar_init(&land_full[i], 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&land_free[i], 4);   // owner i % 4's finalising warps
     mbar_init(setup_bar, 1);
     mbar_init(done_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
+    if (NC > 1)
+      for (int i = 0; i < 2; ++i) mbar_arrive_expect_tx(&land_full[i], C::kLandTile);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -671,33 +677,37 @@ __global__ void __launch_bounds__(kThreads, 1) fs_output_kernel(const __grid_con
                            pack_bf16(__uint_as_float(v[c + 6]) * inv, __uint_as_float(v[c + 7]) * inv));
         }
       } else {
-        // send: every slice of my columns owned by another CTA
+        // send: every slice of my columns owned by another CTA, into the
+        // tile parity's landing rows once the owner has read the ones two
+        // tiles back; bf16 numerators, fp32 normaliser and reference
+        const int par = j & 1;
 #pragma unroll
         for (int sl = 0; sl < 64 / W; ++sl) {
           const int owner = (col0 + sl * W) / W;
           if (owner == rank) continue;
-          if (ok && j >= 1) ok = mbar_wait_cluster(&land_free[owner], (j - 1) & 1, wctx);
+          if (ok && j >= 2) ok = mbar_wait_cluster(&land_free[par * 4 + owner], ((j >> 1) - 1) & 1, wctx);
           const int slot = rank < owner ? rank : rank - 1;
-          const uint32_t dst =
-              map_to_rank(smem_addr(sm + C::kLand + ((size_t)slot * kBM + t) * C::LW * 4), static_cast<uint32_t>(owner));
+          const uint32_t dst = map_to_rank(
+              smem_addr(sm + C::kLand + par * C::kLandTile + ((size_t)slot * kBM + t) * C::RB), static_cast<uint32_t>(owner));
+          const uint32_t mb = map_to_rank(smem_addr(&land_full[par]), static_cast<uint32_t>(owner));
           if (ok) {
 #pragma unroll
-            for (int c = 0; c < W; c += 4)
-              st_cluster_v4(dst + c * 4, __uint_as_float(v[sl * W + c]), __uint_as_float(v[sl * W + c + 1]),
-                            __uint_as_float(v[sl * W + c + 2]), __uint_as_float(v[sl * W + c + 3]));
-            st_cluster_v4(dst + W * 4, den_own, bias, 0.f, 0.f);
+            for (int c = 0; c < W; c += 8)
+              st_async_v4(dst + c * 2, pack_bf16(__uint_as_float(v[sl * W + c]), __uint_as_float(v[sl * W + c + 1])),
+                          pack_bf16(__uint_as_float(v[sl * W + c + 2]), __uint_as_float(v[sl * W + c + 3])),
+                          pack_bf16(__uint_as_float(v[sl * W + c + 4]), __uint_as_float(v[sl * W + c + 5])),
+                          pack_bf16(__uint_as_float(v[sl * W + c + 6]), __uint_as_float(v[sl * W + c + 7])), mb);
+            st_async_v4(dst + W * 2, __float_as_uint(den_own), __float_as_uint(bias), 0u, 0u, mb);
           }
-          // one release per warp covers its lanes' writes (they precede the warp barrier)
-          __syncwarp();
-          if (lane == 0) mbar_arrive_remote(map_to_rank(smem_addr(land_full), static_cast<uint32_t>(owner)));
         }
         if (wg == wg_fin) {
           // finalise my columns: every partial rescaled to the largest
           // reference; mine first, then the others in rank order
-          if (ok) ok = mbar_wait_cluster(land_full, j & 1, wctx);
-          const float* land = reinterpret_cast<const float*>(sm + C::kLand);
+          if (ok) ok = mbar_wait(&land_full[par], (j >> 1) & 1, wctx);
+          const uint8_t* land = sm + C::kLand + par * C::kLandTile;
           float bmax = bias;
-          for (int sl = 0; sl < NC - 1; ++sl) bmax = fmaxf(bmax, land[((size_t)sl * kBM + t) * C::LW + W + 1]);
+          for (int sl = 0; sl < NC - 1; ++sl)
+            bmax = fmaxf(bmax, *reinterpret_cast<const float*>(land + ((size_t)sl * kBM + t) * C::RB + 2 * W + 4));
           const bool hi = (rank * W - col0) != 0;   // my slice is the upper half of this thread's 64 columns
           const float sc_own = ex2(bias - bmax);
           float acc[W];
@@ -705,23 +715,29 @@ __global__ void __launch_bounds__(kThreads, 1) fs_output_kernel(const __grid_con
           for (int c = 0; c < W; ++c) acc[c] = sc_own * __uint_as_float(W == 64 ? v[c] : (hi ? v[(32 + c) & 63] : v[c]));
           float den = sc_own * den_own;
           for (int sl = 0; sl < NC - 1; ++sl) {
-            const float* lr = land + ((size_t)sl * kBM + t) * C::LW;
-            const float sc = ex2(lr[W + 1] - bmax);
+            const uint8_t* lr = land + ((size_t)sl * kBM + t) * C::RB;
+            const float2 dr = *reinterpret_cast<const float2*>(lr + 2 * W);   // normaliser, reference
+            const float sc = ex2(dr.y - bmax);
 #pragma unroll
-            for (int c = 0; c < W; c += 4) {
-              const float4 p4 = *reinterpret_cast<const float4*>(lr + c);
-              acc[c] = fmaf(sc, p4.x, acc[c]);
-              acc[c + 1] = fmaf(sc, p4.y, acc[c + 1]);
-              acc[c + 2] = fmaf(sc, p4.z, acc[c + 2]);
-              acc[c + 3] = fmaf(sc, p4.w, acc[c + 3]);
+            for (int c = 0; c < W; c += 8) {
+              const uint4 p4 = *reinterpret_cast<const uint4*>(lr + c * 2);
+              const uint32_t w4[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                acc[c + 2 * e] = fmaf(sc, __uint_as_float(w4[e] << 16), acc[c + 2 * e]);
+                acc[c + 2 * e + 1] = fmaf(sc, __uint_as_float(w4[e] & 0xFFFF0000u), acc[c + 2 * e + 1]);
+              }
             }
-            den = fmaf(sc, lr[W], den);
+            den = fmaf(sc, dr.x, den);
           }
-          // the landing rows are read: their writers may send the next tile
+          // the rows are read: re-arm this parity for tile j + 2, then let
+          // their writers send it
+          if (threadIdx.x == kEpiTid0 + kBM * wg_fin && ok) mbar_arrive_expect_tx(&land_full[par], C::kLandTile);
           __syncwarp();
           if (lane == 0)
             for (int src = 0; src < NC; ++src)
-              if (src != rank) mbar_arrive_remote(map_to_rank(smem_addr(&land_free[rank]), static_cast<uint32_t>(src)));
+              if (src != rank)
+                mbar_arrive_remote(map_to_rank(smem_addr(&land_free[par * 4 + rank]), static_cast<uint32_t>(src)));
           if (have && valid) {
             if (!(den > 0.f) || !isfinite(den)) report_status(prm.status, FAVOR_ERR_NONFINITE);
             const float inv = __fdividef(1.0f, den);
