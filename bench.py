@@ -272,8 +272,13 @@ def run_gpu(args, rank, world, local_rank):
     omegas = [torch.empty((m, d), dtype=torch.float32, device=dev) for _ in range(2)]
     omega = omegas[0]
     side = torch.cuda.Stream(device=dev)
+    # the causal pass runs on its own stream beside the bidirectional one:
+    # the passes are independent and each kernel leaves SMs idle (grids of
+    # whole heads' tiles), so their kernels overlap
+    second = torch.cuda.Stream(device=dev)
     ev_fork = torch.cuda.Event()
     ev_join = torch.cuda.Event()
+    ev_join2 = torch.cuda.Event()
     ws_b = favor.new_workspace(False, B, H, L, d, m, dt, device=dev)
     ws_c = favor.new_workspace(True, B, H, L, d, m, dt, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -285,13 +290,16 @@ def run_gpu(args, rank, world, local_rank):
         cur, nxt = omegas[i % 2], omegas[(i + 1) % 2]
         ev_fork.record(stream)
         side.wait_event(ev_fork)
+        second.wait_event(ev_fork)
         favor.build_orf(seed_call, nxt, stream=side)
+        favor.causal_state(k, v, cur, s, ws_c, dev_status=status, stream=second)
+        favor.causal_output(q, k, v, cur, s, ws_c, O=O_c, dev_status=status, stream=second)
         favor.bidir_state(k, v, cur, s, ws_b, dev_status=status, stream=stream)
         favor.bidir_output(q, cur, s, ws_b, O=O_b, dev_status=status, stream=stream)
-        favor.causal_state(k, v, cur, s, ws_c, dev_status=status, stream=stream)
-        favor.causal_output(q, k, v, cur, s, ws_c, O=O_c, dev_status=status, stream=stream)
         ev_join.record(side)
         stream.wait_event(ev_join)
+        ev_join2.record(second)
+        stream.wait_event(ev_join2)
 
     # the input sets and workspaces were made on the current stream; every
     # step runs on `stream`
@@ -411,6 +419,7 @@ def run_gpu(args, rank, world, local_rank):
         ev_comp = [torch.cuda.Event() for _ in range(2)]
         ev_out = [torch.cuda.Event() for _ in range(2)]
         om_e2e = torch.empty((m, d), dtype=torch.float32, device=dev)
+        ev_om, ev_c2 = torch.cuda.Event(), torch.cuda.Event()
 
         def e2e_step(i):
             b_ = i % 2
@@ -427,8 +436,12 @@ def run_gpu(args, rank, world, local_rank):
             if i >= 2:
                 stream.wait_event(ev_out[b_])               # step i-2's outputs have left
             favor.build_orf(wl.omega_seed_for_call(w, i), om_e2e, stream=stream)
+            ev_om.record(stream)
+            second.wait_event(ev_om)
+            favor.fwd_causal(dq, dk, dv, om_e2e, s, ws_c, O=oc, dev_status=status, stream=second)
             favor.fwd_bidir(dq, dk, dv, om_e2e, s, ws_b, O=ob, dev_status=status, stream=stream)
-            favor.fwd_causal(dq, dk, dv, om_e2e, s, ws_c, O=oc, dev_status=status, stream=stream)
+            ev_c2.record(second)
+            stream.wait_event(ev_c2)
             ev_comp[b_].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_comp[b_])
@@ -522,7 +535,8 @@ def run_gpu(args, rank, world, local_rank):
                    "step": "build Omega + bidirectional + causal forward", "tokens_per_step": tokens_per_step,
                    "path": favor.path_name(False, d, m, dt), "l2": f"{n_sets} rotating input sets "
                    f"({n_sets * bytes_per_set / 2**20:.0f} MiB > L2)", "timing": "CUDA graph replay per step; per-kernel times from per-stage graphs with events between stages",
-                   "omega": "each step builds the next step's Omega on a second stream (double-buffered) while its attention kernels run",
+                   "omega": "each step builds the next step's Omega on a side stream (double-buffered) while its attention kernels run",
+                   "streams": "the bidirectional and the causal pass on two streams (independent passes; their kernels overlap)",
                    "parallelism": f"replicas x{world}"},
         "modes": {"head_tokens_per_s": value * H,
                   "bidir_tokens_per_s": tokens_per_step / (bidir_ms / 1e3),
