@@ -63,6 +63,8 @@ def parse():
                     help="only run WORKLOAD's full forward call --calls times and print its mean time "
                          "(a small driver for profilers)")
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--call-mode", default=None, choices=["bidir", "causal"],
+                    help="with --call: run this pass instead of the workload's own")
     return ap.parse_args()
 
 
@@ -202,7 +204,8 @@ class ClockSampler:
 # The sources the tensor-core kernels (the profiled stages) are built from:
 # a committed profile's counters stay valid while their code (comments and
 # layout aside) does not change.
-KERNEL_SOURCES = ("linear_softmax_attention_gb300/csrc/tc.cu", "linear_softmax_attention_gb300/csrc/tc_ptx.cuh",
+KERNEL_SOURCES = ("linear_softmax_attention_gb300/csrc/tc.cu", "linear_softmax_attention_gb300/csrc/tc_fs.cu",
+                  "linear_softmax_attention_gb300/csrc/tc_util.cuh", "linear_softmax_attention_gb300/csrc/tc_ptx.cuh",
                   "linear_softmax_attention_gb300/csrc/common.cuh", "linear_softmax_attention_gb300/csrc/prep.cu",
                   "include/favor.h")
 _C_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
@@ -943,7 +946,7 @@ def run_call_only(args):
     favor.load()
     dev = torch.device("cuda", 0)
     w = workload_for(args.call)
-    causal = w.mode == "causal"
+    causal = (args.call_mode or w.mode) == "causal"
     q, k, v = wl.make_qkv(w, seed=0, device=dev)
     om = favor.new_omega(wl.omega_seed_for_call(w, 0), w.m, w.d, device=dev)
     ws = favor.new_workspace(causal, w.B, w.H, w.L, w.d, w.m, w.torch_dtype, device=dev)
@@ -959,7 +962,8 @@ def run_call_only(args):
     torch.cuda.synchronize(dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} on {w.name}")
-    print(json.dumps({"call": w.name, "calls": args.calls, "ms_per_call": e0.elapsed_time(e1) / args.calls,
+    print(json.dumps({"call": w.name, "mode": "causal" if causal else "bidir", "calls": args.calls,
+                      "ms_per_call": e0.elapsed_time(e1) / args.calls,
                       "path": favor.path_name(causal, w.d, w.m, w.torch_dtype)}))
 
 

@@ -76,14 +76,13 @@ FsPlan fs_plan(const Shape& s) {
 
 // Causal: superchunks of tiles_per_sc tiles, one cluster each; the key-state
 // kernel writes the partials of every superchunk but the last in sub_per_sc
-// sub-splits; the clusters exchange partial outputs through xbuf.
+// sub-splits; the clusters exchange partial outputs in shared memory.
 struct FsCausalPlan {
   int n_fb, n_tiles;
   int tiles_per_sc, n_sc, sub_per_sc, tiles_per_split, n_split;
-  size_t off_omega_img, off_partS, off_pre, off_xbuf, bytes;
+  size_t off_omega_img, off_partS, off_pre, bytes;
 };
 
-constexpr int kXWidth = kD + 4;   // floats per row of the exchange buffer
 
 FsCausalPlan fsc_plan(const Shape& s) {
   FsCausalPlan p{};
@@ -116,8 +115,6 @@ FsCausalPlan fsc_plan(const Shape& s) {
   off = align_up(off + (size_t)BH * p.n_fb * max(p.n_split, 1) * (s.d + 1) * kFB * sizeof(float), 1024);
   p.off_pre = off;     // fp32 [BH][n_fb][n_sc][d+1][128]: each superchunk's initial state
   off = align_up(off + (size_t)BH * p.n_fb * p.n_sc * (s.d + 1) * kFB * sizeof(float), 1024);
-  p.off_xbuf = off;    // fp32 [BH][n_sc][2][n_fb][128][d+4]
-  if (p.n_fb > 1) off = align_up(off + (size_t)BH * p.n_sc * 2 * p.n_fb * kBM * kXWidth * sizeof(float), 1024);
   p.bytes = off;
   return p;
 }
@@ -818,37 +815,40 @@ struct FsCausalParams {
   const float* key_ref;
   const uint8_t* omega_img;
   const float* pre;       // [BH][n_fb][n_sc][d+1][128] initial states
-  float* xbuf;            // [BH][n_sc][2][NC][128][kXW] partial outputs
   __nv_bfloat16* O;
   int32_t* status;
   int L, m, n_fb, tiles_per_sc, n_sc;
   float scale;
 };
 
-constexpr int kXW = kXWidth;   // exchange row: d numerators, normaliser, reference, pad
 
+template <int NC>
 struct FsCausalCfg {
+  static constexpr int W = kD / NC;                        // output columns finalised per CTA
+  static constexpr int RB = 2 * W + 16;                    // landing row bytes: W bf16 numerators, fp32 normaliser and reference, pad
+  static constexpr int kLandChunk = (NC - 1) * kBM * RB;   // one chunk's rows from the other CTAs
+  static constexpr int NB = NC == 4 ? 1 : 2;               // landing buffers (chunks in flight) that fit
   static constexpr int kOmega = 0;                         // [2 atoms][128 feature rows][128 B]
   static constexpr int kK = kOmega + 2 * kAtom;            // K_c, then phi(K_c) over it
-  static constexpr int kQ = kK + kTile;                    // Q_c, then phi(Q_c) over it
+  static constexpr int kQ = kK + kTile;                    // Q_c, then phi(Q_c), then the masked scores over it
   static constexpr int kV = kQ + kTile;                    // V_c, then the ones atom
   static constexpr int kGs = kV + kTile + kAtom;           // [2 atoms][kGN rows][128 B]
-  static constexpr int kMA = kGs + 2 * kGN * 128;          // masked A: [2 atoms][128 query rows][128 B]
-  static constexpr int kNorm = kMA + kTile;                // [128] squared key norms
+  static constexpr int kNorm = kGs + 2 * kGN * 128;        // [128] squared key norms
   static constexpr int kXmax = kNorm + kBM * 4;            // [2][2][128] row maxima
-  static constexpr int kBars = kXmax + 2 * 2 * kBM * 4;
+  static constexpr int kLand = kXmax + 2 * 2 * kBM * 4;    // [NB][NC - 1 sources][128][RB]
+  static constexpr int kBars = kLand + (NC > 1 ? NB * kLandChunk : 0);
   static constexpr int kSmem = kBars + 512 + 1024;
 };
-static_assert(FsCausalCfg::kSmem <= 232448, "shared memory");
-static_assert(FsCausalCfg::kGs % 1024 == 0 && FsCausalCfg::kMA % 1024 == 0, "operand alignment");
+static_assert(FsCausalCfg<4>::kSmem <= 232448 && FsCausalCfg<2>::kSmem <= 232448, "shared memory");
+static_assert(FsCausalCfg<4>::kGs % 1024 == 0 && FsCausalCfg<4>::kQ % 1024 == 0, "operand alignment");
 
 template <int NC, int FM>
 __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_constant__ CUtensorMap mapQ,
                                                                 const __grid_constant__ CUtensorMap mapK,
                                                                 const __grid_constant__ CUtensorMap mapV,
                                                                 FsCausalParams prm) {
-  using C = FsCausalCfg;
-  constexpr int W = kD / NC;
+  using C = FsCausalCfg<NC>;
+  constexpr int W = C::W;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* b = reinterpret_cast<uint64_t*>(sm + C::kBars);
@@ -861,10 +861,10 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
   uint64_t *g_done = b + 15, *oin_done = b + 16;                     // G step, O = phi(Q) G_s step complete
   uint64_t *ma_full = b + 17, *ma_free = b + 18;
   uint64_t *o_full = b + 19, *o_free = b + 20;
-  uint64_t *xch_full = b + 21;                                       // the other CTAs' partials written
-  uint64_t *xch_free = b + 22;                                       // [2] my partial read by every owner
-  uint64_t *setup_bar = b + 24, *done_bar = b + 25;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b + 26);
+  uint64_t *land_full = b + 21;                                      // [NB] the other CTAs' partials for my columns
+  uint64_t *land_free = b + 23;                                      // [NB][4] owner r has read my partial
+  uint64_t *setup_bar = b + 31, *done_bar = b + 32;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b + 33);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* norms = reinterpret_cast<float*>(sm + C::kNorm);
   float* xmax = reinterpret_cast<float*>(sm + C::kXmax);
@@ -893,12 +893,17 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
     mbar_init(ma_free, 1);
     mbar_init(o_full, 1);
     mbar_init(o_free, kEpiWarps);
-    mbar_init(xch_full, NC > 1 ? (NC - 1) * kEpiWarps : 1);   // every epilogue warp of each other CTA
-    for (int i = 0; i < 2; ++i) mbar_init(&xch_free[i], NC > 1 ? (NC - 1) * 4 : 1);   // the owners' finalising warps
+    // partials arrive by st.async, counted in bytes (one arrival per phase:
+    // the expected byte count, posted here for the first NB chunks and by the
+    // finalising warpgroup for chunk j + NB once chunk j is read)
+    for (int i = 0; i < 2; ++i) mbar_init(&land_full[i], 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&land_free[i], 4);   // owner i % 4's finalising warps
     mbar_init(setup_bar, 1);
     mbar_init(done_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
+    if (NC > 1)
+      for (int i = 0; i < C::NB; ++i) mbar_arrive_expect_tx(&land_full[i], C::kLandChunk);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -933,7 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
       for (int c = 0; ok && c < n_chunks; ++c) {
         const int row = (tile0 + c) * kBM;
         uint64_t* fulls[3] = {k_full, q_full, v_full};
-        uint64_t* frees[3] = {k_free, q_free, v_free};
+        uint64_t* frees[3] = {k_free, ma_free, v_free};   // the Q slot holds the masked scores until O += mask(A)[V|1]
         const CUtensorMap* maps[3] = {&mapK, &mapQ, &mapV};
         const int offs[3] = {C::kK, C::kQ, C::kV};
         for (int kind = 0; ok && kind < 3; ++kind) {
@@ -958,7 +963,7 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
       constexpr uint32_t id_o = idesc_bf16(kBM, kGN, false, false);
       constexpr uint32_t id_oi = idesc_bf16(kBM, kGN, false, true);
       const uint32_t om_a = smem_addr(sm + C::kOmega), k_a = smem_addr(sm + C::kK), q_a = smem_addr(sm + C::kQ);
-      const uint32_t v_a = smem_addr(sm + C::kV), gs_a = smem_addr(sm + C::kGs), ma_a = smem_addr(sm + C::kMA);
+      const uint32_t v_a = smem_addr(sm + C::kV), gs_a = smem_addr(sm + C::kGs), ma_a = smem_addr(sm + C::kQ);
       bool ok = mbar_wait(setup_bar, 0, wctx);
       auto ready = [](uint64_t* bar, int parity) { return mbar_test_wait(smem_addr(bar), parity & 1); };
       // Event-driven issue.  X is used in order P_K(c), P_Q(c), A(c), each
@@ -993,7 +998,6 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
                 mma_bf16(tmem + X_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, kAtom)), id_a, k > 0);
               mma_commit(a_full);
               if (ng > c) mma_commit(k_free);    // G(c) issued too: phi(K_c)'s slot is done
-              if (no > c) mma_commit(q_free);    // O(c) issued too: phi(Q_c)'s slot is done
             }
             ++nx;
             progress = true;
@@ -1022,7 +1026,6 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
             for (int k = 0; k < kFB / 16; ++k)
               mma_bf16(tmem + O_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, kGN * 128)), id_o, k > 0);
             mma_commit(oin_done);
-            if (nx > 3 * c + 2) mma_commit(q_free);   // A(c) issued too
             ++no;
             progress = true;
           }
@@ -1078,7 +1081,7 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
     key_reference(prm.key_ref, prm.m, &R, &W_unused);
     const float c1 = feature_c1<FM>(prm.scale);
     const float hs2 = 0.5f * prm.scale * prm.scale;
-    const uint32_t k_a = smem_addr(sm + C::kK), q_a = smem_addr(sm + C::kQ), ma_a = smem_addr(sm + C::kMA);
+    const uint32_t k_a = smem_addr(sm + C::kK), q_a = smem_addr(sm + C::kQ), ma_a = q_a;   // masked scores over phi(Q)
     const uint32_t gs_a = smem_addr(sm + C::kGs);
     const int wg_fin = (rank * W) / 64;   // the warpgroup holding my output columns (NC > 1)
     bool ok = true;
@@ -1153,57 +1156,67 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
                            pack_bf16(__uint_as_float(v[c + 6]) * inv, __uint_as_float(v[c + 7]) * inv));
         }
       } else {
-        const int par = j & 1;
-        float* xc = prm.xbuf + ((((size_t)bh * prm.n_sc + sc) * 2 + par) * NC) * kBM * kXW;
-        // my partial, once every owner has read the one two chunks back
-        if (ok && j >= 2) ok = mbar_wait_cluster(&xch_free[par], ((j >> 1) - 1) & 1, wctx);
-        if (ok) {
-          float* dst = xc + ((size_t)rank * kBM + t) * kXW + col0;
+        // send: every slice of my columns owned by another CTA, into landing
+        // buffer j % NB of the owner once it has read that buffer's previous
+        // chunk; bf16 numerators, fp32 normaliser and reference, by st.async
+        const int buf = j % C::NB;
 #pragma unroll
-          for (int c = 0; c < 64; c += 4)
-            *reinterpret_cast<float4*>(dst + c) = make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]),
-                                                              __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-          if (wg == 1) *reinterpret_cast<float4*>(dst + 64) = make_float4(den_own, bias, 0.f, 0.f);
+        for (int sl = 0; sl < 64 / W; ++sl) {
+          const int owner = (col0 + sl * W) / W;
+          if (owner == rank) continue;
+          if (ok && j >= C::NB) ok = mbar_wait_cluster(&land_free[buf * 4 + owner], ((j / C::NB) - 1) & 1, wctx);
+          const int slot = rank < owner ? rank : rank - 1;
+          const uint32_t dst = map_to_rank(
+              smem_addr(sm + C::kLand + buf * C::kLandChunk + ((size_t)slot * kBM + t) * C::RB),
+              static_cast<uint32_t>(owner));
+          const uint32_t mb = map_to_rank(smem_addr(&land_full[buf]), static_cast<uint32_t>(owner));
+          if (ok) {
+#pragma unroll
+            for (int c = 0; c < W; c += 8)
+              st_async_v4(dst + c * 2, pack_bf16(__uint_as_float(v[sl * W + c]), __uint_as_float(v[sl * W + c + 1])),
+                          pack_bf16(__uint_as_float(v[sl * W + c + 2]), __uint_as_float(v[sl * W + c + 3])),
+                          pack_bf16(__uint_as_float(v[sl * W + c + 4]), __uint_as_float(v[sl * W + c + 5])),
+                          pack_bf16(__uint_as_float(v[sl * W + c + 6]), __uint_as_float(v[sl * W + c + 7])), mb);
+            st_async_v4(dst + W * 2, __float_as_uint(den_own), __float_as_uint(bias), 0u, 0u, mb);
+          }
         }
-        // one release per warp covers its lanes' writes (they precede the warp barrier)
-        __syncwarp();
-        if (lane == 0)
-          for (int p = 0; p < NC; ++p)
-            if (p != rank) mbar_arrive_remote(map_to_rank(smem_addr(xch_full), static_cast<uint32_t>(p)));
         if (wg == wg_fin) {
           // my columns: every partial rescaled to the largest reference; mine
           // first, then the others in rank order
-          if (ok) ok = mbar_wait_cluster(xch_full, j & 1, wctx);
+          if (ok) ok = mbar_wait(&land_full[buf], (j / C::NB) & 1, wctx);
+          const uint8_t* land = sm + C::kLand + buf * C::kLandChunk;
           float bmax = bias;
-          for (int p = 0; p < NC; ++p) {
-            if (p == rank) continue;
-            bmax = fmaxf(bmax, __ldcg(xc + ((size_t)p * kBM + t) * kXW + kD + 1));
-          }
+          for (int sl = 0; sl < NC - 1; ++sl)
+            bmax = fmaxf(bmax, *reinterpret_cast<const float*>(land + ((size_t)sl * kBM + t) * C::RB + 2 * W + 4));
           const bool hi = (rank * W - col0) != 0;
           const float sc_own = ex2(bias - bmax);
           float acc[W];
 #pragma unroll
           for (int c = 0; c < W; ++c) acc[c] = sc_own * __uint_as_float(W == 64 ? v[c] : (hi ? v[(32 + c) & 63] : v[c]));
           float den = sc_own * den_own;
-          for (int p = 0; p < NC; ++p) {
-            if (p == rank) continue;
-            const float* lr = xc + ((size_t)p * kBM + t) * kXW;
-            const float sc = ex2(__ldcg(lr + kD + 1) - bmax);
+          for (int sl = 0; sl < NC - 1; ++sl) {
+            const uint8_t* lr = land + ((size_t)sl * kBM + t) * C::RB;
+            const float2 dr = *reinterpret_cast<const float2*>(lr + 2 * W);   // normaliser, reference
+            const float sc = ex2(dr.y - bmax);
 #pragma unroll
-            for (int c = 0; c < W; c += 4) {
-              const float4 p4 = __ldcg(reinterpret_cast<const float4*>(lr + rank * W + c));
-              acc[c] = fmaf(sc, p4.x, acc[c]);
-              acc[c + 1] = fmaf(sc, p4.y, acc[c + 1]);
-              acc[c + 2] = fmaf(sc, p4.z, acc[c + 2]);
-              acc[c + 3] = fmaf(sc, p4.w, acc[c + 3]);
+            for (int c = 0; c < W; c += 8) {
+              const uint4 p4 = *reinterpret_cast<const uint4*>(lr + c * 2);
+              const uint32_t w4[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                acc[c + 2 * e] = fmaf(sc, __uint_as_float(w4[e] << 16), acc[c + 2 * e]);
+                acc[c + 2 * e + 1] = fmaf(sc, __uint_as_float(w4[e] & 0xFFFF0000u), acc[c + 2 * e + 1]);
+              }
             }
-            den = fmaf(sc, __ldcg(lr + kD), den);
+            den = fmaf(sc, dr.x, den);
           }
-          // read: the writers may reuse this parity's rows two chunks on
+          // read: re-arm the buffer for chunk j + NB, then let its writers send
+          if (threadIdx.x == kEpiTid0 + kBM * wg_fin && ok) mbar_arrive_expect_tx(&land_full[buf], C::kLandChunk);
           __syncwarp();
           if (lane == 0)
-            for (int p = 0; p < NC; ++p)
-              if (p != rank) mbar_arrive_remote(map_to_rank(smem_addr(&xch_free[par]), static_cast<uint32_t>(p)));
+            for (int src = 0; src < NC; ++src)
+              if (src != rank)
+                mbar_arrive_remote(map_to_rank(smem_addr(&land_free[buf * 4 + rank]), static_cast<uint32_t>(src)));
           if (have && valid) {
             if (!(den > 0.f) || !isfinite(den)) report_status(prm.status, FAVOR_ERR_NONFINITE);
             const float inv = __fdividef(1.0f, den);
@@ -1285,7 +1298,8 @@ __global__ void __launch_bounds__(kThreads, 1) fs_causal_kernel(const __grid_con
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(x_free);
-        if (ok && c >= 1) ok = mbar_wait(ma_free, (c - 1) & 1, wctx);
+        // the masked scores go over phi(Q_c): O(c) = phi(Q_c) G_s must have read it
+        if (ok) ok = mbar_wait(oin_done, c & 1, wctx);
         if (ok) {
           // this warp's rows 32q .. 32q+31 against keys col0 .. col0+63:
           // entirely kept, entirely masked, or on the diagonal
@@ -1449,14 +1463,13 @@ cudaError_t launch_fs_causal(const void* Q, const void* K, const void* V, void* 
                              const FsCausalPlan& p, float scale, char* ws, int32_t* status, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, Q, s) || !make_map(&mk, K, s) || !make_map(&mv, V, s)) return cudaErrorInvalidValue;
-  const size_t smem = FsCausalCfg::kSmem;
+  const size_t smem = FsCausalCfg<NC>::kSmem;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(fs_causal_kernel<NC, FM>), smem);
   if (e != cudaSuccess) return e;
   FsCausalParams prm{};
   prm.key_ref = reinterpret_cast<const float*>(ws);
   prm.omega_img = reinterpret_cast<const uint8_t*>(ws + p.off_omega_img);
   prm.pre = reinterpret_cast<const float*>(ws + p.off_pre);
-  prm.xbuf = reinterpret_cast<float*>(ws + p.off_xbuf);
   prm.O = static_cast<__nv_bfloat16*>(O);
   prm.status = status;
   prm.L = s.L;
