@@ -53,7 +53,7 @@ struct TcPlan {
                                      // superchunks but the last)
   int out_tiles_per_cta, out_ctas;   // output kernel (bidir) / superchunks (causal)
   int sub_per_sc;                    // causal: state sub-splits per superchunk
-  size_t off_omega_img, off_counters, off_partS, off_state_img, bytes;
+  size_t off_omega_img, off_counters, off_partS, off_state_img, off_pre, bytes;
 };
 
 TcPlan tc_plan(bool causal, const Shape& s) {
@@ -101,6 +101,8 @@ TcPlan tc_plan(bool causal, const Shape& s) {
   off = align_up(off + (size_t)BH * p.n_fb * max(p.n_split, 1) * (s.d + 1) * kFB * sizeof(float), 1024);
   p.off_state_img = off;
   if (!causal) off = align_up(off + (size_t)BH * s.m * (s.d + 16) * 2, 1024);
+  p.off_pre = off;   // causal: fp32 [BH][n_fb][superchunks][d+1][128], each superchunk's initial state
+  if (causal) off = align_up(off + (size_t)BH * p.n_fb * p.out_ctas * (s.d + 1) * kFB * sizeof(float), 1024);
   p.bytes = off;
   return p;
 }
@@ -127,14 +129,19 @@ constexpr int kStateThreads = 384;   // warps 0 TMA, 1 MMA, 2-3 norms, 4-11 epil
 
 template <int D>
 struct StateCfg {
-  static constexpr int NS = 3;                     // K/V stages
+  // K and V have rings of their own: a K slot is released once the tile's
+  // projections have read it, a V slot once the state MMA has; the squared
+  // norms of a K tile live one slot longer than the tile (the epilogue reads
+  // them after the projection has released the K slot)
+  static constexpr int NK = 4, NV = 3, NN = NK + 1;
   static constexpr int kTileBytes = D * kBM * 2;   // one K or V tile
   static constexpr int kOmega = 0;                 // fp16 image, up to 256 x D
-  static constexpr int kStages = kOmega + 256 * D * 2;
-  static constexpr int kOnes = kStages + NS * 2 * kTileBytes;   // above every V tile
+  static constexpr int kK = kOmega + 256 * D * 2;
+  static constexpr int kV = kK + NK * kTileBytes;
+  static constexpr int kOnes = kV + NV * kTileBytes;             // above every V tile
   static constexpr int kPhi = kOnes + kOnesBytes;                // [fb][2 atoms][128][128 B]
-  static constexpr int kNorm = kPhi + 2 * 2 * kAtom;
-  static constexpr int kBars = kNorm + NS * kBM * 4;
+  static constexpr int kNorm = kPhi + 2 * 2 * kAtom;             // [NN][128]
+  static constexpr int kBars = kNorm + NN * kBM * 4;
   static constexpr int kSmem = kBars + 512 + 1024;
 };
 
@@ -147,10 +154,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBars);
-  uint64_t* full = bars;                      // [NS] K, V landed
-  uint64_t* empty = full + C::NS;             // [NS]
-  uint64_t* kn_full = empty + C::NS;          // [NS] K in fp16, norms written
-  uint64_t* p_full = kn_full + C::NS;         // [2] per feature block
+  uint64_t* k_full = bars;                    // [NK] K landed
+  uint64_t* k_empty = k_full + C::NK;         // [NK] the tile's projections have read it
+  uint64_t* v_full = k_empty + C::NK;         // [NV]
+  uint64_t* v_empty = v_full + C::NV;         // [NV] the state MMA has read it
+  uint64_t* kn_full = v_empty + C::NV;        // [NN] K in fp16, norms written
+  uint64_t* p_full = kn_full + C::NN;         // [2] per feature block
   uint64_t* p_free = p_full + 2;              // [2]
   uint64_t* phi_full = p_free + 2;            // [2]
   uint64_t* phi_free = phi_full + 2;          // [2]
@@ -159,7 +168,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* is_last = const_cast<int*>(abort_flag) + 1;
-  float* norm_s = reinterpret_cast<float*>(sm + C::kNorm);   // [NS][128]
+  float* norm_s = reinterpret_cast<float*>(sm + C::kNorm);   // [NN][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x, bh = blockIdx.y;
@@ -170,11 +179,15 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
   constexpr uint32_t S_COL = 256;              // S~ of block fb at S_COL + 128 fb; P at 0
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NS; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-      mbar_init(&kn_full[i], kNormWarps);
+    for (int i = 0; i < C::NK; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
     }
+    for (int i = 0; i < C::NV; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < C::NN; ++i) mbar_init(&kn_full[i], kNormWarps);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 1);
       mbar_init(&p_free[i], kEpiWarps / NFB);     // the warps that own block i
@@ -205,24 +218,39 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
       prefetch_tmap(&mapV);
       mbar_arrive_expect_tx(setup_bar, M * D * 2);
       bulk_load(sm + C::kOmega, prm.omega_img, M * D * 2, setup_bar);
-      int last_issue[C::NS];
-      for (int i = 0; i < C::NS; ++i) last_issue[i] = -1;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int st = i % C::NS;
-        if (i >= C::NS && !mbar_wait(&empty[st], ((i / C::NS) - 1) & 1, wctx)) break;
-        mbar_arrive_expect_tx(&full[st], 2 * C::kTileBytes);
-        uint8_t* kt = sm + C::kStages + st * 2 * C::kTileBytes;
-        uint8_t* vt = kt + C::kTileBytes;
-        const int row = (tile0 + i) * kBM;
+      // K tile x goes to K slot x % NK once the projections of tile x - NK
+      // have read it, V tile x to V slot x % NV once the state MMA of tile
+      // x - NV has; K is issued ahead of V
+      Watchdog wd(wctx);
+      int nk = 0, nv = 0;
+      bool ok = true;
+      while (ok && (nk < n_tiles || nv < n_tiles)) {
+        bool progress = false;
+        if (nk < n_tiles &&
+            (nk < C::NK || mbar_test_wait(smem_addr(&k_empty[nk % C::NK]), ((nk / C::NK) - 1) & 1))) {
+          const int st = nk % C::NK;
+          mbar_arrive_expect_tx(&k_full[st], C::kTileBytes);
 #pragma unroll
-        for (int a = 0; a < D / 64; ++a) {
-          tma_load_3d(kt + a * kAtom, &mapK, a * 64, row, bh, &full[st]);
-          tma_load_3d(vt + a * kAtom, &mapV, a * 64, row, bh, &full[st]);
+          for (int a = 0; a < D / 64; ++a)
+            tma_load_3d(sm + C::kK + st * C::kTileBytes + a * kAtom, &mapK, a * 64, (tile0 + nk) * kBM, bh, &k_full[st]);
+          ++nk;
+          progress = true;
         }
-        last_issue[st] = i;
+        if (nv < nk && (nv < C::NV || mbar_test_wait(smem_addr(&v_empty[nv % C::NV]), ((nv / C::NV) - 1) & 1))) {
+          const int st = nv % C::NV;
+          mbar_arrive_expect_tx(&v_full[st], C::kTileBytes);
+#pragma unroll
+          for (int a = 0; a < D / 64; ++a)
+            tma_load_3d(sm + C::kV + st * C::kTileBytes + a * kAtom, &mapV, a * 64, (tile0 + nv) * kBM, bh, &v_full[st]);
+          ++nv;
+          progress = true;
+        }
+        if (progress) wd.progress();
+        else ok = wd.idle();
       }
-      for (int st = 0; st < C::NS; ++st)
-        if (last_issue[st] >= 0) mbar_wait(&full[st], (last_issue[st] / C::NS) & 1, wctx);
+      // drain: the last loads of each ring have landed
+      for (int x = max(0, nk - C::NK); x < nk; ++x) mbar_wait(&k_full[x % C::NK], (x / C::NK) & 1, wctx);
+      for (int x = max(0, nv - C::NV); x < nv; ++x) mbar_wait(&v_full[x % C::NV], (x / C::NV) & 1, wctx);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -239,35 +267,36 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
       while (ok && (pi < n_tiles || si < n_tiles)) {
         bool progress = false;
         if (pi < n_tiles) {
-          const int st = pi % C::NS;
-          const bool ready = (pf > 0 || mbar_test_wait(smem_addr(&kn_full[st]), (pi / C::NS) & 1)) &&
+          const int ks = pi % C::NK;
+          const bool ready = (pf > 0 || mbar_test_wait(smem_addr(&kn_full[pi % C::NN]), (pi / C::NN) & 1)) &&
                              (pi == 0 || mbar_test_wait(smem_addr(&p_free[pf]), (pi - 1) & 1));
           if (ready) {
             tc_fence_after();
-            const uint64_t a0 = sdesc(smem_addr(sm + C::kStages + st * 2 * C::kTileBytes), 16, 1024);
+            const uint64_t a0 = sdesc(smem_addr(sm + C::kK + ks * C::kTileBytes), 16, 1024);
             const uint64_t b0 = sdesc(omega_a + pf * kFB * 128, 16, 1024);
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
               mma_bf16(tmem + pf * kFB, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
             mma_commit(&p_full[pf]);
+            if (pf == NFB - 1) mma_commit(&k_empty[ks]);
             if (++pf == NFB) { pf = 0; ++pi; }
             progress = true;
           }
         }
         if (si < n_tiles) {
-          const int st = si % C::NS;
+          const int vs = si % C::NV;
           const bool ready = mbar_test_wait(smem_addr(&phi_full[sf]), si & 1) &&
-                             (sf > 0 || mbar_test_wait(smem_addr(&full[st]), (si / C::NS) & 1));
+                             (sf > 0 || mbar_test_wait(smem_addr(&v_full[vs]), (si / C::NV) & 1));
           if (ready) {
             tc_fence_after();
-            const uint32_t v_a = smem_addr(sm + C::kStages + st * 2 * C::kTileBytes + C::kTileBytes);
+            const uint32_t v_a = smem_addr(sm + C::kV + vs * C::kTileBytes);
             const uint64_t a0 = sdesc(smem_addr(sm + C::kPhi + sf * 2 * kAtom), kAtom, 1024);
             const uint64_t b0 = sdesc(v_a, ones_a - v_a, 1024);
 #pragma unroll
             for (int k = 0; k < kBM / 16; ++k)
               mma_bf16(tmem + S_COL + sf * 128, dadd(a0, kstep_mn(k)), vones_k(b0, k), id_state, (si > 0) || (k > 0));
             mma_commit(&phi_free[sf]);
-            if (sf == NFB - 1) mma_commit(&empty[st]);
+            if (sf == NFB - 1) mma_commit(&v_empty[vs]);
             if (++sf == NFB) { sf = 0; ++si; }
             progress = true;
           }
@@ -279,19 +308,19 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
       mbar_wait(done_bar, 0, wctx);
     }
   } else if (warp < 2 + kNormWarps) {
-    // squared norms of the K rows of each stage; K rewritten as fp16
+    // squared norms of the K rows; K rewritten as fp16
     for (int i = 0; i < n_tiles; ++i) {
-      const int st = i % C::NS;
-      if (!mbar_wait(&full[st], (i / C::NS) & 1, wctx)) break;
-      uint8_t* kt = sm + C::kStages + st * 2 * C::kTileBytes;
+      const int ks = i % C::NK, ns = i % C::NN;
+      if (!mbar_wait(&k_full[ks], (i / C::NK) & 1, wctx)) break;
+      uint8_t* kt = sm + C::kK + ks * C::kTileBytes;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int r = (warp - 2) * 64 + lane + 32 * j;
-        norm_s[st * kBM + r] = tile_row_sq_to_f16<D>(kt, r);
+        norm_s[ns * kBM + r] = tile_row_sq_to_f16<D>(kt, r);
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&kn_full[st]);
+      if (lane == 0) mbar_arrive(&kn_full[ns]);
     }
   } else {
     // ---------------- epilogue: two warpgroups x 128 lanes ----------------
@@ -314,11 +343,11 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     const int c0 = (NFB == 2) ? 0 : col0;
     const uint32_t phi_a = smem_addr(sm + C::kPhi + my_fb * 2 * kAtom);
     for (int i = 0; ok && i < n_tiles; ++i) {
-      const int st = i % C::NS;
-      if (!mbar_wait(&kn_full[st], (i / C::NS) & 1, wctx)) { ok = false; break; }
+      const int ns = i % C::NN;
+      if (!mbar_wait(&kn_full[ns], (i / C::NN) & 1, wctx)) { ok = false; break; }
       // rows past L get 2^-inf = 0
       const bool valid = (tile0 + i) * kBM + t < prm.L;
-      const float bias = !valid ? INFINITY : (FM == FAVOR_FM_PRF ? (hs2 * norm_s[st * kBM + t] + R) * kLog2e : 0.f);
+      const float bias = !valid ? INFINITY : (FM == FAVOR_FM_PRF ? (hs2 * norm_s[ns * kBM + t] + R) * kLog2e : 0.f);
       if (!mbar_wait(&p_full[my_fb], i & 1, wctx)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
@@ -447,7 +476,7 @@ constexpr int kOutThreads = 384;   // warps 0 TMA, 1 MMA, 2-3 norms, 4-11 epilog
 
 template <int D>
 struct OutCfg {
-  static constexpr int NSQ = 3;
+  static constexpr int NSQ = 4;
   static constexpr int kTileBytes = D * kBM * 2;
   static constexpr int kOmega = 0;                          // fp16 image, up to 256 x D
   static constexpr int kState = kOmega + 256 * D * 2;       // bf16 S~ image, up to 256 x (D + 16)
@@ -743,9 +772,9 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
 struct CausalParams {
   const float* key_ref;   // row-norm maxima (key_reference)
   const uint8_t* omega_img;
-  const float* partS;     // [BH][n_fb][n_split][d+1][128], sub_per_sc per superchunk
+  const float* pre;       // [BH][n_fb][n_sc][d+1][128] initial states (superchunks > 0)
   int32_t* status;
-  int L, m, n_split, tiles_per_sc, sub_per_sc;
+  int L, m, n_sc, tiles_per_sc;
   float scale;
 };
 
@@ -1022,24 +1051,26 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
     constexpr int kGGroups = D / 8 + 1;
     const int g_first = wg ? (kGGroups + 1) / 2 : 0;
     const int g_end = wg ? kGGroups : (kGGroups + 1) / 2;
-    // G_init = sum of the earlier superchunks' states, in superchunk order
+    // G_init: the superchunk's initial state (the fixed-order sum of the
+    // earlier superchunks' partial states, formed by the prefix kernel); all
+    // of this thread's loads in flight together
     for (int fb = 0; fb < NFB; ++fb) {
-      const float* src = prm.partS + (((size_t)bh * NFB + fb) * max(prm.n_split, 1)) * (D + 1) * kFB;
-      for (int g = 0; g < ng16; ++g) {
-        // partials outer, columns inner: the 16 loads of a partial are in flight together
-        float acc[16];
+      const float* src = prm.pre + (((size_t)bh * NFB + fb) * prm.n_sc + sc) * (D + 1) * kFB;
+      constexpr int kMaxG = (kG0 > GN - kG0 ? kG0 : GN - kG0) / 16;
+      float acc[kMaxG][16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-        for (int p = 0; p < sc * prm.sub_per_sc; ++p) {
+      for (int g = 0; g < kMaxG; ++g)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int n = n0 + 16 * g + j;
-            if (n <= D) acc[j] += src[((size_t)p * (D + 1) + n) * kFB + t];
-          }
+        for (int j = 0; j < 16; ++j) {
+          const int n = n0 + 16 * g + j;
+          acc[g][j] = (sc > 0 && g < ng16 && n <= D) ? src[(size_t)n * kFB + t] : 0.f;
         }
+#pragma unroll
+      for (int g = 0; g < kMaxG; ++g) {
+        if (g >= ng16) break;
         uint32_t r[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(acc[j]);
+        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(acc[g][j]);
         tmem_st16(tmem + lane_off + G_COL + fb * GN + n0 + 16 * g, r);
       }
     }
@@ -1308,13 +1339,12 @@ cudaError_t launch_causal(const void* Q, const void* K, const void* V, void* O, 
   CausalParams prm{};
   prm.key_ref = reinterpret_cast<const float*>(ws);
   prm.omega_img = reinterpret_cast<const uint8_t*>(ws + p.off_omega_img);
-  prm.partS = reinterpret_cast<const float*>(ws + p.off_partS);
+  prm.pre = reinterpret_cast<const float*>(ws + p.off_pre);
   prm.status = status;
   prm.L = s.L;
   prm.m = s.m;
-  prm.n_split = p.n_split;
+  prm.n_sc = p.out_ctas;
   prm.tiles_per_sc = p.out_tiles_per_cta;
-  prm.sub_per_sc = p.sub_per_sc;
   prm.scale = scale;
   const size_t smem = CausalCfg<D>::kSmem;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(causal_kernel<D, M, FM>), smem);
@@ -1347,8 +1377,13 @@ cudaError_t tc_state_fm(bool causal, const void* K, const void* V, const float* 
                               causal ? nullptr : reinterpret_cast<uint32_t*>(w + p.off_counters), causal ? 0 : s.BH(),
                               stream);
   if (e != cudaSuccess) return e;
-  return s.m == 256 ? launch_state<64, 256, FM>(K, V, s, p, scale, w, status, stream)
-                    : launch_state<64, 128, FM>(K, V, s, p, scale, w, status, stream);
+  e = s.m == 256 ? launch_state<64, 256, FM>(K, V, s, p, scale, w, status, stream)
+                 : launch_state<64, 128, FM>(K, V, s, p, scale, w, status, stream);
+  if (e != cudaSuccess || !causal || p.n_split < 1) return e;
+  state_prefix_kernel<64><<<dim3(p.n_fb * 65, s.BH()), kFB, 0, stream>>>(
+      reinterpret_cast<const float*>(w + p.off_partS), reinterpret_cast<float*>(w + p.off_pre), p.n_fb, p.n_split,
+      p.sub_per_sc, p.out_ctas);
+  return cudaGetLastError();
 }
 
 template <int FM>

@@ -769,30 +769,6 @@ __global__ void __launch_bounds__(kThreads, 1) fs_output_kernel(const __grid_con
 // states of the sub-splits of superchunks 0 .. sc - 1 (block = (head,
 // feature block, state row n), thread = feature; eight loads in flight)
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kFB) fs_prefix_kernel(const float* __restrict__ partS, float* __restrict__ pre,
-                                                      int n_fb, int n_split, int sub_per_sc, int n_sc) {
-  const int f = threadIdx.x;
-  const int n = blockIdx.x % (kD + 1), hb = blockIdx.y * n_fb + blockIdx.x / (kD + 1);
-  constexpr size_t kStride = (size_t)(kD + 1) * kFB;
-  const float* src = partS + (size_t)hb * max(n_split, 1) * kStride + (size_t)n * kFB + f;
-  float* dst = pre + (size_t)hb * n_sc * kStride + (size_t)n * kFB + f;
-  float acc = 0.f;
-  for (int p0 = 0; p0 < n_split; p0 += 8) {
-    float v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = (p0 + u < n_split) ? src[(size_t)(p0 + u) * kStride] : 0.f;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int p = p0 + u;
-      if (p >= n_split) break;
-      if (p % sub_per_sc == 0) dst[(size_t)(p / sub_per_sc) * kStride] = acc;
-      acc += v[u];
-    }
-  }
-  dst[(size_t)(n_sc - 1) * kStride] = acc;
-}
-
-// ---------------------------------------------------------------------------
 // causal kernel: a cluster of NC CTAs (NC = m / 128) per superchunk of one
 // head, walking its 128-token chunks; CTA rank r holds feature block r of
 // Omega and the block's rows of the running state G_r (fp32, tensor memory,
@@ -1539,7 +1515,7 @@ cudaError_t fs_state(bool causal, const void* K, const void* V, const float* ome
                           : launch_fs_state<FAVOR_FM_PRF>(K, V, s, sl, scale, w, status, stream);
   if (e != cudaSuccess || !causal) return e;
   const FsCausalPlan p = fsc_plan(s);
-  fs_prefix_kernel<<<dim3(p.n_fb * (kD + 1), s.BH()), kFB, 0, stream>>>(
+  state_prefix_kernel<kD><<<dim3(p.n_fb * (kD + 1), s.BH()), kFB, 0, stream>>>(
       reinterpret_cast<const float*>(w + p.off_partS), reinterpret_cast<float*>(w + p.off_pre), p.n_fb, p.n_split,
       p.sub_per_sc, p.n_sc);
   return cudaGetLastError();

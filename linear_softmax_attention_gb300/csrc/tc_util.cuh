@@ -60,7 +60,11 @@ __device__ __forceinline__ float tile_row_sq_to_f16(uint8_t* tile, int t) {
 #pragma unroll
   for (int c = 0; c < NC; ++c)
     v[c] = *reinterpret_cast<const uint4*>(tile + (c >> 3) * kAtom + t * 128 + (((c & 7) ^ (t & 7)) << 4));
-  float acc = 0.f;
+  // eight partial sums (one per element position of a 16-byte chunk) keep
+  // the dependent chain of multiply-adds short
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
     const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
@@ -69,8 +73,8 @@ __device__ __forceinline__ float tile_row_sq_to_f16(uint8_t* tile, int t) {
     for (int j = 0; j < 4; ++j) {
       const float lo = __uint_as_float(w[j] << 16);
       const float hi = __uint_as_float(w[j] & 0xFFFF0000u);
-      acc = fmaf(lo, lo, acc);
-      acc = fmaf(hi, hi, acc);
+      acc[2 * j] = fmaf(lo, lo, acc[2 * j]);
+      acc[2 * j + 1] = fmaf(hi, hi, acc[2 * j + 1]);
       o[j] = pack_f16_sat(lo, hi);
     }
     v[c] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -78,7 +82,7 @@ __device__ __forceinline__ float tile_row_sq_to_f16(uint8_t* tile, int t) {
 #pragma unroll
   for (int c = 0; c < NC; ++c)
     *reinterpret_cast<uint4*>(tile + (c >> 3) * kAtom + t * 128 + (((c & 7) ^ (t & 7)) << 4)) = v[c];
-  return acc;
+  return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
 // tcgen05.ld 32x32b.x32 into r[OFF .. OFF+31]
@@ -214,6 +218,35 @@ __device__ __forceinline__ void tmem_state_to_rows(uint32_t tmem, uint32_t g_col
                         pack_bf16(__uint_as_float(hi[u][2]), __uint_as_float(hi[u][3])));
     }
   }
+}
+
+// Initial causal states of the superchunks of each (head, feature block):
+// superchunk sc starts from the fixed-order sum of the partial states of the
+// sub-splits of superchunks 0 .. sc - 1 (block = (head, feature block, state
+// row n), thread = feature; eight loads in flight).  partS is
+// [heads x blocks][n_split][D + 1][128], pre [heads x blocks][n_sc][D + 1][128].
+template <int D>
+__global__ void __launch_bounds__(kFB) state_prefix_kernel(const float* __restrict__ partS, float* __restrict__ pre,
+                                                           int n_fb, int n_split, int sub_per_sc, int n_sc) {
+  const int f = threadIdx.x;
+  const int n = blockIdx.x % (D + 1), hb = blockIdx.y * n_fb + blockIdx.x / (D + 1);
+  constexpr size_t kStride = (size_t)(D + 1) * kFB;
+  const float* src = partS + (size_t)hb * max(n_split, 1) * kStride + (size_t)n * kFB + f;
+  float* dst = pre + (size_t)hb * n_sc * kStride + (size_t)n * kFB + f;
+  float acc = 0.f;
+  for (int p0 = 0; p0 < n_split; p0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = (p0 + u < n_split) ? src[(size_t)(p0 + u) * kStride] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int p = p0 + u;
+      if (p >= n_split) break;
+      if (p % sub_per_sc == 0) dst[(size_t)(p / sub_per_sc) * kStride] = acc;
+      acc += v[u];
+    }
+  }
+  dst[(size_t)(n_sc - 1) * kStride] = acc;
 }
 
 // ---------------------------------------------------------------------------
