@@ -11,13 +11,16 @@
 namespace favor {
 namespace tc {
 
-// A bounded wait gives up after this long (a correct kernel waits microseconds).
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// A bounded wait gives up after this many SM cycles, about a second at the
+// GB300's clocks (a correct kernel waits microseconds).  Counted with the
+// SM's own cycle counter, which the waits below read once per probe.
+constexpr long long kWaitLimitCycles = 2200000000ll;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+__device__ __forceinline__ long long sm_cycles() { return clock64(); }
 __device__ __forceinline__ uint64_t global_timer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -74,11 +77,11 @@ struct WaitCtx {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& ctx) {
   const uint32_t a = smem_addr(bar);
   if (mbar_try_wait(a, parity)) return true;
-  const uint64_t t0 = global_timer();
+  const long long t0 = sm_cycles();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
     if (*ctx.abort_flag) return false;
-    if (global_timer() - t0 > kWaitLimitNs) {
+    if (sm_cycles() - t0 > kWaitLimitCycles) {
       *ctx.abort_flag = 1;
       report_status(ctx.status, FAVOR_ERR_TIMEOUT);
       return false;
@@ -91,12 +94,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 // returns false once the kernel aborts or no step was ready for the wait limit.
 struct Watchdog {
   const WaitCtx& ctx;
-  uint64_t t_last;
-  __device__ explicit Watchdog(const WaitCtx& c) : ctx(c), t_last(global_timer()) {}
-  __device__ void progress() { t_last = global_timer(); }
+  long long t_last;
+  __device__ explicit Watchdog(const WaitCtx& c) : ctx(c), t_last(sm_cycles()) {}
+  __device__ void progress() { t_last = sm_cycles(); }
   __device__ bool idle() {
     if (*ctx.abort_flag) return false;
-    if (global_timer() - t_last > kWaitLimitNs) {
+    if (sm_cycles() - t_last > kWaitLimitCycles) {
       *ctx.abort_flag = 1;
       report_status(ctx.status, FAVOR_ERR_TIMEOUT);
       return false;
@@ -154,11 +157,11 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtx& ctx) {
   const uint32_t a = smem_addr(bar);
   if (mbar_try_wait_cluster(a, parity)) return true;
-  const uint64_t t0 = global_timer();
+  const long long t0 = sm_cycles();
   while (true) {
     if (mbar_try_wait_cluster(a, parity)) return true;
     if (*ctx.abort_flag) return false;
-    if (global_timer() - t0 > kWaitLimitNs) {
+    if (sm_cycles() - t0 > kWaitLimitCycles) {
       *ctx.abort_flag = 1;
       report_status(ctx.status, FAVOR_ERR_TIMEOUT);
       return false;
