@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--decode-steps", type=int, default=200)
     ap.add_argument("--relu-steps", type=int, default=100)
-    ap.add_argument("--elu-steps", type=int, default=10)
+    ap.add_argument("--elu-steps", type=int, default=100)
     ap.add_argument("--bwd-steps", type=int, default=10)
     ap.add_argument("--config-steps", type=int, default=20,
                     help="calls timed per configuration line (0: no per-configuration lines)")
@@ -484,13 +484,8 @@ def run_gpu(args, rank, world, local_rank):
                                    status, dev, tokens_per_step)
     elu1 = None
     if args.elu_steps > 0:
-        # 1 + elu runs on the CUDA-core kernels: their workspaces
-        ws_be = favor.new_workspace(False, B, H, L, d, m, dt, device=dev, feature_map="elu1")
-        ws_ce = favor.new_workspace(True, B, H, L, d, m, dt, device=dev, feature_map="elu1")
-        elu1 = measure_feature_map(favor, "elu1", args.elu_steps, sets, omegas[0], s, ws_be, ws_ce, O_b, O_c,
-                                   stream, status, dev, tokens_per_step)
-        elu1["path"] = "CUDA-core kernels"
-        del ws_be, ws_ce
+        elu1 = measure_feature_map(favor, "elu1", args.elu_steps, sets, omegas[0], s, ws_b, ws_c, O_b, O_c, stream,
+                                   status, dev, tokens_per_step)
     configs = measure_configs(favor, args, dev, stream, status, hbm, tc_burst) if args.config_steps > 0 else None
     # dominant kernel: largest share of the step
     # the stage times come from sub-millisecond graph replays of one kernel

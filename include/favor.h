@@ -82,7 +82,9 @@ typedef enum favor_dtype {
  * ("From Performer to Linear Attention", the linear-attention feature map it
  * compares against; the "Performer" digest names it as Linear Attention's),
  * in the same slot as ReLU; with Omega = I_d (m = d) it is linear attention
- * itself.  Its calls run on the CUDA-core kernels (any supported shape).
+ * itself.  Every map takes the path of the plain call for its shape (the
+ * tensor-core kernels where they apply, the CUDA-core kernels otherwise):
+ * the map changes only the epilogue that forms the features.
  */
 typedef enum favor_feature_map {
   FAVOR_FM_PRF = 0,
@@ -176,11 +178,9 @@ favor_status favor_fwd_causal(const void* Q, const void* K, const void* V, void*
 /*
  * favor_fwd_bidir_fm, favor_fwd_causal_fm — favor_fwd_bidir and
  * favor_fwd_causal with the feature map `fm` (favor_feature_map) in place of
- * the positive random features; same arguments.  FAVOR_FM_PRF and
- * FAVOR_FM_RELU take the same workspace sizes and paths as the plain calls;
- * FAVOR_FM_ELU1 runs on the CUDA-core kernels and needs
- * favor_workspace_bytes_fm(..., FAVOR_FM_ELU1) bytes (more than
- * favor_workspace_bytes where the plain call takes the tensor cores).
+ * the positive random features; same arguments.  Every map takes the same
+ * path and workspace size as the plain call (favor_workspace_bytes_fm equals
+ * favor_workspace_bytes for each map).
  * A row whose features are all zero (every s w_i.q <= 0 under ReLU) has a
  * zero normaliser: its output is NaN and dev_status gets
  * FAVOR_ERR_NONFINITE (1 + elu is positive: it never has one).  fm outside

@@ -143,8 +143,8 @@ def new_omega(seed: int, m: int, d: int, orthogonal: bool = True, device="cuda")
 
 
 def workspace_bytes(causal: bool, B: int, H: int, L: int, d: int, m: int, dtype, feature_map=None) -> int:
-    """Workspace bytes of fwd_bidir / fwd_causal for this shape (and feature
-    map: "elu1" runs on the CUDA-core kernels, whose workspace differs)."""
+    """Workspace bytes of fwd_bidir / fwd_causal for this shape and feature
+    map (every map takes the plain call's path and size)."""
     if feature_map in (None, "prf"):
         n = load().favor_workspace_bytes(int(causal), B, H, L, d, m, _DT[dtype])
     else:
@@ -195,8 +195,7 @@ def _out_like(x, O):
 def fwd_bidir(Q, K, V, omega, qk_scale, workspace, O=None, dev_status=None, stream=None, feature_map=None):
     """Bidirectional FAVOR+; returns O [B, H, L, d] (dtype of Q).  feature_map:
     None or "prf" (positive random features, the softmax kernel), "relu"
-    (Performer-ReLU) or "elu1" (1 + elu, the linear-attention map; its
-    workspace comes from new_workspace(..., feature_map="elu1"))."""
+    (Performer-ReLU) or "elu1" (1 + elu, the linear-attention map)."""
     fm = None if feature_map in (None, "prf") else feature_map
     return _call("favor_fwd_bidir", Q, K, V, _out_like(Q, O), omega, qk_scale, workspace, dev_status, stream, fm)
 

@@ -74,10 +74,11 @@ favor_status shape_ok(int B, int H, int L, int d, int m, favor_dtype dt) {
 
 bool use_tc(bool causal, int d, int m, favor_dtype dt) { return favor::tc_supported(causal, d, m, dt == FAVOR_BF16); }
 
-// the tensor-core kernels carry the softmax and ReLU features; 1 + elu runs
-// on the CUDA-core kernels for every shape
+// the tensor-core kernels carry every feature map (the map only changes
+// their epilogue)
 bool use_tc_fm(bool causal, int d, int m, favor_dtype dt, int fm) {
-  return fm != FAVOR_FM_ELU1 && use_tc(causal, d, m, dt);
+  (void)fm;
+  return use_tc(causal, d, m, dt);
 }
 
 bool fm_ok(int fm) { return fm == FAVOR_FM_PRF || fm == FAVOR_FM_RELU || fm == FAVOR_FM_ELU1; }

@@ -1401,16 +1401,18 @@ cudaError_t tc_output_fm(bool causal, const void* Q, const void* K, const void* 
 cudaError_t tc_state(bool causal, const void* K, const void* V, const float* omega, float scale, const Shape& s,
                      void* ws, int32_t* status, cudaStream_t stream, int fm) {
   if (s.d != 64) return fs_state(causal, K, V, omega, scale, s, ws, status, stream, fm);
-  return fm == FAVOR_FM_RELU ? tc_state_fm<FAVOR_FM_RELU>(causal, K, V, omega, scale, s, ws, status, stream)
-                             : tc_state_fm<FAVOR_FM_PRF>(causal, K, V, omega, scale, s, ws, status, stream);
+  if (fm == FAVOR_FM_RELU) return tc_state_fm<FAVOR_FM_RELU>(causal, K, V, omega, scale, s, ws, status, stream);
+  if (fm == FAVOR_FM_ELU1) return tc_state_fm<FAVOR_FM_ELU1>(causal, K, V, omega, scale, s, ws, status, stream);
+  return tc_state_fm<FAVOR_FM_PRF>(causal, K, V, omega, scale, s, ws, status, stream);
 }
 
 cudaError_t tc_output(bool causal, const void* Q, const void* K, const void* V, void* O, const float* omega,
                       float scale, const Shape& s, void* ws, int32_t* status, cudaStream_t stream, int fm) {
   (void)omega;
   if (s.d != 64) return fs_output(causal, Q, K, V, O, scale, s, ws, status, stream, fm);
-  return fm == FAVOR_FM_RELU ? tc_output_fm<FAVOR_FM_RELU>(causal, Q, K, V, O, s, scale, ws, status, stream)
-                             : tc_output_fm<FAVOR_FM_PRF>(causal, Q, K, V, O, s, scale, ws, status, stream);
+  if (fm == FAVOR_FM_RELU) return tc_output_fm<FAVOR_FM_RELU>(causal, Q, K, V, O, s, scale, ws, status, stream);
+  if (fm == FAVOR_FM_ELU1) return tc_output_fm<FAVOR_FM_ELU1>(causal, Q, K, V, O, s, scale, ws, status, stream);
+  return tc_output_fm<FAVOR_FM_PRF>(causal, Q, K, V, O, s, scale, ws, status, stream);
 }
 
 }  // namespace favor

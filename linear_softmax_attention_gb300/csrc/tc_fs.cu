@@ -1511,8 +1511,9 @@ cudaError_t fs_state(bool causal, const void* K, const void* V, const float* ome
                               reinterpret_cast<uint8_t*>(w + sl.off_omega_img),
                               n_counters ? reinterpret_cast<uint32_t*>(w + off_counters) : nullptr, n_counters, stream);
   if (e != cudaSuccess) return e;
-  e = fm == FAVOR_FM_RELU ? launch_fs_state<FAVOR_FM_RELU>(K, V, s, sl, scale, w, status, stream)
-                          : launch_fs_state<FAVOR_FM_PRF>(K, V, s, sl, scale, w, status, stream);
+  e = fm == FAVOR_FM_RELU   ? launch_fs_state<FAVOR_FM_RELU>(K, V, s, sl, scale, w, status, stream)
+      : fm == FAVOR_FM_ELU1 ? launch_fs_state<FAVOR_FM_ELU1>(K, V, s, sl, scale, w, status, stream)
+                            : launch_fs_state<FAVOR_FM_PRF>(K, V, s, sl, scale, w, status, stream);
   if (e != cudaSuccess || !causal) return e;
   const FsCausalPlan p = fsc_plan(s);
   state_prefix_kernel<kD><<<dim3(p.n_fb * (kD + 1), s.BH()), kFB, 0, stream>>>(
@@ -1526,12 +1527,14 @@ cudaError_t fs_output(bool causal, const void* Q, const void* K, const void* V, 
   char* w = static_cast<char*>(ws);
   if (causal) {
     const FsCausalPlan p = fsc_plan(s);
-    return fm == FAVOR_FM_RELU ? fs_causal_nc<FAVOR_FM_RELU>(Q, K, V, O, s, p, scale, w, status, stream)
-                               : fs_causal_nc<FAVOR_FM_PRF>(Q, K, V, O, s, p, scale, w, status, stream);
+    if (fm == FAVOR_FM_RELU) return fs_causal_nc<FAVOR_FM_RELU>(Q, K, V, O, s, p, scale, w, status, stream);
+    if (fm == FAVOR_FM_ELU1) return fs_causal_nc<FAVOR_FM_ELU1>(Q, K, V, O, s, p, scale, w, status, stream);
+    return fs_causal_nc<FAVOR_FM_PRF>(Q, K, V, O, s, p, scale, w, status, stream);
   }
   const FsPlan p = fs_plan(s);
-  return fm == FAVOR_FM_RELU ? fs_output_nc<FAVOR_FM_RELU>(Q, O, s, p, scale, w, status, stream)
-                             : fs_output_nc<FAVOR_FM_PRF>(Q, O, s, p, scale, w, status, stream);
+  if (fm == FAVOR_FM_RELU) return fs_output_nc<FAVOR_FM_RELU>(Q, O, s, p, scale, w, status, stream);
+  if (fm == FAVOR_FM_ELU1) return fs_output_nc<FAVOR_FM_ELU1>(Q, O, s, p, scale, w, status, stream);
+  return fs_output_nc<FAVOR_FM_PRF>(Q, O, s, p, scale, w, status, stream);
 }
 
 }  // namespace favor

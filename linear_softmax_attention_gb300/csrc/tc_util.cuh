@@ -118,8 +118,8 @@ __device__ __forceinline__ void exp_pack(uint32_t (&x)[N], float c1, float b, bo
   }
 }
 
-// Feature maps: positive random features (the softmax kernel) or
-// Performer-ReLU, relu(s w.x) ("Rethinking Attention with Performers"
+// Feature maps: positive random features (the softmax kernel),
+// Performer-ReLU, relu(s w.x), or 1 + elu (below) ("Rethinking Attention with Performers"
 // summary, §2 generalized kernelizable attention: other kernels by changing
 // the feature-map function).  ReLU: b = 0 on valid rows and +inf past the
 // sequence end (feature 0); "y < 0 ? 0 : y" keeps a NaN a NaN.
@@ -134,9 +134,25 @@ __device__ __forceinline__ void relu_pack(uint32_t (&x)[N], float c1, float b) {
     x[j] = pack_bf16(y0, y1);
   }
 }
+// 1 + elu(a) of a = s w.x - b: 1 + a for a >= 0, e^a below ("From
+// Performer to Linear Attention": the linear-attention feature map, here in
+// the slot of f(w_i^T x)).  Past the sequence end b = +inf gives e^-inf = 0;
+// a NaN fails a >= 0 and stays a NaN.
+template <int N>
+__device__ __forceinline__ void elu1_pack(uint32_t (&x)[N], float c1, float b) {
+#pragma unroll
+  for (int j = 0; j < N / 2; ++j) {
+    const float a0 = fmaf(__uint_as_float(x[2 * j]), c1, -b);
+    const float a1 = fmaf(__uint_as_float(x[2 * j + 1]), c1, -b);
+    const float y0 = a0 >= 0.f ? 1.f + a0 : ex2(a0 * kLog2e);
+    const float y1 = a1 >= 0.f ? 1.f + a1 : ex2(a1 * kLog2e);
+    x[j] = pack_bf16(y0, y1);
+  }
+}
 template <int FM, int N>
 __device__ __forceinline__ void feature_pack(uint32_t (&x)[N], float c1, float b) {
   if constexpr (FM == FAVOR_FM_PRF) exp_pack<N>(x, c1, b, true);
+  else if constexpr (FM == FAVOR_FM_ELU1) elu1_pack<N>(x, c1, b);
   else relu_pack<N>(x, c1, b);
 }
 // multiplier of the projection in the feature exponent / argument

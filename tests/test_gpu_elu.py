@@ -1,7 +1,7 @@
-"""GPU parity of the 1 + elu feature map (favor_fwd_*_fm with FAVOR_FM_ELU1,
-on the CUDA-core kernels for every shape) against the fp64 oracle's elu1
-features; bars as for the softmax features.  Omega = I gives plain linear
-attention."""
+"""GPU parity of the 1 + elu feature map (favor_fwd_*_fm with FAVOR_FM_ELU1)
+against the fp64 oracle's elu1 features, on the tensor-core kernels (bf16,
+d = 64 and 128) and the CUDA-core kernels (fp32, other shapes); bars as for
+the softmax features.  Omega = I gives plain linear attention."""
 
 import pytest
 import torch
@@ -27,6 +27,8 @@ def _run(favor, causal, Q, K, V, om, s, status=None):
 
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("dtype,d,m,L", [(torch.bfloat16, 64, 256, 1000), (torch.bfloat16, 64, 128, 300),
+                                         (torch.bfloat16, 64, 256, 4100), (torch.bfloat16, 128, 512, 700),
+                                         (torch.bfloat16, 128, 128, 129),
                                          (torch.float32, 64, 64, 300), (torch.float32, 32, 100, 129)])
 def test_elu1_matches_oracle(cuda_lib, causal, dtype, d, m, L):
     B, H = 2, 3
@@ -53,14 +55,21 @@ def test_identity_projection_is_linear_attention(cuda_lib, causal):
     assert orc.rowwise_rel_err(to_np(O), ref) < TOL[torch.float32]
 
 
-def test_plain_workspace_is_too_small_on_a_tensor_core_shape(cuda_lib):
-    # the bf16 d64 m256 shape takes the tensor cores with softmax features;
-    # 1 + elu needs the CUDA-core workspace, and the call checks its size
+@pytest.mark.parametrize("causal", [False, True])
+def test_elu1_takes_the_plain_calls_workspace(cuda_lib, causal):
+    # every feature map takes the plain call's path: the same workspace size,
+    # and a call with the plain workspace runs
     B, H, L, d, m = 2, 4, 1000, 64, 256
+    assert cuda_lib.workspace_bytes(causal, B, H, L, d, m, torch.bfloat16, feature_map="elu1") == \
+        cuda_lib.workspace_bytes(causal, B, H, L, d, m, torch.bfloat16)
     Q, K, V = _qkv(B, H, L, d, torch.bfloat16, seed=3)
     om = cuda_lib.new_omega(3, m, d)
-    small = cuda_lib.new_workspace(False, B, H, L, d, m, torch.bfloat16)
-    need = cuda_lib.workspace_bytes(False, B, H, L, d, m, torch.bfloat16, feature_map="elu1")
-    if small.numel() < need:
-        with pytest.raises(cuda_lib.FavorError):
-            cuda_lib.fwd_bidir(Q, K, V, om, d ** -0.25, small, feature_map="elu1")
+    ws = cuda_lib.new_workspace(causal, B, H, L, d, m, torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fn = cuda_lib.fwd_causal if causal else cuda_lib.fwd_bidir
+    O = fn(Q, K, V, om, d ** -0.25, ws, dev_status=st, feature_map="elu1")
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = (orc.favor_causal_quadratic if causal else orc.favor_bidirectional)(
+        to_np(Q), to_np(K), to_np(V), to_np(om), d ** -0.25, "elu1")
+    assert orc.rowwise_rel_err(to_np(O), ref) < TOL[torch.bfloat16]
