@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t id_proj = idesc_f16(kBM, kFB, false, false);
+      constexpr uint32_t id_proj_all = idesc_f16(kBM, M, false, false);
       constexpr uint32_t id_state = idesc_bf16(kFB, D + 16, true, true);
       const uint32_t omega_a = smem_addr(sm + C::kOmega);
       const uint32_t ones_a = smem_addr(sm + C::kOnes);
@@ -263,23 +263,27 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
       // next state step (tile, block) are each issued as soon as their inputs
       // are ready, projections first
       Watchdog wd(wctx);
-      int pi = 0, pf = 0, si = 0, sf = 0;
+      int pi = 0, si = 0, sf = 0;
       while (ok && (pi < n_tiles || si < n_tiles)) {
         bool progress = false;
         if (pi < n_tiles) {
+          // m = 256: one N = 256 projection covers both blocks (half the MMA
+          // instructions of two N = 128 ones); it waits until both blocks'
+          // previous tiles were copied out
           const int ks = pi % C::NK;
-          const bool ready = (pf > 0 || mbar_test_wait(smem_addr(&kn_full[pi % C::NN]), (pi / C::NN) & 1)) &&
-                             (pi == 0 || mbar_test_wait(smem_addr(&p_free[pf]), (pi - 1) & 1));
+          const bool ready = mbar_test_wait(smem_addr(&kn_full[pi % C::NN]), (pi / C::NN) & 1) &&
+                             (pi == 0 || (mbar_test_wait(smem_addr(&p_free[0]), (pi - 1) & 1) &&
+                                          (NFB == 1 || mbar_test_wait(smem_addr(&p_free[1]), (pi - 1) & 1))));
           if (ready) {
             tc_fence_after();
             const uint64_t a0 = sdesc(smem_addr(sm + C::kK + ks * C::kTileBytes), 16, 1024);
-            const uint64_t b0 = sdesc(omega_a + pf * kFB * 128, 16, 1024);
+            const uint64_t b0 = sdesc(omega_a, 16, 1024);
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
-              mma_bf16(tmem + pf * kFB, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
-            mma_commit(&p_full[pf]);
-            if (pf == NFB - 1) mma_commit(&k_empty[ks]);
-            if (++pf == NFB) { pf = 0; ++pi; }
+              mma_bf16(tmem, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj_all, k > 0);
+            for (int f = 0; f < NFB; ++f) mma_commit(&p_full[f]);
+            mma_commit(&k_empty[ks]);
+            ++pi;
             progress = true;
           }
         }
@@ -572,7 +576,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t id_proj = idesc_f16(kBM, kFB, false, false);
+      constexpr uint32_t id_proj_all = idesc_f16(kBM, M, false, false);
       constexpr uint32_t id_out = idesc_bf16(kBM, D + 16, false, false);
       const uint32_t omega_a = smem_addr(sm + C::kOmega);
       const uint32_t state_a = smem_addr(sm + C::kState);
@@ -581,23 +585,25 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
       // next output step (tile, block) are each issued as soon as their
       // inputs are ready, projections first
       Watchdog wd(wctx);
-      int pi = 0, pf = 0, oi = 0, of = 0;
+      int pi = 0, oi = 0, of = 0;
       while (ok && (pi < n_tiles || oi < n_tiles)) {
         bool progress = false;
         if (pi < n_tiles) {
+          // one projection of N = m covers every block (see the state kernel)
           const int st = pi % C::NSQ;
-          const bool ready = (pf > 0 || mbar_test_wait(smem_addr(&qn_full[st]), (pi / C::NSQ) & 1)) &&
-                             (pi == 0 || mbar_test_wait(smem_addr(&p_free[pf]), (pi - 1) & 1));
+          const bool ready = mbar_test_wait(smem_addr(&qn_full[st]), (pi / C::NSQ) & 1) &&
+                             (pi == 0 || (mbar_test_wait(smem_addr(&p_free[0]), (pi - 1) & 1) &&
+                                          (NFB == 1 || mbar_test_wait(smem_addr(&p_free[1]), (pi - 1) & 1))));
           if (ready) {
             tc_fence_after();
             const uint64_t a0 = sdesc(smem_addr(sm + C::kQ + st * C::kTileBytes), 16, 1024);
-            const uint64_t b0 = sdesc(omega_a + pf * kFB * 128, 16, 1024);
+            const uint64_t b0 = sdesc(omega_a, 16, 1024);
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
-              mma_bf16(tmem + pf * kFB, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj, k > 0);
-            mma_commit(&p_full[pf]);
-            if (pf == NFB - 1) mma_commit(&q_empty[st]);
-            if (++pf == NFB) { pf = 0; ++pi; }
+              mma_bf16(tmem, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, M * 128)), id_proj_all, k > 0);
+            for (int f = 0; f < NFB; ++f) mma_commit(&p_full[f]);
+            mma_commit(&q_empty[st]);
+            ++pi;
             progress = true;
           }
         }
