@@ -125,7 +125,8 @@ struct StateParams {
   float scale;
 };
 
-constexpr int kStateThreads = 384;   // warps 0 TMA, 1 MMA, 2-3 norms, 4-11 epilogue
+constexpr int kStateThreads = 416;   // warps 0 TMA, 1 projection MMAs, 2-3 norms, 4-11 epilogue, 12 state MMAs
+constexpr int kStateIssuer = 12;
 
 template <int D>
 struct StateCfg {
@@ -164,8 +165,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
   uint64_t* phi_full = p_free + 2;            // [2]
   uint64_t* phi_free = phi_full + 2;          // [2]
   uint64_t* setup_bar = phi_free + 2;
-  uint64_t* done_bar = setup_bar + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  uint64_t* done_bar = setup_bar + 1;         // [2]: every projection MMA, every state MMA complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* is_last = const_cast<int*>(abort_flag) + 1;
   float* norm_s = reinterpret_cast<float*>(sm + C::kNorm);   // [NN][128]
@@ -195,7 +196,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
       mbar_init(&phi_free[i], 1);
     }
     mbar_init(setup_bar, 1);
-    mbar_init(done_bar, 1);
+    mbar_init(&done_bar[0], 1);
+    mbar_init(&done_bar[1], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (warp >= 4) {
+  if (warp >= 4 && warp < kStateIssuer) {
     fill_ones_block(sm + C::kOnes, kEpiTid0, kEpiThreads);
     fence_proxy_async_smem();
   }
@@ -252,24 +254,25 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
       for (int x = max(0, nk - C::NK); x < nk; ++x) mbar_wait(&k_full[x % C::NK], (x / C::NK) & 1, wctx);
       for (int x = max(0, nv - C::NV); x < nv; ++x) mbar_wait(&v_full[x % C::NV], (x / C::NV) & 1, wctx);
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == kStateIssuer) {
+    // two issuers: warp 1 the projections, warp 12 the state MMAs, so that
+    // a tile's projection is never queued behind the previous tile's state
+    // MMAs on one thread (issuing costs ~60 cycles per MMA)
     if (lane == 0) {
       constexpr uint32_t id_proj_all = idesc_f16(kBM, M, false, false);
       constexpr uint32_t id_state = idesc_bf16(kFB, D + 16, true, true);
       const uint32_t omega_a = smem_addr(sm + C::kOmega);
       const uint32_t ones_a = smem_addr(sm + C::kOnes);
+      const bool proj = warp == 1;
       bool ok = mbar_wait(setup_bar, 0, wctx);
-      // event-driven issue: the next projection step (tile, block) and the
-      // next state step (tile, block) are each issued as soon as their inputs
-      // are ready, projections first
       Watchdog wd(wctx);
       int pi = 0, si = 0, sf = 0;
-      while (ok && (pi < n_tiles || si < n_tiles)) {
+      while (ok && (proj ? pi < n_tiles : si < n_tiles)) {
         bool progress = false;
-        if (pi < n_tiles) {
-          // m = 256: one N = 256 projection covers both blocks (half the MMA
-          // instructions of two N = 128 ones); it waits until both blocks'
-          // previous tiles were copied out
+        if (proj) {
+          // one N = m projection covers every block (half the MMA
+          // instructions of one per block); it waits until every block's
+          // previous tile was copied out
           const int ks = pi % C::NK;
           const bool ready = mbar_test_wait(smem_addr(&kn_full[pi % C::NN]), (pi / C::NN) & 1) &&
                              (pi == 0 || (mbar_test_wait(smem_addr(&p_free[0]), (pi - 1) & 1) &&
@@ -286,8 +289,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
             ++pi;
             progress = true;
           }
-        }
-        if (si < n_tiles) {
+        } else {
           const int vs = si % C::NV;
           const bool ready = mbar_test_wait(smem_addr(&phi_full[sf]), si & 1) &&
                              (sf > 0 || mbar_test_wait(smem_addr(&v_full[vs]), (si / C::NV) & 1));
@@ -308,8 +310,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
         if (progress) wd.progress();
         else ok = wd.idle();
       }
-      mma_commit(done_bar);
-      mbar_wait(done_bar, 0, wctx);
+      mma_commit(&done_bar[proj ? 0 : 1]);
+      mbar_wait(&done_bar[proj ? 0 : 1], 0, wctx);
     }
   } else if (warp < 2 + kNormWarps) {
     // squared norms of the K rows; K rewritten as fp16
@@ -326,7 +328,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
       __syncwarp();
       if (lane == 0) mbar_arrive(&kn_full[ns]);
     }
-  } else {
+  } else if (warp < kStateIssuer) {
     // ---------------- epilogue: two warpgroups x 128 lanes ----------------
     const int wg = (warp - 4) >> 2;
     const int q = warp & 3;
@@ -374,7 +376,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     }
     // final state: lane f holds feature f of a block.  Two blocks: warpgroup
     // w reads block w; one block: the warpgroups split the d columns.
-    const bool done = mbar_wait(done_bar, 0, wctx);
+    const bool done = mbar_wait(&done_bar[1], 0, wctx);
     tc_fence_after();
     if (done && !*abort_flag) {
       const int sfb = (NFB == 2) ? wg : 0;
