@@ -25,12 +25,14 @@
 // significant bits (bf16 Omega alone costs ~2.5% in the output).
 //
 // Warp roles: warp 0 issues TMA loads, warp 1 owns tensor memory and issues
-// MMAs (one elected thread), warps 2-3 compute the squared row norms of the K
-// (and Q) tiles and convert them to fp16, and eight epilogue warps form two
+// MMAs (one thread), warps 2-3 compute the squared row norms of the K (and Q)
+// tiles and convert them to fp16, and eight epilogue warps form two
 // warpgroups that split the columns of each 128-row tile (thread = one TMEM
-// lane = one token or one feature).  Epilogues copy a tile out of tensor
-// memory and release it before they compute on it, so that the next MMA into
-// the same columns overlaps their arithmetic.
+// lane = one token or one feature).  The state kernel has a thirteenth warp
+// that issues its state MMAs, so that a tile's projection never waits behind
+// them on one thread (issuing costs ~60 cycles per MMA).  Epilogues copy a
+// tile out of tensor memory and release it before they compute on it, so
+// that the next MMA into the same columns overlaps their arithmetic.
 #include <cudaTypedefs.h>
 
 #include <mutex>
