@@ -110,6 +110,12 @@ TcPlan tc_plan(bool causal, const Shape& s) {
 }
 
 
+// Causal initial states: the last superchunk sums this many partials at most
+// (its predecessors' sub-splits); up to kDirectPartials the scan kernel adds
+// them itself, above that the prefix kernel forms every superchunk's sum once.
+constexpr int kDirectPartials = 4;
+inline bool causal_direct(const TcPlan& p) { return (p.out_ctas - 1) * p.sub_per_sc <= kDirectPartials; }
+
 // ---------------------------------------------------------------------------
 // state kernel: one (token split, head) per CTA, all m features.
 // Bidirectional: the last CTA of a head adds the splits (fixed order) into
@@ -782,9 +788,10 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
 struct CausalParams {
   const float* key_ref;   // row-norm maxima (key_reference)
   const uint8_t* omega_img;
-  const float* pre;       // [BH][n_fb][n_sc][d+1][128] initial states (superchunks > 0)
+  const float* pre;       // [BH][n_fb][n_sc][d+1][128] initial states (superchunks > 0), or null:
+  const float* partS;     // then [BH][n_fb][n_split][d+1][128] partials summed here
   int32_t* status;
-  int L, m, n_sc, tiles_per_sc;
+  int L, m, n_sc, tiles_per_sc, n_split, sub_per_sc;
   float scale;
 };
 
@@ -1061,20 +1068,50 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
     constexpr int kGGroups = D / 8 + 1;
     const int g_first = wg ? (kGGroups + 1) / 2 : 0;
     const int g_end = wg ? kGGroups : (kGGroups + 1) / 2;
-    // G_init: the superchunk's initial state (the fixed-order sum of the
-    // earlier superchunks' partial states, formed by the prefix kernel); all
-    // of this thread's loads in flight together
+    // G_init: the superchunk's initial state, the fixed-order sum of the
+    // earlier superchunks' partial states: formed by the prefix kernel when
+    // the later superchunks have many, summed here in the same order (so to
+    // the same bits) when every superchunk has at most a few; all of this
+    // thread's loads of a partial in flight together
     for (int fb = 0; fb < NFB; ++fb) {
-      const float* src = prm.pre + (((size_t)bh * NFB + fb) * prm.n_sc + sc) * (D + 1) * kFB;
       constexpr int kMaxG = (kG0 > GN - kG0 ? kG0 : GN - kG0) / 16;
       float acc[kMaxG][16];
+      if (prm.pre != nullptr) {
+        const float* src = prm.pre + (((size_t)bh * NFB + fb) * prm.n_sc + sc) * (D + 1) * kFB;
 #pragma unroll
-      for (int g = 0; g < kMaxG; ++g)
+        for (int g = 0; g < kMaxG; ++g)
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int n = n0 + 16 * g + j;
-          acc[g][j] = (sc > 0 && g < ng16 && n <= D) ? src[(size_t)n * kFB + t] : 0.f;
+          for (int j = 0; j < 16; ++j) {
+            const int n = n0 + 16 * g + j;
+            acc[g][j] = (sc > 0 && g < ng16 && n <= D) ? src[(size_t)n * kFB + t] : 0.f;
+          }
+      } else {
+#pragma unroll
+        for (int g = 0; g < kMaxG; ++g)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[g][j] = 0.f;
+        const float* src = prm.partS + ((size_t)bh * NFB + fb) * max(prm.n_split, 1) * (D + 1) * kFB;
+        const int np = sc * prm.sub_per_sc;
+        for (int p = 0; p < np; p += 2) {   // two partials' loads in flight, added in order
+          float v[2][kMaxG][16];
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int g = 0; g < kMaxG; ++g)
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int n = n0 + 16 * g + j;
+                v[u][g][j] = (p + u < np && g < ng16 && n <= D) ? src[((size_t)(p + u) * (D + 1) + n) * kFB + t] : 0.f;
+              }
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int g = 0; g < kMaxG; ++g)
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (p + u < np) acc[g][j] += v[u][g][j];
         }
+      }
 #pragma unroll
       for (int g = 0; g < kMaxG; ++g) {
         if (g >= ng16) break;
@@ -1349,12 +1386,15 @@ cudaError_t launch_causal(const void* Q, const void* K, const void* V, void* O, 
   CausalParams prm{};
   prm.key_ref = reinterpret_cast<const float*>(ws);
   prm.omega_img = reinterpret_cast<const uint8_t*>(ws + p.off_omega_img);
-  prm.pre = reinterpret_cast<const float*>(ws + p.off_pre);
+  prm.pre = causal_direct(p) ? nullptr : reinterpret_cast<const float*>(ws + p.off_pre);
+  prm.partS = reinterpret_cast<const float*>(ws + p.off_partS);
   prm.status = status;
   prm.L = s.L;
   prm.m = s.m;
   prm.n_sc = p.out_ctas;
   prm.tiles_per_sc = p.out_tiles_per_cta;
+  prm.n_split = p.n_split;
+  prm.sub_per_sc = p.sub_per_sc;
   prm.scale = scale;
   const size_t smem = CausalCfg<D>::kSmem;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(causal_kernel<D, M, FM>), smem);
@@ -1389,7 +1429,7 @@ cudaError_t tc_state_fm(bool causal, const void* K, const void* V, const float* 
   if (e != cudaSuccess) return e;
   e = s.m == 256 ? launch_state<64, 256, FM>(K, V, s, p, scale, w, status, stream)
                  : launch_state<64, 128, FM>(K, V, s, p, scale, w, status, stream);
-  if (e != cudaSuccess || !causal || p.n_split < 1) return e;
+  if (e != cudaSuccess || !causal || p.n_split < 1 || causal_direct(p)) return e;
   state_prefix_kernel<64><<<dim3(p.n_fb * 65, s.BH()), kFB, 0, stream>>>(
       reinterpret_cast<const float*>(w + p.off_partS), reinterpret_cast<float*>(w + p.off_pre), p.n_fb, p.n_split,
       p.sub_per_sc, p.out_ctas);
