@@ -27,6 +27,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const float* __restr
                                                             uint8_t* __restrict__ image,
                                                             uint32_t* __restrict__ counters, int n_counters) {
   __shared__ float red[32];
+  // the state kernel that follows may start now (it waits before reading the
+  // header and the image)
+  asm volatile("griddepcontrol.launch_dependents;");
   for (int i = blockIdx.x * kPrepThreads + threadIdx.x; i < n_counters; i += gridDim.x * kPrepThreads) counters[i] = 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x * kPrepRows + warp;

@@ -226,13 +226,25 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     if (lane == 0) {
       prefetch_tmap(&mapK);
       prefetch_tmap(&mapV);
+      // the fp16 image of Omega comes from the preparation kernel, which may
+      // still run (programmatic launch): the first K and V tiles load first
+      if (n_tiles > 0) {
+        mbar_arrive_expect_tx(&k_full[0], C::kTileBytes);
+        mbar_arrive_expect_tx(&v_full[0], C::kTileBytes);
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a) {
+          tma_load_3d(sm + C::kK + a * kAtom, &mapK, a * 64, tile0 * kBM, bh, &k_full[0]);
+          tma_load_3d(sm + C::kV + a * kAtom, &mapV, a * 64, tile0 * kBM, bh, &v_full[0]);
+        }
+      }
+      griddep_wait();
       mbar_arrive_expect_tx(setup_bar, M * D * 2);
       bulk_load(sm + C::kOmega, prm.omega_img, M * D * 2, setup_bar);
       // K tile x goes to K slot x % NK once the projections of tile x - NK
       // have read it, V tile x to V slot x % NV once the state MMA of tile
       // x - NV has; K is issued ahead of V
       Watchdog wd(wctx);
-      int nk = 0, nv = 0;
+      int nk = n_tiles > 0 ? 1 : 0, nv = nk;
       bool ok = true;
       while (ok && (nk < n_tiles || nv < n_tiles)) {
         bool progress = false;
@@ -344,6 +356,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const int col0 = wg * 64;                      // this warpgroup's columns of each feature block
     float R, W_unused;
+    griddep_wait();   // the key reference comes from the preparation kernel
     key_reference(prm.key_ref, prm.m, &R, &W_unused);
     const float c1 = feature_c1<FM>(prm.scale);
     const float hs2 = 0.5f * prm.scale * prm.scale;
@@ -1350,9 +1363,19 @@ cudaError_t launch_state(const void* K, const void* V, const Shape& s, const TcP
   const size_t smem = StateCfg<D>::kSmem;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(state_kernel<D, M, FM>), smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_split, s.BH());
-  state_kernel<D, M, FM><<<grid, kStateThreads, smem, stream>>>(mk, mv, prm);
-  return cudaGetLastError();
+  // programmatic launch: the kernel's set-up and first tile loads overlap the
+  // preparation kernel before it in the stream
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(p.n_split, s.BH());
+  cfg.blockDim = dim3(kStateThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, state_kernel<D, M, FM>, mk, mv, prm);
 }
 
 template <int D, int M, int FM>

@@ -108,6 +108,12 @@ struct Watchdog {
   }
 };
 
+// ---- programmatic dependent launch ------------------------------------------
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel in the stream still runs; before it reads what that
+// kernel wrote, it waits here (a no-op when it was launched normally).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- thread-block clusters (distributed shared memory) ---------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

@@ -221,6 +221,25 @@ def test_causal_multichunk_walk(cuda_lib, m):
     assert orc.rowwise_rel_err(got, ref) < TOL[torch.bfloat16]
 
 
+@pytest.mark.parametrize("L", [640, 768, 4096])
+@pytest.mark.parametrize("m", [128, 256])
+def test_causal_initial_states_summed_either_way(cuda_lib, L, m):
+    # one head split into superchunks of one chunk each on a 152-SM GPU: at
+    # L = 640 the last of 5 superchunks starts from the sum of 4 earlier
+    # partials (the scan kernel adds them), at 768 from 5 (the prefix kernel
+    # does) and at 4096 from 31; whole output against the oracle
+    w = wl.Workload("init", "causal", "bf16", 1, 1, L, 64, m, "normal")
+    Q, K, V = (t.cuda() for t in wl.make_qkv(w, seed=L + m))
+    om = cuda_lib.new_omega(L, m, w.d)
+    st = _status()
+    O = _run(cuda_lib, True, Q, K, V, om, w.qk_scale, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    fn = orc.favor_causal if L <= 800 else orc.favor_causal_quadratic
+    ref = fn(to_np(Q), to_np(K), to_np(V), to_np(om), w.qk_scale)
+    assert orc.rowwise_rel_err(to_np(O), ref) < TOL[torch.bfloat16]
+
+
 def test_redrawn_omega_per_call(cuda_lib):
     # the 12288-token pixel workload draws a fresh Omega (seed base + i) each call
     w = wl.get("causal-bf16-B2H8L12288-d64-m256").with_(B=1, H=2, L=1024)
