@@ -169,14 +169,11 @@ def test_feature_map_calls_reject_bad_arguments(lib, name):
 
 def test_feature_map_workspace_sizes(lib):
     for causal in (0, 1):
-        # softmax and ReLU features take the plain call's workspace
-        for fm in (0, 1):
-            assert lib.favor_workspace_bytes_fm(causal, 2, 4, 1000, 64, 256, 1, fm) == \
-                lib.favor_workspace_bytes(causal, 2, 4, 1000, 64, 256, 1)
-        # 1 + elu runs on the CUDA-core kernels: at least the CUDA-core plan of
-        # the same shape, which fp32 calls of that shape also use
-        assert lib.favor_workspace_bytes_fm(causal, 2, 4, 1000, 64, 256, 1, 2) >= \
-            lib.favor_workspace_bytes(causal, 2, 4, 1000, 64, 256, 0) > 0
+        # every feature map takes the plain call's path, hence its workspace
+        for fm in (0, 1, 2):
+            for dt in (0, 1):
+                assert lib.favor_workspace_bytes_fm(causal, 2, 4, 1000, 64, 256, dt, fm) == \
+                    lib.favor_workspace_bytes(causal, 2, 4, 1000, 64, 256, dt) > 0
         assert lib.favor_workspace_bytes_fm(causal, 2, 4, 1000, 64, 256, 1, 3) == 0
         assert lib.favor_workspace_bytes_fm(causal, 2, 4, 0, 64, 256, 1, 2) == 0
 
