@@ -1,4 +1,5 @@
 // C ABI entry points: argument checks, workspace planning and dispatch.
+#include <algorithm>
 #include <cmath>
 
 #include "backward.cuh"
@@ -160,9 +161,15 @@ favor_status bwd_run(bool causal, const void* Q, const void* K, const void* V, c
   if (dQ == dK || dQ == dV || dK == dV) return FAVOR_ERR_INVALID_ARG;
   if (workspace == nullptr || !aligned(workspace, 256)) return FAVOR_ERR_INVALID_ARG;
   const Shape s{B, H, L, d, m};
-  if (ws_bytes < favor::bwd_plan(s).bytes) return FAVOR_ERR_INVALID_ARG;
   const bool bf16 = dt == FAVOR_BF16;
   cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+  if (favor::tc_bwd_supported(causal, d, m, bf16)) {
+    if (ws_bytes < favor::tc_bwd_workspace_bytes(s)) return FAVOR_ERR_INVALID_ARG;
+    const cudaError_t e = favor::tc_bwd_bidir(Q, K, V, dO, dQ, dK, dV, omega, qk_scale, s, workspace, dev_status,
+                                              st_, static_cast<int>(fm));
+    return e == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
+  }
+  if (ws_bytes < favor::bwd_plan(s).bytes) return FAVOR_ERR_INVALID_ARG;
   cudaError_t e = causal ? favor::simt_bwd_causal(Q, K, V, dO, dQ, dK, dV, omega, qk_scale, s, bf16, workspace,
                                                   dev_status, st_, static_cast<int>(fm))
                          : favor::simt_bwd_bidir(Q, K, V, dO, dQ, dK, dV, omega, qk_scale, s, bf16, workspace,
@@ -238,7 +245,12 @@ favor_status favor_fwd_causal_fm(const void* Q, const void* K, const void* V, vo
 
 size_t favor_bwd_workspace_bytes(int B, int H, int L, int d, int m, favor_dtype dt) {
   if (shape_ok(B, H, L, d, m, dt) != FAVOR_OK) return 0;
-  return favor::bwd_plan(Shape{B, H, L, d, m}).bytes;
+  const Shape s{B, H, L, d, m};
+  // one size serves both passes: the bidirectional pass may take the
+  // tensor-core kernels, the causal pass the CUDA-core ones
+  size_t bytes = favor::bwd_plan(s).bytes;
+  if (favor::tc_bwd_supported(false, d, m, dt == FAVOR_BF16)) bytes = std::max(bytes, favor::tc_bwd_workspace_bytes(s));
+  return bytes;
 }
 
 

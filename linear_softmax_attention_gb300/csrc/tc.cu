@@ -128,6 +128,7 @@ struct StateParams {
   float* partS;            // [BH][n_fb][n_split][d+1][128]
   uint32_t* counters;      // [BH]
   uint8_t* state_img;      // [BH][m/64][d+16][128 B]
+  float* zvec;             // bidirectional, optional: [BH][m] fp32 normaliser row of the merged state
   int32_t* status;
   int L, m, n_split, tiles_per_split, merge;
   float scale;
@@ -434,48 +435,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
   // the last CTA of a head adds the splits' partial states (fixed split order)
-  // into the bf16 state image: every thread, eight items' loads in flight per
-  // split.  Item = (block b, state row n, 4 consecutive features).
+  // into the bf16 state image read by the output kernel
   if (prm.merge && *is_last) {
     __threadfence();
-    uint8_t* img = prm.state_img + (size_t)bh * M * (D + 16) * 2;
-    constexpr int NG = kFB / 4;
-    constexpr int kItems = NFB * (D + 16) * NG;
-    constexpr int kBatch = 8;
-    const float* base = prm.partS + (size_t)bh * NFB * prm.n_split * (D + 1) * kFB;
-    for (int e0 = threadIdx.x; e0 < kItems; e0 += kBatch * kStateThreads) {
-      float4 acc[kBatch];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int p = 0; p < prm.n_split; ++p) {
-        float4 v[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int e = e0 + u * kStateThreads;
-          const int g = e % NG, n = (e / NG) % (D + 16), b = e / (NG * (D + 16));
-          v[u] = (e < kItems && n <= D)
-                     ? *reinterpret_cast<const float4*>(base + (((size_t)b * prm.n_split + p) * (D + 1) + n) * kFB + g * 4)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          acc[u].x += v[u].x;
-          acc[u].y += v[u].y;
-          acc[u].z += v[u].z;
-          acc[u].w += v[u].w;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int e = e0 + u * kStateThreads;
-        if (e >= kItems) break;
-        const int g = e % NG, n = (e / NG) % (D + 16), b = e / (NG * (D + 16));
-        const int f = b * kFB + g * 4;
-        const int atom = f >> 6, cc = f & 63;
-        const size_t off = ((size_t)atom * (D + 16) + n) * 128 + (((cc >> 3) ^ (n & 7)) << 4) + (cc & 7) * 2;
-        *reinterpret_cast<uint2*>(img + off) = make_uint2(pack_bf16(acc[u].x, acc[u].y), pack_bf16(acc[u].z, acc[u].w));
-      }
-    }
+    merge_partials<D, M>(prm.partS + (size_t)bh * NFB * prm.n_split * (D + 1) * kFB, prm.n_split,
+                         prm.state_img + (size_t)bh * M * (D + 16) * 2, kStateThreads,
+                         prm.zvec != nullptr ? prm.zvec + (size_t)bh * M : nullptr);
     if (threadIdx.x == 0) prm.counters[bh] = 0;
   }
 }
@@ -1343,7 +1308,7 @@ __global__ void __launch_bounds__(kCausalThreads, 1) causal_kernel(const __grid_
 // ---------------------------------------------------------------------------
 template <int D, int M, int FM>
 cudaError_t launch_state(const void* K, const void* V, const Shape& s, const TcPlan& p, float scale, char* ws,
-                         int32_t* status, cudaStream_t stream) {
+                         int32_t* status, cudaStream_t stream, float* zvec) {
   if (p.n_split < 1) return cudaSuccess;
   CUtensorMap mk, mv;
   if (!make_map(&mk, K, s) || !make_map(&mv, V, s)) return cudaErrorInvalidValue;
@@ -1353,6 +1318,7 @@ cudaError_t launch_state(const void* K, const void* V, const Shape& s, const TcP
   prm.partS = reinterpret_cast<float*>(ws + p.off_partS);
   prm.counters = reinterpret_cast<uint32_t*>(ws + p.off_counters);
   prm.state_img = reinterpret_cast<uint8_t*>(ws + p.off_state_img);
+  prm.zvec = zvec;
   prm.status = status;
   prm.L = s.L;
   prm.m = s.m;
@@ -1435,13 +1401,28 @@ bool tc_supported(bool causal, int d, int m, bool bf16) {
   return fs_supported(causal, d, m, bf16);
 }
 
+TcLayout tc_bidir_layout(const Shape& s) {
+  const TcPlan p = tc_plan(false, s);
+  TcLayout l{};
+  l.n_split = p.n_split;
+  l.tiles_per_split = p.tiles_per_split;
+  l.out_ctas = p.out_ctas;
+  l.out_tiles_per_cta = p.out_tiles_per_cta;
+  l.off_omega_img = p.off_omega_img;
+  l.off_counters = p.off_counters;
+  l.off_partS = p.off_partS;
+  l.off_state_img = p.off_state_img;
+  l.bytes = p.bytes;
+  return l;
+}
+
 size_t tc_workspace_bytes(bool causal, const Shape& s) {
   return s.d == 64 ? tc_plan(causal, s).bytes : fs_workspace_bytes(causal, s);
 }
 
 template <int FM>
 cudaError_t tc_state_fm(bool causal, const void* K, const void* V, const float* omega, float scale, const Shape& s,
-                        void* ws, int32_t* status, cudaStream_t stream) {
+                        void* ws, int32_t* status, cudaStream_t stream, float* zvec) {
   const TcPlan p = tc_plan(causal, s);
   char* w = static_cast<char*>(ws);
   // prep also zeroes the bidirectional merge counters
@@ -1450,8 +1431,8 @@ cudaError_t tc_state_fm(bool causal, const void* K, const void* V, const float* 
                               causal ? nullptr : reinterpret_cast<uint32_t*>(w + p.off_counters), causal ? 0 : s.BH(),
                               stream);
   if (e != cudaSuccess) return e;
-  e = s.m == 256 ? launch_state<64, 256, FM>(K, V, s, p, scale, w, status, stream)
-                 : launch_state<64, 128, FM>(K, V, s, p, scale, w, status, stream);
+  e = s.m == 256 ? launch_state<64, 256, FM>(K, V, s, p, scale, w, status, stream, zvec)
+                 : launch_state<64, 128, FM>(K, V, s, p, scale, w, status, stream, zvec);
   if (e != cudaSuccess || !causal || p.n_split < 1 || causal_direct(p)) return e;
   state_prefix_kernel<64><<<dim3(p.n_fb * 65, s.BH()), kFB, 0, stream>>>(
       reinterpret_cast<const float*>(w + p.off_partS), reinterpret_cast<float*>(w + p.off_pre), p.n_fb, p.n_split,
@@ -1472,11 +1453,11 @@ cudaError_t tc_output_fm(bool causal, const void* Q, const void* K, const void* 
 }
 
 cudaError_t tc_state(bool causal, const void* K, const void* V, const float* omega, float scale, const Shape& s,
-                     void* ws, int32_t* status, cudaStream_t stream, int fm) {
+                     void* ws, int32_t* status, cudaStream_t stream, int fm, float* zvec) {
   if (s.d != 64) return fs_state(causal, K, V, omega, scale, s, ws, status, stream, fm);
-  if (fm == FAVOR_FM_RELU) return tc_state_fm<FAVOR_FM_RELU>(causal, K, V, omega, scale, s, ws, status, stream);
-  if (fm == FAVOR_FM_ELU1) return tc_state_fm<FAVOR_FM_ELU1>(causal, K, V, omega, scale, s, ws, status, stream);
-  return tc_state_fm<FAVOR_FM_PRF>(causal, K, V, omega, scale, s, ws, status, stream);
+  if (fm == FAVOR_FM_RELU) return tc_state_fm<FAVOR_FM_RELU>(causal, K, V, omega, scale, s, ws, status, stream, zvec);
+  if (fm == FAVOR_FM_ELU1) return tc_state_fm<FAVOR_FM_ELU1>(causal, K, V, omega, scale, s, ws, status, stream, zvec);
+  return tc_state_fm<FAVOR_FM_PRF>(causal, K, V, omega, scale, s, ws, status, stream, zvec);
 }
 
 cudaError_t tc_output(bool causal, const void* Q, const void* K, const void* V, void* O, const float* omega,

@@ -119,15 +119,6 @@ FsCausalPlan fsc_plan(const Shape& s) {
   return p;
 }
 
-// [128 rows][128 B] block whose row r reads, unswizzled, (1, 0, ..., 0): the
-// columns d .. d + 63 of [V | 1] at every 16-row k-step of a V tile
-__device__ __forceinline__ void fill_ones_atom(uint8_t* p, int tid0, int nthreads) {
-  for (int e = threadIdx.x - tid0; e < kAtom / 16; e += nthreads) {
-    const int row = e >> 3, logical = (e & 7) ^ (row & 7);
-    *reinterpret_cast<uint4*>(p + e * 16) = make_uint4(logical == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
-  }
-}
-
 // ---------------------------------------------------------------------------
 // state kernel
 // ---------------------------------------------------------------------------

@@ -185,6 +185,15 @@ __device__ __forceinline__ void fill_ones_block(uint8_t* p, int tid0, int nthrea
   }
 }
 
+// [128 rows][128 B] block whose row r reads, unswizzled, (1, 0, ..., 0): as
+// the atom after a 64-column K-major tile, columns 64 .. 127 of [X | 1]
+__device__ __forceinline__ void fill_ones_atom(uint8_t* p, int tid0, int nthreads) {
+  for (int e = threadIdx.x - tid0; e < kAtom / 16; e += nthreads) {
+    const int row = e >> 3, logical = (e & 7) ^ (row & 7);
+    *reinterpret_cast<uint4*>(p + e * 16) = make_uint4(logical == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
+  }
+}
+
 // Descriptor arithmetic.  A descriptor's start-address field holds bytes >> 4
 // in its low bits, so a k-step is an add to the base descriptor built once
 // per MMA group (rebuilding it per MMA costs the issuing thread ~40 issue
@@ -232,6 +241,57 @@ __device__ __forceinline__ void tmem_state_to_rows(uint32_t tmem, uint32_t g_col
                         pack_bf16(__uint_as_float(lo[u][2]), __uint_as_float(lo[u][3])),
                         pack_bf16(__uint_as_float(hi[u][0]), __uint_as_float(hi[u][1])),
                         pack_bf16(__uint_as_float(hi[u][2]), __uint_as_float(hi[u][3])));
+    }
+  }
+}
+
+// The fixed-order sum of one head's n_split fp32 partial states
+// ([M/128 blocks][n_split][D + 1][128], feature fastest) as its bf16 state
+// image ([M/64 atoms][D + 16 rows][128 B], 128-byte swizzle, the normaliser
+// in row D, rows past it zero), by all `nthreads` threads of the CTA with
+// eight items' loads in flight per split.  Item = (block b, state row n, 4
+// consecutive features).
+// With `zvec` non-null, the normaliser row (n = D) also goes to zvec[0, M)
+// in fp32.
+template <int D, int M>
+__device__ void merge_partials(const float* __restrict__ base, int n_split, uint8_t* __restrict__ img,
+                               int nthreads, float* __restrict__ zvec = nullptr) {
+  constexpr int NFB = M / kFB;
+  constexpr int NG = kFB / 4;
+  constexpr int kItems = NFB * (D + 16) * NG;
+  constexpr int kBatch = 8;
+  for (int e0 = threadIdx.x; e0 < kItems; e0 += kBatch * nthreads) {
+    float4 acc[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p = 0; p < n_split; ++p) {
+      float4 v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = e0 + u * nthreads;
+        const int g = e % NG, n = (e / NG) % (D + 16), b = e / (NG * (D + 16));
+        v[u] = (e < kItems && n <= D)
+                   ? *reinterpret_cast<const float4*>(base + (((size_t)b * n_split + p) * (D + 1) + n) * kFB + g * 4)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        acc[u].x += v[u].x;
+        acc[u].y += v[u].y;
+        acc[u].z += v[u].z;
+        acc[u].w += v[u].w;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int e = e0 + u * nthreads;
+      if (e >= kItems) break;
+      const int g = e % NG, n = (e / NG) % (D + 16), b = e / (NG * (D + 16));
+      const int f = b * kFB + g * 4;
+      const int atom = f >> 6, cc = f & 63;
+      const size_t off = ((size_t)atom * (D + 16) + n) * 128 + (((cc >> 3) ^ (n & 7)) << 4) + (cc & 7) * 2;
+      *reinterpret_cast<uint2*>(img + off) = make_uint2(pack_bf16(acc[u].x, acc[u].y), pack_bf16(acc[u].z, acc[u].w));
+      if (zvec != nullptr && n == D) *reinterpret_cast<float4*>(zvec + f) = acc[u];
     }
   }
 }
