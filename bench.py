@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--call-mode", default=None, choices=["bidir", "causal"],
                     help="with --call: run this pass instead of the workload's own")
+    ap.add_argument("--call-backward", action="store_true",
+                    help="with --call: run the pass's backward (dQ, dK, dV for a seeded dO) instead")
     return ap.parse_args()
 
 
@@ -805,9 +807,10 @@ def time_build(favor, kind, m, d, stream, dev, reps=20):
 
 
 def measure_backward(favor, n_steps, sets, omega, s, stream, status, dev, tokens_per_step, hbm):
-    """favor_bwd_bidir and favor_bwd_causal on the step's workload (CUDA-core
-    kernels): dQ, dK, dV for a seeded dO, inputs rotating over the sets, one
-    CUDA graph per set.
+    """favor_bwd_bidir and favor_bwd_causal on the step's workload (the
+    bidirectional pass on the tensor-core kernels, the causal pass on the
+    CUDA-core ones): dQ, dK, dV for a seeded dO, inputs rotating over the
+    sets, one CUDA graph per set.
     Algorithmic bytes: read Q, K, V, dO and write dQ, dK, dV (7 d e per
     head-token)."""
     q0 = sets[0][0]
@@ -846,7 +849,7 @@ def measure_backward(favor, n_steps, sets, omega, s, stream, status, dev, tokens
         out["causal" if causal else "bidir"] = {
             "value": tokens_per_step / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": n_steps,
             "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm}
-    out["step"] = "backward (dQ, dK, dV) of each pass, CUDA-core kernels"
+    out["step"] = "backward (dQ, dK, dV) of each pass: bidirectional on tcgen05, causal on CUDA cores"
     return out
 
 
@@ -934,8 +937,9 @@ def measure_decode(favor, n_steps, stream, status, hbm, dev):
 
 
 def run_call_only(args):
-    """One workload's public full call (favor_fwd_bidir or favor_fwd_causal),
-    --calls times on the current stream, Omega built once."""
+    """One workload's public full call (favor_fwd_bidir or favor_fwd_causal,
+    or with --call-backward favor_bwd_*), --calls times on the current
+    stream, Omega built once."""
     import linear_softmax_attention_gb300 as favor
 
     favor.load()
@@ -948,16 +952,28 @@ def run_call_only(args):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     fn = favor.fwd_causal if causal else favor.fwd_bidir
     O = torch.empty_like(q)
+    if args.call_backward:
+        gen = torch.Generator(device="cpu")
+        gen.manual_seed(5)
+        dO = torch.randn(q.shape, generator=gen).to(q.dtype).to(dev)
+        ws = torch.empty(favor.bwd_workspace_bytes(w.B, w.H, w.L, w.d, w.m, w.torch_dtype), dtype=torch.uint8,
+                         device=dev)
+        grads = (torch.empty_like(q), torch.empty_like(q), torch.empty_like(q))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
     e0.record()
     for _ in range(args.calls):
-        fn(q, k, v, om, w.qk_scale, ws, O=O, dev_status=status)
+        if args.call_backward:
+            favor.bwd_bidir(q, k, v, dO, om, w.qk_scale, ws, dQ=grads[0], dK=grads[1], dV=grads[2],
+                            dev_status=status, causal=causal)
+        else:
+            fn(q, k, v, om, w.qk_scale, ws, O=O, dev_status=status)
     e1.record()
     torch.cuda.synchronize(dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} on {w.name}")
-    print(json.dumps({"call": w.name, "mode": "causal" if causal else "bidir", "calls": args.calls,
+    print(json.dumps({"call": w.name, "mode": "causal" if causal else "bidir", "backward": args.call_backward,
+                      "calls": args.calls,
                       "ms_per_call": e0.elapsed_time(e1) / args.calls,
                       "path": favor.path_name(causal, w.d, w.m, w.torch_dtype)}))
 

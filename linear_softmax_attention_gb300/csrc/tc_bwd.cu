@@ -41,9 +41,9 @@
 //     the last CTA of a head adds the splits' partials into the dS pair and dz
 //   key kernel    CTA = a run of tiles of one head
 //     P = K Omega^T,  dV = phi(K) dS_hi,  T = V (dS_hi + dS_lo)^T,  dK = s G Omega
-// G = g scaled per row by a power of two that puts its largest entry in
-// [2^14, 2^15), in fp16 (the operand type of the fp16 Omega image); the
-// scale comes off exactly in the epilogue.
+// G = g rounded to bf16, then scaled per row by a power of two that puts
+// its largest entry in [2^14, 2^15), in fp16 (the operand type of the fp16
+// Omega image); the scale comes off exactly in the epilogue.
 //
 // Warp roles as in the forward kernels: warp 0 TMA, warp 1 MMA issue (one
 // thread), warps 2-3 rewrite each Q or K tile as fp16 (and take the squared
@@ -100,10 +100,15 @@ __device__ __forceinline__ void row_scale(float gmax, float* beta, float* inv_be
   *inv_beta = __uint_as_float(static_cast<uint32_t>(254 - be) << 23);
 }
 
-// In place: x[j] = fp16x2(g_2j beta, g_2j+1 beta) for j < 16 (g as fp32 bits)
-__device__ __forceinline__ void pack_g(uint32_t (&x)[32], float beta) {
+// In place: x[j] = bf16x2(g_2j, g_2j+1) for j < 16 (g as fp32 bits)
+__device__ __forceinline__ void pack_g_bf16(uint32_t (&x)[32]) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j) x[j] = pack_f16_sat(__uint_as_float(x[2 * j]) * beta, __uint_as_float(x[2 * j + 1]) * beta);
+  for (int j = 0; j < 16; ++j) x[j] = pack_bf16(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+}
+// In place: bf16 pairs -> fp16 pairs times beta (16 words)
+__device__ __forceinline__ void rescale_f16(uint32_t (&w)[16], float beta) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) w[j] = pack_f16_sat(__uint_as_float(w[j] << 16) * beta, __uint_as_float(w[j] & 0xFFFF0000u) * beta);
 }
 
 // Four 16-byte chunks (32 bf16 values) of row t of a swizzle atom, from
@@ -550,24 +555,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_query_kernel(const __grid
 
       // ---- delta = dO . N / D; the -delta columns; phi(Q) -> Psi = phi(Q) / D
       if (ok) ok = mbar_wait(n_full, i & 1, wctx);
-      tc_fence_after();
-      uint32_t nv[32];
-      if (ok) {
-        tmem_ld32(tmem + lane_off + kNQCol + wg * 32, nv);
-        tmem_ld_wait();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(n_free);
       if (ok) ok = mbar_wait(d_full, i & 1, wctx);
+      tc_fence_after();
       float part = 0.f;
-      {
-        uint32_t dw[16];   // this thread's 32 columns of dO, bf16 pairs
-        load_row32(dot, wg * 4, t, dw);
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        // 16 of this thread's 32 columns of N and of dO
+        uint32_t nv[16];
+        if (ok) {
+          tmem_ld16(tmem + lane_off + kNQCol + wg * 32 + 16 * hf, nv);
+          tmem_ld_wait();
+        }
+        if (hf == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(n_free);
+        }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          part = fmaf(bf_lo(dw[j]), __uint_as_float(nv[2 * j]), part);
-          part = fmaf(bf_hi(dw[j]), __uint_as_float(nv[2 * j + 1]), part);
+        for (int c = 0; c < 2; ++c) {
+          const int chunk = wg * 4 + 2 * hf + c;
+          const uint4 u = *reinterpret_cast<const uint4*>(dot + t * 128 + ((chunk ^ (t & 7)) << 4));
+          const uint32_t dw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            part = fmaf(bf_lo(dw[j]), __uint_as_float(nv[8 * c + 2 * j]), part);
+            part = fmaf(bf_hi(dw[j]), __uint_as_float(nv[8 * c + 2 * j + 1]), part);
+          }
         }
       }
       xb[wg * kBM + t] = part;
@@ -625,19 +638,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_query_kernel(const __grid
           }
         }
       };
+      // g (bf16) over Psi, then rescaled by the row's power of two to fp16
       float gmax = 0.f;
-#pragma unroll 1
-      for (int ch = 0; ch < kChunks; ++ch) {
-        if (!ok) break;
-        uint32_t g[32];
-        chunk_g(ch, g);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) gmax = fmaxf(gmax, fabsf(__uint_as_float(g[j])));
-      }
-      xc[wg * kBM + t] = gmax;
-      named_bar(1, kEpiThreads);
-      float beta, inv_beta;
-      row_scale(fmaxf(xc[t], xc[kBM + t]), &beta, &inv_beta);
 #pragma unroll 1
       for (int ch = 0; ch < kChunks; ++ch) {
         uint32_t g[32];
@@ -648,9 +650,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_query_kernel(const __grid
           if (lane == 0) mbar_arrive(t_free);
         }
         if (ok) {
-          pack_g(g, beta);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) gmax = fmaxf(gmax, fabsf(__uint_as_float(g[j])));
+          pack_g_bf16(g);
           store_row<16>(phi_blk_a, kAtom, t, c0 + 32 * ch, g);
         }
+      }
+      xc[wg * kBM + t] = gmax;
+      named_bar(1, kEpiThreads);
+      float beta, inv_beta;
+      row_scale(fmaxf(xc[t], xc[kBM + t]), &beta, &inv_beta);
+#pragma unroll 1
+      for (int ch = 0; ch < kChunks; ++ch) {
+        const int col = c0 + 32 * ch;
+        uint32_t w[16];
+        load_row32(phi_blk + (col >> 6) * kAtom, (col & 63) >> 3, t, w);
+        rescale_f16(w, beta);
+        store_row<16>(phi_blk_a, kAtom, t, col, w);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -660,24 +676,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_query_kernel(const __grid
       // tile's dS product, complete once dQ is)
       if (ok) ok = mbar_wait(dq_full, i & 1, wctx);
       tc_fence_after();
-      uint32_t v[32];
-      if (ok) {
-        tmem_ld32(tmem + lane_off + kNQCol + wg * 32, v);
-        tmem_ld_wait();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_free);
       const float f = prm.scale * inv_beta;
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t v[16];
+        if (ok) {
+          tmem_ld16(tmem + lane_off + kNQCol + wg * 32 + 16 * hf, v);
+          tmem_ld_wait();
+        }
+        if (hf == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dq_free);
+        }
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int chunk = wg * 4 + c;
-        const int o = 8 * c;
-        st_shared_v4(dl_a + t * 128 + ((chunk ^ (t & 7)) << 4),
-                     pack_bf16(__uint_as_float(v[o]) * f, __uint_as_float(v[o + 1]) * f),
-                     pack_bf16(__uint_as_float(v[o + 2]) * f, __uint_as_float(v[o + 3]) * f),
-                     pack_bf16(__uint_as_float(v[o + 4]) * f, __uint_as_float(v[o + 5]) * f),
-                     pack_bf16(__uint_as_float(v[o + 6]) * f, __uint_as_float(v[o + 7]) * f));
+        for (int c = 0; c < 2; ++c) {
+          const int chunk = wg * 4 + 2 * hf + c;
+          const int o = 8 * c;
+          st_shared_v4(dl_a + t * 128 + ((chunk ^ (t & 7)) << 4),
+                       pack_bf16(__uint_as_float(v[o]) * f, __uint_as_float(v[o + 1]) * f),
+                       pack_bf16(__uint_as_float(v[o + 2]) * f, __uint_as_float(v[o + 3]) * f),
+                       pack_bf16(__uint_as_float(v[o + 4]) * f, __uint_as_float(v[o + 5]) * f),
+                       pack_bf16(__uint_as_float(v[o + 6]) * f, __uint_as_float(v[o + 7]) * f));
+        }
       }
       fence_proxy_async_smem();
       named_bar(1, kEpiThreads);
@@ -1012,18 +1033,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_key_kernel(const __grid_c
       // ---- dV, staged over the V tile (read by T, complete with dV)
       if (ok) ok = mbar_wait(t_full, i & 1, wctx);
       tc_fence_after();
-      {
-        uint32_t v[32];
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t v[16];
         if (ok) {
-          tmem_ld32(tmem + lane_off + kDVCol + wg * 32, v);
+          tmem_ld16(tmem + lane_off + kDVCol + wg * 32 + 16 * hf, v);
           tmem_ld_wait();
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(dv_free);
+        if (hf == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dv_free);
+        }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int chunk = wg * 4 + c;
+        for (int c = 0; c < 2; ++c) {
+          const int chunk = wg * 4 + 2 * hf + c;
           const int o = 8 * c;
           st_shared_v4(vt + t * 128 + ((chunk ^ (t & 7)) << 4),
                        pack_bf16(__uint_as_float(v[o]), __uint_as_float(v[o + 1])),
@@ -1031,8 +1055,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_key_kernel(const __grid_c
                        pack_bf16(__uint_as_float(v[o + 4]), __uint_as_float(v[o + 5])),
                        pack_bf16(__uint_as_float(v[o + 6]), __uint_as_float(v[o + 7])));
         }
-        fence_proxy_async_smem();
       }
+      fence_proxy_async_smem();
       // ---- g = (T + dz) * slope(phi): row maximum and (prf) row sum
       auto chunk_g = [&](int ch, uint32_t (&x)[32]) {
         const int col = c0 + 32 * ch;
@@ -1058,21 +1082,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_key_kernel(const __grid_c
           }
         }
       };
+      // g (bf16) over phi(K), then rescaled by the row's power of two to fp16
       float gmax = 0.f, gsum = 0.f;
 #pragma unroll 1
       for (int ch = 0; ch < kChunks; ++ch) {
-        if (!ok) break;
         uint32_t g[32];
-        chunk_g(ch, g);
-        float s8[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s8[j] = 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          gmax = fmaxf(gmax, fabsf(__uint_as_float(g[j])));
-          s8[j & 7] += __uint_as_float(g[j]);
+        if (ok) chunk_g(ch, g);
+        if (ch == kChunks - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(t_free);
         }
-        gsum += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+        if (ok) {
+          float s8[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) s8[j] = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            gmax = fmaxf(gmax, fabsf(__uint_as_float(g[j])));
+            s8[j & 7] += __uint_as_float(g[j]);
+          }
+          gsum += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+          pack_g_bf16(g);
+          store_row<16>(phi_blk_a, kAtom, t, c0 + 32 * ch, g);
+        }
       }
       xa[wg * kBM + t] = gmax;
       xb[wg * kBM + t] = gsum;
@@ -1091,17 +1124,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_key_kernel(const __grid_c
       const float gs = xb[t] + xb[kBM + t];
 #pragma unroll 1
       for (int ch = 0; ch < kChunks; ++ch) {
-        uint32_t g[32];
-        if (ok) chunk_g(ch, g);
-        if (ch == kChunks - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(t_free);
-        }
-        if (ok) {
-          pack_g(g, beta);
-          store_row<16>(phi_blk_a, kAtom, t, c0 + 32 * ch, g);
-        }
+        const int col = c0 + 32 * ch;
+        uint32_t w[16];
+        load_row32(phi_blk + (col >> 6) * kAtom, (col & 63) >> 3, t, w);
+        rescale_f16(w, beta);
+        store_row<16>(phi_blk_a, kAtom, t, col, w);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -1110,33 +1137,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_key_kernel(const __grid_c
       // ---- dK = s ((G Omega) / beta - [prf] s k sum_i g_i), over the K tile
       if (ok) ok = mbar_wait(dk_full, i & 1, wctx);
       tc_fence_after();
-      uint32_t v[32];
-      if (ok) {
-        tmem_ld32(tmem + lane_off + kDKCol + wg * 32, v);
-        tmem_ld_wait();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dk_free);
       uint8_t* kt = sm + C::kK + ks * kTileBytes;
       const float f = prm.scale * inv_beta;
       const float fk = FM == FAVOR_FM_PRF ? prm.scale * prm.scale * gs : 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int chunk = wg * 4 + c;
-        uint8_t* p = kt + t * 128 + ((chunk ^ (t & 7)) << 4);
-        const uint4 u = *reinterpret_cast<const uint4*>(p);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float k0 = __half2float(__ushort_as_half(static_cast<unsigned short>(w[j] & 0xFFFFu)));
-          const float k1 = __half2float(__ushort_as_half(static_cast<unsigned short>(w[j] >> 16)));
-          const float a0 = __uint_as_float(v[8 * c + 2 * j]) * f - fk * k0;
-          const float a1 = __uint_as_float(v[8 * c + 2 * j + 1]) * f - fk * k1;
-          o[j] = pack_bf16(a0, a1);
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t v[16];
+        if (ok) {
+          tmem_ld16(tmem + lane_off + kDKCol + wg * 32 + 16 * hf, v);
+          tmem_ld_wait();
         }
-        st_shared_v4(smem_addr(p), o[0], o[1], o[2], o[3]);
+        if (hf == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dk_free);
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int chunk = wg * 4 + 2 * hf + c;
+          uint8_t* p = kt + t * 128 + ((chunk ^ (t & 7)) << 4);
+          const uint4 u = *reinterpret_cast<const uint4*>(p);
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float k0 = __half2float(__ushort_as_half(static_cast<unsigned short>(w[j] & 0xFFFFu)));
+            const float k1 = __half2float(__ushort_as_half(static_cast<unsigned short>(w[j] >> 16)));
+            const float a0 = __uint_as_float(v[8 * c + 2 * j]) * f - fk * k0;
+            const float a1 = __uint_as_float(v[8 * c + 2 * j + 1]) * f - fk * k1;
+            o[j] = pack_bf16(a0, a1);
+          }
+          st_shared_v4(smem_addr(p), o[0], o[1], o[2], o[3]);
+        }
       }
       fence_proxy_async_smem();
       named_bar(1, kEpiThreads);
