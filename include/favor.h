@@ -278,9 +278,12 @@ size_t favor_static_scratch_bytes(void);
  *   N = phi(Q) S, D = phi(Q) z, O = N / D;  dN^ = [dO / D | -(dO . N) / D^2]
  *   dphi(Q) = S~ dN^,  dS~ = phi(Q)^T dN^,  dphi(K) = dS~ [V | 1]^T,
  *   dV = phi(K) dS~[:, :d],  dx = s (sum_i g_i w_i - [prf] s x sum_i g_i)
- * with g = dphi phi (positive random features) or dphi [s w.x > 0] (ReLU);
- * Omega is not differentiated (it is a fixed random draw).  CUDA-core
- * kernels, fp32 arithmetic, any supported shape; workspace of
+ * with g = dphi phi (positive random features), dphi [s w.x > 0] (ReLU) or
+ * dphi min(phi, 1) (1 + elu); Omega is not differentiated (it is a fixed
+ * random draw).  bf16 with d = 64 and m in {128, 256} runs on the tcgen05
+ * tensor-core kernels (bf16/fp16 operands, fp32 accumulation; D from the
+ * fp32 normaliser, dS~ carried as a bf16 hi + lo pair), every other
+ * supported shape on the CUDA-core kernels in fp32; workspace of
  * favor_bwd_workspace_bytes(...) bytes.  A zero or non-finite normaliser is
  * reported in dev_status.
  */
@@ -297,8 +300,8 @@ favor_status favor_bwd_bidir(const void* Q, const void* K, const void* V, const 
  *   dphi(k_s) = H_c [v_s ; 1] + sum_{t>=s in the tile} (dN^_t . [v_s ; 1]) phi(q_t)
  *   dV_s = H_c[:, :d]^T phi(k_s) + sum_{t>=s in the tile} (phi(k_s).phi(q_t)) dN_t
  * ("Performer" digest, §Methods causal bullet, differentiated).  One CTA per
- * head walks the sequence forward then backward.  Same arguments and
- * workspace size as favor_bwd_bidir.
+ * head walks the sequence forward then backward (CUDA-core kernels, every
+ * shape).  Same arguments and workspace size as favor_bwd_bidir.
  */
 favor_status favor_bwd_causal(const void* Q, const void* K, const void* V, const void* dO,
                               void* dQ, void* dK, void* dV, int B, int H, int L, int d,
