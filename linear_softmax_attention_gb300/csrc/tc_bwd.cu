@@ -55,6 +55,8 @@
 // FAVOR_ERR_TIMEOUT.
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "tc.cuh"
 #include "tc_util.cuh"
 
@@ -80,15 +82,24 @@ struct GradParams {
   const float* zvec;          // query kernel: z; key kernel: dz (fp32 [m] per head)
   const uint8_t* ds_hi;       // key kernel: dS pair (bf16 [m/64][d][128 B] per head)
   const uint8_t* ds_lo;
-  float* partS;               // query kernel: [dS | dz] partials [BH][m/128][n_split][d+1][128]
-  uint32_t* counters;         // query kernel: [BH] merge counters (zero on entry)
-  uint8_t* out_hi;            // query kernel: merged dS pair and dz
-  uint8_t* out_lo;
-  float* out_dz;
+  float* partS;               // query kernel: [dS | dz] partials [BH][m/128][parts][d+1][128], slot = the
+                              // CTA's place among the head's CTAs
   int32_t* status;
-  int L, m, tiles_per_cta, n_split;
+  int L, m;
+  int n_heads;                // B H: the CTAs split the (head, tile) list evenly
+  int parts;                  // query kernel: partial slots per head
   float scale;
 };
+
+// The CTAs of a grid of n_ctas split the list of n_heads * nt (head, tile)
+// pairs evenly: CTA c takes [first(c), first(c + 1)).
+__host__ __device__ __forceinline__ int range_first(long long total, int c, int n_ctas) {
+  return (int)(total * c / n_ctas);
+}
+// the CTA holding list entry x
+__host__ __device__ __forceinline__ int range_cta(long long total, long long x, int n_ctas) {
+  return (int)(((x + 1) * n_ctas + total - 1) / total) - 1;
+}
 
 // power of two that brings a row's largest |g| into [2^14, 2^15) (1 for an
 // all-zero row), and its inverse; both normal floats for every finite max
@@ -130,10 +141,12 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 // which moves w_i.x by at most 2^-11 sum_k |x_k w_ik| <= 2^-11 |x| max|w|;
 // the slope [w_i.x > 0] is a step, so a feature whose fp16 projection lies
 // within tau (twice that bound) of 0 takes its sign from w_i.x recomputed in
-// fp32 from the fp32 Omega and the row (exact in the fp16 tile).  x holds the
-// raw projections of features f0 .. f0 + 31 of row t; such a feature becomes
-// 0 or a positive value below tau / 256 (its true size is below tau either
-// way).
+// fp32 from the fp32 Omega and the row (exact in the fp16 tile), and where
+// that sum is itself within its rounding bound (2 d 2^-24 sum_k |x_k w_ik|)
+// of 0, in fp64 (every product of a bf16 x and an fp32 w is exact there).
+// x holds the raw projections of features f0 .. f0 + 31 of row t; such a
+// feature becomes 0 or a positive value below tau / 256 (its true size is
+// below tau either way).
 __device__ __forceinline__ void relu_guard(uint32_t (&x)[32], int f0, float tau, const uint8_t* tile, int t,
                                            const float* __restrict__ omega) {
   uint32_t flag = 0;
@@ -144,7 +157,7 @@ __device__ __forceinline__ void relu_guard(uint32_t (&x)[32], int f0, float tau,
     const int j = __ffs(todo) - 1;
     todo &= todo - 1u;
     const float4* w = reinterpret_cast<const float4*>(omega + (size_t)(f0 + j) * kD);
-    float acc = 0.f;
+    float acc = 0.f, mag = 0.f;
 #pragma unroll 2
     for (int c = 0; c < kD / 8; ++c) {
       const uint4 u = *reinterpret_cast<const uint4*>(tile + t * 128 + ((c ^ (t & 7)) << 4));
@@ -153,11 +166,33 @@ __device__ __forceinline__ void relu_guard(uint32_t (&x)[32], int f0, float tau,
       const float wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        acc = fmaf(__half2float(__ushort_as_half(static_cast<unsigned short>(h[k] & 0xFFFFu))), wv[2 * k], acc);
-        acc = fmaf(__half2float(__ushort_as_half(static_cast<unsigned short>(h[k] >> 16))), wv[2 * k + 1], acc);
+        const float x0 = __half2float(__ushort_as_half(static_cast<unsigned short>(h[k] & 0xFFFFu)));
+        const float x1 = __half2float(__ushort_as_half(static_cast<unsigned short>(h[k] >> 16)));
+        acc = fmaf(x0, wv[2 * k], acc);
+        acc = fmaf(x1, wv[2 * k + 1], acc);
+        mag = fmaf(fabsf(x0), fabsf(wv[2 * k]), mag);
+        mag = fmaf(fabsf(x1), fabsf(wv[2 * k + 1]), mag);
       }
     }
-    if (acc > 0.f) pos |= 1u << j;
+    bool positive = acc > 0.f;
+    if (fabsf(acc) <= mag * (2.0f * kD * 0x1p-24f)) {
+      double acc64 = 0.0;
+      for (int c = 0; c < kD / 8; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4*>(tile + t * 128 + ((c ^ (t & 7)) << 4));
+        const float4 a = __ldg(w + 2 * c), b = __ldg(w + 2 * c + 1);
+        const uint32_t h[4] = {u.x, u.y, u.z, u.w};
+        const float wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc64 = fma((double)__half2float(__ushort_as_half(static_cast<unsigned short>(h[k] & 0xFFFFu))),
+                      (double)wv[2 * k], acc64);
+          acc64 = fma((double)__half2float(__ushort_as_half(static_cast<unsigned short>(h[k] >> 16))),
+                      (double)wv[2 * k + 1], acc64);
+        }
+      }
+      positive = acc64 > 0.0;
+    }
+    if (positive) pos |= 1u << j;
   }
 #pragma unroll
   for (int j = 0; j < 32; ++j)
@@ -167,29 +202,29 @@ __device__ __forceinline__ void relu_guard(uint32_t (&x)[32], int f0, float tau,
 // fp16 rounding of row entries below the fp16 normal range)
 __device__ __forceinline__ float relu_tau(float x2, float wmax) { return wmax * (sqrtf(x2) * 0x1p-10f + 0x1p-21f); }
 
-// Adds one head's n_split fp32 [dS | dz] partials ([M/128][n_split][D+1][128],
-// feature fastest) in split order: dS as a bf16 pair hi + lo (hi = bf16(x),
+// Adds one head's first `count` fp32 [dS | dz] partials ([M/128][parts][D+1][128],
+// feature fastest) in slot order: dS as a bf16 pair hi + lo (hi = bf16(x),
 // lo = bf16(x - hi); images [M/64 atoms][D rows][128 B], 128-byte swizzle)
-// and dz in fp32.  All `nthreads` threads; item = (block, row n, 4 features).
+// and dz in fp32.  Items [e_begin, e_end) of the NFB (D + 1) 32 items =
+// (block, row n, 4 features), by all `nthreads` threads.
 template <int D, int M>
-__device__ void merge_grad_state(const float* __restrict__ base, int n_split, uint8_t* __restrict__ hi,
-                                 uint8_t* __restrict__ lo, float* __restrict__ dz, int nthreads) {
-  constexpr int NFB = M / kFB;
+__device__ void merge_grad_state(const float* __restrict__ base, int parts, int count, uint8_t* __restrict__ hi,
+                                 uint8_t* __restrict__ lo, float* __restrict__ dz, int e_begin, int e_end,
+                                 int nthreads) {
   constexpr int NG = kFB / 4;
-  constexpr int kItems = NFB * (D + 1) * NG;
-  constexpr int kBatch = 8;
-  for (int e0 = threadIdx.x; e0 < kItems; e0 += kBatch * nthreads) {
+  constexpr int kBatch = 4;
+  for (int e0 = e_begin + threadIdx.x; e0 < e_end; e0 += kBatch * nthreads) {
     float4 acc[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int p = 0; p < n_split; ++p) {
+    for (int p = 0; p < count; ++p) {
       float4 v[kBatch];
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
         const int e = e0 + u * nthreads;
         const int g = e % NG, n = (e / NG) % (D + 1), b = e / (NG * (D + 1));
-        v[u] = e < kItems
-                   ? *reinterpret_cast<const float4*>(base + (((size_t)b * n_split + p) * (D + 1) + n) * kFB + g * 4)
+        v[u] = e < e_end
+                   ? *reinterpret_cast<const float4*>(base + (((size_t)b * parts + p) * (D + 1) + n) * kFB + g * 4)
                    : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
@@ -203,7 +238,7 @@ __device__ void merge_grad_state(const float* __restrict__ base, int n_split, ui
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int e = e0 + u * nthreads;
-      if (e >= kItems) break;
+      if (e >= e_end) break;
       const int g = e % NG, n = (e / NG) % (D + 1), b = e / (NG * (D + 1));
       const int f = b * kFB + g * 4;
       if (n == D) {
@@ -275,18 +310,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_query_kernel(const __grid
   uint64_t* dq_free = dq_full + 1;        // dQ copied out
   uint64_t* setup_bar = dq_free + 1;
   uint64_t* done_bar = setup_bar + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  uint64_t* img_full = done_bar + 1;      // phase k: the k-th head's S image and z landed
+  uint64_t* img_free = img_full + 1;      // phase k: the k-th head's last tile no longer reads them
+  uint64_t* ds_free = img_free + 1;       // phase k: the k-th head's [dS | dz] copied out of tensor memory
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ds_free + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* is_last = const_cast<int*>(abort_flag) + 1;
   float* xch = reinterpret_cast<float*>(sm + C::kX);
   float* norm_s = reinterpret_cast<float*>(sm + C::kNorm);
   const float* z_s = reinterpret_cast<const float*>(sm + C::kZ);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x, bh = blockIdx.y;
-  const int tile0 = split * prm.tiles_per_cta;
-  const int n_tiles_total = (prm.L + kBM - 1) / kBM;
-  const int n_tiles = min(prm.tiles_per_cta, n_tiles_total - tile0);
+  // this CTA's tiles: the contiguous range [g0, g1) of the (head, tile) list,
+  // which may cross from one head into the next; each head's [dS | dz] part
+  // goes to the slot of this CTA's place among the head's CTAs
+  const int nt = (prm.L + kBM - 1) / kBM;
+  const long long total = (long long)prm.n_heads * nt;
+  const int g0 = range_first(total, blockIdx.x, gridDim.x);
+  const int g1 = range_first(total, blockIdx.x + 1, gridDim.x);
+  const int n_tiles = g1 - g0;
+  const int h0 = g0 / nt;
+  const int n_heads = n_tiles > 0 ? (g1 - 1) / nt - h0 + 1 : 0;
+  auto head_of = [&](int i) { return (g0 + i) / nt; };
+  auto tile_of = [&](int i) { return (g0 + i) - head_of(i) * nt; };
+  auto head_starts = [&](int i) { return i == 0 || head_of(i) != head_of(i - 1); };
+  auto head_ends = [&](int i) { return i == n_tiles - 1 || head_of(i + 1) != head_of(i); };
   const WaitCtx wctx{abort_flag, prm.status};
 
   if (threadIdx.x == 0) {
@@ -310,8 +357,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_query_kernel(const __grid
     mbar_init(dq_free, kEpiWarps);
     mbar_init(setup_bar, 1);
     mbar_init(done_bar, 1);
+    mbar_init(img_full, 1);
+    mbar_init(img_free, kEpiWarps);
+    mbar_init(ds_free, kEpiWarps);
     *abort_flag = 0;
-    *is_last = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -329,28 +378,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_query_kernel(const __grid
       prefetch_tmap(&mapDO);
       prefetch_tmap(&mapDQ);
       const uint32_t ob = M * kD * 2, sb = M * kGN * 2, zb = M * 4;
-      mbar_arrive_expect_tx(setup_bar, ob + sb + zb);
+      mbar_arrive_expect_tx(setup_bar, ob);
       bulk_load(sm + C::kOmega, prm.omega_img, ob, setup_bar);
-      bulk_load(sm + C::kState, prm.state_img + (size_t)bh * sb, sb, setup_bar);
-      bulk_load(sm + C::kZ, prm.zvec + (size_t)bh * M, zb, setup_bar);
+      // head k's S image and z go in once head k - 1's last tile is done with them
+      auto load_head = [&](int k) {
+        const size_t hh = (size_t)(h0 + k);
+        mbar_arrive_expect_tx(img_full, sb + zb);
+        bulk_load(sm + C::kState, prm.state_img + hh * sb, sb, img_full);
+        bulk_load(sm + C::kZ, prm.zvec + hh * M, zb, img_full);
+      };
+      int ni = 0;
+      if (n_heads > 0) load_head(ni++);
       // Q tile x goes to slot x % NSQ once tile x - NSQ's reader is done;
       // dO tile x once tile x - 1's products have read the dO slot
       Watchdog wd(wctx);
       int nq = 0, nd = 0;
       bool ok = true;
-      while (ok && (nq < n_tiles || nd < n_tiles)) {
+      while (ok && (nq < n_tiles || nd < n_tiles || ni < n_heads)) {
         bool progress = false;
         if (nq < n_tiles && (nq < NSQ || mbar_test_wait(smem_addr(&q_empty[nq % NSQ]), ((nq / NSQ) - 1) & 1))) {
           const int st = nq % NSQ;
           mbar_arrive_expect_tx(&q_full[st], kTileBytes);
-          tma_load_3d(sm + C::kQ + st * kTileBytes, &mapQ, 0, (tile0 + nq) * kBM, bh, &q_full[st]);
+          tma_load_3d(sm + C::kQ + st * kTileBytes, &mapQ, 0, tile_of(nq) * kBM, head_of(nq), &q_full[st]);
           ++nq;
           progress = true;
         }
         if (nd < nq && (nd == 0 || mbar_test_wait(smem_addr(d_empty), (nd - 1) & 1))) {
           mbar_arrive_expect_tx(d_full, kTileBytes);
-          tma_load_3d(sm + C::kDO, &mapDO, 0, (tile0 + nd) * kBM, bh, d_full);
+          tma_load_3d(sm + C::kDO, &mapDO, 0, tile_of(nd) * kBM, head_of(nd), d_full);
           ++nd;
+          progress = true;
+        }
+        if (ni < n_heads && mbar_test_wait(smem_addr(img_free), (ni - 1) & 1)) {
+          load_head(ni++);
           progress = true;
         }
         if (progress) wd.progress();
@@ -358,6 +418,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_query_kernel(const __grid
       }
       for (int x = max(0, nq - NSQ); x < nq; ++x) mbar_wait(&q_full[x % NSQ], (x / NSQ) & 1, wctx);
       if (nd > 0) mbar_wait(d_full, (nd - 1) & 1, wctx);
+      if (ni > 0) mbar_wait(img_full, (ni - 1) & 1, wctx);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -395,6 +456,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_query_kernel(const __grid
           }
         }
         if (ib < ia && mbar_test_wait(smem_addr(phi_full), ib & 1) &&
+            mbar_test_wait(smem_addr(img_full), (head_of(ib) - h0) & 1) &&
             (ib == 0 || mbar_test_wait(smem_addr(dq_free), (ib - 1) & 1))) {
           // N = phi(Q) S (the first d rows of the image)
           tc_fence_after();
@@ -410,7 +472,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_query_kernel(const __grid
           ++ib;
           progress = true;
         }
-        if (ic < ib && mbar_test_wait(smem_addr(dn_full), ic & 1) && mbar_test_wait(smem_addr(p_free), ic & 1)) {
+        // a head's first tile restarts the [dS | dz] accumulators once the
+        // previous head's were copied out
+        const bool fresh = ic < ib && head_starts(ic);
+        if (ic < ib && mbar_test_wait(smem_addr(dn_full), ic & 1) && mbar_test_wait(smem_addr(p_free), ic & 1) &&
+            (!fresh || ic == 0 || mbar_test_wait(smem_addr(ds_free), (head_of(ic) - h0 - 1) & 1))) {
           tc_fence_after();
           // [dS | dz]_b += Psi_b^T [dO | -delta] (both token-major: MN-major;
           // the -delta columns sit one tile after the dO tile)
@@ -421,7 +487,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_query_kernel(const __grid
 #pragma unroll
             for (int k = 0; k < kBM / 16; ++k)
               mma_bf16(tmem + kDSCol + fb * kGN, dadd(a0, kstep_mn(k)), dadd(bd, kstep_mn(k)), id_ds,
-                       (ic > 0) || (k > 0));
+                       !fresh || (k > 0));
           }
           // T = dO S^T into [0, M): the image's first d rows are the K dimension
           const uint64_t a1 = sdesc(do_a, 16, 1024);
@@ -490,9 +556,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_query_kernel(const __grid
     float* xd = xch + 6 * kBM;        // [2][128] partial D
     float R_unused, W;
     key_reference(prm.key_ref, prm.m, &R_unused, &W);
-    bool ok = mbar_wait(setup_bar, 0, wctx);   // z is read from shared memory below
+    bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
-      const bool valid = (tile0 + i) * kBM + t < prm.L;
+      const int hi_t = head_of(i), ti = tile_of(i);
+      const bool valid = ti * kBM + t < prm.L;
+      if (ok) ok = mbar_wait(img_full, (hi_t - h0) & 1, wctx);   // this head's z
       const int qs = i % NSQ;
       // ---- phi(Q): the row's reference is its largest exponent; rows past
       // the sequence end get 0.  D = phi(Q) . z summed in fp32 alongside.
@@ -656,6 +724,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_query_kernel(const __grid
           store_row<16>(phi_blk_a, kAtom, t, c0 + 32 * ch, g);
         }
       }
+      if (head_ends(i)) {
+        // the head's S image and z: read by this tile's products (complete)
+        // and by the pass above, for the last time
+        __syncwarp();
+        if (lane == 0) mbar_arrive(img_free);
+      }
       xc[wg * kBM + t] = gmax;
       named_bar(1, kEpiThreads);
       float beta, inv_beta;
@@ -671,6 +745,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_query_kernel(const __grid
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(g_full);
+
+      if (head_ends(i)) {
+        // the head's [dS | dz] part (complete with this tile's products) to
+        // its slot: lane f = feature f of a block; dz is the sum of the two
+        // -delta columns.  Two blocks: warpgroup w reads block w; one block:
+        // the warpgroups split the d columns.
+        const int slot = (int)blockIdx.x - range_cta(total, (long long)hi_t * nt, gridDim.x);
+        const int sfb = (NFB == 2) ? wg : 0;
+        float* dst = prm.partS + ((((size_t)hi_t * NFB + sfb) * prm.parts + slot) * (kD + 1)) * kFB;
+        const uint32_t s_col = tmem + lane_off + kDSCol + sfb * kGN;
+#pragma unroll 1
+        for (int cb = 0; cb < kD / 16; ++cb) {
+          if (NFB == 1 && (cb >> 1) != wg) continue;
+          uint32_t v[16];
+          if (ok) {
+            tmem_ld16(s_col + cb * 16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) dst[(size_t)(cb * 16 + j) * kFB + t] = __uint_as_float(v[j]);
+          }
+        }
+        if (NFB == 2 || wg == 1) {
+          uint32_t z[8];
+          if (ok) {
+            tmem_ld8(s_col + kD, z);
+            tmem_ld_wait();
+            dst[(size_t)kD * kFB + t] = __uint_as_float(z[0]) + __uint_as_float(z[1]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ds_free);
+      }
 
       // ---- dQ = s (G Omega) / beta, staged in the -delta tile (read by this
       // tile's dS product, complete once dQ is)
@@ -703,56 +810,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_query_kernel(const __grid
       fence_proxy_async_smem();
       named_bar(1, kEpiThreads);
       if (threadIdx.x == kEpiTid0 && ok && !*abort_flag) {
-        tma_store_3d(&mapDQ, 0, (tile0 + i) * kBM, bh, sm + C::kDl);
+        tma_store_3d(&mapDQ, 0, ti * kBM, hi_t, sm + C::kDl);
         bulk_commit();
       }
     }
     if (threadIdx.x == kEpiTid0) bulk_wait0();
-    // this split's [dS | dz]: lane f = feature f of a block; dz is the sum of
-    // the two -delta columns.  Two blocks: warpgroup w reads block w; one
-    // block: the warpgroups split the d columns.
-    const bool done = mbar_wait(done_bar, 0, wctx);
-    tc_fence_after();
-    if (done && !*abort_flag && n_tiles > 0) {
-      const int sfb = (NFB == 2) ? wg : 0;
-      float* dst = prm.partS + ((((size_t)bh * NFB + sfb) * prm.n_split + split) * (kD + 1)) * kFB;
-      const uint32_t s_col = tmem + lane_off + kDSCol + sfb * kGN;
-#pragma unroll
-      for (int cb = 0; cb < kD / 32; ++cb) {
-        if (NFB == 1 && (cb & 1) != wg) continue;
-        uint32_t v[32];
-        tmem_ld32(s_col + cb * 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) dst[(size_t)(cb * 32 + j) * kFB + t] = __uint_as_float(v[j]);
-      }
-      if (NFB == 2 || wg == 1) {
-        uint32_t z[8];
-        tmem_ld8(s_col + kD, z);
-        tmem_ld_wait();
-        dst[(size_t)kD * kFB + t] = __uint_as_float(z[0]) + __uint_as_float(z[1]);
-      }
-    }
-    tc_fence_before();
-    named_bar(1, kEpiThreads);
-    if (threadIdx.x == kEpiTid0) {
-      __threadfence();
-      const uint32_t old = atomicAdd(&prm.counters[bh], 1u);
-      *is_last = (old == (uint32_t)(prm.n_split - 1)) ? 1 : 0;
-    }
+    mbar_wait(done_bar, 0, wctx);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
-  // the last CTA of a head adds the splits' partials (fixed split order)
-  if (*is_last) {
-    __threadfence();
-    merge_grad_state<kD, M>(prm.partS + (size_t)bh * NFB * prm.n_split * (kD + 1) * kFB, prm.n_split,
-                            prm.out_hi + (size_t)bh * M * kD * 2, prm.out_lo + (size_t)bh * M * kD * 2,
-                            prm.out_dz + (size_t)bh * M, kBwdThreads);
-    if (threadIdx.x == 0) prm.counters[bh] = 0;
-  }
+}
+
+// CTA (head, y): a 1 / kMergeSplit share of the head's items, its [dS | dz]
+// parts (one per query-kernel CTA that covered the head, in CTA order) added
+// into the dS pair and dz
+constexpr int kMergeSplit = 8;
+template <int M>
+__global__ void __launch_bounds__(128) grad_merge_kernel(const float* __restrict__ partS, int parts, int nt,
+                                                         int n_heads, int n_ctas, uint8_t* __restrict__ hi,
+                                                         uint8_t* __restrict__ lo, float* __restrict__ dz) {
+  constexpr int NFB = M / kFB;
+  constexpr int kItems = NFB * (kD + 1) * (kFB / 4);
+  constexpr int kShare = (kItems + kMergeSplit - 1) / kMergeSplit;
+  const int h = blockIdx.x;
+  const long long total = (long long)n_heads * nt;
+  const int count = range_cta(total, (long long)(h + 1) * nt - 1, n_ctas) - range_cta(total, (long long)h * nt, n_ctas) + 1;
+  merge_grad_state<kD, M>(partS + (size_t)h * NFB * parts * (kD + 1) * kFB, parts, count, hi + (size_t)h * M * kD * 2,
+                          lo + (size_t)h * M * kD * 2, dz + (size_t)h * M, blockIdx.y * kShare,
+                          min(kItems, (int)(blockIdx.y + 1) * kShare), blockDim.x);
 }
 
 // ---------------------------------------------------------------------------
@@ -805,17 +892,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_key_kernel(const __grid_c
   uint64_t* dk_free = dk_full + 1;
   uint64_t* setup_bar = dk_free + 1;
   uint64_t* done_bar = setup_bar + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  uint64_t* img_full = done_bar + 1;      // phase k: the k-th head's dS pair and dz landed
+  uint64_t* img_free = img_full + 1;      // phase k: the k-th head's last tile no longer reads them
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(img_free + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* norm_s = reinterpret_cast<float*>(sm + C::kNorm);
   float* xch = reinterpret_cast<float*>(sm + C::kX);
   const float* dz_s = reinterpret_cast<const float*>(sm + C::kZ);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
-  const int tile0 = blockIdx.x * prm.tiles_per_cta;
-  const int n_tiles_total = (prm.L + kBM - 1) / kBM;
-  const int n_tiles = min(prm.tiles_per_cta, n_tiles_total - tile0);
+  // this CTA's tiles: the contiguous range [g0, g1) of the (head, tile) list,
+  // which may cross from one head into the next
+  const int nt = (prm.L + kBM - 1) / kBM;
+  const long long total = (long long)prm.n_heads * nt;
+  const int g0 = (int)(total * blockIdx.x / gridDim.x);
+  const int g1 = (int)(total * (blockIdx.x + 1) / gridDim.x);
+  const int n_tiles = g1 - g0;
+  const int h0 = g0 / nt;
+  const int n_heads = n_tiles > 0 ? (g1 - 1) / nt - h0 + 1 : 0;
+  auto head_of = [&](int i) { return (g0 + i) / nt; };      // the CTA's i-th tile's head
+  auto tile_of = [&](int i) { return (g0 + i) - head_of(i) * nt; };
   const WaitCtx wctx{abort_flag, prm.status};
 
   if (threadIdx.x == 0) {
@@ -837,6 +933,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_key_kernel(const __grid_c
     mbar_init(dk_free, kEpiWarps);
     mbar_init(setup_bar, 1);
     mbar_init(done_bar, 1);
+    mbar_init(img_full, 1);
+    mbar_init(img_free, kEpiWarps);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -856,27 +954,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_key_kernel(const __grid_c
       prefetch_tmap(&mapDK);
       prefetch_tmap(&mapDV);
       const uint32_t ob = M * kD * 2, hb = M * kD * 2, zb = M * 4;
-      mbar_arrive_expect_tx(setup_bar, ob + 2 * hb + zb);
+      mbar_arrive_expect_tx(setup_bar, ob);
       bulk_load(sm + C::kOmega, prm.omega_img, ob, setup_bar);
-      bulk_load(sm + C::kHi, prm.ds_hi + (size_t)bh * hb, hb, setup_bar);
-      bulk_load(sm + C::kLo, prm.ds_lo + (size_t)bh * hb, hb, setup_bar);
-      bulk_load(sm + C::kZ, prm.zvec + (size_t)bh * M, zb, setup_bar);
+      // head k's dS pair and dz go in once head k - 1's last tile is done with them
+      auto load_head = [&](int k) {
+        const size_t hh = (size_t)(h0 + k);
+        mbar_arrive_expect_tx(img_full, 2 * hb + zb);
+        bulk_load(sm + C::kHi, prm.ds_hi + hh * hb, hb, img_full);
+        bulk_load(sm + C::kLo, prm.ds_lo + hh * hb, hb, img_full);
+        bulk_load(sm + C::kZ, prm.zvec + hh * M, zb, img_full);
+      };
+      int ni = 0;
+      if (n_heads > 0) load_head(ni++);
       Watchdog wd(wctx);
       int nk = 0, nv = 0;
       bool ok = true;
-      while (ok && (nk < n_tiles || nv < n_tiles)) {
+      while (ok && (nk < n_tiles || nv < n_tiles || ni < n_heads)) {
         bool progress = false;
         if (nk < n_tiles && (nk < NK || mbar_test_wait(smem_addr(&k_empty[nk % NK]), ((nk / NK) - 1) & 1))) {
           const int st = nk % NK;
           mbar_arrive_expect_tx(&k_full[st], kTileBytes);
-          tma_load_3d(sm + C::kK + st * kTileBytes, &mapK, 0, (tile0 + nk) * kBM, bh, &k_full[st]);
+          tma_load_3d(sm + C::kK + st * kTileBytes, &mapK, 0, tile_of(nk) * kBM, head_of(nk), &k_full[st]);
           ++nk;
           progress = true;
         }
         if (nv < nk && (nv == 0 || mbar_test_wait(smem_addr(v_empty), (nv - 1) & 1))) {
           mbar_arrive_expect_tx(v_full, kTileBytes);
-          tma_load_3d(sm + C::kV, &mapV, 0, (tile0 + nv) * kBM, bh, v_full);
+          tma_load_3d(sm + C::kV, &mapV, 0, tile_of(nv) * kBM, head_of(nv), v_full);
           ++nv;
+          progress = true;
+        }
+        if (ni < n_heads && mbar_test_wait(smem_addr(img_free), (ni - 1) & 1)) {
+          load_head(ni++);
           progress = true;
         }
         if (progress) wd.progress();
@@ -884,6 +993,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_key_kernel(const __grid_c
       }
       for (int x = max(0, nk - NK); x < nk; ++x) mbar_wait(&k_full[x % NK], (x / NK) & 1, wctx);
       if (nv > 0) mbar_wait(v_full, (nv - 1) & 1, wctx);
+      if (ni > 0) mbar_wait(img_full, (ni - 1) & 1, wctx);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -918,6 +1028,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_key_kernel(const __grid_c
         }
         if (ic < ia && mbar_test_wait(smem_addr(phi_full), ic & 1) && mbar_test_wait(smem_addr(p_free), ic & 1) &&
             mbar_test_wait(smem_addr(v_full), ic & 1) &&
+            mbar_test_wait(smem_addr(img_full), (head_of(ic) - h0) & 1) &&
             (ic == 0 || mbar_test_wait(smem_addr(dv_free), (ic - 1) & 1))) {
           tc_fence_after();
           // dV = phi(K) dS_hi (the image's features are the K dimension)
@@ -999,7 +1110,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_key_kernel(const __grid_c
     bool ok = mbar_wait(setup_bar, 0, wctx);   // dz is read from shared memory below
     for (int i = 0; i < n_tiles; ++i) {
       const int ks = i % NK;
-      const bool valid = (tile0 + i) * kBM + t < prm.L;
+      const int hi_t = head_of(i), ti = tile_of(i);
+      const bool valid = ti * kBM + t < prm.L;
+      const bool head_ends = i == n_tiles - 1 || head_of(i + 1) != hi_t;
       // ---- phi(K) = exp(s w.k - s^2 |k|^2 / 2 - R); rows past L get 0
       if (ok) ok = mbar_wait(&kn_full[ks], (i / NK) & 1, wctx);
       const float bias =
@@ -1058,6 +1171,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_key_kernel(const __grid_c
       }
       fence_proxy_async_smem();
       // ---- g = (T + dz) * slope(phi): row maximum and (prf) row sum
+      if (ok) ok = mbar_wait(img_full, (hi_t - h0) & 1, wctx);   // this head's dz
       auto chunk_g = [&](int ch, uint32_t (&x)[32]) {
         const int col = c0 + 32 * ch;
         tmem_ld32(tmem + lane_off + f_base + 32 * ch, x);
@@ -1107,12 +1221,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_key_kernel(const __grid_c
           store_row<16>(phi_blk_a, kAtom, t, c0 + 32 * ch, g);
         }
       }
+      if (head_ends) {
+        // the head's dS pair and dz: read by this tile's products (complete)
+        // and by the pass above, for the last time
+        __syncwarp();
+        if (lane == 0) mbar_arrive(img_free);
+      }
       xa[wg * kBM + t] = gmax;
       xb[wg * kBM + t] = gsum;
       named_bar(1, kEpiThreads);
       if (threadIdx.x == kEpiTid0) {
         if (ok && !*abort_flag) {
-          tma_store_3d(&mapDV, 0, (tile0 + i) * kBM, bh, sm + C::kV);
+          tma_store_3d(&mapDV, 0, ti * kBM, hi_t, sm + C::kV);
           bulk_commit();
         }
         // the V slot takes the next tile once the store has read it
@@ -1174,7 +1294,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_key_kernel(const __grid_c
       named_bar(1, kEpiThreads);
       if (threadIdx.x == kEpiTid0) {
         if (ok && !*abort_flag) {
-          tma_store_3d(&mapDK, 0, (tile0 + i) * kBM, bh, kt);
+          tma_store_3d(&mapDK, 0, ti * kBM, hi_t, kt);
           bulk_commit();
         }
         // the K slot is reused once the store has read it
@@ -1196,17 +1316,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) grad_key_kernel(const __grid_c
 // ---------------------------------------------------------------------------
 struct GradLayout {
   TcLayout fwd;
-  size_t off_z, off_hi, off_lo, off_dz, bytes;
+  int ctas, parts;              // CTAs of each backward kernel; [dS | dz] slots per head
+  size_t off_z, off_part, off_hi, off_lo, off_dz, bytes;
 };
 
 GradLayout grad_layout(const Shape& s) {
   GradLayout g{};
   const size_t BH = s.BH();
+  const long long total = (long long)BH * ((s.L + kBM - 1) / kBM);
   g.fwd = tc_bidir_layout(s);
-  g.off_z = align_up(g.fwd.bytes, 1024);                    // fp32 z [BH][m]
-  g.off_hi = align_up(g.off_z + BH * s.m * 4, 1024);        // bf16 dS pair [BH][m/64][d][128 B]
+  // one CTA per SM (or per tile), each an even share of the (head, tile)
+  // list; a head meets at most ceil(ctas / BH) + 1 of them
+  g.ctas = (int)std::min<long long>(sm_count(), total);
+  g.parts = (g.ctas + (int)BH - 1) / (int)BH + 1;
+  g.off_z = align_up(g.fwd.bytes, 1024);                                  // fp32 z [BH][m]
+  g.off_part = align_up(g.off_z + BH * s.m * 4, 1024);                    // fp32 [BH][m/128][parts][d+1][128]
+  g.off_hi = align_up(g.off_part + BH * s.m * g.parts * (kD + 1) * 4, 1024);  // bf16 dS pair [BH][m/64][d][128 B]
   g.off_lo = align_up(g.off_hi + BH * s.m * kD * 2, 1024);
-  g.off_dz = align_up(g.off_lo + BH * s.m * kD * 2, 1024);  // fp32 dz [BH][m]
+  g.off_dz = align_up(g.off_lo + BH * s.m * kD * 2, 1024);                // fp32 dz [BH][m]
   g.bytes = align_up(g.off_dz + BH * s.m * 4, 1024);
   return g;
 }
@@ -1220,41 +1347,43 @@ cudaError_t launch_grad(const void* Q, const void* K, const void* V, const void*
   if (!make_map(&mq, Q, s) || !make_map(&mdo, dO, s) || !make_map(&mdq, dQ, s) || !make_map(&mk, K, s) ||
       !make_map(&mv, V, s) || !make_map(&mdk, dK, s) || !make_map(&mdv, dV, s))
     return cudaErrorInvalidValue;
+  uint8_t* hi = reinterpret_cast<uint8_t*>(ws + g.off_hi);
+  uint8_t* lo = reinterpret_cast<uint8_t*>(ws + g.off_lo);
+  float* dz = reinterpret_cast<float*>(ws + g.off_dz);
+  float* part = reinterpret_cast<float*>(ws + g.off_part);
   GradParams a{};
   a.key_ref = reinterpret_cast<const float*>(ws);
   a.omega = omega;
   a.omega_img = reinterpret_cast<const uint8_t*>(ws + g.fwd.off_omega_img);
   a.state_img = reinterpret_cast<const uint8_t*>(ws + g.fwd.off_state_img);
   a.zvec = reinterpret_cast<const float*>(ws + g.off_z);
-  a.partS = reinterpret_cast<float*>(ws + g.fwd.off_partS);
-  a.counters = reinterpret_cast<uint32_t*>(ws + g.fwd.off_counters);
-  a.out_hi = reinterpret_cast<uint8_t*>(ws + g.off_hi);
-  a.out_lo = reinterpret_cast<uint8_t*>(ws + g.off_lo);
-  a.out_dz = reinterpret_cast<float*>(ws + g.off_dz);
+  a.partS = part;
   a.status = status;
   a.L = s.L;
   a.m = s.m;
-  a.tiles_per_cta = g.fwd.tiles_per_split;
-  a.n_split = g.fwd.n_split;
+  a.n_heads = s.BH();
+  a.parts = g.parts;
   a.scale = scale;
   GradParams b{};
   b.key_ref = a.key_ref;
   b.omega = omega;
   b.omega_img = a.omega_img;
-  b.zvec = a.out_dz;
-  b.ds_hi = a.out_hi;
-  b.ds_lo = a.out_lo;
+  b.zvec = dz;
+  b.ds_hi = hi;
+  b.ds_lo = lo;
   b.status = status;
   b.L = s.L;
   b.m = s.m;
-  b.tiles_per_cta = g.fwd.out_tiles_per_cta;
+  b.n_heads = s.BH();
   b.scale = scale;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(grad_query_kernel<M, FM>), GqCfg::kSmem);
   if (e == cudaSuccess)
     e = ensure_dynamic_smem(reinterpret_cast<const void*>(grad_key_kernel<M, FM>), GkCfg::kSmem);
   if (e != cudaSuccess) return e;
-  grad_query_kernel<M, FM><<<dim3(g.fwd.n_split, s.BH()), kBwdThreads, GqCfg::kSmem, stream>>>(mq, mdo, mdq, a);
-  grad_key_kernel<M, FM><<<dim3(g.fwd.out_ctas, s.BH()), kBwdThreads, GkCfg::kSmem, stream>>>(mk, mv, mdk, mdv, b);
+  grad_query_kernel<M, FM><<<g.ctas, kBwdThreads, GqCfg::kSmem, stream>>>(mq, mdo, mdq, a);
+  grad_merge_kernel<M><<<dim3(s.BH(), kMergeSplit), 128, 0, stream>>>(part, g.parts, (s.L + kBM - 1) / kBM, s.BH(),
+                                                                      g.ctas, hi, lo, dz);
+  grad_key_kernel<M, FM><<<g.ctas, kBwdThreads, GkCfg::kSmem, stream>>>(mk, mv, mdk, mdv, b);
   return cudaGetLastError();
 }
 
@@ -1275,7 +1404,7 @@ cudaError_t tc_bwd_bidir(const void* Q, const void* K, const void* V, const void
                          const float* omega, float scale, const Shape& s, void* ws, int32_t* status,
                          cudaStream_t stream, int fm) {
   char* w = static_cast<char*>(ws);
-  // prep (key reference, fp16 Omega image, zeroed merge counters) and the
+  // prep (key reference, fp16 Omega image) and the
   // forward's state: the bf16 image of [S | z] and z in fp32
   cudaError_t e = tc_state(false, K, V, omega, scale, s, ws, status, stream, fm,
                            reinterpret_cast<float*>(w + grad_layout(s).off_z));

@@ -121,8 +121,10 @@ def _bwd_case(cuda_lib, B, H, L, m, features, seed, q_scale=1.0, k_scale=1.0):
 @pytest.mark.parametrize("features", ["prf", "relu", "elu1"])
 @pytest.mark.parametrize("B,H,L,m", [(1, 2, 128, 256),     # one tile
                                      (1, 3, 777, 128),     # ragged last tile
-                                     (3, 5, 2500, 128),    # several token splits per head
-                                     (2, 3, 3000, 256)])
+                                     (3, 5, 2500, 128),    # several CTAs per head
+                                     (2, 3, 3000, 256),
+                                     (5, 10, 500, 256),    # CTAs that cross from one head into the next
+                                     (1, 1, 20000, 128)])  # one head over every CTA of the grid
 def test_tc_backward_matches_oracle(cuda_lib, features, B, H, L, m):
     Q, K, V, dO, om = _bwd_case(cuda_lib, B, H, L, m, features, seed=L + m)
     s = 64 ** -0.25
