@@ -53,7 +53,9 @@ struct TcPlan {
   int n_fb, n_tiles;
   int tiles_per_split, n_split;      // state partials (bidir: L splits; causal: sub-splits of all
                                      // superchunks but the last)
-  int out_tiles_per_cta, out_ctas;   // output kernel (bidir) / superchunks (causal)
+  int out_tiles_per_cta, out_ctas;   // causal: tiles per superchunk, superchunks
+  int out_grid;                      // bidir output kernel: one CTA per SM (or tile), each an even
+                                     // share of the (head, tile) list
   int sub_per_sc;                    // causal: state sub-splits per superchunk
   size_t off_omega_img, off_counters, off_partS, off_state_img, off_pre, bytes;
 };
@@ -69,9 +71,7 @@ TcPlan tc_plan(bool causal, const Shape& s) {
     const int sp = pick_split(BH, p.n_tiles, sms);
     p.tiles_per_split = (p.n_tiles + sp - 1) / sp;
     p.n_split = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
-    const int oc = pick_split(BH, p.n_tiles, sms);
-    p.out_tiles_per_cta = (p.n_tiles + oc - 1) / oc;
-    p.out_ctas = (p.n_tiles + p.out_tiles_per_cta - 1) / p.out_tiles_per_cta;
+    p.out_grid = (int)std::min<long long>(sms, (long long)BH * p.n_tiles);
   } else {
     const int sc = pick_split(BH, p.n_tiles, sms);
     p.out_tiles_per_cta = (p.n_tiles + sc - 1) / sc;                          // tiles per superchunk
@@ -438,8 +438,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
   // into the bf16 state image read by the output kernel
   if (prm.merge && *is_last) {
     __threadfence();
-    merge_partials<D, M>(prm.partS + (size_t)bh * NFB * prm.n_split * (D + 1) * kFB, prm.n_split,
-                         prm.state_img + (size_t)bh * M * (D + 16) * 2, kStateThreads,
+    merge_partials<D, M>(prm.partS + (size_t)bh * NFB * prm.n_split * (D + 1) * kFB, prm.n_split, prm.n_split,
+                         prm.state_img + (size_t)bh * M * (D + 16) * 2, threadIdx.x, kStateThreads,
                          prm.zvec != nullptr ? prm.zvec + (size_t)bh * M : nullptr);
     if (threadIdx.x == 0) prm.counters[bh] = 0;
   }
@@ -460,7 +460,8 @@ struct OutParams {
   const uint8_t* omega_img;
   const uint8_t* state_img;
   int32_t* status;
-  int L, m, tiles_per_cta;
+  int L, m;
+  int n_heads;             // B H: the CTAs split the (head, tile) list evenly
   float scale;
 };
 
@@ -500,15 +501,24 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
   uint64_t* o_free = o_full + 2;            // [2]
   uint64_t* setup_bar = o_free + 2;
   uint64_t* done_bar = setup_bar + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  uint64_t* img_full = done_bar + 1;        // phase k: the k-th head's S~ image landed
+  uint64_t* img_free = img_full + 1;        // phase k: the k-th head's last output MMA is complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(img_free + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* xmax = reinterpret_cast<float*>(sm + C::kXmax);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
-  const int n_tiles_total = (prm.L + kBM - 1) / kBM;
-  const int tile0 = blockIdx.x * prm.tiles_per_cta;
-  const int n_tiles = min(prm.tiles_per_cta, n_tiles_total - tile0);
+  // this CTA's tiles: the contiguous range [g0, g1) of the (head, tile) list,
+  // which may cross from one head into the next (the S~ image is reloaded)
+  const int nt = (prm.L + kBM - 1) / kBM;
+  const long long total = (long long)prm.n_heads * nt;
+  const int g0 = range_first(total, blockIdx.x, gridDim.x);
+  const int g1 = range_first(total, blockIdx.x + 1, gridDim.x);
+  const int n_tiles = g1 - g0;
+  const int h0 = g0 / nt;
+  const int n_heads = n_tiles > 0 ? (g1 - 1) / nt - h0 + 1 : 0;
+  auto head_of = [&](int i) { return (g0 + i) / nt; };
+  auto tile_of = [&](int i) { return (g0 + i) - head_of(i) * nt; };
   const WaitCtx wctx{abort_flag, prm.status};
   const uint32_t o_col[2] = {256u, 384u};   // O accumulators (d + 16 columns each); P at 0
 
@@ -528,6 +538,8 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
     }
     mbar_init(setup_bar, 1);
     mbar_init(done_bar, 1);
+    mbar_init(img_full, 1);
+    mbar_init(img_free, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -545,22 +557,39 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
       prefetch_tmap(&mapQ);
       prefetch_tmap(&mapO);
       const uint32_t ob = M * D * 2, sb = M * (D + 16) * 2;
-      mbar_arrive_expect_tx(setup_bar, ob + sb);
+      mbar_arrive_expect_tx(setup_bar, ob);
       bulk_load(sm + C::kOmega, prm.omega_img, ob, setup_bar);
-      bulk_load(sm + C::kState, prm.state_img + (size_t)bh * sb, sb, setup_bar);
-      int last_issue[C::NSQ];
-      for (int i = 0; i < C::NSQ; ++i) last_issue[i] = -1;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int st = i % C::NSQ;
-        if (i >= C::NSQ && !mbar_wait(&q_empty[st], ((i / C::NSQ) - 1) & 1, wctx)) break;
-        mbar_arrive_expect_tx(&q_full[st], C::kTileBytes);
-        uint8_t* qt = sm + C::kQ + st * C::kTileBytes;
+      // head k's S~ image goes in once head k - 1's last output MMA is complete
+      auto load_head = [&](int k) {
+        mbar_arrive_expect_tx(img_full, sb);
+        bulk_load(sm + C::kState, prm.state_img + (size_t)(h0 + k) * sb, sb, img_full);
+      };
+      int ni = 0;
+      if (n_heads > 0) load_head(ni++);
+      Watchdog wd(wctx);
+      int nq = 0;
+      bool ok = true;
+      while (ok && (nq < n_tiles || ni < n_heads)) {
+        bool progress = false;
+        if (nq < n_tiles && (nq < C::NSQ || mbar_test_wait(smem_addr(&q_empty[nq % C::NSQ]), ((nq / C::NSQ) - 1) & 1))) {
+          const int st = nq % C::NSQ;
+          mbar_arrive_expect_tx(&q_full[st], C::kTileBytes);
+          uint8_t* qt = sm + C::kQ + st * C::kTileBytes;
 #pragma unroll
-        for (int a = 0; a < D / 64; ++a) tma_load_3d(qt + a * kAtom, &mapQ, a * 64, (tile0 + i) * kBM, bh, &q_full[st]);
-        last_issue[st] = i;
+          for (int a = 0; a < D / 64; ++a)
+            tma_load_3d(qt + a * kAtom, &mapQ, a * 64, tile_of(nq) * kBM, head_of(nq), &q_full[st]);
+          ++nq;
+          progress = true;
+        }
+        if (ni < n_heads && mbar_test_wait(smem_addr(img_free), (ni - 1) & 1)) {
+          load_head(ni++);
+          progress = true;
+        }
+        if (progress) wd.progress();
+        else ok = wd.idle();
       }
-      for (int st = 0; st < C::NSQ; ++st)
-        if (last_issue[st] >= 0) mbar_wait(&q_full[st], (last_issue[st] / C::NSQ) & 1, wctx);
+      for (int x = max(0, nq - C::NSQ); x < nq; ++x) mbar_wait(&q_full[x % C::NSQ], (x / C::NSQ) & 1, wctx);
+      if (ni > 0) mbar_wait(img_full, (ni - 1) & 1, wctx);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -598,6 +627,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
         if (oi < n_tiles) {
           const int ob = oi & 1;
           const bool ready = mbar_test_wait(smem_addr(&phi_full[of]), oi & 1) &&
+                             mbar_test_wait(smem_addr(img_full), (head_of(oi) - h0) & 1) &&
                              (of > 0 || oi < 2 || mbar_test_wait(smem_addr(&o_free[ob]), ((oi >> 1) - 1) & 1));
           if (ready) {
             tc_fence_after();
@@ -608,7 +638,11 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
               mma_bf16(tmem + o_col[ob], dadd(a0, kstep_k(kk, kAtom)), dadd(b0, kstep_k(kk, (D + 16) * 128)), id_out,
                        (of > 0) || (kk > 0));
             mma_commit(&phi_free[of]);
-            if (of == NFB - 1) mma_commit(&o_full[ob]);
+            if (of == NFB - 1) {
+              mma_commit(&o_full[ob]);
+              // the head's last tile: its S~ image may be replaced
+              if (oi == n_tiles - 1 || head_of(oi + 1) != head_of(oi)) mma_commit(img_free);
+            }
             if (++of == NFB) { of = 0; ++oi; }
             progress = true;
           }
@@ -658,7 +692,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_free[ob]);
       const float den = have ? __uint_as_float(z[0]) : 1.f;
-      const int row = (tile0 + j) * kBM + t;
+      const int row = tile_of(j) * kBM + t;
       if (have && row < prm.L && (!(den > 0.f) || !isfinite(den))) report_status(prm.status, FAVOR_ERR_NONFINITE);
       const float inv = __fdividef(1.0f, den);
       if (threadIdx.x == kEpiTid0 && j > 0) bulk_wait_read0();   // previous store has left the staging tile
@@ -676,7 +710,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const __grid_con
       fence_proxy_async_smem();
       named_bar(1, kEpiThreads);
       if (threadIdx.x == kEpiTid0 && have && !*abort_flag) {
-        tma_store_3d(&mapO, 0, (tile0 + j) * kBM, bh, sm + C::kOut);
+        tma_store_3d(&mapO, 0, tile_of(j) * kBM, head_of(j), sm + C::kOut);
         bulk_commit();
       }
     };
@@ -1356,13 +1390,13 @@ cudaError_t launch_output(const void* Q, void* O, const Shape& s, const TcPlan& 
   prm.status = status;
   prm.L = s.L;
   prm.m = s.m;
-  prm.tiles_per_cta = p.out_tiles_per_cta;
+  prm.n_heads = s.BH();
   prm.scale = scale;
   const size_t smem = OutCfg<D>::kSmem;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(output_kernel<D, M, FM>), smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.out_ctas, s.BH());
-  output_kernel<D, M, FM><<<grid, kOutThreads, smem, stream>>>(mq, mo, prm);
+  // one CTA per SM (or per tile), each an even share of the (head, tile) list
+  output_kernel<D, M, FM><<<p.out_grid, kOutThreads, smem, stream>>>(mq, mo, prm);
   return cudaGetLastError();
 }
 
@@ -1404,10 +1438,6 @@ bool tc_supported(bool causal, int d, int m, bool bf16) {
 TcLayout tc_bidir_layout(const Shape& s) {
   const TcPlan p = tc_plan(false, s);
   TcLayout l{};
-  l.n_split = p.n_split;
-  l.tiles_per_split = p.tiles_per_split;
-  l.out_ctas = p.out_ctas;
-  l.out_tiles_per_cta = p.out_tiles_per_cta;
   l.off_omega_img = p.off_omega_img;
   l.off_counters = p.off_counters;
   l.off_partS = p.off_partS;

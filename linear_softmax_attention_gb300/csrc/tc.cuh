@@ -20,8 +20,6 @@ cudaError_t tc_output(bool causal, const void* Q, const void* K, const void* V, 
 // tensor-core backward (tc_bwd.cu) runs that forward's state stage, keeps its
 // layout and puts the gradient's state image after it.
 struct TcLayout {
-  int n_split, tiles_per_split;       // state kernel: token splits per head
-  int out_ctas, out_tiles_per_cta;    // output kernel: runs of tiles per head
   size_t off_omega_img, off_counters, off_partS, off_state_img, bytes;
 };
 TcLayout tc_bidir_layout(const Shape& s);

@@ -91,15 +91,6 @@ struct GradParams {
   float scale;
 };
 
-// The CTAs of a grid of n_ctas split the list of n_heads * nt (head, tile)
-// pairs evenly: CTA c takes [first(c), first(c + 1)).
-__host__ __device__ __forceinline__ int range_first(long long total, int c, int n_ctas) {
-  return (int)(total * c / n_ctas);
-}
-// the CTA holding list entry x
-__host__ __device__ __forceinline__ int range_cta(long long total, long long x, int n_ctas) {
-  return (int)(((x + 1) * n_ctas + total - 1) / total) - 1;
-}
 
 // power of two that brings a row's largest |g| into [2^14, 2^15) (1 for an
 // all-zero row), and its inverse; both normal floats for every finite max

@@ -6,6 +6,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -42,6 +43,17 @@ inline int pick_split(int units, int tiles, int sms) {
     }
   }
   return best;
+}
+
+// The CTAs of a grid of n_ctas split the list of B H x tiles (head, tile)
+// pairs evenly: CTA c takes entries [range_first(c), range_first(c + 1)),
+// which may cross from one head into the next.
+__host__ __device__ __forceinline__ int range_first(long long total, int c, int n_ctas) {
+  return (int)(total * c / n_ctas);
+}
+// the CTA holding list entry x
+__host__ __device__ __forceinline__ int range_cta(long long total, long long x, int n_ctas) {
+  return (int)(((x + 1) * n_ctas + total - 1) / total) - 1;
 }
 
 // ---------------------------------------------------------------------------
@@ -245,33 +257,32 @@ __device__ __forceinline__ void tmem_state_to_rows(uint32_t tmem, uint32_t g_col
   }
 }
 
-// The fixed-order sum of one head's n_split fp32 partial states
-// ([M/128 blocks][n_split][D + 1][128], feature fastest) as its bf16 state
+// The fixed-order sum of one head's first `count` fp32 partial states
+// ([M/128 blocks][stride][D + 1][128], feature fastest) as its bf16 state
 // image ([M/64 atoms][D + 16 rows][128 B], 128-byte swizzle, the normaliser
-// in row D, rows past it zero), by all `nthreads` threads of the CTA with
-// eight items' loads in flight per split.  Item = (block b, state row n, 4
-// consecutive features).
-// With `zvec` non-null, the normaliser row (n = D) also goes to zvec[0, M)
-// in fp32.
+// in row D, rows past it zero), by `nthreads` threads (this one is number
+// `tid`) with eight items' loads in flight per partial.  Item = (block b,
+// state row n, 4 consecutive features).  With `zvec` non-null, the
+// normaliser row (n = D) also goes to zvec[0, M) in fp32.
 template <int D, int M>
-__device__ void merge_partials(const float* __restrict__ base, int n_split, uint8_t* __restrict__ img,
-                               int nthreads, float* __restrict__ zvec = nullptr) {
+__device__ void merge_partials(const float* __restrict__ base, int stride, int count, uint8_t* __restrict__ img,
+                               int tid, int nthreads, float* __restrict__ zvec = nullptr) {
   constexpr int NFB = M / kFB;
   constexpr int NG = kFB / 4;
   constexpr int kItems = NFB * (D + 16) * NG;
   constexpr int kBatch = 8;
-  for (int e0 = threadIdx.x; e0 < kItems; e0 += kBatch * nthreads) {
+  for (int e0 = tid; e0 < kItems; e0 += kBatch * nthreads) {
     float4 acc[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int p = 0; p < n_split; ++p) {
+    for (int p = 0; p < count; ++p) {
       float4 v[kBatch];
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
         const int e = e0 + u * nthreads;
         const int g = e % NG, n = (e / NG) % (D + 16), b = e / (NG * (D + 16));
         v[u] = (e < kItems && n <= D)
-                   ? *reinterpret_cast<const float4*>(base + (((size_t)b * n_split + p) * (D + 1) + n) * kFB + g * 4)
+                   ? *reinterpret_cast<const float4*>(base + (((size_t)b * stride + p) * (D + 1) + n) * kFB + g * 4)
                    : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
