@@ -419,7 +419,8 @@ struct FsOutParams {
   const uint8_t* state_img;
   __nv_bfloat16* O;
   int32_t* status;
-  int L, m, tiles_per_run;
+  int L, m;
+  int n_heads;             // B H: the clusters split the (head, tile) list evenly
   float scale;
 };
 
@@ -460,16 +461,26 @@ __global__ void __launch_bounds__(kThreads, 1) fs_output_kernel(const __grid_con
   uint64_t* land_free = land_full + 2;      // [tile parity][4] owner r has read my partial of that parity
   uint64_t* setup_bar = land_free + 8;
   uint64_t* done_bar = setup_bar + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  uint64_t* img_full = done_bar + 1;        // phase k: the k-th head's state block landed
+  uint64_t* img_free = img_full + 1;        // phase k: the k-th head's last output MMA is complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(img_free + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* xmax = reinterpret_cast<float*>(sm + C::kXmax);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = NC > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int run = blockIdx.x / NC, bh = blockIdx.y;
-  const int n_tiles_total = (prm.L + kBM - 1) / kBM;
-  const int tile0 = run * prm.tiles_per_run;
-  const int n_tiles = min(prm.tiles_per_run, n_tiles_total - tile0);
+  // this cluster's tiles: the contiguous range [g0, g1) of the (head, tile)
+  // list, which may cross from one head into the next (each CTA reloads its
+  // block of the state)
+  const int nt = (prm.L + kBM - 1) / kBM;
+  const long long total = (long long)prm.n_heads * nt;
+  const int n_cl = (int)gridDim.x / NC, cl = (int)blockIdx.x / NC;
+  const int g0 = range_first(total, cl, n_cl);
+  const int n_tiles = range_first(total, cl + 1, n_cl) - g0;
+  const int h0 = g0 / nt;
+  const int n_heads = n_tiles > 0 ? (g0 + n_tiles - 1) / nt - h0 + 1 : 0;
+  auto head_of = [&](int i) { return (g0 + i) / nt; };
+  auto tile_of = [&](int i) { return (g0 + i) - head_of(i) * nt; };
   const WaitCtx wctx{abort_flag, prm.status};
   constexpr uint32_t O_COL = 256;            // output accumulator; projections at columns 0 and 128
   auto qstage = [&](int st) { return sm + C::kQ + st * kTile; };
@@ -492,6 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1) fs_output_kernel(const __grid_con
     for (int i = 0; i < 8; ++i) mbar_init(&land_free[i], 4);   // owner i % 4's finalising warps
     mbar_init(setup_bar, 1);
     mbar_init(done_bar, 1);
+    mbar_init(img_full, 1);
+    mbar_init(img_free, 1);
     *abort_flag = 0;
     fence_barrier_init();
     if (NC > 1)
@@ -511,22 +524,40 @@ __global__ void __launch_bounds__(kThreads, 1) fs_output_kernel(const __grid_con
     if (lane == 0) {
       prefetch_tmap(&mapQ);
       constexpr uint32_t sb = 2 * kGN * 128;
-      mbar_arrive_expect_tx(setup_bar, 2 * kAtom + sb);
+      mbar_arrive_expect_tx(setup_bar, 2 * kAtom);
       for (int a = 0; a < 2; ++a)
         bulk_load(sm + C::kOmega + a * kAtom, prm.omega_img + ((size_t)a * prm.m + rank * kFB) * 128, kAtom,
                   setup_bar);
-      bulk_load(sm + C::kState, prm.state_img + ((size_t)bh * (prm.m / 64) + 2 * rank) * kGN * 128, sb, setup_bar);
-      int last_issue[2] = {-1, -1};
-      for (int i = 0; i < n_tiles; ++i) {
-        const int st = i & 1;
-        if (i >= 2 && !mbar_wait(&q_empty[st], ((i >> 1) - 1) & 1, wctx)) break;
-        mbar_arrive_expect_tx(&q_full[st], kTile);
-        for (int a = 0; a < 2; ++a)
-          tma_load_3d(qstage(st) + a * kAtom, &mapQ, a * 64, (tile0 + i) * kBM, bh, &q_full[st]);
-        last_issue[st] = i;
+      // head k's block of the state goes in once head k - 1's last output MMA is complete
+      auto load_head = [&](int k) {
+        mbar_arrive_expect_tx(img_full, sb);
+        bulk_load(sm + C::kState, prm.state_img + ((size_t)(h0 + k) * (prm.m / 64) + 2 * rank) * kGN * 128, sb,
+                  img_full);
+      };
+      int ni = 0;
+      if (n_heads > 0) load_head(ni++);
+      Watchdog wd(wctx);
+      int nq = 0;
+      bool ok = true;
+      while (ok && (nq < n_tiles || ni < n_heads)) {
+        bool progress = false;
+        if (nq < n_tiles && (nq < 2 || mbar_test_wait(smem_addr(&q_empty[nq & 1]), ((nq >> 1) - 1) & 1))) {
+          const int st = nq & 1;
+          mbar_arrive_expect_tx(&q_full[st], kTile);
+          for (int a = 0; a < 2; ++a)
+            tma_load_3d(qstage(st) + a * kAtom, &mapQ, a * 64, tile_of(nq) * kBM, head_of(nq), &q_full[st]);
+          ++nq;
+          progress = true;
+        }
+        if (ni < n_heads && mbar_test_wait(smem_addr(img_free), (ni - 1) & 1)) {
+          load_head(ni++);
+          progress = true;
+        }
+        if (progress) wd.progress();
+        else ok = wd.idle();
       }
-      for (int st = 0; st < 2; ++st)
-        if (last_issue[st] >= 0) mbar_wait(&q_full[st], (last_issue[st] >> 1) & 1, wctx);
+      for (int x = max(0, nq - 2); x < nq; ++x) mbar_wait(&q_full[x & 1], (x >> 1) & 1, wctx);
+      if (ni > 0) mbar_wait(img_full, (ni - 1) & 1, wctx);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -558,7 +589,8 @@ __global__ void __launch_bounds__(kThreads, 1) fs_output_kernel(const __grid_con
         }
         if (oi < pi) {
           const int st = oi & 1;
-          if (ready(&phi_full[st], oi >> 1) && (oi == 0 || ready(o_free, oi - 1))) {
+          if (ready(&phi_full[st], oi >> 1) && ready(img_full, head_of(oi) - h0) &&
+              (oi == 0 || ready(o_free, oi - 1))) {
             tc_fence_after();
             const uint64_t a0 = sdesc(smem_addr(qstage(st)), 16, 1024);
             const uint64_t b0 = sdesc(state_a, 16, 1024);
@@ -567,6 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1) fs_output_kernel(const __grid_con
               mma_bf16(tmem + O_COL, dadd(a0, kstep_k(k, kAtom)), dadd(b0, kstep_k(k, kGN * 128)), id_out, k > 0);
             mma_commit(o_full);
             mma_commit(&q_empty[st]);
+            // the head's last tile: its state block may be replaced
+            if (oi == n_tiles - 1 || head_of(oi + 1) != head_of(oi)) mma_commit(img_free);
             ++oi;
             progress = true;
           }
@@ -649,9 +683,9 @@ __global__ void __launch_bounds__(kThreads, 1) fs_output_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free);
       const float den_own = __uint_as_float(z[0]);
-      const int row = (tile0 + j) * kBM + t;
+      const int row = tile_of(j) * kBM + t;
       const bool valid = row < prm.L;
-      __nv_bfloat16* orow = prm.O + ((size_t)bh * prm.L + (valid ? row : 0)) * kD;
+      __nv_bfloat16* orow = prm.O + ((size_t)head_of(j) * prm.L + (valid ? row : 0)) * kD;
       if constexpr (NC == 1) {
         if (have && valid) {
           if (!(den_own > 0.f) || !isfinite(den_own)) report_status(prm.status, FAVOR_ERR_NONFINITE);
@@ -1387,7 +1421,9 @@ cudaError_t launch_fs_output(const void* Q, void* O, const Shape& s, const FsPla
   const size_t smem = FsOutCfg<NC>::kSmem;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(fs_output_kernel<NC, FM>), smem);
   if (e != cudaSuccess) return e;
-  const int runs = pick_split(s.BH(), p.n_tiles, resident_clusters<NC, FM>(smem));
+  // as many clusters as can be resident (or one per tile), each an even share
+  // of the (head, tile) list
+  const int n_cl = (int)std::min<long long>(resident_clusters<NC, FM>(smem), (long long)s.BH() * p.n_tiles);
   FsOutParams prm{};
   prm.omega_img = reinterpret_cast<const uint8_t*>(ws + p.off_omega_img);
   prm.state_img = reinterpret_cast<const uint8_t*>(ws + p.off_state_img);
@@ -1395,11 +1431,10 @@ cudaError_t launch_fs_output(const void* Q, void* O, const Shape& s, const FsPla
   prm.status = status;
   prm.L = s.L;
   prm.m = s.m;
-  prm.tiles_per_run = (p.n_tiles + runs - 1) / runs;
+  prm.n_heads = s.BH();
   prm.scale = scale;
-  const int n_runs = (p.n_tiles + prm.tiles_per_run - 1) / prm.tiles_per_run;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(n_runs * NC, s.BH(), 1);
+  cfg.gridDim = dim3(n_cl * NC, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
