@@ -11,9 +11,9 @@
 // the normaliser sums); its key features
 // use the reference R = max_i |w_i|^2 / 2 - 40 of the sequence kernels, so a
 // state from favor_decode_prefill continues here.  The query features use
-// s |q| max_i |w_i| - 20 (the largest possible exponent less 20): a per-query
-// constant, it cancels in the ratio ("From Performer to Linear Attention",
-// §Simple Derivation).
+// the query's largest exponent max_i s w_i.q, so the largest is exactly 1 at
+// any norm of q: a per-query constant, it cancels in the ratio ("From
+// Performer to Linear Attention", §Simple Derivation).
 //
 // One CTA per head.  Bound by the state's HBM traffic: m (d+1) fp32 read and
 // written per head and token (133 KB at m = 256, d = 64); Omega (m x d fp32)
@@ -27,7 +27,6 @@ namespace {
 
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
-constexpr float kDecQueryHeadroom = 20.0f;
 constexpr int kCB = 16;                              // state columns per block of loads
 
 // NF features per thread: 1 for m <= 256, 2 for m <= 512
@@ -41,8 +40,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_step_kernel(const T* __
   __shared__ float phq[kMaxM], phk[kMaxM];
   __shared__ float part[kDecWarps][kMaxD + 1];
   __shared__ float num[kMaxD + 1];
-  __shared__ float wred[kDecWarps];
-  __shared__ float sqn[2];
+  __shared__ float wred[kDecWarps], qred[kDecWarps];
+  __shared__ float sqn[1];
   const int bh = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ld = d + 1;
@@ -55,12 +54,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_step_kernel(const T* __
   }
   if (tid == 0) vs[d] = 1.f;
   __syncthreads();
-  if (warp < 2) {
-    const float* x = warp == 0 ? qs : ks;
+  if (warp == 0) {
+    // |k|^2 for the key features' exponent
     float a = 0.f;
-    for (int j = lane; j < d; j += 32) a = fmaf(x[j], x[j], a);
+    for (int j = lane; j < d; j += 32) a = fmaf(ks[j], ks[j], a);
     a = warp_sum(a);
-    if (lane == 0) sqn[warp] = a;
+    if (lane == 0) sqn[0] = a;
   }
 
   // the first super-block of state columns is loaded before the
@@ -85,7 +84,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_step_kernel(const T* __
 
   // w_f.q, w_f.k and |w_f|^2 for the features f = tid + 256 i of this thread
   float pq[NF], pk[NF];
-  float w2max = 0.f;
+  float w2max = 0.f, pqmax = -INFINITY;
 #pragma unroll
   for (int i = 0; i < NF; ++i) {
     const int f = tid + i * kDecThreads;
@@ -120,18 +119,26 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_step_kernel(const T* __
         }
       }
       w2max = fmaxf(w2max, w2);
+      pqmax = fmaxf(pqmax, dq);
     }
     pq[i] = dq;
     pk[i] = dk;
   }
   w2max = warp_max(w2max);
-  if (lane == 0) wred[warp] = w2max;
+  pqmax = warp_max(pqmax);
+  if (lane == 0) {
+    wred[warp] = w2max;
+    qred[warp] = pqmax;
+  }
   __syncthreads();
-  float w2 = wred[0];
-  for (int i = 1; i < kDecWarps; ++i) w2 = fmaxf(w2, wred[i]);
+  float w2 = wred[0], qmax = qred[0];
+  for (int i = 1; i < kDecWarps; ++i) {
+    w2 = fmaxf(w2, wred[i]);
+    qmax = fmaxf(qmax, qred[i]);
+  }
   const float R = 0.5f * w2 - kKeyHeadroom;
-  const float bq = scale * sqrtf(w2) * sqrtf(sqn[0]) - kDecQueryHeadroom;
-  const float hk = 0.5f * scale * scale * sqn[1];
+  const float bq = scale * qmax;
+  const float hk = 0.5f * scale * scale * sqn[0];
 #pragma unroll
   for (int i = 0; i < NF; ++i) {
     const int f = tid + i * kDecThreads;

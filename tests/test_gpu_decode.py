@@ -50,6 +50,26 @@ def test_decode_steps_match_causal_rows(cuda_lib, dtype, d, m):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("q_scale", [4.0, 8.0])
+def test_decode_large_norm_queries(cuda_lib, dtype, q_scale):
+    # the query reference is the query's own largest exponent, so phi(q)
+    # never underflows as a whole however large q is
+    B, H, L, d, m = 2, 2, 20, 64, 256
+    Q, K, V = _inputs(B, H, L, d, dtype, seed=7)
+    Q = (Q.float() * q_scale).to(dtype)
+    om = cuda_lib.new_omega(9, m, d)
+    s = d ** -0.25
+    state = cuda_lib.new_decode_state(B, H, m, d)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _decode_all(cuda_lib, Q, K, V, om, s, state, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.isfinite(got.float()).all()
+    ref = orc.favor_causal_quadratic(to_np(Q), to_np(K), to_np(V), to_np(om), s)
+    assert orc.rowwise_rel_err(to_np(got), ref) < TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("B,H,d,m", [(40, 16, 64, 256), (37, 7, 48, 96), (5, 3, 64, 256), (40, 16, 64, 100)])
 def test_decode_many_heads(cuda_lib, dtype, B, H, d, m):
     # more heads than SMs (several heads per CTA, both shared-memory buffers
