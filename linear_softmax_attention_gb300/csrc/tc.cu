@@ -446,7 +446,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
 }
 
 // ---------------------------------------------------------------------------
-// bidirectional output kernel: CTA = a run of 128-token tiles of one head.
+// bidirectional output kernel: one CTA per SM, each an even share of the
+// (head, tile) list (a share may cross into the next head: the S~ image is
+// reloaded).
 // Query row reference: the row's largest exponent max_i s w_i.q, read from
 // the projection tile in tensor memory before any feature is formed ("From
 // Performer to Linear Attention", §Simple Derivation: any per-query constant

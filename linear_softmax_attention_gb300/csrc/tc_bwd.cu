@@ -31,15 +31,17 @@
 // kernel as a pair of bf16 images (hi + lo) and dz in fp32.
 //
 // Two kernels after the forward's state stage (prep, state kernel: S, z as a
-// bf16 image and z in fp32):
-//   query kernel  CTA = a token split of one head (the state kernel's splits)
+// bf16 image and z in fp32), each on one CTA per SM taking an even share of
+// the (head, tile) list (a share may cross from one head into the next):
+//   query kernel
 //     P = Q Omega^T                    M = 128 tokens,   N = m,      K = d   fp16
 //     N = phi(Q) S                     M = 128 tokens,   N = d,      K = m
 //     [dS | dz] += Psi^T [dO | -delta] M = 128 features, N = d + 16, K = 128 tokens
 //     T = dO S^T                       M = 128 tokens,   N = m,      K = d
 //     dQ = s G Omega                   M = 128 tokens,   N = d,      K = m   fp16
-//     the last CTA of a head adds the splits' partials into the dS pair and dz
-//   key kernel    CTA = a run of tiles of one head
+//     each head's [dS | dz] part goes to the slot of the CTA's place among the
+//     head's CTAs; a merge kernel adds the slots in order into the dS pair and dz
+//   key kernel
 //     P = K Omega^T,  dV = phi(K) dS_hi,  T = V (dS_hi + dS_lo)^T,  dK = s G Omega
 // G = g rounded to bf16, then scaled per row by a power of two that puts
 // its largest entry in [2^14, 2^15), in fp16 (the operand type of the fp16

@@ -15,8 +15,9 @@
 //                 in a ones block stored right after each V tile).  The last
 //                 CTA of (head, block) adds the splits in order into the bf16
 //                 state image.
-//   output kernel a thread-block cluster of m / 128 CTAs per run of tiles of
-//                 one head, CTA r holding block r of Omega and of the state.
+//   output kernel thread-block clusters of m / 128 CTAs, as many as can be
+//                 resident, each an even share of the (head, tile) list; CTA
+//                 r holds block r of Omega and of the head's state.
 //                 Each computes phi(Q)_r with its own exact row maximum c_r
 //                 and the partial output O_r = phi(Q)_r S~_r (numerator and
 //                 normaliser).  The partials meet in distributed shared
@@ -410,9 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1) fs_state_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------------------
-// output kernel: a cluster of NC CTAs (NC = m / 128) per run of tiles of one
-// head; CTA rank r owns feature block r and finalises output columns
-// [r W, (r + 1) W), W = d / NC.
+// output kernel: clusters of NC CTAs (NC = m / 128), each an even share of the
+// (head, tile) list; CTA rank r owns feature block r and finalises output
+// columns [r W, (r + 1) W), W = d / NC.
 // ---------------------------------------------------------------------------
 struct FsOutParams {
   const uint8_t* omega_img;
