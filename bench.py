@@ -207,6 +207,7 @@ class ClockSampler:
 # a committed profile's counters stay valid while their code (comments and
 # layout aside) does not change.
 KERNEL_SOURCES = ("linear_softmax_attention_gb300/csrc/tc.cu", "linear_softmax_attention_gb300/csrc/tc_fs.cu",
+                  "linear_softmax_attention_gb300/csrc/tc_bwd.cu",
                   "linear_softmax_attention_gb300/csrc/tc_util.cuh", "linear_softmax_attention_gb300/csrc/tc_ptx.cuh",
                   "linear_softmax_attention_gb300/csrc/common.cuh", "linear_softmax_attention_gb300/csrc/prep.cu",
                   "include/favor.h")
