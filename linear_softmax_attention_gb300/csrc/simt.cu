@@ -735,7 +735,24 @@ __device__ __forceinline__ float bwd_feature(float p, float c) {
 }
 
 
-// features of the tile rows xs against all m rows of Omega into P [TT][ldp]
+// Performer-ReLU's slope [w.x > 0] jumps at w.x = 0, so the backward takes
+// that sign from the exact projection wherever the fp32 one is within its
+// rounding bound: |fl(w.x) - w.x| <= d 2^-24 sum_c |w_c x_c| <= d 2^-24 |x| W
+// (W = max_i |w_i|), with a factor 2 of margin.  The threshold per row is
+// carried in the row constant, which the ReLU features do not use.
+__device__ __forceinline__ float relu_sign_bound(float x_norm2, int d, float W) {
+  return 2.0f * static_cast<float>(d) * 5.9604645e-8f * sqrtf(x_norm2) * W;
+}
+
+// w.x in fp64 (the products of two fp32 numbers are exact in fp64)
+__device__ __forceinline__ float exact_dot(const float* x, const float* w, int d) {
+  double a = 0.0;
+  for (int c = 0; c < d; ++c) a = fma(static_cast<double>(x[c]), static_cast<double>(w[c]), a);
+  return static_cast<float>(a);
+}
+
+// features of the tile rows xs against all m rows of Omega into P [TT][ldp];
+// for Performer-ReLU rowc[t] is the sign bound of row t (relu_sign_bound)
 template <int TT, int FM>
 __device__ void tile_features(const float* xs, const float* rowc, int nt, int d, int m, float scale,
                               const float* __restrict__ omega, float* om, float* P, int ldp) {
@@ -755,7 +772,11 @@ __device__ void tile_features(const float* xs, const float* rowc, int nt, int d,
 #pragma unroll
       for (int k = 0; k < RT::kCols; ++k) {
         const int f = RT::col(k);
-        if (f < nf) P[t * ldp + f0 + f] = t < nt ? bwd_feature<FM>(scale * acc[i][k], rowc[t]) : 0.f;
+        float a = acc[i][k];
+        if constexpr (FM == FAVOR_FM_RELU) {
+          if (t < nt && f < nf && fabsf(a) <= rowc[t]) a = exact_dot(xs + t * ld, om + f * ld, d);
+        }
+        if (f < nf) P[t * ldp + f0 + f] = t < nt ? bwd_feature<FM>(scale * a, rowc[t]) : 0.f;
       }
     }
   }
@@ -845,7 +866,9 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_query_kernel(
   float R, W;
   key_reference(key_ref, m, &R, &W);
   if (threadIdx.x < kBT)
-    rs[threadIdx.x] = FM == FAVOR_FM_PRF ? scale * sqrtf(rs[threadIdx.x]) * W - 20.0f : 0.f;
+    rs[threadIdx.x] = FM == FAVOR_FM_PRF    ? scale * sqrtf(rs[threadIdx.x]) * W - 20.0f
+                      : FM == FAVOR_FM_RELU ? relu_sign_bound(rs[threadIdx.x], d, W)
+                                            : 0.f;
   tile_features<kBT, FM>(xs, rs, nt, d, m, scale, omega, om, P, ldp);
 
   // N | D
@@ -998,7 +1021,9 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_key_kernel(
   float R, W;
   key_reference(key_ref, m, &R, &W);
   if (threadIdx.x < kBT)
-    rs[threadIdx.x] = FM == FAVOR_FM_PRF ? 0.5f * scale * scale * rs[threadIdx.x] + R : 0.f;
+    rs[threadIdx.x] = FM == FAVOR_FM_PRF    ? 0.5f * scale * scale * rs[threadIdx.x] + R
+                      : FM == FAVOR_FM_RELU ? relu_sign_bound(rs[threadIdx.x], d, W)
+                                            : 0.f;
   tile_features<kBT, FM>(xs, rs, nt, d, m, scale, omega, om, P, ldp);
 
   using RT = RegTile<kBT>;
@@ -1128,8 +1153,12 @@ __global__ void __launch_bounds__(kThreads) cbwd_query_kernel(
     tile_norms<kCT>(ks, d, rk);
     __syncthreads();
     if (threadIdx.x < kCT) {
-      rq[threadIdx.x] = FM == FAVOR_FM_PRF ? scale * sqrtf(rq[threadIdx.x]) * W - 20.0f : 0.f;
-      rk[threadIdx.x] = FM == FAVOR_FM_PRF ? 0.5f * scale * scale * rk[threadIdx.x] + R : 0.f;
+      rq[threadIdx.x] = FM == FAVOR_FM_PRF    ? scale * sqrtf(rq[threadIdx.x]) * W - 20.0f
+                        : FM == FAVOR_FM_RELU ? relu_sign_bound(rq[threadIdx.x], d, W)
+                                              : 0.f;
+      rk[threadIdx.x] = FM == FAVOR_FM_PRF    ? 0.5f * scale * scale * rk[threadIdx.x] + R
+                        : FM == FAVOR_FM_RELU ? relu_sign_bound(rk[threadIdx.x], d, W)
+                                              : 0.f;
     }
     tile_features<kCT, FM>(xs, rq, nt, d, m, scale, omega, om, P, ldp);
     tile_features<kCT, FM>(ks, rk, nt, d, m, scale, omega, om, Pk, ldp);
@@ -1263,8 +1292,12 @@ __global__ void __launch_bounds__(kThreads) cbwd_key_kernel(
     tile_norms<kCT>(ks, d, rk);
     __syncthreads();
     if (threadIdx.x < kCT) {
-      rq[threadIdx.x] = FM == FAVOR_FM_PRF ? scale * sqrtf(rq[threadIdx.x]) * W - 20.0f : 0.f;
-      rk[threadIdx.x] = FM == FAVOR_FM_PRF ? 0.5f * scale * scale * rk[threadIdx.x] + R : 0.f;
+      rq[threadIdx.x] = FM == FAVOR_FM_PRF    ? scale * sqrtf(rq[threadIdx.x]) * W - 20.0f
+                        : FM == FAVOR_FM_RELU ? relu_sign_bound(rq[threadIdx.x], d, W)
+                                              : 0.f;
+      rk[threadIdx.x] = FM == FAVOR_FM_PRF    ? 0.5f * scale * scale * rk[threadIdx.x] + R
+                        : FM == FAVOR_FM_RELU ? relu_sign_bound(rk[threadIdx.x], d, W)
+                                              : 0.f;
     }
     tile_features<kCT, FM>(xs, rq, nt, d, m, scale, omega, om, P, ldp);
     tile_features<kCT, FM>(ks, rk, nt, d, m, scale, omega, om, Pk, ldp);
