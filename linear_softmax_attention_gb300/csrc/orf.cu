@@ -30,6 +30,25 @@ __device__ __forceinline__ float normal_from_word(uint64_t w) {
 }
 
 constexpr int kTPR = 4;                 // threads per row of a block
+constexpr int kPanel = 32 / kTPR;       // rows per warp: one panel
+constexpr int kPartPad = 4;             // floats after each part of a stored row
+
+// Layout of one block's rows in shared memory.  Row r, part p (its columns
+// p*CW .. p*CW+CW-1) starts at r*RW + p*PS: with PS = CW + 4 the four parts
+// of a row fall in different banks, so the warp-wide reads of one row (four
+// distinct addresses) take one pass.  With CW <= 16 the rows being
+// subtracted are held in registers between their dot products and their
+// updates, and a second group of warps (helpers, one thread per Gram–Schmidt
+// thread) draws the length vectors and takes half of the
+// re-orthogonalisation; at CW = 32 (d > 64) the registers of 512 threads
+// allow neither, and the rows are read twice instead.
+template <int CW>
+struct OrfLayout {
+  static constexpr int PS = CW + kPartPad;
+  static constexpr int RW = kTPR * PS;
+  static constexpr bool kHeld = CW <= 16;
+  static constexpr int kMaxThreads = (kHeld ? 2 : 1) * kTPR * kTPR * CW;
+};
 
 __device__ __forceinline__ float group4_sum(float v) {
   v += __shfl_xor_sync(0xffffffffu, v, 1);
@@ -37,131 +56,301 @@ __device__ __forceinline__ float group4_sum(float v) {
   return v;
 }
 
-// One CTA per d x d block; thread (row r = tid/4, part p = tid%4) keeps
-// columns p*CW .. p*CW+CW-1 of row r in registers (CW = ceil(d/4) rounded up
-// to a multiple of 4; columns >= d are zero).
-//
-// Sweep 1 is modified Gram–Schmidt, row by row.  fp32 leaves the rows
-// orthogonal only to about kappa * 2^-24, so a second pass re-orthogonalises
-// them; as the rows are then orthonormal up to that small error E, the pass
-// is one classical step q_r - sum_{s<r} (q_s . q_r) q_s computed for all rows
-// at once, which equals a second modified sweep up to O(E^2).  Finally row r
-// is scaled by the length of its own Gaussian vector.
+// Partial dot product of this thread's CW columns with the same columns of a
+// row in shared memory (four accumulators).
 template <int CW>
-__global__ void __launch_bounds__(kMaxD * kTPR) orf_block_kernel(uint64_t seed, int m, int d,
-                                                                 float* __restrict__ omega) {
-  extern __shared__ __align__(16) float orf_smem[];
-  float* qbuf = orf_smem;                         // [2][kTPR * CW] unit row of the current step
-  float* rows = orf_smem + 2 * kTPR * CW;         // [d][kTPR * CW] all rows after sweep 1
-  const int b = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int r = tid / kTPR;
-  const int p = tid % kTPR;
-  const bool row_ok = r < d;
-  constexpr int RW = kTPR * CW;                   // floats per stored row
-
-  float g[CW];
-  float len2 = 0.f;
+__device__ __forceinline__ float dot_part(const float* __restrict__ row, const float (&g)[CW]) {
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int k = 0; k < CW; ++k) {
-    const int c = p * CW + k;
-    g[k] = 0.f;
-    if (c < d && row_ok) {
-      const uint64_t idx = (((uint64_t)b * d + r) * d + c) * 2ull;
-      g[k] = normal_from_word(splitmix_word(seed, idx));
-      const float x = normal_from_word(splitmix_word(seed, idx + 1ull));
-      len2 = fmaf(x, x, len2);
-    }
+  for (int k = 0; k < CW; k += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(row + k);
+    a[0] = fmaf(v.x, g[k], a[0]);
+    a[1] = fmaf(v.y, g[k + 1], a[1]);
+    a[2] = fmaf(v.z, g[k + 2], a[2]);
+    a[3] = fmaf(v.w, g[k + 3], a[3]);
   }
-  const float len = sqrtf(group4_sum(len2));
+  return (a[0] + a[1]) + (a[2] + a[3]);
+}
 
-  // ---- sweep 1: modified Gram–Schmidt.  Every thread executes every shuffle
-  // (full-warp masks); only the values they carry depend on the thread's role.
-  for (int i = 0; i < d; ++i) {
-    float* q = qbuf + (i & 1) * RW;
-    const bool norm_row = (r == i);
-    float n2[4] = {0.f, 0.f, 0.f, 0.f};
-    if (norm_row) {
+// acc -= c * row (this thread's CW columns of a row in shared memory)
+template <int CW>
+__device__ __forceinline__ void axpy_part(float c, const float* __restrict__ row, float (&acc)[CW]) {
 #pragma unroll
-      for (int k = 0; k < CW; ++k) n2[k & 3] = fmaf(g[k], g[k], n2[k & 3]);
-    }
-    const float nn = group4_sum((n2[0] + n2[1]) + (n2[2] + n2[3]));
-    if (norm_row) {
-      const float inv = rsqrtf(nn);
+  for (int k = 0; k < CW; k += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(row + k);
+    acc[k] = fmaf(-c, v.x, acc[k]);
+    acc[k + 1] = fmaf(-c, v.y, acc[k + 1]);
+    acc[k + 2] = fmaf(-c, v.z, acc[k + 2]);
+    acc[k + 3] = fmaf(-c, v.w, acc[k + 3]);
+  }
+}
+
+template <int CW>
+__device__ __forceinline__ void load_part(const float* __restrict__ row, float (&x)[CW]) {
 #pragma unroll
-      for (int k = 0; k < CW; k += 4) {
-        g[k] *= inv;
-        g[k + 1] *= inv;
-        g[k + 2] *= inv;
-        g[k + 3] *= inv;
-        *reinterpret_cast<float4*>(q + p * CW + k) = make_float4(g[k], g[k + 1], g[k + 2], g[k + 3]);
+  for (int k = 0; k < CW; k += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(row + k);
+    x[k] = v.x;
+    x[k + 1] = v.y;
+    x[k + 2] = v.z;
+    x[k + 3] = v.w;
+  }
+}
+
+template <int CW>
+__device__ __forceinline__ void store_part(float* __restrict__ row, const float (&x)[CW]) {
+#pragma unroll
+  for (int k = 0; k < CW; k += 4)
+    *reinterpret_cast<float4*>(row + k) = make_float4(x[k], x[k + 1], x[k + 2], x[k + 3]);
+}
+
+// acc -= sum_j c_j q_j over N unit rows q_j (stride RW) with c_j = q_j . g,
+// the N coefficients taken together; with `below` only rows s0 + j < r count.
+// The rows are read once and held in registers.
+template <int CW, int N>
+__device__ __forceinline__ void subtract_held(const float* __restrict__ q, const float (&g)[CW], float (&acc)[CW],
+                                              int s0, int r, bool below) {
+  constexpr int RW = OrfLayout<CW>::RW;
+  float qv[N][CW];
+#pragma unroll
+  for (int j = 0; j < N; ++j) load_part<CW>(q + j * RW, qv[j]);
+  float c[N];
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < CW; ++k) a[k & 3] = fmaf(qv[j][k], g[k], a[k & 3]);
+    c[j] = group4_sum((a[0] + a[1]) + (a[2] + a[3]));
+  }
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    const float cj = (!below || s0 + j < r) ? c[j] : 0.f;
+#pragma unroll
+    for (int k = 0; k < CW; ++k) acc[k] = fmaf(-cj, qv[j][k], acc[k]);
+  }
+}
+
+// One CTA per d x d block.  Gram–Schmidt thread (row r = t/4, part p = t%4)
+// keeps columns p*CW .. p*CW+CW-1 of row r in registers (CW = ceil(d/4)
+// rounded up to a multiple of 4; columns >= d are zero), so warp w holds rows
+// 8w .. 8w+7, panel w.
+//
+// Sweep 1 is block modified Gram–Schmidt over the panels.  Panel w is
+// orthogonalised inside warp w, row by row, with no block barrier: the
+// pivot u_i reaches the warp through shared memory and every later row g
+// loses (u_i . g / u_i . u_i) u_i, both dots taken from the same copy, so the
+// pivot's own norm is off the dependent chain.  The panel's rows are then
+// normalised and published, and after one barrier every later panel loses
+// its components along them (the panel's coefficients taken together).
+// fp32 leaves the rows orthogonal only to about kappa * 2^-24, so sweep 2
+// re-orthogonalises them: as they are orthonormal up to that small error E,
+// one classical step q_r - sum_{s<r} (q_s . q_r) q_s for all rows at once
+// equals a second modified sweep up to O(E^2); its dots all use the same q_r,
+// so four rows s are taken at a time.  Finally row r is scaled by the length
+// of its own Gaussian vector and the block leaves through shared memory in
+// row order.
+//
+// Shared memory: rows [n_rows][RW] (rows >= d stay zero), lengths [n_rows],
+// and with helpers their half of the corrections [n_rows][RW].
+template <int CW>
+__global__ void __launch_bounds__(OrfLayout<CW>::kMaxThreads) orf_block_kernel(uint64_t seed, int m, int d,
+                                                                                float* __restrict__ omega) {
+  using Lay = OrfLayout<CW>;
+  constexpr int PS = Lay::PS;
+  constexpr int RW = Lay::RW;
+  extern __shared__ __align__(16) float orf_smem[];
+  const int n_panels = (d + kPanel - 1) / kPanel;
+  const int n_rows = n_panels * kPanel;
+  const int gs_threads = n_rows * kTPR;           // whole warps
+  float* const rows = orf_smem;
+  float* const lens = rows + n_rows * RW;
+  float* const hcorr = lens + n_rows;             // 32-byte aligned: n_rows is a multiple of 8
+  const int b = blockIdx.x;
+  const bool helper = Lay::kHeld && threadIdx.x >= gs_threads;   // warp-uniform
+  const int t = helper ? threadIdx.x - gs_threads : threadIdx.x;
+  const int warp = t >> 5;                        // panel of row r
+  const int li = (t & 31) / kTPR;                 // row within the panel
+  const int r = t / kTPR;
+  const int p = t % kTPR;
+  const bool row_ok = r < d;
+  float* const my_part = rows + r * RW + p * PS;
+
+  // ---- the normals: Gaussian row r (Gram–Schmidt threads) and the length
+  // vector of row r (helpers, else the same threads)
+  float g[CW];
+  float len = 0.f;
+#pragma unroll
+  for (int k = 0; k < CW; ++k) g[k] = 0.f;
+  if constexpr (Lay::kHeld) {
+    // every column draws its word and those past d are discarded, so the
+    // loops have no branch and the draws overlap
+    if (!helper) {
+#pragma unroll
+      for (int k = 0; k < CW; ++k) {
+        const int c = p * CW + k;
+        const float x = normal_from_word(splitmix_word(seed, (((uint64_t)b * d + r) * d + c) * 2ull));
+        g[k] = (row_ok && c < d) ? x : 0.f;
       }
+    } else {
+      float len2 = 0.f;
+#pragma unroll
+      for (int k = 0; k < CW; ++k) {
+        const int c = p * CW + k;
+        const float x = normal_from_word(splitmix_word(seed, (((uint64_t)b * d + r) * d + c) * 2ull + 1ull));
+        len2 = fmaf((row_ok && c < d) ? x : 0.f, x, len2);
+      }
+      len = sqrtf(group4_sum(len2));
+      if (p == 0) lens[r] = len;
+    }
+  } else {
+    float len2 = 0.f;
+#pragma unroll
+    for (int k = 0; k < CW; ++k) {
+      const int c = p * CW + k;
+      if (c < d && row_ok) {
+        const uint64_t idx = (((uint64_t)b * d + r) * d + c) * 2ull;
+        g[k] = normal_from_word(splitmix_word(seed, idx));
+        const float x = normal_from_word(splitmix_word(seed, idx + 1ull));
+        len2 = fmaf(x, x, len2);
+      }
+    }
+    len = sqrtf(group4_sum(len2));
+  }
+
+  // ---- sweep 1: block modified Gram–Schmidt.  Branches on `helper`, `warp`
+  // and the panel's row count are warp-uniform, so every shuffle has the
+  // full warp.
+  for (int k = 0; k < n_panels; ++k) {
+    if (!helper && warp == k) {
+      const int rows_k = min(kPanel, d - k * kPanel);
+      float n2_own = 1.f;
+      for (int i = 0; i < rows_k; ++i) {
+        if (li == i) store_part<CW>(my_part, g);
+        __syncwarp();
+        const float* u = rows + (k * kPanel + i) * RW + p * PS;
+        float dp[4] = {0.f, 0.f, 0.f, 0.f};
+        float nn[4] = {0.f, 0.f, 0.f, 0.f};
+        float uv[Lay::kHeld ? CW : 1];
+#pragma unroll
+        for (int kk = 0; kk < CW; kk += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(u + kk);
+          if constexpr (Lay::kHeld) {
+            uv[kk] = v.x;
+            uv[kk + 1] = v.y;
+            uv[kk + 2] = v.z;
+            uv[kk + 3] = v.w;
+          }
+          dp[0] = fmaf(v.x, g[kk], dp[0]);
+          dp[1] = fmaf(v.y, g[kk + 1], dp[1]);
+          dp[2] = fmaf(v.z, g[kk + 2], dp[2]);
+          dp[3] = fmaf(v.w, g[kk + 3], dp[3]);
+          nn[0] = fmaf(v.x, v.x, nn[0]);
+          nn[1] = fmaf(v.y, v.y, nn[1]);
+          nn[2] = fmaf(v.z, v.z, nn[2]);
+          nn[3] = fmaf(v.w, v.w, nn[3]);
+        }
+        float dot = (dp[0] + dp[1]) + (dp[2] + dp[3]);
+        float n2 = (nn[0] + nn[1]) + (nn[2] + nn[3]);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+        n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+        n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
+        if (li == i) n2_own = n2;
+        if (li > i) {
+          const float cf = __fdividef(dot, n2);
+          if constexpr (Lay::kHeld) {
+#pragma unroll
+            for (int kk = 0; kk < CW; ++kk) g[kk] = fmaf(-cf, uv[kk], g[kk]);
+          } else {
+            axpy_part<CW>(cf, u, g);
+          }
+        }
+      }
+      __syncwarp();                               // the last pivot is read before it is overwritten
+      // rows >= d (only in the last panel) are zero and stay zero
+      const float inv = row_ok ? rsqrtf(n2_own) : 0.f;
+#pragma unroll
+      for (int kk = 0; kk < CW; ++kk) g[kk] *= inv;
+      store_part<CW>(my_part, g);
     }
     __syncthreads();
-    const bool upd = row_ok && r > i;
-    float qv[CW];
-    float dp[4] = {0.f, 0.f, 0.f, 0.f};
-    if (upd) {
+    if (!helper && warp > k) {
+      // panel k is full here (only the last panel can be short)
+      const float* q = rows + k * kPanel * RW + p * PS;
+      if constexpr (Lay::kHeld) {
+        subtract_held<CW, 4>(q, g, g, 0, 0, false);
+        subtract_held<CW, 4>(q + 4 * RW, g, g, 0, 0, false);
+      } else {
+        // the rows are read again for the updates rather than held
+        float c[kPanel];
 #pragma unroll
-      for (int k = 0; k < CW; k += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(q + p * CW + k);
-        qv[k] = v.x;
-        qv[k + 1] = v.y;
-        qv[k + 2] = v.z;
-        qv[k + 3] = v.w;
+        for (int j = 0; j < kPanel; ++j) c[j] = dot_part<CW>(q + j * RW, g);
+#pragma unroll
+        for (int j = 0; j < kPanel; ++j) c[j] = group4_sum(c[j]);
+        __syncwarp();     // keeps the compiler from holding the rows in registers
+#pragma unroll
+        for (int j = 0; j < kPanel; ++j) axpy_part<CW>(c[j], q + j * RW, g);
       }
-#pragma unroll
-      for (int k = 0; k < CW; ++k) dp[k & 3] = fmaf(qv[k], g[k], dp[k & 3]);
-    }
-    const float dot = group4_sum((dp[0] + dp[1]) + (dp[2] + dp[3]));
-    if (upd) {
-#pragma unroll
-      for (int k = 0; k < CW; ++k) g[k] = fmaf(-dot, qv[k], g[k]);
     }
   }
 
   // ---- sweep 2: one classical re-orthogonalisation step, all rows at once
-  if (row_ok) {
-#pragma unroll
-    for (int k = 0; k < CW; k += 4)
-      *reinterpret_cast<float4*>(rows + r * RW + p * CW + k) = make_float4(g[k], g[k + 1], g[k + 2], g[k + 3]);
-  }
-  __syncthreads();
-  const int warp_last_row = min(d, (tid / 32 + 1) * (32 / kTPR)) - 1;   // largest row of this warp
+  // (the last barrier of sweep 1 published every row).  Rows s < r of this
+  // warp lie below 8 (warp + 1): 2 (warp + 1) groups of four.
   float corr[CW];
 #pragma unroll
   for (int k = 0; k < CW; ++k) corr[k] = 0.f;
-  for (int s_ = 0; s_ < warp_last_row; ++s_) {
-    float qv[CW];
+  const int n_groups = 2 * (warp + 1);
+  if constexpr (Lay::kHeld) {
+    const int split = (n_groups + 1) / 2;         // the helper takes the upper groups
+    if (helper) load_part<CW>(my_part, g);
+    for (int j = helper ? split : 0; j < (helper ? n_groups : split); ++j)
+      subtract_held<CW, 4>(rows + 4 * j * RW + p * PS, g, corr, 4 * j, r, true);
+    if (helper) store_part<CW>(hcorr + r * RW + p * PS, corr);
+    __syncthreads();
+    if (!helper) {
+      float h[CW];
+      load_part<CW>(hcorr + r * RW + p * PS, h);
 #pragma unroll
-    for (int k = 0; k < CW; k += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(rows + s_ * RW + p * CW + k);
-      qv[k] = v.x;
-      qv[k + 1] = v.y;
-      qv[k + 2] = v.z;
-      qv[k + 3] = v.w;
+      for (int k = 0; k < CW; ++k) corr[k] += h[k];
+      len = lens[r];
     }
-    float dp[4] = {0.f, 0.f, 0.f, 0.f};
+  } else {
+    for (int s0 = 0; s0 < 4 * n_groups; s0 += 4) {
+      const float* q = rows + s0 * RW + p * PS;
+      float c[4];
 #pragma unroll
-    for (int k = 0; k < CW; ++k) dp[k & 3] = fmaf(qv[k], g[k], dp[k & 3]);
-    const float c = (row_ok && s_ < r) ? group4_sum((dp[0] + dp[1]) + (dp[2] + dp[3])) : group4_sum(0.f);
+      for (int j = 0; j < 4; ++j) c[j] = dot_part<CW>(q + j * RW, g);
 #pragma unroll
-    for (int k = 0; k < CW; ++k) corr[k] = fmaf(c, qv[k], corr[k]);
+      for (int j = 0; j < 4; ++j) c[j] = group4_sum(c[j]);
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) axpy_part<CW>(s0 + j < r ? c[j] : 0.f, q + j * RW, corr);
+    }
   }
-  float n2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int k = 0; k < CW; ++k) {
-    g[k] -= corr[k];
-    n2[k & 3] = fmaf(g[k], g[k], n2[k & 3]);
-  }
-  const float inv = rsqrtf(group4_sum((n2[0] + n2[1]) + (n2[2] + n2[3])));
-  const int row = b * d + r;
-  if (row_ok && row < m) {
+  float sc = 0.f;
+  if (!helper) {
+    float n2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < CW; ++k) {
-      const int c = p * CW + k;
-      if (c < d) omega[(size_t)row * d + c] = g[k] * inv * len;
+      g[k] += corr[k];
+      n2[k & 3] = fmaf(g[k], g[k], n2[k & 3]);
     }
+    const float nrm2 = group4_sum((n2[0] + n2[1]) + (n2[2] + n2[3]));
+    sc = row_ok ? rsqrtf(nrm2) * len : 0.f;
+  }
+  __syncthreads();                                // every row has been read
+  if (!helper) {
+#pragma unroll
+    for (int k = 0; k < CW; ++k) g[k] *= sc;
+    store_part<CW>(my_part, g);
+  }
+  __syncthreads();
+  const int n_out = min(d, m - b * d);
+  float* const dst = omega + (size_t)b * d * d;
+  for (int e = threadIdx.x; e < n_out * d; e += blockDim.x) {
+    const int row = e / d, c = e - row * d;
+    dst[e] = rows[row * RW + (c / CW) * PS + (c % CW)];
   }
 }
 
@@ -296,22 +485,27 @@ cudaError_t launch_build_orf(uint64_t seed, int m, int d, int orthogonal, float*
   }
   if (orthogonal) {
     const int nb = (m + d - 1) / d;
-    const int threads = ((d * kTPR + 31) / 32) * 32;
+    const int n_rows = ((d + kPanel - 1) / kPanel) * kPanel;
+    const int gs_threads = n_rows * kTPR;
     const int cw = (d + kTPR - 1) / kTPR;
-    // shared memory: two unit rows + all d rows of kTPR * CW floats
-    auto smem_for = [&](int CW) { return (size_t)(2 + d) * kTPR * CW * sizeof(float); };
     cudaError_t e = cudaSuccess;
+    auto launch = [&](auto kernel, int CW, bool held) {
+      const int RW = kTPR * (CW + kPartPad);
+      const size_t smem = ((size_t)n_rows * RW * (held ? 2 : 1) + n_rows) * sizeof(float);
+      e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), smem);
+      if (e != cudaSuccess) return;
+      kernel<<<nb, gs_threads * (held ? 2 : 1), smem, stream>>>(seed, m, d, omega);
+    };
     if (cw <= 4) {
-      orf_block_kernel<4><<<nb, threads, smem_for(4), stream>>>(seed, m, d, omega);
+      launch(orf_block_kernel<4>, 4, OrfLayout<4>::kHeld);
     } else if (cw <= 8) {
-      orf_block_kernel<8><<<nb, threads, smem_for(8), stream>>>(seed, m, d, omega);
+      launch(orf_block_kernel<8>, 8, OrfLayout<8>::kHeld);
     } else if (cw <= 16) {
-      orf_block_kernel<16><<<nb, threads, smem_for(16), stream>>>(seed, m, d, omega);
+      launch(orf_block_kernel<16>, 16, OrfLayout<16>::kHeld);
     } else {
-      e = ensure_dynamic_smem(reinterpret_cast<const void*>(orf_block_kernel<32>), smem_for(32));
-      if (e != cudaSuccess) return e;
-      orf_block_kernel<32><<<nb, threads, smem_for(32), stream>>>(seed, m, d, omega);
+      launch(orf_block_kernel<32>, 32, OrfLayout<32>::kHeld);
     }
+    if (e != cudaSuccess) return e;
   } else {
     const int n = m * d;
     iid_kernel<<<(n + 255) / 256, 256, 0, stream>>>(seed, m, d, omega);
