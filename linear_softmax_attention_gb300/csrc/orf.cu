@@ -8,6 +8,7 @@
 // the length of an independent N(0, I_d) vector so that its marginal stays
 // N(0, I_d).
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace favor {
 namespace {
@@ -32,6 +33,7 @@ __device__ __forceinline__ float normal_from_word(uint64_t w) {
 constexpr int kTPR = 4;                 // threads per row of a block
 constexpr int kPanel = 32 / kTPR;       // rows per warp: one panel
 constexpr int kPartPad = 4;             // floats after each part of a stored row
+constexpr int kOrfCluster = 8;          // CTAs drawing one block's normals
 
 // Layout of one block's rows in shared memory.  Row r, part p (its columns
 // p*CW .. p*CW+CW-1) starts at r*RW + p*PS: with PS = CW + 4 the four parts
@@ -39,9 +41,9 @@ constexpr int kPartPad = 4;             // floats after each part of a stored ro
 // distinct addresses) take one pass.  With CW <= 16 the rows being
 // subtracted are held in registers between their dot products and their
 // updates, and a second group of warps (helpers, one thread per Gram–Schmidt
-// thread) draws the length vectors and takes half of the
-// re-orthogonalisation; at CW = 32 (d > 64) the registers of 512 threads
-// allow neither, and the rows are read twice instead.
+// thread) derives the lengths and takes half of the re-orthogonalisation;
+// at CW = 32 (d > 64) the registers of 512 threads allow neither, and the
+// rows are read twice instead.
 template <int CW>
 struct OrfLayout {
   static constexpr int PS = CW + kPartPad;
@@ -83,6 +85,15 @@ __device__ __forceinline__ void axpy_part(float c, const float* __restrict__ row
     acc[k + 2] = fmaf(-c, v.z, acc[k + 2]);
     acc[k + 3] = fmaf(-c, v.w, acc[k + 3]);
   }
+}
+
+// Barrier `id` (1..15) over n threads, whole warps: bar.sync waits for all n,
+// bar.arrive counts this warp and goes on.
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 template <int CW>
@@ -150,8 +161,15 @@ __device__ __forceinline__ void subtract_held(const float* __restrict__ q, const
 // of its own Gaussian vector and the block leaves through shared memory in
 // row order.
 //
-// Shared memory: rows [n_rows][RW] (rows >= d stay zero), lengths [n_rows],
-// and with helpers their half of the corrections [n_rows][RW].
+// The normals are drawn by a cluster of 8 CTAs per block: CTA rho draws rows
+// [rho d / 8, (rho + 1) d / 8) of the Gaussian block and of the length
+// vectors into the first CTA's shared memory, and after one cluster barrier
+// the first CTA alone goes on (the draws are 2 d^2 Box–Muller normals, the
+// one part of the build that parallelises).
+//
+// Shared memory: rows [n_rows][RW], lengths [n_rows], and draws [n_rows][RW]:
+// the length vectors, later the helpers' half of the corrections.  Entries
+// past d are never written and never read into the arithmetic.
 template <int CW>
 __global__ void __launch_bounds__(OrfLayout<CW>::kMaxThreads) orf_block_kernel(uint64_t seed, int m, int d,
                                                                                 float* __restrict__ omega) {
@@ -164,10 +182,35 @@ __global__ void __launch_bounds__(OrfLayout<CW>::kMaxThreads) orf_block_kernel(u
   const int gs_threads = n_rows * kTPR;           // whole warps
   float* const rows = orf_smem;
   float* const lens = rows + n_rows * RW;
-  float* const hcorr = lens + n_rows;             // 32-byte aligned: n_rows is a multiple of 8
-  const int b = blockIdx.x;
+  float* const draws = lens + n_rows;             // 32-byte aligned: n_rows is a multiple of 8
+  float* const hcorr = draws;
+  const int b = blockIdx.x / kOrfCluster;
+
+  // ---- the normals: Gaussian entry (r, c) of block b from word 2 e, its
+  // length-vector entry from word 2 e + 1, e = (b d + r) d + c
+  {
+    const int rank = static_cast<int>(tc::cluster_ctarank());
+    const int r0 = rank * d / kOrfCluster, r1 = (rank + 1) * d / kOrfCluster;
+    const uint32_t rows0 = tc::map_to_rank(tc::smem_addr(rows), 0);
+    const uint32_t draws0 = tc::map_to_rank(tc::smem_addr(draws), 0);
+    const int n_e = (r1 - r0) * d;
+    for (int e = threadIdx.x; e < n_e; e += blockDim.x) {
+      const int rr = r0 + e / d, c = e - (e / d) * d;
+      const uint64_t idx = (((uint64_t)b * d + rr) * d + c) * 2ull;
+      const uint32_t off = 4u * static_cast<uint32_t>(rr * RW + (c / CW) * PS + c % CW);
+      tc::st_cluster_f32(rows0 + off, normal_from_word(splitmix_word(seed, idx)));
+      tc::st_cluster_f32(draws0 + off, normal_from_word(splitmix_word(seed, idx + 1ull)));
+    }
+  }
+  tc::cluster_sync();                             // the draws are in the first CTA
+  if (tc::cluster_ctarank() != 0) return;            // nothing reads the other CTAs' memory
+
+  // helper warp j serves Gram–Schmidt warp n_panels - 1 - j: the warps with
+  // the most re-orthogonalisation work pair with the least loaded
+  // sub-partitions (warp w runs on sub-partition w mod 4)
   const bool helper = Lay::kHeld && threadIdx.x >= gs_threads;   // warp-uniform
-  const int t = helper ? threadIdx.x - gs_threads : threadIdx.x;
+  const int t = helper ? (((n_panels - 1 - ((threadIdx.x - gs_threads) >> 5)) << 5) | (threadIdx.x & 31))
+                       : threadIdx.x;
   const int warp = t >> 5;                        // panel of row r
   const int li = (t & 31) / kTPR;                 // row within the panel
   const int r = t / kTPR;
@@ -175,46 +218,22 @@ __global__ void __launch_bounds__(OrfLayout<CW>::kMaxThreads) orf_block_kernel(u
   const bool row_ok = r < d;
   float* const my_part = rows + r * RW + p * PS;
 
-  // ---- the normals: Gaussian row r (Gram–Schmidt threads) and the length
-  // vector of row r (helpers, else the same threads)
+  // Gaussian row r (Gram–Schmidt threads) and the length of row r's own
+  // Gaussian vector (helpers, else the same threads); columns past d are zero
   float g[CW];
   float len = 0.f;
+  load_part<CW>(my_part, g);
 #pragma unroll
-  for (int k = 0; k < CW; ++k) g[k] = 0.f;
-  if constexpr (Lay::kHeld) {
-    // every column draws its word and those past d are discarded, so the
-    // loops have no branch and the draws overlap
-    if (!helper) {
-#pragma unroll
-      for (int k = 0; k < CW; ++k) {
-        const int c = p * CW + k;
-        const float x = normal_from_word(splitmix_word(seed, (((uint64_t)b * d + r) * d + c) * 2ull));
-        g[k] = (row_ok && c < d) ? x : 0.f;
-      }
-    } else {
-      float len2 = 0.f;
-#pragma unroll
-      for (int k = 0; k < CW; ++k) {
-        const int c = p * CW + k;
-        const float x = normal_from_word(splitmix_word(seed, (((uint64_t)b * d + r) * d + c) * 2ull + 1ull));
-        len2 = fmaf((row_ok && c < d) ? x : 0.f, x, len2);
-      }
-      len = sqrtf(group4_sum(len2));
-      if (p == 0) lens[r] = len;
-    }
-  } else {
+  for (int k = 0; k < CW; ++k)
+    if (helper || !row_ok || p * CW + k >= d) g[k] = 0.f;
+  if (!Lay::kHeld || helper) {
+    float x[CW];
+    load_part<CW>(draws + r * RW + p * PS, x);
     float len2 = 0.f;
 #pragma unroll
-    for (int k = 0; k < CW; ++k) {
-      const int c = p * CW + k;
-      if (c < d && row_ok) {
-        const uint64_t idx = (((uint64_t)b * d + r) * d + c) * 2ull;
-        g[k] = normal_from_word(splitmix_word(seed, idx));
-        const float x = normal_from_word(splitmix_word(seed, idx + 1ull));
-        len2 = fmaf(x, x, len2);
-      }
-    }
+    for (int k = 0; k < CW; ++k) len2 = fmaf(row_ok && p * CW + k < d ? x[k] : 0.f, x[k], len2);
     len = sqrtf(group4_sum(len2));
+    if (Lay::kHeld && p == 0) lens[r] = len;
   }
 
   // ---- sweep 1: block modified Gram–Schmidt.  Branches on `helper`, `warp`
@@ -275,7 +294,11 @@ __global__ void __launch_bounds__(OrfLayout<CW>::kMaxThreads) orf_block_kernel(u
     }
     __syncthreads();
     if (!helper && warp > k) {
-      // panel k is full here (only the last panel can be short)
+      // panel k is full here (only the last panel can be short).  Warp k + 1
+      // pivots next, so the later warps leave it the shared-memory pipe: they
+      // start once it has subtracted the panel (barrier 1).
+      const int n_wait = 32 * (n_panels - k - 1);  // warps k + 1 .. n_panels - 1
+      if (warp > k + 1) named_sync(1, n_wait);
       const float* q = rows + k * kPanel * RW + p * PS;
       if constexpr (Lay::kHeld) {
         subtract_held<CW, 4>(q, g, g, 0, 0, false);
@@ -291,6 +314,7 @@ __global__ void __launch_bounds__(OrfLayout<CW>::kMaxThreads) orf_block_kernel(u
 #pragma unroll
         for (int j = 0; j < kPanel; ++j) axpy_part<CW>(c[j], q + j * RW, g);
       }
+      if (warp == k + 1 && k + 2 < n_panels) named_arrive(1, n_wait);
     }
   }
 
@@ -348,9 +372,19 @@ __global__ void __launch_bounds__(OrfLayout<CW>::kMaxThreads) orf_block_kernel(u
   __syncthreads();
   const int n_out = min(d, m - b * d);
   float* const dst = omega + (size_t)b * d * d;
-  for (int e = threadIdx.x; e < n_out * d; e += blockDim.x) {
-    const int row = e / d, c = e - row * d;
-    dst[e] = rows[row * RW + (c / CW) * PS + (c % CW)];
+  if ((d & 3) == 0 && (reinterpret_cast<uintptr_t>(omega) & 15) == 0) {
+    // four columns at a time (CW is a multiple of 4, so they share a part)
+    const int dq = d >> 2;
+    for (int e = threadIdx.x; e < n_out * dq; e += blockDim.x) {
+      const int row = e / dq, c = (e - row * dq) << 2;
+      reinterpret_cast<float4*>(dst)[e] =
+          *reinterpret_cast<const float4*>(rows + row * RW + (c / CW) * PS + (c % CW));
+    }
+  } else {
+    for (int e = threadIdx.x; e < n_out * d; e += blockDim.x) {
+      const int row = e / d, c = e - row * d;
+      dst[e] = rows[row * RW + (c / CW) * PS + (c % CW)];
+    }
   }
 }
 
@@ -491,10 +525,22 @@ cudaError_t launch_build_orf(uint64_t seed, int m, int d, int orthogonal, float*
     cudaError_t e = cudaSuccess;
     auto launch = [&](auto kernel, int CW, bool held) {
       const int RW = kTPR * (CW + kPartPad);
-      const size_t smem = ((size_t)n_rows * RW * (held ? 2 : 1) + n_rows) * sizeof(float);
+      const size_t smem = ((size_t)2 * n_rows * RW + n_rows) * sizeof(float);
       e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), smem);
       if (e != cudaSuccess) return;
-      kernel<<<nb, gs_threads * (held ? 2 : 1), smem, stream>>>(seed, m, d, omega);
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(nb * kOrfCluster);
+      cfg.blockDim = dim3(gs_threads * (held ? 2 : 1));
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kOrfCluster;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, kernel, seed, m, d, omega);
     };
     if (cw <= 4) {
       launch(orf_block_kernel<4>, 4, OrfLayout<4>::kHeld);
