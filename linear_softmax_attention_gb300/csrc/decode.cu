@@ -17,7 +17,12 @@
 //
 // One CTA per head.  Bound by the state's HBM traffic: m (d+1) fp32 read and
 // written per head and token (133 KB at m = 256, d = 64); Omega (m x d fp32)
-// is read by every CTA and stays in L2.
+// is read by every CTA and stays in L2.  Where it fits (m (d + 4) floats up to
+// 100 KB, so two CTAs share an SM) each CTA first copies Omega into shared
+// memory with coalesced 16-byte asynchronous copies, rows padded to d + 4
+// floats so that the row a thread reads sits in its own banks; read straight
+// from L2, every lane's row is a separate line and the requests, not the
+// bytes, set the time.
 #include <type_traits>
 
 #include "common.cuh"
@@ -28,6 +33,7 @@ namespace {
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kCB = 16;                              // state columns per block of loads
+constexpr size_t kStageOmegaMax = 100 * 1024;        // bytes of padded Omega copied into shared memory
 
 // NF features per thread: 1 for m <= 256, 2 for m <= 512
 template <typename T, int NF>
@@ -35,17 +41,28 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_step_kernel(const T* __
                                                                   const T* __restrict__ v, T* __restrict__ o,
                                                                   const float* __restrict__ omega, int d, int m,
                                                                   float scale, float* __restrict__ state,
-                                                                  int32_t* __restrict__ status) {
+                                                                  int32_t* __restrict__ status, int staged) {
   __shared__ float qs[kMaxD], ks[kMaxD], vs[kMaxD + 1];
   __shared__ float phq[kMaxM], phk[kMaxM];
   __shared__ float part[kDecWarps][kMaxD + 1];
   __shared__ float num[kMaxD + 1];
   __shared__ float wred[kDecWarps], qred[kDecWarps];
   __shared__ float sqn[1];
+  extern __shared__ __align__(16) float om_s[];     // [m][d + 4] when staged
   const int bh = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ld = d + 1;
+  const int ldw = d + 4;
 
+  if (staged) {
+    const int dq = d >> 2;
+    for (int e = tid; e < m * dq; e += kDecThreads) {
+      const int f = e / dq, j4 = e - f * dq;
+      const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(om_s + f * ldw + 4 * j4));
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(omega + 4 * (size_t)e) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
   for (int j = tid; j < d; j += kDecThreads) {
     const size_t e = (size_t)bh * d + j;
     qs[j] = to_f32(q[e]);
@@ -81,6 +98,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_step_kernel(const T* __
     }
   };
   load_sb(0);
+  if (staged) asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();                                   // the copy of Omega is complete
 
   // w_f.q, w_f.k and |w_f|^2 for the features f = tid + 256 i of this thread
   float pq[NF], pk[NF];
@@ -91,11 +110,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_step_kernel(const T* __
     float dq = 0.f, dk = 0.f, w2 = 0.f;
     if (f < m) {
       const float* w = omega + (size_t)f * d;
-      if ((d & 3) == 0) {
+      if (staged || (d & 3) == 0) {
         // rows are 16-byte aligned: 16-byte loads, a quarter of the requests
-        const float4* w4 = reinterpret_cast<const float4*>(w);
+        const float4* w4 = staged ? reinterpret_cast<const float4*>(om_s + f * ldw) : reinterpret_cast<const float4*>(w);
         for (int j4 = 0; j4 < d / 4; ++j4) {
-          const float4 x = __ldg(w4 + j4);
+          const float4 x = staged ? w4[j4] : __ldg(w4 + j4);
           const int j = 4 * j4;
           dq = fmaf(x.x, qs[j], dq);
           dk = fmaf(x.x, ks[j], dk);
@@ -222,12 +241,18 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_step_kernel(const T* __
 cudaError_t launch_decode_step(const void* q, const void* k, const void* v, void* o, int BH, int d,
                                const float* omega, int m, bool bf16, float scale, float* state, int32_t* status,
                                cudaStream_t stream) {
+  const size_t stage_bytes = (size_t)m * (d + 4) * sizeof(float);
+  const bool staged = (d & 3) == 0 && (reinterpret_cast<uintptr_t>(omega) & 15) == 0 && stage_bytes <= kStageOmegaMax;
+  cudaError_t err = cudaSuccess;
   auto go = [&](auto tag, auto nf) {
     using T = decltype(tag);
     constexpr int NF = decltype(nf)::value;
-    decode_step_kernel<T, NF><<<BH, kDecThreads, 0, stream>>>(static_cast<const T*>(q), static_cast<const T*>(k),
-                                                              static_cast<const T*>(v), static_cast<T*>(o), omega, d,
-                                                              m, scale, state, status);
+    const size_t smem = staged ? stage_bytes : 0;
+    err = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_step_kernel<T, NF>), smem);
+    if (err != cudaSuccess) return;
+    decode_step_kernel<T, NF><<<BH, kDecThreads, smem, stream>>>(static_cast<const T*>(q), static_cast<const T*>(k),
+                                                                 static_cast<const T*>(v), static_cast<T*>(o), omega,
+                                                                 d, m, scale, state, status, staged ? 1 : 0);
   };
   using One = std::integral_constant<int, 1>;
   using Two = std::integral_constant<int, 2>;
@@ -238,6 +263,7 @@ cudaError_t launch_decode_step(const void* q, const void* k, const void* v, void
     if (m <= kDecThreads) go(float{}, One{});
     else go(float{}, Two{});
   }
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
