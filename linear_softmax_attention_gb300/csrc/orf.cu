@@ -37,8 +37,9 @@ constexpr int kOrfCluster = 8;          // CTAs drawing one block's normals
 
 // Layout of one block's rows in shared memory.  Row r, part p (its columns
 // p*CW .. p*CW+CW-1) starts at r*RW + p*PS: with PS = CW + 4 the four parts
-// of a row fall in different banks, so the warp-wide reads of one row (four
-// distinct addresses) take one pass.  With CW <= 16 the rows being
+// of a row fall in different banks, so a warp-wide 16-byte read of one row
+// (four distinct addresses) meets no bank conflict; unpadded, the four parts
+// share their banks and the read takes four times the passes.  With CW <= 16 the rows being
 // subtracted are held in registers between their dot products and their
 // updates, and a second group of warps (helpers, one thread per Gram–Schmidt
 // thread) derives the lengths and takes half of the re-orthogonalisation;
@@ -168,8 +169,10 @@ __device__ __forceinline__ void subtract_held(const float* __restrict__ q, const
 // one part of the build that parallelises).
 //
 // Shared memory: rows [n_rows][RW], lengths [n_rows], and draws [n_rows][RW]:
-// the length vectors, later the helpers' half of the corrections.  Entries
-// past d are never written and never read into the arithmetic.
+// the length vectors, later the helpers' half of the corrections.  The draws
+// fill only rows and columns below d; the loads of the Gaussian rows and of
+// the length vectors replace the rest by zero, and every row stored from
+// then on carries those zeros.
 template <int CW>
 __global__ void __launch_bounds__(OrfLayout<CW>::kMaxThreads) orf_block_kernel(uint64_t seed, int m, int d,
                                                                                 float* __restrict__ omega) {
