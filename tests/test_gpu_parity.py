@@ -35,7 +35,10 @@ def _status(device="cuda"):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("seed,m,d", [(0, 64, 64), (1, 256, 64), (7, 128, 128), (3, 512, 128), (5, 96, 32),
-                                      (9, 5, 4), (11, 200, 100)])
+                                      (9, 5, 4), (11, 200, 100),
+                                      # odd panel counts (helper pairing, barrier counts), a ragged
+                                      # last part, and blocks with fewer rows than drawing CTAs
+                                      (13, 30, 13), (17, 120, 40), (19, 150, 72), (23, 3, 1), (29, 5, 2)])
 def test_orf_matches_oracle(cuda_lib, seed, m, d):
     om = to_np(cuda_lib.new_omega(seed, m, d))
     want, parts = orc.build_omega(seed, m, d, return_parts=True)
