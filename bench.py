@@ -210,6 +210,7 @@ KERNEL_SOURCES = ("linear_softmax_attention_gb300/csrc/tc.cu", "linear_softmax_a
                   "linear_softmax_attention_gb300/csrc/tc_bwd.cu",
                   "linear_softmax_attention_gb300/csrc/tc_util.cuh", "linear_softmax_attention_gb300/csrc/tc_ptx.cuh",
                   "linear_softmax_attention_gb300/csrc/common.cuh", "linear_softmax_attention_gb300/csrc/prep.cu",
+                  "linear_softmax_attention_gb300/csrc/orf.cu", "linear_softmax_attention_gb300/csrc/decode.cu",
                   "include/favor.h")
 _C_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
 

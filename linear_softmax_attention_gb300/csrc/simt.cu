@@ -246,16 +246,31 @@ __global__ void __launch_bounds__(kThreads, 3) state_partial_kernel(
   }
 }
 
-// Bidirectional: state[h] = sum over splits of S_p, in split order.
+// Bidirectional: state[h] = sum over splits of S_p, in split order.  One
+// thread per state element (grid: element blocks x heads), eight partials'
+// loads in flight at a time.
 __global__ void __launch_bounds__(kThreads) merge_kernel(const float* __restrict__ partS, int d, int m, int n_split,
                                                          float* __restrict__ state) {
-  const int bh = blockIdx.x;
+  const int bh = blockIdx.y;
   const size_t per = (size_t)m * (d + 1);
-  for (int e = threadIdx.x; e < (int)per; e += kThreads) {
-    float acc = 0.f;
-    for (int p = 0; p < n_split; ++p) acc += partS[((size_t)bh * n_split + p) * per + e];
-    state[(size_t)bh * per + e] = acc;
+  const size_t e = (size_t)blockIdx.x * kThreads + threadIdx.x;
+  if (e >= per) return;
+  const float* src = partS + (size_t)bh * n_split * per + e;
+  float acc = 0.f;
+  for (int p0 = 0; p0 < n_split; p0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = p0 + u < n_split ? src[(size_t)(p0 + u) * per] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (p0 + u < n_split) acc += v[u];
   }
+  state[(size_t)bh * per + e] = acc;
+}
+
+dim3 merge_grid(const Shape& s) {
+  const size_t per = (size_t)s.m * (s.d + 1);
+  return dim3(static_cast<unsigned>((per + kThreads - 1) / kThreads), static_cast<unsigned>(s.BH()));
 }
 
 // Query-side features of one tile: pq[t][i] = exp(s w_i.q_t - max_i s w_i.q_t)
@@ -596,7 +611,7 @@ cudaError_t simt_bidir_state(const void* K, const void* V, const float* omega, f
     return state_impl<decltype(t), decltype(f)::value>(K, V, omega, scale, s, p, w, stream);
   });
   if (e != cudaSuccess) return e;
-  merge_kernel<<<s.BH(), kThreads, 0, stream>>>(reinterpret_cast<float*>(w + p.off_partS), s.d, s.m, p.n_split,
+  merge_kernel<<<merge_grid(s), kThreads, 0, stream>>>(reinterpret_cast<float*>(w + p.off_partS), s.d, s.m, p.n_split,
                                                 reinterpret_cast<float*>(w + p.off_state));
   return cudaGetLastError();
 }
@@ -1471,7 +1486,7 @@ cudaError_t simt_bwd_bidir(const void* Q, const void* K, const void* V, const vo
                                                               s.d, s.m, scale, st);
     bwd_dstate_partial_kernel<T, FM><<<dim3(b.fwd.n_split, b.fwd.n_fb, s.BH()), kThreads, dsm, stream>>>(
         static_cast<const T*>(Q), dnw, omega, key_ref, s.L, s.d, s.m, scale, b.fwd.chunk, b.fwd.n_split, dpart);
-    merge_kernel<<<s.BH(), kThreads, 0, stream>>>(dpart, s.d, s.m, b.fwd.n_split, dstate);
+    merge_kernel<<<merge_grid(s), kThreads, 0, stream>>>(dpart, s.d, s.m, b.fwd.n_split, dstate);
     bwd_key_kernel<T, FM><<<tiles, kThreads, tsm, stream>>>(static_cast<const T*>(K), static_cast<const T*>(V),
                                                             static_cast<T*>(dK), static_cast<T*>(dV), omega, key_ref,
                                                             dstate, s.L, s.d, s.m, scale);
