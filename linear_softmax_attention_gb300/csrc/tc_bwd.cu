@@ -210,22 +210,31 @@ __device__ void merge_grad_state(const float* __restrict__ base, int parts, int 
     float4 acc[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int p = 0; p < count; ++p) {
-      float4 v[kBatch];
+    // the loads of up to kPartBatch slots in flight together, added in slot order
+    constexpr int kPartBatch = 4;
+    for (int p0 = 0; p0 < count; p0 += kPartBatch) {
+      float4 v[kPartBatch][kBatch];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int e = e0 + u * nthreads;
-        const int g = e % NG, n = (e / NG) % (D + 1), b = e / (NG * (D + 1));
-        v[u] = e < e_end
-                   ? *reinterpret_cast<const float4*>(base + (((size_t)b * parts + p) * (D + 1) + n) * kFB + g * 4)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+      for (int pp = 0; pp < kPartBatch; ++pp)
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        acc[u].x += v[u].x;
-        acc[u].y += v[u].y;
-        acc[u].z += v[u].z;
-        acc[u].w += v[u].w;
+        for (int u = 0; u < kBatch; ++u) {
+          const int e = e0 + u * nthreads;
+          const int g = e % NG, n = (e / NG) % (D + 1), b = e / (NG * (D + 1));
+          const int p = p0 + pp;
+          v[pp][u] = (e < e_end && p < count)
+                         ? *reinterpret_cast<const float4*>(base + (((size_t)b * parts + p) * (D + 1) + n) * kFB + g * 4)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+      for (int pp = 0; pp < kPartBatch; ++pp) {
+        if (p0 + pp >= count) break;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          acc[u].x += v[pp][u].x;
+          acc[u].y += v[pp][u].y;
+          acc[u].z += v[pp][u].z;
+          acc[u].w += v[pp][u].w;
+        }
       }
     }
 #pragma unroll
