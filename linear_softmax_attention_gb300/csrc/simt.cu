@@ -618,17 +618,27 @@ cudaError_t simt_bidir_state(const void* K, const void* V, const float* omega, f
 
 // The decode state layout [bh][j][f] (j <= d, f < m: feature index fastest)
 // from the split partials, summed in split order.
+// One thread per state element (grid: element blocks x heads), eight
+// partials' loads in flight at a time.
 __global__ void __launch_bounds__(kThreads) merge_transposed_kernel(const float* __restrict__ partS, int d, int m,
                                                                     int n_split, float* __restrict__ state) {
-  const int bh = blockIdx.x;
+  const int bh = blockIdx.y;
   const int ld = d + 1;
   const size_t per = (size_t)m * ld;
-  for (int e = threadIdx.x; e < (int)per; e += kThreads) {
-    const int j = e / m, f = e - j * m;
-    float acc = 0.f;
-    for (int p = 0; p < n_split; ++p) acc += partS[((size_t)bh * n_split + p) * per + (size_t)f * ld + j];
-    state[(size_t)bh * per + e] = acc;
+  const size_t e = (size_t)blockIdx.x * kThreads + threadIdx.x;
+  if (e >= per) return;
+  const int j = static_cast<int>(e / m), f = static_cast<int>(e - (size_t)j * m);
+  const float* src = partS + (size_t)bh * n_split * per + (size_t)f * ld + j;
+  float acc = 0.f;
+  for (int p0 = 0; p0 < n_split; p0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = p0 + u < n_split ? src[(size_t)(p0 + u) * per] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (p0 + u < n_split) acc += v[u];
   }
+  state[(size_t)bh * per + e] = acc;
 }
 
 // The summed state of a whole sequence into `state` in the decode layout
@@ -641,7 +651,7 @@ cudaError_t simt_state_export(const void* K, const void* V, const float* omega, 
   cudaError_t e = bf16 ? state_impl<__nv_bfloat16, FAVOR_FM_PRF>(K, V, omega, scale, s, p, w, stream)
                        : state_impl<float, FAVOR_FM_PRF>(K, V, omega, scale, s, p, w, stream);
   if (e != cudaSuccess) return e;
-  merge_transposed_kernel<<<s.BH(), kThreads, 0, stream>>>(reinterpret_cast<float*>(w + p.off_partS), s.d, s.m,
+  merge_transposed_kernel<<<merge_grid(s), kThreads, 0, stream>>>(reinterpret_cast<float*>(w + p.off_partS), s.d, s.m,
                                                             p.n_split, state);
   return cudaGetLastError();
 }
@@ -1380,11 +1390,25 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(float* __restrict_
   if (e >= per) return;
   float* base = cst + (size_t)bh * n_chunk * per + e;
   float run = 0.f;
-  for (int i = 0; i < n_chunk; ++i) {
-    const int c = reverse ? n_chunk - 1 - i : i;
-    const float x = base[(size_t)c * per];
-    base[(size_t)c * per] = run;
-    run += x;
+  // eight chunks' loads in flight before their stores (the scan is in place,
+  // so the compiler would otherwise wait for each load behind the previous
+  // store); the running sum keeps its order
+  for (int i0 = 0; i0 < n_chunk; i0 += 8) {
+    float x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u;
+      const int c = reverse ? n_chunk - 1 - i : i;
+      x[u] = i < n_chunk ? base[(size_t)c * per] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u;
+      if (i >= n_chunk) break;
+      const int c = reverse ? n_chunk - 1 - i : i;
+      base[(size_t)c * per] = run;
+      run += x[u];
+    }
   }
 }
 
