@@ -395,44 +395,56 @@ __global__ void __launch_bounds__(OrfLayout<CW>::kMaxThreads) orf_block_kernel(u
 // Walsh-Hadamard matrix, D_p = diag(+-1) with sign i of product p from the
 // top bit of SplitMix64 word (b*3 + p)*d + i ("Rethinking Attention with
 // Performers" summary, §A.2 and §B.3 name Hadamard ORFs; the construction is
-// the plain reading).  X starts as the identity; X <- X (H D_p) applies the
-// fast Walsh-Hadamard transform to every row of X, then the column signs.
-// One CTA per block, X [d][d+1] in shared memory; d a power of two.
-__global__ void __launch_bounds__(256) hadamard_block_kernel(uint64_t seed, int m, int d, float* __restrict__ omega) {
-  extern __shared__ float X[];
-  const int b = blockIdx.x;
-  const int ld = d + 1;
-  for (int e = threadIdx.x; e < d * d; e += blockDim.x) {
-    const int r = e / d, c = e - r * d;
-    X[r * ld + c] = (r == c) ? 1.f : 0.f;
-  }
-  __syncthreads();
+// the plain reading).  Row r starts as e_r; X <- X (H D_p) applies the fast
+// Walsh-Hadamard transform to the row (strides 1, 2, 4, ..: a + c, a - c),
+// then the column signs and 1/sqrt(d).  Rows are independent, so one warp
+// carries one row: element i in lane i % 32, slot i / 32 (E = max(1, d/32)
+// slots); strides below 32 pair lanes by shuffles, larger strides pair slots
+// of the same lane.  d is a power of two; for d < 32 lanes >= d idle.
+template <int E>
+__global__ void __launch_bounds__(256) hadamard_rows_kernel(uint64_t seed, int m, int d, float* __restrict__ omega) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);     // global row of Omega, warp-uniform
+  if (row >= m) return;
+  const int b = row / d, r = row - b * d;
+  float x[E];
+#pragma unroll
+  for (int s = 0; s < E; ++s) x[s] = (s * 32 + lane == r) ? 1.f : 0.f;
   const float inv_sqrt_d = rsqrtf(static_cast<float>(d));
   for (int p = 0; p < 3; ++p) {
     for (int h = 1; h < d; h <<= 1) {
-      // d rows x d/2 butterflies (i, i + h) with (i & h) == 0
-      for (int e = threadIdx.x; e < d * (d / 2); e += blockDim.x) {
-        const int r = e / (d / 2), k = e - r * (d / 2);
-        const int i = (k / h) * 2 * h + (k % h);
-        const float a = X[r * ld + i], c = X[r * ld + i + h];
-        X[r * ld + i] = a + c;
-        X[r * ld + i + h] = a - c;
+      if (h < 32) {
+        const bool upper = (lane & h) != 0;
+#pragma unroll
+        for (int s = 0; s < E; ++s) {
+          const float o = __shfl_xor_sync(0xffffffffu, x[s], h);
+          x[s] = upper ? o - x[s] : x[s] + o;
+        }
+      } else {
+        const int k = h >> 5;                                // slot stride
+#pragma unroll
+        for (int s = 0; s < E; ++s) {
+          if ((s & k) == 0) {
+            const float a = x[s], c = x[s + k];
+            x[s] = a + c;
+            x[s + k] = a - c;
+          }
+        }
       }
-      __syncthreads();
     }
-    for (int e = threadIdx.x; e < d * d; e += blockDim.x) {
-      const int r = e / d, c = e - r * d;
+#pragma unroll
+    for (int s = 0; s < E; ++s) {
+      const int c = s * 32 + lane;
       const uint64_t w = splitmix_word(seed, static_cast<uint64_t>(b * 3 + p) * d + c);
       const float sgn = (w >> 63) ? -1.f : 1.f;
-      X[r * ld + c] *= sgn * inv_sqrt_d;
+      x[s] *= sgn * inv_sqrt_d;
     }
-    __syncthreads();
   }
   const float sqrt_d = sqrtf(static_cast<float>(d));
-  for (int e = threadIdx.x; e < d * d; e += blockDim.x) {
-    const int r = e / d, c = e - r * d;
-    const int row = b * d + r;
-    if (row < m) omega[(size_t)row * d + c] = sqrt_d * X[r * ld + c];
+#pragma unroll
+  for (int s = 0; s < E; ++s) {
+    const int c = s * 32 + lane;
+    if (c < d) omega[(size_t)row * d + c] = sqrt_d * x[s];
   }
 }
 
@@ -514,10 +526,10 @@ cudaError_t launch_build_orf(uint64_t seed, int m, int d, int orthogonal, float*
     return cudaGetLastError();
   }
   if (orthogonal == 2) {
-    const size_t smem = (size_t)d * (d + 1) * sizeof(float);
-    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(hadamard_block_kernel), smem);
-    if (e != cudaSuccess) return e;
-    hadamard_block_kernel<<<(m + d - 1) / d, 256, smem, stream>>>(seed, m, d, omega);
+    const int grid = (m + 7) / 8;                            // one warp per row
+    if (d <= 32) hadamard_rows_kernel<1><<<grid, 256, 0, stream>>>(seed, m, d, omega);
+    else if (d <= 64) hadamard_rows_kernel<2><<<grid, 256, 0, stream>>>(seed, m, d, omega);
+    else hadamard_rows_kernel<4><<<grid, 256, 0, stream>>>(seed, m, d, omega);
     return cudaGetLastError();
   }
   if (orthogonal) {
